@@ -1,0 +1,123 @@
+"""Planted mistakes in a copy of the oracle must be caught by its pins.
+
+Each case copies ``oracle/mbglu_oracle.c`` to a temporary directory, applies
+one textual slip of the kind a hand-written oracle might carry (a wrong sign,
+a dropped term, a transposed operand, a wrong tie rule, a wrong index, a
+missing epsilon), builds it with the oracle's own flags, and runs a compact
+set of the pins from ``test_oracle_pins.py`` against it.  The unmodified
+source must pass the same set.  Everything runs on the CPU.
+"""
+import os
+import shutil
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import glu_inputs as gi
+from exact_ref import bf16_bits_to_fraction, glu_exact, rmsnorm_exact_row, rne_bf16, silu_exact
+
+pytest.importorskip("mpmath")
+EPS32 = float(np.float32(1e-6))
+
+MUTATIONS = {
+    "silu_sign": ("x / (1.0 + exp(-x))", "x / (1.0 + exp(x))"),
+    "dropped_first_term": ("for (int k = 0; k < j->K; ++k)", "for (int k = 1; k < j->K; ++k)"),
+    "up_reads_gate": ("const double pu = hk * oracle_bf16_to_double(urow[k]);",
+                      "const double pu = hk * oracle_bf16_to_double(grow[k]);"),
+    "hf_up_rounds_gate": ("const uint16_t ub = oracle_bf16_round(U);", "const uint16_t ub = oracle_bf16_round(G);"),
+    "hf_silu_on_unrounded_gate": ("oracle_silu(oracle_bf16_to_double(gb))", "oracle_silu(G)"),
+    "fused_rounds_twice": ("o = oracle_bf16_round(oracle_silu(G) * U);",
+                           "o = oracle_bf16_round(oracle_bf16_to_double(oracle_bf16_round(oracle_silu(G))) * U);"),
+    "ties_away": ("(rem == half && (n & 1))", "(rem == half)"),
+    "no_subnormals": ("(e >= -126) ? (e - 7) : -133", "(e - 7)"),
+    "batch_row_index": ("hrow = j->h + (int64_t)m * j->ldh", "hrow = j->h"),
+    "norm_mean_divisor": ("ss / (double)K", "ss / (double)(K + 1)"),
+    "norm_scale_not_centred": ("1.0 + oracle_bf16_to_double(norm_w[k])", "oracle_bf16_to_double(norm_w[k])"),
+    "norm_eps_dropped": ("sqrt(var + e)", "sqrt(var)"),
+    "residual_sign": ("oracle_bf16_to_double(xr[k]) +", "oracle_bf16_to_double(xr[k]) -"),
+}
+
+
+def quick_pins(lib) -> list:
+    """Returns the names of the pins that fail for ``lib``."""
+    fails = []
+    # rounding: random doubles over the whole range, plus ties
+    rng = np.random.default_rng(5)
+    vals = np.ldexp(rng.random(400) + 1.0, rng.integers(-140, 130, 400)) * rng.choice([-1, 1], 400)
+    ties = [1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, 2.0 ** -134, 3 * 2.0 ** -134]
+    for v in list(vals) + ties:
+        want = rne_bf16(Fraction(float(v)))
+        if want == 0 and v < 0:
+            want = 0x8000
+        if lib.oracle_bf16_round(float(v)) != want:
+            fails.append("round")
+            break
+    # SiLU closed forms
+    for x in (-3.0, 0.5, 2.0):
+        if abs(lib.oracle_silu(x) - float(silu_exact(Fraction(x)))) > 1e-15:
+            fails.append("silu")
+            break
+    # exact GLU on small integers and on N(0,1) draws, both modes
+    for mode in ("fused", "hf"):
+        for (M, N, K), kind in [((2, 5, 8), "int"), ((3, 6, 7), "normal"), ((2, 24, 8), "normal")]:
+            if kind == "int":
+                h = gi.small_int_bf16((M, K), seed=1 + M)
+                gw = gi.small_int_bf16((N, K), seed=2 + N)
+                uw = gi.small_int_bf16((N, K), seed=3 + K, lo=-3, hi=3)
+            else:
+                h = gi.bits(gi.normal_bf16((M, K), 1.0, 0, "mut-h", N))
+                gw = gi.bits(gi.normal_bf16((N, K), 0.5, 0, "mut-g", N))
+                uw = gi.bits(gi.normal_bf16((N, K), 0.5, 0, "mut-u", N))
+            out = oracle.glu_gemv(h, gw, uw, mode, lib=lib)
+            want, _, _ = glu_exact(h, gw, uw, mode)
+            nz = (want & 0x7FFF) != 0
+            if not (np.array_equal(out[nz], want[nz]) and np.all((out[~nz] & 0x7FFF) == 0)):
+                fails.append(f"glu_{mode}_{kind}")
+    # norm: high precision, and the cancelled residual
+    x = gi.bits(gi.normal_bf16((2, 48), 1.0, 0, "mut-x"))
+    r = gi.bits(gi.normal_bf16((2, 48), 1.0, 0, "mut-r"))
+    w = gi.bits(gi.normal_bf16((48,), 0.1, 0, "mut-w"))
+    s, hh = oracle.add_rmsnorm(x, r, w, 1e-6, lib=lib)
+    for m in range(2):
+        ws, wh = rmsnorm_exact_row(x[m], r[m], w, EPS32)
+        if list(s[m]) != ws or list(hh[m]) != wh:
+            fails.append("norm")
+            break
+    s0, h0 = oracle.add_rmsnorm(x, x ^ np.uint16(0x8000), w, 1e-6, lib=lib)
+    if not (np.all(s0 == 0) and np.all(h0 == 0)):
+        fails.append("norm_cancelled")
+    return fails
+
+
+@pytest.fixture(scope="module")
+def workdir(tmp_path_factory):
+    return tmp_path_factory.mktemp("oracle_mut")
+
+
+def _build_variant(workdir, name, old=None, new=None):
+    src = open(oracle.SRC).read()
+    if old is not None:
+        assert src.count(old) == 1, f"mutation anchor for {name} not unique/present"
+        src = src.replace(old, new)
+    d = os.path.join(str(workdir), name)
+    os.makedirs(d, exist_ok=True)
+    cpath = os.path.join(d, "m.c")
+    with open(cpath, "w") as f:
+        f.write(src)
+    so = oracle.build(src=cpath, out=os.path.join(d, "libm.so"))
+    return oracle.load(path=so)
+
+
+def test_unmodified_oracle_passes_quick_pins(workdir):
+    lib = _build_variant(workdir, "clean")
+    assert quick_pins(lib) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(workdir, name):
+    old, new = MUTATIONS[name]
+    lib = _build_variant(workdir, name, old, new)
+    assert quick_pins(lib), f"mutation {name} went unnoticed"

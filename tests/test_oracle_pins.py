@@ -1,0 +1,458 @@
+"""Pins for the fp64 CPU oracle: checks against things other than itself.
+
+Each test ties the oracle to exact rational arithmetic, 120-bit SiLU, a
+closed form, an invariant or a library routine, so that a plausible slip in
+the oracle (a dropped term, a wrong sign or index, a transposed operand, a
+wrong tie rule) fails at least one of them.  ``test_oracle_mutations.py``
+plants such slips in a copy of the oracle and checks they are caught.
+
+Method sources: DeepSpeed PR #8602 "Plan B: Dual-Weight GEMV" (kernel listing:
+fp32 dot products, SiLU(gate)*up, one round-to-nearest-even to bf16; b>1
+fallback F.silu(h@Wg.T)*(h@Wu.T) on bf16 tensors) and PR #9057 "Changes"
+(HF's intermediate bf16 rounding in residual/RMSNorm and GLU; zero-centred
+norm scale built in fp32).
+"""
+import math
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import glu_inputs as gi
+from exact_ref import (bf16_bits_to_fraction, fraction_to_mpf, glu_exact, mpf_to_fraction, rmsnorm_exact_row,
+                       rne_bf16, silu_exact)
+import tolerance as tol
+
+mpmath = pytest.importorskip("mpmath")
+EPS32 = float(np.float32(1e-6))
+
+
+def f2b(x: float) -> int:
+    """bf16 pattern of a value known to be exactly representable."""
+    b = struct.unpack("<I", struct.pack("<f", x))[0]
+    assert b & 0xFFFF == 0, x
+    return b >> 16
+
+
+# --------------------------------------------------------------------------
+# bf16 rounding and widening
+# --------------------------------------------------------------------------
+
+def test_bf16_widening_matches_torch_for_all_patterns(oracle_lib):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = gi.from_bits(pats).to(torch.float64).numpy()
+    got = np.array([oracle_lib.oracle_bf16_to_double(int(p)) for p in pats])
+    fin = np.isfinite(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(got[np.isinf(ref)], ref[np.isinf(ref)])
+
+
+def _random_doubles(rng, n):
+    # magnitudes across the whole bf16 range, incl. subnormal and overflow
+    e = rng.integers(-140, 130, size=n)
+    m = rng.random(n) + 1.0
+    s = rng.choice([-1.0, 1.0], size=n)
+    return s * np.ldexp(m, e)
+
+
+def _ties_and_edges():
+    vals = []
+    for b in [0x0001, 0x0002, 0x007F, 0x0080, 0x0081, 0x3F80, 0x3F81, 0x4049, 0x7F7E, 0x7F7F, 0x00FF]:
+        lo = bf16_bits_to_fraction(b)
+        hi = bf16_bits_to_fraction(b + 1) if b + 1 < 0x7F80 else Fraction(2) ** 128
+        mid = (lo + hi) / 2
+        for q in (mid, mid + (hi - lo) / 1024, mid - (hi - lo) / 1024, lo, (lo + mid) / 2):
+            f = float(q)
+            if Fraction(f) == q:   # exactly representable in binary64
+                vals.extend([f, -f])
+    vals += [2.0 ** -134, 2.0 ** -133, 3 * 2.0 ** -134, 2.0 ** -150, 1e-300, 5e-324,
+             3.4028234663852886e38, 3.3961775292304416e38, 3.3961775292304417e38, 1e39, 1e308]
+    return vals
+
+
+def test_bf16_round_equals_bruteforce_nearest_even(oracle_lib):
+    """Random doubles + constructed ties: oracle == exhaustive-table RNE."""
+    rng = np.random.default_rng(1234)
+    vals = list(_random_doubles(rng, 4000)) + _ties_and_edges()
+    for v in vals:
+        got = oracle_lib.oracle_bf16_round(float(v))
+        want = rne_bf16(Fraction(float(v)))
+        if want == 0 and v < 0:
+            want = 0x8000   # a negative value that rounds to zero keeps its sign
+        assert got == want, (v, hex(got), hex(want))
+
+
+def test_bf16_round_matches_torch_on_float32_values(oracle_lib):
+    """For binary32 inputs a single rounding equals torch's float32->bf16."""
+    g = torch.Generator().manual_seed(7)
+    x = torch.randn(20000, generator=g) * (10.0 ** torch.randint(-30, 30, (20000,), generator=g).float())
+    x = torch.cat([x, torch.tensor([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(1.0 + 2 ** -8), 2 ** -130, 3e38])])
+    want = gi.bits(x.to(torch.bfloat16))
+    got = np.array([oracle_lib.oracle_bf16_round(float(v)) for v in x.tolist()], dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_bf16_round_specials(oracle_lib):
+    assert oracle_lib.oracle_bf16_round(float("inf")) == 0x7F80
+    assert oracle_lib.oracle_bf16_round(float("-inf")) == 0xFF80
+    assert oracle_lib.oracle_bf16_round(float("nan")) & 0x7FFF > 0x7F80
+    assert oracle_lib.oracle_bf16_round(-0.0) == 0x8000
+    assert oracle_lib.oracle_bf16_round(0.0) == 0x0000
+    assert oracle_lib.oracle_bf16_round(1.0) == 0x3F80
+    # 1 + 2^-8 is the tie between 1 and 1 + 2^-7: goes to the even pattern (1)
+    assert oracle_lib.oracle_bf16_round(1.0 + 2 ** -8) == 0x3F80
+    assert oracle_lib.oracle_bf16_round(1.0 + 3 * 2 ** -8) == 0x3F82
+
+
+# --------------------------------------------------------------------------
+# SiLU
+# --------------------------------------------------------------------------
+
+def _all_finite_bf16():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    return pats[(pats & 0x7FFF) < 0x7F80]
+
+
+@pytest.mark.slow
+def test_silu_exhaustive_over_bf16_gate_values(oracle_lib):
+    """K=1, h=[1], W_gate[:,0] = every finite bf16, W_up = 1:
+    out = bf16(SiLU(g)) for every g, against 120-bit SiLU rounded by brute
+    force.  Same in HF mode (g and u=1 are already bf16)."""
+    g = _all_finite_bf16()
+    N = g.size
+    h = np.array([[f2b(1.0)]], dtype=np.uint16)
+    gw = g.reshape(N, 1)
+    uw = np.full((N, 1), f2b(1.0), dtype=np.uint16)
+    out_f = oracle.glu_gemv(h, gw, uw, "fused", lib=oracle_lib)
+    out_h = oracle.glu_gemv(h, gw, uw, "hf", lib=oracle_lib)
+    want = np.empty(N, dtype=np.uint16)
+    for i, b in enumerate(g):
+        v = rne_bf16(silu_exact(bf16_bits_to_fraction(int(b))))
+        if v == 0 and (int(b) & 0x8000):
+            v = 0x8000   # SiLU of a negative value that rounds to zero: -0
+        want[i] = v
+    # +0 and -0 are one point (G = 0 + (-0) sums to +0)
+    for out in (out_f[0], out_h[0]):
+        assert np.array_equal(tol.ordered(out), tol.ordered(want)), np.flatnonzero(out != want)[:10]
+        nz = (want & 0x7FFF) != 0
+        assert np.array_equal(out[nz], want[nz])
+
+
+def test_silu_closed_forms(oracle_lib):
+    assert oracle_lib.oracle_silu(0.0) == 0.0
+    for x in (-5.0, -1.0, -0.25, 0.5, 1.0, 3.0, 20.0):
+        want = float(silu_exact(Fraction(x)))
+        assert abs(oracle_lib.oracle_silu(x) - want) <= 4 * abs(want) * 2 ** -53
+    # SiLU(x) - SiLU(-x) = x
+    for x in (0.3, 1.7, 6.0):
+        assert abs(oracle_lib.oracle_silu(x) - oracle_lib.oracle_silu(-x) - x) < 1e-15 * max(1, x)
+
+
+# --------------------------------------------------------------------------
+# Dot products and epilogues against exact arithmetic
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 3, 4), (2, 3, 4), (3, 2, 5), (2, 5, 8)])
+def test_glu_exact_small_integers(oracle_lib, mode, shape):
+    """Small-integer operands: G and U are exact integers; the output is the
+    brute-force rounding of the 120-bit SiLU(G)*U (or the HF chain)."""
+    M, N, K = shape
+    h = gi.small_int_bf16((M, K), seed=11 + M)
+    gw = gi.small_int_bf16((N, K), seed=23 + N)
+    uw = gi.small_int_bf16((N, K), seed=37 + K, lo=-3, hi=3)
+    out, diag = oracle.glu_gemv(h, gw, uw, mode, diagnostics=True, lib=oracle_lib)
+    want, Gx, Ux = glu_exact(h, gw, uw, mode)
+    nz = (want & 0x7FFF) != 0
+    assert np.array_equal(out[nz], want[nz])
+    assert np.all((out[~nz] & 0x7FFF) == 0)
+    for m in range(M):
+        for n in range(N):
+            assert Fraction(diag["G"][m, n]) == Gx[m][n]
+            assert Fraction(diag["U"][m, n]) == Ux[m][n]
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_glu_exact_random_normal(oracle_lib, mode):
+    """N(0,1) bf16 operands, K<=8: the binary64 sums are still exact."""
+    for seed, (M, N, K) in enumerate([(1, 6, 7), (2, 4, 8), (3, 5, 3)]):
+        h = gi.bits(gi.normal_bf16((M, K), 1.0, seed, "pin-h"))
+        gw = gi.bits(gi.normal_bf16((N, K), 0.5, seed, "pin-g"))
+        uw = gi.bits(gi.normal_bf16((N, K), 0.5, seed, "pin-u"))
+        out, diag = oracle.glu_gemv(h, gw, uw, mode, diagnostics=True, lib=oracle_lib)
+        want, Gx, Ux = glu_exact(h, gw, uw, mode)
+        assert np.array_equal(out, want)
+        assert all(Fraction(diag["G"][m, n]) == Gx[m][n] for m in range(M) for n in range(N))
+        assert all(Fraction(diag["U"][m, n]) == Ux[m][n] for m in range(M) for n in range(N))
+
+
+def test_glu_abs_sums(oracle_lib):
+    h = gi.small_int_bf16((2, 6), seed=3)
+    gw = gi.small_int_bf16((3, 6), seed=4)
+    uw = gi.small_int_bf16((3, 6), seed=5)
+    _, d = oracle.glu_gemv(h, gw, uw, "fused", diagnostics=True, lib=oracle_lib)
+    hf = tol.bf16_bits_to_f64(h)
+    assert np.array_equal(d["Ag"], np.abs(hf) @ np.abs(tol.bf16_bits_to_f64(gw)).T)
+    assert np.array_equal(d["Au"], np.abs(hf) @ np.abs(tol.bf16_bits_to_f64(uw)).T)
+
+
+# --------------------------------------------------------------------------
+# Closed forms and invariants
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_zero_weights_give_positive_zero(oracle_lib, mode):
+    h = gi.bits(gi.normal_bf16((3, 64), 1.0, 0, "z-h"))
+    z = np.zeros((17, 64), dtype=np.uint16)
+    out = oracle.glu_gemv(h, z, z, mode, lib=oracle_lib)
+    assert np.all(out == 0)
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_zero_hidden_gives_zero(oracle_lib, mode):
+    h = np.zeros((2, 48), dtype=np.uint16)
+    w = gi.bits(gi.normal_bf16((9, 48), 1.0, 0, "zh-w"))
+    out = oracle.glu_gemv(h, w, w, mode, lib=oracle_lib)
+    assert np.all((out & 0x7FFF) == 0)
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_identity_rows(oracle_lib, mode):
+    """N = K, W_gate = W_up = I: out_i = SiLU(h_i) * h_i (fused: one rounding;
+    HF: bf16(bf16(SiLU(h_i)) * h_i))."""
+    K = 40
+    hb = gi.bits(gi.normal_bf16((2, K), 2.0, 5, "id-h"))
+    eye = gi.bits(torch.eye(K, dtype=torch.bfloat16))
+    out = oracle.glu_gemv(hb, eye, eye, mode, lib=oracle_lib)
+    for m in range(2):
+        for i in range(K):
+            hi = bf16_bits_to_fraction(int(hb[m, i]))
+            if mode == "fused":
+                want = rne_bf16(silu_exact(hi) * hi)
+            else:
+                want = rne_bf16(bf16_bits_to_fraction(rne_bf16(silu_exact(hi))) * hi)
+            if hi == 0:
+                assert out[m, i] & 0x7FFF == 0
+            else:
+                assert out[m, i] == want, (m, i)
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_swapping_gate_and_up_moves_only_the_silu(oracle_lib, mode):
+    """glu(h, W_up, W_gate) = bf16(SiLU(U) * G): the roles of the two dot
+    products swap and nothing else changes."""
+    M, N, K = 2, 33, 96
+    h = gi.bits(gi.normal_bf16((M, K), 1.0, 2, "sw-h"))
+    gw = gi.bits(gi.normal_bf16((N, K), 0.1, 2, "sw-g"))
+    uw = gi.bits(gi.normal_bf16((N, K), 0.1, 2, "sw-u"))
+    _, d = oracle.glu_gemv(h, gw, uw, mode, diagnostics=True, lib=oracle_lib)
+    out_sw, d_sw = oracle.glu_gemv(h, uw, gw, mode, diagnostics=True, lib=oracle_lib)
+    assert np.array_equal(d_sw["G"], d["U"]) and np.array_equal(d_sw["U"], d["G"])
+    for m in range(M):
+        for n in range(N):
+            G, U = Fraction(d["G"][m, n]), Fraction(d["U"][m, n])
+            if mode == "fused":
+                want = rne_bf16(silu_exact(U) * G)
+            else:
+                ub = bf16_bits_to_fraction(rne_bf16(U))
+                gb = bf16_bits_to_fraction(rne_bf16(G))
+                want = rne_bf16(bf16_bits_to_fraction(rne_bf16(silu_exact(ub))) * gb)
+            assert out_sw[m, n] == want
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_power_of_two_scaling_of_up(oracle_lib, mode):
+    """W_up -> 2*W_up doubles every output exactly (scaling by 2 commutes with
+    round-to-nearest-even away from overflow and subnormals)."""
+    M, N, K = 2, 50, 128
+    h = gi.bits(gi.normal_bf16((M, K), 1.0, 3, "p2-h"))
+    gw = gi.bits(gi.normal_bf16((N, K), 0.1, 3, "p2-g"))
+    u = gi.normal_bf16((N, K), 0.1, 3, "p2-u")
+    o1 = oracle.glu_gemv(h, gw, gi.bits(u), mode, lib=oracle_lib)
+    o2 = oracle.glu_gemv(h, gw, gi.bits(u * 2), mode, lib=oracle_lib)
+    v1, v2 = tol.bf16_bits_to_f64(o1), tol.bf16_bits_to_f64(o2)
+    ok = np.abs(v1) > 2.0 ** -120
+    assert ok.mean() > 0.9
+    assert np.array_equal(v2[ok], 2 * v1[ok])
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_row_permutation_permutes_outputs(oracle_lib, mode):
+    M, N, K = 3, 41, 72
+    h = gi.bits(gi.normal_bf16((M, K), 1.0, 4, "pm-h"))
+    gw = gi.bits(gi.normal_bf16((N, K), 0.1, 4, "pm-g"))
+    uw = gi.bits(gi.normal_bf16((N, K), 0.1, 4, "pm-u"))
+    perm = np.random.default_rng(0).permutation(N)
+    o = oracle.glu_gemv(h, gw, uw, mode, lib=oracle_lib)
+    op = oracle.glu_gemv(h, gw[perm], uw[perm], mode, lib=oracle_lib)
+    assert np.array_equal(op, o[:, perm])
+
+
+def test_thread_count_does_not_change_results(oracle_lib):
+    M, N, K = 2, 257, 300
+    h = gi.bits(gi.normal_bf16((M, K), 1.0, 6, "th-h"))
+    gw = gi.bits(gi.normal_bf16((N, K), 0.06, 6, "th-g"))
+    uw = gi.bits(gi.normal_bf16((N, K), 0.06, 6, "th-u"))
+    a = oracle.glu_gemv(h, gw, uw, "hf", nthreads=1, lib=oracle_lib)
+    b = oracle.glu_gemv(h, gw, uw, "hf", nthreads=7, lib=oracle_lib)
+    assert np.array_equal(a, b)
+
+
+def test_empty_shapes(oracle_lib):
+    h = np.zeros((0, 8), dtype=np.uint16)
+    w = np.zeros((4, 8), dtype=np.uint16)
+    assert oracle.glu_gemv(h, w, w, lib=oracle_lib).shape == (0, 4)
+    # K == 0: empty sums, SiLU(0) * 0 = +0
+    h0 = np.zeros((2, 0), dtype=np.uint16)
+    w0 = np.zeros((3, 0), dtype=np.uint16)
+    assert np.all(oracle.glu_gemv(h0, w0, w0, "hf", lib=oracle_lib) == 0)
+    assert np.all(oracle.glu_gemv(h0, w0, w0, "fused", lib=oracle_lib) == 0)
+
+
+# --------------------------------------------------------------------------
+# Library composite cross-checks
+# --------------------------------------------------------------------------
+
+def test_fused_matches_float64_torch_composite(oracle_lib):
+    """F.silu(h@Wg.T) * (h@Wu.T) in float64 (a BLAS sum, another order), then
+    one brute-force rounding: equal away from near-ties."""
+    M, N, K = 2, 64, 256
+    h = gi.normal_bf16((M, K), 1.0, 8, "c64-h")
+    gw = gi.normal_bf16((N, K), 0.0625, 8, "c64-g")
+    uw = gi.normal_bf16((N, K), 0.0625, 8, "c64-u")
+    out = oracle.glu_gemv(gi.bits(h), gi.bits(gw), gi.bits(uw), "fused", lib=oracle_lib)
+    h64, g64, u64 = (t.to(torch.float64) for t in (h, gw, uw))
+    ref = (torch.nn.functional.silu(h64 @ g64.T) * (h64 @ u64.T)).numpy()
+    want = np.array([[rne_bf16(Fraction(float(v))) for v in row] for row in ref], dtype=np.uint16)
+    assert np.mean(out == want) >= 0.999
+    assert tol.ulp_distance(out, want).max() <= 1
+
+
+def test_hf_matches_bf16_torch_composite(oracle_lib):
+    """The HF composite on bf16 CPU tensors (fp32 accumulation inside the
+    matmul, bf16 tensors between ops) agrees within the parity bar."""
+    M, N, K = 4, 512, 1024
+    h = gi.normal_bf16((M, K), 1.0, 9, "cbf-h")
+    gw = gi.normal_bf16((N, K), 1 / 32, 9, "cbf-g")
+    uw = gi.normal_bf16((N, K), 1 / 32, 9, "cbf-u")
+    out, diag = oracle.glu_gemv(gi.bits(h), gi.bits(gw), gi.bits(uw), "hf", diagnostics=True, lib=oracle_lib)
+    ref = torch.nn.functional.silu(h @ gw.T) * (h @ uw.T)
+    tau = tol.conditioning_floor(diag, K, "hf")
+    st = tol.compare(gi.bits(ref), out, tau)
+    assert tol.passes(st), st
+    assert st["exact_frac"] > 0.95
+
+
+# --------------------------------------------------------------------------
+# Residual add + zero-centred RMSNorm
+# --------------------------------------------------------------------------
+
+def test_norm_against_high_precision(oracle_lib):
+    M, K = 3, 96
+    x = gi.bits(gi.normal_bf16((M, K), 1.0, 10, "n-x"))
+    r = gi.bits(gi.normal_bf16((M, K), 1.0, 10, "n-r"))
+    w = gi.bits(gi.normal_bf16((K,), 0.1, 10, "n-w"))
+    s, h = oracle.add_rmsnorm(x, r, w, 1e-6, lib=oracle_lib)
+    for m in range(M):
+        ws, wh = rmsnorm_exact_row(x[m], r[m], w, EPS32)
+        assert list(s[m]) == ws
+        assert list(h[m]) == wh
+
+
+def test_norm_small_rows_eps_matters(oracle_lib):
+    """Rows with mean(s^2) near eps: the eps term is visible in h."""
+    M, K = 2, 32
+    x = gi.bits(gi.normal_bf16((M, K), 1e-3, 17, "ne-x"))
+    r = np.zeros((M, K), dtype=np.uint16)
+    w = gi.bits(gi.normal_bf16((K,), 0.1, 17, "ne-w"))
+    _, h = oracle.add_rmsnorm(x, r, w, 1e-6, lib=oracle_lib)
+    for m in range(M):
+        _, wh = rmsnorm_exact_row(x[m], r[m], w, EPS32)
+        assert list(h[m]) == wh
+    _, h_noeps = oracle.add_rmsnorm(x, r, w, 0.0, lib=oracle_lib)
+    assert not np.array_equal(h, h_noeps)
+
+
+def test_norm_zero_weight_is_plain_rmsnorm(oracle_lib):
+    """norm_w = 0 gives (1 + 0) = 1: h = bf16(s / sqrt(mean(s^2) + eps))."""
+    K = 64
+    x = gi.bits(gi.normal_bf16((1, K), 1.0, 12, "nz-x"))
+    r = np.zeros((1, K), dtype=np.uint16)
+    w = np.zeros((K,), dtype=np.uint16)
+    s, h = oracle.add_rmsnorm(x, r, w, 1e-6, lib=oracle_lib)
+    assert np.array_equal(s, x)
+    xv = tol.bf16_bits_to_f64(x[0])
+    ref = xv / np.sqrt(np.mean(xv * xv) + EPS32)
+    want = np.array([rne_bf16(Fraction(float(v))) for v in ref], dtype=np.uint16)
+    assert tol.ulp_distance(h[0], want).max() == 0
+
+
+def test_norm_constant_row(oracle_lib):
+    """s = c everywhere: h = bf16(c / sqrt(c^2 + eps))."""
+    K = 128
+    for c in (0.5, -3.0, 1e-3):
+        cb = oracle_lib.oracle_bf16_round(c)
+        x = np.full((1, K), cb, dtype=np.uint16)
+        r = np.zeros((1, K), dtype=np.uint16)
+        w = np.zeros((K,), dtype=np.uint16)
+        _, h = oracle.add_rmsnorm(x, r, w, 1e-6, lib=oracle_lib)
+        cv = bf16_bits_to_fraction(cb)
+        val = fraction_to_mpf(cv) / mpmath.sqrt(fraction_to_mpf(cv * cv + Fraction(EPS32)))
+        assert np.all(h == rne_bf16(mpf_to_fraction(val)))
+
+
+def test_norm_cancelled_residual_gives_zero(oracle_lib):
+    """x = -residual: s = +0 everywhere, var = 0, h = 0 / sqrt(eps) = 0."""
+    K = 80
+    x = gi.bits(gi.normal_bf16((2, K), 1.0, 13, "nc-x"))
+    r = x ^ np.uint16(0x8000)
+    w = gi.bits(gi.normal_bf16((K,), 0.1, 13, "nc-w"))
+    s, h = oracle.add_rmsnorm(x, r, w, 1e-6, lib=oracle_lib)
+    assert np.all(s == 0) and np.all(h == 0)
+
+
+def test_residual_sum_is_one_correct_rounding(oracle_lib):
+    M, K = 4, 200
+    x = gi.bits(gi.normal_bf16((M, K), 1.0, 14, "rs-x"))
+    r = gi.bits(gi.normal_bf16((M, K), 3.0, 14, "rs-r"))
+    w = np.zeros((K,), dtype=np.uint16)
+    s, _ = oracle.add_rmsnorm(x, r, w, 1e-6, lib=oracle_lib)
+    want = np.array([[rne_bf16(bf16_bits_to_fraction(int(a)) + bf16_bits_to_fraction(int(b)))
+                      for a, b in zip(xr, rr)] for xr, rr in zip(x, r)], dtype=np.uint16)
+    nz = (want & 0x7FFF) != 0
+    assert np.array_equal(s[nz], want[nz])
+    assert np.all((s[~nz] & 0x7FFF) == 0)
+
+
+def test_norm_matches_fp32_torch_formula(oracle_lib):
+    """HF's zero-centred RMSNorm in fp32 torch (x.float(); rsqrt(mean+eps);
+    *(1+w.float()); to bf16): within one bf16 step, nearly always equal."""
+    M, K = 8, 2560
+    x = gi.normal_bf16((M, K), 1.0, 15, "nt-x")
+    r = gi.normal_bf16((M, K), 1.0, 15, "nt-r")
+    w = gi.normal_bf16((K,), 0.1, 15, "nt-w")
+    s, h = oracle.add_rmsnorm(gi.bits(x), gi.bits(r), gi.bits(w), 1e-6, lib=oracle_lib)
+    st = (x + r)  # bf16 add on CPU: one rounding
+    assert np.array_equal(gi.bits(st), s)
+    sf = st.float()
+    ref = (sf * torch.rsqrt(sf.pow(2).mean(-1, keepdim=True) + 1e-6)) * (1.0 + w.float())
+    d = tol.ulp_distance(gi.bits(ref.to(torch.bfloat16)), h)
+    assert d.max() <= 1 and np.mean(d == 0) > 0.99
+
+
+def test_fused_segment_is_norm_then_glu(oracle_lib):
+    M, N, K = 2, 40, 64
+    x = gi.bits(gi.normal_bf16((M, K), 1.0, 16, "fs-x"))
+    r = gi.bits(gi.normal_bf16((M, K), 1.0, 16, "fs-r"))
+    w = gi.bits(gi.normal_bf16((K,), 0.1, 16, "fs-w"))
+    gw = gi.bits(gi.normal_bf16((N, K), 0.125, 16, "fs-g"))
+    uw = gi.bits(gi.normal_bf16((N, K), 0.125, 16, "fs-u"))
+    out, res, h = oracle.add_rmsnorm_glu(x, r, w, 1e-6, gw, uw, "hf", lib=oracle_lib)
+    s2, h2 = oracle.add_rmsnorm(x, r, w, 1e-6, lib=oracle_lib)
+    assert np.array_equal(res, s2) and np.array_equal(h, h2)
+    want, _, _ = glu_exact(h2, gw, uw, "hf")
+    assert np.array_equal(out, want)
