@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark of the dual-weight GLU GEMV on GB300.
+
+Default workload: glu_gemv at M=1, K=2560, N=9728 (Qwen3.5-4B MLP gate/up),
+HF-boundary rounding, 32 independent weight pairs (3.19 GB) cycled so every
+call streams its ~100 MB of weights from HBM (inputs larger than L2).
+
+A step is one pass over the cycled layers (one call per layer), captured
+once as a CUDA graph and replayed, as a decode step replays its graph.
+Metric: achieved HBM GB/s of algorithmic bytes (both weights once, h, out),
+plus us/call.  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+                  [--workload NAME] [--M M] [--mode fused|hf] [--layers L]
+Under torchrun every rank runs its own replica (weak scaling, no collective
+on the data path); the timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import glu_inputs as gi  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["memory_bound_glu_gb300/csrc/glu_kernels.cuh", "memory_bound_glu_gb300/csrc/ptx.cuh",
+                  "memory_bound_glu_gb300/csrc/mbglu_api.cu"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--workload", default=gi.HEADLINE, choices=sorted(gi.WORKLOADS))
+    ap.add_argument("--M", type=int, default=None)
+    ap.add_argument("--mode", default=None, choices=["fused", "hf"])
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload, M, mode):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    sources still hash to what was profiled; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    rec = d.get(f"{workload}/M{M}/{mode}")
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region (200 ms period)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if not self.proc:
+            return None
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1 + 0.25):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(w, M, mode, seconds, max_rows=None):
+    """Times oracle calls on row slices of layer 0 until `seconds` pass.
+    Returns (GB/s of algorithmic bytes, description, threads)."""
+    import oracle
+    g, u = gi.layer_weights(w, 0)
+    gb, ub = gi.bits(g), gi.bits(u)
+    threads = oracle.default_threads()
+    rows = w.N if max_rows is None else min(w.N, max_rows)
+    gb, ub = np.ascontiguousarray(gb[:rows]), np.ascontiguousarray(ub[:rows])
+    if w.op == "glu_gemv":
+        hb = gi.bits(gi.hidden(w, M))
+        call = lambda: oracle.glu_gemv(hb, gb, ub, mode, nthreads=threads)  # noqa: E731
+        per_call = 2 * rows * w.K * 2 + M * w.K * 2 + M * rows * 2
+    else:
+        x, r, nw = (gi.bits(t) for t in gi.norm_inputs(w, M))
+        call = lambda: oracle.add_rmsnorm_glu(x, r, nw, w.eps, gb, ub, mode, nthreads=threads)  # noqa: E731
+        per_call = 2 * rows * w.K * 2 + 3 * M * w.K * 2 + w.K * 2 + M * rows * 2
+    call()  # warm
+    n, t0 = 0, time.perf_counter()
+    while True:
+        call()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    desc = (f"{n} oracle calls of {w.op} M={M} K={w.K} N={rows} ({mode}) on layer 0 "
+            f"(rows 0..{rows - 1} of {w.N}), {threads} threads, {el:.1f} s")
+    return per_call * n / el / 1e9, desc, threads, el / n, per_call
+
+
+def run_reference(args, w, M, mode, world, rank):
+    """Reference arm: the fp64 oracle on the host cores, bounded steps."""
+    if rank != 0:
+        return
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    import oracle
+    g, u = gi.layer_weights(w, 0)
+    threads = oracle.default_threads()
+    # size the per-step row sample so the whole run stays within ~2 minutes
+    hb = gi.bits(gi.hidden(w, M)) if w.op == "glu_gemv" else None
+    probe_rows = min(w.N, 256)
+    t0 = time.perf_counter()
+    oracle.glu_gemv(hb if hb is not None else gi.bits(gi.norm_inputs(w, M)[0]),
+                    gi.bits(g[:probe_rows]), gi.bits(u[:probe_rows]), mode, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / probe_rows
+    budget = 120.0 / (steps + warm)
+    rows = int(max(8, min(w.N, budget / max(per_row, 1e-9))))
+    gb, ub = np.ascontiguousarray(gi.bits(g)[:rows]), np.ascontiguousarray(gi.bits(u)[:rows])
+    if w.op == "glu_gemv":
+        call = lambda: oracle.glu_gemv(hb, gb, ub, mode, nthreads=threads)  # noqa: E731
+        per_step = 2 * rows * w.K * 2 + M * w.K * 2 + M * rows * 2
+    else:
+        x, r, nw = (gi.bits(t) for t in gi.norm_inputs(w, M))
+        call = lambda: oracle.add_rmsnorm_glu(x, r, nw, w.eps, gb, ub, mode, nthreads=threads)  # noqa: E731
+        per_step = 2 * rows * w.K * 2 + 3 * M * w.K * 2 + w.K * 2 + M * rows * 2
+    for _ in range(warm):
+        call()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        call()
+    el = time.perf_counter() - t0
+    value = per_step * steps / el / 1e9
+    sample = (f"each step: one oracle call of {w.op} M={M} K={w.K} on rows 0..{rows - 1} of layer 0 "
+              f"(of N={w.N}), {mode} mode")
+    line = {
+        "impl": "reference", "metric": "GLU GEMV achieved HBM GB/s (cold L2), us/call at M=1",
+        "value": round(value, 4), "unit": "GB/s", "higher_is_better": True, "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": round(el / steps * 1e3, 4),
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, M, mode, w.layers),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w, M, mode, layers):
+    wb = w.weight_bytes() * layers
+    return {"workload": w.name, "op": w.op, "M": M, "K": w.K, "N": w.N, "mode": mode, "layers": layers,
+            "l2": f"inputs larger than L2: {layers} cycled weight pairs, {wb / 1e9:.2f} GB",
+            "launch": f"one CUDA graph of {layers} calls per step"}
+
+
+# ---------------------------------------------------------------------------
+# my arm
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    w = gi.WORKLOADS[args.workload]
+    M = args.M if args.M is not None else w.Ms[0]
+    mode = args.mode or w.modes[0]
+    L = args.layers or w.layers
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        run_reference(args, w, M, mode, world, rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    import memory_bound_glu_gb300 as mb
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mb.lib()
+
+    # inputs: resident in HBM before the timed region
+    gates, ups = [], []
+    for layer in range(L):
+        g, u = gi.layer_weights(w, layer)
+        gates.append(g.to(dev))
+        ups.append(u.to(dev))
+        del g, u
+    if w.op == "glu_gemv":
+        h_cpu = gi.hidden(w, M)
+        h = h_cpu.to(dev)
+    else:
+        x_cpu, r_cpu, nw_cpu = gi.norm_inputs(w, M)
+        x, nw = x_cpu.to(dev), nw_cpu.to(dev)
+        residuals = [r_cpu.to(dev) for _ in range(L)]
+    outs = torch.empty((L, M, w.N), dtype=torch.bfloat16, device=dev)
+    launches_per_call = 1 if w.op == "glu_gemv" else 2
+
+    def one_step():
+        for i in range(L):
+            if w.op == "glu_gemv":
+                mb.glu_gemv(h, gates[i], ups[i], out=outs[i], mode=mode)
+            else:
+                mb.add_rmsnorm_glu(x, residuals[i], nw, w.eps, gates[i], ups[i], out=outs[i], mode=mode)
+
+    stream = torch.cuda.Stream(dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(stream):
+        one_step()  # first calls initialise the library's per-device table before capture
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            one_step()
+    torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            graph.replay()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local)
+    if not args.no_clocks:
+        sampler.start()
+        time.sleep(1.0)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(world)
+    ms = start.elapsed_time(end)
+    clocks = None if args.no_clocks else sampler.stop(t_wall0, t_wall1)
+    ms_max = max_over_ranks(ms, world, dev)
+    err = mb.read_device_error()
+    if err:
+        raise RuntimeError(f"device error word {err} after the timed region")
+
+    bytes_per_call = w.algorithmic_bytes(M)
+    calls = args.steps * L
+    us_per_call = ms_max * 1e3 / calls
+    gbs = bytes_per_call / (us_per_call * 1e-6) / 1e9
+    value = gbs * world
+    peak, peak_kind = measured_peaks()
+
+    # e2e: the public Python API, pinned host input -> device, results -> host
+    e2e = None
+    if args.e2e_steps > 0:
+        if w.op == "glu_gemv":
+            h_host = h_cpu.pin_memory()
+            in_bytes = h_host.numel() * 2
+        else:
+            x_host = x_cpu.pin_memory()
+            r_host = r_cpu.pin_memory()
+            in_bytes = (x_host.numel() + r_host.numel() * L) * 2
+        out_host = torch.empty((L, M, w.N), dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step():
+            if w.op == "glu_gemv":
+                h.copy_(h_host, non_blocking=True)
+            else:
+                x.copy_(x_host, non_blocking=True)
+                for i in range(L):
+                    residuals[i].copy_(r_host, non_blocking=True)
+            one_step()
+            out_host.copy_(outs, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(5):
+                e2e_step()
+            torch.cuda.synchronize(dev)
+            barrier(world)
+            t0 = time.perf_counter()
+            for _ in range(args.e2e_steps):
+                e2e_step()
+            torch.cuda.synchronize(dev)
+            el = max_over_ranks(time.perf_counter() - t0, world, dev)
+            barrier(world)
+        e2e = {"value": round(bytes_per_call * L * args.e2e_steps / el / 1e9 * world, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_host.numel() * 2,
+               "ms_per_step": round(el / args.e2e_steps * 1e3, 4),
+               "how": "eager public-API calls (no graph), host copies inside the timed region"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, thr, _, _ = oracle_sample_rate(w, M, mode, args.cpu_seconds)
+        cpu = {"value": round(v, 4), "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        traffic = recorded_traffic(w.name, M, mode)
+        line = {
+            "metric": "GLU GEMV achieved HBM GB/s (cold L2), us/call at M=1",
+            "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms_max / args.steps, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded torch.randn, bf16)", "config": config_dict(w, M, mode, L),
+            "us_per_call": round(us_per_call, 3), "bytes_per_call": bytes_per_call,
+            "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                         if peak_kind == "measured" else "fallback 6.8 TB/s",
+                         "traffic": traffic, "kernel": "glu_stream_kernel",
+                         "achieved_how": "algorithmic bytes per launch / (CUDA-event time of the timed "
+                                         "graph replays / launches)"},
+            "gpu_launches": calls * launches_per_call,
+            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

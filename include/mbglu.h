@@ -1,0 +1,166 @@
+/*
+ * mbglu.h -- C ABI of libmbglu.so: the decode-step dual-weight GLU GEMV on
+ * GB300 (sm_103a).
+ *
+ *   out[m, n] = SiLU( sum_k h[m,k] * gate_w[n,k] ) * ( sum_k h[m,k] * up_w[n,k] )
+ *
+ * for a small batch (1 <= M <= 16) of bf16 hidden rows, reading the two
+ * nn.Linear-layout weight matrices in place (no concatenated copy), with an
+ * optional fused residual-add + zero-centred RMSNorm in front.
+ *
+ * Sources (DeepSpeed pull requests, as printed on their web pages):
+ *   [8602/PlanB]   PR #8602 "feat(rollout): HybridEngineRollout graph capture
+ *                  + segment-KI for Qwen3.5 hybrid", comment "Plan B:
+ *                  Dual-Weight GEMV -- Investigation Results & Implementation"
+ *                  (sections "Plan B Design: kernel adapts to the weights",
+ *                  "Why cuBLAS-level performance is achievable at b=1").
+ *   [8602/fused_glu] PR #8602 commit "expr(segment-ki): native CUDA fused_glu
+ *                  kernel + GPU perf matrix" (single vs double rounding).
+ *   [9057/Changes] PR #9057 "fix(module-inject): preserve HF precision
+ *                  boundaries in segKI kernels", section "Changes"; its
+ *                  commit "decode attention ... real row stride" (pass the
+ *                  true row stride, fail closed on a mismatch).
+ *
+ * Conventions for every entry point:
+ *   - bf16 values are passed as raw 16-bit patterns (mbglu_bf16).
+ *   - Matrices are row-major; ld* are row strides in ELEMENTS, the K (inner)
+ *     dimension is contiguous.
+ *   - All data pointers are DEVICE pointers on the current CUDA device,
+ *     owned by the caller (any allocator).  The library allocates nothing
+ *     per call and keeps no state derived from the weights, so in-place
+ *     weight updates are always seen.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream); no
+ *     host synchronisation, no host reads of device data.
+ *   - Arguments are validated on the host before anything is launched; a
+ *     non-zero status means nothing was launched.  No C++ exception crosses
+ *     this boundary.
+ *   - The fast kernels stream both weight matrices through shared memory
+ *     with bulk asynchronous copies; they need gate_w/up_w 16-byte aligned,
+ *     ld_gate and ld_up multiples of 8, and K a multiple of 8.  Other
+ *     2-byte-aligned inputs run on a slower generic kernel with identical
+ *     arithmetic rules.
+ *   - Results are bitwise deterministic run to run (no atomics in any sum).
+ */
+#ifndef MBGLU_H
+#define MBGLU_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MBGLU_ABI_VERSION 1
+#define MBGLU_MAX_M 16
+
+typedef uint16_t mbglu_bf16;   /* raw bf16 bits */
+
+/*
+ * Rounding mode of the GLU epilogue.
+ *  MBGLU_MODE_FUSED  single rounding: out = bf16( SiLU(g) * u ), g and u fp32
+ *                    accumulations, SiLU and the product in fp32.
+ *                    [8602/PlanB] kernel listing; [8602/fused_glu].
+ *  MBGLU_MODE_HF     HF-boundary rounding, as the bf16 composite
+ *                    F.silu(h @ Wg.T) * (h @ Wu.T) materialises it:
+ *                    gb = bf16(g), ub = bf16(u), sb = bf16(SiLU(gb)) with SiLU
+ *                    in fp32, out = bf16(sb * ub).
+ *                    [8602/PlanB] b>1 fallback; [9057/Changes] "Restore HF's
+ *                    intermediate BF16 rounding in ... GLU".
+ * SiLU(x) = x / (1 + exp(-x)) with the precise expf and IEEE division.
+ */
+typedef enum { MBGLU_MODE_FUSED = 0, MBGLU_MODE_HF = 1 } mbglu_mode;
+
+typedef int mbglu_status;
+#define MBGLU_OK            0
+#define MBGLU_ERR_NULL      1   /* a required pointer is NULL */
+#define MBGLU_ERR_SHAPE     2   /* M, N or K negative; M > MBGLU_MAX_M; K == 0 with the norm;
+                                   add_rmsnorm_glu with M*K*2 bytes above its shared-memory limit */
+#define MBGLU_ERR_STRIDE    3   /* a leading dimension smaller than the row it holds */
+#define MBGLU_ERR_ALIGN     4   /* a pointer not 2-byte aligned */
+#define MBGLU_ERR_MODE      5   /* mode is neither FUSED nor HF */
+#define MBGLU_ERR_ALIAS     6   /* an output overlaps an input it must not overlap */
+#define MBGLU_ERR_CUDA      7   /* a CUDA runtime call failed; see mbglu_last_cuda_error() */
+#define MBGLU_ERR_TIMEOUT   8   /* a bounded device-side wait gave up (reported by
+                                   mbglu_read_device_error, never by a launch) */
+
+/*
+ * glu_gemv -- the dual-weight GLU GEMV.  [8602/PlanB] "Plan B Design": the
+ * kernel reads gate.weight and up.weight directly, fp32 accumulation, SiLU on
+ * the gate product times the up product, one output per feature.
+ *
+ *   h       [M, K] bf16, row stride ldh >= K          (read)
+ *   gate_w  [N, K] bf16, row stride ld_gate >= K      (read, in place)
+ *   up_w    [N, K] bf16, row stride ld_up >= K        (read, in place)
+ *   out     [M, N] bf16, row stride ldo >= N          (written)
+ *   0 <= M <= MBGLU_MAX_M, N >= 0, K >= 0.
+ *   M == 0 or N == 0: no-op, MBGLU_OK.  K == 0: out = +0 (SiLU(0) * 0).
+ *   out must not overlap h, gate_w or up_w (MBGLU_ERR_ALIAS).
+ * Row strides are explicit because decode code slices operands out of fused
+ * buffers ([9057/Changes] strided-view fixes: pass the real row stride, fail
+ * closed on a mismatch).
+ */
+mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh,
+                      const mbglu_bf16 *gate_w, int64_t ld_gate,
+                      const mbglu_bf16 *up_w, int64_t ld_up,
+                      mbglu_bf16 *out, int64_t ldo,
+                      int M, int N, int K, mbglu_mode mode,
+                      cudaStream_t stream);
+
+/*
+ * add_rmsnorm_glu -- residual add + zero-centred RMSNorm, then glu_gemv on
+ * the normed rows.  [9057/Changes] "Restore HF's intermediate BF16 rounding in
+ * residual/RMSNorm ... construct zero-centered norm scales in FP32".
+ *
+ *   x         [M, K] bf16, contiguous                        (read)
+ *   residual  [M, K] bf16, contiguous                        (read, then
+ *             overwritten with s = bf16(x + residual): the updated residual
+ *             stream the next layer needs)
+ *   norm_w    [K] bf16                                       (read)
+ *   eps       added to the mean square inside the root (e.g. 1e-6)
+ *   gate_w, up_w  [N, K] bf16, contiguous (row stride K)     (read, in place)
+ *   out       [M, N] bf16, contiguous                        (written)
+ * Per row, in fp32:  var = mean_k s^2;  h = bf16( (s * rsqrt(var + eps)) *
+ * (1 + (float)norm_w) );  then out = GLU(h) in `mode` (mode affects only
+ * the GLU epilogue; s and h round to bf16 in both modes).
+ *   1 <= K, 0 <= M <= MBGLU_MAX_M, M*K*2 bytes must fit the kernel's
+ *   shared-memory budget (M*K <= 81920, e.g. M=16 with K=5120).
+ *   out must not overlap any input; residual must not overlap x partially,
+ *   nor norm_w, gate_w, up_w (MBGLU_ERR_ALIAS).  residual == x is allowed.
+ * Two kernels run on `stream`: the residual add, then the GEMV, launched
+ * with programmatic dependent launch so the GEMV prefetches weights while the
+ * add finishes; it reads residual only after the add has completed.
+ */
+mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual,
+                             const mbglu_bf16 *norm_w, float eps,
+                             const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w,
+                             mbglu_bf16 *out, int M, int N, int K,
+                             mbglu_mode mode, cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *mbglu_status_string(mbglu_status s);
+
+/* MBGLU_ABI_VERSION of the loaded library. */
+int mbglu_abi_version(void);
+
+/* cudaError_t of the most recent failing CUDA call made by this library on
+ * the calling host thread (0 if none). */
+int mbglu_last_cuda_error(void);
+
+/* Which kernel the calling thread's last successful call launched:
+ * 0 none (no-op), 1 streaming fast kernel, 2 generic kernel, 3 zero fill. */
+int mbglu_last_variant(void);
+
+/*
+ * Reads and clears the device error word of the current device.  Kernels
+ * never trap: a bounded wait that gives up records MBGLU_ERR_TIMEOUT here and
+ * the kernel returns.  SYNCHRONOUS: waits for the device to finish its work.
+ * Returns MBGLU_OK or MBGLU_ERR_CUDA; *word receives the recorded code.
+ */
+mbglu_status mbglu_read_device_error(int *word);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MBGLU_H */

@@ -1,0 +1,162 @@
+"""ctypes binding of libmbglu.so (C ABI in include/mbglu.h).
+
+Argument marshalling only: tensors become device pointers, row strides and
+the current CUDA stream; every step of the computation runs in the library's
+kernels.  There is no fallback: if the library is missing or a call fails,
+an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmbglu.so")
+
+MODE_FUSED = 0
+MODE_HF = 1
+_MODES = {"fused": MODE_FUSED, "hf": MODE_HF, MODE_FUSED: MODE_FUSED, MODE_HF: MODE_HF}
+MAX_M = 16
+
+# Every symbol include/mbglu.h declares.
+EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "mbglu_status_string", "mbglu_abi_version",
+           "mbglu_last_cuda_error", "mbglu_last_variant", "mbglu_read_device_error")
+
+_lib = None
+
+
+class MbgluError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = lib().mbglu_status_string(status).decode()
+        if status == 7:
+            msg += f" (cudaError {lib().mbglu_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}")
+
+
+def _bind(l):
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    l.glu_gemv.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp]
+    l.glu_gemv.restype = i32
+    l.add_rmsnorm_glu.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32, i32, vp]
+    l.add_rmsnorm_glu.restype = i32
+    l.mbglu_status_string.argtypes = [i32]
+    l.mbglu_status_string.restype = ctypes.c_char_p
+    l.mbglu_abi_version.restype = i32
+    l.mbglu_last_cuda_error.restype = i32
+    l.mbglu_last_variant.restype = i32
+    l.mbglu_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    l.mbglu_read_device_error.restype = i32
+    return l
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        _lib = _bind(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def _stream_handle(device, stream):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t, name, dim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must be {dim}-D, got shape {tuple(t.shape)}")
+    if t.numel() and t.stride(-1) != 1:
+        raise ValueError(f"{name} must have a contiguous last dimension")
+
+
+def glu_gemv(h, gate_w, up_w, out=None, mode="fused", stream=None):
+    """out[M,N] = SiLU(h @ gate_w.T) * (h @ up_w.T) in one pass (bf16).
+
+    h is [M,K] (or [K]); gate_w, up_w are [N,K] nn.Linear weights read in
+    place; mode "fused" (one rounding) or "hf" (HF bf16 boundaries).  Row
+    strides are passed through, so sliced views work without copies.
+    """
+    squeeze = h.dim() == 1
+    h2 = h.unsqueeze(0) if squeeze else h
+    _check(h2, "h", 2)
+    _check(gate_w, "gate_w", 2)
+    _check(up_w, "up_w", 2)
+    M, K = h2.shape
+    N = gate_w.shape[0]
+    if tuple(gate_w.shape) != (N, K) or tuple(up_w.shape) != (N, K):
+        raise ValueError(f"weights must be [N,K]=[{N},{K}], got {tuple(gate_w.shape)}, {tuple(up_w.shape)}")
+    dev = h2.device
+    if gate_w.device != dev or up_w.device != dev:
+        raise ValueError("all tensors must be on one device")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    out2 = out.unsqueeze(0) if out.dim() == 1 else out
+    _check(out2, "out", 2)
+    if tuple(out2.shape) != (M, N) or out2.device != dev:
+        raise ValueError(f"out must be [{M},{N}] on {dev}")
+    with torch.cuda.device(dev):
+        st = lib().glu_gemv(h2.data_ptr(), h2.stride(0), gate_w.data_ptr(), gate_w.stride(0),
+                            up_w.data_ptr(), up_w.stride(0), out2.data_ptr(), out2.stride(0),
+                            M, N, K, _MODES[mode], _stream_handle(dev, stream))
+    if st != 0:
+        raise MbgluError(st, "glu_gemv")
+    return out2.view(N) if squeeze else out
+
+
+def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf", stream=None):
+    """residual <- bf16(x + residual); h = zero-centred RMSNorm(residual);
+    out = GLU(h).  Returns out; residual is updated in place."""
+    _check(x, "x", 2)
+    _check(residual, "residual", 2)
+    _check(norm_w, "norm_w", 1)
+    _check(gate_w, "gate_w", 2)
+    _check(up_w, "up_w", 2)
+    M, K = x.shape
+    N = gate_w.shape[0]
+    for t, name in ((x, "x"), (residual, "residual"), (norm_w, "norm_w"), (gate_w, "gate_w"), (up_w, "up_w")):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if tuple(residual.shape) != (M, K) or tuple(norm_w.shape) != (K,):
+        raise ValueError("residual must be [M,K] and norm_w [K]")
+    if tuple(gate_w.shape) != (N, K) or tuple(up_w.shape) != (N, K):
+        raise ValueError("weights must be [N,K]")
+    dev = x.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    _check(out, "out", 2)
+    if tuple(out.shape) != (M, N) or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous [{M},{N}] tensor")
+    with torch.cuda.device(dev):
+        st = lib().add_rmsnorm_glu(x.data_ptr(), residual.data_ptr(), norm_w.data_ptr(), float(eps),
+                                   gate_w.data_ptr(), up_w.data_ptr(), out.data_ptr(), M, N, K, _MODES[mode],
+                                   _stream_handle(dev, stream))
+    if st != 0:
+        raise MbgluError(st, "add_rmsnorm_glu")
+    return out
+
+
+def last_variant() -> int:
+    """Kernel the calling thread's last call launched: 0 none, 1 streaming,
+    2 generic, 3 zero fill."""
+    return lib().mbglu_last_variant()
+
+
+def read_device_error() -> int:
+    """Synchronises the current device, returns and clears its error word."""
+    w = ctypes.c_int(0)
+    st = lib().mbglu_read_device_error(ctypes.byref(w))
+    if st != 0:
+        raise MbgluError(st, "mbglu_read_device_error")
+    return w.value

@@ -1,0 +1,438 @@
+// glu_kernels.cuh -- sm_103a kernels of the dual-weight GLU GEMV.
+//
+//   out[m,n] = SiLU(g[m,n]) * u[m,n],  g = h . W_gate[n],  u = h . W_up[n]
+//
+// DeepSpeed PR #8602, comment "Plan B: Dual-Weight GEMV", section "Plan B
+// Design: kernel adapts to the weights": both nn.Linear weights are read in
+// place, fp32 accumulation, SiLU(gate) * up with one round-to-nearest-even at
+// the end.  Section "Why cuBLAS-level performance is achievable at b=1": the
+// op is memory-bound -- every weight element is read once and multiplied
+// once -- so the design target is the HBM roofline.
+//
+// GB300 design (the pages' warp-per-row Ada kernel with scalar loads is prior
+// art only):
+//   * one persistent CTA per SM, a balanced contiguous range of rows each;
+//   * every warp owns a private ring of shared-memory stages that its lane 0
+//     fills with bulk asynchronous copies (cp.async.bulk, mbarrier completion,
+//     L2 evict-first hint): one stage = one K-segment of one row of BOTH
+//     matrices, so ~160 KB of weights are in flight per SM;
+//   * h (or the normed h) sits in shared memory for the whole kernel;
+//   * lanes take 16-byte chunks, fp32 FMAs, a warp butterfly reduction, and
+//     the epilogue of the requested rounding mode;
+//   * every wait is bounded (globaltimer); a timeout records an error word and
+//     returns instead of hanging or trapping.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace mbglu {
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+constexpr int kErrTimeout = 8;                    // == MBGLU_ERR_TIMEOUT
+constexpr int kMaxWarps = 16;
+constexpr int kMaxM = 16;
+
+// Error word of the device (read and cleared by mbglu_read_device_error).
+__device__ int g_device_error;
+
+struct GluParams {
+    const uint16_t *h;
+    int64_t ldh;
+    const uint16_t *gate;
+    int64_t ld_gate;
+    const uint16_t *up;
+    int64_t ld_up;
+    uint16_t *out;
+    int64_t ldo;
+    const uint16_t *s;       // norm prologue: updated residual rows [M][K], contiguous
+    const uint16_t *norm_w;  // norm prologue: [K]
+    float eps;
+    int M, N, K, mode;
+    int KS, nseg, stages;    // streaming kernel: segment length, #segments, ring depth
+    uint32_t off_h, off_ring;
+    int vec_in;              // 1: h (or s, norm_w) may be read with 16-byte loads
+};
+
+// ---------------------------------------------------------------------------
+// scalar helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+__device__ __forceinline__ uint16_t f32_to_bf16(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ float round_to_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    return static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
+}
+
+// SiLU(x) = x / (1 + e^-x): precise expf and IEEE division (no fast math).
+__device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
+
+// mode 0 (FUSED): one rounding.  mode 1 (HF): the bf16 composite's roundings
+// of g, u, SiLU(g) and the product (PR #9057 "Changes": "Restore HF's
+// intermediate BF16 rounding in ... GLU").  sb * ub is exact in fp32.
+__device__ __forceinline__ uint16_t glu_epilogue(float g, float u, int mode)
+{
+    if (mode == 0) return f32_to_bf16(silu_f32(g) * u);
+    const float gb = round_to_bf16(g);
+    const float ub = round_to_bf16(u);
+    const float sb = round_to_bf16(silu_f32(gb));
+    return f32_to_bf16(sb * ub);
+}
+
+__device__ __forceinline__ float warp_allsum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// prologues: h into shared memory
+// ---------------------------------------------------------------------------
+
+// Copies h[M][K] (row stride ldh) to h_s[MB][K]; rows M..MB-1 become zero.
+template <int MB>
+__device__ __forceinline__ void load_h_to_smem(const GluParams &p, uint16_t *h_s)
+{
+    const int K = p.K;
+    if (p.vec_in) {
+        const int nch = K >> 3;
+        for (int i = threadIdx.x; i < MB * nch; i += blockDim.x) {
+            const int m = i / nch, c = i - m * nch;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (m < p.M) v = *reinterpret_cast<const uint4 *>(p.h + m * p.ldh + c * 8);
+            *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * K + c * 8) = v;
+        }
+    } else {
+        for (int i = threadIdx.x; i < MB * K; i += blockDim.x) {
+            const int m = i / K, k = i - m * K;
+            h_s[i] = (m < p.M) ? p.h[m * p.ldh + k] : static_cast<uint16_t>(0);
+        }
+    }
+}
+
+// Zero-centred RMSNorm of the updated residual rows (PR #9057 "Changes"):
+//   var = mean_k s^2 (fp32, fixed reduction order), inv = 1 / sqrt(var + eps),
+//   h = bf16( (s * inv) * (1 + w) ) with the (1 + w) scale built in fp32.
+// Every CTA runs the same code on the same data, so every CTA gets the same h.
+// red: [kMaxWarps][MB] shared floats; inv_s: [MB].  Writes rows_out rows of
+// h_s (rows M..rows_out-1 zero); M <= MB.
+template <int MB>
+__device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s, float (*red)[MB],
+                                              float *inv_s, int rows_out)
+{
+    const int K = p.K, tid = threadIdx.x, nthr = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
+    float ss[MB];
+#pragma unroll
+    for (int m = 0; m < MB; ++m) ss[m] = 0.0f;
+    if (p.vec_in) {
+        const int nch = K >> 3;
+        for (int c = tid; c < nch; c += nthr) {
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                if (m < p.M) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(p.s + static_cast<int64_t>(m) * K + c * 8);
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+                        ss[m] = fmaf(a, a, ss[m]);
+                        ss[m] = fmaf(b, b, ss[m]);
+                    }
+                }
+            }
+        }
+    } else {
+        for (int k = tid; k < K; k += nthr) {
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                if (m < p.M) {
+                    const float a = bf16_to_f32(p.s[static_cast<int64_t>(m) * K + k]);
+                    ss[m] = fmaf(a, a, ss[m]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+        const float t = warp_allsum(ss[m]);
+        if (lane == 0) red[warp][m] = t;
+    }
+    __syncthreads();
+    if (tid < MB) {
+        float t = 0.0f;
+        for (int w = 0; w < nw; ++w) t += red[w][tid];
+        inv_s[tid] = 1.0f / sqrtf(t / static_cast<float>(K) + p.eps);
+    }
+    __syncthreads();
+    if (p.vec_in) {
+        const int nch = K >> 3;
+        for (int i = tid; i < rows_out * nch; i += nthr) {
+            const int m = i / nch, c = i - m * nch;
+            uint4 o = make_uint4(0, 0, 0, 0);
+            if (m < p.M) {
+                const float inv = inv_s[m];
+                const uint4 v = *reinterpret_cast<const uint4 *>(p.s + static_cast<int64_t>(m) * K + c * 8);
+                const uint4 wv = *reinterpret_cast<const uint4 *>(p.norm_w + c * 8);
+                const uint32_t sv[4] = {v.x, v.y, v.z, v.w};
+                const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+                uint32_t r[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float lo = (bf16_lo(sv[j]) * inv) * (1.0f + bf16_lo(ww[j]));
+                    const float hi = (bf16_hi(sv[j]) * inv) * (1.0f + bf16_hi(ww[j]));
+                    r[j] = pack_bf16x2(lo, hi);
+                }
+                o = make_uint4(r[0], r[1], r[2], r[3]);
+            }
+            *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * K + c * 8) = o;
+        }
+    } else {
+        for (int i = tid; i < rows_out * K; i += nthr) {
+            const int m = i / K, k = i - m * K;
+            uint16_t o = 0;
+            if (m < p.M) {
+                const float sv = bf16_to_f32(p.s[static_cast<int64_t>(m) * K + k]);
+                o = f32_to_bf16((sv * inv_s[m]) * (1.0f + bf16_to_f32(p.norm_w[k])));
+            }
+            h_s[i] = o;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the streaming kernel
+// ---------------------------------------------------------------------------
+//
+// Shared memory (dynamic):  [0, off_h)        mbarriers, [warp][stage]
+//                           [off_h, off_ring) h_s[MB][K] bf16
+//                           [off_ring, ...)   ring[warp][stage][2][KS] bf16
+// Unit u of a warp = (row i of the warp, K-segment seg): rows r0 + warp +
+// i*NW of this CTA's range [r0, r1), segments of KS elements (the last one
+// may be shorter, always a multiple of 8).  Stage of unit u = u % S, its
+// barrier phase = (u / S) & 1.
+//
+// NORM: the launch follows the residual-add kernel with programmatic
+// dependent launch; the weight prefetch (independent of the add) is issued
+// before griddepcontrol.wait, the residual rows are read after it.  Without
+// NORM nothing global is touched before the wait, so any predecessor is safe.
+template <int MB, bool NORM>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) glu_stream_kernel(const GluParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[kMaxWarps][MB];
+    __shared__ float inv_s[MB];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, NW = blockDim.x >> 5;
+    const int S = p.stages, KS = p.KS, K = p.K, nseg = p.nseg;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * S;
+    uint16_t *h_s = reinterpret_cast<uint16_t *>(smem + p.off_h);
+    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + p.off_ring) + static_cast<int64_t>(warp) * S * 2 * KS;
+
+    const int r0 = static_cast<int>((static_cast<int64_t>(p.N) * blockIdx.x) / gridDim.x);
+    const int r1 = static_cast<int>((static_cast<int64_t>(p.N) * (blockIdx.x + 1)) / gridDim.x);
+    const int span = r1 - r0;
+    const int nrows = span > warp ? (span - warp + NW - 1) / NW : 0;
+    const int units = nrows * nseg;
+
+    if (lane == 0)
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+    __syncthreads();
+
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int u) {
+        const int st = u % S;
+        const int i = u / nseg, seg = u - i * nseg;
+        const int64_t row = r0 + warp + static_cast<int64_t>(i) * NW;
+        const int k0 = seg * KS;
+        const int len = min(KS, K - k0);
+        const uint32_t bytes = static_cast<uint32_t>(len) * 2u;
+        uint16_t *dst = ring + static_cast<int64_t>(st) * 2 * KS;
+        mbar_arrive_expect_tx(&bars[st], 2u * bytes);
+        bulk_g2s(dst, p.gate + row * p.ld_gate + k0, bytes, &bars[st], policy);
+        bulk_g2s(dst + KS, p.up + row * p.ld_up + k0, bytes, &bars[st], policy);
+    };
+
+    if constexpr (NORM) {
+        if (lane == 0)
+            for (int u = 0; u < S && u < units; ++u) issue(u);
+        grid_dependency_wait();
+        grid_launch_dependents();
+        norm_prologue<MB>(p, h_s, red, inv_s, MB);
+    } else {
+        grid_dependency_wait();
+        grid_launch_dependents();
+        if (lane == 0)
+            for (int u = 0; u < S && u < units; ++u) issue(u);
+        load_h_to_smem<MB>(p, h_s);
+    }
+    __syncthreads();
+
+    float ag[MB], au[MB];
+#pragma unroll
+    for (int m = 0; m < MB; ++m) ag[m] = au[m] = 0.0f;
+
+    for (int u = 0; u < units; ++u) {
+        const int st = u % S;
+        const bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) {
+                atomicExch(&g_device_error, kErrTimeout);
+                // let the copies this warp still has in flight land before exiting
+                for (int v = u; v < u + S && v < units; ++v)
+                    mbar_wait_bounded(&bars[v % S], static_cast<uint32_t>((v / S) & 1), kWaitLimitNs);
+            }
+            __syncwarp();
+            return;
+        }
+        const int i = u / nseg, seg = u - i * nseg;
+        const int k0 = seg * KS;
+        const int nch = min(KS, K - k0) >> 3;
+        const uint16_t *wg = ring + static_cast<int64_t>(st) * 2 * KS;
+        const uint16_t *wu = wg + KS;
+        const uint16_t *hk = h_s + k0;
+#pragma unroll 2
+        for (int c = lane; c < nch; c += 32) {
+            const uint4 g4 = *reinterpret_cast<const uint4 *>(wg + c * 8);
+            const uint4 u4 = *reinterpret_cast<const uint4 *>(wu + c * 8);
+            const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+            const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
+            float gf[8], uf[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                gf[2 * j] = bf16_lo(gw[j]);
+                gf[2 * j + 1] = bf16_hi(gw[j]);
+                uf[2 * j] = bf16_lo(uw[j]);
+                uf[2 * j + 1] = bf16_hi(uw[j]);
+            }
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                const uint4 h4 = *reinterpret_cast<const uint4 *>(hk + static_cast<int64_t>(m) * K + c * 8);
+                const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float a = bf16_lo(hw[j]), b = bf16_hi(hw[j]);
+                    ag[m] = fmaf(a, gf[2 * j], ag[m]);
+                    au[m] = fmaf(a, uf[2 * j], au[m]);
+                    ag[m] = fmaf(b, gf[2 * j + 1], ag[m]);
+                    au[m] = fmaf(b, uf[2 * j + 1], au[m]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && u + S < units) {
+            fence_proxy_async_smem();
+            issue(u + S);
+        }
+        if (seg == nseg - 1) {
+            const int64_t row = r0 + warp + static_cast<int64_t>(i) * NW;
+            float gsel = 0.0f, usel = 0.0f;
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                const float g = warp_allsum(ag[m]);
+                const float v = warp_allsum(au[m]);
+                if (lane == m) { gsel = g; usel = v; }
+                ag[m] = au[m] = 0.0f;
+            }
+            if (lane < p.M) p.out[lane * p.ldo + row] = glu_epilogue(gsel, usel, p.mode);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// generic kernel: any 2-byte-aligned operands, same arithmetic rules
+// ---------------------------------------------------------------------------
+// One warp per output feature (grid-stride), lanes stride K with 2-byte loads,
+// a runtime loop over the batch rows.  NORM computes the normed rows into
+// dynamic shared memory h_s[M][K] first.
+template <bool NORM>
+__global__ void __launch_bounds__(256) glu_generic_kernel(const GluParams p)
+{
+    extern __shared__ __align__(16) unsigned char smem_g[];
+    __shared__ float red[kMaxWarps][kMaxM];
+    __shared__ float inv_s[kMaxM];
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const uint16_t *hp = p.h;
+    int64_t hld = p.ldh;
+    if constexpr (NORM) {
+        uint16_t *h_s = reinterpret_cast<uint16_t *>(smem_g);
+        GluParams q = p;
+        q.vec_in = 0;
+        norm_prologue<kMaxM>(q, h_s, red, inv_s, p.M);
+        __syncthreads();
+        hp = h_s;
+        hld = p.K;
+    }
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); row < p.N;
+         row += nwarps) {
+        const uint16_t *grow = p.gate + row * p.ld_gate;
+        const uint16_t *urow = p.up + row * p.ld_up;
+        for (int m = 0; m < p.M; ++m) {
+            const uint16_t *hrow = hp + m * hld;
+            float g = 0.0f, u = 0.0f;
+            for (int k = lane; k < p.K; k += 32) {
+                const float a = bf16_to_f32(hrow[k]);
+                g = fmaf(a, bf16_to_f32(grow[k]), g);
+                u = fmaf(a, bf16_to_f32(urow[k]), u);
+            }
+            g = warp_allsum(g);
+            u = warp_allsum(u);
+            if (lane == 0) p.out[m * p.ldo + row] = glu_epilogue(g, u, p.mode);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// small kernels
+// ---------------------------------------------------------------------------
+
+// s = bf16(x + residual), written back into residual (one rounding: the fp32
+// sum of two bf16 values rounds to the same bf16 as the exact sum).  Starts
+// the dependent GEMV launch at once: that grid only prefetches weights until
+// this grid has completed.
+__global__ void __launch_bounds__(256) residual_add_kernel(const uint16_t *x, uint16_t *res, int64_t count,
+                                                           int vec)
+{
+    grid_launch_dependents();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (vec) {
+        for (; i < count / 8; i += stride) {
+            const uint4 a = reinterpret_cast<const uint4 *>(x)[i];
+            const uint4 b = reinterpret_cast<const uint4 *>(res)[i];
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+            uint32_t r[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                r[j] = pack_bf16x2(bf16_lo(aw[j]) + bf16_lo(bw[j]), bf16_hi(aw[j]) + bf16_hi(bw[j]));
+            reinterpret_cast<uint4 *>(res)[i] = make_uint4(r[0], r[1], r[2], r[3]);
+        }
+    } else {
+        for (; i < count; i += stride) res[i] = f32_to_bf16(bf16_to_f32(x[i]) + bf16_to_f32(res[i]));
+    }
+}
+
+// K == 0: empty dot products, SiLU(0) * 0 = +0 in both modes.
+__global__ void __launch_bounds__(256) zero_fill_kernel(uint16_t *out, int64_t ldo, int M, int N)
+{
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int64_t total = static_cast<int64_t>(M) * N;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / N, n = i - m * N;
+        out[m * ldo + n] = 0;
+    }
+}
+
+}  // namespace mbglu

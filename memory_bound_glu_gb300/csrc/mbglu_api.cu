@@ -1,0 +1,414 @@
+// mbglu_api.cu -- the C ABI of libmbglu.so (declared in include/mbglu.h):
+// host-side validation, launch planning and dispatch to the sm_103a kernels.
+//
+// The library is stateless apart from a per-device table of attributes (SM
+// count, shared-memory limit) filled on first use under a mutex; it allocates
+// nothing and caches nothing derived from the weights (DeepSpeed PR #9057
+// commits on stale pointer-keyed caches: in-place weight updates must always
+// be seen).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "mbglu.h"
+#include "glu_kernels.cuh"
+
+namespace {
+
+using mbglu::GluParams;
+
+thread_local int t_last_cuda_error = 0;
+thread_local int t_last_variant = 0;
+
+enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3 };
+
+constexpr int kMaxDevices = 64;
+constexpr uint32_t kBarRegion = 1024;        // mbarriers: up to 16 warps x 8 stages x 8 B
+constexpr int kMaxStages = 8;
+constexpr int64_t kNormMaxMK = 81920;        // add_rmsnorm_glu: M*K*2 bytes of normed rows in smem
+
+struct DeviceInfo {
+    bool ready = false;
+    int sm_count = 0;
+    int smem_optin = 0;       // max dynamic + static shared memory per block
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+struct Tuning {
+    int warps = 8;            // warps per CTA of the streaming kernel
+    int ks = 0;               // K-segment length (0: automatic)
+    int stages = 0;           // ring depth cap (0: as many as fit, <= 8)
+    int smem_kb = 0;          // shared-memory budget cap in KiB (0: device limit)
+    int pdl = 1;              // programmatic dependent launch
+};
+
+int env_int(const char *name, int dflt)
+{
+    const char *v = std::getenv(name);
+    return (v && *v) ? std::atoi(v) : dflt;
+}
+
+const Tuning &tuning()
+{
+    static const Tuning t = [] {
+        Tuning x;
+        x.warps = std::min(16, std::max(1, env_int("MBGLU_WARPS", 8)));
+        x.ks = std::max(0, env_int("MBGLU_KS", 0)) & ~7;
+        x.stages = std::min(kMaxStages, std::max(0, env_int("MBGLU_STAGES", 0)));
+        x.smem_kb = std::max(0, env_int("MBGLU_SMEM_KB", 0));
+        x.pdl = env_int("MBGLU_PDL", 1) != 0;
+        return x;
+    }();
+    return t;
+}
+
+mbglu_status cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = static_cast<int>(e);
+    return MBGLU_ERR_CUDA;
+}
+
+template <int MB, bool NORM>
+cudaError_t allow_smem(int optin)
+{
+    cudaFuncAttributes a{};
+    cudaError_t e = cudaFuncGetAttributes(&a, mbglu::glu_stream_kernel<MB, NORM>);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(mbglu::glu_stream_kernel<MB, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin - static_cast<int>(a.sharedSizeBytes));
+}
+
+cudaError_t allow_smem_generic(int optin)
+{
+    cudaFuncAttributes a{};
+    cudaError_t e = cudaFuncGetAttributes(&a, mbglu::glu_generic_kernel<true>);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(mbglu::glu_generic_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin - static_cast<int>(a.sharedSizeBytes));
+}
+
+mbglu_status device_info(const DeviceInfo **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e);
+        const cudaError_t errs[] = {
+            allow_smem<1, false>(d.smem_optin), allow_smem<2, false>(d.smem_optin),
+            allow_smem<4, false>(d.smem_optin), allow_smem<8, false>(d.smem_optin),
+            allow_smem<16, false>(d.smem_optin), allow_smem<1, true>(d.smem_optin),
+            allow_smem<2, true>(d.smem_optin), allow_smem<4, true>(d.smem_optin),
+            allow_smem<8, true>(d.smem_optin), allow_smem<16, true>(d.smem_optin),
+            allow_smem_generic(d.smem_optin)};
+        for (cudaError_t x : errs)
+            if (x != cudaSuccess) return cuda_fail(x);
+        d.ready = true;
+    }
+    *out = &d;
+    return MBGLU_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// [p, p + bytes) and [q, q + bytes_q) intersect
+bool overlaps(const void *p, int64_t bytes, const void *q, int64_t bytes_q)
+{
+    if (bytes <= 0 || bytes_q <= 0) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + static_cast<uintptr_t>(bytes_q) && b < a + static_cast<uintptr_t>(bytes);
+}
+
+int64_t matrix_bytes(int rows, int cols, int64_t ld)
+{
+    if (rows <= 0 || cols <= 0) return 0;
+    return ((static_cast<int64_t>(rows) - 1) * ld + cols) * 2;
+}
+
+int batch_tile(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
+
+// K-segment: the whole row up to 2048 elements; otherwise a multiple of 256
+// in [1024, 2048] that divides K, else 2048 (the last segment is shorter).
+int default_ks(int K)
+{
+    if (K <= 2048) return K;
+    for (int ks = 2048; ks >= 1024; ks -= 256)
+        if (K % ks == 0) return ks;
+    return 2048;
+}
+
+struct Plan {
+    int MB = 1, warps = 8, KS = 0, nseg = 0, stages = 0, grid = 0;
+    uint32_t off_h = 0, off_ring = 0, smem = 0;
+};
+
+// Streaming-kernel plan; false if h plus a two-stage ring does not fit.
+bool plan_stream(const DeviceInfo &d, int M, int N, int K, Plan &pl)
+{
+    const Tuning &t = tuning();
+    pl.MB = batch_tile(M);
+    pl.warps = t.warps;
+    const int static_reserve = 2048;  // the kernel's static shared arrays
+    int budget = d.smem_optin - static_reserve;
+    if (t.smem_kb > 0) budget = std::min(budget, t.smem_kb * 1024 - static_reserve);
+    const uint32_t hbytes = (static_cast<uint32_t>(pl.MB) * static_cast<uint32_t>(K) * 2u + 127u) & ~127u;
+    int ks = t.ks > 0 ? std::min(t.ks, ((K + 7) / 8) * 8) : default_ks(K);
+    ks = std::max(8, ks & ~7);
+    for (;;) {
+        const int64_t per_stage = static_cast<int64_t>(pl.warps) * 4 * ks;
+        int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes;
+        int s = room > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, room / per_stage)) : 0;
+        if (t.stages > 0) s = std::min(s, t.stages);
+        if (s >= 2) {
+            pl.stages = s;
+            break;
+        }
+        if (ks <= 256) return false;
+        ks = std::max(256, (ks / 2) & ~7);
+    }
+    pl.KS = ks;
+    pl.nseg = (K + ks - 1) / ks;
+    pl.off_h = kBarRegion;
+    pl.off_ring = kBarRegion + hbytes;
+    pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 4u * static_cast<uint32_t>(ks);
+    pl.grid = std::max(1, std::min(d.sm_count, N));
+    return true;
+}
+
+template <typename... Args>
+mbglu_status launch(void (*kernel)(Args...), dim3 grid, dim3 block, uint32_t smem, cudaStream_t stream,
+                    bool pdl, const GluParams &p)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
+    return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
+}
+
+template <bool NORM>
+mbglu_status launch_stream(const Plan &pl, const GluParams &p, cudaStream_t stream, bool pdl)
+{
+    const dim3 grid(pl.grid), block(pl.warps * 32);
+    switch (pl.MB) {
+    case 1: return launch(mbglu::glu_stream_kernel<1, NORM>, grid, block, pl.smem, stream, pdl, p);
+    case 2: return launch(mbglu::glu_stream_kernel<2, NORM>, grid, block, pl.smem, stream, pdl, p);
+    case 4: return launch(mbglu::glu_stream_kernel<4, NORM>, grid, block, pl.smem, stream, pdl, p);
+    case 8: return launch(mbglu::glu_stream_kernel<8, NORM>, grid, block, pl.smem, stream, pdl, p);
+    default: return launch(mbglu::glu_stream_kernel<16, NORM>, grid, block, pl.smem, stream, pdl, p);
+    }
+}
+
+int generic_grid(const DeviceInfo &d, int N) { return std::max(1, std::min(d.sm_count * 4, (N + 7) / 8)); }
+
+GluParams base_params(int M, int N, int K, int mode)
+{
+    GluParams p = {};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.mode = mode;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mbglu_abi_version(void) { return MBGLU_ABI_VERSION; }
+int mbglu_last_cuda_error(void) { return t_last_cuda_error; }
+int mbglu_last_variant(void) { return t_last_variant; }
+
+const char *mbglu_status_string(mbglu_status s)
+{
+    switch (s) {
+    case MBGLU_OK: return "MBGLU_OK";
+    case MBGLU_ERR_NULL: return "MBGLU_ERR_NULL: a required pointer is NULL";
+    case MBGLU_ERR_SHAPE: return "MBGLU_ERR_SHAPE: unsupported M, N or K";
+    case MBGLU_ERR_STRIDE: return "MBGLU_ERR_STRIDE: a leading dimension is smaller than its row";
+    case MBGLU_ERR_ALIGN: return "MBGLU_ERR_ALIGN: a pointer is not 2-byte aligned";
+    case MBGLU_ERR_MODE: return "MBGLU_ERR_MODE: mode must be MBGLU_MODE_FUSED or MBGLU_MODE_HF";
+    case MBGLU_ERR_ALIAS: return "MBGLU_ERR_ALIAS: an output overlaps an input";
+    case MBGLU_ERR_CUDA: return "MBGLU_ERR_CUDA: a CUDA runtime call failed";
+    case MBGLU_ERR_TIMEOUT: return "MBGLU_ERR_TIMEOUT: a bounded device-side wait gave up";
+    default: return "unknown mbglu status";
+    }
+}
+
+mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
+                      const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
+                      mbglu_mode mode, cudaStream_t stream)
+{
+    t_last_variant = kNone;
+    if (mode != MBGLU_MODE_FUSED && mode != MBGLU_MODE_HF) return MBGLU_ERR_MODE;
+    if (M < 0 || N < 0 || K < 0 || M > MBGLU_MAX_M) return MBGLU_ERR_SHAPE;
+    if (M == 0 || N == 0) return MBGLU_OK;
+    if (!out || (K > 0 && (!h || !gate_w || !up_w))) return MBGLU_ERR_NULL;
+    if (ldo < N || (K > 0 && (ldh < K || ld_gate < K || ld_up < K))) return MBGLU_ERR_STRIDE;
+    if (!aligned(out, 2) || (K > 0 && (!aligned(h, 2) || !aligned(gate_w, 2) || !aligned(up_w, 2))))
+        return MBGLU_ERR_ALIGN;
+    const int64_t ob = matrix_bytes(M, N, ldo);
+    if (K > 0 && (overlaps(out, ob, h, matrix_bytes(M, K, ldh)) || overlaps(out, ob, gate_w, matrix_bytes(N, K, ld_gate)) ||
+                  overlaps(out, ob, up_w, matrix_bytes(N, K, ld_up))))
+        return MBGLU_ERR_ALIAS;
+
+    const DeviceInfo *d = nullptr;
+    mbglu_status st = device_info(&d);
+    if (st != MBGLU_OK) return st;
+    const bool pdl = tuning().pdl;
+
+    GluParams p = base_params(M, N, K, static_cast<int>(mode));
+    p.out = out;
+    p.ldo = ldo;
+    if (K == 0) {
+        const int grid = std::max(1, std::min(d->sm_count, static_cast<int>((static_cast<int64_t>(M) * N + 255) / 256)));
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, mbglu::zero_fill_kernel, reinterpret_cast<uint16_t *>(out),
+                                                 ldo, M, N);
+        if (e != cudaSuccess) return cuda_fail(e);
+        t_last_variant = kZeroFill;
+        return MBGLU_OK;
+    }
+    p.h = h;
+    p.ldh = ldh;
+    p.gate = gate_w;
+    p.ld_gate = ld_gate;
+    p.up = up_w;
+    p.ld_up = ld_up;
+
+    Plan pl;
+    const bool fast = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && (ld_gate % 8 == 0) &&
+                      (ld_up % 8 == 0) && plan_stream(*d, M, N, K, pl);
+    if (fast) {
+        p.KS = pl.KS;
+        p.nseg = pl.nseg;
+        p.stages = pl.stages;
+        p.off_h = pl.off_h;
+        p.off_ring = pl.off_ring;
+        p.vec_in = aligned(h, 16) && (ldh % 8 == 0);
+        st = launch_stream<false>(pl, p, stream, pdl);
+        if (st == MBGLU_OK) t_last_variant = kStream;
+        return st;
+    }
+    st = launch(mbglu::glu_generic_kernel<false>, dim3(generic_grid(*d, N)), dim3(256), 0, stream, pdl, p);
+    if (st == MBGLU_OK) t_last_variant = kGeneric;
+    return st;
+}
+
+mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
+                             const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w, mbglu_bf16 *out, int M, int N, int K,
+                             mbglu_mode mode, cudaStream_t stream)
+{
+    t_last_variant = kNone;
+    if (mode != MBGLU_MODE_FUSED && mode != MBGLU_MODE_HF) return MBGLU_ERR_MODE;
+    if (M < 0 || N < 0 || K <= 0 || M > MBGLU_MAX_M) return MBGLU_ERR_SHAPE;
+    if (static_cast<int64_t>(M) * K > kNormMaxMK) return MBGLU_ERR_SHAPE;
+    if (M == 0) return MBGLU_OK;
+    if (!x || !residual || !norm_w || (N > 0 && (!gate_w || !up_w || !out))) return MBGLU_ERR_NULL;
+    if (!aligned(x, 2) || !aligned(residual, 2) || !aligned(norm_w, 2) ||
+        (N > 0 && (!aligned(gate_w, 2) || !aligned(up_w, 2) || !aligned(out, 2))))
+        return MBGLU_ERR_ALIGN;
+    const int64_t xb = static_cast<int64_t>(M) * K * 2, wb = static_cast<int64_t>(N) * K * 2;
+    const int64_t ob = static_cast<int64_t>(M) * N * 2, nb = static_cast<int64_t>(K) * 2;
+    if (x != residual && overlaps(x, xb, residual, xb)) return MBGLU_ERR_ALIAS;
+    if (overlaps(residual, xb, norm_w, nb) || overlaps(residual, xb, gate_w, wb) || overlaps(residual, xb, up_w, wb))
+        return MBGLU_ERR_ALIAS;
+    if (N > 0 && (overlaps(out, ob, x, xb) || overlaps(out, ob, residual, xb) || overlaps(out, ob, norm_w, nb) ||
+                  overlaps(out, ob, gate_w, wb) || overlaps(out, ob, up_w, wb)))
+        return MBGLU_ERR_ALIAS;
+
+    const DeviceInfo *d = nullptr;
+    mbglu_status st = device_info(&d);
+    if (st != MBGLU_OK) return st;
+    const bool pdl = tuning().pdl;
+
+    // 1) residual <- bf16(x + residual); launched normally (full ordering after
+    //    whatever precedes it on the stream).
+    {
+        const int64_t count = static_cast<int64_t>(M) * K;
+        const int vec = aligned(x, 16) && aligned(residual, 16) && (count % 8 == 0);
+        const int64_t work = vec ? count / 8 : count;
+        const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(d->sm_count, (work + 255) / 256)));
+        mbglu::residual_add_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint16_t *>(x),
+                                                              reinterpret_cast<uint16_t *>(residual), count, vec);
+        const cudaError_t e = cudaPeekAtLastError();
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (N == 0) {
+        t_last_variant = kNone;
+        return MBGLU_OK;
+    }
+
+    // 2) the GEMV with the norm prologue, as a programmatic dependent launch
+    GluParams p = base_params(M, N, K, static_cast<int>(mode));
+    p.gate = gate_w;
+    p.ld_gate = K;
+    p.up = up_w;
+    p.ld_up = K;
+    p.out = out;
+    p.ldo = N;
+    p.s = residual;
+    p.norm_w = norm_w;
+    p.eps = eps;
+    p.vec_in = (K % 8 == 0) && aligned(residual, 16) && aligned(norm_w, 16);
+
+    Plan pl;
+    const bool fast = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && p.vec_in &&
+                      plan_stream(*d, M, N, K, pl);
+    if (fast) {
+        p.KS = pl.KS;
+        p.nseg = pl.nseg;
+        p.stages = pl.stages;
+        p.off_h = pl.off_h;
+        p.off_ring = pl.off_ring;
+        st = launch_stream<true>(pl, p, stream, pdl);
+        if (st == MBGLU_OK) t_last_variant = kStream;
+        return st;
+    }
+    const uint32_t smem = static_cast<uint32_t>(M) * static_cast<uint32_t>(K) * 2u;
+    st = launch(mbglu::glu_generic_kernel<true>, dim3(generic_grid(*d, N)), dim3(256), smem, stream, pdl, p);
+    if (st == MBGLU_OK) t_last_variant = kGeneric;
+    return st;
+}
+
+mbglu_status mbglu_read_device_error(int *word)
+{
+    if (!word) return MBGLU_ERR_NULL;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    int w = 0;
+    if ((e = cudaMemcpyFromSymbol(&w, mbglu::g_device_error, sizeof w)) != cudaSuccess) return cuda_fail(e);
+    const int zero = 0;
+    if ((e = cudaMemcpyToSymbol(mbglu::g_device_error, &zero, sizeof zero)) != cudaSuccess) return cuda_fail(e);
+    *word = w;
+    return MBGLU_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,97 @@
+"""The C-ABI library on a host without a GPU: it loads, exports every symbol
+include/mbglu.h declares, and its host-side validation rejects bad arguments
+before any CUDA call (pointers here are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import memory_bound_glu_gb300 as mb
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mbglu.h")
+
+OK, NULL, SHAPE, STRIDE, ALIGN, MODE, ALIAS, CUDA, TIMEOUT = range(9)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_expected_api():
+    assert declared_functions() == sorted(mb.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = mb.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {mb.LIB_PATH}").read()
+    exported = set(re.findall(r" T (\w+)", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_abi_version_matches_header():
+    m = re.search(r"#define MBGLU_ABI_VERSION (\d+)", open(HEADER).read())
+    assert mb.lib().mbglu_abi_version() == int(m.group(1))
+
+
+def test_status_strings():
+    lib = mb.lib()
+    for code, tag in [(OK, b"MBGLU_OK"), (NULL, b"NULL"), (SHAPE, b"SHAPE"), (STRIDE, b"STRIDE"),
+                      (ALIGN, b"ALIGN"), (MODE, b"MODE"), (ALIAS, b"ALIAS"), (CUDA, b"CUDA"),
+                      (TIMEOUT, b"TIMEOUT")]:
+        assert tag in lib.mbglu_status_string(code)
+    assert b"unknown" in lib.mbglu_status_string(99)
+
+
+# fake, never-dereferenced device addresses: 256-byte aligned and far apart
+H, G, U, O, X, R, W = (0x7F0000000000 + i * (1 << 32) for i in range(7))
+
+
+def gemv(h=H, ldh=64, g=G, ldg=64, u=U, ldu=64, o=O, ldo=32, M=2, N=32, K=64, mode=0):
+    return mb.lib().glu_gemv(h, ldh, g, ldg, u, ldu, o, ldo, M, N, K, mode, None)
+
+
+def norm(x=X, r=R, w=W, g=G, u=U, o=O, M=2, N=32, K=64, mode=1):
+    return mb.lib().add_rmsnorm_glu(x, r, w, 1e-6, g, u, o, M, N, K, mode, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(mode=2), MODE), (dict(mode=-1), MODE),
+    (dict(M=-1), SHAPE), (dict(N=-1), SHAPE), (dict(K=-1), SHAPE), (dict(M=17), SHAPE),
+    (dict(h=0), NULL), (dict(g=0), NULL), (dict(u=0), NULL), (dict(o=0), NULL),
+    (dict(ldh=63), STRIDE), (dict(ldg=10), STRIDE), (dict(ldu=0), STRIDE), (dict(ldo=31), STRIDE),
+    (dict(h=H + 1), ALIGN), (dict(g=G + 1), ALIGN), (dict(u=U + 3), ALIGN), (dict(o=O + 1), ALIGN),
+    (dict(o=H), ALIAS), (dict(o=G + 128), ALIAS), (dict(o=U + 64 * 31 * 2), ALIAS),
+    (dict(M=0), OK), (dict(N=0), OK), (dict(M=0, h=0, g=0, u=0, o=0), OK),
+])
+def test_glu_gemv_validation(kw, code):
+    assert gemv(**kw) == code
+    if code != OK:
+        assert mb.lib().mbglu_last_variant() == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(mode=3), MODE), (dict(K=0), SHAPE), (dict(M=17), SHAPE), (dict(M=16, K=8192), SHAPE),
+    (dict(x=0), NULL), (dict(r=0), NULL), (dict(w=0), NULL), (dict(g=0), NULL), (dict(o=0), NULL),
+    (dict(x=X + 1), ALIGN), (dict(r=R + 1), ALIGN), (dict(o=O + 1), ALIGN),
+    (dict(o=X), ALIAS), (dict(o=R + 2), ALIAS), (dict(o=W), ALIAS), (dict(o=G), ALIAS),
+    (dict(r=X + 2), ALIAS), (dict(r=G + 256), ALIAS), (dict(r=W), ALIAS),
+    (dict(M=0), OK),
+])
+def test_add_rmsnorm_glu_validation(kw, code):
+    assert norm(**kw) == code
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    h = torch.zeros(2, 64, dtype=torch.bfloat16)
+    w = torch.zeros(8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        mb.glu_gemv(h, w, w)
+    with pytest.raises(TypeError):
+        mb.glu_gemv(h.float(), w, w)

@@ -1,0 +1,321 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Bar (tolerance.py): |delta| <= 1 bf16 ULP on >= 99.9% of outputs, relative
+error <= 1e-2 elsewhere (floored at the fp32-accumulation conditioning
+bound); the updated residual of add_rmsnorm_glu must match bit for bit (one
+correctly rounded addition).  Every workload is checked at its full size on
+a sampled layer, plus small shapes that span several tiles and ragged tails,
+strided and unaligned operands, and the degenerate cases.
+"""
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import glu_inputs as gi
+import oracle
+import tolerance as tol
+
+pytestmark = pytest.mark.gpu
+
+mb = pytest.importorskip("memory_bound_glu_gb300")
+DEV = torch.device("cuda:0")
+
+
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    _need_gpu()
+    yield
+
+
+def oracle_glu(h, g, u, mode):
+    out, diag = oracle.glu_gemv(gi.bits(h), gi.bits(g), gi.bits(u), mode, diagnostics=True)
+    return out, tol.conditioning_floor(diag, h.shape[1], mode)
+
+
+def run_gpu(h, g, u, mode, **kw):
+    out = mb.glu_gemv(h.to(DEV), g.to(DEV), u.to(DEV), mode=mode, **kw)
+    torch.cuda.synchronize()
+    return gi.bits(out.cpu())
+
+
+def check(h, g, u, mode, what="", variant=None):
+    got = run_gpu(h, g, u, mode)
+    if variant is not None:
+        assert mb.last_variant() == variant
+    ref, tau = oracle_glu(h, g, u, mode)
+    return tol.assert_parity(got, ref, tau, what)
+
+
+# ---------------------------------------------------------------------------
+# small shapes: tiles, tails, every batch size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+@pytest.mark.parametrize("M", list(range(1, 17)))
+def test_every_batch_size(M, mode):
+    N, K = 1337, 1024 + 256 + 8   # ragged N over 152 CTAs, K with a short last chunk
+    h = gi.normal_bf16((M, K), 1.0, M, "bs-h")
+    g = gi.normal_bf16((N, K), K ** -0.5, M, "bs-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, M, "bs-u")
+    check(h, g, u, mode, f"M={M}", variant=1)
+
+
+@pytest.mark.parametrize("N,K", [(1, 8), (7, 64), (152, 256), (153, 2048), (4096, 2056), (300, 4104),
+                                 (2000, 5120), (513, 8192)])
+def test_shapes_fast_path(N, K):
+    M = 3
+    h = gi.normal_bf16((M, K), 1.0, N, "sh-h")
+    g = gi.normal_bf16((N, K), K ** -0.5, N, "sh-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, N, "sh-u")
+    check(h, g, u, "hf", f"N={N} K={K}", variant=1)
+
+
+@pytest.mark.parametrize("K", [1, 7, 9, 1001])
+def test_ragged_k_uses_generic_kernel(K):
+    M, N = 2, 517
+    h = gi.normal_bf16((M, K), 1.0, K, "rk-h")
+    g = gi.normal_bf16((N, K), K ** -0.5, K, "rk-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, K, "rk-u")
+    for mode in ("fused", "hf"):
+        check(h, g, u, mode, f"K={K}", variant=2)
+
+
+def test_large_m16_k_uses_generic_when_h_does_not_fit():
+    M, N, K = 16, 300, 16384
+    h = gi.normal_bf16((M, K), 1.0, 1, "bigk-h")
+    g = gi.normal_bf16((N, K), K ** -0.5, 1, "bigk-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, 1, "bigk-u")
+    check(h, g, u, "fused", "M=16 K=16384", variant=2)
+
+
+def test_strided_views_fast_and_generic():
+    """Row strides are honoured: operands sliced out of wider buffers."""
+    M, N, K = 4, 999, 1536
+    hb = gi.normal_bf16((M, K + 40), 1.0, 2, "st-h")
+    gb = gi.normal_bf16((N, K + 64), K ** -0.5, 2, "st-g")
+    ub = gi.normal_bf16((N, K + 16), K ** -0.5, 2, "st-u")
+    h, g, u = hb[:, 8:8 + K], gb[:, :K], ub[:, 16:16 + K]
+    ref, tau = oracle_glu(h.contiguous(), g.contiguous(), u.contiguous(), "hf")
+    hd, gd, ud = hb.to(DEV)[:, 8:8 + K], gb.to(DEV)[:, :K], ub.to(DEV)[:, 16:16 + K]
+    outb = torch.full((M, N + 24), float("nan"), dtype=torch.bfloat16, device=DEV)
+    out = outb[:, 24:]
+    mb.glu_gemv(hd, gd, ud, out=out, mode="hf")
+    torch.cuda.synchronize()
+    assert mb.last_variant() == 1
+    tol.assert_parity(gi.bits(out.cpu()), ref, tau, "strided")
+    assert torch.isnan(outb[:, :24].float()).all(), "wrote outside out"
+    # an odd element offset breaks 16-byte alignment of the weights: generic kernel
+    g2 = gb.to(DEV)[:, 1:1 + K]
+    ref2, tau2 = oracle_glu(h.contiguous(), gb[:, 1:1 + K].contiguous(), u.contiguous(), "fused")
+    o2 = mb.glu_gemv(hd, g2, ud, mode="fused")
+    torch.cuda.synchronize()
+    assert mb.last_variant() == 2
+    tol.assert_parity(gi.bits(o2.cpu()), ref2, tau2, "unaligned")
+
+
+def test_guard_band_untouched():
+    M, N, K = 5, 2049, 1024
+    h = gi.normal_bf16((M, K), 1.0, 3, "gd-h")
+    g = gi.normal_bf16((N, K), K ** -0.5, 3, "gd-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, 3, "gd-u")
+    buf = torch.full((M + 2, N + 64), -7.0, dtype=torch.bfloat16, device=DEV)
+    out = buf[1:1 + M, 32:32 + N]
+    mb.glu_gemv(h.to(DEV), g.to(DEV), u.to(DEV), out=out, mode="fused")
+    torch.cuda.synchronize()
+    b = buf.float().cpu()
+    mask = torch.ones_like(b, dtype=torch.bool)
+    mask[1:1 + M, 32:32 + N] = False
+    assert (b[mask] == -7.0).all()
+    ref, tau = oracle_glu(h, g, u, "fused")
+    tol.assert_parity(gi.bits(out.cpu()), ref, tau, "guard")
+
+
+def test_degenerate_sizes():
+    K = 64
+    h = gi.normal_bf16((2, K), 1.0, 4, "dg-h").to(DEV)
+    w = gi.normal_bf16((10, K), 0.1, 4, "dg-w").to(DEV)
+    # N == 0 and M == 0: no-op
+    o = torch.empty((2, 0), dtype=torch.bfloat16, device=DEV)
+    mb.glu_gemv(h, w[:0], w[:0], out=o)
+    assert mb.last_variant() == 0
+    o = torch.full((0, 10), 1.0, dtype=torch.bfloat16, device=DEV)
+    mb.glu_gemv(h[:0], w, w, out=o)
+    # K == 0: +0 everywhere
+    o = torch.full((2, 10), 3.0, dtype=torch.bfloat16, device=DEV)
+    mb.glu_gemv(h[:, :0], w[:, :0], w[:, :0], out=o, mode="hf")
+    torch.cuda.synchronize()
+    assert mb.last_variant() == 3
+    assert (gi.bits(o.cpu()) == 0).all()
+    with pytest.raises(mb.MbgluError):
+        mb.glu_gemv(torch.zeros((17, K), dtype=torch.bfloat16, device=DEV), w, w)
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_closed_forms_on_gpu(mode):
+    K, N = 256, 300
+    h = gi.normal_bf16((4, K), 1.0, 5, "cf-h")
+    z = torch.zeros((N, K), dtype=torch.bfloat16)
+    assert (run_gpu(h, z, z, mode) == 0).all()            # zero weights -> +0
+    eye = torch.eye(K, dtype=torch.bfloat16)
+    got = run_gpu(h, eye, eye, mode)                       # identity rows: SiLU(h_i)*h_i
+    ref = oracle.glu_gemv(gi.bits(h), gi.bits(eye), gi.bits(eye), mode)
+    assert np.array_equal(tol.ordered(got), tol.ordered(ref))
+
+
+def test_deterministic_and_row_permutation_bitwise():
+    M, N, K = 8, 3000, 2560
+    h = gi.normal_bf16((M, K), 1.0, 6, "dp-h").to(DEV)
+    g = gi.normal_bf16((N, K), K ** -0.5, 6, "dp-g").to(DEV)
+    u = gi.normal_bf16((N, K), K ** -0.5, 6, "dp-u").to(DEV)
+    a = mb.glu_gemv(h, g, u, mode="hf")
+    b = mb.glu_gemv(h, g, u, mode="hf")
+    perm = torch.randperm(N, generator=torch.Generator().manual_seed(0)).to(DEV)
+    c = mb.glu_gemv(h, g[perm], u[perm], mode="hf")
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a[:, perm].view(torch.int16), c.view(torch.int16))
+
+
+def test_swap_gate_and_up_matches_oracle_swap():
+    M, N, K = 2, 777, 1024
+    h = gi.normal_bf16((M, K), 1.0, 7, "sw-h")
+    g = gi.normal_bf16((N, K), K ** -0.5, 7, "sw-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, 7, "sw-u")
+    check(h, u, g, "fused", "swapped")
+
+
+def test_in_place_weight_update_is_seen():
+    """No state derived from the weights: an in-place update shows at once."""
+    M, N, K = 1, 2000, 2048
+    h = gi.normal_bf16((M, K), 1.0, 8, "ip-h")
+    g = gi.normal_bf16((N, K), K ** -0.5, 8, "ip-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, 8, "ip-u")
+    hd, gd, ud = h.to(DEV), g.to(DEV), u.to(DEV)
+    mb.glu_gemv(hd, gd, ud, mode="hf")
+    g2 = gi.normal_bf16((N, K), K ** -0.5, 9, "ip-g")
+    gd.copy_(g2.to(DEV))
+    out = mb.glu_gemv(hd, gd, ud, mode="hf")
+    torch.cuda.synchronize()
+    ref, tau = oracle_glu(h, g2, u, "hf")
+    tol.assert_parity(gi.bits(out.cpu()), ref, tau, "after in-place update")
+
+
+def test_cuda_graph_replay_matches_eager():
+    M, N, K = 4, 4000, 2560
+    h = gi.normal_bf16((M, K), 1.0, 10, "cg-h").to(DEV)
+    g = gi.normal_bf16((N, K), K ** -0.5, 10, "cg-g").to(DEV)
+    u = gi.normal_bf16((N, K), K ** -0.5, 10, "cg-u").to(DEV)
+    x = gi.normal_bf16((M, K), 1.0, 10, "cg-x").to(DEV)
+    r0 = gi.normal_bf16((M, K), 1.0, 10, "cg-r").to(DEV)
+    w = gi.normal_bf16((K,), 0.1, 10, "cg-w").to(DEV)
+    eager = mb.glu_gemv(h, g, u, mode="fused")
+    r_e = r0.clone()
+    eager2 = mb.add_rmsnorm_glu(x, r_e, w, 1e-6, g, u, mode="hf")
+    out = torch.empty_like(eager)
+    out2 = torch.empty_like(eager2)
+    r_g = r0.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            mb.glu_gemv(h, g, u, out=out, mode="fused")
+            mb.add_rmsnorm_glu(x, r_g, w, 1e-6, g, u, out=out2, mode="hf")
+    r_g.copy_(r0)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    assert torch.equal(out2.view(torch.int16), eager2.view(torch.int16))
+    assert torch.equal(r_g.view(torch.int16), r_e.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# add_rmsnorm_glu
+# ---------------------------------------------------------------------------
+
+def check_norm(x, r, w, g, u, mode, eps=1e-6, what="", variant=None):
+    rd = r.to(DEV)
+    out = mb.add_rmsnorm_glu(x.to(DEV), rd, w.to(DEV), eps, g.to(DEV), u.to(DEV), mode=mode)
+    torch.cuda.synchronize()
+    if variant is not None:
+        assert mb.last_variant() == variant
+    ref, res, hn = oracle.add_rmsnorm_glu(gi.bits(x), gi.bits(r), gi.bits(w), eps, gi.bits(g), gi.bits(u), mode)
+    assert np.array_equal(gi.bits(rd.cpu()), res), f"residual {what}"
+    _, diag = oracle.glu_gemv(hn, gi.bits(g), gi.bits(u), mode, diagnostics=True)
+    tau = tol.conditioning_floor(diag, x.shape[1], mode)
+    return tol.assert_parity(gi.bits(out.cpu()), ref, tau, what)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 13, 16])
+def test_add_rmsnorm_glu_small(M):
+    N, K = 1500, 2048
+    x = gi.normal_bf16((M, K), 1.0, M, "an-x")
+    r = gi.normal_bf16((M, K), 1.0, M, "an-r")
+    w = gi.normal_bf16((K,), 0.1, M, "an-w")
+    g = gi.normal_bf16((N, K), K ** -0.5, M, "an-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, M, "an-u")
+    for mode in ("hf", "fused"):
+        check_norm(x, r, w, g, u, mode, what=f"M={M} {mode}", variant=1)
+
+
+def test_add_rmsnorm_glu_generic_and_edge_cases():
+    M, N, K = 3, 400, 1000 + 4   # K % 8 != 0 -> generic kernel with the norm in smem
+    x = gi.normal_bf16((M, K), 1.0, 1, "ae-x")
+    r = gi.normal_bf16((M, K), 1.0, 1, "ae-r")
+    w = gi.normal_bf16((K,), 0.1, 1, "ae-w")
+    g = gi.normal_bf16((N, K), K ** -0.5, 1, "ae-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, 1, "ae-u")
+    check_norm(x, r, w, g, u, "hf", what="generic", variant=2)
+    # x = -residual: s = 0, h = 0, out = +0
+    K2 = 512
+    x2 = gi.normal_bf16((2, K2), 1.0, 2, "ae-x2")
+    g2 = gi.normal_bf16((N, K2), 0.05, 2, "ae-g2")
+    rd = (-x2).to(DEV)
+    out = mb.add_rmsnorm_glu(x2.to(DEV), rd, torch.zeros(K2, dtype=torch.bfloat16, device=DEV), 1e-6,
+                             g2.to(DEV), g2.to(DEV), mode="hf")
+    torch.cuda.synchronize()
+    assert (gi.bits(rd.cpu()) & 0x7FFF == 0).all()
+    assert (gi.bits(out.cpu()) & 0x7FFF == 0).all()
+    # residual == x is allowed: s = bf16(2x)
+    xd = x2.to(DEV)
+    mb.add_rmsnorm_glu(xd, xd, torch.zeros(K2, dtype=torch.bfloat16, device=DEV), 1e-6, g2.to(DEV),
+                       g2.to(DEV), mode="hf")
+    torch.cuda.synchronize()
+    assert torch.equal(xd.cpu(), (x2.float() * 2).to(torch.bfloat16))
+
+
+# ---------------------------------------------------------------------------
+# every workload at full size, one sampled layer
+# ---------------------------------------------------------------------------
+
+@functools.lru_cache(maxsize=1)
+def _layer(name, layer):
+    return gi.layer_weights(gi.WORKLOADS[name], layer)
+
+
+FULL_CASES = [(w.name, M, mode) for w in gi.WORKLOADS.values() for M in w.Ms for mode in w.modes]
+
+
+@pytest.mark.parametrize("name,M,mode", FULL_CASES)
+def test_full_size_workload(name, M, mode):
+    w = gi.WORKLOADS[name]
+    layer = w.layers - 1          # the last layer of the cycled set
+    g, u = _layer(name, layer)
+    if w.op == "glu_gemv":
+        h = gi.hidden(w, M)
+        st = check(h, g, u, mode, f"{name} M={M} {mode}", variant=1)
+    else:
+        x, r, nw = gi.norm_inputs(w, M)
+        st = check_norm(x, r, nw, g, u, mode, eps=w.eps, what=f"{name} M={M}", variant=1)
+    assert st["exact_frac"] > 0.9
+
+
+def test_device_error_word_is_clear():
+    assert mb.read_device_error() == 0
