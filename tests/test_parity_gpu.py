@@ -36,7 +36,12 @@ def _gpu():
 
 def oracle_glu(h, g, u, mode):
     out, diag = oracle.glu_gemv(gi.bits(h), gi.bits(g), gi.bits(u), mode, diagnostics=True)
-    return out, tol.conditioning_floor(diag, h.shape[1], mode)
+    return out, (tol.conditioning_floor(diag, h.shape[1], mode), diag, h.shape[1], mode)
+
+
+def parity(got, ref, tau_info, what=""):
+    tau, diag, K, mode = tau_info
+    return tol.assert_parity(got, ref, tau, what, diag=diag, K=K, mode=mode)
 
 
 def run_gpu(h, g, u, mode, **kw):
@@ -50,7 +55,7 @@ def check(h, g, u, mode, what="", variant=None):
     if variant is not None:
         assert mb.last_variant() == variant
     ref, tau = oracle_glu(h, g, u, mode)
-    return tol.assert_parity(got, ref, tau, what)
+    return parity(got, ref, tau, what)
 
 
 # ---------------------------------------------------------------------------
@@ -109,7 +114,7 @@ def test_strided_views_fast_and_generic():
     mb.glu_gemv(hd, gd, ud, out=out, mode="hf")
     torch.cuda.synchronize()
     assert mb.last_variant() == 1
-    tol.assert_parity(gi.bits(out.cpu()), ref, tau, "strided")
+    parity(gi.bits(out.cpu()), ref, tau, "strided")
     assert torch.isnan(outb[:, :24].float()).all(), "wrote outside out"
     # an odd element offset breaks 16-byte alignment of the weights: generic kernel
     g2 = gb.to(DEV)[:, 1:1 + K]
@@ -117,7 +122,7 @@ def test_strided_views_fast_and_generic():
     o2 = mb.glu_gemv(hd, g2, ud, mode="fused")
     torch.cuda.synchronize()
     assert mb.last_variant() == 2
-    tol.assert_parity(gi.bits(o2.cpu()), ref2, tau2, "unaligned")
+    parity(gi.bits(o2.cpu()), ref2, tau2, "unaligned")
 
 
 def test_guard_band_untouched():
@@ -134,7 +139,7 @@ def test_guard_band_untouched():
     mask[1:1 + M, 32:32 + N] = False
     assert (b[mask] == -7.0).all()
     ref, tau = oracle_glu(h, g, u, "fused")
-    tol.assert_parity(gi.bits(out.cpu()), ref, tau, "guard")
+    parity(gi.bits(out.cpu()), ref, tau, "guard")
 
 
 def test_degenerate_sizes():
@@ -204,7 +209,7 @@ def test_in_place_weight_update_is_seen():
     out = mb.glu_gemv(hd, gd, ud, mode="hf")
     torch.cuda.synchronize()
     ref, tau = oracle_glu(h, g2, u, "hf")
-    tol.assert_parity(gi.bits(out.cpu()), ref, tau, "after in-place update")
+    parity(gi.bits(out.cpu()), ref, tau, "after in-place update")
 
 
 def test_cuda_graph_replay_matches_eager():
@@ -249,8 +254,8 @@ def check_norm(x, r, w, g, u, mode, eps=1e-6, what="", variant=None):
     ref, res, hn = oracle.add_rmsnorm_glu(gi.bits(x), gi.bits(r), gi.bits(w), eps, gi.bits(g), gi.bits(u), mode)
     assert np.array_equal(gi.bits(rd.cpu()), res), f"residual {what}"
     _, diag = oracle.glu_gemv(hn, gi.bits(g), gi.bits(u), mode, diagnostics=True)
-    tau = tol.conditioning_floor(diag, x.shape[1], mode)
-    return tol.assert_parity(gi.bits(out.cpu()), ref, tau, what)
+    K = x.shape[1]
+    return parity(gi.bits(out.cpu()), ref, (tol.conditioning_floor(diag, K, mode), diag, K, mode), what)
 
 
 @pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 13, 16])

@@ -1,0 +1,123 @@
+"""The parity checker accepts what fp32 accumulation may legitimately produce
+and rejects plausible kernel mistakes.  CPU only: "GPU" results are simulated
+from the oracle's own dot products."""
+import numpy as np
+import pytest
+
+import glu_inputs as gi
+import oracle
+import tolerance as tol
+
+
+def _case(mode, seed=0, M=4, N=3000, K=2560):
+    h = gi.bits(gi.normal_bf16((M, K), 1.0, seed, "tol-h"))
+    g = gi.bits(gi.normal_bf16((N, K), K ** -0.5, seed, "tol-g"))
+    u = gi.bits(gi.normal_bf16((N, K), K ** -0.5, seed, "tol-u"))
+    out, diag = oracle.glu_gemv(h, g, u, mode, diagnostics=True)
+    return out, diag, K
+
+
+def _chain(G, U, mode):
+    b = tol._bf16_bits
+    f = tol.bf16_bits_to_f64
+    if mode == "fused":
+        return b(tol._silu(G) * U)
+    sb = f(b(tol._silu(f(b(G)))))
+    return b(sb * f(b(U)))
+
+
+def _fp32_chain(h, g, u, mode, lanes=32):
+    """A realistic kernel: exact products, fp32 partial sums per lane over a
+    strided K split, a fp32 tree over lanes, fp32 epilogue."""
+    hf = tol.bf16_bits_to_f64(h).astype(np.float32)
+    gf = tol.bf16_bits_to_f64(g).astype(np.float32)
+    uf = tol.bf16_bits_to_f64(u).astype(np.float32)
+    M, K = hf.shape
+    def dot(w):
+        acc = np.zeros((M, w.shape[0], lanes), dtype=np.float32)
+        for k0 in range(0, K, lanes):
+            blk = (hf[:, None, k0:k0 + lanes] * w[None, :, k0:k0 + lanes]).astype(np.float32)
+            acc[:, :, :blk.shape[2]] += blk
+        while acc.shape[2] > 1:
+            half = acc.shape[2] // 2
+            acc = (acc[:, :, :half] + acc[:, :, half:]).astype(np.float32)
+        return acc[:, :, 0]
+    G, U = dot(gf), dot(uf)
+    silu = lambda x: (x / (np.float32(1) + np.exp(-x))).astype(np.float32)  # noqa: E731
+    if mode == "fused":
+        return tol._bf16_bits((silu(G) * U).astype(np.float64))
+    f = lambda b: tol.bf16_bits_to_f64(b).astype(np.float32)  # noqa: E731
+    sb = f(tol._bf16_bits(silu(f(tol._bf16_bits(G)))))
+    return tol._bf16_bits((sb * f(tol._bf16_bits(U))).astype(np.float64))
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_fp32_accumulation_in_another_order_passes(mode):
+    M, N, K = 4, 1500, 2560
+    h = gi.bits(gi.normal_bf16((M, K), 1.0, 2, "tol-h"))
+    g = gi.bits(gi.normal_bf16((N, K), K ** -0.5, 2, "tol-g"))
+    u = gi.bits(gi.normal_bf16((N, K), K ** -0.5, 2, "tol-u"))
+    out, diag = oracle.glu_gemv(h, g, u, mode, diagnostics=True)
+    sim = _fp32_chain(h, g, u, mode)
+    st = tol.compare(sim, out, tol.conditioning_floor(diag, K, mode), diag, K, mode)
+    assert tol.passes(st), st
+    assert st["exact_frac"] > 0.95
+
+
+def test_hf_gate_flip_is_admissible_only_inside_the_box():
+    out, diag, K = _case("hf", seed=3)
+    gamma = tol.accumulation_gamma(K)
+    G, U = diag["G"].reshape(-1), diag["U"].reshape(-1)
+    dG = gamma * diag["Ag"].reshape(-1)
+    dU = gamma * diag["Au"].reshape(-1)
+    flat = out.reshape(-1)
+    accepted = rejected = 0
+    # accept cases from the steep negative tail, reject cases from anywhere
+    for i in list(np.argsort(G)[:400]) + list(range(0, G.size, 7)):
+        gb = tol._bf16_bits(G[i:i + 1])
+        cur = tol.bf16_bits_to_f64(gb)[0]
+        up, dn = tol.bf16_bits_to_f64(gb + np.uint16(1))[0], tol.bf16_bits_to_f64(gb - np.uint16(1))[0]
+        mids = ((cur + up) / 2, (cur + dn) / 2)
+        reach = [abs(m - G[i]) <= dG[i] for m in mids]
+        tau = tol.conditioning_floor(diag, K, "hf")
+        if reach[0]:
+            flipped = _chain(np.array([up]), U[i:i + 1], "hf")[0]
+            if tol.ulp_distance(np.array([flipped]), flat[i:i + 1])[0] > 1:
+                sim = flat.copy()
+                sim[i] = flipped
+                st = tol.compare(sim.reshape(out.shape), out, tau, diag, K, "hf")
+                assert st["alt_rounding"] == 1 and st["max_rel_elsewhere"] == 0.0
+                accepted += 1
+        elif not any(reach) and dU[i] < abs(U[i]) * 2.0 ** -12:   # u well conditioned
+            o = tol.ordered(flat[i:i + 1])[0]
+            off = o + 6 if o >= 0 else o - 6   # a ub flip moves out by ~1 ULP at most
+            bits = np.uint16(off) if off >= 0 else np.uint16(0x8000 | (-off))
+            sim = flat.copy()
+            sim[i] = bits
+            st = tol.compare(sim.reshape(out.shape), out, tau, diag, K, "hf")
+            assert st["alt_rounding"] == 0 and st["max_rel_elsewhere"] > 0
+            rejected += 1
+    assert accepted > 0 and rejected > 0
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+@pytest.mark.parametrize("mistake", ["dropped_term", "swapped_roles", "sign", "row_shift", "stale_rows"])
+def test_plausible_kernel_mistakes_fail(mode, mistake):
+    M, N, K = 4, 3000, 2560
+    h = gi.bits(gi.normal_bf16((M, K), 1.0, 5, "tm-h"))
+    g = gi.bits(gi.normal_bf16((N, K), K ** -0.5, 5, "tm-g"))
+    u = gi.bits(gi.normal_bf16((N, K), K ** -0.5, 5, "tm-u"))
+    out, diag = oracle.glu_gemv(h, g, u, mode, diagnostics=True)
+    if mistake == "dropped_term":     # last 8 columns of K ignored
+        bad = oracle.glu_gemv(np.ascontiguousarray(h[:, :K - 8]), np.ascontiguousarray(g[:, :K - 8]),
+                              np.ascontiguousarray(u[:, :K - 8]), mode)
+    elif mistake == "swapped_roles":  # SiLU applied to the up product
+        bad = oracle.glu_gemv(h, u, g, mode)
+    elif mistake == "sign":
+        bad = out ^ np.uint16(0x8000)
+    elif mistake == "row_shift":      # output feature n written at n+1
+        bad = np.roll(out, 1, axis=1)
+    else:                             # rows past the first batch row reuse row 0
+        bad = np.repeat(out[:1], M, axis=0)
+    st = tol.compare(bad, out, tol.conditioning_floor(diag, K, mode), diag, K, mode)
+    assert not tol.passes(st), (mistake, st)

@@ -7,14 +7,23 @@ Readings used here:
   * ULP distance: the two bf16 patterns mapped to ordered integers
     (sign-magnitude -> two's complement), with +0 and -0 the same point.
   * Relative error of an output outside 1 ULP: |gpu - ref| / max(|ref|, tau),
-    where tau bounds what fp32 accumulation alone can move the output.  With
-    gamma = K * 2^-24 (the classical bound on a K-term fp32 sum) and the
-    oracle's sums of |h*w| (Ag, Au):
+    where tau bounds what fp32 accumulation alone can move the output.  The
+    kernels sum each dot product as 32 strided lane sums of ceil(K/32) terms
+    (exact bf16 x bf16 products, one rounding per FMA) followed by a 5-level
+    butterfly, so |g - G| <= gamma * Ag with gamma = (ceil(K/32) + 5) * 2^-24
+    (the classical depth bound) and Ag the oracle's sum of |h*w| (likewise u):
         dg = gamma*Ag,  du = gamma*Au,
         tau = |SiLU'(G)*U|*dg + |SiLU(G)|*du  (HF mode adds 2^-8*|G| to dg
               and 2^-8*|U| to du for the bf16 roundings of g and u).
-    An output with |ref| < tau sits where u or SiLU(g)*u cancels; any fp32
-    summation order may legitimately land anywhere inside tau of it.
+    An output with |ref| < tau sits where u or SiLU(g)*u cancels.
+  * Rounding decisions taken from a sum (HF mode rounds g and u to bf16
+    before SiLU) may legitimately go either way when the exact sum lies
+    within dg (du) of a rounding midpoint; SiLU can then amplify one flip of
+    gb into a few output ULPs (its log-slope is about 4 at g = -5).  An output
+    outside 1 ULP is therefore also accepted when it lies within 1 ULP of the
+    range the mode's chain takes over g in [G - dg, G + dg], u in
+    [U - du, U + du] (interval arithmetic over the monotone pieces, SiLU's
+    minimum near g = -1.2785 included).  These are counted as "alt_rounding".
   * Non-finite outputs must match exactly.
 """
 from __future__ import annotations
@@ -51,9 +60,14 @@ def _dsilu(x):
     return s * (1.0 + x * (1.0 - s))
 
 
+def accumulation_gamma(K: int) -> float:
+    """Relative bound of the kernels' fp32 dot products (depth ceil(K/32)+5)."""
+    return (-(-K // 32) + 5) * 2.0 ** -24
+
+
 def conditioning_floor(diag, K: int, mode: str) -> np.ndarray:
     G, U, Ag, Au = diag["G"], diag["U"], diag["Ag"], diag["Au"]
-    gamma = K * 2.0 ** -24
+    gamma = accumulation_gamma(K)
     dg, du = gamma * Ag, gamma * Au
     if mode == "hf":
         dg = dg + 2.0 ** -8 * np.abs(G)
@@ -61,7 +75,55 @@ def conditioning_floor(diag, K: int, mode: str) -> np.ndarray:
     return np.abs(_dsilu(G) * U) * dg + np.abs(_silu(G)) * du
 
 
-def compare(gpu_bits, ref_bits, tau=None) -> dict:
+def _bf16_bits(x) -> np.ndarray:
+    """float64 -> bf16 bits (via float32; used for candidate values only)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).to(torch.float32).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+SILU_ARGMIN = -1.2784645427610738
+
+
+def _silu_range(lo, hi):
+    """[min, max] of SiLU over [lo, hi] (decreasing, then increasing)."""
+    a, b = _silu(lo), _silu(hi)
+    inside = (lo <= SILU_ARGMIN) & (SILU_ARGMIN <= hi)
+    mn = np.where(inside, _silu(np.full_like(lo, SILU_ARGMIN)), np.minimum(a, b))
+    return mn, np.maximum(a, b)
+
+
+def _product_range(alo, ahi, blo, bhi):
+    c = np.stack([alo * blo, alo * bhi, ahi * blo, ahi * bhi])
+    return c.min(0), c.max(0)
+
+
+def alternative_ok(gpu_bits, diag, K: int, mode: str, idx) -> np.ndarray:
+    """For the flat indices idx: does the GPU output lie within 1 ULP of the
+    range the mode's chain takes with g, u anywhere in their fp32 error box?"""
+    g = np.asarray(gpu_bits).reshape(-1)[idx]
+    G = diag["G"].reshape(-1)[idx]
+    U = diag["U"].reshape(-1)[idx]
+    gamma = accumulation_gamma(K)
+    dG = gamma * diag["Ag"].reshape(-1)[idx]
+    dU = gamma * diag["Au"].reshape(-1)[idx]
+    f, b = bf16_bits_to_f64, _bf16_bits
+    if mode == "hf":
+        # rounding is monotone: the reachable gb, ub are the roundings of the ends
+        glo, ghi = f(b(G - dG)), f(b(G + dG))
+        smin, smax = _silu_range(glo, ghi)
+        slo, shi = f(b(smin)), f(b(smax))
+        ulo, uhi = f(b(U - dU)), f(b(U + dU))
+        lo, hi = _product_range(slo, shi, ulo, uhi)
+    else:
+        smin, smax = _silu_range(G - dG, G + dG)
+        lo, hi = _product_range(smin, smax, U - dU, U + dU)
+    lob, hib = b(lo), b(hi)
+    gv = f(g)
+    return ((gv >= f(lob)) & (gv <= f(hib))) | (ulp_distance(g, lob) <= 1) | (ulp_distance(g, hib) <= 1)
+
+
+def compare(gpu_bits, ref_bits, tau=None, diag=None, K=None, mode=None) -> dict:
     gpu_bits = np.asarray(gpu_bits, dtype=np.uint16)
     ref_bits = np.asarray(ref_bits, dtype=np.uint16)
     assert gpu_bits.shape == ref_bits.shape, (gpu_bits.shape, ref_bits.shape)
@@ -78,6 +140,14 @@ def compare(gpu_bits, ref_bits, tau=None) -> dict:
         raw = np.where(floor > 0, np.abs(g - r) / floor, np.where(g == r, 0.0, np.inf))
     rel = np.where(within | ~fin_r, 0.0, raw)
     rel = np.where(np.isnan(rel), np.inf, rel)
+    alt = 0
+    if diag is not None and np.any(rel > 0):
+        idx = np.flatnonzero((rel > 0).reshape(-1))
+        okf = alternative_ok(gpu_bits, diag, K, mode, idx)
+        flat = rel.reshape(-1).copy()
+        flat[idx[okf]] = 0.0
+        alt = int(okf.sum())
+        rel = flat.reshape(rel.shape)
     ill = 0 if tau is None else int(np.sum(~within & fin_r & (np.abs(r) < np.asarray(tau))))
     return {
         "n": n,
@@ -86,6 +156,7 @@ def compare(gpu_bits, ref_bits, tau=None) -> dict:
         "max_ulp": int(d.max()) if n else 0,
         "max_rel_elsewhere": float(rel.max()) if n else 0.0,
         "ill_conditioned": ill,
+        "alt_rounding": alt,
         "nonfinite_mismatch": nonfinite_mismatch,
     }
 
@@ -96,7 +167,7 @@ def passes(stats: dict) -> bool:
             and stats["nonfinite_mismatch"] == 0)
 
 
-def assert_parity(gpu_bits, ref_bits, tau=None, what=""):
-    st = compare(gpu_bits, ref_bits, tau)
+def assert_parity(gpu_bits, ref_bits, tau=None, what="", diag=None, K=None, mode=None):
+    st = compare(gpu_bits, ref_bits, tau, diag, K, mode)
     assert passes(st), f"parity failed {what}: {st}"
     return st
