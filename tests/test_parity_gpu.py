@@ -254,6 +254,7 @@ def check_norm(x, r, w, g, u, mode, eps=1e-6, what="", variant=None):
     ref, res, hn = oracle.add_rmsnorm_glu(gi.bits(x), gi.bits(r), gi.bits(w), eps, gi.bits(g), gi.bits(u), mode)
     assert np.array_equal(gi.bits(rd.cpu()), res), f"residual {what}"
     _, diag = oracle.glu_gemv(hn, gi.bits(g), gi.bits(u), mode, diagnostics=True)
+    diag["dG_extra"], diag["dU_extra"] = tol.norm_rounding_slack(res, gi.bits(w), eps, gi.bits(g), gi.bits(u))
     K = x.shape[1]
     return parity(gi.bits(out.cpu()), ref, (tol.conditioning_floor(diag, K, mode), diag, K, mode), what)
 

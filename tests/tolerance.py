@@ -23,7 +23,14 @@ Readings used here:
     outside 1 ULP is therefore also accepted when it lies within 1 ULP of the
     range the mode's chain takes over g in [G - dg, G + dg], u in
     [U - du, U + du] (interval arithmetic over the monotone pieces, SiLU's
-    minimum near g = -1.2785 included).  These are counted as "alt_rounding".
+    minimum near g = -1.2785 included).  These are counted as "alt_rounding"
+    and, being correct results, count toward the 99.9%; plain 1-ULP agreement
+    with the oracle's own result must still reach 99%.
+  * add_rmsnorm_glu: the normed h is rounded to bf16 from an fp32 chain
+    (the pages fix the norm's precision at fp32).  Elements whose exact value
+    lies within that chain's error of a bf16 midpoint may round either way;
+    norm_rounding_slack() widens dg, du per row by sum_k ulp(h_k)*|w_nk| over
+    those elements.
   * Non-finite outputs must match exactly.
 """
 from __future__ import annotations
@@ -68,7 +75,7 @@ def accumulation_gamma(K: int) -> float:
 def conditioning_floor(diag, K: int, mode: str) -> np.ndarray:
     G, U, Ag, Au = diag["G"], diag["U"], diag["Ag"], diag["Au"]
     gamma = accumulation_gamma(K)
-    dg, du = gamma * Ag, gamma * Au
+    dg, du = gamma * Ag + diag.get("dG_extra", 0.0), gamma * Au + diag.get("dU_extra", 0.0)
     if mode == "hf":
         dg = dg + 2.0 ** -8 * np.abs(G)
         du = du + 2.0 ** -8 * np.abs(U)
@@ -107,6 +114,9 @@ def alternative_ok(gpu_bits, diag, K: int, mode: str, idx) -> np.ndarray:
     gamma = accumulation_gamma(K)
     dG = gamma * diag["Ag"].reshape(-1)[idx]
     dU = gamma * diag["Au"].reshape(-1)[idx]
+    if "dG_extra" in diag:
+        dG = dG + np.broadcast_to(diag["dG_extra"], diag["G"].shape).reshape(-1)[idx]
+        dU = dU + np.broadcast_to(diag["dU_extra"], diag["U"].shape).reshape(-1)[idx]
     f, b = bf16_bits_to_f64, _bf16_bits
     if mode == "hf":
         # rounding is monotone: the reachable gb, ub are the roundings of the ends
@@ -141,6 +151,7 @@ def compare(gpu_bits, ref_bits, tau=None, diag=None, K=None, mode=None) -> dict:
     rel = np.where(within | ~fin_r, 0.0, raw)
     rel = np.where(np.isnan(rel), np.inf, rel)
     alt = 0
+    strict = frac
     if diag is not None and np.any(rel > 0):
         idx = np.flatnonzero((rel > 0).reshape(-1))
         okf = alternative_ok(gpu_bits, diag, K, mode, idx)
@@ -148,11 +159,13 @@ def compare(gpu_bits, ref_bits, tau=None, diag=None, K=None, mode=None) -> dict:
         flat[idx[okf]] = 0.0
         alt = int(okf.sum())
         rel = flat.reshape(rel.shape)
+        frac = frac + alt / n
     ill = 0 if tau is None else int(np.sum(~within & fin_r & (np.abs(r) < np.asarray(tau))))
     return {
         "n": n,
         "exact_frac": float(np.mean(d == 0)) if n else 1.0,
-        "within_1ulp_frac": frac,
+        "within_1ulp_frac": frac,          # of a correct result (oracle or admissible alternative)
+        "within_1ulp_of_oracle": strict,
         "max_ulp": int(d.max()) if n else 0,
         "max_rel_elsewhere": float(rel.max()) if n else 0.0,
         "ill_conditioned": ill,
@@ -161,8 +174,12 @@ def compare(gpu_bits, ref_bits, tau=None, diag=None, K=None, mode=None) -> dict:
     }
 
 
+STRICT_FLOOR = 0.99   # sanity floor on plain 1-ULP agreement with the oracle's own result
+
+
 def passes(stats: dict) -> bool:
     return (stats["within_1ulp_frac"] >= ULP_FRAC_REQUIRED
+            and stats.get("within_1ulp_of_oracle", 1.0) >= STRICT_FLOOR
             and stats["max_rel_elsewhere"] <= MAX_REL_ELSEWHERE
             and stats["nonfinite_mismatch"] == 0)
 
@@ -171,3 +188,27 @@ def assert_parity(gpu_bits, ref_bits, tau=None, what="", diag=None, K=None, mode
     st = compare(gpu_bits, ref_bits, tau, diag, K, mode)
     assert passes(st), f"parity failed {what}: {st}"
     return st
+
+
+def norm_rounding_slack(s_bits, norm_w_bits, eps, gate_bits, up_bits):
+    """(dG_extra, dU_extra) [M, N]: how far the GEMV's dot products may move
+    when the fp32 norm rounds an element of h to the other bf16 neighbour.
+    The kernels' statistic sums K/256 terms per thread, then 5 + 16 levels;
+    the scale adds sqrt, division and two products: eps_rel below bounds it."""
+    sv = bf16_bits_to_f64(s_bits)
+    w = bf16_bits_to_f64(norm_w_bits)
+    M, K = sv.shape
+    var = np.mean(sv * sv, axis=1, keepdims=True)
+    v = sv / np.sqrt(var + float(np.float32(eps))) * (1.0 + w)[None, :]
+    eps_rel = (-(-K // 256) + 32) * 2.0 ** -24
+    av = np.abs(v)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(av > 0, av, 1.0)))
+    ulp = np.exp2(np.maximum(e, -126.0) - 7.0)
+    r = np.round(v / ulp)                      # nearest multiple of ulp (tie rule irrelevant here)
+    mid_dist = np.abs(np.abs(v / ulp - r) - 0.5) * ulp
+    amb = (mid_dist <= eps_rel * av + 1e-300) & (av > 0)
+    slack = np.where(amb, ulp, 0.0)            # [M, K]
+    dG = slack @ np.abs(bf16_bits_to_f64(gate_bits)).T
+    dU = slack @ np.abs(bf16_bits_to_f64(up_bits)).T
+    return dG, dU
