@@ -69,8 +69,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
 }
 
-// SiLU(x) = x / (1 + e^-x): precise expf and IEEE division (no fast math).
-__device__ __forceinline__ float silu_f32(float x) { return x / (1.0f + expf(-x)); }
+// SiLU(x) = x / (1 + e^-x) = x * e^x / (1 + e^x), evaluated with t = e^-|x| so
+// that nothing overflows: for x < -88.7 the first form's e^-x is +inf in fp32
+// and would flush SiLU to -0, although x * e^x is still a normal bf16 value
+// down to x ~ -92 (bf16 keeps fp32's exponent range).  Precise expf and IEEE
+// division (no fast math).
+__device__ __forceinline__ float silu_f32(float x)
+{
+    const float t = expf(-fabsf(x));
+    return (x >= 0.0f ? x : x * t) / (1.0f + t);
+}
 
 // mode 0 (FUSED): one rounding.  mode 1 (HF): the bf16 composite's roundings
 // of g, u, SiLU(g) and the product (PR #9057 "Changes": "Restore HF's

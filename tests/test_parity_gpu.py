@@ -174,6 +174,27 @@ def test_closed_forms_on_gpu(mode):
     assert np.array_equal(tol.ordered(got), tol.ordered(ref))
 
 
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_silu_exhaustive_over_bf16_gate_values_on_gpu(mode):
+    """h = e_0, W_gate[:,0] = every finite bf16, W_up[:,0] = 1: out = bf16(SiLU(g))
+    for every g, including the far negative tail where e^-g overflows fp32."""
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    g = pats[(pats & 0x7FFF) < 0x7F80]
+    N, K = g.size, 8
+    gw = np.zeros((N, K), dtype=np.uint16)
+    gw[:, 0] = g
+    uw = np.zeros((N, K), dtype=np.uint16)
+    uw[:, 0] = 0x3F80
+    h = np.zeros((1, K), dtype=np.uint16)
+    h[0, 0] = 0x3F80
+    got = run_gpu(gi.from_bits(h), gi.from_bits(gw), gi.from_bits(uw), mode)
+    assert mb.last_variant() == 1
+    ref = oracle.glu_gemv(h, gw, uw, mode)
+    d = tol.ulp_distance(got, ref)
+    assert d.max() <= 1, (g[d.argmax()], got[0, d.argmax()], ref[0, d.argmax()])
+    assert np.mean(d == 0) > 0.999
+
+
 def test_deterministic_and_row_permutation_bitwise():
     M, N, K = 8, 3000, 2560
     h = gi.normal_bf16((M, K), 1.0, 6, "dp-h").to(DEV)
