@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--policy", type=int, default=None, choices=[0, 1, 2],
+                    help="launch policy (default: the library's, 2 = PDL + weight prefetch)")
     return ap.parse_args()
 
 
@@ -268,7 +270,16 @@ def config_dict(w, M, mode, layers):
     wb = w.weight_bytes() * layers
     return {"workload": w.name, "op": w.op, "M": M, "K": w.K, "N": w.N, "mode": mode, "layers": layers,
             "l2": f"inputs larger than L2: {layers} cycled weight pairs, {wb / 1e9:.2f} GB",
-            "launch": f"one CUDA graph of {layers} calls per step"}
+            "launch": f"one CUDA graph of {layers} calls per step",
+            "launch_policy": _policy_name()}
+
+
+def _policy_name():
+    try:
+        import memory_bound_glu_gb300 as mb
+        return {0: "serial", 1: "pdl", 2: "pdl+weight-prefetch"}[mb.get_launch_policy()]
+    except Exception:
+        return None
 
 
 # ---------------------------------------------------------------------------
@@ -294,6 +305,8 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     mb.lib()
+    if args.policy is not None:
+        mb.set_launch_policy(args.policy)
 
     # inputs: resident in HBM before the timed region
     gates, ups = [], []

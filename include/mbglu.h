@@ -127,15 +127,42 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh,
  *   shared-memory budget (M*K <= 81920, e.g. M=16 with K=5120).
  *   out must not overlap any input; residual must not overlap x partially,
  *   nor norm_w, gate_w, up_w (MBGLU_ERR_ALIAS).  residual == x is allowed.
- * Two kernels run on `stream`: the residual add, then the GEMV, launched
- * with programmatic dependent launch so the GEMV prefetches weights while the
- * add finishes; it reads residual only after the add has completed.
+ * Two kernels run on `stream`: the residual add, then the GEMV, which reads
+ * residual only after the add has completed (see the launch policy below
+ * for what each may do before its predecessor has finished).
  */
 mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual,
                              const mbglu_bf16 *norm_w, float eps,
                              const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w,
                              mbglu_bf16 *out, int M, int N, int K,
                              mbglu_mode mode, cudaStream_t stream);
+
+/*
+ * Launch policy, process-wide (default MBGLU_POLICY_PREFETCH).  It decides how
+ * a call's kernels are ordered after the kernel that precedes them on the
+ * stream; results are identical under every policy.
+ *   MBGLU_POLICY_SERIAL    plain stream-ordered launches.
+ *   MBGLU_POLICY_PDL       programmatic dependent launch: the kernels may be
+ *                          scheduled while the preceding kernel drains, but
+ *                          read and write nothing in global memory before it
+ *                          has completed.
+ *   MBGLU_POLICY_PREFETCH  as PDL, and the first weight stages (gate_w and
+ *                          up_w only) are requested before that wait, so a
+ *                          decode step's back-to-back calls overlap one call's
+ *                          tail with the next call's ramp.  Contract: the
+ *                          kernel immediately preceding a call on its stream
+ *                          must not write gate_w / up_w after releasing its
+ *                          dependents early (kernels that do not use
+ *                          programmatic dependent launch never do: they
+ *                          release at completion).  Use SERIAL or PDL around
+ *                          custom early-releasing kernels that update weights.
+ * Returns MBGLU_ERR_MODE for an unknown value.
+ */
+#define MBGLU_POLICY_SERIAL   0
+#define MBGLU_POLICY_PDL      1
+#define MBGLU_POLICY_PREFETCH 2
+mbglu_status mbglu_set_launch_policy(int policy);
+int mbglu_get_launch_policy(void);
 
 /* Human-readable name of a status code (static storage). */
 const char *mbglu_status_string(mbglu_status s);

@@ -21,8 +21,10 @@ _MODES = {"fused": MODE_FUSED, "hf": MODE_HF, MODE_FUSED: MODE_FUSED, MODE_HF: M
 MAX_M = 16
 
 # Every symbol include/mbglu.h declares.
-EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "mbglu_status_string", "mbglu_abi_version",
-           "mbglu_last_cuda_error", "mbglu_last_variant", "mbglu_read_device_error")
+EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "mbglu_set_launch_policy", "mbglu_get_launch_policy",
+           "mbglu_status_string", "mbglu_abi_version", "mbglu_last_cuda_error", "mbglu_last_variant",
+           "mbglu_read_device_error")
+POLICY_SERIAL, POLICY_PDL, POLICY_PREFETCH = 0, 1, 2
 
 _lib = None
 
@@ -49,6 +51,9 @@ def _bind(l):
     l.mbglu_last_variant.restype = i32
     l.mbglu_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     l.mbglu_read_device_error.restype = i32
+    l.mbglu_set_launch_policy.argtypes = [i32]
+    l.mbglu_set_launch_policy.restype = i32
+    l.mbglu_get_launch_policy.restype = i32
     return l
 
 
@@ -160,3 +165,15 @@ def read_device_error() -> int:
     if st != 0:
         raise MbgluError(st, "mbglu_read_device_error")
     return w.value
+
+
+def set_launch_policy(policy: int) -> None:
+    """0 serial, 1 programmatic dependent launch, 2 PDL + weight prefetch
+    before the dependency wait (default; see include/mbglu.h for the contract)."""
+    st = lib().mbglu_set_launch_policy(int(policy))
+    if st != 0:
+        raise MbgluError(st, "mbglu_set_launch_policy")
+
+
+def get_launch_policy() -> int:
+    return lib().mbglu_get_launch_policy()

@@ -14,11 +14,14 @@
 //   * one persistent CTA per SM, a balanced contiguous range of rows each;
 //   * every warp owns a private ring of shared-memory stages that its lane 0
 //     fills with bulk asynchronous copies (cp.async.bulk, mbarrier completion,
-//     L2 evict-first hint): one stage = one K-segment of one row of BOTH
-//     matrices, so ~160 KB of weights are in flight per SM;
+//     L2 evict-first hint): one stage = a group of consecutive rows of BOTH
+//     matrices, >= 8 KB per copy, ~160 KB of weights in flight per SM;
+//   * with programmatic dependent launch the first stages are requested
+//     before waiting on the preceding kernel, so consecutive calls overlap
+//     one call's tail with the next call's ramp;
 //   * h (or the normed h) sits in shared memory for the whole kernel;
-//   * lanes take 16-byte chunks, fp32 FMAs, a warp butterfly reduction, and
-//     the epilogue of the requested rounding mode;
+//   * lanes take 16-byte chunks, packed fp32x2 FMAs, a warp butterfly
+//     reduction, and the epilogue of the requested rounding mode;
 //   * every wait is bounded (globaltimer); a timeout records an error word and
 //     returns instead of hanging or trapping.
 #pragma once
@@ -31,7 +34,8 @@ namespace mbglu {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 constexpr int kErrTimeout = 8;                    // == MBGLU_ERR_TIMEOUT
-constexpr int kMaxWarps = 16;
+constexpr int kMaxWarps = 16;        // any kernel's block, for the norm reduction
+constexpr int kMaxStreamWarps = 8;   // the streaming kernel's block
 constexpr int kMaxM = 16;
 
 // Error word of the device (read and cleared by mbglu_read_device_error).
@@ -53,6 +57,7 @@ struct GluParams {
     int KS, nseg, stages;    // streaming kernel: segment length, #segments, ring depth
     uint32_t off_h, off_ring;
     int vec_in;              // 1: h (or s, norm_w) may be read with 16-byte loads
+    int prefetch;            // 1: first weight stages requested before the dependency wait
 };
 
 // ---------------------------------------------------------------------------
@@ -218,20 +223,30 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
 // the streaming kernel
 // ---------------------------------------------------------------------------
 //
-// Shared memory (dynamic):  [0, off_h)        mbarriers, [warp][stage]
-//                           [off_h, off_ring) h_s[MB][K] bf16
-//                           [off_ring, ...)   ring[warp][stage][2][KS] bf16
-// Unit u of a warp = (row i of the warp, K-segment seg): rows r0 + warp +
-// i*NW of this CTA's range [r0, r1), segments of KS elements (the last one
-// may be shorter, always a multiple of 8).  Stage of unit u = u % S, its
-// barrier phase = (u / S) & 1.
+// Work: this CTA owns rows [r0, r1) (a balanced contiguous share of N).  They
+// are cut into groups of R consecutive rows; warp w takes groups w, w+NW, ...
+// A unit = (group, K-segment of KS elements).  Stage of unit u = u % S, its
+// barrier phase = (u / S) & 1.  A stage holds the group's rows of BOTH
+// matrices: [R][KS] of W_gate then [R][KS] of W_up.  When the rows are
+// contiguous in memory (ld == K == KS) the group's rows arrive in one bulk
+// copy per matrix (R*K*2 bytes, >= 8 KB where possible); otherwise one copy
+// per row and matrix.
 //
-// NORM: the launch follows the residual-add kernel with programmatic
-// dependent launch; the weight prefetch (independent of the add) is issued
-// before griddepcontrol.wait, the residual rows are read after it.  Without
-// NORM nothing global is touched before the wait, so any predecessor is safe.
-template <int MB, bool NORM>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1) glu_stream_kernel(const GluParams p)
+// Shared memory (dynamic):  [0, off_h)        mbarriers [warp][stage]
+//                           [off_h, off_ring) h_s[MB][K] bf16
+//                           [off_ring, ...)   ring[warp][stage][2][R][KS] bf16
+//
+// Ordering with the preceding grid (programmatic dependent launch):
+//   prefetch == 1: the first S stages of weights are requested BEFORE
+//     griddepcontrol.wait -- weights are never written by this op, and the
+//     launch policy that selects this promises the preceding kernel does
+//     not write them either; h / the residual rows and `out` are touched
+//     only after the wait.
+//   prefetch == 0: nothing global is read before the wait.
+// Dot products: exact bf16 x bf16 products, fp32 FMAs on (even, odd) element
+// pairs (packed fp32x2 FMA), pairs added, then a warp butterfly.
+template <int MB, int R, bool NORM>
+__global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(const GluParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[kMaxWarps][MB];
@@ -239,15 +254,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) glu_stream_kernel(const Glu
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, NW = blockDim.x >> 5;
     const int S = p.stages, KS = p.KS, K = p.K, nseg = p.nseg;
+    const int64_t stage_elems = static_cast<int64_t>(2) * R * KS;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * S;
     uint16_t *h_s = reinterpret_cast<uint16_t *>(smem + p.off_h);
-    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + p.off_ring) + static_cast<int64_t>(warp) * S * 2 * KS;
+    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + p.off_ring) + static_cast<int64_t>(warp) * S * stage_elems;
 
     const int r0 = static_cast<int>((static_cast<int64_t>(p.N) * blockIdx.x) / gridDim.x);
     const int r1 = static_cast<int>((static_cast<int64_t>(p.N) * (blockIdx.x + 1)) / gridDim.x);
-    const int span = r1 - r0;
-    const int nrows = span > warp ? (span - warp + NW - 1) / NW : 0;
-    const int units = nrows * nseg;
+    const int ngroups = (r1 - r0 + R - 1) / R;
+    const int mygroups = ngroups > warp ? (ngroups - warp + NW - 1) / NW : 0;
+    const int units = mygroups * nseg;
+    const bool contig = (p.ld_gate == K) && (p.ld_up == K) && (KS == K);
 
     if (lane == 0)
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
@@ -258,34 +275,46 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) glu_stream_kernel(const Glu
     auto issue = [&](int u) {
         const int st = u % S;
         const int i = u / nseg, seg = u - i * nseg;
-        const int64_t row = r0 + warp + static_cast<int64_t>(i) * NW;
+        const int row0 = r0 + (warp + i * NW) * R;
+        const int nr = min(R, r1 - row0);
         const int k0 = seg * KS;
         const int len = min(KS, K - k0);
-        const uint32_t bytes = static_cast<uint32_t>(len) * 2u;
-        uint16_t *dst = ring + static_cast<int64_t>(st) * 2 * KS;
-        mbar_arrive_expect_tx(&bars[st], 2u * bytes);
-        bulk_g2s(dst, p.gate + row * p.ld_gate + k0, bytes, &bars[st], policy);
-        bulk_g2s(dst + KS, p.up + row * p.ld_up + k0, bytes, &bars[st], policy);
+        const uint32_t row_bytes = static_cast<uint32_t>(len) * 2u;
+        uint16_t *dg = ring + st * stage_elems;
+        uint16_t *du = dg + R * KS;
+        mbar_arrive_expect_tx(&bars[st], 2u * static_cast<uint32_t>(nr) * row_bytes);
+        if (contig) {
+            bulk_g2s(dg, p.gate + static_cast<int64_t>(row0) * K, static_cast<uint32_t>(nr) * row_bytes, &bars[st],
+                     policy);
+            bulk_g2s(du, p.up + static_cast<int64_t>(row0) * K, static_cast<uint32_t>(nr) * row_bytes, &bars[st],
+                     policy);
+        } else {
+            for (int r = 0; r < nr; ++r) {
+                bulk_g2s(dg + r * KS, p.gate + static_cast<int64_t>(row0 + r) * p.ld_gate + k0, row_bytes, &bars[st],
+                         policy);
+                bulk_g2s(du + r * KS, p.up + static_cast<int64_t>(row0 + r) * p.ld_up + k0, row_bytes, &bars[st],
+                         policy);
+            }
+        }
     };
 
-    if constexpr (NORM) {
-        if (lane == 0)
-            for (int u = 0; u < S && u < units; ++u) issue(u);
-        grid_dependency_wait();
-        grid_launch_dependents();
+    if (p.prefetch && lane == 0)
+        for (int u = 0; u < S && u < units; ++u) issue(u);
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (!p.prefetch && lane == 0)
+        for (int u = 0; u < S && u < units; ++u) issue(u);
+    if constexpr (NORM)
         norm_prologue<MB>(p, h_s, red, inv_s, MB);
-    } else {
-        grid_dependency_wait();
-        grid_launch_dependents();
-        if (lane == 0)
-            for (int u = 0; u < S && u < units; ++u) issue(u);
+    else
         load_h_to_smem<MB>(p, h_s);
-    }
     __syncthreads();
 
-    float ag[MB], au[MB];
+    float2 ag[R][MB], au[R][MB];
 #pragma unroll
-    for (int m = 0; m < MB; ++m) ag[m] = au[m] = 0.0f;
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < MB; ++m) ag[r][m] = au[r][m] = make_float2(0.0f, 0.0f);
 
     for (int u = 0; u < units; ++u) {
         const int st = u % S;
@@ -303,35 +332,37 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) glu_stream_kernel(const Glu
         const int i = u / nseg, seg = u - i * nseg;
         const int k0 = seg * KS;
         const int nch = min(KS, K - k0) >> 3;
-        const uint16_t *wg = ring + static_cast<int64_t>(st) * 2 * KS;
-        const uint16_t *wu = wg + KS;
+        const uint16_t *wg = ring + st * stage_elems;
+        const uint16_t *wu = wg + R * KS;
         const uint16_t *hk = h_s + k0;
 #pragma unroll 2
         for (int c = lane; c < nch; c += 32) {
-            const uint4 g4 = *reinterpret_cast<const uint4 *>(wg + c * 8);
-            const uint4 u4 = *reinterpret_cast<const uint4 *>(wu + c * 8);
-            const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
-            const uint32_t uw[4] = {u4.x, u4.y, u4.z, u4.w};
-            float gf[8], uf[8];
+            float2 gv[R][4], uv[R][4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                gf[2 * j] = bf16_lo(gw[j]);
-                gf[2 * j + 1] = bf16_hi(gw[j]);
-                uf[2 * j] = bf16_lo(uw[j]);
-                uf[2 * j + 1] = bf16_hi(uw[j]);
+            for (int r = 0; r < R; ++r) {
+                const uint4 g4 = *reinterpret_cast<const uint4 *>(wg + r * KS + c * 8);
+                const uint4 u4 = *reinterpret_cast<const uint4 *>(wu + r * KS + c * 8);
+                gv[r][0] = make_float2(bf16_lo(g4.x), bf16_hi(g4.x));
+                gv[r][1] = make_float2(bf16_lo(g4.y), bf16_hi(g4.y));
+                gv[r][2] = make_float2(bf16_lo(g4.z), bf16_hi(g4.z));
+                gv[r][3] = make_float2(bf16_lo(g4.w), bf16_hi(g4.w));
+                uv[r][0] = make_float2(bf16_lo(u4.x), bf16_hi(u4.x));
+                uv[r][1] = make_float2(bf16_lo(u4.y), bf16_hi(u4.y));
+                uv[r][2] = make_float2(bf16_lo(u4.z), bf16_hi(u4.z));
+                uv[r][3] = make_float2(bf16_lo(u4.w), bf16_hi(u4.w));
             }
 #pragma unroll
             for (int m = 0; m < MB; ++m) {
                 const uint4 h4 = *reinterpret_cast<const uint4 *>(hk + static_cast<int64_t>(m) * K + c * 8);
-                const uint32_t hw[4] = {h4.x, h4.y, h4.z, h4.w};
+                const float2 hv[4] = {make_float2(bf16_lo(h4.x), bf16_hi(h4.x)), make_float2(bf16_lo(h4.y), bf16_hi(h4.y)),
+                                      make_float2(bf16_lo(h4.z), bf16_hi(h4.z)), make_float2(bf16_lo(h4.w), bf16_hi(h4.w))};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float a = bf16_lo(hw[j]), b = bf16_hi(hw[j]);
-                    ag[m] = fmaf(a, gf[2 * j], ag[m]);
-                    au[m] = fmaf(a, uf[2 * j], au[m]);
-                    ag[m] = fmaf(b, gf[2 * j + 1], ag[m]);
-                    au[m] = fmaf(b, uf[2 * j + 1], au[m]);
-                }
+                for (int r = 0; r < R; ++r)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        ag[r][m] = __ffma2_rn(hv[j], gv[r][j], ag[r][m]);
+                        au[r][m] = __ffma2_rn(hv[j], uv[r][j], au[r][m]);
+                    }
             }
         }
         __syncwarp();
@@ -340,16 +371,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) glu_stream_kernel(const Glu
             issue(u + S);
         }
         if (seg == nseg - 1) {
-            const int64_t row = r0 + warp + static_cast<int64_t>(i) * NW;
+            const int row0 = r0 + (warp + i * NW) * R;
             float gsel = 0.0f, usel = 0.0f;
 #pragma unroll
-            for (int m = 0; m < MB; ++m) {
-                const float g = warp_allsum(ag[m]);
-                const float v = warp_allsum(au[m]);
-                if (lane == m) { gsel = g; usel = v; }
-                ag[m] = au[m] = 0.0f;
-            }
-            if (lane < p.M) p.out[lane * p.ldo + row] = glu_epilogue(gsel, usel, p.mode);
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int m = 0; m < MB; ++m) {
+                    const float g = warp_allsum(ag[r][m].x + ag[r][m].y);
+                    const float v = warp_allsum(au[r][m].x + au[r][m].y);
+                    if (lane == r * MB + m) { gsel = g; usel = v; }
+                    ag[r][m] = au[r][m] = make_float2(0.0f, 0.0f);
+                }
+            const int r = lane / MB, m = lane - (lane / MB) * MB;
+            if (lane < R * MB && m < p.M && row0 + r < r1)
+                p.out[m * p.ldo + row0 + r] = glu_epilogue(gsel, usel, p.mode);
         }
     }
 }
@@ -405,13 +440,15 @@ __global__ void __launch_bounds__(256) glu_generic_kernel(const GluParams p)
 // ---------------------------------------------------------------------------
 
 // s = bf16(x + residual), written back into residual (one rounding: the fp32
-// sum of two bf16 values rounds to the same bf16 as the exact sum).  Starts
-// the dependent GEMV launch at once: that grid only prefetches weights until
-// this grid has completed.
+// sum of two bf16 values rounds to the same bf16 as the exact sum).  Releases
+// the dependent GEMV launch at once (that grid touches nothing but weights
+// until this grid has completed), then waits for its own predecessor before
+// reading x and residual.
 __global__ void __launch_bounds__(256) residual_add_kernel(const uint16_t *x, uint16_t *res, int64_t count,
                                                            int vec)
 {
     grid_launch_dependents();
+    grid_dependency_wait();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (vec) {

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
@@ -39,13 +40,16 @@ struct DeviceInfo {
 std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 
+// Overrides for tuning sweeps only; every default is chosen by plan_stream.
 struct Tuning {
-    int warps = 8;            // warps per CTA of the streaming kernel
+    int warps = 0;            // warps per CTA of the streaming kernel (0: automatic)
+    int rows = 0;             // rows per stage R in {1,2,4} (0: automatic)
     int ks = 0;               // K-segment length (0: automatic)
     int stages = 0;           // ring depth cap (0: as many as fit, <= 8)
     int smem_kb = 0;          // shared-memory budget cap in KiB (0: device limit)
-    int pdl = 1;              // programmatic dependent launch
 };
+
+std::atomic<int> g_policy{MBGLU_POLICY_PREFETCH};
 
 int env_int(const char *name, int dflt)
 {
@@ -57,11 +61,12 @@ const Tuning &tuning()
 {
     static const Tuning t = [] {
         Tuning x;
-        x.warps = std::min(16, std::max(1, env_int("MBGLU_WARPS", 8)));
+        x.warps = std::min(mbglu::kMaxStreamWarps, std::max(0, env_int("MBGLU_WARPS", 0)));
+        x.rows = env_int("MBGLU_ROWS", 0);
+        if (x.rows != 1 && x.rows != 2 && x.rows != 4) x.rows = 0;
         x.ks = std::max(0, env_int("MBGLU_KS", 0)) & ~7;
         x.stages = std::min(kMaxStages, std::max(0, env_int("MBGLU_STAGES", 0)));
         x.smem_kb = std::max(0, env_int("MBGLU_SMEM_KB", 0));
-        x.pdl = env_int("MBGLU_PDL", 1) != 0;
         return x;
     }();
     return t;
@@ -73,14 +78,29 @@ mbglu_status cuda_fail(cudaError_t e)
     return MBGLU_ERR_CUDA;
 }
 
-template <int MB, bool NORM>
+template <int MB, int R, bool NORM>
 cudaError_t allow_smem(int optin)
 {
     cudaFuncAttributes a{};
-    cudaError_t e = cudaFuncGetAttributes(&a, mbglu::glu_stream_kernel<MB, NORM>);
+    cudaError_t e = cudaFuncGetAttributes(&a, mbglu::glu_stream_kernel<MB, R, NORM>);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(mbglu::glu_stream_kernel<MB, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(mbglu::glu_stream_kernel<MB, R, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 optin - static_cast<int>(a.sharedSizeBytes));
+}
+
+// (MB, R) pairs instantiated: R * MB <= 16 keeps the accumulators in registers.
+#define MBGLU_FOR_EACH_TILE(X) \
+    X(1, 1) X(1, 2) X(1, 4) X(2, 1) X(2, 2) X(2, 4) X(4, 1) X(4, 2) X(4, 4) X(8, 1) X(8, 2) X(16, 1)
+
+cudaError_t allow_all_stream_kernels(int optin)
+{
+    cudaError_t e = cudaSuccess;
+#define MBGLU_ALLOW(TMB, TR)                                                      \
+    if (e == cudaSuccess) e = allow_smem<TMB, TR, false>(optin);                  \
+    if (e == cudaSuccess) e = allow_smem<TMB, TR, true>(optin);
+    MBGLU_FOR_EACH_TILE(MBGLU_ALLOW)
+#undef MBGLU_ALLOW
+    return e;
 }
 
 cudaError_t allow_smem_generic(int optin)
@@ -106,13 +126,7 @@ mbglu_status device_info(const DeviceInfo **out)
         if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
             cudaSuccess)
             return cuda_fail(e);
-        const cudaError_t errs[] = {
-            allow_smem<1, false>(d.smem_optin), allow_smem<2, false>(d.smem_optin),
-            allow_smem<4, false>(d.smem_optin), allow_smem<8, false>(d.smem_optin),
-            allow_smem<16, false>(d.smem_optin), allow_smem<1, true>(d.smem_optin),
-            allow_smem<2, true>(d.smem_optin), allow_smem<4, true>(d.smem_optin),
-            allow_smem<8, true>(d.smem_optin), allow_smem<16, true>(d.smem_optin),
-            allow_smem_generic(d.smem_optin)};
+        const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_generic(d.smem_optin)};
         for (cudaError_t x : errs)
             if (x != cudaSuccess) return cuda_fail(x);
         d.ready = true;
@@ -139,41 +153,56 @@ int64_t matrix_bytes(int rows, int cols, int64_t ld)
 
 int batch_tile(int M) { return M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16; }
 
-// K-segment: the whole row up to 2048 elements; otherwise a multiple of 256
-// in [1024, 2048] that divides K, else 2048 (the last segment is shorter).
-int default_ks(int K)
+// Rows per stage: whole rows of ~8 KB or more per bulk copy when the matrix
+// rows are contiguous, bounded by R * MB <= 16 accumulators per kind.
+int default_rows(int MB, int K, bool contiguous)
 {
-    if (K <= 2048) return K;
-    for (int ks = 2048; ks >= 1024; ks -= 256)
-        if (K % ks == 0) return ks;
-    return 2048;
+    const int rmax = MB >= 16 ? 1 : MB >= 8 ? 2 : 4;
+    if (!contiguous) return 1;
+    int r = 1;
+    while (r < rmax && r * K * 2 < 8192) r *= 2;
+    return r;
 }
 
 struct Plan {
-    int MB = 1, warps = 8, KS = 0, nseg = 0, stages = 0, grid = 0;
+    int MB = 1, R = 1, warps = 4, KS = 0, nseg = 0, stages = 0, grid = 0;
     uint32_t off_h = 0, off_ring = 0, smem = 0;
 };
 
-// Streaming-kernel plan; false if h plus a two-stage ring does not fit.
-bool plan_stream(const DeviceInfo &d, int M, int N, int K, Plan &pl)
+// Streaming-kernel plan: whole rows per stage (K-segments only if a row pair
+// does not fit), one CTA per SM, as many warps (<= 4) and stages (<= 8) as the
+// shared memory left after h holds, preferring >= 2 stages per warp.  False if
+// h plus a two-stage ring does not fit at all.
+bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, Plan &pl)
 {
     const Tuning &t = tuning();
     pl.MB = batch_tile(M);
-    pl.warps = t.warps;
     const int static_reserve = 2048;  // the kernel's static shared arrays
     int budget = d.smem_optin - static_reserve;
     if (t.smem_kb > 0) budget = std::min(budget, t.smem_kb * 1024 - static_reserve);
     const uint32_t hbytes = (static_cast<uint32_t>(pl.MB) * static_cast<uint32_t>(K) * 2u + 127u) & ~127u;
-    int ks = t.ks > 0 ? std::min(t.ks, ((K + 7) / 8) * 8) : default_ks(K);
-    ks = std::max(8, ks & ~7);
+    const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes;
+    if (room <= 0) return false;
+    int ks = t.ks > 0 ? std::min(t.ks, ((K + 7) / 8) * 8) : ((K + 7) / 8) * 8;
+    pl.R = t.rows > 0 ? t.rows : default_rows(pl.MB, K, contiguous);
+    if (pl.R * pl.MB > 16) pl.R = pl.MB >= 16 ? 1 : 16 / pl.MB;
     for (;;) {
-        const int64_t per_stage = static_cast<int64_t>(pl.warps) * 4 * ks;
-        int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes;
-        int s = room > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, room / per_stage)) : 0;
-        if (t.stages > 0) s = std::min(s, t.stages);
-        if (s >= 2) {
+        const int64_t stage = static_cast<int64_t>(pl.R) * 4 * ks;
+        int warps = t.warps > 0 ? t.warps : 4;
+        int s = 0;
+        for (; warps >= 1; --warps) {
+            s = static_cast<int>(std::min<int64_t>(kMaxStages, room / (stage * warps)));
+            if (t.stages > 0) s = std::min(s, t.stages);
+            if (s >= 2 || t.warps > 0) break;
+        }
+        if (s >= 2 && warps >= 1) {
+            pl.warps = warps;
             pl.stages = s;
             break;
+        }
+        if (pl.R > 1) {
+            pl.R /= 2;
+            continue;
         }
         if (ks <= 256) return false;
         ks = std::max(256, (ks / 2) & ~7);
@@ -182,7 +211,7 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, Plan &pl)
     pl.nseg = (K + ks - 1) / ks;
     pl.off_h = kBarRegion;
     pl.off_ring = kBarRegion + hbytes;
-    pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 4u * static_cast<uint32_t>(ks);
+    pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 4u * pl.R * static_cast<uint32_t>(ks);
     pl.grid = std::max(1, std::min(d.sm_count, N));
     return true;
 }
@@ -209,13 +238,12 @@ template <bool NORM>
 mbglu_status launch_stream(const Plan &pl, const GluParams &p, cudaStream_t stream, bool pdl)
 {
     const dim3 grid(pl.grid), block(pl.warps * 32);
-    switch (pl.MB) {
-    case 1: return launch(mbglu::glu_stream_kernel<1, NORM>, grid, block, pl.smem, stream, pdl, p);
-    case 2: return launch(mbglu::glu_stream_kernel<2, NORM>, grid, block, pl.smem, stream, pdl, p);
-    case 4: return launch(mbglu::glu_stream_kernel<4, NORM>, grid, block, pl.smem, stream, pdl, p);
-    case 8: return launch(mbglu::glu_stream_kernel<8, NORM>, grid, block, pl.smem, stream, pdl, p);
-    default: return launch(mbglu::glu_stream_kernel<16, NORM>, grid, block, pl.smem, stream, pdl, p);
-    }
+#define MBGLU_CASE(TMB, TR)                                                                                   \
+    if (pl.MB == TMB && pl.R == TR)                                                                               \
+        return launch(mbglu::glu_stream_kernel<TMB, TR, NORM>, grid, block, pl.smem, stream, pdl, p);
+    MBGLU_FOR_EACH_TILE(MBGLU_CASE)
+#undef MBGLU_CASE
+    return MBGLU_ERR_SHAPE;  // unreachable: plan_stream only produces listed tiles
 }
 
 int generic_grid(const DeviceInfo &d, int N) { return std::max(1, std::min(d.sm_count * 4, (N + 7) / 8)); }
@@ -235,6 +263,16 @@ GluParams base_params(int M, int N, int K, int mode)
 extern "C" {
 
 int mbglu_abi_version(void) { return MBGLU_ABI_VERSION; }
+
+mbglu_status mbglu_set_launch_policy(int policy)
+{
+    if (policy != MBGLU_POLICY_SERIAL && policy != MBGLU_POLICY_PDL && policy != MBGLU_POLICY_PREFETCH)
+        return MBGLU_ERR_MODE;
+    g_policy.store(policy, std::memory_order_relaxed);
+    return MBGLU_OK;
+}
+
+int mbglu_get_launch_policy(void) { return g_policy.load(std::memory_order_relaxed); }
 int mbglu_last_cuda_error(void) { return t_last_cuda_error; }
 int mbglu_last_variant(void) { return t_last_variant; }
 
@@ -274,9 +312,11 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
     const DeviceInfo *d = nullptr;
     mbglu_status st = device_info(&d);
     if (st != MBGLU_OK) return st;
-    const bool pdl = tuning().pdl;
+    const int policy = g_policy.load(std::memory_order_relaxed);
+    const bool pdl = policy != MBGLU_POLICY_SERIAL;
 
     GluParams p = base_params(M, N, K, static_cast<int>(mode));
+    p.prefetch = policy == MBGLU_POLICY_PREFETCH;
     p.out = out;
     p.ldo = ldo;
     if (K == 0) {
@@ -305,7 +345,7 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
 
     Plan pl;
     const bool fast = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && (ld_gate % 8 == 0) &&
-                      (ld_up % 8 == 0) && plan_stream(*d, M, N, K, pl);
+                      (ld_up % 8 == 0) && plan_stream(*d, M, N, K, ld_gate == K && ld_up == K, pl);
     if (fast) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;
@@ -347,18 +387,27 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mb
     const DeviceInfo *d = nullptr;
     mbglu_status st = device_info(&d);
     if (st != MBGLU_OK) return st;
-    const bool pdl = tuning().pdl;
+    const int policy = g_policy.load(std::memory_order_relaxed);
+    const bool pdl = policy != MBGLU_POLICY_SERIAL;
 
-    // 1) residual <- bf16(x + residual); launched normally (full ordering after
-    //    whatever precedes it on the stream).
+    // 1) residual <- bf16(x + residual); it waits for its predecessor before
+    //    reading and releases the GEMV launch at once.
     {
         const int64_t count = static_cast<int64_t>(M) * K;
         const int vec = aligned(x, 16) && aligned(residual, 16) && (count % 8 == 0);
         const int64_t work = vec ? count / 8 : count;
         const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(d->sm_count, (work + 255) / 256)));
-        mbglu::residual_add_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const uint16_t *>(x),
-                                                              reinterpret_cast<uint16_t *>(residual), count, vec);
-        const cudaError_t e = cudaPeekAtLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = pdl ? 1 : 0;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, mbglu::residual_add_kernel, reinterpret_cast<const uint16_t *>(x),
+                                                 reinterpret_cast<uint16_t *>(residual), count, vec);
         if (e != cudaSuccess) return cuda_fail(e);
     }
     if (N == 0) {
@@ -378,10 +427,11 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mb
     p.norm_w = norm_w;
     p.eps = eps;
     p.vec_in = (K % 8 == 0) && aligned(residual, 16) && aligned(norm_w, 16);
+    p.prefetch = policy == MBGLU_POLICY_PREFETCH;
 
     Plan pl;
     const bool fast = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && p.vec_in &&
-                      plan_stream(*d, M, N, K, pl);
+                      plan_stream(*d, M, N, K, true, pl);
     if (fast) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;

@@ -95,3 +95,18 @@ def test_binding_rejects_cpu_tensors():
         mb.glu_gemv(h, w, w)
     with pytest.raises(TypeError):
         mb.glu_gemv(h.float(), w, w)
+
+
+def test_launch_policy_roundtrip_and_validation():
+    lib = mb.lib()
+    old = lib.mbglu_get_launch_policy()
+    assert old == mb.POLICY_PREFETCH          # the default
+    try:
+        for p in (mb.POLICY_SERIAL, mb.POLICY_PDL, mb.POLICY_PREFETCH):
+            assert lib.mbglu_set_launch_policy(p) == OK
+            assert lib.mbglu_get_launch_policy() == p
+        assert lib.mbglu_set_launch_policy(3) == MODE
+        assert lib.mbglu_set_launch_policy(-1) == MODE
+        assert lib.mbglu_get_launch_policy() == mb.POLICY_PREFETCH
+    finally:
+        lib.mbglu_set_launch_policy(old)

@@ -209,6 +209,37 @@ def test_deterministic_and_row_permutation_bitwise():
     assert torch.equal(a[:, perm].view(torch.int16), c.view(torch.int16))
 
 
+@pytest.mark.parametrize("policy", [0, 1, 2])
+def test_launch_policies_give_identical_results(policy):
+    """Serial, programmatic dependent launch and weight prefetch before the
+    dependency wait: bitwise the same outputs, also back to back in a graph."""
+    M, N, K = 4, 3001, 2560
+    h = gi.normal_bf16((M, K), 1.0, 11, "pol-h").to(DEV)
+    gs = [gi.normal_bf16((N, K), K ** -0.5, 11, "pol-g", i).to(DEV) for i in range(3)]
+    us = [gi.normal_bf16((N, K), K ** -0.5, 11, "pol-u", i).to(DEV) for i in range(3)]
+    x = gi.normal_bf16((M, K), 1.0, 11, "pol-x").to(DEV)
+    r0 = gi.normal_bf16((M, K), 1.0, 11, "pol-r").to(DEV)
+    w = gi.normal_bf16((K,), 0.1, 11, "pol-w").to(DEV)
+
+    def run():
+        outs = [mb.glu_gemv(h, gs[i], us[i], mode="hf") for i in range(3)]
+        r = r0.clone()
+        outs += [mb.add_rmsnorm_glu(x, r, w, 1e-6, gs[i], us[i], mode="fused") for i in range(3)]
+        torch.cuda.synchronize()
+        return [o.view(torch.int16).cpu() for o in outs] + [r.view(torch.int16).cpu()]
+
+    old = mb.get_launch_policy()
+    try:
+        mb.set_launch_policy(0)
+        ref = run()
+        mb.set_launch_policy(policy)
+        got = run()
+    finally:
+        mb.set_launch_policy(old)
+    for a, b in zip(ref, got):
+        assert torch.equal(a, b)
+
+
 def test_swap_gate_and_up_matches_oracle_swap():
     M, N, K = 2, 777, 1024
     h = gi.normal_bf16((M, K), 1.0, 7, "sw-h")
