@@ -390,6 +390,137 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
 }
 
 // ---------------------------------------------------------------------------
+// the single-row (M = 1) streaming kernel
+// ---------------------------------------------------------------------------
+//
+// Batch-1 decode, the headline case.  Differences from glu_stream_kernel:
+//   * a unit is ONE row of ONE matrix (gate row, then up row), K*2 bytes in one
+//     bulk copy, so a stage is released as soon as that matrix row is used and
+//     the per-warp ring holds up to 8 such rows (~200 KB per SM);
+//   * each lane keeps its slice of h in registers (chunks lane, lane+32, ...,
+//     K <= 4096), loaded by the warp itself right after the dependency wait:
+//     no CTA-wide barrier stands between the wait and the first FMA.
+// Rows of this CTA [r0, r1) go to warps round-robin (row r0 + warp + i*NW);
+// unit u of a warp = row i = u / 2, matrix u % 2.  Stage = u % S, phase =
+// (u / S) & 1.  Ordering with the preceding grid as in glu_stream_kernel.
+constexpr int kM1MaxChunksPerLane = 16;   // K <= 32 * 16 * 8 = 4096
+
+template <bool NORM>
+__global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_m1_kernel(const GluParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[kMaxWarps][1];
+    __shared__ float inv_s[1];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, NW = blockDim.x >> 5;
+    const int S = p.stages, K = p.K;
+    const int KP = p.KS;                      // stage stride in elements (K rounded up to 64)
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * S;
+    uint16_t *h_s = reinterpret_cast<uint16_t *>(smem + p.off_h);
+    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + p.off_ring) + static_cast<int64_t>(warp) * S * KP;
+
+    const int r0 = static_cast<int>((static_cast<int64_t>(p.N) * blockIdx.x) / gridDim.x);
+    const int r1 = static_cast<int>((static_cast<int64_t>(p.N) * (blockIdx.x + 1)) / gridDim.x);
+    const int span = r1 - r0;
+    const int nrows = span > warp ? (span - warp + NW - 1) / NW : 0;
+    const int units = 2 * nrows;
+    const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
+
+    if (lane == 0)
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+    __syncthreads();
+
+    const uint64_t policy = l2_policy_evict_first();
+    auto issue = [&](int u) {
+        const int st = u % S;
+        const int64_t row = r0 + warp + static_cast<int64_t>(u >> 1) * NW;
+        const uint16_t *src = (u & 1) ? p.up + row * p.ld_up : p.gate + row * p.ld_gate;
+        mbar_arrive_expect_tx(&bars[st], row_bytes);
+        bulk_g2s(ring + static_cast<int64_t>(st) * KP, src, row_bytes, &bars[st], policy);
+    };
+
+    if (p.prefetch && lane == 0)
+        for (int u = 0; u < S && u < units; ++u) issue(u);
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (!p.prefetch && lane == 0)
+        for (int u = 0; u < S && u < units; ++u) issue(u);
+
+    const int nch = K >> 3;
+    uint4 hreg[kM1MaxChunksPerLane];
+    if constexpr (NORM) {
+        norm_prologue<1>(p, h_s, red, inv_s, 1);
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kM1MaxChunksPerLane; ++j) {
+            const int c = lane + 32 * j;
+            hreg[j] = c < nch ? *reinterpret_cast<const uint4 *>(h_s + c * 8) : make_uint4(0, 0, 0, 0);
+        }
+    } else {
+        if (p.vec_in) {
+#pragma unroll
+            for (int j = 0; j < kM1MaxChunksPerLane; ++j) {
+                const int c = lane + 32 * j;
+                hreg[j] = c < nch ? *reinterpret_cast<const uint4 *>(p.h + c * 8) : make_uint4(0, 0, 0, 0);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < kM1MaxChunksPerLane; ++j) {
+                const int c = lane + 32 * j;
+                uint32_t w[4] = {0, 0, 0, 0};
+                if (c < nch)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        w[q] = static_cast<uint32_t>(p.h[c * 8 + 2 * q]) |
+                               (static_cast<uint32_t>(p.h[c * 8 + 2 * q + 1]) << 16);
+                hreg[j] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+
+    float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+    for (int u = 0; u < units; ++u) {
+        const int st = u % S;
+        const bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) {
+                atomicExch(&g_device_error, kErrTimeout);
+                for (int v = u; v < u + S && v < units; ++v)
+                    mbar_wait_bounded(&bars[v % S], static_cast<uint32_t>((v / S) & 1), kWaitLimitNs);
+            }
+            __syncwarp();
+            return;
+        }
+        const uint16_t *w = ring + static_cast<int64_t>(st) * KP;
+        float2 a = make_float2(0.0f, 0.0f), b = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int j = 0; j < kM1MaxChunksPerLane; ++j) {
+            const int c = lane + 32 * j;
+            if (c < nch) {
+                const uint4 w4 = *reinterpret_cast<const uint4 *>(w + c * 8);
+                const uint4 h4 = hreg[j];
+                a = __ffma2_rn(make_float2(bf16_lo(h4.x), bf16_hi(h4.x)), make_float2(bf16_lo(w4.x), bf16_hi(w4.x)), a);
+                b = __ffma2_rn(make_float2(bf16_lo(h4.y), bf16_hi(h4.y)), make_float2(bf16_lo(w4.y), bf16_hi(w4.y)), b);
+                a = __ffma2_rn(make_float2(bf16_lo(h4.z), bf16_hi(h4.z)), make_float2(bf16_lo(w4.z), bf16_hi(w4.z)), a);
+                b = __ffma2_rn(make_float2(bf16_lo(h4.w), bf16_hi(h4.w)), make_float2(bf16_lo(w4.w), bf16_hi(w4.w)), b);
+            }
+        }
+        acc[u & 1] = make_float2((a.x + b.x), (a.y + b.y));
+        __syncwarp();
+        if (lane == 0 && u + S < units) {
+            fence_proxy_async_smem();
+            issue(u + S);
+        }
+        if (u & 1) {
+            const float g = warp_allsum(acc[0].x + acc[0].y);
+            const float v = warp_allsum(acc[1].x + acc[1].y);
+            if (lane == 0) p.out[r0 + warp + static_cast<int64_t>(u >> 1) * NW] = glu_epilogue(g, v, p.mode);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // generic kernel: any 2-byte-aligned operands, same arithmetic rules
 // ---------------------------------------------------------------------------
 // One warp per output feature (grid-stride), lanes stride K with 2-byte loads,

@@ -24,7 +24,7 @@ using mbglu::GluParams;
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_variant = 0;
 
-enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3 };
+enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kSingleRow = 4 };
 
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kBarRegion = 1024;        // mbarriers: up to 16 warps x 8 stages x 8 B
@@ -47,6 +47,8 @@ struct Tuning {
     int ks = 0;               // K-segment length (0: automatic)
     int stages = 0;           // ring depth cap (0: as many as fit, <= 8)
     int smem_kb = 0;          // shared-memory budget cap in KiB (0: device limit)
+    int ctas_per_sm = 0;      // 1 or 2 streaming CTAs per SM (0: automatic)
+    int single_row = 1;       // use the M = 1 kernel where it applies
 };
 
 std::atomic<int> g_policy{MBGLU_POLICY_PREFETCH};
@@ -67,6 +69,8 @@ const Tuning &tuning()
         x.ks = std::max(0, env_int("MBGLU_KS", 0)) & ~7;
         x.stages = std::min(kMaxStages, std::max(0, env_int("MBGLU_STAGES", 0)));
         x.smem_kb = std::max(0, env_int("MBGLU_SMEM_KB", 0));
+        x.ctas_per_sm = std::min(2, std::max(0, env_int("MBGLU_CTAS_PER_SM", 0)));
+        x.single_row = env_int("MBGLU_SINGLE_ROW", 1) != 0;
         return x;
     }();
     return t;
@@ -103,6 +107,16 @@ cudaError_t allow_all_stream_kernels(int optin)
     return e;
 }
 
+template <bool NORM>
+cudaError_t allow_smem_m1(int optin)
+{
+    cudaFuncAttributes a{};
+    cudaError_t e = cudaFuncGetAttributes(&a, mbglu::glu_m1_kernel<NORM>);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(mbglu::glu_m1_kernel<NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin - static_cast<int>(a.sharedSizeBytes));
+}
+
 cudaError_t allow_smem_generic(int optin)
 {
     cudaFuncAttributes a{};
@@ -126,7 +140,8 @@ mbglu_status device_info(const DeviceInfo **out)
         if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
             cudaSuccess)
             return cuda_fail(e);
-        const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_generic(d.smem_optin)};
+        const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_m1<false>(d.smem_optin),
+                                    allow_smem_m1<true>(d.smem_optin), allow_smem_generic(d.smem_optin)};
         for (cudaError_t x : errs)
             if (x != cudaSuccess) return cuda_fail(x);
         d.ready = true;
@@ -165,7 +180,7 @@ int default_rows(int MB, int K, bool contiguous)
 }
 
 struct Plan {
-    int MB = 1, R = 1, warps = 4, KS = 0, nseg = 0, stages = 0, grid = 0;
+    int MB = 1, R = 1, warps = 4, KS = 0, nseg = 0, stages = 0, grid = 0, ctas_per_sm = 1;
     uint32_t off_h = 0, off_ring = 0, smem = 0;
 };
 
@@ -177,8 +192,11 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, Plan
 {
     const Tuning &t = tuning();
     pl.MB = batch_tile(M);
+    pl.ctas_per_sm = t.ctas_per_sm > 0 ? t.ctas_per_sm : 1;
     const int static_reserve = 2048;  // the kernel's static shared arrays
-    int budget = d.smem_optin - static_reserve;
+    // two co-resident CTAs share the SM's shared memory (1 KB of it is
+    // reserved per CTA by the hardware)
+    int budget = (pl.ctas_per_sm == 2 ? (d.smem_optin + 1024) / 2 - 1024 : d.smem_optin) - static_reserve;
     if (t.smem_kb > 0) budget = std::min(budget, t.smem_kb * 1024 - static_reserve);
     const uint32_t hbytes = (static_cast<uint32_t>(pl.MB) * static_cast<uint32_t>(K) * 2u + 127u) & ~127u;
     const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes;
@@ -212,7 +230,41 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, Plan
     pl.off_h = kBarRegion;
     pl.off_ring = kBarRegion + hbytes;
     pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 4u * pl.R * static_cast<uint32_t>(ks);
+    pl.grid = std::max(1, std::min(d.sm_count * pl.ctas_per_sm, N));
+    return true;
+}
+
+// Single-row (M = 1) plan: one matrix row per stage, 8 warps (fewer only if
+// two stages per warp would not fit), as many stages (<= 8) as fit.
+bool plan_single_row(const DeviceInfo &d, int N, int K, bool norm, Plan &pl)
+{
+    const Tuning &t = tuning();
+    if (!t.single_row || K > 32 * 8 * mbglu::kM1MaxChunksPerLane) return false;
+    const int static_reserve = 2048;
+    int budget = d.smem_optin - static_reserve;
+    if (t.smem_kb > 0) budget = std::min(budget, t.smem_kb * 1024 - static_reserve);
+    const uint32_t hbytes = norm ? ((static_cast<uint32_t>(K) * 2u + 127u) & ~127u) : 0u;
+    const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes;
+    const int64_t stage = static_cast<int64_t>(K) * 2;
+    int warps = t.warps > 0 ? t.warps : 8;
+    int s = 0;
+    for (; warps >= 1; --warps) {
+        s = room > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, room / (stage * warps))) : 0;
+        if (t.stages > 0) s = std::min(s, t.stages);
+        if (s >= 2 || t.warps > 0) break;
+    }
+    if (s < 2 || warps < 1) return false;
+    pl.MB = 1;
+    pl.R = 1;
+    pl.warps = warps;
+    pl.stages = s;
+    pl.KS = K;
+    pl.nseg = 1;
+    pl.off_h = kBarRegion;
+    pl.off_ring = kBarRegion + hbytes;
+    pl.smem = pl.off_ring + static_cast<uint32_t>(warps) * s * static_cast<uint32_t>(stage);
     pl.grid = std::max(1, std::min(d.sm_count, N));
+    pl.ctas_per_sm = 1;
     return true;
 }
 
@@ -344,8 +396,20 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
     p.ld_up = ld_up;
 
     Plan pl;
-    const bool fast = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && (ld_gate % 8 == 0) &&
-                      (ld_up % 8 == 0) && plan_stream(*d, M, N, K, ld_gate == K && ld_up == K, pl);
+    const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && (ld_gate % 8 == 0) &&
+                         (ld_up % 8 == 0);
+    if (bulk_ok && M == 1 && plan_single_row(*d, N, K, false, pl)) {
+        p.KS = pl.KS;
+        p.nseg = 1;
+        p.stages = pl.stages;
+        p.off_h = pl.off_h;
+        p.off_ring = pl.off_ring;
+        p.vec_in = aligned(h, 16);
+        st = launch(mbglu::glu_m1_kernel<false>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
+        if (st == MBGLU_OK) t_last_variant = kSingleRow;
+        return st;
+    }
+    const bool fast = bulk_ok && plan_stream(*d, M, N, K, ld_gate == K && ld_up == K, pl);
     if (fast) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;
@@ -430,8 +494,18 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mb
     p.prefetch = policy == MBGLU_POLICY_PREFETCH;
 
     Plan pl;
-    const bool fast = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && p.vec_in &&
-                      plan_stream(*d, M, N, K, true, pl);
+    const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && p.vec_in;
+    if (bulk_ok && M == 1 && plan_single_row(*d, N, K, true, pl)) {
+        p.KS = pl.KS;
+        p.nseg = 1;
+        p.stages = pl.stages;
+        p.off_h = pl.off_h;
+        p.off_ring = pl.off_ring;
+        st = launch(mbglu::glu_m1_kernel<true>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
+        if (st == MBGLU_OK) t_last_variant = kSingleRow;
+        return st;
+    }
+    const bool fast = bulk_ok && plan_stream(*d, M, N, K, true, pl);
     if (fast) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;

@@ -50,9 +50,14 @@ def run_gpu(h, g, u, mode, **kw):
     return gi.bits(out.cpu())
 
 
+FAST = (1, 4)   # streaming kernels: row groups (any M), single row (M = 1)
+
+
 def check(h, g, u, mode, what="", variant=None):
     got = run_gpu(h, g, u, mode)
-    if variant is not None:
+    if variant == 1:
+        assert mb.last_variant() in FAST
+    elif variant is not None:
         assert mb.last_variant() == variant
     ref, tau = oracle_glu(h, g, u, mode)
     return parity(got, ref, tau, what)
@@ -113,7 +118,7 @@ def test_strided_views_fast_and_generic():
     out = outb[:, 24:]
     mb.glu_gemv(hd, gd, ud, out=out, mode="hf")
     torch.cuda.synchronize()
-    assert mb.last_variant() == 1
+    assert mb.last_variant() in FAST
     parity(gi.bits(out.cpu()), ref, tau, "strided")
     assert torch.isnan(outb[:, :24].float()).all(), "wrote outside out"
     # an odd element offset breaks 16-byte alignment of the weights: generic kernel
@@ -123,6 +128,23 @@ def test_strided_views_fast_and_generic():
     torch.cuda.synchronize()
     assert mb.last_variant() == 2
     parity(gi.bits(o2.cpu()), ref2, tau2, "unaligned")
+
+
+@pytest.mark.parametrize("K,ld_pad,h_off,expect", [(2560, 0, 0, 4), (2560, 64, 8, 4), (4096, 8, 1, 4),
+                                                    (1024, 0, 3, 4), (5120, 0, 0, 1), (2568, 0, 0, 4)])
+def test_single_row_kernel(K, ld_pad, h_off, expect):
+    """M = 1: strided weight rows, an h that is not 16-byte aligned, K above
+    the register-resident limit (falls back to the row-group kernel)."""
+    N = 2111
+    hb = gi.normal_bf16((1, K + 8), 1.0, K, "m1-h")
+    gb = gi.normal_bf16((N, K + ld_pad), K ** -0.5, K, "m1-g")
+    ub = gi.normal_bf16((N, K + ld_pad), K ** -0.5, K, "m1-u")
+    h, g, u = hb[:, h_off:h_off + K], gb[:, :K], ub[:, :K]
+    ref, tau = oracle_glu(h.contiguous(), g.contiguous(), u.contiguous(), "hf")
+    out = mb.glu_gemv(hb.to(DEV)[:, h_off:h_off + K], gb.to(DEV)[:, :K], ub.to(DEV)[:, :K], mode="hf")
+    torch.cuda.synchronize()
+    assert mb.last_variant() == expect
+    parity(gi.bits(out.cpu()), ref, tau, f"M=1 K={K}")
 
 
 def test_guard_band_untouched():
@@ -188,7 +210,7 @@ def test_silu_exhaustive_over_bf16_gate_values_on_gpu(mode):
     h = np.zeros((1, K), dtype=np.uint16)
     h[0, 0] = 0x3F80
     got = run_gpu(gi.from_bits(h), gi.from_bits(gw), gi.from_bits(uw), mode)
-    assert mb.last_variant() == 1
+    assert mb.last_variant() in FAST
     ref = oracle.glu_gemv(h, gw, uw, mode)
     d = tol.ulp_distance(got, ref)
     assert d.max() <= 1, (g[d.argmax()], got[0, d.argmax()], ref[0, d.argmax()])
@@ -301,7 +323,9 @@ def check_norm(x, r, w, g, u, mode, eps=1e-6, what="", variant=None):
     rd = r.to(DEV)
     out = mb.add_rmsnorm_glu(x.to(DEV), rd, w.to(DEV), eps, g.to(DEV), u.to(DEV), mode=mode)
     torch.cuda.synchronize()
-    if variant is not None:
+    if variant == 1:
+        assert mb.last_variant() in FAST
+    elif variant is not None:
         assert mb.last_variant() == variant
     ref, res, hn = oracle.add_rmsnorm_glu(gi.bits(x), gi.bits(r), gi.bits(w), eps, gi.bits(g), gi.bits(u), mode)
     assert np.array_equal(gi.bits(rd.cpu()), res), f"residual {what}"
