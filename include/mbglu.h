@@ -175,8 +175,7 @@ int mbglu_abi_version(void);
 int mbglu_last_cuda_error(void);
 
 /* Which kernel the calling thread's last successful call launched:
- * 0 none (no-op), 1 streaming kernel (row groups, any M), 2 generic kernel,
- * 3 zero fill, 4 single-row streaming kernel (M = 1, K <= 4096). */
+ * 0 none (no-op), 1 streaming kernel, 2 generic kernel, 3 zero fill. */
 int mbglu_last_variant(void);
 
 /*

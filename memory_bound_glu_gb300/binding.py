@@ -154,7 +154,7 @@ def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf",
 
 def last_variant() -> int:
     """Kernel the calling thread's last call launched: 0 none, 1 streaming,
-    2 generic, 3 zero fill, 4 single-row streaming (M = 1)."""
+    2 generic, 3 zero fill."""
     return lib().mbglu_last_variant()
 
 

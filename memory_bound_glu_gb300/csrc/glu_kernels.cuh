@@ -223,59 +223,74 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
 // the streaming kernel
 // ---------------------------------------------------------------------------
 //
-// Work: this CTA owns rows [r0, r1) (a balanced contiguous share of N).  They
-// are cut into groups of R consecutive rows; warp w takes groups w, w+NW, ...
-// A unit = (group, K-segment of KS elements).  Stage of unit u = u % S, its
-// barrier phase = (u / S) & 1.  A stage holds the group's rows of BOTH
-// matrices: [R][KS] of W_gate then [R][KS] of W_up.  When the rows are
-// contiguous in memory (ld == K == KS) the group's rows arrive in one bulk
-// copy per matrix (R*K*2 bytes, >= 8 KB where possible); otherwise one copy
-// per row and matrix.
+// Work: this CTA owns rows [r0, r1) (a balanced contiguous share of N), cut
+// into groups of R consecutive rows.  Warps claim groups from a shared-memory
+// counter whenever they have a free stage, so every warp count stays
+// balanced inside the CTA.  Each warp owns a private ring of S stages: a
+// stage holds its group's rows of BOTH matrices, [R][KS] of W_gate then
+// [R][KS] of W_up, and remembers which group it holds (slot_grp, -1 = none).
+// A unit is (group, K-segment); the u-th unit a warp consumes sits in stage
+// u % S with barrier phase (u / S) & 1 -- the ring is private and consumed in
+// order, so a phase is never awaited twice.  When the rows are contiguous in
+// memory (ld == K == KS) a group arrives in one bulk copy per matrix
+// (R*K*2 bytes); otherwise one copy per row and matrix.
 //
-// Shared memory (dynamic):  [0, off_h)        mbarriers [warp][stage]
-//                           [off_h, off_ring) h_s[MB][K] bf16
+// Shared memory (dynamic):  [0, 512)          mbarriers [warp][stage]
+//                           [512, 768)        slot_grp [warp][stage]
+//                           [768, 772)        group counter
+//                           [off_h, off_ring) h_s[MB][K] bf16 (not with HREG)
 //                           [off_ring, ...)   ring[warp][stage][2][R][KS] bf16
 //
+// HREG (batch 1, K <= 4096): each lane keeps its slice of h -- chunks lane,
+// lane+32, ... -- in registers, loaded by the warp itself after the
+// dependency wait, so no CTA barrier sits between the wait and the first FMA.
+//
 // Ordering with the preceding grid (programmatic dependent launch):
-//   prefetch == 1: the first S stages of weights are requested BEFORE
+//   prefetch == 1: the first S units of weights are requested BEFORE
 //     griddepcontrol.wait -- weights are never written by this op, and the
 //     launch policy that selects this promises the preceding kernel does
 //     not write them either; h / the residual rows and `out` are touched
 //     only after the wait.
 //   prefetch == 0: nothing global is read before the wait.
 // Dot products: exact bf16 x bf16 products, fp32 FMAs on (even, odd) element
-// pairs (packed fp32x2 FMA), pairs added, then a warp butterfly.
-template <int MB, int R, bool NORM>
+// pairs (packed fp32x2 FMA), pairs added, then a warp butterfly.  Which warp
+// computes a group does not change its arithmetic: results are bitwise
+// deterministic.
+constexpr int kHregChunks = 16;           // K <= 32 lanes * 16 chunks * 8 = 4096
+constexpr uint32_t kSlotGrpOffset = 512;  // bytes
+constexpr uint32_t kCounterOffset = 768;
+
+template <int MB, int R, bool NORM, bool HREG>
 __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(const GluParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[kMaxWarps][MB];
     __shared__ float inv_s[MB];
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, NW = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.stages, KS = p.KS, K = p.K, nseg = p.nseg;
     const int64_t stage_elems = static_cast<int64_t>(2) * R * KS;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * S;
+    int *slot_grp = reinterpret_cast<int *>(smem + kSlotGrpOffset) + warp * S;
+    int *counter = reinterpret_cast<int *>(smem + kCounterOffset);
     uint16_t *h_s = reinterpret_cast<uint16_t *>(smem + p.off_h);
     uint16_t *ring = reinterpret_cast<uint16_t *>(smem + p.off_ring) + static_cast<int64_t>(warp) * S * stage_elems;
 
     const int r0 = static_cast<int>((static_cast<int64_t>(p.N) * blockIdx.x) / gridDim.x);
     const int r1 = static_cast<int>((static_cast<int64_t>(p.N) * (blockIdx.x + 1)) / gridDim.x);
     const int ngroups = (r1 - r0 + R - 1) / R;
-    const int mygroups = ngroups > warp ? (ngroups - warp + NW - 1) / NW : 0;
-    const int units = mygroups * nseg;
     const bool contig = (p.ld_gate == K) && (p.ld_up == K) && (KS == K);
 
     if (lane == 0)
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    if (threadIdx.x == 0) *counter = 0;
     fence_mbar_init();
     __syncthreads();
 
     const uint64_t policy = l2_policy_evict_first();
-    auto issue = [&](int u) {
-        const int st = u % S;
-        const int i = u / nseg, seg = u - i * nseg;
-        const int row0 = r0 + (warp + i * NW) * R;
+    // lane 0: request unit (group g, segment seg) into stage st
+    auto issue = [&](int st, int g, int seg) {
+        const int row0 = r0 + g * R;
         const int nr = min(R, r1 - row0);
         const int k0 = seg * KS;
         const int len = min(KS, K - k0);
@@ -297,18 +312,64 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
             }
         }
     };
+    // lane 0: the unit that follows (g, seg) in this warp's stream, claiming
+    // a new group after the last segment; returns the group (-1: none left)
+    // and updates seg.
+    auto next_unit = [&](int g, int &seg) -> int {
+        if (g >= 0 && seg + 1 < nseg) {
+            ++seg;
+            return g;
+        }
+        seg = 0;
+        const int ng = atomicAdd(counter, 1);
+        return ng < ngroups ? ng : -1;
+    };
+    // lane 0 state: the last unit requested
+    int last_g = -1, last_seg = nseg;
+    auto fill = [&](int st) {
+        last_g = next_unit(last_g, last_seg);
+        slot_grp[st] = last_g;
+        if (last_g >= 0) issue(st, last_g, last_seg);
+    };
 
     if (p.prefetch && lane == 0)
-        for (int u = 0; u < S && u < units; ++u) issue(u);
+        for (int st = 0; st < S; ++st) fill(st);
     grid_dependency_wait();
     grid_launch_dependents();
     if (!p.prefetch && lane == 0)
-        for (int u = 0; u < S && u < units; ++u) issue(u);
-    if constexpr (NORM)
+        for (int st = 0; st < S; ++st) fill(st);
+    __syncwarp();
+
+    uint4 hreg[HREG ? kHregChunks : 1];
+    if constexpr (NORM) {
         norm_prologue<MB>(p, h_s, red, inv_s, MB);
-    else
+        __syncthreads();
+    } else if constexpr (!HREG) {
         load_h_to_smem<MB>(p, h_s);
-    __syncthreads();
+        __syncthreads();
+    }
+    if constexpr (HREG) {
+        const uint16_t *hsrc = NORM ? h_s : p.h;
+        const bool vec = NORM || p.vec_in;
+#pragma unroll
+        for (int j = 0; j < kHregChunks; ++j) {
+            const int c = lane + 32 * j;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (c < (K >> 3)) {
+                if (vec) {
+                    v = *reinterpret_cast<const uint4 *>(hsrc + c * 8);
+                } else {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        w[q] = static_cast<uint32_t>(hsrc[c * 8 + 2 * q]) |
+                               (static_cast<uint32_t>(hsrc[c * 8 + 2 * q + 1]) << 16);
+                    v = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+            hreg[j] = v;
+        }
+    }
 
     float2 ag[R][MB], au[R][MB];
 #pragma unroll
@@ -316,206 +377,109 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
 #pragma unroll
         for (int m = 0; m < MB; ++m) ag[r][m] = au[r][m] = make_float2(0.0f, 0.0f);
 
-    for (int u = 0; u < units; ++u) {
+    int seg = nseg;   // consumer-side segment of the current group
+    for (int u = 0;; ++u) {
         const int st = u % S;
+        const int g = slot_grp[st];
+        if (g < 0) break;
+        seg = (seg + 1 < nseg) ? seg + 1 : 0;
         const bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) {
                 atomicExch(&g_device_error, kErrTimeout);
                 // let the copies this warp still has in flight land before exiting
-                for (int v = u; v < u + S && v < units; ++v)
-                    mbar_wait_bounded(&bars[v % S], static_cast<uint32_t>((v / S) & 1), kWaitLimitNs);
+                for (int v = u; v < u + S; ++v)
+                    if (slot_grp[v % S] >= 0)
+                        mbar_wait_bounded(&bars[v % S], static_cast<uint32_t>((v / S) & 1), kWaitLimitNs);
             }
             __syncwarp();
             return;
         }
-        const int i = u / nseg, seg = u - i * nseg;
         const int k0 = seg * KS;
         const int nch = min(KS, K - k0) >> 3;
         const uint16_t *wg = ring + st * stage_elems;
         const uint16_t *wu = wg + R * KS;
-        const uint16_t *hk = h_s + k0;
-#pragma unroll 2
-        for (int c = lane; c < nch; c += 32) {
-            float2 gv[R][4], uv[R][4];
+        if constexpr (HREG) {
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const uint4 g4 = *reinterpret_cast<const uint4 *>(wg + r * KS + c * 8);
-                const uint4 u4 = *reinterpret_cast<const uint4 *>(wu + r * KS + c * 8);
-                gv[r][0] = make_float2(bf16_lo(g4.x), bf16_hi(g4.x));
-                gv[r][1] = make_float2(bf16_lo(g4.y), bf16_hi(g4.y));
-                gv[r][2] = make_float2(bf16_lo(g4.z), bf16_hi(g4.z));
-                gv[r][3] = make_float2(bf16_lo(g4.w), bf16_hi(g4.w));
-                uv[r][0] = make_float2(bf16_lo(u4.x), bf16_hi(u4.x));
-                uv[r][1] = make_float2(bf16_lo(u4.y), bf16_hi(u4.y));
-                uv[r][2] = make_float2(bf16_lo(u4.z), bf16_hi(u4.z));
-                uv[r][3] = make_float2(bf16_lo(u4.w), bf16_hi(u4.w));
-            }
+            for (int j = 0; j < kHregChunks; ++j) {
+                const int c = lane + 32 * j;
+                if (c < nch) {
+                    const uint4 h4 = hreg[j];
+                    const float2 hv[4] = {make_float2(bf16_lo(h4.x), bf16_hi(h4.x)),
+                                          make_float2(bf16_lo(h4.y), bf16_hi(h4.y)),
+                                          make_float2(bf16_lo(h4.z), bf16_hi(h4.z)),
+                                          make_float2(bf16_lo(h4.w), bf16_hi(h4.w))};
 #pragma unroll
-            for (int m = 0; m < MB; ++m) {
-                const uint4 h4 = *reinterpret_cast<const uint4 *>(hk + static_cast<int64_t>(m) * K + c * 8);
-                const float2 hv[4] = {make_float2(bf16_lo(h4.x), bf16_hi(h4.x)), make_float2(bf16_lo(h4.y), bf16_hi(h4.y)),
-                                      make_float2(bf16_lo(h4.z), bf16_hi(h4.z)), make_float2(bf16_lo(h4.w), bf16_hi(h4.w))};
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        ag[r][m] = __ffma2_rn(hv[j], gv[r][j], ag[r][m]);
-                        au[r][m] = __ffma2_rn(hv[j], uv[r][j], au[r][m]);
+                    for (int r = 0; r < R; ++r) {
+                        const uint4 g4 = *reinterpret_cast<const uint4 *>(wg + r * KS + c * 8);
+                        const uint4 u4 = *reinterpret_cast<const uint4 *>(wu + r * KS + c * 8);
+                        ag[r][0] = __ffma2_rn(hv[0], make_float2(bf16_lo(g4.x), bf16_hi(g4.x)), ag[r][0]);
+                        au[r][0] = __ffma2_rn(hv[0], make_float2(bf16_lo(u4.x), bf16_hi(u4.x)), au[r][0]);
+                        ag[r][0] = __ffma2_rn(hv[1], make_float2(bf16_lo(g4.y), bf16_hi(g4.y)), ag[r][0]);
+                        au[r][0] = __ffma2_rn(hv[1], make_float2(bf16_lo(u4.y), bf16_hi(u4.y)), au[r][0]);
+                        ag[r][0] = __ffma2_rn(hv[2], make_float2(bf16_lo(g4.z), bf16_hi(g4.z)), ag[r][0]);
+                        au[r][0] = __ffma2_rn(hv[2], make_float2(bf16_lo(u4.z), bf16_hi(u4.z)), au[r][0]);
+                        ag[r][0] = __ffma2_rn(hv[3], make_float2(bf16_lo(g4.w), bf16_hi(g4.w)), ag[r][0]);
+                        au[r][0] = __ffma2_rn(hv[3], make_float2(bf16_lo(u4.w), bf16_hi(u4.w)), au[r][0]);
                     }
+                }
+            }
+        } else {
+            const uint16_t *hk = h_s + k0;
+#pragma unroll 2
+            for (int c = lane; c < nch; c += 32) {
+                float2 gv[R][4], uv[R][4];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const uint4 g4 = *reinterpret_cast<const uint4 *>(wg + r * KS + c * 8);
+                    const uint4 u4 = *reinterpret_cast<const uint4 *>(wu + r * KS + c * 8);
+                    gv[r][0] = make_float2(bf16_lo(g4.x), bf16_hi(g4.x));
+                    gv[r][1] = make_float2(bf16_lo(g4.y), bf16_hi(g4.y));
+                    gv[r][2] = make_float2(bf16_lo(g4.z), bf16_hi(g4.z));
+                    gv[r][3] = make_float2(bf16_lo(g4.w), bf16_hi(g4.w));
+                    uv[r][0] = make_float2(bf16_lo(u4.x), bf16_hi(u4.x));
+                    uv[r][1] = make_float2(bf16_lo(u4.y), bf16_hi(u4.y));
+                    uv[r][2] = make_float2(bf16_lo(u4.z), bf16_hi(u4.z));
+                    uv[r][3] = make_float2(bf16_lo(u4.w), bf16_hi(u4.w));
+                }
+#pragma unroll
+                for (int m = 0; m < MB; ++m) {
+                    const uint4 h4 = *reinterpret_cast<const uint4 *>(hk + static_cast<int64_t>(m) * K + c * 8);
+                    const float2 hv[4] = {make_float2(bf16_lo(h4.x), bf16_hi(h4.x)),
+                                          make_float2(bf16_lo(h4.y), bf16_hi(h4.y)),
+                                          make_float2(bf16_lo(h4.z), bf16_hi(h4.z)),
+                                          make_float2(bf16_lo(h4.w), bf16_hi(h4.w))};
+#pragma unroll
+                    for (int r = 0; r < R; ++r)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            ag[r][m] = __ffma2_rn(hv[j], gv[r][j], ag[r][m]);
+                            au[r][m] = __ffma2_rn(hv[j], uv[r][j], au[r][m]);
+                        }
+                }
             }
         }
         __syncwarp();
-        if (lane == 0 && u + S < units) {
+        if (lane == 0) {
             fence_proxy_async_smem();
-            issue(u + S);
+            fill(st);   // the unit S ahead of u, or -1 once the CTA's groups run out
         }
+        __syncwarp();
         if (seg == nseg - 1) {
-            const int row0 = r0 + (warp + i * NW) * R;
+            const int row0 = r0 + g * R;
             float gsel = 0.0f, usel = 0.0f;
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int m = 0; m < MB; ++m) {
-                    const float g = warp_allsum(ag[r][m].x + ag[r][m].y);
-                    const float v = warp_allsum(au[r][m].x + au[r][m].y);
-                    if (lane == r * MB + m) { gsel = g; usel = v; }
+                    const float gs = warp_allsum(ag[r][m].x + ag[r][m].y);
+                    const float us = warp_allsum(au[r][m].x + au[r][m].y);
+                    if (lane == r * MB + m) { gsel = gs; usel = us; }
                     ag[r][m] = au[r][m] = make_float2(0.0f, 0.0f);
                 }
             const int r = lane / MB, m = lane - (lane / MB) * MB;
             if (lane < R * MB && m < p.M && row0 + r < r1)
                 p.out[m * p.ldo + row0 + r] = glu_epilogue(gsel, usel, p.mode);
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// the single-row (M = 1) streaming kernel
-// ---------------------------------------------------------------------------
-//
-// Batch-1 decode, the headline case.  Differences from glu_stream_kernel:
-//   * a unit is ONE row of ONE matrix (gate row, then up row), K*2 bytes in one
-//     bulk copy, so a stage is released as soon as that matrix row is used and
-//     the per-warp ring holds up to 8 such rows (~200 KB per SM);
-//   * each lane keeps its slice of h in registers (chunks lane, lane+32, ...,
-//     K <= 4096), loaded by the warp itself right after the dependency wait:
-//     no CTA-wide barrier stands between the wait and the first FMA.
-// Rows of this CTA [r0, r1) go to warps round-robin (row r0 + warp + i*NW);
-// unit u of a warp = row i = u / 2, matrix u % 2.  Stage = u % S, phase =
-// (u / S) & 1.  Ordering with the preceding grid as in glu_stream_kernel.
-constexpr int kM1MaxChunksPerLane = 16;   // K <= 32 * 16 * 8 = 4096
-
-template <bool NORM>
-__global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_m1_kernel(const GluParams p)
-{
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[kMaxWarps][1];
-    __shared__ float inv_s[1];
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, NW = blockDim.x >> 5;
-    const int S = p.stages, K = p.K;
-    const int KP = p.KS;                      // stage stride in elements (K rounded up to 64)
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * S;
-    uint16_t *h_s = reinterpret_cast<uint16_t *>(smem + p.off_h);
-    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + p.off_ring) + static_cast<int64_t>(warp) * S * KP;
-
-    const int r0 = static_cast<int>((static_cast<int64_t>(p.N) * blockIdx.x) / gridDim.x);
-    const int r1 = static_cast<int>((static_cast<int64_t>(p.N) * (blockIdx.x + 1)) / gridDim.x);
-    const int span = r1 - r0;
-    const int nrows = span > warp ? (span - warp + NW - 1) / NW : 0;
-    const int units = 2 * nrows;
-    const uint32_t row_bytes = static_cast<uint32_t>(K) * 2u;
-
-    if (lane == 0)
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-    fence_mbar_init();
-    __syncthreads();
-
-    const uint64_t policy = l2_policy_evict_first();
-    auto issue = [&](int u) {
-        const int st = u % S;
-        const int64_t row = r0 + warp + static_cast<int64_t>(u >> 1) * NW;
-        const uint16_t *src = (u & 1) ? p.up + row * p.ld_up : p.gate + row * p.ld_gate;
-        mbar_arrive_expect_tx(&bars[st], row_bytes);
-        bulk_g2s(ring + static_cast<int64_t>(st) * KP, src, row_bytes, &bars[st], policy);
-    };
-
-    if (p.prefetch && lane == 0)
-        for (int u = 0; u < S && u < units; ++u) issue(u);
-    grid_dependency_wait();
-    grid_launch_dependents();
-    if (!p.prefetch && lane == 0)
-        for (int u = 0; u < S && u < units; ++u) issue(u);
-
-    const int nch = K >> 3;
-    uint4 hreg[kM1MaxChunksPerLane];
-    if constexpr (NORM) {
-        norm_prologue<1>(p, h_s, red, inv_s, 1);
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < kM1MaxChunksPerLane; ++j) {
-            const int c = lane + 32 * j;
-            hreg[j] = c < nch ? *reinterpret_cast<const uint4 *>(h_s + c * 8) : make_uint4(0, 0, 0, 0);
-        }
-    } else {
-        if (p.vec_in) {
-#pragma unroll
-            for (int j = 0; j < kM1MaxChunksPerLane; ++j) {
-                const int c = lane + 32 * j;
-                hreg[j] = c < nch ? *reinterpret_cast<const uint4 *>(p.h + c * 8) : make_uint4(0, 0, 0, 0);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < kM1MaxChunksPerLane; ++j) {
-                const int c = lane + 32 * j;
-                uint32_t w[4] = {0, 0, 0, 0};
-                if (c < nch)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        w[q] = static_cast<uint32_t>(p.h[c * 8 + 2 * q]) |
-                               (static_cast<uint32_t>(p.h[c * 8 + 2 * q + 1]) << 16);
-                hreg[j] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
-    }
-
-    float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-    for (int u = 0; u < units; ++u) {
-        const int st = u % S;
-        const bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs);
-        if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) {
-                atomicExch(&g_device_error, kErrTimeout);
-                for (int v = u; v < u + S && v < units; ++v)
-                    mbar_wait_bounded(&bars[v % S], static_cast<uint32_t>((v / S) & 1), kWaitLimitNs);
-            }
-            __syncwarp();
-            return;
-        }
-        const uint16_t *w = ring + static_cast<int64_t>(st) * KP;
-        float2 a = make_float2(0.0f, 0.0f), b = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int j = 0; j < kM1MaxChunksPerLane; ++j) {
-            const int c = lane + 32 * j;
-            if (c < nch) {
-                const uint4 w4 = *reinterpret_cast<const uint4 *>(w + c * 8);
-                const uint4 h4 = hreg[j];
-                a = __ffma2_rn(make_float2(bf16_lo(h4.x), bf16_hi(h4.x)), make_float2(bf16_lo(w4.x), bf16_hi(w4.x)), a);
-                b = __ffma2_rn(make_float2(bf16_lo(h4.y), bf16_hi(h4.y)), make_float2(bf16_lo(w4.y), bf16_hi(w4.y)), b);
-                a = __ffma2_rn(make_float2(bf16_lo(h4.z), bf16_hi(h4.z)), make_float2(bf16_lo(w4.z), bf16_hi(w4.z)), a);
-                b = __ffma2_rn(make_float2(bf16_lo(h4.w), bf16_hi(h4.w)), make_float2(bf16_lo(w4.w), bf16_hi(w4.w)), b);
-            }
-        }
-        acc[u & 1] = make_float2((a.x + b.x), (a.y + b.y));
-        __syncwarp();
-        if (lane == 0 && u + S < units) {
-            fence_proxy_async_smem();
-            issue(u + S);
-        }
-        if (u & 1) {
-            const float g = warp_allsum(acc[0].x + acc[0].y);
-            const float v = warp_allsum(acc[1].x + acc[1].y);
-            if (lane == 0) p.out[r0 + warp + static_cast<int64_t>(u >> 1) * NW] = glu_epilogue(g, v, p.mode);
         }
     }
 }

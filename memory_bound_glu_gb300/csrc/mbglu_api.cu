@@ -24,10 +24,14 @@ using mbglu::GluParams;
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_variant = 0;
 
-enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kSingleRow = 4 };
+enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3 };
 
 constexpr int kMaxDevices = 64;
-constexpr uint32_t kBarRegion = 1024;        // mbarriers: up to 16 warps x 8 stages x 8 B
+constexpr uint32_t kBarRegion = 1024;        // mbarriers, stage -> group table, group counter
+static_assert(mbglu::kMaxStreamWarps * 8 * 8 <= mbglu::kSlotGrpOffset, "mbarriers overflow their region");
+static_assert(mbglu::kSlotGrpOffset + mbglu::kMaxStreamWarps * 8 * 4 <= mbglu::kCounterOffset,
+              "stage table overflows its region");
+static_assert(mbglu::kCounterOffset + 4 <= kBarRegion, "counter outside the region");
 constexpr int kMaxStages = 8;
 constexpr int64_t kNormMaxMK = 81920;        // add_rmsnorm_glu: M*K*2 bytes of normed rows in smem
 
@@ -48,7 +52,7 @@ struct Tuning {
     int stages = 0;           // ring depth cap (0: as many as fit, <= 8)
     int smem_kb = 0;          // shared-memory budget cap in KiB (0: device limit)
     int ctas_per_sm = 0;      // 1 or 2 streaming CTAs per SM (0: automatic)
-    int single_row = 1;       // use the M = 1 kernel where it applies
+    int hreg = 1;             // batch 1: keep h in registers where K allows
 };
 
 std::atomic<int> g_policy{MBGLU_POLICY_PREFETCH};
@@ -70,7 +74,7 @@ const Tuning &tuning()
         x.stages = std::min(kMaxStages, std::max(0, env_int("MBGLU_STAGES", 0)));
         x.smem_kb = std::max(0, env_int("MBGLU_SMEM_KB", 0));
         x.ctas_per_sm = std::min(2, std::max(0, env_int("MBGLU_CTAS_PER_SM", 0)));
-        x.single_row = env_int("MBGLU_SINGLE_ROW", 1) != 0;
+        x.hreg = env_int("MBGLU_HREG", 1) != 0;
         return x;
     }();
     return t;
@@ -82,39 +86,32 @@ mbglu_status cuda_fail(cudaError_t e)
     return MBGLU_ERR_CUDA;
 }
 
-template <int MB, int R, bool NORM>
+template <int MB, int R, bool NORM, bool HREG>
 cudaError_t allow_smem(int optin)
 {
     cudaFuncAttributes a{};
-    cudaError_t e = cudaFuncGetAttributes(&a, mbglu::glu_stream_kernel<MB, R, NORM>);
+    cudaError_t e = cudaFuncGetAttributes(&a, mbglu::glu_stream_kernel<MB, R, NORM, HREG>);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(mbglu::glu_stream_kernel<MB, R, NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                optin - static_cast<int>(a.sharedSizeBytes));
+    return cudaFuncSetAttribute(mbglu::glu_stream_kernel<MB, R, NORM, HREG>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, optin - static_cast<int>(a.sharedSizeBytes));
 }
 
-// (MB, R) pairs instantiated: R * MB <= 16 keeps the accumulators in registers.
-#define MBGLU_FOR_EACH_TILE(X) \
-    X(1, 1) X(1, 2) X(1, 4) X(2, 1) X(2, 2) X(2, 4) X(4, 1) X(4, 2) X(4, 4) X(8, 1) X(8, 2) X(16, 1)
+// (MB, R, HREG) tiles instantiated: R * MB <= 16 keeps the accumulators in
+// registers; h lives in registers only at batch 1.
+#define MBGLU_FOR_EACH_TILE(X)                                                                          \
+    X(1, 1, false) X(1, 2, false) X(1, 4, false) X(2, 1, false) X(2, 2, false) X(2, 4, false)         \
+    X(4, 1, false) X(4, 2, false) X(4, 4, false) X(8, 1, false) X(8, 2, false) X(16, 1, false)        \
+    X(1, 1, true) X(1, 2, true) X(1, 4, true)
 
 cudaError_t allow_all_stream_kernels(int optin)
 {
     cudaError_t e = cudaSuccess;
-#define MBGLU_ALLOW(TMB, TR)                                                      \
-    if (e == cudaSuccess) e = allow_smem<TMB, TR, false>(optin);                  \
-    if (e == cudaSuccess) e = allow_smem<TMB, TR, true>(optin);
+#define MBGLU_ALLOW(TMB, TR, TH)                                                  \
+    if (e == cudaSuccess) e = allow_smem<TMB, TR, false, TH>(optin);              \
+    if (e == cudaSuccess) e = allow_smem<TMB, TR, true, TH>(optin);
     MBGLU_FOR_EACH_TILE(MBGLU_ALLOW)
 #undef MBGLU_ALLOW
     return e;
-}
-
-template <bool NORM>
-cudaError_t allow_smem_m1(int optin)
-{
-    cudaFuncAttributes a{};
-    cudaError_t e = cudaFuncGetAttributes(&a, mbglu::glu_m1_kernel<NORM>);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(mbglu::glu_m1_kernel<NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                optin - static_cast<int>(a.sharedSizeBytes));
 }
 
 cudaError_t allow_smem_generic(int optin)
@@ -140,8 +137,7 @@ mbglu_status device_info(const DeviceInfo **out)
         if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
             cudaSuccess)
             return cuda_fail(e);
-        const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_m1<false>(d.smem_optin),
-                                    allow_smem_m1<true>(d.smem_optin), allow_smem_generic(d.smem_optin)};
+        const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_generic(d.smem_optin)};
         for (cudaError_t x : errs)
             if (x != cudaSuccess) return cuda_fail(x);
         d.ready = true;
@@ -181,24 +177,30 @@ int default_rows(int MB, int K, bool contiguous)
 
 struct Plan {
     int MB = 1, R = 1, warps = 4, KS = 0, nseg = 0, stages = 0, grid = 0, ctas_per_sm = 1;
+    bool hreg = false;
     uint32_t off_h = 0, off_ring = 0, smem = 0;
 };
 
-// Streaming-kernel plan: whole rows per stage (K-segments only if a row pair
-// does not fit), one CTA per SM, as many warps (<= 4) and stages (<= 8) as the
-// shared memory left after h holds, preferring >= 2 stages per warp.  False if
-// h plus a two-stage ring does not fit at all.
-bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, Plan &pl)
+// Streaming-kernel plan.  Whole rows per stage (K-segments only if a stage of
+// R rows does not fit), one CTA per SM; among warp counts 1..8 with >= 2
+// stages each (<= 8), the largest ring (warps * stages * stage bytes) wins,
+// ties going to more warps.  Rows per stage as default_rows, halved while
+// no two-stage ring fits.  False if h plus a two-stage ring cannot fit.
+bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool norm, Plan &pl,
+                 bool allow_hreg = true)
 {
     const Tuning &t = tuning();
     pl.MB = batch_tile(M);
+    pl.hreg = allow_hreg && t.hreg && pl.MB == 1 && K <= 32 * 8 * mbglu::kHregChunks;
     pl.ctas_per_sm = t.ctas_per_sm > 0 ? t.ctas_per_sm : 1;
     const int static_reserve = 2048;  // the kernel's static shared arrays
     // two co-resident CTAs share the SM's shared memory (1 KB of it is
     // reserved per CTA by the hardware)
     int budget = (pl.ctas_per_sm == 2 ? (d.smem_optin + 1024) / 2 - 1024 : d.smem_optin) - static_reserve;
     if (t.smem_kb > 0) budget = std::min(budget, t.smem_kb * 1024 - static_reserve);
-    const uint32_t hbytes = (static_cast<uint32_t>(pl.MB) * static_cast<uint32_t>(K) * 2u + 127u) & ~127u;
+    const bool need_hs = !pl.hreg || norm;
+    const uint32_t hbytes =
+        need_hs ? (static_cast<uint32_t>(pl.MB) * static_cast<uint32_t>(K) * 2u + 127u) & ~127u : 0u;
     const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes;
     if (room <= 0) return false;
     int ks = t.ks > 0 ? std::min(t.ks, ((K + 7) / 8) * 8) : ((K + 7) / 8) * 8;
@@ -206,16 +208,23 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, Plan
     if (pl.R * pl.MB > 16) pl.R = pl.MB >= 16 ? 1 : 16 / pl.MB;
     for (;;) {
         const int64_t stage = static_cast<int64_t>(pl.R) * 4 * ks;
-        int warps = t.warps > 0 ? t.warps : 4;
-        int s = 0;
-        for (; warps >= 1; --warps) {
-            s = static_cast<int>(std::min<int64_t>(kMaxStages, room / (stage * warps)));
-            if (t.stages > 0) s = std::min(s, t.stages);
-            if (s >= 2 || t.warps > 0) break;
+        int best_w = 0, best_s = 0;
+        int64_t best_ring = 0;
+        for (int w = 1; w <= mbglu::kMaxStreamWarps; ++w) {
+            if (t.warps > 0 && w != t.warps) continue;
+            int sn = static_cast<int>(std::min<int64_t>(kMaxStages, room / (stage * w)));
+            if (t.stages > 0) sn = std::min(sn, t.stages);
+            if (sn < 2) continue;
+            const int64_t ring = stage * w * sn;
+            if (ring >= best_ring) {
+                best_ring = ring;
+                best_w = w;
+                best_s = sn;
+            }
         }
-        if (s >= 2 && warps >= 1) {
-            pl.warps = warps;
-            pl.stages = s;
+        if (best_w > 0) {
+            pl.warps = best_w;
+            pl.stages = best_s;
             break;
         }
         if (pl.R > 1) {
@@ -227,44 +236,12 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, Plan
     }
     pl.KS = ks;
     pl.nseg = (K + ks - 1) / ks;
+    if (pl.hreg && pl.nseg != 1)   // registers hold whole rows of h only
+        return plan_stream(d, M, N, K, contiguous, norm, pl, false);
     pl.off_h = kBarRegion;
     pl.off_ring = kBarRegion + hbytes;
     pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 4u * pl.R * static_cast<uint32_t>(ks);
     pl.grid = std::max(1, std::min(d.sm_count * pl.ctas_per_sm, N));
-    return true;
-}
-
-// Single-row (M = 1) plan: one matrix row per stage, 8 warps (fewer only if
-// two stages per warp would not fit), as many stages (<= 8) as fit.
-bool plan_single_row(const DeviceInfo &d, int N, int K, bool norm, Plan &pl)
-{
-    const Tuning &t = tuning();
-    if (!t.single_row || K > 32 * 8 * mbglu::kM1MaxChunksPerLane) return false;
-    const int static_reserve = 2048;
-    int budget = d.smem_optin - static_reserve;
-    if (t.smem_kb > 0) budget = std::min(budget, t.smem_kb * 1024 - static_reserve);
-    const uint32_t hbytes = norm ? ((static_cast<uint32_t>(K) * 2u + 127u) & ~127u) : 0u;
-    const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes;
-    const int64_t stage = static_cast<int64_t>(K) * 2;
-    int warps = t.warps > 0 ? t.warps : 8;
-    int s = 0;
-    for (; warps >= 1; --warps) {
-        s = room > 0 ? static_cast<int>(std::min<int64_t>(kMaxStages, room / (stage * warps))) : 0;
-        if (t.stages > 0) s = std::min(s, t.stages);
-        if (s >= 2 || t.warps > 0) break;
-    }
-    if (s < 2 || warps < 1) return false;
-    pl.MB = 1;
-    pl.R = 1;
-    pl.warps = warps;
-    pl.stages = s;
-    pl.KS = K;
-    pl.nseg = 1;
-    pl.off_h = kBarRegion;
-    pl.off_ring = kBarRegion + hbytes;
-    pl.smem = pl.off_ring + static_cast<uint32_t>(warps) * s * static_cast<uint32_t>(stage);
-    pl.grid = std::max(1, std::min(d.sm_count, N));
-    pl.ctas_per_sm = 1;
     return true;
 }
 
@@ -290,9 +267,9 @@ template <bool NORM>
 mbglu_status launch_stream(const Plan &pl, const GluParams &p, cudaStream_t stream, bool pdl)
 {
     const dim3 grid(pl.grid), block(pl.warps * 32);
-#define MBGLU_CASE(TMB, TR)                                                                                   \
-    if (pl.MB == TMB && pl.R == TR)                                                                               \
-        return launch(mbglu::glu_stream_kernel<TMB, TR, NORM>, grid, block, pl.smem, stream, pdl, p);
+#define MBGLU_CASE(TMB, TR, TH)                                                                               \
+    if (pl.MB == TMB && pl.R == TR && pl.hreg == TH)                                                             \
+        return launch(mbglu::glu_stream_kernel<TMB, TR, NORM, TH>, grid, block, pl.smem, stream, pdl, p);
     MBGLU_FOR_EACH_TILE(MBGLU_CASE)
 #undef MBGLU_CASE
     return MBGLU_ERR_SHAPE;  // unreachable: plan_stream only produces listed tiles
@@ -398,18 +375,7 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
     Plan pl;
     const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && (ld_gate % 8 == 0) &&
                          (ld_up % 8 == 0);
-    if (bulk_ok && M == 1 && plan_single_row(*d, N, K, false, pl)) {
-        p.KS = pl.KS;
-        p.nseg = 1;
-        p.stages = pl.stages;
-        p.off_h = pl.off_h;
-        p.off_ring = pl.off_ring;
-        p.vec_in = aligned(h, 16);
-        st = launch(mbglu::glu_m1_kernel<false>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
-        if (st == MBGLU_OK) t_last_variant = kSingleRow;
-        return st;
-    }
-    const bool fast = bulk_ok && plan_stream(*d, M, N, K, ld_gate == K && ld_up == K, pl);
+    const bool fast = bulk_ok && plan_stream(*d, M, N, K, ld_gate == K && ld_up == K, false, pl);
     if (fast) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;
@@ -495,17 +461,7 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mb
 
     Plan pl;
     const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && p.vec_in;
-    if (bulk_ok && M == 1 && plan_single_row(*d, N, K, true, pl)) {
-        p.KS = pl.KS;
-        p.nseg = 1;
-        p.stages = pl.stages;
-        p.off_h = pl.off_h;
-        p.off_ring = pl.off_ring;
-        st = launch(mbglu::glu_m1_kernel<true>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
-        if (st == MBGLU_OK) t_last_variant = kSingleRow;
-        return st;
-    }
-    const bool fast = bulk_ok && plan_stream(*d, M, N, K, true, pl);
+    const bool fast = bulk_ok && plan_stream(*d, M, N, K, true, true, pl);
     if (fast) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;
