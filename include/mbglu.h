@@ -175,7 +175,8 @@ int mbglu_abi_version(void);
 int mbglu_last_cuda_error(void);
 
 /* Which kernel the calling thread's last successful call launched:
- * 0 none (no-op), 1 streaming kernel, 2 generic kernel, 3 zero fill. */
+ * 0 none (no-op), 1 streaming kernel (CUDA-core FMA), 2 generic kernel,
+ * 3 zero fill, 4 tensor-core streaming kernel (batch >= 3). */
 int mbglu_last_variant(void);
 
 /*

@@ -153,8 +153,8 @@ def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf",
 
 
 def last_variant() -> int:
-    """Kernel the calling thread's last call launched: 0 none, 1 streaming,
-    2 generic, 3 zero fill."""
+    """Kernel the calling thread's last call launched: 0 none, 1 streaming
+    (CUDA-core), 2 generic, 3 zero fill, 4 tensor-core streaming (batch >= 3)."""
     return lib().mbglu_last_variant()
 
 

@@ -58,6 +58,7 @@ struct GluParams {
     uint32_t off_h, off_ring;
     int vec_in;              // 1: h (or s, norm_w) may be read with 16-byte loads
     int prefetch;            // 1: first weight stages requested before the dependency wait
+    int interleave;          // 1: this CTA's row groups are blockIdx.x, +gridDim.x, ... of all groups
 };
 
 // ---------------------------------------------------------------------------
@@ -137,8 +138,9 @@ __device__ __forceinline__ void load_h_to_smem(const GluParams &p, uint16_t *h_s
 // h_s (rows M..rows_out-1 zero); M <= MB.
 template <int MB>
 __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s, float (*red)[MB],
-                                              float *inv_s, int rows_out)
+                                              float *inv_s, int rows_out, int hstride = 0)
 {
+    if (hstride == 0) hstride = p.K;
     const int K = p.K, tid = threadIdx.x, nthr = blockDim.x;
     const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
     float ss[MB];
@@ -204,7 +206,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
                 }
                 o = make_uint4(r[0], r[1], r[2], r[3]);
             }
-            *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * K + c * 8) = o;
+            *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * hstride + c * 8) = o;
         }
     } else {
         for (int i = tid; i < rows_out * K; i += nthr) {
@@ -214,7 +216,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
                 const float sv = bf16_to_f32(p.s[static_cast<int64_t>(m) * K + k]);
                 o = f32_to_bf16((sv * inv_s[m]) * (1.0f + bf16_to_f32(p.norm_w[k])));
             }
-            h_s[i] = o;
+            h_s[static_cast<int64_t>(m) * hstride + k] = o;
         }
     }
 }
@@ -276,9 +278,21 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
     uint16_t *h_s = reinterpret_cast<uint16_t *>(smem + p.off_h);
     uint16_t *ring = reinterpret_cast<uint16_t *>(smem + p.off_ring) + static_cast<int64_t>(warp) * S * stage_elems;
 
-    const int r0 = static_cast<int>((static_cast<int64_t>(p.N) * blockIdx.x) / gridDim.x);
-    const int r1 = static_cast<int>((static_cast<int64_t>(p.N) * (blockIdx.x + 1)) / gridDim.x);
-    const int ngroups = (r1 - r0 + R - 1) / R;
+    // Row groups of this CTA: a contiguous block [r0, r1) cut into groups of R
+    // rows, or (interleave) the groups blockIdx.x, blockIdx.x + gridDim.x, ...
+    // of the whole matrix.  group_row0(g) is the first row of local group g;
+    // its rows end at min(row0 + R, rend).
+    const int r0 = p.interleave ? 0 : static_cast<int>((static_cast<int64_t>(p.N) * blockIdx.x) / gridDim.x);
+    const int r1 = p.interleave ? p.N : static_cast<int>((static_cast<int64_t>(p.N) * (blockIdx.x + 1)) / gridDim.x);
+    const int all_groups = (p.N + R - 1) / R;
+    const int ngroups = p.interleave
+                            ? (all_groups > static_cast<int>(blockIdx.x)
+                                   ? (all_groups - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
+                                   : 0)
+                            : (r1 - r0 + R - 1) / R;
+    auto group_row0 = [&](int g) -> int {
+        return p.interleave ? (g * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x)) * R : r0 + g * R;
+    };
     const bool contig = (p.ld_gate == K) && (p.ld_up == K) && (KS == K);
 
     if (lane == 0)
@@ -290,7 +304,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
     const uint64_t policy = l2_policy_evict_first();
     // lane 0: request unit (group g, segment seg) into stage st
     auto issue = [&](int st, int g, int seg) {
-        const int row0 = r0 + g * R;
+        const int row0 = group_row0(g);
         const int nr = min(R, r1 - row0);
         const int k0 = seg * KS;
         const int len = min(KS, K - k0);
@@ -466,7 +480,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
         }
         __syncwarp();
         if (seg == nseg - 1) {
-            const int row0 = r0 + g * R;
+            const int row0 = group_row0(g);
             float gsel = 0.0f, usel = 0.0f;
 #pragma unroll
             for (int r = 0; r < R; ++r)
@@ -480,6 +494,216 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
             const int r = lane / MB, m = lane - (lane / MB) * MB;
             if (lane < R * MB && m < p.M && row0 + r < r1)
                 p.out[m * p.ldo + row0 + r] = glu_epilogue(gsel, usel, p.mode);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the tensor-core streaming kernel (batch 3..16)
+// ---------------------------------------------------------------------------
+//
+// For batches where CUDA-core issue, not HBM, would bound the GEMV (about
+// 150 instructions per KB of weights at M = 8), the same streaming scheme
+// feeds mma.sync.m16n8k16 (bf16 in, fp32 accumulate):
+//   A (16 x 16) = h rows 0..15 at k..k+15 -- rows >= M read a zero row;
+//   B (16 x 8)  = 8 consecutive weight rows at k..k+15 (gate, then up);
+//   D (16 x 8)  = g (or u) for 16 batch rows x 8 output features.
+// A group is 8 consecutive rows; a unit is (group, K-segment of KS).  A stage
+// holds the unit's 8 gate rows then 8 up rows, each row a separate bulk copy
+// into a row padded by 16 bytes, so ldmatrix's 8 row addresses fall in 8
+// different 16-byte bank groups (no conflicts).  Lanes 0..15 issue the 16
+// copies of a stage together.  Rings, claiming, ordering with the preceding
+// grid and bounded waits are those of glu_stream_kernel.
+//
+// Shared memory (dynamic):  [0, 1024)          mbarriers, slot_grp, counter
+//                           [off_h, off_ring)  h_s[M + 1][K + 8] bf16 (row M = 0)
+//                           [off_ring, ...)    ring[warp][stage][16][KS + 8] bf16
+__device__ __forceinline__ void ldmatrix_x4(uint32_t &a0, uint32_t &a1, uint32_t &a2, uint32_t &a3,
+                                            const void *row)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(smem_addr(row)));
+}
+
+__device__ __forceinline__ void ldmatrix_x2(uint32_t &b0, uint32_t &b1, const void *row)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(b0), "=r"(b1)
+                 : "r"(smem_addr(row)));
+}
+
+__device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+constexpr int kMmaRows = 8;   // weight rows per group (the MMA's n)
+
+template <bool NORM>
+__global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const GluParams p)
+{
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float red[kMaxWarps][kMaxM];
+    __shared__ float inv_s[kMaxM];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.stages, KS = p.KS, K = p.K, nseg = p.nseg;
+    const int RS = KS + 8;                                   // padded ring row, elements
+    const int HS = K + 8;                                    // padded h row, elements
+    const int64_t stage_elems = static_cast<int64_t>(2) * kMmaRows * RS;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * S;
+    int *slot_grp = reinterpret_cast<int *>(smem + kSlotGrpOffset) + warp * S;
+    int *counter = reinterpret_cast<int *>(smem + kCounterOffset);
+    uint16_t *h_s = reinterpret_cast<uint16_t *>(smem + p.off_h);
+    uint16_t *ring = reinterpret_cast<uint16_t *>(smem + p.off_ring) + static_cast<int64_t>(warp) * S * stage_elems;
+
+    const int R = kMmaRows;
+    const int r0 = p.interleave ? 0 : static_cast<int>((static_cast<int64_t>(p.N) * blockIdx.x) / gridDim.x);
+    const int r1 = p.interleave ? p.N : static_cast<int>((static_cast<int64_t>(p.N) * (blockIdx.x + 1)) / gridDim.x);
+    const int all_groups = (p.N + R - 1) / R;
+    const int ngroups = p.interleave
+                            ? (all_groups > static_cast<int>(blockIdx.x)
+                                   ? (all_groups - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
+                                   : 0)
+                            : (r1 - r0 + R - 1) / R;
+    auto group_row0 = [&](int g) -> int {
+        return p.interleave ? (g * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x)) * R : r0 + g * R;
+    };
+
+    if (lane == 0)
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    if (threadIdx.x == 0) *counter = 0;
+    fence_mbar_init();
+    __syncthreads();
+
+    const uint64_t policy = l2_policy_evict_first();
+    // whole warp: request unit (group g, segment seg) into stage st.  Lane 0
+    // posts the byte count first; lanes 0..nr-1 copy gate rows, 8..8+nr-1 up rows.
+    auto issue = [&](int st, int g, int seg) {
+        const int row0 = group_row0(g);
+        const int nr = min(R, r1 - row0);
+        const int k0 = seg * KS;
+        const int len = min(KS, K - k0);
+        const uint32_t row_bytes = static_cast<uint32_t>(len) * 2u;
+        if (lane == 0) mbar_arrive_expect_tx(&bars[st], 2u * static_cast<uint32_t>(nr) * row_bytes);
+        __syncwarp();
+        const int r = lane & 7;
+        if (lane < 16 && r < nr) {
+            const bool up = lane >= 8;
+            const uint16_t *src = up ? p.up + static_cast<int64_t>(row0 + r) * p.ld_up + k0
+                                     : p.gate + static_cast<int64_t>(row0 + r) * p.ld_gate + k0;
+            uint16_t *dst = ring + st * stage_elems + static_cast<int64_t>((up ? R : 0) + r) * RS;
+            bulk_g2s(dst, src, row_bytes, &bars[st], policy);
+        }
+    };
+    int last_g = -1, last_seg = nseg;   // warp-uniform
+    auto fill = [&](int st) {
+        if (last_g >= 0 && last_seg + 1 < nseg) {
+            ++last_seg;
+        } else {
+            last_seg = 0;
+            int ng = 0;
+            if (lane == 0) ng = atomicAdd(counter, 1);
+            ng = __shfl_sync(0xffffffffu, ng, 0);
+            last_g = ng < ngroups ? ng : -1;
+        }
+        if (lane == 0) slot_grp[st] = last_g;
+        if (last_g >= 0) issue(st, last_g, last_seg);
+    };
+
+    if (p.prefetch)
+        for (int st = 0; st < S; ++st) fill(st);
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (!p.prefetch)
+        for (int st = 0; st < S; ++st) fill(st);
+    __syncwarp();
+
+    // h rows 0..M-1, then a zero row M (padded stride HS)
+    if constexpr (NORM) {
+        norm_prologue<kMaxM>(p, h_s, red, inv_s, p.M, HS);
+    } else {
+        const int nch = K >> 3;
+        for (int i = threadIdx.x; i < p.M * nch; i += blockDim.x) {
+            const int m = i / nch, c = i - m * nch;
+            uint4 v;
+            if (p.vec_in) {
+                v = *reinterpret_cast<const uint4 *>(p.h + m * p.ldh + c * 8);
+            } else {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    w[q] = static_cast<uint32_t>(p.h[m * p.ldh + c * 8 + 2 * q]) |
+                           (static_cast<uint32_t>(p.h[m * p.ldh + c * 8 + 2 * q + 1]) << 16);
+                v = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * HS + c * 8) = v;
+        }
+    }
+    for (int c = threadIdx.x; c < (K >> 3); c += blockDim.x)
+        *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(p.M) * HS + c * 8) = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+
+    // ldmatrix.x4 row addresses for A: lane l -> h row (l & 15) (zero row if
+    // >= M), k offset (l >> 4) * 8.  ldmatrix.x2 for B: lane l (l < 16) -> ring
+    // row (l & 7), k offset ((l >> 3) & 1) * 8.
+    const int arow = (lane & 15) < p.M ? (lane & 15) : p.M;
+    const uint16_t *a_base = h_s + static_cast<int64_t>(arow) * HS + (lane >> 4) * 8;
+    const int b_off = (lane & 7) * RS + ((lane >> 3) & 1) * 8;
+
+    float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
+    int seg = nseg;
+    for (int u = 0;; ++u) {
+        const int st = u % S;
+        const int g = slot_grp[st];
+        if (g < 0) break;
+        seg = (seg + 1 < nseg) ? seg + 1 : 0;
+        const bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) {
+                atomicExch(&g_device_error, kErrTimeout);
+                for (int v = u; v < u + S; ++v)
+                    if (slot_grp[v % S] >= 0)
+                        mbar_wait_bounded(&bars[v % S], static_cast<uint32_t>((v / S) & 1), kWaitLimitNs);
+            }
+            __syncwarp();
+            return;
+        }
+        const int k0 = seg * KS;
+        const int nk = min(KS, K - k0) >> 4;                 // whole k16 steps
+        const uint16_t *wg = ring + st * stage_elems + b_off;
+        const uint16_t *wu = wg + R * RS;
+        const uint16_t *ha = a_base + k0;
+#pragma unroll 4
+        for (int kk = 0; kk < nk; ++kk) {
+            uint32_t a0, a1, a2, a3, g0, g1, u0, u1;
+            ldmatrix_x4(a0, a1, a2, a3, ha + kk * 16);
+            ldmatrix_x2(g0, g1, wg + kk * 16);
+            ldmatrix_x2(u0, u1, wu + kk * 16);
+            mma_bf16_16x8x16(dg, a0, a1, a2, a3, g0, g1);
+            mma_bf16_16x8x16(du, a0, a1, a2, a3, u0, u1);
+        }
+        __syncwarp();
+        if (lane == 0) fence_proxy_async_smem();
+        fill(st);   // the unit S ahead of u, or -1 once the CTA's groups run out
+        __syncwarp();
+        if (seg == nseg - 1) {
+            // D layout: d[0], d[1] -> batch row lane/4, features 2*(lane%4) + 0, 1;
+            //           d[2], d[3] -> batch row lane/4 + 8, same features.
+            const int row0 = group_row0(g);
+            const int m0 = lane >> 2, n = row0 + 2 * (lane & 3);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int m = m0 + (q >> 1) * 8, nn = n + (q & 1);
+                if (m < p.M && nn < r1 && nn < row0 + R) p.out[m * p.ldo + nn] = glu_epilogue(dg[q], du[q], p.mode);
+                dg[q] = du[q] = 0.f;
+            }
         }
     }
 }

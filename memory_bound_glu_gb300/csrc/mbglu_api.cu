@@ -24,7 +24,7 @@ using mbglu::GluParams;
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_variant = 0;
 
-enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3 };
+enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4 };
 
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kBarRegion = 1024;        // mbarriers, stage -> group table, group counter
@@ -53,6 +53,9 @@ struct Tuning {
     int smem_kb = 0;          // shared-memory budget cap in KiB (0: device limit)
     int ctas_per_sm = 0;      // 1 or 2 streaming CTAs per SM (0: automatic)
     int hreg = 1;             // batch 1: keep h in registers where K allows
+    int waves = 1;            // CTAs per resident CTA slot (grid = SMs * ctas_per_sm * waves)
+    int interleave = 0;       // row groups dealt round-robin over CTAs instead of contiguous blocks
+    int mma_min_m = 3;        // smallest batch that takes the tensor-core kernel (17: never)
 };
 
 std::atomic<int> g_policy{MBGLU_POLICY_PREFETCH};
@@ -75,6 +78,9 @@ const Tuning &tuning()
         x.smem_kb = std::max(0, env_int("MBGLU_SMEM_KB", 0));
         x.ctas_per_sm = std::min(2, std::max(0, env_int("MBGLU_CTAS_PER_SM", 0)));
         x.hreg = env_int("MBGLU_HREG", 1) != 0;
+        x.waves = std::min(16, std::max(1, env_int("MBGLU_WAVES", 1)));
+        x.interleave = env_int("MBGLU_INTERLEAVE", 0) != 0;
+        x.mma_min_m = std::min(17, std::max(1, env_int("MBGLU_MMA_MIN_M", 3)));
         return x;
     }();
     return t;
@@ -114,6 +120,16 @@ cudaError_t allow_all_stream_kernels(int optin)
     return e;
 }
 
+template <bool NORM>
+cudaError_t allow_smem_mma(int optin)
+{
+    cudaFuncAttributes a{};
+    cudaError_t e = cudaFuncGetAttributes(&a, mbglu::glu_mma_kernel<NORM>);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(mbglu::glu_mma_kernel<NORM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                optin - static_cast<int>(a.sharedSizeBytes));
+}
+
 cudaError_t allow_smem_generic(int optin)
 {
     cudaFuncAttributes a{};
@@ -137,7 +153,8 @@ mbglu_status device_info(const DeviceInfo **out)
         if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
             cudaSuccess)
             return cuda_fail(e);
-        const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_generic(d.smem_optin)};
+        const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_mma<false>(d.smem_optin),
+                                    allow_smem_mma<true>(d.smem_optin), allow_smem_generic(d.smem_optin)};
         for (cudaError_t x : errs)
             if (x != cudaSuccess) return cuda_fail(x);
         d.ready = true;
@@ -182,10 +199,11 @@ struct Plan {
 };
 
 // Streaming-kernel plan.  Whole rows per stage (K-segments only if a stage of
-// R rows does not fit), one CTA per SM; among warp counts 1..8 with >= 2
-// stages each (<= 8), the largest ring (warps * stages * stage bytes) wins,
-// ties going to more warps.  Rows per stage as default_rows, halved while
-// no two-stage ring fits.  False if h plus a two-stage ring cannot fit.
+// R rows does not fit), one CTA per SM, two stages per warp and as many warps
+// (<= 8) as then fit: measured on GB300, more warps beat deeper per-warp
+// rings (3-5 stages per warp ran 15-40% slower at equal ring bytes).  Rows
+// per stage as default_rows, halved while not even one warp fits.  False if
+// h plus a two-stage ring cannot fit.
 bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool norm, Plan &pl,
                  bool allow_hreg = true)
 {
@@ -210,10 +228,10 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
         const int64_t stage = static_cast<int64_t>(pl.R) * 4 * ks;
         int best_w = 0, best_s = 0;
         int64_t best_ring = 0;
+        const int want_s = t.stages > 0 ? t.stages : 2;
         for (int w = 1; w <= mbglu::kMaxStreamWarps; ++w) {
             if (t.warps > 0 && w != t.warps) continue;
-            int sn = static_cast<int>(std::min<int64_t>(kMaxStages, room / (stage * w)));
-            if (t.stages > 0) sn = std::min(sn, t.stages);
+            const int sn = static_cast<int>(std::min<int64_t>(want_s, room / (stage * w)));
             if (sn < 2) continue;
             const int64_t ring = stage * w * sn;
             if (ring >= best_ring) {
@@ -241,7 +259,56 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
     pl.off_h = kBarRegion;
     pl.off_ring = kBarRegion + hbytes;
     pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 4u * pl.R * static_cast<uint32_t>(ks);
-    pl.grid = std::max(1, std::min(d.sm_count * pl.ctas_per_sm, N));
+    pl.grid = std::max(1, std::min(d.sm_count * pl.ctas_per_sm * t.waves, N));
+    return true;
+}
+
+// Tensor-core plan (batch >= mma_min_m, K % 16 == 0): groups of 8 rows,
+// K-segments of a multiple of 16 dividing K (<= 768 elements), each row
+// padded by 16 bytes; h_s holds M rows plus a zero row.  Two stages per warp,
+// as many warps (<= 8) as fit; segments shrink (>= 256) while fewer than 4
+// warps fit.  False if nothing fits.
+bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl)
+{
+    const Tuning &t = tuning();
+    if (M < t.mma_min_m || K % 16 != 0) return false;
+    const int static_reserve = 2048;
+    int budget = d.smem_optin - static_reserve;
+    if (t.smem_kb > 0) budget = std::min(budget, t.smem_kb * 1024 - static_reserve);
+    const uint32_t hbytes = (static_cast<uint32_t>(M + 1) * static_cast<uint32_t>(K + 8) * 2u + 127u) & ~127u;
+    const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes;
+    if (room <= 0) return false;
+    int ks = 0;
+    if (t.ks > 0) {
+        ks = std::max(16, std::min(t.ks, K) & ~15);
+    } else {
+        for (int c = 768; c >= 16; c -= 16)
+            if (K % c == 0) { ks = c; break; }
+        if (ks < 256) ks = std::min(K, 512);
+    }
+    const int want_s = t.stages > 0 ? t.stages : 2;
+    for (;;) {
+        const int64_t stage = static_cast<int64_t>(2) * mbglu::kMmaRows * (ks + 8) * 2;
+        int w = t.warps > 0 ? t.warps : mbglu::kMaxStreamWarps;
+        while (w > 1 && static_cast<int64_t>(w) * want_s * stage > room) --w;
+        if (static_cast<int64_t>(w) * 2 * stage > room) w = 0;
+        if (w >= 4 || (w >= 1 && (ks <= 256 || t.warps > 0 || t.ks > 0))) {
+            pl.warps = w;
+            pl.stages = static_cast<int>(std::min<int64_t>(want_s, room / (stage * w)));
+            pl.KS = ks;
+            break;
+        }
+        if (ks <= 256) return false;
+        ks = std::max(256, (ks / 2) & ~15);
+    }
+    pl.MB = 16;
+    pl.R = mbglu::kMmaRows;
+    pl.nseg = (K + pl.KS - 1) / pl.KS;
+    pl.off_h = kBarRegion;
+    pl.off_ring = kBarRegion + hbytes;
+    pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 2u * mbglu::kMmaRows *
+                                static_cast<uint32_t>(pl.KS + 8) * 2u;
+    pl.grid = std::max(1, std::min(d.sm_count, N));
     return true;
 }
 
@@ -375,6 +442,18 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
     Plan pl;
     const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && (ld_gate % 8 == 0) &&
                          (ld_up % 8 == 0);
+    if (bulk_ok && plan_mma(*d, M, N, K, pl)) {
+        p.KS = pl.KS;
+        p.nseg = pl.nseg;
+        p.stages = pl.stages;
+        p.off_h = pl.off_h;
+        p.off_ring = pl.off_ring;
+        p.vec_in = aligned(h, 16) && (ldh % 8 == 0);
+        p.interleave = tuning().interleave;
+        st = launch(mbglu::glu_mma_kernel<false>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
+        if (st == MBGLU_OK) t_last_variant = kTensor;
+        return st;
+    }
     const bool fast = bulk_ok && plan_stream(*d, M, N, K, ld_gate == K && ld_up == K, false, pl);
     if (fast) {
         p.KS = pl.KS;
@@ -383,6 +462,7 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
         p.off_h = pl.off_h;
         p.off_ring = pl.off_ring;
         p.vec_in = aligned(h, 16) && (ldh % 8 == 0);
+        p.interleave = tuning().interleave;
         st = launch_stream<false>(pl, p, stream, pdl);
         if (st == MBGLU_OK) t_last_variant = kStream;
         return st;
@@ -461,6 +541,17 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mb
 
     Plan pl;
     const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && p.vec_in;
+    if (bulk_ok && plan_mma(*d, M, N, K, pl)) {
+        p.KS = pl.KS;
+        p.nseg = pl.nseg;
+        p.stages = pl.stages;
+        p.off_h = pl.off_h;
+        p.off_ring = pl.off_ring;
+        p.interleave = tuning().interleave;
+        st = launch(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
+        if (st == MBGLU_OK) t_last_variant = kTensor;
+        return st;
+    }
     const bool fast = bulk_ok && plan_stream(*d, M, N, K, true, true, pl);
     if (fast) {
         p.KS = pl.KS;
@@ -468,6 +559,7 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mb
         p.stages = pl.stages;
         p.off_h = pl.off_h;
         p.off_ring = pl.off_ring;
+        p.interleave = tuning().interleave;
         st = launch_stream<true>(pl, p, stream, pdl);
         if (st == MBGLU_OK) t_last_variant = kStream;
         return st;

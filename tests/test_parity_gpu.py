@@ -41,6 +41,9 @@ def oracle_glu(h, g, u, mode):
 
 def parity(got, ref, tau_info, what=""):
     tau, diag, K, mode = tau_info
+    if mb.last_variant() == 4:      # tensor-core accumulation bound
+        diag["acc"] = "mma"
+        tau = tol.conditioning_floor(diag, K, mode)
     return tol.assert_parity(got, ref, tau, what, diag=diag, K=K, mode=mode)
 
 
@@ -50,7 +53,7 @@ def run_gpu(h, g, u, mode, **kw):
     return gi.bits(out.cpu())
 
 
-FAST = (1,)     # the streaming kernel
+FAST = (1, 4)   # the streaming kernels: CUDA-core FMA, tensor core
 
 
 def check(h, g, u, mode, what="", variant=None):
@@ -145,6 +148,32 @@ def test_batch_one_paths(K, ld_pad, h_off, expect):
     torch.cuda.synchronize()
     assert mb.last_variant() == expect
     parity(gi.bits(out.cpu()), ref, tau, f"M=1 K={K}")
+
+
+@pytest.mark.parametrize("M", [3, 4, 5, 8, 9, 12, 16])
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_tensor_core_kernel(M, mode):
+    """Batch >= 3 on the tensor-core kernel: ragged N (partial last 8-row
+    group), several K-segments, rows padded in shared memory."""
+    N, K = 1339, 2560
+    h = gi.normal_bf16((M, K), 1.0, M, "tc-h")
+    g = gi.normal_bf16((N, K), K ** -0.5, M, "tc-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, M, "tc-u")
+    check(h, g, u, mode, f"tc M={M}", variant=4)
+
+
+@pytest.mark.parametrize("K,ld_pad,h_off", [(1024, 8, 8), (4096, 0, 0), (2576, 16, 1), (1040, 0, 0)])
+def test_tensor_core_kernel_strides_and_k(K, ld_pad, h_off):
+    M, N = 8, 611
+    hb = gi.normal_bf16((M, K + 8), 1.0, K, "tcs-h")
+    gb = gi.normal_bf16((N, K + ld_pad), K ** -0.5, K, "tcs-g")
+    ub = gi.normal_bf16((N, K + ld_pad), K ** -0.5, K, "tcs-u")
+    h, g, u = hb[:, h_off:h_off + K], gb[:, :K], ub[:, :K]
+    ref, tau = oracle_glu(h.contiguous(), g.contiguous(), u.contiguous(), "hf")
+    out = mb.glu_gemv(hb.to(DEV)[:, h_off:h_off + K], gb.to(DEV)[:, :K], ub.to(DEV)[:, :K], mode="hf")
+    torch.cuda.synchronize()
+    assert mb.last_variant() == 4
+    parity(gi.bits(out.cpu()), ref, tau, f"tc K={K}")
 
 
 def test_guard_band_untouched():

@@ -67,14 +67,20 @@ def _dsilu(x):
     return s * (1.0 + x * (1.0 - s))
 
 
-def accumulation_gamma(K: int) -> float:
-    """Relative bound of the kernels' fp32 dot products (depth ceil(K/32)+5)."""
+def accumulation_gamma(K: int, diag=None) -> float:
+    """Relative bound of the kernels' fp32 dot products: the CUDA-core kernels
+    sum at depth ceil(K/32)+5 with one rounding (2^-24) per step; the
+    tensor-core kernel chains K/16 MMAs whose fp32 accumulation is not
+    specified to round to nearest, bounded as depth K/16 + 16 with unit 2^-23
+    (diag["acc"] == "mma")."""
+    if diag is not None and diag.get("acc") == "mma":
+        return (-(-K // 16) + 16) * 2.0 ** -23
     return (-(-K // 32) + 5) * 2.0 ** -24
 
 
 def conditioning_floor(diag, K: int, mode: str) -> np.ndarray:
     G, U, Ag, Au = diag["G"], diag["U"], diag["Ag"], diag["Au"]
-    gamma = accumulation_gamma(K)
+    gamma = accumulation_gamma(K, diag)
     dg, du = gamma * Ag + diag.get("dG_extra", 0.0), gamma * Au + diag.get("dU_extra", 0.0)
     if mode == "hf":
         dg = dg + 2.0 ** -8 * np.abs(G)
@@ -111,7 +117,7 @@ def alternative_ok(gpu_bits, diag, K: int, mode: str, idx) -> np.ndarray:
     g = np.asarray(gpu_bits).reshape(-1)[idx]
     G = diag["G"].reshape(-1)[idx]
     U = diag["U"].reshape(-1)[idx]
-    gamma = accumulation_gamma(K)
+    gamma = accumulation_gamma(K, diag)
     dG = gamma * diag["Ag"].reshape(-1)[idx]
     dU = gamma * diag["Au"].reshape(-1)[idx]
     if "dG_extra" in diag:
