@@ -44,6 +44,7 @@
 #ifndef MBGLU_H
 #define MBGLU_H
 
+#include <stddef.h>
 #include <stdint.h>
 #include <cuda_runtime_api.h>
 
@@ -136,6 +137,37 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual,
                              const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w,
                              mbglu_bf16 *out, int M, int N, int K,
                              mbglu_mode mode, cudaStream_t stream);
+
+/*
+ * add_rmsnorm_glu_ws -- the same operation and arguments as add_rmsnorm_glu,
+ * as ONE kernel: every CTA forms s = bf16(x + residual) in shared memory, and
+ * the CTA that arrives last on an arrival counter in `workspace` -- when no CTA
+ * reads residual any more -- writes s back to residual and returns the counter
+ * to zero.  Saves the residual-add launch and its dependency on the critical
+ * path.
+ *   workspace        device memory of at least MBGLU_WORKSPACE_BYTES,
+ *                    16-byte aligned, owned by the caller, ALL ZERO before its
+ *                    first use (cudaMemset once); every completed call leaves
+ *                    it zero again.
+ *   Calls that may run at the same time (on different streams, or in
+ *   concurrently launched graphs) need different workspaces; consecutive
+ *   calls on one stream may share one.  A call that does not complete (a
+ *   bounded wait gave up, see mbglu_read_device_error) may leave it non-zero:
+ *   zero it again before reuse.
+ * Where the single kernel does not apply (operands not 16-byte aligned,
+ * K % 8 != 0, or M*K*2 bytes of s not fitting beside the weight ring) the
+ * call runs the two-kernel path of add_rmsnorm_glu and leaves the workspace
+ * untouched.  Errors as add_rmsnorm_glu, plus MBGLU_ERR_NULL for a NULL
+ * workspace, MBGLU_ERR_SHAPE for workspace_bytes < MBGLU_WORKSPACE_BYTES,
+ * MBGLU_ERR_ALIGN, MBGLU_ERR_ALIAS if it overlaps an operand.
+ */
+#define MBGLU_WORKSPACE_BYTES 256
+mbglu_status add_rmsnorm_glu_ws(const mbglu_bf16 *x, mbglu_bf16 *residual,
+                                const mbglu_bf16 *norm_w, float eps,
+                                const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w,
+                                mbglu_bf16 *out, int M, int N, int K,
+                                mbglu_mode mode, void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
 
 /*
  * Launch policy, process-wide (default MBGLU_POLICY_PREFETCH).  It decides how

@@ -19,9 +19,10 @@ MODE_FUSED = 0
 MODE_HF = 1
 _MODES = {"fused": MODE_FUSED, "hf": MODE_HF, MODE_FUSED: MODE_FUSED, MODE_HF: MODE_HF}
 MAX_M = 16
+WORKSPACE_BYTES = 256
 
 # Every symbol include/mbglu.h declares.
-EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "mbglu_set_launch_policy", "mbglu_get_launch_policy",
+EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "mbglu_set_launch_policy", "mbglu_get_launch_policy",
            "mbglu_status_string", "mbglu_abi_version", "mbglu_last_cuda_error", "mbglu_last_variant",
            "mbglu_read_device_error")
 POLICY_SERIAL, POLICY_PDL, POLICY_PREFETCH = 0, 1, 2
@@ -44,6 +45,8 @@ def _bind(l):
     l.glu_gemv.restype = i32
     l.add_rmsnorm_glu.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32, i32, vp]
     l.add_rmsnorm_glu.restype = i32
+    l.add_rmsnorm_glu_ws.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32, i32, vp, ctypes.c_size_t, vp]
+    l.add_rmsnorm_glu_ws.restype = i32
     l.mbglu_status_string.argtypes = [i32]
     l.mbglu_status_string.restype = ctypes.c_char_p
     l.mbglu_abi_version.restype = i32
@@ -120,9 +123,15 @@ def glu_gemv(h, gate_w, up_w, out=None, mode="fused", stream=None):
     return out2.view(N) if squeeze else out
 
 
-def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf", stream=None):
+def new_workspace(device=None):
+    """A zeroed workspace for add_rmsnorm_glu (one per concurrently running stream)."""
+    return torch.zeros(WORKSPACE_BYTES, dtype=torch.uint8, device=device or "cuda")
+
+
+def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf", stream=None, workspace=None):
     """residual <- bf16(x + residual); h = zero-centred RMSNorm(residual);
-    out = GLU(h).  Returns out; residual is updated in place."""
+    out = GLU(h).  Returns out; residual is updated in place.  With a
+    workspace (new_workspace()) the whole segment runs as one kernel."""
     _check(x, "x", 2)
     _check(residual, "residual", 2)
     _check(norm_w, "norm_w", 1)
@@ -144,9 +153,17 @@ def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf",
     if tuple(out.shape) != (M, N) or not out.is_contiguous():
         raise ValueError(f"out must be a contiguous [{M},{N}] tensor")
     with torch.cuda.device(dev):
-        st = lib().add_rmsnorm_glu(x.data_ptr(), residual.data_ptr(), norm_w.data_ptr(), float(eps),
-                                   gate_w.data_ptr(), up_w.data_ptr(), out.data_ptr(), M, N, K, _MODES[mode],
-                                   _stream_handle(dev, stream))
+        if workspace is None:
+            st = lib().add_rmsnorm_glu(x.data_ptr(), residual.data_ptr(), norm_w.data_ptr(), float(eps),
+                                       gate_w.data_ptr(), up_w.data_ptr(), out.data_ptr(), M, N, K, _MODES[mode],
+                                       _stream_handle(dev, stream))
+        else:
+            if not (workspace.is_cuda and workspace.device == dev and workspace.is_contiguous()):
+                raise ValueError("workspace must be a contiguous CUDA tensor on the operands' device")
+            st = lib().add_rmsnorm_glu_ws(x.data_ptr(), residual.data_ptr(), norm_w.data_ptr(), float(eps),
+                                          gate_w.data_ptr(), up_w.data_ptr(), out.data_ptr(), M, N, K, _MODES[mode],
+                                          workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                          _stream_handle(dev, stream))
     if st != 0:
         raise MbgluError(st, "add_rmsnorm_glu")
     return out

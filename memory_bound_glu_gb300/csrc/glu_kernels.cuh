@@ -59,6 +59,13 @@ struct GluParams {
     int vec_in;              // 1: h (or s, norm_w) may be read with 16-byte loads
     int prefetch;            // 1: first weight stages requested before the dependency wait
     int interleave;          // 1: this CTA's row groups are blockIdx.x, +gridDim.x, ... of all groups
+    // single-kernel add_rmsnorm_glu (fused != 0): s = bf16(x + residual) is formed in
+    // shared memory at off_s, and the last CTA to arrive on *ws writes it to residual
+    int fused;
+    const uint16_t *x;
+    uint16_t *residual;
+    int *ws;                 // arrival counter, 0 between calls
+    uint32_t off_s;
 };
 
 // ---------------------------------------------------------------------------
@@ -138,9 +145,11 @@ __device__ __forceinline__ void load_h_to_smem(const GluParams &p, uint16_t *h_s
 // h_s (rows M..rows_out-1 zero); M <= MB.
 template <int MB>
 __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s, float (*red)[MB],
-                                              float *inv_s, int rows_out, int hstride = 0)
+                                              float *inv_s, int rows_out, int hstride = 0,
+                                              const uint16_t *src = nullptr)
 {
     if (hstride == 0) hstride = p.K;
+    const uint16_t *sp = src ? src : p.s;
     const int K = p.K, tid = threadIdx.x, nthr = blockDim.x;
     const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
     float ss[MB];
@@ -152,7 +161,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
 #pragma unroll
             for (int m = 0; m < MB; ++m) {
                 if (m < p.M) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(p.s + static_cast<int64_t>(m) * K + c * 8);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sp + static_cast<int64_t>(m) * K + c * 8);
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -168,7 +177,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
 #pragma unroll
             for (int m = 0; m < MB; ++m) {
                 if (m < p.M) {
-                    const float a = bf16_to_f32(p.s[static_cast<int64_t>(m) * K + k]);
+                    const float a = bf16_to_f32(sp[static_cast<int64_t>(m) * K + k]);
                     ss[m] = fmaf(a, a, ss[m]);
                 }
             }
@@ -193,7 +202,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
             uint4 o = make_uint4(0, 0, 0, 0);
             if (m < p.M) {
                 const float inv = inv_s[m];
-                const uint4 v = *reinterpret_cast<const uint4 *>(p.s + static_cast<int64_t>(m) * K + c * 8);
+                const uint4 v = *reinterpret_cast<const uint4 *>(sp + static_cast<int64_t>(m) * K + c * 8);
                 const uint4 wv = *reinterpret_cast<const uint4 *>(p.norm_w + c * 8);
                 const uint32_t sv[4] = {v.x, v.y, v.z, v.w};
                 const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -213,10 +222,63 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
             const int m = i / K, k = i - m * K;
             uint16_t o = 0;
             if (m < p.M) {
-                const float sv = bf16_to_f32(p.s[static_cast<int64_t>(m) * K + k]);
+                const float sv = bf16_to_f32(sp[static_cast<int64_t>(m) * K + k]);
                 o = f32_to_bf16((sv * inv_s[m]) * (1.0f + bf16_to_f32(p.norm_w[k])));
             }
             h_s[static_cast<int64_t>(m) * hstride + k] = o;
+        }
+    }
+}
+
+// Single-kernel add_rmsnorm_glu, part 1: s = bf16(x + residual) for rows
+// 0..M-1 into s_s[M][K] (contiguous).  The fp32 sum of two bf16 values rounds
+// to the same bf16 as the exact sum.
+__device__ __forceinline__ void fused_add_to_smem(const GluParams &p, uint16_t *s_s)
+{
+    const int64_t count = static_cast<int64_t>(p.M) * p.K;
+    if (p.vec_in) {
+        for (int64_t i = threadIdx.x; i < count / 8; i += blockDim.x) {
+            const uint4 a = reinterpret_cast<const uint4 *>(p.x)[i];
+            const uint4 b = reinterpret_cast<const uint4 *>(p.residual)[i];
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+            uint32_t r[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                r[j] = pack_bf16x2(bf16_lo(aw[j]) + bf16_lo(bw[j]), bf16_hi(aw[j]) + bf16_hi(bw[j]));
+            reinterpret_cast<uint4 *>(s_s)[i] = make_uint4(r[0], r[1], r[2], r[3]);
+        }
+    } else {
+        for (int64_t i = threadIdx.x; i < count; i += blockDim.x)
+            s_s[i] = f32_to_bf16(bf16_to_f32(p.x[i]) + bf16_to_f32(p.residual[i]));
+    }
+}
+
+// Part 2, after the whole CTA has read `residual` (every CTA reads all of it
+// for the row statistic): arrive on the workspace counter; the CTA that
+// arrives last -- when no CTA will read residual any more -- writes s back
+// and returns the counter to 0 for the next call.  The next call on the
+// stream touches the counter only after its dependency wait, i.e. after this
+// grid has completed.  flag: one shared int.
+__device__ __forceinline__ void fused_residual_writeback(const GluParams &p, const uint16_t *s_s, int *flag)
+{
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        *flag = atomicAdd(p.ws, 1) == static_cast<int>(gridDim.x) - 1;
+    }
+    __syncthreads();
+    if (*flag) {
+        const int64_t count = static_cast<int64_t>(p.M) * p.K;
+        if (p.vec_in) {
+            for (int64_t i = threadIdx.x; i < count / 8; i += blockDim.x)
+                reinterpret_cast<uint4 *>(p.residual)[i] = reinterpret_cast<const uint4 *>(s_s)[i];
+        } else {
+            for (int64_t i = threadIdx.x; i < count; i += blockDim.x) p.residual[i] = s_s[i];
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicExch(p.ws, 0);
         }
     }
 }
@@ -356,7 +418,14 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
 
     uint4 hreg[HREG ? kHregChunks : 1];
     if constexpr (NORM) {
-        norm_prologue<MB>(p, h_s, red, inv_s, MB);
+        __shared__ int last_flag;
+        uint16_t *s_s = reinterpret_cast<uint16_t *>(smem + p.off_s);
+        if (p.fused) {
+            fused_add_to_smem(p, s_s);
+            __syncthreads();
+        }
+        norm_prologue<MB>(p, h_s, red, inv_s, MB, 0, p.fused ? s_s : nullptr);
+        if (p.fused) fused_residual_writeback(p, s_s, &last_flag);
         __syncthreads();
     } else if constexpr (!HREG) {
         load_h_to_smem<MB>(p, h_s);
@@ -627,7 +696,14 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
 
     // h rows 0..M-1, then a zero row M (padded stride HS)
     if constexpr (NORM) {
-        norm_prologue<kMaxM>(p, h_s, red, inv_s, p.M, HS);
+        __shared__ int last_flag;
+        uint16_t *s_s = reinterpret_cast<uint16_t *>(smem + p.off_s);
+        if (p.fused) {
+            fused_add_to_smem(p, s_s);
+            __syncthreads();
+        }
+        norm_prologue<kMaxM>(p, h_s, red, inv_s, p.M, HS, p.fused ? s_s : nullptr);
+        if (p.fused) fused_residual_writeback(p, s_s, &last_flag);
     } else {
         const int nch = K >> 3;
         for (int i = threadIdx.x; i < p.M * nch; i += blockDim.x) {

@@ -195,7 +195,7 @@ int default_rows(int MB, int K, bool contiguous)
 struct Plan {
     int MB = 1, R = 1, warps = 4, KS = 0, nseg = 0, stages = 0, grid = 0, ctas_per_sm = 1;
     bool hreg = false;
-    uint32_t off_h = 0, off_ring = 0, smem = 0;
+    uint32_t off_h = 0, off_s = 0, off_ring = 0, smem = 0;
 };
 
 // Streaming-kernel plan.  Whole rows per stage (K-segments only if a stage of
@@ -205,7 +205,7 @@ struct Plan {
 // per stage as default_rows, halved while not even one warp fits.  False if
 // h plus a two-stage ring cannot fit.
 bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool norm, Plan &pl,
-                 bool allow_hreg = true)
+                 bool allow_hreg = true, uint32_t extra = 0)
 {
     const Tuning &t = tuning();
     pl.MB = batch_tile(M);
@@ -219,7 +219,7 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
     const bool need_hs = !pl.hreg || norm;
     const uint32_t hbytes =
         need_hs ? (static_cast<uint32_t>(pl.MB) * static_cast<uint32_t>(K) * 2u + 127u) & ~127u : 0u;
-    const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes;
+    const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes - extra;
     if (room <= 0) return false;
     int ks = t.ks > 0 ? std::min(t.ks, ((K + 7) / 8) * 8) : ((K + 7) / 8) * 8;
     pl.R = t.rows > 0 ? t.rows : default_rows(pl.MB, K, contiguous);
@@ -255,9 +255,10 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
     pl.KS = ks;
     pl.nseg = (K + ks - 1) / ks;
     if (pl.hreg && pl.nseg != 1)   // registers hold whole rows of h only
-        return plan_stream(d, M, N, K, contiguous, norm, pl, false);
+        return plan_stream(d, M, N, K, contiguous, norm, pl, false, extra);
     pl.off_h = kBarRegion;
-    pl.off_ring = kBarRegion + hbytes;
+    pl.off_s = kBarRegion + hbytes;
+    pl.off_ring = kBarRegion + hbytes + extra;
     pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 4u * pl.R * static_cast<uint32_t>(ks);
     pl.grid = std::max(1, std::min(d.sm_count * pl.ctas_per_sm * t.waves, N));
     return true;
@@ -268,7 +269,7 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
 // padded by 16 bytes; h_s holds M rows plus a zero row.  Two stages per warp,
 // as many warps (<= 8) as fit; segments shrink (>= 256) while fewer than 4
 // warps fit.  False if nothing fits.
-bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl)
+bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl, uint32_t extra = 0)
 {
     const Tuning &t = tuning();
     if (M < t.mma_min_m || K % 16 != 0) return false;
@@ -276,7 +277,7 @@ bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl)
     int budget = d.smem_optin - static_reserve;
     if (t.smem_kb > 0) budget = std::min(budget, t.smem_kb * 1024 - static_reserve);
     const uint32_t hbytes = (static_cast<uint32_t>(M + 1) * static_cast<uint32_t>(K + 8) * 2u + 127u) & ~127u;
-    const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes;
+    const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes - extra;
     if (room <= 0) return false;
     int ks = 0;
     if (t.ks > 0) {
@@ -305,7 +306,8 @@ bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl)
     pl.R = mbglu::kMmaRows;
     pl.nseg = (K + pl.KS - 1) / pl.KS;
     pl.off_h = kBarRegion;
-    pl.off_ring = kBarRegion + hbytes;
+    pl.off_s = kBarRegion + hbytes;
+    pl.off_ring = kBarRegion + hbytes + extra;
     pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 2u * mbglu::kMmaRows *
                                 static_cast<uint32_t>(pl.KS + 8) * 2u;
     pl.grid = std::max(1, std::min(d.sm_count, N));
@@ -472,9 +474,17 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
     return st;
 }
 
-mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
-                             const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w, mbglu_bf16 *out, int M, int N, int K,
-                             mbglu_mode mode, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+// Both add_rmsnorm_glu entry points.  ws == nullptr: residual-add kernel, then
+// the GEMV with the norm prologue.  ws != nullptr: one kernel (the add is
+// formed in shared memory, residual written back by the last CTA), where the
+// fast kernels apply; otherwise the two-kernel path.
+mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
+                                  const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w, mbglu_bf16 *out, int M, int N,
+                                  int K, mbglu_mode mode, int *ws, cudaStream_t stream)
 {
     t_last_variant = kNone;
     if (mode != MBGLU_MODE_FUSED && mode != MBGLU_MODE_HF) return MBGLU_ERR_MODE;
@@ -493,12 +503,69 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mb
     if (N > 0 && (overlaps(out, ob, x, xb) || overlaps(out, ob, residual, xb) || overlaps(out, ob, norm_w, nb) ||
                   overlaps(out, ob, gate_w, wb) || overlaps(out, ob, up_w, wb)))
         return MBGLU_ERR_ALIAS;
+    if (ws) {
+        const int64_t wsb = MBGLU_WORKSPACE_BYTES;
+        if (overlaps(ws, wsb, x, xb) || overlaps(ws, wsb, residual, xb) || overlaps(ws, wsb, norm_w, nb) ||
+            (N > 0 && (overlaps(ws, wsb, gate_w, wb) || overlaps(ws, wsb, up_w, wb) || overlaps(ws, wsb, out, ob))))
+            return MBGLU_ERR_ALIAS;
+    }
 
     const DeviceInfo *d = nullptr;
     mbglu_status st = device_info(&d);
     if (st != MBGLU_OK) return st;
     const int policy = g_policy.load(std::memory_order_relaxed);
     const bool pdl = policy != MBGLU_POLICY_SERIAL;
+
+    GluParams p = base_params(M, N, K, static_cast<int>(mode));
+    p.gate = gate_w;
+    p.ld_gate = K;
+    p.up = up_w;
+    p.ld_up = K;
+    p.out = out;
+    p.ldo = N;
+    p.s = residual;
+    p.norm_w = norm_w;
+    p.eps = eps;
+    p.vec_in = (K % 8 == 0) && aligned(residual, 16) && aligned(norm_w, 16);
+    p.prefetch = policy == MBGLU_POLICY_PREFETCH;
+    p.interleave = tuning().interleave;
+    const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && p.vec_in;
+
+    // single kernel: needs the fast kernels, 16-byte aligned x, and N > 0
+    if (ws && N > 0 && bulk_ok && aligned(x, 16)) {
+        const uint32_t sbytes = (static_cast<uint32_t>(M) * static_cast<uint32_t>(K) * 2u + 127u) & ~127u;
+        Plan pl;
+        p.fused = 1;
+        p.x = x;
+        p.residual = residual;
+        p.ws = ws;
+        if (plan_mma(*d, M, N, K, pl, sbytes)) {
+            p.KS = pl.KS;
+            p.nseg = pl.nseg;
+            p.stages = pl.stages;
+            p.off_h = pl.off_h;
+            p.off_s = pl.off_s;
+            p.off_ring = pl.off_ring;
+            st = launch(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
+            if (st == MBGLU_OK) t_last_variant = kTensor;
+            return st;
+        }
+        if (plan_stream(*d, M, N, K, true, true, pl, true, sbytes)) {
+            p.KS = pl.KS;
+            p.nseg = pl.nseg;
+            p.stages = pl.stages;
+            p.off_h = pl.off_h;
+            p.off_s = pl.off_s;
+            p.off_ring = pl.off_ring;
+            st = launch_stream<true>(pl, p, stream, pdl);
+            if (st == MBGLU_OK) t_last_variant = kStream;
+            return st;
+        }
+        p.fused = 0;
+        p.x = nullptr;
+        p.residual = nullptr;
+        p.ws = nullptr;
+    }
 
     // 1) residual <- bf16(x + residual); it waits for its predecessor before
     //    reading and releases the GEMV launch at once.
@@ -526,28 +593,14 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mb
     }
 
     // 2) the GEMV with the norm prologue, as a programmatic dependent launch
-    GluParams p = base_params(M, N, K, static_cast<int>(mode));
-    p.gate = gate_w;
-    p.ld_gate = K;
-    p.up = up_w;
-    p.ld_up = K;
-    p.out = out;
-    p.ldo = N;
-    p.s = residual;
-    p.norm_w = norm_w;
-    p.eps = eps;
-    p.vec_in = (K % 8 == 0) && aligned(residual, 16) && aligned(norm_w, 16);
-    p.prefetch = policy == MBGLU_POLICY_PREFETCH;
-
     Plan pl;
-    const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && p.vec_in;
     if (bulk_ok && plan_mma(*d, M, N, K, pl)) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;
         p.stages = pl.stages;
         p.off_h = pl.off_h;
+        p.off_s = pl.off_s;
         p.off_ring = pl.off_ring;
-        p.interleave = tuning().interleave;
         st = launch(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
         if (st == MBGLU_OK) t_last_variant = kTensor;
         return st;
@@ -558,16 +611,41 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mb
         p.nseg = pl.nseg;
         p.stages = pl.stages;
         p.off_h = pl.off_h;
+        p.off_s = pl.off_s;
         p.off_ring = pl.off_ring;
-        p.interleave = tuning().interleave;
         st = launch_stream<true>(pl, p, stream, pdl);
         if (st == MBGLU_OK) t_last_variant = kStream;
         return st;
     }
+    p.vec_in = 0;
     const uint32_t smem = static_cast<uint32_t>(M) * static_cast<uint32_t>(K) * 2u;
     st = launch(mbglu::glu_generic_kernel<true>, dim3(generic_grid(*d, N)), dim3(256), smem, stream, pdl, p);
     if (st == MBGLU_OK) t_last_variant = kGeneric;
     return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
+                             const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w, mbglu_bf16 *out, int M, int N, int K,
+                             mbglu_mode mode, cudaStream_t stream)
+{
+    return add_rmsnorm_glu_impl(x, residual, norm_w, eps, gate_w, up_w, out, M, N, K, mode, nullptr, stream);
+}
+
+mbglu_status add_rmsnorm_glu_ws(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
+                                const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w, mbglu_bf16 *out, int M, int N,
+                                int K, mbglu_mode mode, void *workspace, size_t workspace_bytes,
+                                cudaStream_t stream)
+{
+    t_last_variant = kNone;
+    if (!workspace) return MBGLU_ERR_NULL;
+    if (workspace_bytes < MBGLU_WORKSPACE_BYTES) return MBGLU_ERR_SHAPE;
+    if (!aligned(workspace, 16)) return MBGLU_ERR_ALIGN;
+    return add_rmsnorm_glu_impl(x, residual, norm_w, eps, gate_w, up_w, out, M, N, K, mode,
+                                static_cast<int *>(workspace), stream);
 }
 
 mbglu_status mbglu_read_device_error(int *word)

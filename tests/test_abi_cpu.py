@@ -110,3 +110,22 @@ def test_launch_policy_roundtrip_and_validation():
         assert lib.mbglu_get_launch_policy() == mb.POLICY_PREFETCH
     finally:
         lib.mbglu_set_launch_policy(old)
+
+
+WS = 0x7F0000000000 + 9 * (1 << 32)
+
+
+def norm_ws(ws=WS, nbytes=256, **kw):
+    a = dict(x=X, r=R, w=W, g=G, u=U, o=O, M=2, N=32, K=64, mode=1)
+    a.update(kw)
+    return mb.lib().add_rmsnorm_glu_ws(a["x"], a["r"], a["w"], 1e-6, a["g"], a["u"], a["o"], a["M"], a["N"], a["K"],
+                                       a["mode"], ws, nbytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), NULL), (dict(nbytes=255), SHAPE), (dict(ws=WS + 8), ALIGN),
+    (dict(ws=X), ALIAS), (dict(ws=O + 64), ALIAS), (dict(ws=G + 1024), ALIAS),
+    (dict(M=17), SHAPE), (dict(mode=2), MODE), (dict(x=0), NULL), (dict(M=0), OK),
+])
+def test_add_rmsnorm_glu_ws_validation(kw, code):
+    assert norm_ws(**kw) == code

@@ -348,10 +348,12 @@ def test_cuda_graph_replay_matches_eager():
 # add_rmsnorm_glu
 # ---------------------------------------------------------------------------
 
-def check_norm(x, r, w, g, u, mode, eps=1e-6, what="", variant=None):
+def check_norm(x, r, w, g, u, mode, eps=1e-6, what="", variant=None, ws=None):
     rd = r.to(DEV)
-    out = mb.add_rmsnorm_glu(x.to(DEV), rd, w.to(DEV), eps, g.to(DEV), u.to(DEV), mode=mode)
+    out = mb.add_rmsnorm_glu(x.to(DEV), rd, w.to(DEV), eps, g.to(DEV), u.to(DEV), mode=mode, workspace=ws)
     torch.cuda.synchronize()
+    if ws is not None:
+        assert int(ws.sum()) == 0, "workspace not returned to zero"
     if variant == 1:
         assert mb.last_variant() in FAST
     elif variant is not None:
@@ -374,6 +376,84 @@ def test_add_rmsnorm_glu_small(M):
     u = gi.normal_bf16((N, K), K ** -0.5, M, "an-u")
     for mode in ("hf", "fused"):
         check_norm(x, r, w, g, u, mode, what=f"M={M} {mode}", variant=1)
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 8, 13, 16])
+@pytest.mark.parametrize("mode", ["hf", "fused"])
+def test_add_rmsnorm_glu_single_kernel(M, mode):
+    """The workspace entry point: one kernel, residual written back by the
+    last CTA, the workspace left at zero."""
+    N, K = 1500, 2048
+    x = gi.normal_bf16((M, K), 1.0, M, "ws-x")
+    r = gi.normal_bf16((M, K), 1.0, M, "ws-r")
+    w = gi.normal_bf16((K,), 0.1, M, "ws-w")
+    g = gi.normal_bf16((N, K), K ** -0.5, M, "ws-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, M, "ws-u")
+    ws = mb.new_workspace(DEV)
+    check_norm(x, r, w, g, u, mode, what=f"ws M={M} {mode}", variant=1, ws=ws)
+
+
+def test_add_rmsnorm_glu_single_kernel_back_to_back_and_graph():
+    """Consecutive calls on one stream share a workspace (also replayed in a
+    CUDA graph), each reading the residual the previous one wrote."""
+    M, N, K = 4, 2000, 2560
+    x = [gi.normal_bf16((M, K), 1.0, i, "bb-x").to(DEV) for i in range(3)]
+    r0 = gi.normal_bf16((M, K), 1.0, 0, "bb-r").to(DEV)
+    w = gi.normal_bf16((K,), 0.1, 0, "bb-w").to(DEV)
+    gs = [gi.normal_bf16((N, K), K ** -0.5, i, "bb-g").to(DEV) for i in range(3)]
+    us = [gi.normal_bf16((N, K), K ** -0.5, i, "bb-u").to(DEV) for i in range(3)]
+    ws = mb.new_workspace(DEV)
+
+    def chain(res, use_ws):
+        return [mb.add_rmsnorm_glu(x[i], res, w, 1e-6, gs[i], us[i], mode="hf", workspace=ws if use_ws else None)
+                for i in range(3)]
+
+    r_ref = r0.clone()
+    ref = chain(r_ref, False)
+    r_ws = r0.clone()
+    got = chain(r_ws, True)
+    torch.cuda.synchronize()
+    assert int(ws.sum()) == 0
+    assert torch.equal(r_ws.view(torch.int16), r_ref.view(torch.int16))
+    for a, b in zip(ref, got):
+        d = tol.ulp_distance(gi.bits(a.cpu()), gi.bits(b.cpu()))
+        assert np.mean(d == 0) > 0.999 and d.max() <= 4
+    # the same chain captured once and replayed twice
+    r_g = r0.clone()
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=DEV) for _ in range(3)]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for i in range(3):
+                mb.add_rmsnorm_glu(x[i], r_g, w, 1e-6, gs[i], us[i], out=outs[i], mode="hf", workspace=ws)
+    for _ in range(2):
+        r_g.copy_(r0)
+        graph.replay()
+    torch.cuda.synchronize()
+    assert int(ws.sum()) == 0
+    assert torch.equal(r_g.view(torch.int16), r_ref.view(torch.int16))
+    for a, b in zip(got, outs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_add_rmsnorm_glu_single_kernel_falls_back():
+    """K % 8 != 0: the two-kernel path runs and the workspace is not touched."""
+    M, N, K = 2, 300, 1004
+    x = gi.normal_bf16((M, K), 1.0, 5, "fb-x")
+    r = gi.normal_bf16((M, K), 1.0, 5, "fb-r")
+    w = gi.normal_bf16((K,), 0.1, 5, "fb-w")
+    g = gi.normal_bf16((N, K), K ** -0.5, 5, "fb-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, 5, "fb-u")
+    ws = mb.new_workspace(DEV)
+    ws[17] = 5                     # a marker the fallback must leave alone
+    rd = r.to(DEV)
+    out = mb.add_rmsnorm_glu(x.to(DEV), rd, w.to(DEV), 1e-6, g.to(DEV), u.to(DEV), mode="hf", workspace=ws)
+    torch.cuda.synchronize()
+    assert mb.last_variant() == 2 and int(ws[17]) == 5 and int(ws.sum()) == 5
+    ref, res, _ = oracle.add_rmsnorm_glu(gi.bits(x), gi.bits(r), gi.bits(w), 1e-6, gi.bits(g), gi.bits(u), "hf")
+    assert np.array_equal(gi.bits(rd.cpu()), res)
 
 
 def test_add_rmsnorm_glu_generic_and_edge_cases():
@@ -425,6 +505,8 @@ def test_full_size_workload(name, M, mode):
     else:
         x, r, nw = gi.norm_inputs(w, M)
         st = check_norm(x, r, nw, g, u, mode, eps=w.eps, what=f"{name} M={M}", variant=1)
+        check_norm(x, r, nw, g, u, mode, eps=w.eps, what=f"{name} M={M} single kernel", variant=1,
+                   ws=mb.new_workspace(DEV))
     assert st["exact_frac"] > 0.9
 
 
