@@ -143,12 +143,15 @@ __device__ __forceinline__ void load_h_to_smem(const GluParams &p, uint16_t *h_s
 // Every CTA runs the same code on the same data, so every CTA gets the same h.
 // red: [kMaxWarps][MB] shared floats; inv_s: [MB].  Writes rows_out rows of
 // h_s (rows M..rows_out-1 zero); M <= MB.
+// src: the s rows (row stride sstride; default: residual in global memory);
+// may be h_s itself (each chunk is read before the same thread overwrites it).
 template <int MB>
 __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s, float (*red)[MB],
                                               float *inv_s, int rows_out, int hstride = 0,
-                                              const uint16_t *src = nullptr)
+                                              const uint16_t *src = nullptr, int sstride = 0)
 {
     if (hstride == 0) hstride = p.K;
+    if (sstride == 0) sstride = p.K;
     const uint16_t *sp = src ? src : p.s;
     const int K = p.K, tid = threadIdx.x, nthr = blockDim.x;
     const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
@@ -161,7 +164,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
 #pragma unroll
             for (int m = 0; m < MB; ++m) {
                 if (m < p.M) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(sp + static_cast<int64_t>(m) * K + c * 8);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sp + static_cast<int64_t>(m) * sstride + c * 8);
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -177,7 +180,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
 #pragma unroll
             for (int m = 0; m < MB; ++m) {
                 if (m < p.M) {
-                    const float a = bf16_to_f32(sp[static_cast<int64_t>(m) * K + k]);
+                    const float a = bf16_to_f32(sp[static_cast<int64_t>(m) * sstride + k]);
                     ss[m] = fmaf(a, a, ss[m]);
                 }
             }
@@ -202,7 +205,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
             uint4 o = make_uint4(0, 0, 0, 0);
             if (m < p.M) {
                 const float inv = inv_s[m];
-                const uint4 v = *reinterpret_cast<const uint4 *>(sp + static_cast<int64_t>(m) * K + c * 8);
+                const uint4 v = *reinterpret_cast<const uint4 *>(sp + static_cast<int64_t>(m) * sstride + c * 8);
                 const uint4 wv = *reinterpret_cast<const uint4 *>(p.norm_w + c * 8);
                 const uint32_t sv[4] = {v.x, v.y, v.z, v.w};
                 const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
@@ -222,7 +225,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
             const int m = i / K, k = i - m * K;
             uint16_t o = 0;
             if (m < p.M) {
-                const float sv = bf16_to_f32(sp[static_cast<int64_t>(m) * K + k]);
+                const float sv = bf16_to_f32(sp[static_cast<int64_t>(m) * sstride + k]);
                 o = f32_to_bf16((sv * inv_s[m]) * (1.0f + bf16_to_f32(p.norm_w[k])));
             }
             h_s[static_cast<int64_t>(m) * hstride + k] = o;
@@ -230,26 +233,50 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
     }
 }
 
-// Single-kernel add_rmsnorm_glu, part 1: s = bf16(x + residual) for rows
-// 0..M-1 into s_s[M][K] (contiguous).  The fp32 sum of two bf16 values rounds
-// to the same bf16 as the exact sum.
-__device__ __forceinline__ void fused_add_to_smem(const GluParams &p, uint16_t *s_s)
+// Prologue operands (h; residual; x) arrive by bulk copies on their own
+// mbarrier (kProBarOffset), issued by thread 0 after the dependency wait:
+// one copy when the rows are contiguous on both sides, else one per row.
+constexpr uint32_t kProBarOffset = 784;
+
+__device__ __forceinline__ void copy_rows_async(uint16_t *dst, int dstride, const uint16_t *src, int64_t ld,
+                                                int rows, int K, uint64_t *bar)
 {
-    const int64_t count = static_cast<int64_t>(p.M) * p.K;
-    if (p.vec_in) {
-        for (int64_t i = threadIdx.x; i < count / 8; i += blockDim.x) {
-            const uint4 a = reinterpret_cast<const uint4 *>(p.x)[i];
-            const uint4 b = reinterpret_cast<const uint4 *>(p.residual)[i];
-            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-            uint32_t r[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                r[j] = pack_bf16x2(bf16_lo(aw[j]) + bf16_lo(bw[j]), bf16_hi(aw[j]) + bf16_hi(bw[j]));
-            reinterpret_cast<uint4 *>(s_s)[i] = make_uint4(r[0], r[1], r[2], r[3]);
-        }
+    if (ld == K && dstride == K) {
+        bulk_g2s_plain(dst, src, static_cast<uint32_t>(rows) * static_cast<uint32_t>(K) * 2u, bar);
     } else {
-        for (int64_t i = threadIdx.x; i < count; i += blockDim.x)
-            s_s[i] = f32_to_bf16(bf16_to_f32(p.x[i]) + bf16_to_f32(p.residual[i]));
+        for (int r = 0; r < rows; ++r)
+            bulk_g2s_plain(dst + static_cast<int64_t>(r) * dstride, src + r * ld, static_cast<uint32_t>(K) * 2u, bar);
+    }
+}
+
+// All threads: bounded wait for the prologue copies (phase 0).  A timeout is
+// recorded; the kernel then waits once more (bounded) so that no copy is
+// still writing shared memory when it goes on.
+__device__ __forceinline__ void prologue_wait(uint64_t *bar)
+{
+    if (!mbar_wait_bounded(bar, 0u, kWaitLimitNs)) {
+        atomicExch(&g_device_error, kErrTimeout);
+        mbar_wait_bounded(bar, 0u, kWaitLimitNs);
+    }
+}
+
+// Single-kernel add_rmsnorm_glu, part 1: with x in s_s[M][K] and residual in
+// r_s (row stride rstride), s = bf16(x + residual) in place in s_s.  The fp32
+// sum of two bf16 values rounds to the same bf16 as the exact sum.
+__device__ __forceinline__ void fused_add_smem(const GluParams &p, uint16_t *s_s, const uint16_t *r_s, int rstride)
+{
+    const int nch = p.K >> 3;
+    for (int i = threadIdx.x; i < p.M * nch; i += blockDim.x) {
+        const int m = i / nch, c = i - m * nch;
+        uint4 *sp = reinterpret_cast<uint4 *>(s_s + static_cast<int64_t>(m) * p.K + c * 8);
+        const uint4 a = *sp;
+        const uint4 b = *reinterpret_cast<const uint4 *>(r_s + static_cast<int64_t>(m) * rstride + c * 8);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+        uint32_t r[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            r[j] = pack_bf16x2(bf16_lo(aw[j]) + bf16_lo(bw[j]), bf16_hi(aw[j]) + bf16_hi(bw[j]));
+        *sp = make_uint4(r[0], r[1], r[2], r[3]);
     }
 }
 
@@ -357,9 +384,13 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
     };
     const bool contig = (p.ld_gate == K) && (p.ld_up == K) && (KS == K);
 
+    uint64_t *pro_bar = reinterpret_cast<uint64_t *>(smem + kProBarOffset);
     if (lane == 0)
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-    if (threadIdx.x == 0) *counter = 0;
+    if (threadIdx.x == 0) {
+        *counter = 0;
+        mbar_init(pro_bar, 1);
+    }
     fence_mbar_init();
     __syncthreads();
 
@@ -418,17 +449,35 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
 
     uint4 hreg[HREG ? kHregChunks : 1];
     if constexpr (NORM) {
+        // the norm path always has 16-byte aligned operands (the host checks)
         __shared__ int last_flag;
         uint16_t *s_s = reinterpret_cast<uint16_t *>(smem + p.off_s);
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u;
+            mbar_arrive_expect_tx(pro_bar, p.fused ? 2u * bytes : bytes);
+            if (p.fused) bulk_g2s_plain(s_s, p.x, bytes, pro_bar);
+            bulk_g2s_plain(h_s, p.s, bytes, pro_bar);   // residual rows into h_s rows 0..M-1
+        }
+        prologue_wait(pro_bar);
         if (p.fused) {
-            fused_add_to_smem(p, s_s);
+            fused_add_smem(p, s_s, h_s, K);
             __syncthreads();
         }
-        norm_prologue<MB>(p, h_s, red, inv_s, MB, 0, p.fused ? s_s : nullptr);
+        norm_prologue<MB>(p, h_s, red, inv_s, MB, K, p.fused ? s_s : h_s, K);
         if (p.fused) fused_residual_writeback(p, s_s, &last_flag);
         __syncthreads();
     } else if constexpr (!HREG) {
-        load_h_to_smem<MB>(p, h_s);
+        if (p.vec_in) {
+            if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u);
+                copy_rows_async(h_s, K, p.h, p.ldh, p.M, K, pro_bar);
+            }
+            for (int i = threadIdx.x; i < (MB - p.M) * (K >> 3); i += blockDim.x)
+                reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(p.M) * K)[i] = make_uint4(0, 0, 0, 0);
+            prologue_wait(pro_bar);
+        } else {
+            load_h_to_smem<MB>(p, h_s);
+        }
         __syncthreads();
     }
     if constexpr (HREG) {
@@ -645,9 +694,13 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
         return p.interleave ? (g * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x)) * R : r0 + g * R;
     };
 
+    uint64_t *pro_bar = reinterpret_cast<uint64_t *>(smem + kProBarOffset);
     if (lane == 0)
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-    if (threadIdx.x == 0) *counter = 0;
+    if (threadIdx.x == 0) {
+        *counter = 0;
+        mbar_init(pro_bar, 1);
+    }
     fence_mbar_init();
     __syncthreads();
 
@@ -698,12 +751,25 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
     if constexpr (NORM) {
         __shared__ int last_flag;
         uint16_t *s_s = reinterpret_cast<uint16_t *>(smem + p.off_s);
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u;
+            mbar_arrive_expect_tx(pro_bar, p.fused ? 2u * bytes : bytes);
+            if (p.fused) bulk_g2s_plain(s_s, p.x, bytes, pro_bar);
+            copy_rows_async(h_s, HS, p.s, K, p.M, K, pro_bar);   // residual rows, padded
+        }
+        prologue_wait(pro_bar);
         if (p.fused) {
-            fused_add_to_smem(p, s_s);
+            fused_add_smem(p, s_s, h_s, HS);
             __syncthreads();
         }
-        norm_prologue<kMaxM>(p, h_s, red, inv_s, p.M, HS, p.fused ? s_s : nullptr);
+        norm_prologue<kMaxM>(p, h_s, red, inv_s, p.M, HS, p.fused ? s_s : h_s, p.fused ? K : HS);
         if (p.fused) fused_residual_writeback(p, s_s, &last_flag);
+    } else if (p.vec_in) {
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u);
+            copy_rows_async(h_s, HS, p.h, p.ldh, p.M, K, pro_bar);
+        }
+        prologue_wait(pro_bar);
     } else {
         const int nch = K >> 3;
         for (int i = threadIdx.x; i < p.M * nch; i += blockDim.x) {

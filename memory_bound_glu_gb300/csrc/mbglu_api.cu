@@ -31,7 +31,8 @@ constexpr uint32_t kBarRegion = 1024;        // mbarriers, stage -> group table,
 static_assert(mbglu::kMaxStreamWarps * 8 * 8 <= mbglu::kSlotGrpOffset, "mbarriers overflow their region");
 static_assert(mbglu::kSlotGrpOffset + mbglu::kMaxStreamWarps * 8 * 4 <= mbglu::kCounterOffset,
               "stage table overflows its region");
-static_assert(mbglu::kCounterOffset + 4 <= kBarRegion, "counter outside the region");
+static_assert(mbglu::kCounterOffset + 4 <= mbglu::kProBarOffset, "counter overlaps the prologue barrier");
+static_assert(mbglu::kProBarOffset % 8 == 0 && mbglu::kProBarOffset + 8 <= kBarRegion, "prologue barrier outside the region");
 constexpr int kMaxStages = 8;
 constexpr int64_t kNormMaxMK = 81920;        // add_rmsnorm_glu: M*K*2 bytes of normed rows in smem
 

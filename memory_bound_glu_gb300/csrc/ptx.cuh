@@ -79,6 +79,15 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Bulk copy without an L2 hint (small operands that every CTA reads).
+__device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
 // Orders this thread's earlier generic-proxy shared-memory accesses before
 // later asynchronous-proxy accesses (a bulk copy refilling a consumed stage).
 __device__ __forceinline__ void fence_proxy_async_smem()
