@@ -260,53 +260,77 @@ __device__ __forceinline__ void prologue_wait(uint64_t *bar)
     }
 }
 
-// Single-kernel add_rmsnorm_glu, part 1: with x in s_s[M][K] and residual in
-// r_s (row stride rstride), s = bf16(x + residual) in place in s_s.  The fp32
-// sum of two bf16 values rounds to the same bf16 as the exact sum.
-__device__ __forceinline__ void fused_add_smem(const GluParams &p, uint16_t *s_s, const uint16_t *r_s, int rstride)
+// Single-kernel add_rmsnorm_glu, part 1.  The residual rows have been
+// copied into h_s (row stride hstride); s = bf16(x + residual) is formed there
+// in place, x read straight from global memory (the first kXPre chunks per
+// thread are loaded before the copy is awaited).  The fp32 sum of two bf16
+// values rounds to the same bf16 as the exact sum.
+constexpr int kXPre = 4;
+
+struct XPrefetch {
+    uint4 v[kXPre];
+};
+
+__device__ __forceinline__ void fused_x_prefetch(const GluParams &p, XPrefetch &xp)
 {
-    const int nch = p.K >> 3;
-    for (int i = threadIdx.x; i < p.M * nch; i += blockDim.x) {
-        const int m = i / nch, c = i - m * nch;
-        uint4 *sp = reinterpret_cast<uint4 *>(s_s + static_cast<int64_t>(m) * p.K + c * 8);
-        const uint4 a = *sp;
-        const uint4 b = *reinterpret_cast<const uint4 *>(r_s + static_cast<int64_t>(m) * rstride + c * 8);
-        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-        uint32_t r[4];
+    const int n = p.M * (p.K >> 3);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            r[j] = pack_bf16x2(bf16_lo(aw[j]) + bf16_lo(bw[j]), bf16_hi(aw[j]) + bf16_hi(bw[j]));
-        *sp = make_uint4(r[0], r[1], r[2], r[3]);
+    for (int j = 0; j < kXPre; ++j) {
+        const int i = threadIdx.x + j * blockDim.x;
+        xp.v[j] = i < n ? reinterpret_cast<const uint4 *>(p.x)[i] : make_uint4(0, 0, 0, 0);
     }
 }
 
-// Part 2, after the whole CTA has read `residual` (every CTA reads all of it
-// for the row statistic): arrive on the workspace counter; the CTA that
-// arrives last -- when no CTA will read residual any more -- writes s back
-// and returns the counter to 0 for the next call.  The next call on the
-// stream touches the counter only after its dependency wait, i.e. after this
-// grid has completed.  flag: one shared int.
-__device__ __forceinline__ void fused_residual_writeback(const GluParams &p, const uint16_t *s_s, int *flag)
+__device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b)
 {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        *flag = atomicAdd(p.ws, 1) == static_cast<int>(gridDim.x) - 1;
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+    uint32_t r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r[j] = pack_bf16x2(bf16_lo(aw[j]) + bf16_lo(bw[j]), bf16_hi(aw[j]) + bf16_hi(bw[j]));
+    return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
+__device__ __forceinline__ void fused_add_in_place(const GluParams &p, uint16_t *h_s, int hstride,
+                                                   const XPrefetch &xp)
+{
+    const int nch = p.K >> 3, n = p.M * nch;
+#pragma unroll
+    for (int j = 0; j < kXPre; ++j) {
+        const int i = threadIdx.x + j * blockDim.x;
+        if (i < n) {
+            const int m = i / nch, c = i - m * nch;
+            uint4 *hp = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * hstride + c * 8);
+            *hp = add_bf16x8(xp.v[j], *hp);
+        }
     }
-    __syncthreads();
-    if (*flag) {
-        const int64_t count = static_cast<int64_t>(p.M) * p.K;
-        if (p.vec_in) {
-            for (int64_t i = threadIdx.x; i < count / 8; i += blockDim.x)
-                reinterpret_cast<uint4 *>(p.residual)[i] = reinterpret_cast<const uint4 *>(s_s)[i];
-        } else {
-            for (int64_t i = threadIdx.x; i < count; i += blockDim.x) p.residual[i] = s_s[i];
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            atomicExch(p.ws, 0);
-        }
+    for (int i = threadIdx.x + kXPre * blockDim.x; i < n; i += blockDim.x) {
+        const int m = i / nch, c = i - m * nch;
+        uint4 *hp = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * hstride + c * 8);
+        *hp = add_bf16x8(reinterpret_cast<const uint4 *>(p.x)[i], *hp);
+    }
+}
+
+// Part 2.  Thread 0 arrives on the workspace counter once its CTA holds the
+// residual rows (the bulk copy has landed: this CTA reads residual no more);
+// the result is looked at only when warp 0 has finished streaming.  The CTA
+// that arrived last -- no CTA reads residual any more -- then writes
+// residual = bf16(x + residual) from global memory and returns the counter to
+// 0.  The next call on the stream touches the counter only after its
+// dependency wait, i.e. after this grid has completed.
+__device__ __forceinline__ void fused_residual_writeback_at_end(const GluParams &p, int arrive_old)
+{
+    const bool last = __shfl_sync(0xffffffffu, arrive_old, 0) == static_cast<int>(gridDim.x) - 1;
+    if (!last) return;
+    const int n = p.M * (p.K >> 3);
+    const int lane = threadIdx.x & 31;
+    for (int i = lane; i < n; i += 32) {
+        uint4 *rp = reinterpret_cast<uint4 *>(p.residual) + i;
+        *rp = add_bf16x8(reinterpret_cast<const uint4 *>(p.x)[i], *rp);
+    }
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence();
+        atomicExch(p.ws, 0);
     }
 }
 
@@ -448,23 +472,23 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
     __syncwarp();
 
     uint4 hreg[HREG ? kHregChunks : 1];
+    int arrive_old = -1;   // thread 0, single-kernel path: position on the workspace counter
     if constexpr (NORM) {
         // the norm path always has 16-byte aligned operands (the host checks)
-        __shared__ int last_flag;
-        uint16_t *s_s = reinterpret_cast<uint16_t *>(smem + p.off_s);
         if (threadIdx.x == 0) {
             const uint32_t bytes = static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u;
-            mbar_arrive_expect_tx(pro_bar, p.fused ? 2u * bytes : bytes);
-            if (p.fused) bulk_g2s_plain(s_s, p.x, bytes, pro_bar);
+            mbar_arrive_expect_tx(pro_bar, bytes);
             bulk_g2s_plain(h_s, p.s, bytes, pro_bar);   // residual rows into h_s rows 0..M-1
         }
+        XPrefetch xp;
+        if (p.fused) fused_x_prefetch(p, xp);
         prologue_wait(pro_bar);
         if (p.fused) {
-            fused_add_smem(p, s_s, h_s, K);
+            if (threadIdx.x == 0) arrive_old = atomicAdd(p.ws, 1);
+            fused_add_in_place(p, h_s, K, xp);
             __syncthreads();
         }
-        norm_prologue<MB>(p, h_s, red, inv_s, MB, K, p.fused ? s_s : h_s, K);
-        if (p.fused) fused_residual_writeback(p, s_s, &last_flag);
+        norm_prologue<MB>(p, h_s, red, inv_s, MB, K, h_s, K);
         __syncthreads();
     } else if constexpr (!HREG) {
         if (p.vec_in) {
@@ -614,6 +638,8 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
                 p.out[m * p.ldo + row0 + r] = glu_epilogue(gsel, usel, p.mode);
         }
     }
+    if constexpr (NORM)
+        if (p.fused && warp == 0) fused_residual_writeback_at_end(p, arrive_old);
 }
 
 // ---------------------------------------------------------------------------
@@ -748,22 +774,21 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
     __syncwarp();
 
     // h rows 0..M-1, then a zero row M (padded stride HS)
+    int arrive_old = -1;   // thread 0, single-kernel path: position on the workspace counter
     if constexpr (NORM) {
-        __shared__ int last_flag;
-        uint16_t *s_s = reinterpret_cast<uint16_t *>(smem + p.off_s);
         if (threadIdx.x == 0) {
-            const uint32_t bytes = static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u;
-            mbar_arrive_expect_tx(pro_bar, p.fused ? 2u * bytes : bytes);
-            if (p.fused) bulk_g2s_plain(s_s, p.x, bytes, pro_bar);
+            mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u);
             copy_rows_async(h_s, HS, p.s, K, p.M, K, pro_bar);   // residual rows, padded
         }
+        XPrefetch xp;
+        if (p.fused) fused_x_prefetch(p, xp);
         prologue_wait(pro_bar);
         if (p.fused) {
-            fused_add_smem(p, s_s, h_s, HS);
+            if (threadIdx.x == 0) arrive_old = atomicAdd(p.ws, 1);
+            fused_add_in_place(p, h_s, HS, xp);
             __syncthreads();
         }
-        norm_prologue<kMaxM>(p, h_s, red, inv_s, p.M, HS, p.fused ? s_s : h_s, p.fused ? K : HS);
-        if (p.fused) fused_residual_writeback(p, s_s, &last_flag);
+        norm_prologue<kMaxM>(p, h_s, red, inv_s, p.M, HS, h_s, HS);
     } else if (p.vec_in) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u);
@@ -848,6 +873,8 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
             }
         }
     }
+    if constexpr (NORM)
+        if (p.fused && warp == 0) fused_residual_writeback_at_end(p, arrive_old);
 }
 
 // ---------------------------------------------------------------------------

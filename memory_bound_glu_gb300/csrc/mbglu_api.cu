@@ -534,7 +534,7 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
 
     // single kernel: needs the fast kernels, 16-byte aligned x, and N > 0
     if (ws && N > 0 && bulk_ok && aligned(x, 16)) {
-        const uint32_t sbytes = (static_cast<uint32_t>(M) * static_cast<uint32_t>(K) * 2u + 127u) & ~127u;
+        const uint32_t sbytes = 0;   // s is formed in place where the residual rows land
         Plan pl;
         p.fused = 1;
         p.x = x;
