@@ -140,11 +140,12 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual,
 
 /*
  * add_rmsnorm_glu_ws -- the same operation and arguments as add_rmsnorm_glu,
- * as ONE kernel: every CTA forms s = bf16(x + residual) in shared memory, and
- * the CTA that arrives last on an arrival counter in `workspace` -- when no CTA
- * reads residual any more -- writes s back to residual and returns the counter
- * to zero.  Saves the residual-add launch and its dependency on the critical
- * path.
+ * as ONE kernel: every CTA forms s = bf16(x + residual) in shared memory for
+ * the row statistic and arrives on a counter in `workspace` once it holds the
+ * residual rows; at its end each CTA, after all have arrived (no CTA reads
+ * residual any more), writes its slice of s to residual; the last one returns
+ * the counters to zero.  Saves the residual-add launch and its dependency on
+ * the critical path.
  *   workspace        device memory of at least MBGLU_WORKSPACE_BYTES,
  *                    16-byte aligned, owned by the caller, ALL ZERO before its
  *                    first use (cudaMemset once); every completed call leaves

@@ -310,27 +310,60 @@ __device__ __forceinline__ void fused_add_in_place(const GluParams &p, uint16_t 
     }
 }
 
-// Part 2.  Thread 0 arrives on the workspace counter once its CTA holds the
-// residual rows (the bulk copy has landed: this CTA reads residual no more);
-// the result is looked at only when warp 0 has finished streaming.  The CTA
-// that arrived last -- no CTA reads residual any more -- then writes
-// residual = bf16(x + residual) from global memory and returns the counter to
-// 0.  The next call on the stream touches the counter only after its
-// dependency wait, i.e. after this grid has completed.
-__device__ __forceinline__ void fused_residual_writeback_at_end(const GluParams &p, int arrive_old)
+// Part 2.  Workspace: ws[0] counts CTAs that hold their residual rows (the
+// bulk copy has landed: that CTA reads residual no more), ws[1] counts CTAs
+// that have written their share of the result.  Thread 0 arrives on ws[0]
+// right after the copy lands.  At the end, warp 0 of every CTA waits (bounded)
+// until all gridDim.x CTAs have arrived -- long true by then, since every CTA
+// arrives early in its life and all of them are resident at once (grid <=
+// one CTA per SM, and no dependent grid launches before all have started) --
+// then writes its 1/gridDim.x slice of residual = bf16(x + residual) and
+// arrives on ws[1]; the CTA arriving there last returns both counters to 0.
+// The next call on the stream touches the counters only after its dependency
+// wait, i.e. after this grid has completed.
+__device__ __forceinline__ void fused_arrive(const GluParams &p)
 {
-    const bool last = __shfl_sync(0xffffffffu, arrive_old, 0) == static_cast<int>(gridDim.x) - 1;
-    if (!last) return;
-    const int n = p.M * (p.K >> 3);
+    __threadfence();
+    atomicAdd(p.ws, 1);
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int *ptr)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fused_residual_slice_at_end(const GluParams &p)
+{
     const int lane = threadIdx.x & 31;
-    for (int i = lane; i < n; i += 32) {
+    const int G = static_cast<int>(gridDim.x);
+    int ok = 1;
+    if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (ld_acquire_gpu(p.ws) < G) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                atomicExch(&g_device_error, kErrTimeout);
+                ok = 0;
+                break;
+            }
+        }
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    const int n = p.M * (p.K >> 3);
+    const int i0 = static_cast<int>((static_cast<int64_t>(n) * blockIdx.x) / G);
+    const int i1 = static_cast<int>((static_cast<int64_t>(n) * (blockIdx.x + 1)) / G);
+    for (int i = i0 + lane; i < i1; i += 32) {
         uint4 *rp = reinterpret_cast<uint4 *>(p.residual) + i;
         *rp = add_bf16x8(reinterpret_cast<const uint4 *>(p.x)[i], *rp);
     }
     __syncwarp();
     if (lane == 0) {
         __threadfence();
-        atomicExch(p.ws, 0);
+        if (atomicAdd(p.ws + 1, 1) == G - 1) {
+            atomicExch(p.ws, 0);
+            atomicExch(p.ws + 1, 0);
+        }
     }
 }
 
@@ -472,7 +505,6 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
     __syncwarp();
 
     uint4 hreg[HREG ? kHregChunks : 1];
-    int arrive_old = -1;   // thread 0, single-kernel path: position on the workspace counter
     if constexpr (NORM) {
         // the norm path always has 16-byte aligned operands (the host checks)
         if (threadIdx.x == 0) {
@@ -484,7 +516,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
         if (p.fused) fused_x_prefetch(p, xp);
         prologue_wait(pro_bar);
         if (p.fused) {
-            if (threadIdx.x == 0) arrive_old = atomicAdd(p.ws, 1);
+            if (threadIdx.x == 0) fused_arrive(p);
             fused_add_in_place(p, h_s, K, xp);
             __syncthreads();
         }
@@ -639,7 +671,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
         }
     }
     if constexpr (NORM)
-        if (p.fused && warp == 0) fused_residual_writeback_at_end(p, arrive_old);
+        if (p.fused && warp == 0) fused_residual_slice_at_end(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -774,7 +806,6 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
     __syncwarp();
 
     // h rows 0..M-1, then a zero row M (padded stride HS)
-    int arrive_old = -1;   // thread 0, single-kernel path: position on the workspace counter
     if constexpr (NORM) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u);
@@ -784,7 +815,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
         if (p.fused) fused_x_prefetch(p, xp);
         prologue_wait(pro_bar);
         if (p.fused) {
-            if (threadIdx.x == 0) arrive_old = atomicAdd(p.ws, 1);
+            if (threadIdx.x == 0) fused_arrive(p);
             fused_add_in_place(p, h_s, HS, xp);
             __syncthreads();
         }
@@ -874,7 +905,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
         }
     }
     if constexpr (NORM)
-        if (p.fused && warp == 0) fused_residual_writeback_at_end(p, arrive_old);
+        if (p.fused && warp == 0) fused_residual_slice_at_end(p);
 }
 
 // ---------------------------------------------------------------------------
