@@ -145,14 +145,17 @@ __device__ __forceinline__ void load_h_to_smem(const GluParams &p, uint16_t *h_s
 // h_s (rows M..rows_out-1 zero); M <= MB.
 // src: the s rows (row stride sstride; default: residual in global memory);
 // may be h_s itself (each chunk is read before the same thread overwrites it).
+// w_src: norm_w (default: global memory).
 template <int MB>
 __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s, float (*red)[MB],
                                               float *inv_s, int rows_out, int hstride = 0,
-                                              const uint16_t *src = nullptr, int sstride = 0)
+                                              const uint16_t *src = nullptr, int sstride = 0,
+                                              const uint16_t *w_src = nullptr)
 {
     if (hstride == 0) hstride = p.K;
     if (sstride == 0) sstride = p.K;
     const uint16_t *sp = src ? src : p.s;
+    const uint16_t *wp = w_src ? w_src : p.norm_w;   // norm_w: shared-memory copy or global
     const int K = p.K, tid = threadIdx.x, nthr = blockDim.x;
     const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
     float ss[MB];
@@ -206,7 +209,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
             if (m < p.M) {
                 const float inv = inv_s[m];
                 const uint4 v = *reinterpret_cast<const uint4 *>(sp + static_cast<int64_t>(m) * sstride + c * 8);
-                const uint4 wv = *reinterpret_cast<const uint4 *>(p.norm_w + c * 8);
+                const uint4 wv = *reinterpret_cast<const uint4 *>(wp + c * 8);
                 const uint32_t sv[4] = {v.x, v.y, v.z, v.w};
                 const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
                 uint32_t r[4];
@@ -226,7 +229,7 @@ __device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s,
             uint16_t o = 0;
             if (m < p.M) {
                 const float sv = bf16_to_f32(sp[static_cast<int64_t>(m) * sstride + k]);
-                o = f32_to_bf16((sv * inv_s[m]) * (1.0f + bf16_to_f32(p.norm_w[k])));
+                o = f32_to_bf16((sv * inv_s[m]) * (1.0f + bf16_to_f32(wp[k])));
             }
             h_s[static_cast<int64_t>(m) * hstride + k] = o;
         }
@@ -323,8 +326,8 @@ __device__ __forceinline__ void fused_add_in_place(const GluParams &p, uint16_t 
 // wait, i.e. after this grid has completed.
 __device__ __forceinline__ void fused_arrive(const GluParams &p)
 {
-    __threadfence();
-    atomicAdd(p.ws, 1);
+    // the residual rows are already in shared memory: nothing to order before
+    asm volatile("red.relaxed.gpu.global.add.s32 [%0], 1;" ::"l"(p.ws) : "memory");
 }
 
 __device__ __forceinline__ int ld_acquire_gpu(const int *ptr)
@@ -334,22 +337,12 @@ __device__ __forceinline__ int ld_acquire_gpu(const int *ptr)
     return v;
 }
 
-__device__ __forceinline__ void fused_residual_slice_at_end(const GluParams &p)
+// Warp 0: write this CTA's slice of residual and arrive on ws[1]; the CTA
+// arriving there last returns both counters to 0.
+__device__ __forceinline__ void fused_residual_slice(const GluParams &p)
 {
     const int lane = threadIdx.x & 31;
     const int G = static_cast<int>(gridDim.x);
-    int ok = 1;
-    if (lane == 0) {
-        const uint64_t t0 = global_timer_ns();
-        while (ld_acquire_gpu(p.ws) < G) {
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
-                atomicExch(&g_device_error, kErrTimeout);
-                ok = 0;
-                break;
-            }
-        }
-    }
-    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
     const int n = p.M * (p.K >> 3);
     const int i0 = static_cast<int>((static_cast<int64_t>(n) * blockIdx.x) / G);
     const int i1 = static_cast<int>((static_cast<int64_t>(n) * (blockIdx.x + 1)) / G);
@@ -365,6 +358,25 @@ __device__ __forceinline__ void fused_residual_slice_at_end(const GluParams &p)
             atomicExch(p.ws + 1, 0);
         }
     }
+}
+
+// Warp 0, at its end, if the slice has not been written mid-stream: wait
+// (bounded) for all CTAs to have arrived, then write it.
+__device__ __forceinline__ void fused_residual_slice_at_end(const GluParams &p)
+{
+    const int lane = threadIdx.x & 31;
+    int ok = 1;
+    if (lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (ld_acquire_gpu(p.ws) < static_cast<int>(gridDim.x)) {
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                atomicExch(&g_device_error, kErrTimeout);
+                ok = 0;
+                break;
+            }
+        }
+    }
+    if (__shfl_sync(0xffffffffu, ok, 0)) fused_residual_slice(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -446,7 +458,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     if (threadIdx.x == 0) {
         *counter = 0;
-        mbar_init(pro_bar, 1);
+        mbar_init(pro_bar, NORM ? 2 : 1);   // norm: the norm_w copy and the residual copy
     }
     fence_mbar_init();
     __syncthreads();
@@ -496,12 +508,27 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
         if (last_g >= 0) issue(st, last_g, last_seg);
     };
 
-    if (p.prefetch && lane == 0)
-        for (int st = 0; st < S; ++st) fill(st);
+    uint16_t *nw_s = reinterpret_cast<uint16_t *>(smem + p.off_s);   // norm: norm_w, K elements
+    auto copy_norm_w = [&]() {
+        if constexpr (NORM) {
+            if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(K) * 2u);
+                bulk_g2s_plain(nw_s, p.norm_w, static_cast<uint32_t>(K) * 2u, pro_bar);
+            }
+        }
+    };
+    if (p.prefetch) {
+        copy_norm_w();   // a weight, like gate_w / up_w
+        if (lane == 0)
+            for (int st = 0; st < S; ++st) fill(st);
+    }
     grid_dependency_wait();
     grid_launch_dependents();
-    if (!p.prefetch && lane == 0)
-        for (int st = 0; st < S; ++st) fill(st);
+    if (!p.prefetch) {
+        copy_norm_w();
+        if (lane == 0)
+            for (int st = 0; st < S; ++st) fill(st);
+    }
     __syncwarp();
 
     uint4 hreg[HREG ? kHregChunks : 1];
@@ -520,7 +547,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
             fused_add_in_place(p, h_s, K, xp);
             __syncthreads();
         }
-        norm_prologue<MB>(p, h_s, red, inv_s, MB, K, h_s, K);
+        norm_prologue<MB>(p, h_s, red, inv_s, MB, K, h_s, K, nw_s);
         __syncthreads();
     } else if constexpr (!HREG) {
         if (p.vec_in) {
@@ -565,11 +592,16 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
 #pragma unroll
         for (int m = 0; m < MB; ++m) ag[r][m] = au[r][m] = make_float2(0.0f, 0.0f);
 
+    // single-kernel add_rmsnorm_glu: warp 0 writes its residual slice as soon as
+    // a load issued at the top of an iteration shows every CTA has arrived
+    bool slice_pending = NORM && p.fused && warp == 0;
     int seg = nseg;   // consumer-side segment of the current group
     for (int u = 0;; ++u) {
         const int st = u % S;
         const int g = slot_grp[st];
         if (g < 0) break;
+        int arrived = 0;
+        if (slice_pending && lane == 0) arrived = ld_acquire_gpu(p.ws);
         seg = (seg + 1 < nseg) ? seg + 1 : 0;
         const bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -653,6 +685,10 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
             fill(st);   // the unit S ahead of u, or -1 once the CTA's groups run out
         }
         __syncwarp();
+        if (slice_pending && __shfl_sync(0xffffffffu, arrived, 0) >= static_cast<int>(gridDim.x)) {
+            fused_residual_slice(p);
+            slice_pending = false;
+        }
         if (seg == nseg - 1) {
             const int row0 = group_row0(g);
             float gsel = 0.0f, usel = 0.0f;
@@ -670,8 +706,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
                 p.out[m * p.ldo + row0 + r] = glu_epilogue(gsel, usel, p.mode);
         }
     }
-    if constexpr (NORM)
-        if (p.fused && warp == 0) fused_residual_slice_at_end(p);
+    if (slice_pending) fused_residual_slice_at_end(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -757,7 +792,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     if (threadIdx.x == 0) {
         *counter = 0;
-        mbar_init(pro_bar, 1);
+        mbar_init(pro_bar, NORM ? 2 : 1);   // norm: the norm_w copy and the residual copy
     }
     fence_mbar_init();
     __syncthreads();
@@ -797,12 +832,25 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
         if (last_g >= 0) issue(st, last_g, last_seg);
     };
 
-    if (p.prefetch)
+    uint16_t *nw_s = reinterpret_cast<uint16_t *>(smem + p.off_s);   // norm: norm_w, K elements
+    auto copy_norm_w = [&]() {
+        if constexpr (NORM) {
+            if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(K) * 2u);
+                bulk_g2s_plain(nw_s, p.norm_w, static_cast<uint32_t>(K) * 2u, pro_bar);
+            }
+        }
+    };
+    if (p.prefetch) {
+        copy_norm_w();   // a weight, like gate_w / up_w
         for (int st = 0; st < S; ++st) fill(st);
+    }
     grid_dependency_wait();
     grid_launch_dependents();
-    if (!p.prefetch)
+    if (!p.prefetch) {
+        copy_norm_w();
         for (int st = 0; st < S; ++st) fill(st);
+    }
     __syncwarp();
 
     // h rows 0..M-1, then a zero row M (padded stride HS)
@@ -819,7 +867,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
             fused_add_in_place(p, h_s, HS, xp);
             __syncthreads();
         }
-        norm_prologue<kMaxM>(p, h_s, red, inv_s, p.M, HS, h_s, HS);
+        norm_prologue<kMaxM>(p, h_s, red, inv_s, p.M, HS, h_s, HS, nw_s);
     } else if (p.vec_in) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u);
@@ -856,11 +904,14 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
     const int b_off = (lane & 7) * RS + ((lane >> 3) & 1) * 8;
 
     float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
+    bool slice_pending = NORM && p.fused && warp == 0;   // as in glu_stream_kernel
     int seg = nseg;
     for (int u = 0;; ++u) {
         const int st = u % S;
         const int g = slot_grp[st];
         if (g < 0) break;
+        int arrived = 0;
+        if (slice_pending && lane == 0) arrived = ld_acquire_gpu(p.ws);
         seg = (seg + 1 < nseg) ? seg + 1 : 0;
         const bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -891,6 +942,10 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
         if (lane == 0) fence_proxy_async_smem();
         fill(st);   // the unit S ahead of u, or -1 once the CTA's groups run out
         __syncwarp();
+        if (slice_pending && __shfl_sync(0xffffffffu, arrived, 0) >= static_cast<int>(gridDim.x)) {
+            fused_residual_slice(p);
+            slice_pending = false;
+        }
         if (seg == nseg - 1) {
             // D layout: d[0], d[1] -> batch row lane/4, features 2*(lane%4) + 0, 1;
             //           d[2], d[3] -> batch row lane/4 + 8, same features.
@@ -904,8 +959,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
             }
         }
     }
-    if constexpr (NORM)
-        if (p.fused && warp == 0) fused_residual_slice_at_end(p);
+    if (slice_pending) fused_residual_slice_at_end(p);
 }
 
 // ---------------------------------------------------------------------------

@@ -533,8 +533,9 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
     const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && p.vec_in;
 
     // single kernel: needs the fast kernels, 16-byte aligned x, and N > 0
+    const uint32_t nwbytes = (static_cast<uint32_t>(K) * 2u + 127u) & ~127u;   // norm_w in shared memory
     if (ws && N > 0 && bulk_ok && aligned(x, 16)) {
-        const uint32_t sbytes = 0;   // s is formed in place where the residual rows land
+        const uint32_t sbytes = nwbytes;   // s is formed in place where the residual rows land
         Plan pl;
         p.fused = 1;
         p.x = x;
@@ -595,7 +596,7 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
 
     // 2) the GEMV with the norm prologue, as a programmatic dependent launch
     Plan pl;
-    if (bulk_ok && plan_mma(*d, M, N, K, pl)) {
+    if (bulk_ok && plan_mma(*d, M, N, K, pl, nwbytes)) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;
         p.stages = pl.stages;
@@ -606,7 +607,7 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
         if (st == MBGLU_OK) t_last_variant = kTensor;
         return st;
     }
-    const bool fast = bulk_ok && plan_stream(*d, M, N, K, true, true, pl);
+    const bool fast = bulk_ok && plan_stream(*d, M, N, K, true, true, pl, true, nwbytes);
     if (fast) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;
