@@ -268,7 +268,7 @@ __device__ __forceinline__ void prologue_wait(uint64_t *bar)
 // in place, x read straight from global memory (the first kXPre chunks per
 // thread are loaded before the copy is awaited).  The fp32 sum of two bf16
 // values rounds to the same bf16 as the exact sum.
-constexpr int kXPre = 4;
+constexpr int kXPre = 8;   // x chunks per thread loaded before the residual copy is awaited, and per batch after
 
 struct XPrefetch {
     uint4 v[kXPre];
@@ -293,23 +293,34 @@ __device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b)
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-__device__ __forceinline__ void fused_add_in_place(const GluParams &p, uint16_t *h_s, int hstride,
-                                                   const XPrefetch &xp)
+// Adds the chunks base + j*blockDim (j < kXPre) of x, held in xp, into h_s.
+__device__ __forceinline__ void fused_add_batch(const GluParams &p, uint16_t *h_s, int hstride, const XPrefetch &xp,
+                                                int base)
 {
     const int nch = p.K >> 3, n = p.M * nch;
 #pragma unroll
     for (int j = 0; j < kXPre; ++j) {
-        const int i = threadIdx.x + j * blockDim.x;
+        const int i = base + j * blockDim.x;
         if (i < n) {
             const int m = i / nch, c = i - m * nch;
             uint4 *hp = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * hstride + c * 8);
             *hp = add_bf16x8(xp.v[j], *hp);
         }
     }
-    for (int i = threadIdx.x + kXPre * blockDim.x; i < n; i += blockDim.x) {
-        const int m = i / nch, c = i - m * nch;
-        uint4 *hp = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * hstride + c * 8);
-        *hp = add_bf16x8(reinterpret_cast<const uint4 *>(p.x)[i], *hp);
+}
+
+__device__ __forceinline__ void fused_add_in_place(const GluParams &p, uint16_t *h_s, int hstride, XPrefetch &xp)
+{
+    const int n = p.M * (p.K >> 3);
+    fused_add_batch(p, h_s, hstride, xp, threadIdx.x);
+    // the rest in batches of kXPre independent loads, so their latencies overlap
+    for (int base = threadIdx.x + kXPre * blockDim.x; base < n; base += kXPre * blockDim.x) {
+#pragma unroll
+        for (int j = 0; j < kXPre; ++j) {
+            const int i = base + j * blockDim.x;
+            xp.v[j] = i < n ? reinterpret_cast<const uint4 *>(p.x)[i] : make_uint4(0, 0, 0, 0);
+        }
+        fused_add_batch(p, h_s, hstride, xp, base);
     }
 }
 
