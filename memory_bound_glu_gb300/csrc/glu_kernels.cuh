@@ -35,7 +35,7 @@ namespace mbglu {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
 constexpr int kErrTimeout = 8;                    // == MBGLU_ERR_TIMEOUT
 constexpr int kMaxWarps = 16;        // any kernel's block, for the norm reduction
-constexpr int kMaxStreamWarps = 8;   // the streaming kernel's block
+constexpr int kMaxStreamWarps = 8;   // the streaming kernels' block, a helper warp included
 constexpr int kMaxM = 16;
 
 // Error word of the device (read and cleared by mbglu_read_device_error).
@@ -64,8 +64,9 @@ struct GluParams {
     int fused;
     const uint16_t *x;
     uint16_t *residual;
-    int *ws;                 // arrival counter, 0 between calls
+    int *ws;                 // arrival counters, 0 between calls
     uint32_t off_s;
+    int helper_warp;         // single-kernel path: the extra warp that writes the residual slice (-1: none)
 };
 
 // ---------------------------------------------------------------------------
@@ -371,9 +372,11 @@ __device__ __forceinline__ void fused_residual_slice(const GluParams &p)
     }
 }
 
-// Warp 0, at its end, if the slice has not been written mid-stream: wait
-// (bounded) for all CTAs to have arrived, then write it.
-__device__ __forceinline__ void fused_residual_slice_at_end(const GluParams &p)
+// The helper warp (one extra warp that never streams): wait (bounded, with
+// short sleeps) until every CTA has arrived, then write this CTA's slice.  It
+// keeps the counter traffic and the slice's L2 round trips off the streaming
+// warps.
+__device__ __forceinline__ void fused_residual_helper(const GluParams &p)
 {
     const int lane = threadIdx.x & 31;
     int ok = 1;
@@ -385,6 +388,7 @@ __device__ __forceinline__ void fused_residual_slice_at_end(const GluParams &p)
                 ok = 0;
                 break;
             }
+            __nanosleep(256);
         }
     }
     if (__shfl_sync(0xffffffffu, ok, 0)) fused_residual_slice(p);
@@ -465,7 +469,8 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
     const bool contig = (p.ld_gate == K) && (p.ld_up == K) && (KS == K);
 
     uint64_t *pro_bar = reinterpret_cast<uint64_t *>(smem + kProBarOffset);
-    if (lane == 0)
+    const bool helper = warp == p.helper_warp;   // single-kernel norm path only; owns no ring
+    if (lane == 0 && !helper)
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     if (threadIdx.x == 0) {
         *counter = 0;
@@ -530,14 +535,14 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
     };
     if (p.prefetch) {
         copy_norm_w();   // a weight, like gate_w / up_w
-        if (lane == 0)
+        if (lane == 0 && !helper)
             for (int st = 0; st < S; ++st) fill(st);
     }
     grid_dependency_wait();
     grid_launch_dependents();
     if (!p.prefetch) {
         copy_norm_w();
-        if (lane == 0)
+        if (lane == 0 && !helper)
             for (int st = 0; st < S; ++st) fill(st);
     }
     __syncwarp();
@@ -597,22 +602,22 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
         }
     }
 
+    if (helper) {
+        fused_residual_helper(p);
+        return;
+    }
+
     float2 ag[R][MB], au[R][MB];
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
         for (int m = 0; m < MB; ++m) ag[r][m] = au[r][m] = make_float2(0.0f, 0.0f);
 
-    // single-kernel add_rmsnorm_glu: warp 0 writes its residual slice as soon as
-    // a load issued at the top of an iteration shows every CTA has arrived
-    bool slice_pending = NORM && p.fused && warp == 0;
     int seg = nseg;   // consumer-side segment of the current group
     for (int u = 0;; ++u) {
         const int st = u % S;
         const int g = slot_grp[st];
         if (g < 0) break;
-        int arrived = 0;
-        if (slice_pending && lane == 0) arrived = ld_acquire_gpu(p.ws);
         seg = (seg + 1 < nseg) ? seg + 1 : 0;
         const bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -696,10 +701,6 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
             fill(st);   // the unit S ahead of u, or -1 once the CTA's groups run out
         }
         __syncwarp();
-        if (slice_pending && __shfl_sync(0xffffffffu, arrived, 0) >= static_cast<int>(gridDim.x)) {
-            fused_residual_slice(p);
-            slice_pending = false;
-        }
         if (seg == nseg - 1) {
             const int row0 = group_row0(g);
             float gsel = 0.0f, usel = 0.0f;
@@ -717,7 +718,6 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
                 p.out[m * p.ldo + row0 + r] = glu_epilogue(gsel, usel, p.mode);
         }
     }
-    if (slice_pending) fused_residual_slice_at_end(p);
 }
 
 // ---------------------------------------------------------------------------
@@ -799,7 +799,8 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
     };
 
     uint64_t *pro_bar = reinterpret_cast<uint64_t *>(smem + kProBarOffset);
-    if (lane == 0)
+    const bool helper = warp == p.helper_warp;   // single-kernel norm path only; owns no ring
+    if (lane == 0 && !helper)
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     if (threadIdx.x == 0) {
         *counter = 0;
@@ -854,13 +855,15 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
     };
     if (p.prefetch) {
         copy_norm_w();   // a weight, like gate_w / up_w
-        for (int st = 0; st < S; ++st) fill(st);
+        if (!helper)
+            for (int st = 0; st < S; ++st) fill(st);
     }
     grid_dependency_wait();
     grid_launch_dependents();
     if (!p.prefetch) {
         copy_norm_w();
-        for (int st = 0; st < S; ++st) fill(st);
+        if (!helper)
+            for (int st = 0; st < S; ++st) fill(st);
     }
     __syncwarp();
 
@@ -914,15 +917,17 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
     const uint16_t *a_base = h_s + static_cast<int64_t>(arow) * HS + (lane >> 4) * 8;
     const int b_off = (lane & 7) * RS + ((lane >> 3) & 1) * 8;
 
+    if (helper) {
+        fused_residual_helper(p);
+        return;
+    }
+
     float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
-    bool slice_pending = NORM && p.fused && warp == 0;   // as in glu_stream_kernel
     int seg = nseg;
     for (int u = 0;; ++u) {
         const int st = u % S;
         const int g = slot_grp[st];
         if (g < 0) break;
-        int arrived = 0;
-        if (slice_pending && lane == 0) arrived = ld_acquire_gpu(p.ws);
         seg = (seg + 1 < nseg) ? seg + 1 : 0;
         const bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -953,10 +958,6 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
         if (lane == 0) fence_proxy_async_smem();
         fill(st);   // the unit S ahead of u, or -1 once the CTA's groups run out
         __syncwarp();
-        if (slice_pending && __shfl_sync(0xffffffffu, arrived, 0) >= static_cast<int>(gridDim.x)) {
-            fused_residual_slice(p);
-            slice_pending = false;
-        }
         if (seg == nseg - 1) {
             // D layout: d[0], d[1] -> batch row lane/4, features 2*(lane%4) + 0, 1;
             //           d[2], d[3] -> batch row lane/4 + 8, same features.
@@ -970,7 +971,6 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
             }
         }
     }
-    if (slice_pending) fused_residual_slice_at_end(p);
 }
 
 // ---------------------------------------------------------------------------

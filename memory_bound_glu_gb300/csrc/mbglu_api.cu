@@ -206,7 +206,7 @@ struct Plan {
 // per stage as default_rows, halved while not even one warp fits.  False if
 // h plus a two-stage ring cannot fit.
 bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool norm, Plan &pl,
-                 bool allow_hreg = true, uint32_t extra = 0)
+                 bool allow_hreg = true, uint32_t extra = 0, int max_warps = mbglu::kMaxStreamWarps)
 {
     const Tuning &t = tuning();
     pl.MB = batch_tile(M);
@@ -230,8 +230,8 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
         int best_w = 0, best_s = 0;
         int64_t best_ring = 0;
         const int want_s = t.stages > 0 ? t.stages : 2;
-        for (int w = 1; w <= mbglu::kMaxStreamWarps; ++w) {
-            if (t.warps > 0 && w != t.warps) continue;
+        for (int w = 1; w <= max_warps; ++w) {
+            if (t.warps > 0 && w != std::min(t.warps, max_warps)) continue;
             const int sn = static_cast<int>(std::min<int64_t>(want_s, room / (stage * w)));
             if (sn < 2) continue;
             const int64_t ring = stage * w * sn;
@@ -256,7 +256,7 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
     pl.KS = ks;
     pl.nseg = (K + ks - 1) / ks;
     if (pl.hreg && pl.nseg != 1)   // registers hold whole rows of h only
-        return plan_stream(d, M, N, K, contiguous, norm, pl, false, extra);
+        return plan_stream(d, M, N, K, contiguous, norm, pl, false, extra, max_warps);
     pl.off_h = kBarRegion;
     pl.off_s = kBarRegion + hbytes;
     pl.off_ring = kBarRegion + hbytes + extra;
@@ -270,7 +270,8 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
 // padded by 16 bytes; h_s holds M rows plus a zero row.  Two stages per warp,
 // as many warps (<= 8) as fit; segments shrink (>= 256) while fewer than 4
 // warps fit.  False if nothing fits.
-bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl, uint32_t extra = 0)
+bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl, uint32_t extra = 0,
+              int max_warps = mbglu::kMaxStreamWarps)
 {
     const Tuning &t = tuning();
     if (M < t.mma_min_m || K % 16 != 0) return false;
@@ -291,7 +292,7 @@ bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl, uint32_t extra
     const int want_s = t.stages > 0 ? t.stages : 2;
     for (;;) {
         const int64_t stage = static_cast<int64_t>(2) * mbglu::kMmaRows * (ks + 8) * 2;
-        int w = t.warps > 0 ? t.warps : mbglu::kMaxStreamWarps;
+        int w = t.warps > 0 ? std::min(t.warps, max_warps) : max_warps;
         while (w > 1 && static_cast<int64_t>(w) * want_s * stage > room) --w;
         if (static_cast<int64_t>(w) * 2 * stage > room) w = 0;
         if (w >= 4 || (w >= 1 && (ks <= 256 || t.warps > 0 || t.ks > 0))) {
@@ -336,7 +337,7 @@ mbglu_status launch(void (*kernel)(Args...), dim3 grid, dim3 block, uint32_t sme
 template <bool NORM>
 mbglu_status launch_stream(const Plan &pl, const GluParams &p, cudaStream_t stream, bool pdl)
 {
-    const dim3 grid(pl.grid), block(pl.warps * 32);
+    const dim3 grid(pl.grid), block((pl.warps + (p.helper_warp >= 0 ? 1 : 0)) * 32);
 #define MBGLU_CASE(TMB, TR, TH)                                                                               \
     if (pl.MB == TMB && pl.R == TR && pl.hreg == TH)                                                             \
         return launch(mbglu::glu_stream_kernel<TMB, TR, NORM, TH>, grid, block, pl.smem, stream, pdl, p);
@@ -350,6 +351,7 @@ int generic_grid(const DeviceInfo &d, int N) { return std::max(1, std::min(d.sm_
 GluParams base_params(int M, int N, int K, int mode)
 {
     GluParams p = {};
+    p.helper_warp = -1;
     p.M = M;
     p.N = N;
     p.K = K;
@@ -541,24 +543,27 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
         p.x = x;
         p.residual = residual;
         p.ws = ws;
-        if (plan_mma(*d, M, N, K, pl, sbytes)) {
+        if (plan_mma(*d, M, N, K, pl, sbytes, mbglu::kMaxStreamWarps - 1)) {
             p.KS = pl.KS;
             p.nseg = pl.nseg;
             p.stages = pl.stages;
             p.off_h = pl.off_h;
             p.off_s = pl.off_s;
             p.off_ring = pl.off_ring;
-            st = launch(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
+            p.helper_warp = pl.warps;   // one extra warp writes the residual slice
+            st = launch(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3((pl.warps + 1) * 32), pl.smem, stream,
+                        pdl, p);
             if (st == MBGLU_OK) t_last_variant = kTensor;
             return st;
         }
-        if (plan_stream(*d, M, N, K, true, true, pl, true, sbytes)) {
+        if (plan_stream(*d, M, N, K, true, true, pl, true, sbytes, mbglu::kMaxStreamWarps - 1)) {
             p.KS = pl.KS;
             p.nseg = pl.nseg;
             p.stages = pl.stages;
             p.off_h = pl.off_h;
             p.off_s = pl.off_s;
             p.off_ring = pl.off_ring;
+            p.helper_warp = pl.warps;   // one extra warp writes the residual slice
             st = launch_stream<true>(pl, p, stream, pdl);
             if (st == MBGLU_OK) t_last_variant = kStream;
             return st;
@@ -567,6 +572,7 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
         p.x = nullptr;
         p.residual = nullptr;
         p.ws = nullptr;
+        p.helper_warp = -1;
     }
 
     // 1) residual <- bf16(x + residual); it waits for its predecessor before
