@@ -171,6 +171,38 @@ mbglu_status add_rmsnorm_glu_ws(const mbglu_bf16 *x, mbglu_bf16 *residual,
                                 cudaStream_t stream);
 
 /*
+ * add_rmsnorm_glu_noalloc -- add_rmsnorm_glu_ws for callers that cannot
+ * allocate device memory: code running where the memory is owned by someone
+ * else (a serving runtime's planner, a plugin host, a framework that hands
+ * out only the tensors of the op), or where cudaMalloc is not allowed at all
+ * (inside stream capture, in paths that must not synchronise the device).
+ * No counterpart on the pages: it exists for such callers only.
+ * Same arguments as add_rmsnorm_glu; the caller still provides every input and
+ * output.  The workspace the single kernel needs comes from a fixed device
+ * array inside the library, MBGLU_NOALLOC_SCRATCH_BYTES per GPU, held by every
+ * GPU that loads the library until the process exits; a call needing more
+ * than that returns MBGLU_ERR_SHAPE.  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and keeps it: make that first call before any
+ *     stream capture on that device.
+ *   - Each call clears the counters with a stream-ordered cudaMemsetAsync
+ *     before its kernel, because the array keeps what the last call left.
+ *   - All calls share the one array: calls that may overlap on the GPU (on
+ *     different streams, or in concurrently running graphs) race on it and
+ *     give wrong results.  Use add_rmsnorm_glu_ws with one workspace per stream
+ *     for that.
+ * Falls back to the two-kernel path (scratch untouched) exactly where
+ * add_rmsnorm_glu_ws does.  Errors as add_rmsnorm_glu_ws.
+ */
+#define MBGLU_NOALLOC_SCRATCH_BYTES 256
+mbglu_status add_rmsnorm_glu_noalloc(const mbglu_bf16 *x, mbglu_bf16 *residual,
+                                     const mbglu_bf16 *norm_w, float eps,
+                                     const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w,
+                                     mbglu_bf16 *out, int M, int N, int K,
+                                     mbglu_mode mode, cudaStream_t stream);
+
+/*
  * Launch policy, process-wide (default MBGLU_POLICY_PREFETCH).  It decides how
  * a call's kernels are ordered after the kernel that precedes them on the
  * stream; results are identical under every policy.

@@ -22,7 +22,8 @@ MAX_M = 16
 WORKSPACE_BYTES = 256
 
 # Every symbol include/mbglu.h declares.
-EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "mbglu_set_launch_policy", "mbglu_get_launch_policy",
+EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu_noalloc", "mbglu_set_launch_policy",
+           "mbglu_get_launch_policy",
            "mbglu_status_string", "mbglu_abi_version", "mbglu_last_cuda_error", "mbglu_last_variant",
            "mbglu_read_device_error")
 POLICY_SERIAL, POLICY_PDL, POLICY_PREFETCH = 0, 1, 2
@@ -47,6 +48,8 @@ def _bind(l):
     l.add_rmsnorm_glu.restype = i32
     l.add_rmsnorm_glu_ws.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32, i32, vp, ctypes.c_size_t, vp]
     l.add_rmsnorm_glu_ws.restype = i32
+    l.add_rmsnorm_glu_noalloc.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32, i32, vp]
+    l.add_rmsnorm_glu_noalloc.restype = i32
     l.mbglu_status_string.argtypes = [i32]
     l.mbglu_status_string.restype = ctypes.c_char_p
     l.mbglu_abi_version.restype = i32

@@ -670,3 +670,60 @@ mbglu_status mbglu_read_device_error(int *word)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// add_rmsnorm_glu_noalloc: the single-kernel add_rmsnorm_glu for callers that
+// cannot allocate device memory.  Its scratch -- the two arrival counters the
+// single kernel needs -- lives in this file-scope device array instead of a
+// caller-provided workspace.  Every GPU that loads the library holds it until
+// the process exits.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) int g_noalloc_scratch[MBGLU_NOALLOC_SCRATCH_BYTES / sizeof(int)];
+static_assert(MBGLU_WORKSPACE_BYTES <= MBGLU_NOALLOC_SCRATCH_BYTES, "the array must hold one workspace");
+
+std::mutex g_noalloc_mu;
+int *g_noalloc_ptr[kMaxDevices] = {};
+
+// The array's device address on the current device.  In host code the name
+// g_noalloc_scratch is only a host-side stand-in, so the address is asked of
+// the runtime once per device (with that device current) and kept.
+mbglu_status noalloc_scratch(int **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        int *ptr = nullptr;
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr), g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MBGLU_OK;
+}
+
+}  // namespace
+
+extern "C" mbglu_status add_rmsnorm_glu_noalloc(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w,
+                                                float eps, const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w,
+                                                mbglu_bf16 *out, int M, int N, int K, mbglu_mode mode,
+                                                cudaStream_t stream)
+{
+    t_last_variant = kNone;
+    // the scratch this call needs must fit the array (the single kernel needs
+    // one workspace whatever the shapes; the check states the limit)
+    const size_t need = MBGLU_WORKSPACE_BYTES;
+    if (need > MBGLU_NOALLOC_SCRATCH_BYTES) return MBGLU_ERR_SHAPE;
+    int *scratch = nullptr;
+    mbglu_status st = noalloc_scratch(&scratch);
+    if (st != MBGLU_OK) return st;
+    // the counters must start at zero; the array keeps whatever the last call
+    // (on any stream) left there, so clear them, in stream order
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, need, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return add_rmsnorm_glu_ws(x, residual, norm_w, eps, gate_w, up_w, out, M, N, K, mode, scratch, need, stream);
+}
