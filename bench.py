@@ -56,8 +56,6 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
-    ap.add_argument("--gemv-ws", type=int, default=1, choices=[0, 1],
-                    help="glu_gemv with a workspace (row groups balanced across SMs) or without")
     ap.add_argument("--norm-kernels", type=int, default=1, choices=[1, 2],
                     help="add_rmsnorm_glu as one kernel (workspace entry point) or as two")
     ap.add_argument("--policy", type=int, default=None, choices=[0, 1, 2],
@@ -270,12 +268,9 @@ def run_reference(args, w, M, mode, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def config_dict(w, M, mode, layers, norm_kernels=None, gemv_ws=None):
+def config_dict(w, M, mode, layers, norm_kernels=None):
     wb = w.weight_bytes() * layers
-    if w.op == "glu_gemv":
-        extra = {} if gemv_ws is None else {"workspace": bool(gemv_ws)}
-    else:
-        extra = {} if norm_kernels is None else {"norm_kernels": norm_kernels}
+    extra = {} if w.op == "glu_gemv" or norm_kernels is None else {"norm_kernels": norm_kernels}
     return {"workload": w.name, "op": w.op, "M": M, "K": w.K, "N": w.N, "mode": mode, "layers": layers, **extra,
             "l2": f"inputs larger than L2: {layers} cycled weight pairs, {wb / 1e9:.2f} GB",
             "launch": f"one CUDA graph of {layers} calls per step",
@@ -332,13 +327,13 @@ def main():
         residuals = [r_cpu.to(dev) for _ in range(L)]
     outs = torch.empty((L, M, w.N), dtype=torch.bfloat16, device=dev)
     single = w.op != "glu_gemv" and args.norm_kernels == 1
-    ws = mb.new_workspace(dev) if (single or (w.op == "glu_gemv" and args.gemv_ws)) else None
+    ws = mb.new_workspace(dev) if single else None
     launches_per_call = 1 if (w.op == "glu_gemv" or single) else 2
 
     def one_step():
         for i in range(L):
             if w.op == "glu_gemv":
-                mb.glu_gemv(h, gates[i], ups[i], out=outs[i], mode=mode, workspace=ws)
+                mb.glu_gemv(h, gates[i], ups[i], out=outs[i], mode=mode)
             else:
                 mb.add_rmsnorm_glu(x, residuals[i], nw, w.eps, gates[i], ups[i], out=outs[i], mode=mode,
                                    workspace=ws)
@@ -438,7 +433,7 @@ def main():
             "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": round(ms_max / args.steps, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded torch.randn, bf16)", "config": config_dict(w, M, mode, L, args.norm_kernels, args.gemv_ws),
+            "data": "synthetic (seeded torch.randn, bf16)", "config": config_dict(w, M, mode, L, args.norm_kernels),
             "us_per_call": round(us_per_call, 3), "bytes_per_call": bytes_per_call,
             "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",

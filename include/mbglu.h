@@ -109,25 +109,6 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh,
                       cudaStream_t stream);
 
 /*
- * glu_gemv_ws -- glu_gemv with a workspace (same arguments, plus `workspace`
- * as for add_rmsnorm_glu_ws below).  Where the CUDA-core streaming kernel
- * runs with whole rows per stage (batch 1..2, K <= about 8K), row groups past
- * each warp's first prefetched stages are claimed from a counter in the
- * workspace by all CTAs, so every SM finishes at nearly the same time instead
- * of each working off a fixed share.  Elsewhere it runs as glu_gemv and leaves
- * the workspace untouched.  Results are identical to glu_gemv's bit for bit
- * (which CTA computes a row does not change its arithmetic).  Workspace rules
- * and extra errors as add_rmsnorm_glu_ws.
- */
-mbglu_status glu_gemv_ws(const mbglu_bf16 *h, int64_t ldh,
-                         const mbglu_bf16 *gate_w, int64_t ld_gate,
-                         const mbglu_bf16 *up_w, int64_t ld_up,
-                         mbglu_bf16 *out, int64_t ldo,
-                         int M, int N, int K, mbglu_mode mode,
-                         void *workspace, size_t workspace_bytes,
-                         cudaStream_t stream);
-
-/*
  * add_rmsnorm_glu -- residual add + zero-centred RMSNorm, then glu_gemv on
  * the normed rows.  [9057/Changes] "Restore HF's intermediate BF16 rounding in
  * residual/RMSNorm ... construct zero-centered norm scales in FP32".

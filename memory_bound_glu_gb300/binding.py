@@ -22,7 +22,7 @@ MAX_M = 16
 WORKSPACE_BYTES = 256
 
 # Every symbol include/mbglu.h declares.
-EXPORTS = ("glu_gemv", "glu_gemv_ws", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu_noalloc", "mbglu_set_launch_policy",
+EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu_noalloc", "mbglu_set_launch_policy",
            "mbglu_get_launch_policy",
            "mbglu_status_string", "mbglu_abi_version", "mbglu_last_cuda_error", "mbglu_last_variant",
            "mbglu_read_device_error")
@@ -44,8 +44,6 @@ def _bind(l):
     vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     l.glu_gemv.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp]
     l.glu_gemv.restype = i32
-    l.glu_gemv_ws.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32, vp, ctypes.c_size_t, vp]
-    l.glu_gemv_ws.restype = i32
     l.add_rmsnorm_glu.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32, i32, vp]
     l.add_rmsnorm_glu.restype = i32
     l.add_rmsnorm_glu_ws.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32, i32, vp, ctypes.c_size_t, vp]
@@ -94,14 +92,12 @@ def _check(t, name, dim=None):
         raise ValueError(f"{name} must have a contiguous last dimension")
 
 
-def glu_gemv(h, gate_w, up_w, out=None, mode="fused", stream=None, workspace=None):
+def glu_gemv(h, gate_w, up_w, out=None, mode="fused", stream=None):
     """out[M,N] = SiLU(h @ gate_w.T) * (h @ up_w.T) in one pass (bf16).
 
     h is [M,K] (or [K]); gate_w, up_w are [N,K] nn.Linear weights read in
     place; mode "fused" (one rounding) or "hf" (HF bf16 boundaries).  Row
-    strides are passed through, so sliced views work without copies.  With a
-    workspace (new_workspace(), one per concurrently running stream) row
-    groups are balanced across SMs at run time where that applies.
+    strides are passed through, so sliced views work without copies.
     """
     squeeze = h.dim() == 1
     h2 = h.unsqueeze(0) if squeeze else h
@@ -122,17 +118,9 @@ def glu_gemv(h, gate_w, up_w, out=None, mode="fused", stream=None, workspace=Non
     if tuple(out2.shape) != (M, N) or out2.device != dev:
         raise ValueError(f"out must be [{M},{N}] on {dev}")
     with torch.cuda.device(dev):
-        if workspace is None:
-            st = lib().glu_gemv(h2.data_ptr(), h2.stride(0), gate_w.data_ptr(), gate_w.stride(0),
-                                up_w.data_ptr(), up_w.stride(0), out2.data_ptr(), out2.stride(0),
-                                M, N, K, _MODES[mode], _stream_handle(dev, stream))
-        else:
-            if not (workspace.is_cuda and workspace.device == dev and workspace.is_contiguous()):
-                raise ValueError("workspace must be a contiguous CUDA tensor on the operands' device")
-            st = lib().glu_gemv_ws(h2.data_ptr(), h2.stride(0), gate_w.data_ptr(), gate_w.stride(0),
-                                   up_w.data_ptr(), up_w.stride(0), out2.data_ptr(), out2.stride(0),
-                                   M, N, K, _MODES[mode], workspace.data_ptr(),
-                                   workspace.numel() * workspace.element_size(), _stream_handle(dev, stream))
+        st = lib().glu_gemv(h2.data_ptr(), h2.stride(0), gate_w.data_ptr(), gate_w.stride(0),
+                            up_w.data_ptr(), up_w.stride(0), out2.data_ptr(), out2.stride(0),
+                            M, N, K, _MODES[mode], _stream_handle(dev, stream))
     if st != 0:
         raise MbgluError(st, "glu_gemv")
     return out2.view(N) if squeeze else out

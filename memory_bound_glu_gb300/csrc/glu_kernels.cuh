@@ -67,9 +67,6 @@ struct GluParams {
     int *ws;                 // arrival counters, 0 between calls
     uint32_t off_s;
     int helper_warp;         // single-kernel path: the extra warp that writes the residual slice (-1: none)
-    // glu_gemv_ws: row groups past each warp's prefetched stages are claimed from
-    // claim[0] by all CTAs (claim[1] counts finished CTAs); nullptr: static shares
-    int *claim;
 };
 
 // ---------------------------------------------------------------------------
@@ -437,7 +434,6 @@ __device__ __forceinline__ void fused_residual_helper(const GluParams &p)
 constexpr int kHregChunks = 16;           // K <= 32 lanes * 16 chunks * 8 = 4096
 constexpr uint32_t kSlotGrpOffset = 512;  // bytes
 constexpr uint32_t kCounterOffset = 768;
-constexpr uint32_t kDoneOffset = 772;     // warps of this CTA done (claim mode)
 
 template <int MB, int R, bool NORM, bool HREG>
 __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(const GluParams p)
@@ -467,11 +463,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
                                    ? (all_groups - static_cast<int>(blockIdx.x) + gridDim.x - 1) / gridDim.x
                                    : 0)
                             : (r1 - r0 + R - 1) / R;
-    // claim mode: g is a global group index (rows g*R ..), rows end at N
-    const bool claim = p.claim != nullptr;
-    const int gr1 = claim ? p.N : r1;
     auto group_row0 = [&](int g) -> int {
-        if (claim) return g * R;
         return p.interleave ? (g * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x)) * R : r0 + g * R;
     };
     const bool contig = (p.ld_gate == K) && (p.ld_up == K) && (KS == K);
@@ -482,7 +474,6 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     if (threadIdx.x == 0) {
         *counter = 0;
-        *reinterpret_cast<int *>(smem + kDoneOffset) = 0;
         mbar_init(pro_bar, NORM ? 2 : 1);   // norm: the norm_w copy and the residual copy
     }
     fence_mbar_init();
@@ -492,7 +483,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
     // lane 0: request unit (group g, segment seg) into stage st
     auto issue = [&](int st, int g, int seg) {
         const int row0 = group_row0(g);
-        const int nr = min(R, gr1 - row0);
+        const int nr = min(R, r1 - row0);
         const int k0 = seg * KS;
         const int len = min(KS, K - k0);
         const uint32_t row_bytes = static_cast<uint32_t>(len) * 2u;
@@ -527,28 +518,8 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
     };
     // lane 0 state: the last unit requested
     int last_g = -1, last_seg = nseg;
-    // claim mode (whole rows, nseg == 1): the warp's first S groups are static
-    // (k * gridDim * NW + blockIdx * NW + warp), the rest come from claim[0]
-    // after the dependency wait; `pending` is a claim issued early
-    const int NWs = static_cast<int>(blockDim.x >> 5);
-    const int all_g = (p.N + R - 1) / R;
-    const int claim_base = S * static_cast<int>(gridDim.x) * NWs;
-    int prologue_k = 0, pending = -1;
     auto fill = [&](int st) {
-        if (claim) {
-            int gg;
-            if (prologue_k < S) {
-                gg = prologue_k * static_cast<int>(gridDim.x) * NWs + static_cast<int>(blockIdx.x) * NWs + warp;
-                ++prologue_k;
-            } else {
-                gg = pending >= 0 ? claim_base + pending : all_g;
-                pending = -1;
-            }
-            last_g = gg < all_g ? gg : -1;
-            last_seg = 0;
-        } else {
-            last_g = next_unit(last_g, last_seg);
-        }
+        last_g = next_unit(last_g, last_seg);
         slot_grp[st] = last_g;
         if (last_g >= 0) issue(st, last_g, last_seg);
     };
@@ -660,9 +631,6 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
             __syncwarp();
             return;
         }
-        // claim mode: ask for the group that will refill this stage now, so the
-        // atomic's round trip overlaps this unit's arithmetic
-        if (claim && lane == 0 && last_g >= 0 && prologue_k >= S) pending = atomicAdd(p.claim, 1);
         const int k0 = seg * KS;
         const int nch = min(KS, K - k0) >> 3;
         const uint16_t *wg = ring + st * stage_elems;
@@ -746,21 +714,8 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
                     ag[r][m] = au[r][m] = make_float2(0.0f, 0.0f);
                 }
             const int r = lane / MB, m = lane - (lane / MB) * MB;
-            if (lane < R * MB && m < p.M && row0 + r < gr1)
+            if (lane < R * MB && m < p.M && row0 + r < r1)
                 p.out[m * p.ldo + row0 + r] = glu_epilogue(gsel, usel, p.mode);
-        }
-    }
-    // claim mode: the last warp of the last CTA returns the counters to 0 (all
-    // claims are over by then); the next call touches them only after its
-    // dependency wait
-    if (claim) {
-        __syncwarp();
-        if (lane == 0 && atomicAdd(reinterpret_cast<int *>(smem + kDoneOffset), 1) == NWs - 1) {
-            __threadfence();
-            if (atomicAdd(p.claim + 1, 1) == static_cast<int>(gridDim.x) - 1) {
-                atomicExch(p.claim, 0);
-                atomicExch(p.claim + 1, 0);
-            }
         }
     }
 }

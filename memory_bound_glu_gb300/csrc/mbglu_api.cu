@@ -361,11 +361,41 @@ GluParams base_params(int M, int N, int K, int mode)
 
 }  // namespace
 
-namespace {
+extern "C" {
 
-mbglu_status glu_gemv_impl(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
-                           const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
-                           mbglu_mode mode, int *ws, cudaStream_t stream)
+int mbglu_abi_version(void) { return MBGLU_ABI_VERSION; }
+
+mbglu_status mbglu_set_launch_policy(int policy)
+{
+    if (policy != MBGLU_POLICY_SERIAL && policy != MBGLU_POLICY_PDL && policy != MBGLU_POLICY_PREFETCH)
+        return MBGLU_ERR_MODE;
+    g_policy.store(policy, std::memory_order_relaxed);
+    return MBGLU_OK;
+}
+
+int mbglu_get_launch_policy(void) { return g_policy.load(std::memory_order_relaxed); }
+int mbglu_last_cuda_error(void) { return t_last_cuda_error; }
+int mbglu_last_variant(void) { return t_last_variant; }
+
+const char *mbglu_status_string(mbglu_status s)
+{
+    switch (s) {
+    case MBGLU_OK: return "MBGLU_OK";
+    case MBGLU_ERR_NULL: return "MBGLU_ERR_NULL: a required pointer is NULL";
+    case MBGLU_ERR_SHAPE: return "MBGLU_ERR_SHAPE: unsupported M, N or K";
+    case MBGLU_ERR_STRIDE: return "MBGLU_ERR_STRIDE: a leading dimension is smaller than its row";
+    case MBGLU_ERR_ALIGN: return "MBGLU_ERR_ALIGN: a pointer is not 2-byte aligned";
+    case MBGLU_ERR_MODE: return "MBGLU_ERR_MODE: mode must be MBGLU_MODE_FUSED or MBGLU_MODE_HF";
+    case MBGLU_ERR_ALIAS: return "MBGLU_ERR_ALIAS: an output overlaps an input";
+    case MBGLU_ERR_CUDA: return "MBGLU_ERR_CUDA: a CUDA runtime call failed";
+    case MBGLU_ERR_TIMEOUT: return "MBGLU_ERR_TIMEOUT: a bounded device-side wait gave up";
+    default: return "unknown mbglu status";
+    }
+}
+
+mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
+                      const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
+                      mbglu_mode mode, cudaStream_t stream)
 {
     t_last_variant = kNone;
     if (mode != MBGLU_MODE_FUSED && mode != MBGLU_MODE_HF) return MBGLU_ERR_MODE;
@@ -379,13 +409,6 @@ mbglu_status glu_gemv_impl(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *g
     if (K > 0 && (overlaps(out, ob, h, matrix_bytes(M, K, ldh)) || overlaps(out, ob, gate_w, matrix_bytes(N, K, ld_gate)) ||
                   overlaps(out, ob, up_w, matrix_bytes(N, K, ld_up))))
         return MBGLU_ERR_ALIAS;
-    if (ws) {
-        const int64_t wsb = MBGLU_WORKSPACE_BYTES;
-        if (overlaps(ws, wsb, out, ob) ||
-            (K > 0 && (overlaps(ws, wsb, h, matrix_bytes(M, K, ldh)) || overlaps(ws, wsb, gate_w, matrix_bytes(N, K, ld_gate)) ||
-                       overlaps(ws, wsb, up_w, matrix_bytes(N, K, ld_up)))))
-            return MBGLU_ERR_ALIAS;
-    }
 
     const DeviceInfo *d = nullptr;
     mbglu_status st = device_info(&d);
@@ -445,7 +468,6 @@ mbglu_status glu_gemv_impl(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *g
         p.off_ring = pl.off_ring;
         p.vec_in = aligned(h, 16) && (ldh % 8 == 0);
         p.interleave = tuning().interleave;
-        if (ws && pl.nseg == 1) p.claim = ws;   // row groups claimed across CTAs
         st = launch_stream<false>(pl, p, stream, pdl);
         if (st == MBGLU_OK) t_last_variant = kStream;
         return st;
@@ -453,60 +475,6 @@ mbglu_status glu_gemv_impl(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *g
     st = launch(mbglu::glu_generic_kernel<false>, dim3(generic_grid(*d, N)), dim3(256), 0, stream, pdl, p);
     if (st == MBGLU_OK) t_last_variant = kGeneric;
     return st;
-}
-
-
-}  // namespace
-
-extern "C" {
-
-int mbglu_abi_version(void) { return MBGLU_ABI_VERSION; }
-
-mbglu_status mbglu_set_launch_policy(int policy)
-{
-    if (policy != MBGLU_POLICY_SERIAL && policy != MBGLU_POLICY_PDL && policy != MBGLU_POLICY_PREFETCH)
-        return MBGLU_ERR_MODE;
-    g_policy.store(policy, std::memory_order_relaxed);
-    return MBGLU_OK;
-}
-
-int mbglu_get_launch_policy(void) { return g_policy.load(std::memory_order_relaxed); }
-int mbglu_last_cuda_error(void) { return t_last_cuda_error; }
-int mbglu_last_variant(void) { return t_last_variant; }
-
-const char *mbglu_status_string(mbglu_status s)
-{
-    switch (s) {
-    case MBGLU_OK: return "MBGLU_OK";
-    case MBGLU_ERR_NULL: return "MBGLU_ERR_NULL: a required pointer is NULL";
-    case MBGLU_ERR_SHAPE: return "MBGLU_ERR_SHAPE: unsupported M, N or K";
-    case MBGLU_ERR_STRIDE: return "MBGLU_ERR_STRIDE: a leading dimension is smaller than its row";
-    case MBGLU_ERR_ALIGN: return "MBGLU_ERR_ALIGN: a pointer is not 2-byte aligned";
-    case MBGLU_ERR_MODE: return "MBGLU_ERR_MODE: mode must be MBGLU_MODE_FUSED or MBGLU_MODE_HF";
-    case MBGLU_ERR_ALIAS: return "MBGLU_ERR_ALIAS: an output overlaps an input";
-    case MBGLU_ERR_CUDA: return "MBGLU_ERR_CUDA: a CUDA runtime call failed";
-    case MBGLU_ERR_TIMEOUT: return "MBGLU_ERR_TIMEOUT: a bounded device-side wait gave up";
-    default: return "unknown mbglu status";
-    }
-}
-
-mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
-                      const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
-                      mbglu_mode mode, cudaStream_t stream)
-{
-    return glu_gemv_impl(h, ldh, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode, nullptr, stream);
-}
-
-mbglu_status glu_gemv_ws(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
-                         const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
-                         mbglu_mode mode, void *workspace, size_t workspace_bytes, cudaStream_t stream)
-{
-    t_last_variant = kNone;
-    if (!workspace) return MBGLU_ERR_NULL;
-    if (workspace_bytes < MBGLU_WORKSPACE_BYTES) return MBGLU_ERR_SHAPE;
-    if (!aligned(workspace, 16)) return MBGLU_ERR_ALIGN;
-    return glu_gemv_impl(h, ldh, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode,
-                         static_cast<int *>(workspace), stream);
 }
 
 }  // extern "C"

@@ -129,18 +129,3 @@ def norm_ws(ws=WS, nbytes=256, **kw):
 ])
 def test_add_rmsnorm_glu_ws_validation(kw, code):
     assert norm_ws(**kw) == code
-
-
-def gemv_ws(ws=WS, nbytes=256, **kw):
-    a = dict(h=H, ldh=64, g=G, ldg=64, u=U, ldu=64, o=O, ldo=32, M=2, N=32, K=64, mode=0)
-    a.update(kw)
-    return mb.lib().glu_gemv_ws(a["h"], a["ldh"], a["g"], a["ldg"], a["u"], a["ldu"], a["o"], a["ldo"], a["M"],
-                                a["N"], a["K"], a["mode"], ws, nbytes, None)
-
-
-@pytest.mark.parametrize("kw,code", [
-    (dict(ws=0), NULL), (dict(nbytes=8), SHAPE), (dict(ws=WS + 4), ALIGN), (dict(ws=O + 16), ALIAS),
-    (dict(ws=H), ALIAS), (dict(M=17), SHAPE), (dict(mode=9), MODE), (dict(M=0), OK),
-])
-def test_glu_gemv_ws_validation(kw, code):
-    assert gemv_ws(**kw) == code

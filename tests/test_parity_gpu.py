@@ -291,51 +291,6 @@ def test_launch_policies_give_identical_results(policy):
         assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 9728, 2560), (1, 3001, 1024), (2, 5000, 2560), (1, 100, 4096),
-                                   (1, 777, 5120), (2, 1, 64)])
-def test_glu_gemv_ws_claims_rows_and_matches_bitwise(M, N, K):
-    """Row groups claimed across CTAs: the same bits as glu_gemv, the
-    workspace back at zero, also back to back and replayed in a graph."""
-    h = gi.normal_bf16((M, K), 1.0, N, "cw-h").to(DEV)
-    gs = [gi.normal_bf16((N, K), K ** -0.5, N, "cw-g", i).to(DEV) for i in range(2)]
-    us = [gi.normal_bf16((N, K), K ** -0.5, N, "cw-u", i).to(DEV) for i in range(2)]
-    ws = mb.new_workspace(DEV)
-    for mode in ("hf", "fused"):
-        refs = [mb.glu_gemv(h, gs[i], us[i], mode=mode) for i in range(2)]
-        gots = [mb.glu_gemv(h, gs[i], us[i], mode=mode, workspace=ws) for i in range(2)]
-        torch.cuda.synchronize()
-        assert int(ws.sum()) == 0
-        for a, b in zip(refs, gots):
-            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=DEV) for _ in range(2)]
-    s = torch.cuda.Stream()
-    s.wait_stream(torch.cuda.current_stream())
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(s):
-        with torch.cuda.graph(graph, stream=s):
-            for i in range(2):
-                mb.glu_gemv(h, gs[i], us[i], out=outs[i], mode="fused", workspace=ws)
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    assert int(ws.sum()) == 0
-    for a, b in zip(gots, outs):
-        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-    assert mb.read_device_error() == 0
-
-
-def test_glu_gemv_ws_other_kernels_leave_workspace_alone():
-    M, N, K = 8, 1000, 2560          # tensor-core kernel: no claiming
-    h = gi.normal_bf16((M, K), 1.0, 1, "cwo-h").to(DEV)
-    g = gi.normal_bf16((N, K), K ** -0.5, 1, "cwo-g").to(DEV)
-    ws = mb.new_workspace(DEV)
-    ws[3] = 7
-    a = mb.glu_gemv(h, g, g, mode="hf")
-    b = mb.glu_gemv(h, g, g, mode="hf", workspace=ws)
-    torch.cuda.synchronize()
-    assert torch.equal(a.view(torch.int16), b.view(torch.int16)) and int(ws.sum()) == 7
-
-
 def test_swap_gate_and_up_matches_oracle_swap():
     M, N, K = 2, 777, 1024
     h = gi.normal_bf16((M, K), 1.0, 7, "sw-h")
