@@ -56,6 +56,8 @@ struct GluParams {
     int M, N, K, mode;
     int KS, nseg, stages;    // streaming kernel: segment length, #segments, ring depth
     uint32_t off_h, off_ring;
+    uint32_t off_piece;      // tensor-core kernel: handed-off accumulators, [warp][16][32] fp32
+    int tma;                 // tensor-core kernel: whole 8-row groups arrive as one tensor copy per matrix
     int vec_in;              // 1: h (or s, norm_w) may be read with 16-byte loads
     int prefetch;            // 1: first weight stages requested before the dependency wait
     int interleave;          // 1: this CTA's row groups are blockIdx.x, +gridDim.x, ... of all groups
@@ -731,15 +733,35 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
 //   B (16 x 8)  = 8 consecutive weight rows at k..k+15 (gate, then up);
 //   D (16 x 8)  = g (or u) for 16 batch rows x 8 output features.
 // A group is 8 consecutive rows; a unit is (group, K-segment of KS).  A stage
-// holds the unit's 8 gate rows then 8 up rows, each row a separate bulk copy
-// into a row padded by 16 bytes, so ldmatrix's 8 row addresses fall in 8
-// different 16-byte bank groups (no conflicts).  Lanes 0..15 issue the 16
-// copies of a stage together.  Rings, claiming, ordering with the preceding
-// grid and bounded waits are those of glu_stream_kernel.
+// holds the unit's 8 gate rows then 8 up rows at a pitch of KS + 8 elements:
+// (KS + 8) / 8 is odd, so ldmatrix's 8 row addresses fall in 8 different
+// 16-byte bank groups (no conflicts).  A whole group arrives as ONE tensor
+// copy per matrix: a (KS + 8) x 8 box at (k0, row0), whose 8 extra columns
+// are the next segment's first elements (read again from L2 by the next
+// unit) or zeros past K.  One request per matrix instead of one per row:
+// measured on GB300, 16 row copies of 0.5-0.6 KB per stage cost 9-30% of the
+// call.  A CTA's last, partial group is copied row by row (lanes 0..15)
+// into the same layout, so no row of another CTA's share is read.
 //
-// Shared memory (dynamic):  [0, 1024)          mbarriers, slot_grp, counter
-//                           [off_h, off_ring)  h_s[M + 1][K + 8] bf16 (row M = 0)
-//                           [off_ring, ...)    ring[warp][stage][16][KS + 8] bf16
+// Work split: the CTA's units, in (group, segment) order, are cut into one
+// contiguous range per ring-owning warp, equal to within one unit.  A CTA
+// holds only ~10 groups of 8 rows, so dealing out whole groups would leave
+// some warps a third more work than others.  A group cut between warps keeps
+// the exact arithmetic of an uncut one: the warp holding its first segments
+// runs them FIRST and parks its raw MMA accumulators in shared memory; the
+// next warp runs the rest of the group LAST, resuming those accumulators.
+// So each warp streams: [head of its last group, if cut] [whole groups]
+// [tail of its first group, if cut].  Heads never wait; a tail waits only on
+// a lower warp, so the hand-offs cannot deadlock, and every output's
+// arithmetic is independent of where its row falls.  Within a segment, even
+// and odd k16 steps go to two accumulator chains (halving the dependent MMA
+// chain), added in the epilogue.
+//
+// Shared memory (dynamic):  [0, 1024)            mbarriers (ring, prologue, hand-off)
+//                           [off_h, off_s)       h_s[M + 1][K + 8] bf16 (row M = 0)
+//                           [off_s, off_piece)   norm: norm_w[K] bf16
+//                           [off_piece, off_ring) parked[warp][16][32] fp32
+//                           [off_ring, ...)      ring[warp][stage][16][KS + 8] bf16
 __device__ __forceinline__ void ldmatrix_x4(uint32_t &a0, uint32_t &a1, uint32_t &a2, uint32_t &a3,
                                             const void *row)
 {
@@ -765,10 +787,17 @@ __device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], uint32_t a0, uin
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-constexpr int kMmaRows = 8;   // weight rows per group (the MMA's n)
+constexpr int kMmaRows = 8;                 // weight rows per group (the MMA's n)
+constexpr uint32_t kPieceBarOffset = 800;   // one mbarrier per ring-owning warp
+constexpr uint32_t kPieceBytes = 2048;      // one warp's parked accumulators: [16][32] fp32
+
+struct MmaMaps {
+    TensorMap gate, up;   // [N][K] bf16, row stride ld; box (KS + 8) x 8 rows
+};
 
 template <bool NORM>
-__global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const GluParams p)
+__global__ void __launch_bounds__(kMaxStreamWarps * 32, 1)
+    glu_mma_kernel(const GluParams p, const __grid_constant__ MmaMaps maps)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[kMaxWarps][kMaxM];
@@ -779,9 +808,10 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
     const int RS = KS + 8;                                   // padded ring row, elements
     const int HS = K + 8;                                    // padded h row, elements
     const int64_t stage_elems = static_cast<int64_t>(2) * kMmaRows * RS;
+    const bool helper = warp == p.helper_warp;   // single-kernel norm path only; owns no ring
+    const int W = p.helper_warp >= 0 ? p.helper_warp : static_cast<int>(blockDim.x >> 5);   // ring owners
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem) + warp * S;
-    int *slot_grp = reinterpret_cast<int *>(smem + kSlotGrpOffset) + warp * S;
-    int *counter = reinterpret_cast<int *>(smem + kCounterOffset);
+    uint64_t *piece_bar = reinterpret_cast<uint64_t *>(smem + kPieceBarOffset);
     uint16_t *h_s = reinterpret_cast<uint16_t *>(smem + p.off_h);
     uint16_t *ring = reinterpret_cast<uint16_t *>(smem + p.off_ring) + static_cast<int64_t>(warp) * S * stage_elems;
 
@@ -797,26 +827,55 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
     auto group_row0 = [&](int g) -> int {
         return p.interleave ? (g * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x)) * R : r0 + g * R;
     };
+    // warp w owns units [unit_begin(w), unit_begin(w + 1)), streamed as
+    //   A = [a0, u_end)      head of a group that continues in the next warp
+    //   B = [c1, a0)         whole groups
+    //   C = [u_begin, c1)    tail of a group begun by the previous warp
+    const int units = ngroups * nseg;
+    auto unit_begin = [&](int w) -> int { return static_cast<int>((static_cast<int64_t>(units) * w) / W); };
+    const int u_begin = helper ? 0 : unit_begin(warp);
+    const int u_end = helper ? 0 : unit_begin(warp + 1);
+    const bool cont = u_begin < u_end && u_begin % nseg != 0;
+    const int c1 = cont ? min(u_end, (u_begin / nseg + 1) * nseg) : u_begin;
+    const int a0 = (u_end % nseg != 0 && c1 < u_end) ? ((u_end - 1) / nseg) * nseg : u_end;
+    const int len_a = u_end - a0, len_ab = len_a + (a0 - c1), n_units = u_end - u_begin;
+    auto unit_of = [&](int i) -> int {
+        return i < len_a ? a0 + i : (i < len_ab ? c1 + (i - len_a) : u_begin + (i - len_ab));
+    };
 
     uint64_t *pro_bar = reinterpret_cast<uint64_t *>(smem + kProBarOffset);
-    const bool helper = warp == p.helper_warp;   // single-kernel norm path only; owns no ring
     if (lane == 0 && !helper)
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
     if (threadIdx.x == 0) {
-        *counter = 0;
         mbar_init(pro_bar, NORM ? 2 : 1);   // norm: the norm_w copy and the residual copy
+        for (int w = 0; w < W; ++w) mbar_init(&piece_bar[w], 32);
     }
     fence_mbar_init();
     __syncthreads();
 
     const uint64_t policy = l2_policy_evict_first();
-    // whole warp: request unit (group g, segment seg) into stage st.  Lane 0
-    // posts the byte count first; lanes 0..nr-1 copy gate rows, 8..8+nr-1 up rows.
-    auto issue = [&](int st, int g, int seg) {
+    // Tensor copies need 128-byte aligned destinations: every stage and its
+    // up half sit at multiples of 128 bytes from the ring (32 * (KS + 8) and
+    // 16 * (KS + 8) bytes with KS % 16 == 0), so checking the ring suffices.
+    const bool use_tma = p.tma && (smem_addr(smem + p.off_ring) & 127u) == 0u;
+    // whole warp: request unit u into stage st.  Lane 0 posts the byte count
+    // first; lanes 0..nr-1 copy gate rows, 8..8+nr-1 up rows.
+    auto issue = [&](int st, int u) {
+        const int g = u / nseg, seg = u - g * nseg;
         const int row0 = group_row0(g);
         const int nr = min(R, r1 - row0);
         const int k0 = seg * KS;
         const int len = min(KS, K - k0);
+        uint16_t *stage = ring + st * stage_elems;
+        if (use_tma && nr == R) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars[st], 2u * static_cast<uint32_t>(R * RS) * 2u);
+                tma_load_2d(stage, &maps.gate, k0, row0, &bars[st], policy);
+                tma_load_2d(stage + R * RS, &maps.up, k0, row0, &bars[st], policy);
+            }
+            __syncwarp();
+            return;
+        }
         const uint32_t row_bytes = static_cast<uint32_t>(len) * 2u;
         if (lane == 0) mbar_arrive_expect_tx(&bars[st], 2u * static_cast<uint32_t>(nr) * row_bytes);
         __syncwarp();
@@ -825,23 +884,12 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
             const bool up = lane >= 8;
             const uint16_t *src = up ? p.up + static_cast<int64_t>(row0 + r) * p.ld_up + k0
                                      : p.gate + static_cast<int64_t>(row0 + r) * p.ld_gate + k0;
-            uint16_t *dst = ring + st * stage_elems + static_cast<int64_t>((up ? R : 0) + r) * RS;
+            uint16_t *dst = stage + static_cast<int64_t>((up ? R : 0) + r) * RS;
             bulk_g2s(dst, src, row_bytes, &bars[st], policy);
         }
     };
-    int last_g = -1, last_seg = nseg;   // warp-uniform
-    auto fill = [&](int st) {
-        if (last_g >= 0 && last_seg + 1 < nseg) {
-            ++last_seg;
-        } else {
-            last_seg = 0;
-            int ng = 0;
-            if (lane == 0) ng = atomicAdd(counter, 1);
-            ng = __shfl_sync(0xffffffffu, ng, 0);
-            last_g = ng < ngroups ? ng : -1;
-        }
-        if (lane == 0) slot_grp[st] = last_g;
-        if (last_g >= 0) issue(st, last_g, last_seg);
+    auto prefill = [&]() {
+        for (int i = 0; i < S && i < n_units; ++i) issue(i, unit_of(i));
     };
 
     uint16_t *nw_s = reinterpret_cast<uint16_t *>(smem + p.off_s);   // norm: norm_w, K elements
@@ -855,15 +903,13 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
     };
     if (p.prefetch) {
         copy_norm_w();   // a weight, like gate_w / up_w
-        if (!helper)
-            for (int st = 0; st < S; ++st) fill(st);
+        prefill();
     }
     grid_dependency_wait();
     grid_launch_dependents();
     if (!p.prefetch) {
         copy_norm_w();
-        if (!helper)
-            for (int st = 0; st < S; ++st) fill(st);
+        prefill();
     }
     __syncwarp();
 
@@ -892,18 +938,12 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
         const int nch = K >> 3;
         for (int i = threadIdx.x; i < p.M * nch; i += blockDim.x) {
             const int m = i / nch, c = i - m * nch;
-            uint4 v;
-            if (p.vec_in) {
-                v = *reinterpret_cast<const uint4 *>(p.h + m * p.ldh + c * 8);
-            } else {
-                uint32_t w[4];
+            uint32_t w[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    w[q] = static_cast<uint32_t>(p.h[m * p.ldh + c * 8 + 2 * q]) |
-                           (static_cast<uint32_t>(p.h[m * p.ldh + c * 8 + 2 * q + 1]) << 16);
-                v = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * HS + c * 8) = v;
+            for (int q = 0; q < 4; ++q)
+                w[q] = static_cast<uint32_t>(p.h[m * p.ldh + c * 8 + 2 * q]) |
+                       (static_cast<uint32_t>(p.h[m * p.ldh + c * 8 + 2 * q + 1]) << 16);
+            *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * HS + c * 8) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
     for (int c = threadIdx.x; c < (K >> 3); c += blockDim.x)
@@ -922,20 +962,46 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
         return;
     }
 
-    float dg[4] = {0.f, 0.f, 0.f, 0.f}, du[4] = {0.f, 0.f, 0.f, 0.f};
-    int seg = nseg;
-    for (int u = 0;; ++u) {
-        const int st = u % S;
-        const int g = slot_grp[st];
-        if (g < 0) break;
-        seg = (seg + 1 < nseg) ? seg + 1 : 0;
-        const bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs);
+    // two chains per matrix: even k16 steps in *0, odd ones in *1
+    float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
+    float v0[4] = {0.f, 0.f, 0.f, 0.f}, v1[4] = {0.f, 0.f, 0.f, 0.f};
+    float *const parked = reinterpret_cast<float *>(smem + p.off_piece);
+    auto park = [&]() {   // hand this warp's accumulators to the next warp
+        float *slot = parked + warp * (kPieceBytes / 4);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            slot[q * 32 + lane] = g0[q];
+            slot[(4 + q) * 32 + lane] = g1[q];
+            slot[(8 + q) * 32 + lane] = v0[q];
+            slot[(12 + q) * 32 + lane] = v1[q];
+            g0[q] = g1[q] = v0[q] = v1[q] = 0.f;
+        }
+        mbar_arrive(&piece_bar[warp]);   // every lane: releases its own stores
+    };
+    for (int i = 0; i < n_units; ++i) {
+        const int u = unit_of(i), st = i % S;
+        const int g = u / nseg, seg = u - g * nseg;
+        bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((i / S) & 1), kWaitLimitNs);
+        if (i == len_ab && cont) {
+            // resume the accumulators of the warp holding the group's earlier
+            // segments: the nearest lower warp that owns units
+            int prev = warp - 1;
+            while (prev > 0 && unit_begin(prev) == unit_begin(prev + 1)) --prev;
+            ok = mbar_wait_bounded(&piece_bar[prev], 0u, kWaitLimitNs) && ok;
+            const float *slot = parked + prev * (kPieceBytes / 4);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                g0[q] = slot[q * 32 + lane];
+                g1[q] = slot[(4 + q) * 32 + lane];
+                v0[q] = slot[(8 + q) * 32 + lane];
+                v1[q] = slot[(12 + q) * 32 + lane];
+            }
+        }
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) {
                 atomicExch(&g_device_error, kErrTimeout);
-                for (int v = u; v < u + S; ++v)
-                    if (slot_grp[v % S] >= 0)
-                        mbar_wait_bounded(&bars[v % S], static_cast<uint32_t>((v / S) & 1), kWaitLimitNs);
+                for (int j = i; j < min(i + S, n_units); ++j)   // drain this warp's copies in flight
+                    mbar_wait_bounded(&bars[j % S], static_cast<uint32_t>((j / S) & 1), kWaitLimitNs);
             }
             __syncwarp();
             return;
@@ -945,30 +1011,53 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_mma_kernel(const 
         const uint16_t *wg = ring + st * stage_elems + b_off;
         const uint16_t *wu = wg + R * RS;
         const uint16_t *ha = a_base + k0;
-#pragma unroll 4
-        for (int kk = 0; kk < nk; ++kk) {
-            uint32_t a0, a1, a2, a3, g0, g1, u0, u1;
-            ldmatrix_x4(a0, a1, a2, a3, ha + kk * 16);
-            ldmatrix_x2(g0, g1, wg + kk * 16);
-            ldmatrix_x2(u0, u1, wu + kk * 16);
-            mma_bf16_16x8x16(dg, a0, a1, a2, a3, g0, g1);
-            mma_bf16_16x8x16(du, a0, a1, a2, a3, u0, u1);
+        int kk = 0;
+#pragma unroll 2
+        for (; kk + 1 < nk; kk += 2) {
+            uint32_t a0r, a1r, a2r, a3r, b0, b1, c0, c1r;
+            ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16);
+            ldmatrix_x2(b0, b1, wg + kk * 16);
+            ldmatrix_x2(c0, c1r, wu + kk * 16);
+            mma_bf16_16x8x16(g0, a0r, a1r, a2r, a3r, b0, b1);
+            mma_bf16_16x8x16(v0, a0r, a1r, a2r, a3r, c0, c1r);
+            ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16 + 16);
+            ldmatrix_x2(b0, b1, wg + kk * 16 + 16);
+            ldmatrix_x2(c0, c1r, wu + kk * 16 + 16);
+            mma_bf16_16x8x16(g1, a0r, a1r, a2r, a3r, b0, b1);
+            mma_bf16_16x8x16(v1, a0r, a1r, a2r, a3r, c0, c1r);
+        }
+        if (kk < nk) {
+            uint32_t a0r, a1r, a2r, a3r, b0, b1, c0, c1r;
+            ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16);
+            ldmatrix_x2(b0, b1, wg + kk * 16);
+            ldmatrix_x2(c0, c1r, wu + kk * 16);
+            mma_bf16_16x8x16(g0, a0r, a1r, a2r, a3r, b0, b1);
+            mma_bf16_16x8x16(v0, a0r, a1r, a2r, a3r, c0, c1r);
         }
         __syncwarp();
-        if (lane == 0) fence_proxy_async_smem();
-        fill(st);   // the unit S ahead of u, or -1 once the CTA's groups run out
+        if (i + S < n_units) {
+            if (lane == 0) fence_proxy_async_smem();
+            issue(st, unit_of(i + S));   // the unit S ahead, into the stage just read
+        }
         __syncwarp();
-        if (seg == nseg - 1) {
-            // D layout: d[0], d[1] -> batch row lane/4, features 2*(lane%4) + 0, 1;
-            //           d[2], d[3] -> batch row lane/4 + 8, same features.
-            const int row0 = group_row0(g);
-            const int m0 = lane >> 2, n = row0 + 2 * (lane & 3);
+        if (i == len_a - 1) {   // end of A: the group continues in the next warp
+            park();
+            continue;
+        }
+        if (seg != nseg - 1) {
+            if (i == n_units - 1) park();   // C inside one group: it continues in the next warp too
+            continue;
+        }
+        // the group is complete.  D layout: d[0], d[1] -> batch row lane/4,
+        // features 2*(lane%4) + 0, 1; d[2], d[3] -> batch row lane/4 + 8.
+        const int row0 = group_row0(g);
+        const int m0 = lane >> 2, n = row0 + 2 * (lane & 3);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int m = m0 + (q >> 1) * 8, nn = n + (q & 1);
-                if (m < p.M && nn < r1 && nn < row0 + R) p.out[m * p.ldo + nn] = glu_epilogue(dg[q], du[q], p.mode);
-                dg[q] = du[q] = 0.f;
-            }
+        for (int q = 0; q < 4; ++q) {
+            const int m = m0 + (q >> 1) * 8, nn = n + (q & 1);
+            if (m < p.M && nn < r1 && nn < row0 + R)
+                p.out[m * p.ldo + nn] = glu_epilogue(g0[q] + g1[q], v0[q] + v1[q], p.mode);
+            g0[q] = g1[q] = v0[q] = v1[q] = 0.f;
         }
     }
 }

@@ -7,11 +7,13 @@
 // commits on stale pointer-keyed caches: in-place weight updates must always
 // be seen).
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "mbglu.h"
@@ -32,8 +34,12 @@ static_assert(mbglu::kMaxStreamWarps * 8 * 8 <= mbglu::kSlotGrpOffset, "mbarrier
 static_assert(mbglu::kSlotGrpOffset + mbglu::kMaxStreamWarps * 8 * 4 <= mbglu::kCounterOffset,
               "stage table overflows its region");
 static_assert(mbglu::kCounterOffset + 4 <= mbglu::kProBarOffset, "counter overlaps the prologue barrier");
-static_assert(mbglu::kProBarOffset % 8 == 0 && mbglu::kProBarOffset + 8 <= kBarRegion, "prologue barrier outside the region");
+static_assert(mbglu::kProBarOffset % 8 == 0 && mbglu::kProBarOffset + 8 <= mbglu::kPieceBarOffset,
+              "prologue barrier overlaps the piece barriers");
+static_assert(mbglu::kPieceBarOffset % 8 == 0 && mbglu::kPieceBarOffset + mbglu::kMaxStreamWarps * 8 <= kBarRegion,
+              "piece barriers outside the region");
 constexpr int kMaxStages = 8;
+constexpr int kMmaKsCap = 240;               // tensor-core segment: its box (KS + 8) x 8 must be <= 256 wide
 constexpr int64_t kNormMaxMK = 81920;        // add_rmsnorm_glu: M*K*2 bytes of normed rows in smem
 
 struct DeviceInfo {
@@ -57,6 +63,8 @@ struct Tuning {
     int waves = 1;            // CTAs per resident CTA slot (grid = SMs * ctas_per_sm * waves)
     int interleave = 0;       // row groups dealt round-robin over CTAs instead of contiguous blocks
     int mma_min_m = 3;        // smallest batch that takes the tensor-core kernel (17: never)
+    int mma_ks_min = 192;     // tensor-core plan: shortest K-segment worth one more warp
+    int tma = 1;              // tensor-core kernel: whole groups by tensor copy (0: row by row)
 };
 
 std::atomic<int> g_policy{MBGLU_POLICY_PREFETCH};
@@ -82,6 +90,8 @@ const Tuning &tuning()
         x.waves = std::min(16, std::max(1, env_int("MBGLU_WAVES", 1)));
         x.interleave = env_int("MBGLU_INTERLEAVE", 0) != 0;
         x.mma_min_m = std::min(17, std::max(1, env_int("MBGLU_MMA_MIN_M", 3)));
+        x.mma_ks_min = std::max(16, env_int("MBGLU_MMA_KS_MIN", 192));
+        x.tma = env_int("MBGLU_TMA", 1) != 0;
         return x;
     }();
     return t;
@@ -196,7 +206,7 @@ int default_rows(int MB, int K, bool contiguous)
 struct Plan {
     int MB = 1, R = 1, warps = 4, KS = 0, nseg = 0, stages = 0, grid = 0, ctas_per_sm = 1;
     bool hreg = false;
-    uint32_t off_h = 0, off_s = 0, off_ring = 0, smem = 0;
+    uint32_t off_h = 0, off_s = 0, off_piece = 0, off_ring = 0, smem = 0;
 };
 
 // Streaming-kernel plan.  Whole rows per stage (K-segments only if a stage of
@@ -265,11 +275,15 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
     return true;
 }
 
-// Tensor-core plan (batch >= mma_min_m, K % 16 == 0): groups of 8 rows,
-// K-segments of a multiple of 16 dividing K (<= 768 elements), each row
-// padded by 16 bytes; h_s holds M rows plus a zero row.  Two stages per warp,
-// as many warps (<= 8) as fit; segments shrink (>= 256) while fewer than 4
-// warps fit.  False if nothing fits.
+// Tensor-core plan (batch >= mma_min_m, K % 16 == 0): groups of 8 rows, each
+// row of a stage padded by 16 bytes; h_s holds M rows plus a zero row; 2 KB
+// per warp for handed-off accumulators; two stages per warp.  For each warp
+// count the longest K-segment (multiple of 16, <= 240: the tensor copy's box
+// is KS + 8 <= 256 elements wide) that fits is taken;
+// the plan is the most warps whose segment is still >= mma_ks_min elements
+// (measured on GB300: at equal ring bytes more warps win, while row copies
+// under 512 bytes lose), else the warp count with the largest ring.
+// Segments are then evened out over K.  False if nothing fits.
 bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl, uint32_t extra = 0,
               int max_warps = mbglu::kMaxStreamWarps)
 {
@@ -281,35 +295,44 @@ bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl, uint32_t extra
     const uint32_t hbytes = (static_cast<uint32_t>(M + 1) * static_cast<uint32_t>(K + 8) * 2u + 127u) & ~127u;
     const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes - extra;
     if (room <= 0) return false;
-    int ks = 0;
-    if (t.ks > 0) {
-        ks = std::max(16, std::min(t.ks, K) & ~15);
-    } else {
-        for (int c = 768; c >= 16; c -= 16)
-            if (K % c == 0) { ks = c; break; }
-        if (ks < 256) ks = std::min(K, 512);
-    }
     const int want_s = t.stages > 0 ? t.stages : 2;
-    for (;;) {
-        const int64_t stage = static_cast<int64_t>(2) * mbglu::kMmaRows * (ks + 8) * 2;
-        int w = t.warps > 0 ? std::min(t.warps, max_warps) : max_warps;
-        while (w > 1 && static_cast<int64_t>(w) * want_s * stage > room) --w;
-        if (static_cast<int64_t>(w) * 2 * stage > room) w = 0;
-        if (w >= 4 || (w >= 1 && (ks <= 256 || t.warps > 0 || t.ks > 0))) {
-            pl.warps = w;
-            pl.stages = static_cast<int>(std::min<int64_t>(want_s, room / (stage * w)));
-            pl.KS = ks;
-            break;
-        }
-        if (ks <= 256) return false;
-        ks = std::max(256, (ks / 2) & ~15);
+    const int64_t piece = mbglu::kPieceBytes;
+    const int64_t row_unit = 2 * mbglu::kMmaRows * 2;   // stage bytes per padded element of a row
+    const int ks_cap = std::min(kMmaKsCap, K);
+    int best_w = 0;
+    int64_t best_ring = 0;
+    int ks_of[mbglu::kMaxStreamWarps + 1] = {};
+    int64_t ring_of[mbglu::kMaxStreamWarps + 1] = {};
+    for (int w = 1; w <= max_warps; ++w) {
+        if (t.warps > 0 && w != std::min(t.warps, max_warps)) continue;
+        const int64_t per_stage = (room / w - piece) / want_s;
+        int ks = static_cast<int>(std::min<int64_t>(ks_cap, (per_stage / row_unit - 8) & ~int64_t{15}));
+        if (t.ks > 0) ks = (std::min(t.ks, K) & ~15) <= ks ? (std::min(t.ks, K) & ~15) : 0;
+        if (ks < 16) continue;
+        ks_of[w] = ks;
+        ring_of[w] = static_cast<int64_t>(w) * want_s * row_unit * (ks + 8);
+        if (ring_of[w] > best_ring) best_ring = ring_of[w];
     }
+    if (best_ring == 0) return false;
+    for (int w = max_warps; w >= 1 && best_w == 0; --w)
+        if (ring_of[w] > 0 && ks_of[w] >= std::min(t.mma_ks_min, ks_cap)) best_w = w;
+    for (int w = max_warps; w >= 1 && best_w == 0; --w)
+        if (ring_of[w] == best_ring) best_w = w;
+    int ks = ks_of[best_w];
+    if (t.ks <= 0) {   // even the segments out: same count, lengths within 16
+        const int nseg = (K + ks - 1) / ks;
+        ks = ((K + nseg - 1) / nseg + 15) & ~15;
+    }
+    pl.warps = best_w;
+    pl.stages = want_s;
+    pl.KS = ks;
     pl.MB = 16;
     pl.R = mbglu::kMmaRows;
     pl.nseg = (K + pl.KS - 1) / pl.KS;
     pl.off_h = kBarRegion;
     pl.off_s = kBarRegion + hbytes;
-    pl.off_ring = kBarRegion + hbytes + extra;
+    pl.off_piece = kBarRegion + hbytes + extra;
+    pl.off_ring = pl.off_piece + static_cast<uint32_t>(pl.warps) * mbglu::kPieceBytes;
     pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 2u * mbglu::kMmaRows *
                                 static_cast<uint32_t>(pl.KS + 8) * 2u;
     pl.grid = std::max(1, std::min(d.sm_count, N));
@@ -332,6 +355,72 @@ mbglu_status launch(void (*kernel)(Args...), dim3 grid, dim3 block, uint32_t sme
     cfg.numAttrs = pdl ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p);
     return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
+}
+
+mbglu_status launch_mma(void (*kernel)(GluParams, mbglu::MmaMaps), dim3 grid, dim3 block, uint32_t smem,
+                        cudaStream_t stream, bool pdl, const GluParams &p, const mbglu::MmaMaps &maps)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, p, maps);
+    return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
+}
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link against libcuda); null if unavailable.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+
+// Descriptor of an [N][K] bf16 weight (row stride ld elements) read in boxes
+// of box_k x 8 rows; elements past K or N read as zero.  False if the driver
+// rejects it (the kernel then copies row by row).
+bool encode_weight_map(mbglu::TensorMap *out, const void *base, int64_t ld, int N, int K, int box_k)
+{
+    static_assert(sizeof(CUtensorMap) == sizeof(mbglu::TensorMap), "tensor map size");
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (!fn || box_k > 256) return false;
+    CUtensorMap m;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(mbglu::kMmaRows)};
+    const cuuint32_t elem_strides[2] = {1u, 1u};
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::memcpy(out, &m, sizeof m);
+    return true;
+}
+
+// Both weight descriptors for a tensor-core launch; p.tma says whether they
+// are used.
+mbglu::MmaMaps weight_maps(GluParams &p)
+{
+    mbglu::MmaMaps maps = {};
+    p.tma = (tuning().tma && encode_weight_map(&maps.gate, p.gate, p.ld_gate, p.N, p.K, p.KS + 8) &&
+             encode_weight_map(&maps.up, p.up, p.ld_up, p.N, p.K, p.KS + 8))
+                ? 1
+                : 0;
+    return maps;
 }
 
 template <bool NORM>
@@ -453,9 +542,12 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
         p.stages = pl.stages;
         p.off_h = pl.off_h;
         p.off_ring = pl.off_ring;
+        p.off_piece = pl.off_piece;
         p.vec_in = aligned(h, 16) && (ldh % 8 == 0);
         p.interleave = tuning().interleave;
-        st = launch(mbglu::glu_mma_kernel<false>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
+        const mbglu::MmaMaps maps = weight_maps(p);
+        st = launch_mma(mbglu::glu_mma_kernel<false>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p,
+                        maps);
         if (st == MBGLU_OK) t_last_variant = kTensor;
         return st;
     }
@@ -550,9 +642,11 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
             p.off_h = pl.off_h;
             p.off_s = pl.off_s;
             p.off_ring = pl.off_ring;
+            p.off_piece = pl.off_piece;
             p.helper_warp = pl.warps;   // one extra warp writes the residual slice
-            st = launch(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3((pl.warps + 1) * 32), pl.smem, stream,
-                        pdl, p);
+            const mbglu::MmaMaps maps = weight_maps(p);
+            st = launch_mma(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3((pl.warps + 1) * 32), pl.smem, stream,
+                            pdl, p, maps);
             if (st == MBGLU_OK) t_last_variant = kTensor;
             return st;
         }
@@ -609,7 +703,10 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
         p.off_h = pl.off_h;
         p.off_s = pl.off_s;
         p.off_ring = pl.off_ring;
-        st = launch(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p);
+        p.off_piece = pl.off_piece;
+        const mbglu::MmaMaps maps = weight_maps(p);
+        st = launch_mma(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p,
+                        maps);
         if (st == MBGLU_OK) t_last_variant = kTensor;
         return st;
     }

@@ -28,6 +28,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// Plain arrival (release at CTA scope: the arriving thread's earlier shared
+// stores are visible to a thread whose wait on the phase succeeds).
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase)
 {
     uint32_t ok;
@@ -85,6 +92,26 @@ __device__ __forceinline__ void bulk_g2s_plain(void *dst, const void *src, uint3
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// A TMA tensor descriptor (CUtensorMap: 128 opaque bytes, 64-byte aligned),
+// encoded on the host and passed as a __grid_constant__ kernel parameter.
+struct alignas(64) TensorMap {
+    uint64_t opaque[16];
+};
+
+// Tiled tensor copy of one 2-D box at element coordinates (x, y) (x
+// innermost) into this CTA's shared memory (128-byte aligned); the whole
+// box's bytes -- elements outside the tensor arrive as zeros -- are counted
+// on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *dst, const TensorMap *map, int x, int y, uint64_t *bar,
+                                            uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
 
