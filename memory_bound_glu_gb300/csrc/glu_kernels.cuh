@@ -266,25 +266,42 @@ __device__ __forceinline__ void prologue_wait(uint64_t *bar)
     }
 }
 
-// Single-kernel add_rmsnorm_glu, part 1.  The residual rows have been
-// copied into h_s (row stride hstride); s = bf16(x + residual) is formed there
-// in place, x read straight from global memory (the first kXPre chunks per
-// thread are loaded before the copy is awaited).  The fp32 sum of two bf16
-// values rounds to the same bf16 as the exact sum.
-constexpr int kXPre = 8;   // x chunks per thread loaded before the residual copy is awaited, and per batch after
-
-struct XPrefetch {
-    uint4 v[kXPre];
+// Row-owned prologue of the streaming kernels (operands 16-byte aligned, the
+// residual rows already copied into shared memory h_s).  The block's threads
+// are split evenly over the M rows: thread t owns row m = t / P (P = blockDim
+// / M threads per row) and its 16-byte chunks c = t % P + j * P.  A thread's
+// row never changes, so its sum of squares is one register and no chunk
+// needs a division; consecutive threads touch consecutive chunks of a row,
+// so shared accesses are conflict-free for any row pitch and global loads of
+// x are coalesced.  Measured on GB300 at M = 8, K = 2560: the earlier
+// chunk-major loops (a division and 16 unrolled row slots per chunk) took
+// 4.4 us for the statistic and the scale alone.
+struct RowMap {
+    int m, c0, P, nch;
+    bool active;
 };
 
-__device__ __forceinline__ void fused_x_prefetch(const GluParams &p, XPrefetch &xp)
+__device__ __forceinline__ RowMap row_map(int M, int K)
 {
-    const int n = p.M * (p.K >> 3);
+    RowMap r;
+    r.P = static_cast<int>(blockDim.x) / M;
+    r.m = static_cast<int>(threadIdx.x) / r.P;
+    r.c0 = static_cast<int>(threadIdx.x) - r.m * r.P;
+    r.active = r.m < M;
+    r.nch = K >> 3;
+    return r;
+}
+
+__device__ __forceinline__ float sum_squares_bf16x8(uint4 v, float ss)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int j = 0; j < kXPre; ++j) {
-        const int i = threadIdx.x + j * blockDim.x;
-        xp.v[j] = i < n ? reinterpret_cast<const uint4 *>(p.x)[i] : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < 4; ++j) {
+        const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+        ss = fmaf(a, a, ss);
+        ss = fmaf(b, b, ss);
     }
+    return ss;
 }
 
 __device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b)
@@ -296,35 +313,107 @@ __device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b)
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-// Adds the chunks base + j*blockDim (j < kXPre) of x, held in xp, into h_s.
-__device__ __forceinline__ void fused_add_batch(const GluParams &p, uint16_t *h_s, int hstride, const XPrefetch &xp,
-                                                int base)
+// Single-kernel add_rmsnorm_glu: x is read straight from global memory, the
+// first kXRows chunks of each thread before the residual copy is awaited (one
+// round trip for M*K <= 16 * blockDim * 8, e.g. M = 8, K = 4096 at 256
+// threads), the rest in batches of kXRows independent loads.
+constexpr int kXRows = 16;
+
+struct XRows {
+    uint4 v[kXRows];
+};
+
+__device__ __forceinline__ void x_prefetch_rows(const GluParams &p, const RowMap &r, XRows &x, int j0 = 0)
 {
-    const int nch = p.K >> 3, n = p.M * nch;
+    const uint4 *xrow = reinterpret_cast<const uint4 *>(p.x) + static_cast<int64_t>(r.m) * r.nch;
 #pragma unroll
-    for (int j = 0; j < kXPre; ++j) {
-        const int i = base + j * blockDim.x;
-        if (i < n) {
-            const int m = i / nch, c = i - m * nch;
-            uint4 *hp = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * hstride + c * 8);
-            *hp = add_bf16x8(xp.v[j], *hp);
-        }
+    for (int j = 0; j < kXRows; ++j) {
+        const int c = r.c0 + (j0 + j) * r.P;
+        x.v[j] = (r.active && c < r.nch) ? xrow[c] : make_uint4(0, 0, 0, 0);
     }
 }
 
-__device__ __forceinline__ void fused_add_in_place(const GluParams &p, uint16_t *h_s, int hstride, XPrefetch &xp)
+// s = bf16(x + residual) formed in place in h_s (the fp32 sum of two bf16
+// values rounds to the same bf16 as the exact sum); returns this thread's
+// sum of s^2 over its chunks, in chunk order.
+__device__ __forceinline__ float add_rows_in_place(const GluParams &p, const RowMap &r, uint16_t *h_s, int hstride,
+                                                   XRows &x)
 {
-    const int n = p.M * (p.K >> 3);
-    fused_add_batch(p, h_s, hstride, xp, threadIdx.x);
-    // the rest in batches of kXPre independent loads, so their latencies overlap
-    for (int base = threadIdx.x + kXPre * blockDim.x; base < n; base += kXPre * blockDim.x) {
+    float ss = 0.0f;
+    uint4 *row = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
+    for (int j0 = 0;; j0 += kXRows) {
+        if (j0 > 0) x_prefetch_rows(p, r, x, j0);
 #pragma unroll
-        for (int j = 0; j < kXPre; ++j) {
-            const int i = base + j * blockDim.x;
-            xp.v[j] = i < n ? reinterpret_cast<const uint4 *>(p.x)[i] : make_uint4(0, 0, 0, 0);
+        for (int j = 0; j < kXRows; ++j) {
+            const int c = r.c0 + (j0 + j) * r.P;
+            if (r.active && c < r.nch) {
+                const uint4 sv = add_bf16x8(x.v[j], row[c]);
+                row[c] = sv;
+                ss = sum_squares_bf16x8(sv, ss);
+            }
         }
-        fused_add_batch(p, h_s, hstride, xp, base);
+        if (!r.active || r.c0 + (j0 + kXRows) * r.P >= r.nch) break;
     }
+    return ss;
+}
+
+// This thread's sum of s^2 over its chunks of h_s, in chunk order.
+__device__ __forceinline__ float square_rows(const RowMap &r, const uint16_t *h_s, int hstride)
+{
+    float ss = 0.0f;
+    if (!r.active) return ss;
+    const uint4 *row = reinterpret_cast<const uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
+#pragma unroll 4
+    for (int c = r.c0; c < r.nch; c += r.P) ss = sum_squares_bf16x8(row[c], ss);
+    return ss;
+}
+
+// Zero-centred RMSNorm of the rows in h_s, in place (PR #9057 "Changes"):
+//   var = mean_k s^2 (fp32), inv = 1 / sqrt(var + eps),
+//   h = bf16( (s * inv) * (1 + w) ) with the (1 + w) scale built in fp32.
+// ss: this thread's partial sum from square_rows or add_rows_in_place.  Row
+// m's partials are added by one warp (lane-strided, then a butterfly): a
+// fixed order, and every CTA computes the identical h.  part: blockDim
+// floats of shared memory; inv_s: M floats.  Rows M..rows_out-1 of h_s
+// become zero.  Ends with a barrier.
+__device__ __forceinline__ void norm_rows_in_place(const GluParams &p, const RowMap &r, float ss, uint16_t *h_s,
+                                                   int hstride, const uint16_t *w_s, float *part, float *inv_s,
+                                                   int rows_out)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    part[tid] = ss;
+    __syncthreads();
+    for (int m = warp; m < p.M; m += nw) {
+        float t = 0.0f;
+        for (int i = lane; i < r.P; i += 32) t += part[m * r.P + i];
+        t = warp_allsum(t);
+        if (lane == 0) inv_s[m] = 1.0f / sqrtf(t / static_cast<float>(p.K) + p.eps);
+    }
+    __syncthreads();
+    if (r.active) {
+        const float inv = inv_s[r.m];
+        uint4 *row = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
+        const uint4 *wv = reinterpret_cast<const uint4 *>(w_s);
+#pragma unroll 4
+        for (int c = r.c0; c < r.nch; c += r.P) {
+            const uint4 v = row[c], w = wv[c];
+            const uint32_t sv[4] = {v.x, v.y, v.z, v.w};
+            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float lo = (bf16_lo(sv[j]) * inv) * (1.0f + bf16_lo(ww[j]));
+                const float hi = (bf16_hi(sv[j]) * inv) * (1.0f + bf16_hi(ww[j]));
+                o[j] = pack_bf16x2(lo, hi);
+            }
+            row[c] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    }
+    for (int i = tid; i < (rows_out - p.M) * r.nch; i += blockDim.x) {
+        const int m = p.M + i / r.nch, c = i - (i / r.nch) * r.nch;
+        *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * hstride + c * 8) = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();
 }
 
 // Part 2.  Workspace: ws[0] counts CTAs that hold their residual rows (the
@@ -441,7 +530,7 @@ template <int MB, int R, bool NORM, bool HREG>
 __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(const GluParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[kMaxWarps][MB];
+    __shared__ float red[kMaxStreamWarps * 32];   // norm: one partial sum per thread
     __shared__ float inv_s[MB];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -557,16 +646,18 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
             mbar_arrive_expect_tx(pro_bar, bytes);
             bulk_g2s_plain(h_s, p.s, bytes, pro_bar);   // residual rows into h_s rows 0..M-1
         }
-        XPrefetch xp;
-        if (p.fused) fused_x_prefetch(p, xp);
+        const RowMap rm = row_map(p.M, K);
+        XRows xr;
+        if (p.fused) x_prefetch_rows(p, rm, xr);
         prologue_wait(pro_bar);
+        float ss;
         if (p.fused) {
             if (threadIdx.x == 0) fused_arrive(p);
-            fused_add_in_place(p, h_s, K, xp);
-            __syncthreads();
+            ss = add_rows_in_place(p, rm, h_s, K, xr);
+        } else {
+            ss = square_rows(rm, h_s, K);
         }
-        norm_prologue<MB>(p, h_s, red, inv_s, MB, K, h_s, K, nw_s);
-        __syncthreads();
+        norm_rows_in_place(p, rm, ss, h_s, K, nw_s, red, inv_s, MB);
     } else if constexpr (!HREG) {
         if (p.vec_in) {
             if (threadIdx.x == 0) {
@@ -800,7 +891,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1)
     glu_mma_kernel(const GluParams p, const __grid_constant__ MmaMaps maps)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[kMaxWarps][kMaxM];
+    __shared__ float red[kMaxStreamWarps * 32];   // norm: one partial sum per thread
     __shared__ float inv_s[kMaxM];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -919,15 +1010,18 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1)
             mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u);
             copy_rows_async(h_s, HS, p.s, K, p.M, K, pro_bar);   // residual rows, padded
         }
-        XPrefetch xp;
-        if (p.fused) fused_x_prefetch(p, xp);
+        const RowMap rm = row_map(p.M, K);
+        XRows xr;
+        if (p.fused) x_prefetch_rows(p, rm, xr);
         prologue_wait(pro_bar);
+        float ss;
         if (p.fused) {
             if (threadIdx.x == 0) fused_arrive(p);
-            fused_add_in_place(p, h_s, HS, xp);
-            __syncthreads();
+            ss = add_rows_in_place(p, rm, h_s, HS, xr);
+        } else {
+            ss = square_rows(rm, h_s, HS);
         }
-        norm_prologue<kMaxM>(p, h_s, red, inv_s, p.M, HS, h_s, HS, nw_s);
+        norm_rows_in_place(p, rm, ss, h_s, HS, nw_s, red, inv_s, p.M);
     } else if (p.vec_in) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u);
