@@ -886,12 +886,14 @@ struct MmaMaps {
     TensorMap gate, up;   // [N][K] bf16, row stride ld; box (KS + 8) x 8 rows
 };
 
+// Up to kMaxStreamWarps ring-owning warps, plus the helper warp on the
+// single-kernel norm path.
 template <bool NORM>
-__global__ void __launch_bounds__(kMaxStreamWarps * 32, 1)
+__global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     glu_mma_kernel(const GluParams p, const __grid_constant__ MmaMaps maps)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[kMaxStreamWarps * 32];   // norm: one partial sum per thread
+    __shared__ float red[(kMaxStreamWarps + 1) * 32];   // norm: one partial sum per thread
     __shared__ float inv_s[kMaxM];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

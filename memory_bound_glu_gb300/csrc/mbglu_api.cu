@@ -635,7 +635,7 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
         p.x = x;
         p.residual = residual;
         p.ws = ws;
-        if (plan_mma(*d, M, N, K, pl, sbytes, mbglu::kMaxStreamWarps - 1)) {
+        if (plan_mma(*d, M, N, K, pl, sbytes)) {   // + the helper warp: up to kMaxStreamWarps + 1 warps
             p.KS = pl.KS;
             p.nseg = pl.nseg;
             p.stages = pl.stages;
