@@ -38,6 +38,8 @@ import glu_inputs as gi  # noqa: E402
 
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+# mbglu_last_variant() -> the kernel that streams the weights
+KERNEL_NAMES = {1: "glu_stream_kernel", 2: "glu_generic_kernel", 4: "glu_mma_kernel"}
 KERNEL_SOURCES = ["memory_bound_glu_gb300/csrc/glu_kernels.cuh", "memory_bound_glu_gb300/csrc/ptx.cuh",
                   "memory_bound_glu_gb300/csrc/mbglu_api.cu"]
 
@@ -343,6 +345,7 @@ def main():
     with torch.cuda.stream(stream):
         one_step()  # first calls initialise the library's per-device table before capture
         torch.cuda.synchronize(dev)
+        kernel_name = KERNEL_NAMES.get(mb.last_variant(), f"variant {mb.last_variant()}")
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             one_step()
@@ -439,7 +442,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": round(gbs, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "traffic": traffic, "kernel": "glu_stream_kernel",
+                         "traffic": traffic, "kernel": kernel_name,
                          "achieved_how": "algorithmic bytes per launch / (CUDA-event time of the timed "
                                          "graph replays / launches)"},
             "gpu_launches": calls * launches_per_call,
