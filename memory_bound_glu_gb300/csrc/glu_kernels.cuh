@@ -57,6 +57,8 @@ struct GluParams {
     int KS, nseg, stages;    // streaming kernel: segment length, #segments, ring depth
     uint32_t off_h, off_ring;
     uint32_t off_piece;      // tensor-core kernel: handed-off accumulators, [warp][16][32] fp32
+    uint32_t off_carry;      // tensor-core kernel, nphase > 1: accumulators between phases, [group][16][32] fp32
+    int nphase, nsp;         // tensor-core kernel: K staged through h_s in nphase phases of nsp segments
     int tma;                 // tensor-core kernel: whole 8-row groups arrive as one tensor copy per matrix
     int vec_in;              // 1: h (or s, norm_w) may be read with 16-byte loads
     int prefetch;            // 1: first weight stages requested before the dependency wait
@@ -849,7 +851,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
 // chain), added in the epilogue.
 //
 // Shared memory (dynamic):  [0, 1024)            mbarriers (ring, prologue, hand-off)
-//                           [off_h, off_s)       h_s[M + 1][K + 8] bf16 (row M = 0)
+//                           [off_h, off_s)       h_s[M + 1][K + 8] bf16 (row M = 0; no row M at M = 16)
 //                           [off_s, off_piece)   norm: norm_w[K] bf16
 //                           [off_piece, off_ring) parked[warp][16][32] fp32
 //                           [off_ring, ...)      ring[warp][stage][16][KS + 8] bf16
@@ -880,7 +882,10 @@ __device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], uint32_t a0, uin
 
 constexpr int kMmaRows = 8;                 // weight rows per group (the MMA's n)
 constexpr uint32_t kPieceBarOffset = 800;   // one mbarrier per ring-owning warp
+constexpr uint32_t kPhaseBarOffset = 872;   // K-phases: every ring warp has finished the phase
+constexpr uint32_t kHBarOffset = 880;       // K-phases: the next phase's h rows have landed
 constexpr uint32_t kPieceBytes = 2048;      // one warp's parked accumulators: [16][32] fp32
+constexpr int kMaxPhases = 2;
 
 struct MmaMaps {
     TensorMap gate, up;   // [N][K] bf16, row stride ld; box (KS + 8) x 8 rows
@@ -899,7 +904,11 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.stages, KS = p.KS, K = p.K, nseg = p.nseg;
     const int RS = KS + 8;                                   // padded ring row, elements
-    const int HS = K + 8;                                    // padded h row, elements
+    // K-phases: h_s holds NSP segments (HW columns) of h at a time; with one
+    // phase it holds all of K.
+    const int P = p.nphase, NSP = p.nsp;
+    const int HW = min(K, NSP * KS);
+    const int HS = HW + 8;                                   // padded h row, elements
     const int64_t stage_elems = static_cast<int64_t>(2) * kMmaRows * RS;
     const bool helper = warp == p.helper_warp;   // single-kernel norm path only; owns no ring
     const int W = p.helper_warp >= 0 ? p.helper_warp : static_cast<int>(blockDim.x >> 5);   // ring owners
@@ -920,20 +929,48 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     auto group_row0 = [&](int g) -> int {
         return p.interleave ? (g * static_cast<int>(gridDim.x) + static_cast<int>(blockIdx.x)) * R : r0 + g * R;
     };
-    // warp w owns units [unit_begin(w), unit_begin(w + 1)), streamed as
-    //   A = [a0, u_end)      head of a group that continues in the next warp
-    //   B = [c1, a0)         whole groups
-    //   C = [u_begin, c1)    tail of a group begun by the previous warp
-    const int units = ngroups * nseg;
-    auto unit_begin = [&](int w) -> int { return static_cast<int>((static_cast<int64_t>(units) * w) / W); };
-    const int u_begin = helper ? 0 : unit_begin(warp);
-    const int u_end = helper ? 0 : unit_begin(warp + 1);
-    const bool cont = u_begin < u_end && u_begin % nseg != 0;
-    const int c1 = cont ? min(u_end, (u_begin / nseg + 1) * nseg) : u_begin;
-    const int a0 = (u_end % nseg != 0 && c1 < u_end) ? ((u_end - 1) / nseg) * nseg : u_end;
-    const int len_a = u_end - a0, len_ab = len_a + (a0 - c1), n_units = u_end - u_begin;
-    auto unit_of = [&](int i) -> int {
-        return i < len_a ? a0 + i : (i < len_ab ? c1 + (i - len_a) : u_begin + (i - len_ab));
+    // In phase ph, warp w owns the phase's units (group, segment), in that
+    // order, [ub, ue) -- an equal share -- and streams them as
+    //   A = [a0, ue)      head of a group that continues in the next warp
+    //   B = [c1, a0)      whole groups
+    //   C = [ub, c1)      tail of a group begun by the previous warp
+    // The phases follow one another; a warp streams all of its phase-0 units,
+    // then its phase-1 units.
+    struct Range {
+        int ub, ue, c1, a0, len_a, len_ab, n, nsp;
+        bool cont;
+    };
+    auto range_of = [&](int ph, int w) -> Range {
+        Range r;
+        r.nsp = min(NSP, nseg - ph * NSP);
+        const int units = ngroups * r.nsp;
+        r.ub = static_cast<int>((static_cast<int64_t>(units) * w) / W);
+        r.ue = static_cast<int>((static_cast<int64_t>(units) * (w + 1)) / W);
+        if (w >= W) r.ub = r.ue = units;   // the helper warp streams nothing
+        r.cont = r.ub < r.ue && r.ub % r.nsp != 0;
+        r.c1 = r.cont ? min(r.ue, (r.ub / r.nsp + 1) * r.nsp) : r.ub;
+        r.a0 = (r.ue % r.nsp != 0 && r.c1 < r.ue) ? ((r.ue - 1) / r.nsp) * r.nsp : r.ue;
+        r.len_a = r.ue - r.a0;
+        r.len_ab = r.len_a + (r.a0 - r.c1);
+        r.n = r.ue - r.ub;
+        return r;
+    };
+    // the j-th unit of range r (phase ph) -> group g, segment seg of K
+    auto unit_at = [&](const Range &r, int ph, int j, int &g, int &seg) {
+        const int v = j < r.len_a ? r.a0 + j : (j < r.len_ab ? r.c1 + (j - r.len_a) : r.ub + (j - r.len_ab));
+        g = v / r.nsp;
+        seg = ph * NSP + (v - g * r.nsp);
+    };
+    // this warp's ranges, computed once (kMaxPhases == 2)
+    const Range rg0 = range_of(0, warp);
+    const Range rg1 = range_of(P > 1 ? 1 : 0, warp);
+    const int n_total = rg0.n + (P > 1 ? rg1.n : 0);
+    // the i-th unit this warp streams, counted over all phases
+    auto unit_seq = [&](int i, int &g, int &seg) {
+        if (P == 1 || i < rg0.n)
+            unit_at(rg0, 0, i, g, seg);
+        else
+            unit_at(rg1, 1, i - rg0.n, g, seg);
     };
 
     uint64_t *pro_bar = reinterpret_cast<uint64_t *>(smem + kProBarOffset);
@@ -942,6 +979,10 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     if (threadIdx.x == 0) {
         mbar_init(pro_bar, NORM ? 2 : 1);   // norm: the norm_w copy and the residual copy
         for (int w = 0; w < W; ++w) mbar_init(&piece_bar[w], 32);
+        if (P > 1) {
+            mbar_init(reinterpret_cast<uint64_t *>(smem + kPhaseBarOffset), W);
+            mbar_init(reinterpret_cast<uint64_t *>(smem + kHBarOffset), 1);
+        }
     }
     fence_mbar_init();
     __syncthreads();
@@ -951,10 +992,9 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     // up half sit at multiples of 128 bytes from the ring (32 * (KS + 8) and
     // 16 * (KS + 8) bytes with KS % 16 == 0), so checking the ring suffices.
     const bool use_tma = p.tma && (smem_addr(smem + p.off_ring) & 127u) == 0u;
-    // whole warp: request unit u into stage st.  Lane 0 posts the byte count
-    // first; lanes 0..nr-1 copy gate rows, 8..8+nr-1 up rows.
-    auto issue = [&](int st, int u) {
-        const int g = u / nseg, seg = u - g * nseg;
+    // whole warp: request unit (g, seg) into stage st.  Lane 0 posts the byte
+    // count first; lanes 0..nr-1 copy gate rows, 8..8+nr-1 up rows.
+    auto issue = [&](int st, int g, int seg) {
         const int row0 = group_row0(g);
         const int nr = min(R, r1 - row0);
         const int k0 = seg * KS;
@@ -982,7 +1022,11 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         }
     };
     auto prefill = [&]() {
-        for (int i = 0; i < S && i < n_units; ++i) issue(i, unit_of(i));
+        for (int i = 0; i < S && i < n_total; ++i) {
+            int g, seg;
+            unit_seq(i, g, seg);
+            issue(i, g, seg);
+        }
     };
 
     uint16_t *nw_s = reinterpret_cast<uint16_t *>(smem + p.off_s);   // norm: norm_w, K elements
@@ -1006,7 +1050,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     }
     __syncwarp();
 
-    // h rows 0..M-1, then a zero row M (padded stride HS)
+    // h rows 0..M-1, then a zero row M when M < 16 (padded stride HS)
     if constexpr (NORM) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u);
@@ -1026,12 +1070,12 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         norm_rows_in_place(p, rm, ss, h_s, HS, nw_s, red, inv_s, p.M);
     } else if (p.vec_in) {
         if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(K) * 2u);
-            copy_rows_async(h_s, HS, p.h, p.ldh, p.M, K, pro_bar);
+            mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(HW) * 2u);
+            copy_rows_async(h_s, HS, p.h, p.ldh, p.M, HW, pro_bar);   // phase 0's columns
         }
         prologue_wait(pro_bar);
     } else {
-        const int nch = K >> 3;
+        const int nch = HW >> 3;   // one phase here (the planner stages K only from aligned h)
         for (int i = threadIdx.x; i < p.M * nch; i += blockDim.x) {
             const int m = i / nch, c = i - m * nch;
             uint32_t w[4];
@@ -1042,8 +1086,9 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
             *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * HS + c * 8) = make_uint4(w[0], w[1], w[2], w[3]);
         }
     }
-    for (int c = threadIdx.x; c < (K >> 3); c += blockDim.x)
-        *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(p.M) * HS + c * 8) = make_uint4(0, 0, 0, 0);
+    if (p.M < kMaxM)   // at M = 16 every A row is a real row: no zero row is allocated or read
+        for (int c = threadIdx.x; c < (HW >> 3); c += blockDim.x)
+            *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(p.M) * HS + c * 8) = make_uint4(0, 0, 0, 0);
     __syncthreads();
 
     // ldmatrix.x4 row addresses for A: lane l -> h row (l & 15) (zero row if
@@ -1062,8 +1107,10 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
     float v0[4] = {0.f, 0.f, 0.f, 0.f}, v1[4] = {0.f, 0.f, 0.f, 0.f};
     float *const parked = reinterpret_cast<float *>(smem + p.off_piece);
-    auto park = [&]() {   // hand this warp's accumulators to the next warp
-        float *slot = parked + warp * (kPieceBytes / 4);
+    float *const carry = reinterpret_cast<float *>(smem + p.off_carry);
+    uint64_t *phase_bar = reinterpret_cast<uint64_t *>(smem + kPhaseBarOffset);
+    uint64_t *h_bar = reinterpret_cast<uint64_t *>(smem + kHBarOffset);
+    auto store_acc = [&](float *slot) {   // [16][32] fp32; the accumulators restart from zero
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             slot[q * 32 + lane] = g0[q];
@@ -1072,88 +1119,142 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
             slot[(12 + q) * 32 + lane] = v1[q];
             g0[q] = g1[q] = v0[q] = v1[q] = 0.f;
         }
-        mbar_arrive(&piece_bar[warp]);   // every lane: releases its own stores
     };
-    for (int i = 0; i < n_units; ++i) {
-        const int u = unit_of(i), st = i % S;
-        const int g = u / nseg, seg = u - g * nseg;
-        bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((i / S) & 1), kWaitLimitNs);
-        if (i == len_ab && cont) {
-            // resume the accumulators of the warp holding the group's earlier
-            // segments: the nearest lower warp that owns units
-            int prev = warp - 1;
-            while (prev > 0 && unit_begin(prev) == unit_begin(prev + 1)) --prev;
-            ok = mbar_wait_bounded(&piece_bar[prev], 0u, kWaitLimitNs) && ok;
-            const float *slot = parked + prev * (kPieceBytes / 4);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                g0[q] = slot[q * 32 + lane];
-                g1[q] = slot[(4 + q) * 32 + lane];
-                v0[q] = slot[(8 + q) * 32 + lane];
-                v1[q] = slot[(12 + q) * 32 + lane];
-            }
-        }
-        if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0) {
-                atomicExch(&g_device_error, kErrTimeout);
-                for (int j = i; j < min(i + S, n_units); ++j)   // drain this warp's copies in flight
-                    mbar_wait_bounded(&bars[j % S], static_cast<uint32_t>((j / S) & 1), kWaitLimitNs);
-            }
-            __syncwarp();
-            return;
-        }
-        const int k0 = seg * KS;
-        const int nk = min(KS, K - k0) >> 4;                 // whole k16 steps
-        const uint16_t *wg = ring + st * stage_elems + b_off;
-        const uint16_t *wu = wg + R * RS;
-        const uint16_t *ha = a_base + k0;
-        int kk = 0;
-#pragma unroll 2
-        for (; kk + 1 < nk; kk += 2) {
-            uint32_t a0r, a1r, a2r, a3r, b0, b1, c0, c1r;
-            ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16);
-            ldmatrix_x2(b0, b1, wg + kk * 16);
-            ldmatrix_x2(c0, c1r, wu + kk * 16);
-            mma_bf16_16x8x16(g0, a0r, a1r, a2r, a3r, b0, b1);
-            mma_bf16_16x8x16(v0, a0r, a1r, a2r, a3r, c0, c1r);
-            ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16 + 16);
-            ldmatrix_x2(b0, b1, wg + kk * 16 + 16);
-            ldmatrix_x2(c0, c1r, wu + kk * 16 + 16);
-            mma_bf16_16x8x16(g1, a0r, a1r, a2r, a3r, b0, b1);
-            mma_bf16_16x8x16(v1, a0r, a1r, a2r, a3r, c0, c1r);
-        }
-        if (kk < nk) {
-            uint32_t a0r, a1r, a2r, a3r, b0, b1, c0, c1r;
-            ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16);
-            ldmatrix_x2(b0, b1, wg + kk * 16);
-            ldmatrix_x2(c0, c1r, wu + kk * 16);
-            mma_bf16_16x8x16(g0, a0r, a1r, a2r, a3r, b0, b1);
-            mma_bf16_16x8x16(v0, a0r, a1r, a2r, a3r, c0, c1r);
-        }
-        __syncwarp();
-        if (i + S < n_units) {
-            if (lane == 0) fence_proxy_async_smem();
-            issue(st, unit_of(i + S));   // the unit S ahead, into the stage just read
-        }
-        __syncwarp();
-        if (i == len_a - 1) {   // end of A: the group continues in the next warp
-            park();
-            continue;
-        }
-        if (seg != nseg - 1) {
-            if (i == n_units - 1) park();   // C inside one group: it continues in the next warp too
-            continue;
-        }
-        // the group is complete.  D layout: d[0], d[1] -> batch row lane/4,
-        // features 2*(lane%4) + 0, 1; d[2], d[3] -> batch row lane/4 + 8.
-        const int row0 = group_row0(g);
-        const int m0 = lane >> 2, n = row0 + 2 * (lane & 3);
+    auto load_acc = [&](const float *slot) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int m = m0 + (q >> 1) * 8, nn = n + (q & 1);
-            if (m < p.M && nn < r1 && nn < row0 + R)
-                p.out[m * p.ldo + nn] = glu_epilogue(g0[q] + g1[q], v0[q] + v1[q], p.mode);
-            g0[q] = g1[q] = v0[q] = v1[q] = 0.f;
+            g0[q] = slot[q * 32 + lane];
+            g1[q] = slot[(4 + q) * 32 + lane];
+            v0[q] = slot[(8 + q) * 32 + lane];
+            v1[q] = slot[(12 + q) * 32 + lane];
+        }
+    };
+    // bounded waits for this warp's copies in flight, units i..i+S-1
+    auto drain = [&](int i) {
+        if (lane == 0)
+            for (int j = i; j < min(i + S, n_total); ++j)
+                mbar_wait_bounded(&bars[j % S], static_cast<uint32_t>((j / S) & 1), kWaitLimitNs);
+        __syncwarp();
+    };
+    int i = 0;   // units streamed so far, over all phases
+    for (int ph = 0; ph < P; ++ph) {
+        const Range &r = ph == 0 ? rg0 : rg1;
+        const int k_lo = ph * NSP * KS;
+        bool parked_now = false;
+        if (ph > 0) {   // h_s holds this phase's columns once every warp finished the last phase
+            const bool okh = mbar_wait_bounded(h_bar, static_cast<uint32_t>((ph - 1) & 1), kWaitLimitNs);
+            if (!__all_sync(0xffffffffu, okh)) {
+                if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
+                drain(i);
+                return;
+            }
+        }
+        for (int j = 0; j < r.n; ++j, ++i) {
+            int g, seg;
+            unit_at(r, ph, j, g, seg);
+            const int sp = seg - ph * NSP, st = i % S;
+            bool ok = mbar_wait_bounded(&bars[st], static_cast<uint32_t>((i / S) & 1), kWaitLimitNs);
+            if (j == r.len_ab && r.cont) {
+                // resume the accumulators of the warp holding the group's earlier
+                // segments of this phase: the nearest lower warp with units
+                int prev = warp - 1;
+                while (prev > 0 && range_of(ph, prev).n == 0) --prev;
+                ok = mbar_wait_bounded(&piece_bar[prev], static_cast<uint32_t>(ph & 1), kWaitLimitNs) && ok;
+                load_acc(parked + prev * (kPieceBytes / 4));
+            } else if (sp == 0 && ph > 0) {
+                load_acc(carry + static_cast<int64_t>(g) * (kPieceBytes / 4));   // the group's earlier phases
+            }
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
+                drain(i);
+                return;
+            }
+            const int k0 = seg * KS;
+            const int nk = min(KS, K - k0) >> 4;                 // whole k16 steps
+            const uint16_t *wg = ring + st * stage_elems + b_off;
+            const uint16_t *wu = wg + R * RS;
+            const uint16_t *ha = a_base + (k0 - k_lo);
+            int kk = 0;
+#pragma unroll 2
+            for (; kk + 1 < nk; kk += 2) {
+                uint32_t a0r, a1r, a2r, a3r, b0, b1, c0, c1r;
+                ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16);
+                ldmatrix_x2(b0, b1, wg + kk * 16);
+                ldmatrix_x2(c0, c1r, wu + kk * 16);
+                mma_bf16_16x8x16(g0, a0r, a1r, a2r, a3r, b0, b1);
+                mma_bf16_16x8x16(v0, a0r, a1r, a2r, a3r, c0, c1r);
+                ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16 + 16);
+                ldmatrix_x2(b0, b1, wg + kk * 16 + 16);
+                ldmatrix_x2(c0, c1r, wu + kk * 16 + 16);
+                mma_bf16_16x8x16(g1, a0r, a1r, a2r, a3r, b0, b1);
+                mma_bf16_16x8x16(v1, a0r, a1r, a2r, a3r, c0, c1r);
+            }
+            if (kk < nk) {
+                uint32_t a0r, a1r, a2r, a3r, b0, b1, c0, c1r;
+                ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16);
+                ldmatrix_x2(b0, b1, wg + kk * 16);
+                ldmatrix_x2(c0, c1r, wu + kk * 16);
+                mma_bf16_16x8x16(g0, a0r, a1r, a2r, a3r, b0, b1);
+                mma_bf16_16x8x16(v0, a0r, a1r, a2r, a3r, c0, c1r);
+            }
+            __syncwarp();
+            if (i + S < n_total) {
+                int gn, segn;
+                unit_seq(i + S, gn, segn);
+                if (lane == 0) fence_proxy_async_smem();
+                issue(st, gn, segn);   // the unit S ahead, into the stage just read
+            }
+            __syncwarp();
+            if (j == r.len_a - 1) {   // end of A: the group continues in the next warp
+                store_acc(parked + warp * (kPieceBytes / 4));
+                mbar_arrive(&piece_bar[warp]);   // every lane: releases its own stores
+                parked_now = true;
+                continue;
+            }
+            if (sp != r.nsp - 1) {
+                if (j == r.n - 1) {   // C inside one group: it continues in the next warp too
+                    store_acc(parked + warp * (kPieceBytes / 4));
+                    mbar_arrive(&piece_bar[warp]);
+                    parked_now = true;
+                }
+                continue;
+            }
+            if (ph < P - 1) {   // the group goes on in the next phase
+                store_acc(carry + static_cast<int64_t>(g) * (kPieceBytes / 4));
+                continue;
+            }
+            // the group is complete.  D layout: d[0], d[1] -> batch row lane/4,
+            // features 2*(lane%4) + 0, 1; d[2], d[3] -> batch row lane/4 + 8.
+            const int row0 = group_row0(g);
+            const int m0 = lane >> 2, n = row0 + 2 * (lane & 3);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int m = m0 + (q >> 1) * 8, nn = n + (q & 1);
+                if (m < p.M && nn < r1 && nn < row0 + R)
+                    p.out[m * p.ldo + nn] = glu_epilogue(g0[q] + g1[q], v0[q] + v1[q], p.mode);
+                g0[q] = g1[q] = v0[q] = v1[q] = 0.f;
+            }
+        }
+        if (P == 1) break;
+        // one arrival per warp and phase on its piece barrier keeps the phase
+        // parities of all piece barriers equal to the phase index
+        if (!parked_now) mbar_arrive(&piece_bar[warp]);
+        if (ph < P - 1) {
+            // every warp has finished reading this phase's h: thread 0 then
+            // copies the next phase's columns (the rings keep streaming)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(phase_bar);
+            if (warp == 0 && lane == 0) {
+                if (mbar_wait_bounded(phase_bar, static_cast<uint32_t>(ph & 1), kWaitLimitNs)) {
+                    const int k_next = (ph + 1) * NSP * KS, w_next = min(HW, K - k_next);
+                    fence_proxy_async_smem();   // the warps' reads of h_s (acquired above) before the copy's writes
+                    mbar_arrive_expect_tx(h_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(w_next) * 2u);
+                    copy_rows_async(h_s, HS, p.h + k_next, p.ldh, p.M, w_next, h_bar);
+                } else {
+                    atomicExch(&g_device_error, kErrTimeout);   // the other warps give up on h_bar
+                }
+            }
+            __syncwarp();
         }
     }
 }

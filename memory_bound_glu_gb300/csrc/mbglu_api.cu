@@ -36,8 +36,11 @@ static_assert(mbglu::kSlotGrpOffset + mbglu::kMaxStreamWarps * 8 * 4 <= mbglu::k
 static_assert(mbglu::kCounterOffset + 4 <= mbglu::kProBarOffset, "counter overlaps the prologue barrier");
 static_assert(mbglu::kProBarOffset % 8 == 0 && mbglu::kProBarOffset + 8 <= mbglu::kPieceBarOffset,
               "prologue barrier overlaps the piece barriers");
-static_assert(mbglu::kPieceBarOffset % 8 == 0 && mbglu::kPieceBarOffset + mbglu::kMaxStreamWarps * 8 <= kBarRegion,
-              "piece barriers outside the region");
+static_assert(mbglu::kPieceBarOffset % 8 == 0 && mbglu::kPieceBarOffset + mbglu::kMaxStreamWarps * 8 <= mbglu::kPhaseBarOffset,
+              "piece barriers overlap the phase barrier");
+static_assert(mbglu::kPhaseBarOffset % 8 == 0 && mbglu::kPhaseBarOffset + 8 <= mbglu::kHBarOffset &&
+                  mbglu::kHBarOffset % 8 == 0 && mbglu::kHBarOffset + 8 <= kBarRegion,
+              "phase barriers outside the region");
 constexpr int kMaxStages = 8;
 constexpr int kMmaKsCap = 240;               // tensor-core segment: its box (KS + 8) x 8 must be <= 256 wide
 constexpr int64_t kNormMaxMK = 81920;        // add_rmsnorm_glu: M*K*2 bytes of normed rows in smem
@@ -65,6 +68,7 @@ struct Tuning {
     int mma_min_m = 3;        // smallest batch that takes the tensor-core kernel (17: never)
     int mma_ks_min = 192;     // tensor-core plan: shortest K-segment worth one more warp
     int tma = 1;              // tensor-core kernel: whole groups by tensor copy (0: row by row)
+    int phases = 0;           // tensor-core kernel: K-phases (0: automatic, 1: never, 2: always where allowed)
 };
 
 std::atomic<int> g_policy{MBGLU_POLICY_PREFETCH};
@@ -92,6 +96,7 @@ const Tuning &tuning()
         x.mma_min_m = std::min(17, std::max(1, env_int("MBGLU_MMA_MIN_M", 3)));
         x.mma_ks_min = std::max(16, env_int("MBGLU_MMA_KS_MIN", 192));
         x.tma = env_int("MBGLU_TMA", 1) != 0;
+        x.phases = std::min(2, std::max(0, env_int("MBGLU_PHASES", 0)));
         return x;
     }();
     return t;
@@ -206,7 +211,8 @@ int default_rows(int MB, int K, bool contiguous)
 struct Plan {
     int MB = 1, R = 1, warps = 4, KS = 0, nseg = 0, stages = 0, grid = 0, ctas_per_sm = 1;
     bool hreg = false;
-    uint32_t off_h = 0, off_s = 0, off_piece = 0, off_ring = 0, smem = 0;
+    uint32_t off_h = 0, off_s = 0, off_carry = 0, off_piece = 0, off_ring = 0, smem = 0;
+    int nphase = 1, nsp = 0;   // tensor-core kernel: K staged in nphase phases of nsp segments
 };
 
 // Streaming-kernel plan.  Whole rows per stage (K-segments only if a stage of
@@ -276,7 +282,8 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
 }
 
 // Tensor-core plan (batch >= mma_min_m, K % 16 == 0): groups of 8 rows, each
-// row of a stage padded by 16 bytes; h_s holds M rows plus a zero row; 2 KB
+// row of a stage padded by 16 bytes; h_s holds M rows plus a zero row (none at
+// M = 16, where every A row is real); 2 KB
 // per warp for handed-off accumulators; two stages per warp.  For each warp
 // count the longest K-segment (multiple of 16, <= 240: the tensor copy's box
 // is KS + 8 <= 256 elements wide) that fits is taken;
@@ -284,25 +291,20 @@ bool plan_stream(const DeviceInfo &d, int M, int N, int K, bool contiguous, bool
 // (measured on GB300: at equal ring bytes more warps win, while row copies
 // under 512 bytes lose), else the warp count with the largest ring.
 // Segments are then evened out over K.  False if nothing fits.
-bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl, uint32_t extra = 0,
-              int max_warps = mbglu::kMaxStreamWarps)
+// Warp count and K-segment for `room` bytes of hand-off slots and rings: for
+// each warp count the longest segment that fits; the most warps whose
+// segment is >= mma_ks_min, else the largest ring.  False if nothing fits.
+bool choose_mma_ring(int K, int64_t room, int max_warps, int &w_out, int &ks_out, int64_t &ring_out)
 {
     const Tuning &t = tuning();
-    if (M < t.mma_min_m || K % 16 != 0) return false;
-    const int static_reserve = 2048;
-    int budget = d.smem_optin - static_reserve;
-    if (t.smem_kb > 0) budget = std::min(budget, t.smem_kb * 1024 - static_reserve);
-    const uint32_t hbytes = (static_cast<uint32_t>(M + 1) * static_cast<uint32_t>(K + 8) * 2u + 127u) & ~127u;
-    const int64_t room = static_cast<int64_t>(budget) - kBarRegion - hbytes - extra;
-    if (room <= 0) return false;
     const int want_s = t.stages > 0 ? t.stages : 2;
     const int64_t piece = mbglu::kPieceBytes;
     const int64_t row_unit = 2 * mbglu::kMmaRows * 2;   // stage bytes per padded element of a row
     const int ks_cap = std::min(kMmaKsCap, K);
-    int best_w = 0;
     int64_t best_ring = 0;
     int ks_of[mbglu::kMaxStreamWarps + 1] = {};
     int64_t ring_of[mbglu::kMaxStreamWarps + 1] = {};
+    if (room <= 0) return false;
     for (int w = 1; w <= max_warps; ++w) {
         if (t.warps > 0 && w != std::min(t.warps, max_warps)) continue;
         const int64_t per_stage = (room / w - piece) / want_s;
@@ -314,6 +316,7 @@ bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl, uint32_t extra
         if (ring_of[w] > best_ring) best_ring = ring_of[w];
     }
     if (best_ring == 0) return false;
+    int best_w = 0;
     for (int w = max_warps; w >= 1 && best_w == 0; --w)
         if (ring_of[w] > 0 && ks_of[w] >= std::min(t.mma_ks_min, ks_cap)) best_w = w;
     for (int w = max_warps; w >= 1 && best_w == 0; --w)
@@ -323,19 +326,77 @@ bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl, uint32_t extra
         const int nseg = (K + ks - 1) / ks;
         ks = ((K + nseg - 1) / nseg + 15) & ~15;
     }
-    pl.warps = best_w;
-    pl.stages = want_s;
-    pl.KS = ks;
+    w_out = best_w;
+    ks_out = ks;
+    ring_out = ring_of[best_w];
+    return true;
+}
+
+// Tensor-core plan (batch >= mma_min_m, K % 16 == 0): groups of 8 rows, each
+// row of a stage padded by 16 bytes; h_s holds M rows plus a zero row (none at
+// M = 16, where every A row is real); 2 KB per warp for handed-off
+// accumulators; two stages per warp (choose_mma_ring).  Measured on GB300: at
+// equal ring bytes more warps win, row copies under 512 bytes lose.
+// K-phases (allow_phases: plain GEMV with 16-byte aligned h): h_s holds about
+// half of K, plus 2 KB per group for the accumulators carried between the
+// phases; taken where that ring is >= 1.25x the one-phase ring (the phase
+// boundary costs a copy of h from L2), e.g. M = 16, K = 4096.  False if
+// nothing fits.
+bool plan_mma(const DeviceInfo &d, int M, int N, int K, Plan &pl, uint32_t extra = 0,
+              int max_warps = mbglu::kMaxStreamWarps, bool allow_phases = false)
+{
+    const Tuning &t = tuning();
+    if (M < t.mma_min_m || K % 16 != 0) return false;
+    const int static_reserve = 2048;
+    int budget = d.smem_optin - static_reserve;
+    if (t.smem_kb > 0) budget = std::min(budget, t.smem_kb * 1024 - static_reserve);
+    const uint32_t hrows = static_cast<uint32_t>(M < mbglu::kMaxM ? M + 1 : M);   // + the zero row below 16
+    auto h_bytes = [&](int width) -> uint32_t {
+        return (hrows * static_cast<uint32_t>(width + 8) * 2u + 127u) & ~127u;
+    };
+    const int grid = std::max(1, std::min(d.sm_count, N));
+
+    int w1 = 0, ks1 = 0;
+    int64_t ring1 = 0;
+    const bool ok1 = choose_mma_ring(K, static_cast<int64_t>(budget) - kBarRegion - h_bytes(K) - extra, max_warps,
+                                     w1, ks1, ring1);
+    int w2 = 0, ks2 = 0, nsp2 = 0;
+    int64_t ring2 = 0;
+    uint32_t carry2 = 0;
+    bool ok2 = false;
+    if (allow_phases && t.phases != 1 && extra == 0 && K >= 2 * 16) {
+        const int half = ((K + 1) / 2 + 15) & ~15;
+        const int64_t groups = t.interleave ? ((N + mbglu::kMmaRows - 1) / mbglu::kMmaRows + grid - 1) / grid
+                                            : ((N + grid - 1) / grid + mbglu::kMmaRows - 1) / mbglu::kMmaRows;
+        carry2 = static_cast<uint32_t>(groups) * mbglu::kPieceBytes;
+        // h_s is reserved for half of K plus up to one segment (phases end on segment boundaries)
+        ok2 = choose_mma_ring(K, static_cast<int64_t>(budget) - kBarRegion - h_bytes(half + kMmaKsCap) - carry2,
+                              max_warps, w2, ks2, ring2);
+        if (ok2) {
+            nsp2 = (half + ks2 - 1) / ks2;
+            const int nseg2 = (K + ks2 - 1) / ks2;
+            ok2 = nsp2 < nseg2 && (nseg2 + nsp2 - 1) / nsp2 <= mbglu::kMaxPhases;
+        }
+    }
+    const bool two = ok2 && (!ok1 || t.phases == 2 || ring2 * 4 >= ring1 * 5);
+    if (!ok1 && !two) return false;
+    pl.warps = two ? w2 : w1;
+    pl.stages = t.stages > 0 ? t.stages : 2;
+    pl.KS = two ? ks2 : ks1;
     pl.MB = 16;
     pl.R = mbglu::kMmaRows;
     pl.nseg = (K + pl.KS - 1) / pl.KS;
+    pl.nsp = two ? nsp2 : pl.nseg;
+    pl.nphase = (pl.nseg + pl.nsp - 1) / pl.nsp;
+    const int hw = std::min(K, pl.nsp * pl.KS);   // h_s columns
     pl.off_h = kBarRegion;
-    pl.off_s = kBarRegion + hbytes;
-    pl.off_piece = kBarRegion + hbytes + extra;
+    pl.off_s = kBarRegion + h_bytes(hw);
+    pl.off_carry = pl.off_s + extra;
+    pl.off_piece = pl.off_carry + (pl.nphase > 1 ? carry2 : 0u);
     pl.off_ring = pl.off_piece + static_cast<uint32_t>(pl.warps) * mbglu::kPieceBytes;
     pl.smem = pl.off_ring + static_cast<uint32_t>(pl.warps) * pl.stages * 2u * mbglu::kMmaRows *
                                 static_cast<uint32_t>(pl.KS + 8) * 2u;
-    pl.grid = std::max(1, std::min(d.sm_count, N));
+    pl.grid = grid;
     return true;
 }
 
@@ -441,6 +502,7 @@ GluParams base_params(int M, int N, int K, int mode)
 {
     GluParams p = {};
     p.helper_warp = -1;
+    p.nphase = 1;   // the tensor-core planner sets its phases
     p.M = M;
     p.N = N;
     p.K = K;
@@ -536,14 +598,18 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
     Plan pl;
     const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && (ld_gate % 8 == 0) &&
                          (ld_up % 8 == 0);
-    if (bulk_ok && plan_mma(*d, M, N, K, pl)) {
+    const bool h_vec = aligned(h, 16) && (ldh % 8 == 0);
+    if (bulk_ok && plan_mma(*d, M, N, K, pl, 0, mbglu::kMaxStreamWarps, h_vec)) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;
+        p.nphase = pl.nphase;
+        p.nsp = pl.nsp;
         p.stages = pl.stages;
         p.off_h = pl.off_h;
         p.off_ring = pl.off_ring;
         p.off_piece = pl.off_piece;
-        p.vec_in = aligned(h, 16) && (ldh % 8 == 0);
+        p.off_carry = pl.off_carry;
+        p.vec_in = h_vec;
         p.interleave = tuning().interleave;
         const mbglu::MmaMaps maps = weight_maps(p);
         st = launch_mma(mbglu::glu_mma_kernel<false>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p,
@@ -643,6 +709,9 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
             p.off_s = pl.off_s;
             p.off_ring = pl.off_ring;
             p.off_piece = pl.off_piece;
+            p.off_carry = pl.off_carry;
+            p.nphase = pl.nphase;
+            p.nsp = pl.nsp;
             p.helper_warp = pl.warps;   // one extra warp writes the residual slice
             const mbglu::MmaMaps maps = weight_maps(p);
             st = launch_mma(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3((pl.warps + 1) * 32), pl.smem, stream,
@@ -704,6 +773,9 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
         p.off_s = pl.off_s;
         p.off_ring = pl.off_ring;
         p.off_piece = pl.off_piece;
+        p.off_carry = pl.off_carry;
+        p.nphase = pl.nphase;
+        p.nsp = pl.nsp;
         const mbglu::MmaMaps maps = weight_maps(p);
         st = launch_mma(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3(pl.warps * 32), pl.smem, stream, pdl, p,
                         maps);

@@ -108,6 +108,38 @@ def test_large_m16_k_uses_generic_when_h_does_not_fit():
     check(h, g, u, "fused", "M=16 K=16384", variant=2)
 
 
+@pytest.mark.parametrize("M,N,K", [(16, 700, 4096), (13, 1337, 4096), (16, 153, 6144), (9, 700, 8192),
+                                   (16, 300, 8192)])
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_tensor_core_k_phases(M, N, K, mode):
+    """M*K too large to keep h whole beside a deep ring: the tensor-core kernel
+    stages h through shared memory in two K-phases and carries every group's
+    accumulators across the boundary (the last two shapes did not fit the
+    tensor-core kernel at all with h whole)."""
+    h = gi.normal_bf16((M, K), 1.0, M, "kp-h")
+    g = gi.normal_bf16((N, K), K ** -0.5, M, "kp-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, M, "kp-u")
+    check(h, g, u, mode, f"M={M} N={N} K={K}", variant=4)
+
+
+def test_k_phases_deterministic_and_row_permutation_bitwise():
+    """With K-phases, as with one phase, a row's bits do not depend on where
+    the row falls (how the CTA's units are cut between warps and phases)."""
+    M, N, K = 16, 1500, 4096
+    h = gi.normal_bf16((M, K), 1.0, 7, "kpp-h").to(DEV)
+    g = gi.normal_bf16((N, K), K ** -0.5, 7, "kpp-g").to(DEV)
+    u = gi.normal_bf16((N, K), K ** -0.5, 7, "kpp-u").to(DEV)
+    a = mb.glu_gemv(h, g, u, mode="hf")
+    assert mb.last_variant() == 4
+    b = mb.glu_gemv(h, g, u, mode="hf")
+    perm = torch.randperm(N, generator=torch.Generator().manual_seed(1)).to(DEV)
+    c = mb.glu_gemv(h, g[perm], u[perm], mode="hf")
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a[:, perm].view(torch.int16), c.view(torch.int16))
+    assert mb.read_device_error() == 0
+
+
 def test_strided_views_fast_and_generic():
     """Row strides are honoured: operands sliced out of wider buffers."""
     M, N, K = 4, 999, 1536
