@@ -58,6 +58,8 @@ def _bind(lib):
     lib.oracle_add_rmsnorm_glu.argtypes = [u16p, u16p, u16p, ctypes.c_float, u16p, u16p,
                                            u16p, i32, i32, i32, i32, u16p, i32]
     lib.oracle_add_rmsnorm_glu.restype = i32
+    lib.oracle_silu_mul.argtypes = [u16p, i64, u16p, i64, i32, i32, i32]
+    lib.oracle_silu_mul.restype = i32
     return lib
 
 
@@ -163,3 +165,19 @@ def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, mode="hf", nthreads=
     if rc != 0:
         raise RuntimeError(f"oracle_add_rmsnorm_glu failed: {rc}")
     return out, res, h
+
+
+def silu_mul(x, mode="fused", lib=None):
+    """out[M,N] = epilogue(x[:, :N], x[:, N:2N]) on the halves layout (x is
+    [M, 2N] bf16 bits, rows may be wider); see oracle_silu_mul."""
+    x = _u16(x)
+    if x.ndim != 2 or (x.size and x.strides[1] != 2):
+        x = np.ascontiguousarray(x).reshape(x.shape[0], -1)
+    M, W = x.shape
+    N = W // 2
+    out = np.zeros((M, N), dtype=np.uint16)
+    ldx = x.strides[0] // 2 if M > 1 else W   # a lone row's stride is arbitrary (numpy gives 0 to a new axis)
+    st = (lib or load()).oracle_silu_mul(_ptr(x), ldx, _ptr(out), N, M, N, MODES[mode])
+    if st != 0:
+        raise ValueError("oracle_silu_mul: bad arguments")
+    return out

@@ -326,3 +326,46 @@ int oracle_add_rmsnorm_glu(const uint16_t *x, uint16_t *residual,
     if (!h_out) free(h);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* silu_mul: the GLU epilogue on projections already computed              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The standalone epilogue of the prefill / large-batch route
+ * ([8602/fused_glu]: a native "fused silu-mul kernel (halves layout, no
+ * chunked views ...)", single rounding against the composite's double
+ * rounding).  Each row of x holds both projections side by side, as a GEMM on
+ * the concatenated [gate; up] weight leaves them: the gate half in columns
+ * [0, N) and the up half in columns [N, 2N).  For every m < M, n < N:
+ *   g = x[m, n], u = x[m, N + n]                 (bf16, exact in binary64)
+ *   mode FUSED: out = bf16( SiLU(g) * u )        one rounding
+ *   mode HF:    out = bf16( bf16(SiLU(g)) * u )  F.silu(g) * u on bf16 tensors
+ * g and u are bf16 already, so the HF rounding of the two projections is the
+ * identity here.  ldx >= 2N and ldo >= N are row strides in elements.
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_silu_mul(const uint16_t *x, int64_t ldx, uint16_t *out, int64_t ldo, int M, int N, int mode)
+{
+    if (M < 0 || N < 0) return -1;
+    if (mode != ORACLE_MODE_FUSED && mode != ORACLE_MODE_HF) return -1;
+    if (M == 0 || N == 0) return 0;
+    if (!x || !out || ldx < 2 * (int64_t)N || ldo < N) return -1;
+    for (int m = 0; m < M; ++m) {
+        const uint16_t *gate = x + (int64_t)m * ldx;
+        const uint16_t *up = gate + N;
+        for (int n = 0; n < N; ++n) {
+            const double g = oracle_bf16_to_double(gate[n]);
+            const double u = oracle_bf16_to_double(up[n]);
+            uint16_t o;
+            if (mode == ORACLE_MODE_FUSED) {
+                o = oracle_bf16_round(oracle_silu(g) * u);
+            } else {
+                const uint16_t sb = oracle_bf16_round(oracle_silu(g));
+                o = oracle_bf16_round(oracle_bf16_to_double(sb) * u);
+            }
+            out[(int64_t)m * ldo + n] = o;
+        }
+    }
+    return 0;
+}

@@ -38,6 +38,10 @@ MUTATIONS = {
     "norm_scale_not_centred": ("1.0 + oracle_bf16_to_double(norm_w[k])", "oracle_bf16_to_double(norm_w[k])"),
     "norm_eps_dropped": ("sqrt(var + e)", "sqrt(var)"),
     "residual_sign": ("oracle_bf16_to_double(xr[k]) +", "oracle_bf16_to_double(xr[k]) -"),
+    "silu_mul_halves_swapped": ("const double g = oracle_bf16_to_double(gate[n]);",
+                                "const double g = oracle_bf16_to_double(up[n]);"),
+    "silu_mul_hf_unrounded_silu": ("o = oracle_bf16_round(oracle_bf16_to_double(sb) * u);",
+                                   "o = oracle_bf16_round(oracle_silu(g) * u);"),
 }
 
 
@@ -89,6 +93,18 @@ def quick_pins(lib) -> list:
     s0, h0 = oracle.add_rmsnorm(x, x ^ np.uint16(0x8000), w, 1e-6, lib=lib)
     if not (np.all(s0 == 0) and np.all(h0 == 0)):
         fails.append("norm_cancelled")
+    # silu_mul, both modes, against exact rounding (gate half first)
+    g = gi.bits(gi.normal_bf16((64,), 2.0, 0, "mut-sg"))
+    u = gi.bits(gi.normal_bf16((64,), 2.0, 0, "mut-su"))
+    for mode in ("fused", "hf"):
+        got = oracle.silu_mul(np.concatenate([g, u])[None, :], mode, lib=lib)[0]
+        for i in range(64):
+            gv, uv = bf16_bits_to_fraction(int(g[i])), bf16_bits_to_fraction(int(u[i]))
+            sv = silu_exact(gv) if mode == "fused" else bf16_bits_to_fraction(rne_bf16(silu_exact(gv)))
+            want = rne_bf16(sv * uv)
+            if got[i] != want and not ((got[i] & 0x7FFF) == 0 and (want & 0x7FFF) == 0):
+                fails.append(f"silu_mul_{mode}")
+                break
     return fails
 
 

@@ -456,3 +456,77 @@ def test_fused_segment_is_norm_then_glu(oracle_lib):
     assert np.array_equal(res, s2) and np.array_equal(h, h2)
     want, _, _ = glu_exact(h2, gw, uw, "hf")
     assert np.array_equal(out, want)
+
+
+# ---------------------------------------------------------------------------
+# silu_mul (halves layout): the standalone epilogue
+# ---------------------------------------------------------------------------
+
+def _silu_mul_exact(g_bits, u_bits, mode):
+    """Exactly rounded silu_mul from arbitrary-precision SiLU (exact_ref)."""
+    out = np.zeros(len(g_bits), dtype=np.uint16)
+    for i, (gb, ub) in enumerate(zip(g_bits, u_bits)):
+        g, u = bf16_bits_to_fraction(int(gb)), bf16_bits_to_fraction(int(ub))
+        if mode == "fused":
+            out[i] = rne_bf16(silu_exact(g) * u)
+        else:
+            sb = bf16_bits_to_fraction(rne_bf16(silu_exact(g)))
+            out[i] = rne_bf16(sb * u)
+    return out
+
+
+def _same_up_to_zero_sign(a, b):
+    a, b = np.asarray(a), np.asarray(b)
+    zero = ((a & 0x7FFF) == 0) & ((b & 0x7FFF) == 0)
+    return bool(np.all((a == b) | zero))
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_silu_mul_matches_exact_rounding(mode):
+    """Every output is the correctly rounded value of the exact SiLU(g) * u
+    (FUSED) or of bf16(SiLU(g)) * u (HF), over N(0, 2) draws, SiLU's far
+    negative tail and small integers."""
+    pytest.importorskip("mpmath")
+    rng = np.random.default_rng(11)
+    g = np.concatenate([gi.bits(gi.normal_bf16((200,), 2.0, 0, "smx-g")),
+                        gi.bits(torch.tensor(-rng.uniform(20, 95, 40), dtype=torch.float32).to(torch.bfloat16)),
+                        gi.small_int_bf16((20,), seed=3, lo=-4, hi=4)])
+    u = np.concatenate([gi.bits(gi.normal_bf16((200,), 2.0, 0, "smx-u")),
+                        gi.bits(gi.normal_bf16((40,), 1.0, 0, "smx-u2")),
+                        gi.small_int_bf16((20,), seed=4, lo=-4, hi=4)])
+    x = np.concatenate([g, u])[None, :]
+    got = oracle.silu_mul(x, mode)[0]
+    assert _same_up_to_zero_sign(got, _silu_mul_exact(g, u, mode))
+
+
+@pytest.mark.parametrize("mode", ["fused", "hf"])
+def test_silu_mul_equals_glu_gemv_with_k_one(mode):
+    """With K = 1 and h = 1 the GEMV's dot products are exactly the weights,
+    so glu_gemv (pinned on its own above) must give silu_mul's bits."""
+    N = 300
+    g = gi.bits(gi.normal_bf16((N,), 3.0, 0, "smk-g"))
+    u = gi.bits(gi.normal_bf16((N,), 1.0, 0, "smk-u"))
+    h = np.array([[0x3F80]], dtype=np.uint16)   # 1.0
+    want = oracle.glu_gemv(h, g[:, None].copy(), u[:, None].copy(), mode)[0]
+    got = oracle.silu_mul(np.concatenate([g, u])[None, :], mode)[0]
+    assert np.array_equal(got, want)
+
+
+def test_silu_mul_halves_orientation_strides_and_closed_forms():
+    one, m20, zero = 0x3F80, gi.bits(torch.tensor([-20.0]).to(torch.bfloat16))[0], 0x0000
+    # gate half first: SiLU(-20) * 1 is tiny; SiLU(1) * -20 is not
+    a = oracle.silu_mul(np.array([[m20, one]], dtype=np.uint16), "fused")[0, 0]
+    b = oracle.silu_mul(np.array([[one, m20]], dtype=np.uint16), "fused")[0, 0]
+    assert abs(oracle.bf16_to_float(int(a))) < 1e-7
+    assert abs(oracle.bf16_to_float(int(b)) - (-20.0 / (1.0 + math.exp(-1.0)))) < 0.06
+    # u = 0 -> zero; g = 0 -> zero; g = 100 -> SiLU(g) = g (to binary64) so out = bf16(g * u)
+    x = np.array([[one, zero, 0x42C8, one, 0x4000, 0x4000]], dtype=np.uint16)   # g = 1, 0, 100; u = 1, 2, 2
+    out = oracle.silu_mul(x, "hf")[0]
+    assert oracle.bf16_to_float(int(out[1])) == 0.0
+    assert oracle.bf16_to_float(int(out[2])) == 200.0
+    # a row stride wider than 2N is honoured; the padding is never read
+    M, N = 3, 5
+    wide = np.full((M, 2 * N + 3), 0x7FC0, dtype=np.uint16)   # NaN padding
+    body = gi.bits(gi.normal_bf16((M, 2 * N), 1.0, 0, "sms"))
+    wide[:, :2 * N] = body
+    assert np.array_equal(oracle.silu_mul(wide[:, :2 * N], "fused"), oracle.silu_mul(body, "fused"))
