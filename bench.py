@@ -39,7 +39,7 @@ import glu_inputs as gi  # noqa: E402
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 # mbglu_last_variant() -> the kernel that streams the weights
-KERNEL_NAMES = {1: "glu_stream_kernel", 2: "glu_generic_kernel", 4: "glu_mma_kernel"}
+KERNEL_NAMES = {1: "glu_stream_kernel", 2: "glu_generic_kernel", 4: "glu_mma_kernel", 5: "silu_mul_kernel"}
 KERNEL_SOURCES = ["memory_bound_glu_gb300/csrc/glu_kernels.cuh", "memory_bound_glu_gb300/csrc/ptx.cuh",
                   "memory_bound_glu_gb300/csrc/mbglu_api.cu"]
 
@@ -197,9 +197,11 @@ def oracle_sample_rate(w, M, mode, seconds, max_rows=None):
     """Times oracle calls on row slices of layer 0 until `seconds` pass.
     Returns (GB/s of algorithmic bytes, description, threads)."""
     import oracle
+    threads = oracle.default_threads()
+    if w.op == "silu_mul":
+        return _oracle_silu_mul_rate(w, M, mode, seconds)
     g, u = gi.layer_weights(w, 0)
     gb, ub = gi.bits(g), gi.bits(u)
-    threads = oracle.default_threads()
     rows = w.N if max_rows is None else min(w.N, max_rows)
     gb, ub = np.ascontiguousarray(gb[:rows]), np.ascontiguousarray(ub[:rows])
     if w.op == "glu_gemv":
@@ -223,12 +225,33 @@ def oracle_sample_rate(w, M, mode, seconds, max_rows=None):
     return per_call * n / el / 1e9, desc, threads, el / n, per_call
 
 
+def _oracle_silu_mul_rate(w, M, mode, seconds, rows=64):
+    """silu_mul: the oracle (single-threaded C) on the first `rows` tokens of
+    input 0, repeated until `seconds` pass."""
+    import oracle
+    xb = gi.bits(gi.projections(w, min(M, rows), 0))
+    per_call = xb.shape[0] * 3 * w.N * 2
+    oracle.silu_mul(xb, mode)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.silu_mul(xb, mode)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    desc = (f"{n} oracle calls of silu_mul on tokens 0..{xb.shape[0] - 1} of input 0 (of M={M}), N={w.N}, "
+            f"{mode} mode, 1 thread, {el:.1f} s")
+    return per_call * n / el / 1e9, desc, 1, el / n, per_call
+
+
 def run_reference(args, w, M, mode, world, rank):
     """Reference arm: the fp64 oracle on the host cores, bounded steps."""
     if rank != 0:
         return
     steps, warm = max(1, args.steps), max(0, args.warmup)
     import oracle
+    if w.op == "silu_mul":
+        return _reference_silu_mul(args, w, M, mode, world, steps, warm)
     g, u = gi.layer_weights(w, 0)
     threads = oracle.default_threads()
     # size the per-step row sample so the whole run stays within ~2 minutes
@@ -270,11 +293,37 @@ def run_reference(args, w, M, mode, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def _reference_silu_mul(args, w, M, mode, world, steps, warm):
+    import oracle
+    rows = min(M, 64)
+    xb = gi.bits(gi.projections(w, rows, 0))
+    for _ in range(warm):
+        oracle.silu_mul(xb, mode)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.silu_mul(xb, mode)
+    el = time.perf_counter() - t0
+    value = rows * 3 * w.N * 2 * steps / el / 1e9
+    line = {
+        "impl": "reference", "metric": "GLU GEMV achieved HBM GB/s (cold L2), us/call at M=1",
+        "value": round(value, 4), "unit": "GB/s", "higher_is_better": True, "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": round(el / steps * 1e3, 4),
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, M, mode, w.layers),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"each step: one oracle call of silu_mul on tokens 0..{rows - 1} (of M={M}), "
+                                   f"N={w.N}, {mode} mode"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def config_dict(w, M, mode, layers, norm_kernels=None):
-    wb = w.weight_bytes() * layers
+    wb = w.input_bytes(M) * layers
     extra = {} if w.op == "glu_gemv" or norm_kernels is None else {"norm_kernels": norm_kernels}
     return {"workload": w.name, "op": w.op, "M": M, "K": w.K, "N": w.N, "mode": mode, "layers": layers, **extra,
-            "l2": f"inputs larger than L2: {layers} cycled weight pairs, {wb / 1e9:.2f} GB",
+            "l2": f"inputs larger than L2: {layers} cycled {'inputs' if w.op == 'silu_mul' else 'weight pairs'}, "
+                  f"{wb / 1e9:.2f} GB",
             "launch": f"one CUDA graph of {layers} calls per step",
             "launch_policy": _policy_name()}
 
@@ -315,12 +364,15 @@ def main():
 
     # inputs: resident in HBM before the timed region
     gates, ups = [], []
-    for layer in range(L):
+    for layer in range(L if w.op != "silu_mul" else 0):
         g, u = gi.layer_weights(w, layer)
         gates.append(g.to(dev))
         ups.append(u.to(dev))
         del g, u
-    if w.op == "glu_gemv":
+    if w.op == "silu_mul":
+        xs_cpu = [gi.projections(w, M, layer) for layer in range(L)]
+        xs = [t.to(dev) for t in xs_cpu]
+    elif w.op == "glu_gemv":
         h_cpu = gi.hidden(w, M)
         h = h_cpu.to(dev)
     else:
@@ -328,13 +380,15 @@ def main():
         x, nw = x_cpu.to(dev), nw_cpu.to(dev)
         residuals = [r_cpu.to(dev) for _ in range(L)]
     outs = torch.empty((L, M, w.N), dtype=torch.bfloat16, device=dev)
-    single = w.op != "glu_gemv" and args.norm_kernels == 1
+    single = w.op == "add_rmsnorm_glu" and args.norm_kernels == 1
     ws = mb.new_workspace(dev) if single else None
-    launches_per_call = 1 if (w.op == "glu_gemv" or single) else 2
+    launches_per_call = 2 if (w.op == "add_rmsnorm_glu" and not single) else 1
 
     def one_step():
         for i in range(L):
-            if w.op == "glu_gemv":
+            if w.op == "silu_mul":
+                mb.silu_mul(xs[i], out=outs[i], mode=mode)
+            elif w.op == "glu_gemv":
                 mb.glu_gemv(h, gates[i], ups[i], out=outs[i], mode=mode)
             else:
                 mb.add_rmsnorm_glu(x, residuals[i], nw, w.eps, gates[i], ups[i], out=outs[i], mode=mode,
@@ -388,8 +442,12 @@ def main():
 
     # e2e: the public Python API, pinned host input -> device, results -> host
     e2e = None
-    if args.e2e_steps > 0:
-        if w.op == "glu_gemv":
+    e2e_steps = min(args.e2e_steps, 10) if w.op == "silu_mul" else args.e2e_steps   # 318 MB to copy per step
+    if e2e_steps > 0:
+        if w.op == "silu_mul":
+            xs_host = [t.pin_memory() for t in xs_cpu]
+            in_bytes = sum(t.numel() for t in xs_host) * 2
+        elif w.op == "glu_gemv":
             h_host = h_cpu.pin_memory()
             in_bytes = h_host.numel() * 2
         else:
@@ -399,7 +457,10 @@ def main():
         out_host = torch.empty((L, M, w.N), dtype=torch.bfloat16).pin_memory()
 
         def e2e_step():
-            if w.op == "glu_gemv":
+            if w.op == "silu_mul":
+                for i in range(L):
+                    xs[i].copy_(xs_host[i], non_blocking=True)
+            elif w.op == "glu_gemv":
                 h.copy_(h_host, non_blocking=True)
             else:
                 x.copy_(x_host, non_blocking=True)
@@ -414,14 +475,14 @@ def main():
             torch.cuda.synchronize(dev)
             barrier(world)
             t0 = time.perf_counter()
-            for _ in range(args.e2e_steps):
+            for _ in range(e2e_steps):
                 e2e_step()
             torch.cuda.synchronize(dev)
             el = max_over_ranks(time.perf_counter() - t0, world, dev)
             barrier(world)
-        e2e = {"value": round(bytes_per_call * L * args.e2e_steps / el / 1e9 * world, 2), "unit": "GB/s",
+        e2e = {"value": round(bytes_per_call * L * e2e_steps / el / 1e9 * world, 2), "unit": "GB/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_host.numel() * 2,
-               "ms_per_step": round(el / args.e2e_steps * 1e3, 4),
+               "ms_per_step": round(el / e2e_steps * 1e3, 4),
                "how": "eager public-API calls (no graph), host copies inside the timed region"}
 
     cpu = None

@@ -99,7 +99,7 @@ def small_int_bf16(shape: Sequence[int], seed: int, lo: int = -8, hi: int = 8) -
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                      # "glu_gemv" or "add_rmsnorm_glu"
+    op: str                      # "glu_gemv", "add_rmsnorm_glu" or "silu_mul"
     Ms: tuple                    # batch rows exercised
     K: int
     N: int
@@ -113,12 +113,18 @@ class Workload:
     seed: int = 0
 
     def weight_bytes(self) -> int:
-        return 2 * self.N * self.K * 2
+        return 0 if self.op == "silu_mul" else 2 * self.N * self.K * 2
+
+    def input_bytes(self, M: int) -> int:
+        """Per call: both weights for the GEMV paths; x [M, 2N] for silu_mul."""
+        return M * 2 * self.N * 2 if self.op == "silu_mul" else self.weight_bytes()
 
     def algorithmic_bytes(self, M: int) -> int:
         """Bytes a call must move at least once: both weights, inputs, outputs."""
         b = self.weight_bytes() + M * self.N * 2
-        if self.op == "glu_gemv":
+        if self.op == "silu_mul":     # x [M, 2N] read, out [M, N] written
+            b += M * 2 * self.N * 2
+        elif self.op == "glu_gemv":
             b += M * self.K * 2
         else:  # x, residual read; residual written; norm_w read
             b += 3 * M * self.K * 2 + self.K * 2
@@ -142,6 +148,9 @@ WORKLOADS = {
                  outliers=True),
         Workload("gemv_k4096_n14336", "glu_gemv", (1, 8, 16), 4096, 14336, ("fused", "hf"), 24, 1 / 64.0,
                  outliers=True),
+        # the standalone epilogue on a prefill batch (halves layout [M, 2N]):
+        # 4096 tokens of the Qwen3.5-4B MLP; two inputs of 159 MB cycled for cold L2
+        Workload("silu_mul_m4096_n9728", "silu_mul", (4096,), 0, 9728, ("hf", "fused"), 2, 0.0),
     ]
 }
 
@@ -163,6 +172,13 @@ def layer_weights(w: Workload, layer: int, seed: Optional[int] = None):
 def hidden(w: Workload, M: int, seed: Optional[int] = None) -> torch.Tensor:
     """h [M, K] bf16 CPU tensor (glu_gemv input)."""
     return normal_bf16((M, w.K), w.h_std, w.seed if seed is None else seed, w.name, "h", M)
+
+
+def projections(w: Workload, M: int, layer: int = 0, seed: Optional[int] = None) -> torch.Tensor:
+    """x [M, 2N] bf16 CPU tensor for silu_mul: the gate and up projections of
+    M tokens side by side, N(0, h_std) (projections of a unit-variance hidden
+    state through N(0, 1/sqrt(K)) weights)."""
+    return normal_bf16((M, 2 * w.N), w.h_std, w.seed if seed is None else seed, w.name, "x", layer)
 
 
 def norm_inputs(w: Workload, M: int, seed: Optional[int] = None):

@@ -203,6 +203,31 @@ mbglu_status add_rmsnorm_glu_noalloc(const mbglu_bf16 *x, mbglu_bf16 *residual,
                                      mbglu_mode mode, cudaStream_t stream);
 
 /*
+ * silu_mul -- the GLU epilogue alone, on projections computed elsewhere: the
+ * prefill / large-batch route, where one GEMM on a concatenated [gate; up]
+ * weight leaves both projections side by side.  DeepSpeed PR #8602, commit
+ * "expr(segment-ki): native CUDA fused_glu kernel + GPU perf matrix": a fused
+ * silu-mul kernel on the "halves layout", with single rounding against the
+ * composite's double rounding.
+ *   x    [M][2N] bf16, row stride ldx >= 2N elements: the gate projection in
+ *        columns [0, N), the up projection in columns [N, 2N).
+ *   out  [M][N] bf16, row stride ldo >= N elements; must not overlap x.
+ *   mode MBGLU_MODE_FUSED: out = bf16(SiLU(g) * u), one rounding;
+ *        MBGLU_MODE_HF:    out = bf16(bf16(SiLU(g)) * u), F.silu(g) * u on
+ *        bf16 tensors (g and u are bf16 already).
+ * Device pointers owned by the caller; asynchronous on `stream`, no
+ * allocation, capturable.  Any M >= 0 (no batch limit).  M == 0 or N == 0 is
+ * a no-op.  Errors: MBGLU_ERR_MODE, MBGLU_ERR_SHAPE (M or N negative, or 2N
+ * beyond INT32_MAX),
+ * MBGLU_ERR_NULL, MBGLU_ERR_STRIDE (ldx < 2N or ldo < N), MBGLU_ERR_ALIGN (a
+ * pointer not 2-byte aligned), MBGLU_ERR_ALIAS (out overlaps x),
+ * MBGLU_ERR_CUDA.  16-byte aligned rows with N % 8 == 0 take the vectorised
+ * path; anything else runs element by element, with the same results.
+ */
+mbglu_status silu_mul(const mbglu_bf16 *x, int64_t ldx, mbglu_bf16 *out, int64_t ldo,
+                      int M, int N, mbglu_mode mode, cudaStream_t stream);
+
+/*
  * Launch policy, process-wide (default MBGLU_POLICY_PREFETCH).  It decides how
  * a call's kernels are ordered after the kernel that precedes them on the
  * stream; results are identical under every policy.
@@ -241,7 +266,7 @@ int mbglu_last_cuda_error(void);
 
 /* Which kernel the calling thread's last successful call launched:
  * 0 none (no-op), 1 streaming kernel (CUDA-core FMA), 2 generic kernel,
- * 3 zero fill, 4 tensor-core streaming kernel (batch >= 3). */
+ * 3 zero fill, 4 tensor-core streaming kernel (batch >= 3), 5 silu_mul. */
 int mbglu_last_variant(void);
 
 /*

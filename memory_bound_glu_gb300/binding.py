@@ -22,7 +22,8 @@ MAX_M = 16
 WORKSPACE_BYTES = 256
 
 # Every symbol include/mbglu.h declares.
-EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu_noalloc", "mbglu_set_launch_policy",
+EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu_noalloc", "silu_mul",
+           "mbglu_set_launch_policy",
            "mbglu_get_launch_policy",
            "mbglu_status_string", "mbglu_abi_version", "mbglu_last_cuda_error", "mbglu_last_variant",
            "mbglu_read_device_error")
@@ -50,6 +51,8 @@ def _bind(l):
     l.add_rmsnorm_glu_ws.restype = i32
     l.add_rmsnorm_glu_noalloc.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32, i32, vp]
     l.add_rmsnorm_glu_noalloc.restype = i32
+    l.silu_mul.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp]
+    l.silu_mul.restype = i32
     l.mbglu_status_string.argtypes = [i32]
     l.mbglu_status_string.restype = ctypes.c_char_p
     l.mbglu_abi_version.restype = i32
@@ -172,9 +175,38 @@ def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf",
     return out
 
 
+def silu_mul(x, out=None, mode="fused", stream=None):
+    """out[M,N] = SiLU(x[:, :N]) * x[:, N:2N] on the halves layout (the gate
+    projection in the first half of each row, the up projection in the second,
+    as a GEMM on the concatenated [gate; up] weight leaves them); mode "fused"
+    (one rounding) or "hf" (SiLU rounded to bf16 first).  x is [M, 2N] (or
+    [2N]) bf16 with a contiguous last dimension; any row stride."""
+    squeeze = x.dim() == 1
+    x2 = x.unsqueeze(0) if squeeze else x
+    _check(x2, "x", 2)
+    M, W = x2.shape
+    if W % 2:
+        raise ValueError(f"x must have an even number of columns (gate half, up half), got {W}")
+    N = W // 2
+    dev = x2.device
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    out2 = out.unsqueeze(0) if out.dim() == 1 else out
+    _check(out2, "out", 2)
+    if tuple(out2.shape) != (M, N) or out2.device != dev:
+        raise ValueError(f"out must be [{M},{N}] on {dev}")
+    with torch.cuda.device(dev):
+        st = lib().silu_mul(x2.data_ptr(), x2.stride(0), out2.data_ptr(), out2.stride(0), M, N, _MODES[mode],
+                            _stream_handle(dev, stream))
+    if st != 0:
+        raise MbgluError(st, "silu_mul")
+    return out2.view(N) if squeeze else out
+
+
 def last_variant() -> int:
     """Kernel the calling thread's last call launched: 0 none, 1 streaming
-    (CUDA-core), 2 generic, 3 zero fill, 4 tensor-core streaming (batch >= 3)."""
+    (CUDA-core), 2 generic, 3 zero fill, 4 tensor-core streaming (batch >= 3),
+    5 silu_mul."""
     return lib().mbglu_last_variant()
 
 

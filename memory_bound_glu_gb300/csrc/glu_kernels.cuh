@@ -1350,4 +1350,78 @@ __global__ void __launch_bounds__(256) zero_fill_kernel(uint16_t *out, int64_t l
     }
 }
 
+// ---------------------------------------------------------------------------
+// silu_mul: the GLU epilogue on projections computed elsewhere
+// ---------------------------------------------------------------------------
+// Halves layout (PR #8602, "fused_glu" commit): row m of x holds the gate
+// projection in columns [0, N) and the up projection in [N, 2N); out[m, n] =
+// epilogue(x[m, n], x[m, N + n]).  g and u are bf16 already, so the HF
+// roundings of g and u are identities.  Per element the work is one SiLU, so
+// unlike the GEMVs the epilogue's instruction count sets the pace: SiLU here
+// takes a correctly rounded reciprocal and a product instead of an IEEE
+// division (three roundings in all, a few fp32 ulps, far below a bf16 ulp).
+__device__ __forceinline__ float silu_rcp_f32(float x)
+{
+    const float t = expf(-fabsf(x));
+    return (x >= 0.0f ? x : x * t) * __frcp_rn(1.0f + t);
+}
+
+__device__ __forceinline__ uint16_t silu_mul_epilogue(float g, float u, int mode)
+{
+    if (mode == 0) return f32_to_bf16(silu_rcp_f32(g) * u);
+    return f32_to_bf16(round_to_bf16(silu_rcp_f32(g)) * u);   // sb * ub is exact in fp32
+}
+
+__device__ __forceinline__ uint4 silu_mul_chunk(uint4 gv, uint4 uv, int mode)
+{
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        o[j] = static_cast<uint32_t>(silu_mul_epilogue(bf16_lo(gw[j]), bf16_lo(uw[j]), mode)) |
+               (static_cast<uint32_t>(silu_mul_epilogue(bf16_hi(gw[j]), bf16_hi(uw[j]), mode)) << 16);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// HBM traffic: 4 bytes read and 2 written per output.  vec: one thread per 8
+// outputs, two chunks per iteration so that four 16-byte streaming loads are
+// in flight per thread; else one thread per output.  Waits for the preceding
+// grid, which produces x.
+__global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *x, int64_t ldx, uint16_t *out, int64_t ldo,
+                                                       int M, int N, int mode, int vec)
+{
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (vec) {
+        const int nch = N >> 3;
+        const int64_t total = static_cast<int64_t>(M) * nch;
+        int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+        for (; i + stride < total; i += 2 * stride) {
+            const int64_t m0 = i / nch, c0 = i - m0 * nch;
+            const int64_t i1 = i + stride, m1 = i1 / nch, c1 = i1 - m1 * nch;
+            const uint16_t *r0 = x + m0 * ldx + c0 * 8, *r1 = x + m1 * ldx + c1 * 8;
+            const uint4 g0 = __ldcs(reinterpret_cast<const uint4 *>(r0));
+            const uint4 u0 = __ldcs(reinterpret_cast<const uint4 *>(r0 + N));
+            const uint4 g1 = __ldcs(reinterpret_cast<const uint4 *>(r1));
+            const uint4 u1 = __ldcs(reinterpret_cast<const uint4 *>(r1 + N));
+            __stcs(reinterpret_cast<uint4 *>(out + m0 * ldo + c0 * 8), silu_mul_chunk(g0, u0, mode));
+            __stcs(reinterpret_cast<uint4 *>(out + m1 * ldo + c1 * 8), silu_mul_chunk(g1, u1, mode));
+        }
+        if (i < total) {
+            const int64_t m0 = i / nch, c0 = i - m0 * nch;
+            const uint16_t *r0 = x + m0 * ldx + c0 * 8;
+            const uint4 g0 = __ldcs(reinterpret_cast<const uint4 *>(r0));
+            const uint4 u0 = __ldcs(reinterpret_cast<const uint4 *>(r0 + N));
+            __stcs(reinterpret_cast<uint4 *>(out + m0 * ldo + c0 * 8), silu_mul_chunk(g0, u0, mode));
+        }
+    } else {
+        const int64_t total = static_cast<int64_t>(M) * N;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+            const int64_t m = i / N, n = i - m * N;
+            out[m * ldo + n] = silu_mul_epilogue(bf16_to_f32(x[m * ldx + n]), bf16_to_f32(x[m * ldx + N + n]), mode);
+        }
+    }
+}
+
 }  // namespace mbglu

@@ -26,7 +26,7 @@ using mbglu::GluParams;
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_variant = 0;
 
-enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4 };
+enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4, kSiluMul = 5 };
 
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kBarRegion = 1024;        // mbarriers, stage -> group table, group counter
@@ -527,6 +527,42 @@ mbglu_status mbglu_set_launch_policy(int policy)
 int mbglu_get_launch_policy(void) { return g_policy.load(std::memory_order_relaxed); }
 int mbglu_last_cuda_error(void) { return t_last_cuda_error; }
 int mbglu_last_variant(void) { return t_last_variant; }
+
+mbglu_status silu_mul(const mbglu_bf16 *x, int64_t ldx, mbglu_bf16 *out, int64_t ldo, int M, int N,
+                      mbglu_mode mode, cudaStream_t stream)
+{
+    t_last_variant = kNone;
+    if (mode != MBGLU_MODE_FUSED && mode != MBGLU_MODE_HF) return MBGLU_ERR_MODE;
+    if (M < 0 || N < 0 || N > INT32_MAX / 2) return MBGLU_ERR_SHAPE;   // 2N columns must fit an int
+    if (M == 0 || N == 0) return MBGLU_OK;
+    if (!x || !out) return MBGLU_ERR_NULL;
+    if (ldx < 2 * static_cast<int64_t>(N) || ldo < N) return MBGLU_ERR_STRIDE;
+    if (!aligned(x, 2) || !aligned(out, 2)) return MBGLU_ERR_ALIGN;
+    if (overlaps(out, matrix_bytes(M, N, ldo), x, matrix_bytes(M, 2 * N, ldx)))
+        return MBGLU_ERR_ALIAS;
+    const DeviceInfo *d = nullptr;
+    mbglu_status st = device_info(&d);
+    if (st != MBGLU_OK) return st;
+    const int policy = g_policy.load(std::memory_order_relaxed);
+    const int vec = aligned(x, 16) && aligned(out, 16) && N % 8 == 0 && ldx % 8 == 0 && ldo % 8 == 0;
+    const int64_t work = vec ? static_cast<int64_t>(M) * (N / 8) : static_cast<int64_t>(M) * N;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(d->sm_count) * 8,
+                                                                            (work + 255) / 256)));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = policy != MBGLU_POLICY_SERIAL ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, mbglu::silu_mul_kernel, reinterpret_cast<const uint16_t *>(x), ldx,
+                                             reinterpret_cast<uint16_t *>(out), ldo, M, N, static_cast<int>(mode), vec);
+    if (e != cudaSuccess) return cuda_fail(e);
+    t_last_variant = kSiluMul;
+    return MBGLU_OK;
+}
 
 const char *mbglu_status_string(mbglu_status s)
 {

@@ -87,6 +87,25 @@ def test_add_rmsnorm_glu_validation(kw, code):
     assert norm(**kw) == code
 
 
+def silu(x=X, ldx=64, o=O, ldo=32, M=2, N=32, mode=0):
+    return mb.lib().silu_mul(x, ldx, o, ldo, M, N, mode, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(mode=2), MODE), (dict(M=-1), SHAPE), (dict(N=-1), SHAPE), (dict(N=2 ** 30), SHAPE),
+    (dict(x=0), NULL), (dict(o=0), NULL),
+    (dict(ldx=63), STRIDE), (dict(ldo=31), STRIDE),
+    (dict(x=X + 1), ALIGN), (dict(o=O + 3), ALIGN),
+    (dict(o=X), ALIAS), (dict(o=X + 64 * 2), ALIAS), (dict(o=X - 2 * 31), ALIAS),
+    (dict(M=0), OK), (dict(N=0), OK), (dict(M=0, x=0, o=0), OK),
+])
+def test_silu_mul_validation(kw, code):
+    """Host-side validation of silu_mul (no GPU: only rejections and the
+    no-op sizes, which launch nothing)."""
+    assert silu(**kw) == code
+    assert mb.lib().mbglu_last_variant() == 0
+
+
 def test_binding_rejects_cpu_tensors():
     import torch
     h = torch.zeros(2, 64, dtype=torch.bfloat16)
