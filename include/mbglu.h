@@ -171,6 +171,28 @@ mbglu_status add_rmsnorm_glu_ws(const mbglu_bf16 *x, mbglu_bf16 *residual,
                                 cudaStream_t stream);
 
 /*
+ * add_rmsnorm_glu_strided -- add_rmsnorm_glu (or, with a workspace,
+ * add_rmsnorm_glu_ws) on weights and an output with explicit row strides:
+ * gate_w and up_w [N][K] with row strides ld_gate, ld_up >= K, out [M][N]
+ * with row stride ldo >= N (elements), e.g. views into a packed parameter
+ * buffer or a wider activation buffer.  PR #9057, commit on decode attention
+ * and the "real row stride": kernels take the true stride instead of assuming
+ * a contiguous tensor, and reject a stride that cannot hold the row.  x,
+ * residual and norm_w stay contiguous.  workspace: NULL runs the two-kernel
+ * path; otherwise as add_rmsnorm_glu_ws (MBGLU_WORKSPACE_BYTES, 16-byte
+ * aligned, zero before first use).  Errors as add_rmsnorm_glu_ws, plus
+ * MBGLU_ERR_STRIDE for ld_gate < K, ld_up < K or ldo < N.  Strides that are
+ * not multiples of 8 elements run the generic kernel.
+ */
+mbglu_status add_rmsnorm_glu_strided(const mbglu_bf16 *x, mbglu_bf16 *residual,
+                                     const mbglu_bf16 *norm_w, float eps,
+                                     const mbglu_bf16 *gate_w, int64_t ld_gate,
+                                     const mbglu_bf16 *up_w, int64_t ld_up,
+                                     mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
+                                     mbglu_mode mode, void *workspace, size_t workspace_bytes,
+                                     cudaStream_t stream);
+
+/*
  * add_rmsnorm_glu_noalloc -- add_rmsnorm_glu_ws for callers that cannot
  * allocate device memory: code running where the memory is owned by someone
  * else (a serving runtime's planner, a plugin host, a framework that hands

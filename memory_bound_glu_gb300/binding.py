@@ -22,7 +22,8 @@ MAX_M = 16
 WORKSPACE_BYTES = 256
 
 # Every symbol include/mbglu.h declares.
-EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu_noalloc", "silu_mul",
+EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu_strided", "add_rmsnorm_glu_noalloc",
+           "silu_mul",
            "mbglu_set_launch_policy",
            "mbglu_get_launch_policy",
            "mbglu_status_string", "mbglu_abi_version", "mbglu_last_cuda_error", "mbglu_last_variant",
@@ -51,6 +52,9 @@ def _bind(l):
     l.add_rmsnorm_glu_ws.restype = i32
     l.add_rmsnorm_glu_noalloc.argtypes = [vp, vp, vp, ctypes.c_float, vp, vp, vp, i32, i32, i32, i32, vp]
     l.add_rmsnorm_glu_noalloc.restype = i32
+    l.add_rmsnorm_glu_strided.argtypes = [vp, vp, vp, ctypes.c_float, vp, i64, vp, i64, vp, i64, i32, i32, i32, i32,
+                                          vp, ctypes.c_size_t, vp]
+    l.add_rmsnorm_glu_strided.restype = i32
     l.silu_mul.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp]
     l.silu_mul.restype = i32
     l.mbglu_status_string.argtypes = [i32]
@@ -137,7 +141,9 @@ def new_workspace(device=None):
 def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf", stream=None, workspace=None):
     """residual <- bf16(x + residual); h = zero-centred RMSNorm(residual);
     out = GLU(h).  Returns out; residual is updated in place.  With a
-    workspace (new_workspace()) the whole segment runs as one kernel."""
+    workspace (new_workspace()) the whole segment runs as one kernel.  x,
+    residual and norm_w are contiguous; the weights and out may be row-strided
+    views (contiguous last dimension)."""
     _check(x, "x", 2)
     _check(residual, "residual", 2)
     _check(norm_w, "norm_w", 1)
@@ -145,7 +151,7 @@ def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf",
     _check(up_w, "up_w", 2)
     M, K = x.shape
     N = gate_w.shape[0]
-    for t, name in ((x, "x"), (residual, "residual"), (norm_w, "norm_w"), (gate_w, "gate_w"), (up_w, "up_w")):
+    for t, name in ((x, "x"), (residual, "residual"), (norm_w, "norm_w")):
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     if tuple(residual.shape) != (M, K) or tuple(norm_w.shape) != (K,):
@@ -156,16 +162,23 @@ def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf",
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
     _check(out, "out", 2)
-    if tuple(out.shape) != (M, N) or not out.is_contiguous():
-        raise ValueError(f"out must be a contiguous [{M},{N}] tensor")
+    if tuple(out.shape) != (M, N):
+        raise ValueError(f"out must be a [{M},{N}] tensor")
+    if workspace is not None and not (workspace.is_cuda and workspace.device == dev and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor on the operands' device")
     with torch.cuda.device(dev):
-        if workspace is None:
+        if not (gate_w.is_contiguous() and up_w.is_contiguous() and out.is_contiguous()):
+            wsp = workspace.data_ptr() if workspace is not None else None
+            wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+            st = lib().add_rmsnorm_glu_strided(x.data_ptr(), residual.data_ptr(), norm_w.data_ptr(), float(eps),
+                                               gate_w.data_ptr(), gate_w.stride(0), up_w.data_ptr(), up_w.stride(0),
+                                               out.data_ptr(), out.stride(0), M, N, K, _MODES[mode], wsp, wsb,
+                                               _stream_handle(dev, stream))
+        elif workspace is None:
             st = lib().add_rmsnorm_glu(x.data_ptr(), residual.data_ptr(), norm_w.data_ptr(), float(eps),
                                        gate_w.data_ptr(), up_w.data_ptr(), out.data_ptr(), M, N, K, _MODES[mode],
                                        _stream_handle(dev, stream))
         else:
-            if not (workspace.is_cuda and workspace.device == dev and workspace.is_contiguous()):
-                raise ValueError("workspace must be a contiguous CUDA tensor on the operands' device")
             st = lib().add_rmsnorm_glu_ws(x.data_ptr(), residual.data_ptr(), norm_w.data_ptr(), float(eps),
                                           gate_w.data_ptr(), up_w.data_ptr(), out.data_ptr(), M, N, K, _MODES[mode],
                                           workspace.data_ptr(), workspace.numel() * workspace.element_size(),

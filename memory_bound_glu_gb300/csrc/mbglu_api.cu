@@ -680,8 +680,9 @@ namespace {
 // formed in shared memory, residual written back by the last CTA), where the
 // fast kernels apply; otherwise the two-kernel path.
 mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
-                                  const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w, mbglu_bf16 *out, int M, int N,
-                                  int K, mbglu_mode mode, int *ws, cudaStream_t stream)
+                                  const mbglu_bf16 *gate_w, int64_t ld_gate, const mbglu_bf16 *up_w, int64_t ld_up,
+                                  mbglu_bf16 *out, int64_t ldo, int M, int N, int K, mbglu_mode mode, int *ws,
+                                  cudaStream_t stream)
 {
     t_last_variant = kNone;
     if (mode != MBGLU_MODE_FUSED && mode != MBGLU_MODE_HF) return MBGLU_ERR_MODE;
@@ -689,21 +690,22 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
     if (static_cast<int64_t>(M) * K > kNormMaxMK) return MBGLU_ERR_SHAPE;
     if (M == 0) return MBGLU_OK;
     if (!x || !residual || !norm_w || (N > 0 && (!gate_w || !up_w || !out))) return MBGLU_ERR_NULL;
+    if (N > 0 && (ld_gate < K || ld_up < K || ldo < N)) return MBGLU_ERR_STRIDE;
     if (!aligned(x, 2) || !aligned(residual, 2) || !aligned(norm_w, 2) ||
         (N > 0 && (!aligned(gate_w, 2) || !aligned(up_w, 2) || !aligned(out, 2))))
         return MBGLU_ERR_ALIGN;
-    const int64_t xb = static_cast<int64_t>(M) * K * 2, wb = static_cast<int64_t>(N) * K * 2;
-    const int64_t ob = static_cast<int64_t>(M) * N * 2, nb = static_cast<int64_t>(K) * 2;
+    const int64_t xb = static_cast<int64_t>(M) * K * 2, nb = static_cast<int64_t>(K) * 2;
+    const int64_t gb = matrix_bytes(N, K, ld_gate), ub = matrix_bytes(N, K, ld_up), ob = matrix_bytes(M, N, ldo);
     if (x != residual && overlaps(x, xb, residual, xb)) return MBGLU_ERR_ALIAS;
-    if (overlaps(residual, xb, norm_w, nb) || overlaps(residual, xb, gate_w, wb) || overlaps(residual, xb, up_w, wb))
+    if (overlaps(residual, xb, norm_w, nb) || overlaps(residual, xb, gate_w, gb) || overlaps(residual, xb, up_w, ub))
         return MBGLU_ERR_ALIAS;
     if (N > 0 && (overlaps(out, ob, x, xb) || overlaps(out, ob, residual, xb) || overlaps(out, ob, norm_w, nb) ||
-                  overlaps(out, ob, gate_w, wb) || overlaps(out, ob, up_w, wb)))
+                  overlaps(out, ob, gate_w, gb) || overlaps(out, ob, up_w, ub)))
         return MBGLU_ERR_ALIAS;
     if (ws) {
         const int64_t wsb = MBGLU_WORKSPACE_BYTES;
         if (overlaps(ws, wsb, x, xb) || overlaps(ws, wsb, residual, xb) || overlaps(ws, wsb, norm_w, nb) ||
-            (N > 0 && (overlaps(ws, wsb, gate_w, wb) || overlaps(ws, wsb, up_w, wb) || overlaps(ws, wsb, out, ob))))
+            (N > 0 && (overlaps(ws, wsb, gate_w, gb) || overlaps(ws, wsb, up_w, ub) || overlaps(ws, wsb, out, ob))))
             return MBGLU_ERR_ALIAS;
     }
 
@@ -715,18 +717,19 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
 
     GluParams p = base_params(M, N, K, static_cast<int>(mode));
     p.gate = gate_w;
-    p.ld_gate = K;
+    p.ld_gate = ld_gate;
     p.up = up_w;
-    p.ld_up = K;
+    p.ld_up = ld_up;
     p.out = out;
-    p.ldo = N;
+    p.ldo = ldo;
     p.s = residual;
     p.norm_w = norm_w;
     p.eps = eps;
     p.vec_in = (K % 8 == 0) && aligned(residual, 16) && aligned(norm_w, 16);
     p.prefetch = policy == MBGLU_POLICY_PREFETCH;
     p.interleave = tuning().interleave;
-    const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && p.vec_in;
+    const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && (ld_gate % 8 == 0) &&
+                         (ld_up % 8 == 0) && p.vec_in;
 
     // single kernel: needs the fast kernels, 16-byte aligned x, and N > 0
     const uint32_t nwbytes = (static_cast<uint32_t>(K) * 2u + 127u) & ~127u;   // norm_w in shared memory
@@ -845,7 +848,21 @@ mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual, const mb
                              const mbglu_bf16 *gate_w, const mbglu_bf16 *up_w, mbglu_bf16 *out, int M, int N, int K,
                              mbglu_mode mode, cudaStream_t stream)
 {
-    return add_rmsnorm_glu_impl(x, residual, norm_w, eps, gate_w, up_w, out, M, N, K, mode, nullptr, stream);
+    return add_rmsnorm_glu_impl(x, residual, norm_w, eps, gate_w, K, up_w, K, out, N, M, N, K, mode, nullptr, stream);
+}
+
+mbglu_status add_rmsnorm_glu_strided(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
+                                     const mbglu_bf16 *gate_w, int64_t ld_gate, const mbglu_bf16 *up_w, int64_t ld_up,
+                                     mbglu_bf16 *out, int64_t ldo, int M, int N, int K, mbglu_mode mode,
+                                     void *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    t_last_variant = kNone;
+    if (workspace) {
+        if (workspace_bytes < MBGLU_WORKSPACE_BYTES) return MBGLU_ERR_SHAPE;
+        if (!aligned(workspace, 16)) return MBGLU_ERR_ALIGN;
+    }
+    return add_rmsnorm_glu_impl(x, residual, norm_w, eps, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode,
+                                static_cast<int *>(workspace), stream);
 }
 
 mbglu_status add_rmsnorm_glu_ws(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
@@ -857,7 +874,7 @@ mbglu_status add_rmsnorm_glu_ws(const mbglu_bf16 *x, mbglu_bf16 *residual, const
     if (!workspace) return MBGLU_ERR_NULL;
     if (workspace_bytes < MBGLU_WORKSPACE_BYTES) return MBGLU_ERR_SHAPE;
     if (!aligned(workspace, 16)) return MBGLU_ERR_ALIGN;
-    return add_rmsnorm_glu_impl(x, residual, norm_w, eps, gate_w, up_w, out, M, N, K, mode,
+    return add_rmsnorm_glu_impl(x, residual, norm_w, eps, gate_w, K, up_w, K, out, N, M, N, K, mode,
                                 static_cast<int *>(workspace), stream);
 }
 

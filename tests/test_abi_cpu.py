@@ -87,6 +87,25 @@ def test_add_rmsnorm_glu_validation(kw, code):
     assert norm(**kw) == code
 
 
+def norm_strided(x=X, r=R, w=W, g=G, ldg=96, u=U, ldu=72, o=O, ldo=40, M=2, N=32, K=64, mode=1, ws=None,
+                 wsb=256):
+    return mb.lib().add_rmsnorm_glu_strided(x, r, w, 1e-6, g, ldg, u, ldu, o, ldo, M, N, K, mode, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ldg=63), STRIDE), (dict(ldu=10), STRIDE), (dict(ldo=31), STRIDE),
+    (dict(mode=3), MODE), (dict(K=0), SHAPE), (dict(M=17), SHAPE),
+    (dict(g=G + 1), ALIGN), (dict(ws=X + 0x1000000 + 8), ALIGN), (dict(ws=X + 0x1000000, wsb=255), SHAPE),
+    (dict(o=G + 2 * 96 * 31), ALIAS), (dict(r=U + 2 * 72 * 5), ALIAS), (dict(ws=O + 2 * 40), ALIAS),
+    (dict(M=0), OK),
+])
+def test_add_rmsnorm_glu_strided_validation(kw, code):
+    """Strides are checked against K and N, and the alias checks cover each
+    strided operand's true extent (rows times its stride)."""
+    assert norm_strided(**kw) == code
+    assert mb.lib().mbglu_last_variant() == 0
+
+
 def silu(x=X, ldx=64, o=O, ldo=32, M=2, N=32, mode=0):
     return mb.lib().silu_mul(x, ldx, o, ldo, M, N, mode, None)
 

@@ -425,6 +425,51 @@ def test_add_rmsnorm_glu_single_kernel(M, mode):
     check_norm(x, r, w, g, u, mode, what=f"ws M={M} {mode}", variant=1, ws=ws)
 
 
+@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("single", [False, True])
+def test_add_rmsnorm_glu_strided_weights_and_out(M, single):
+    """Weights and out as row-strided views (add_rmsnorm_glu_strided): the same
+    bytes reach the same arithmetic, so the bits equal the contiguous call's;
+    a stride that is not a multiple of 8 elements runs the generic kernel and
+    is checked against the oracle."""
+    N, K = 1500, 2048
+    x = gi.normal_bf16((M, K), 1.0, M, "st-x").to(DEV)
+    r = gi.normal_bf16((M, K), 1.0, M, "st-r")
+    w = gi.normal_bf16((K,), 0.1, M, "st-w").to(DEV)
+    g = gi.normal_bf16((N, K), K ** -0.5, M, "st-g").to(DEV)
+    u = gi.normal_bf16((N, K), K ** -0.5, M, "st-u").to(DEV)
+    ws = (lambda: mb.new_workspace(DEV)) if single else (lambda: None)
+    r_ref = r.to(DEV)
+    ref = mb.add_rmsnorm_glu(x, r_ref, w, 1e-6, g, u, mode="hf", workspace=ws())
+    variant = mb.last_variant()
+    gw = torch.zeros((N, K + 64), dtype=torch.bfloat16, device=DEV)
+    uw = torch.zeros((N, K + 8), dtype=torch.bfloat16, device=DEV)
+    gw[:, :K], uw[:, :K] = g, u
+    out_w = torch.full((M, N + 16), float("nan"), dtype=torch.bfloat16, device=DEV)
+    r_st = r.to(DEV)
+    mb.add_rmsnorm_glu(x, r_st, w, 1e-6, gw[:, :K], uw[:, :K], out=out_w[:, :N], mode="hf", workspace=ws())
+    torch.cuda.synchronize()
+    assert mb.last_variant() == variant
+    assert torch.equal(r_st.view(torch.int16), r_ref.view(torch.int16))
+    assert torch.equal(out_w[:, :N].view(torch.int16), ref.view(torch.int16))
+    assert torch.isnan(out_w[:, N:].float()).all()
+    # an odd stride: the generic kernel, against the oracle
+    go = torch.zeros((N, K + 3), dtype=torch.bfloat16, device=DEV)
+    go[:, :K] = g
+    r_odd = r.to(DEV)
+    out_odd = mb.add_rmsnorm_glu(x, r_odd, w, 1e-6, go[:, :K], u, mode="hf", workspace=ws())
+    torch.cuda.synchronize()
+    assert mb.last_variant() == 2
+    assert torch.equal(r_odd.view(torch.int16), r_ref.view(torch.int16))
+    ref_o, _, hn = oracle.add_rmsnorm_glu(gi.bits(x.cpu()), gi.bits(r), gi.bits(w.cpu()), 1e-6, gi.bits(g.cpu()),
+                                          gi.bits(u.cpu()), "hf")
+    _, diag = oracle.glu_gemv(hn, gi.bits(g.cpu()), gi.bits(u.cpu()), "hf", diagnostics=True)
+    diag["dG_extra"], diag["dU_extra"] = tol.norm_rounding_slack(gi.bits(r_odd.cpu()), gi.bits(w.cpu()), 1e-6,
+                                                                 gi.bits(g.cpu()), gi.bits(u.cpu()))
+    tol.assert_parity(gi.bits(out_odd.cpu()), ref_o, tol.conditioning_floor(diag, K, "hf"), "odd stride",
+                      diag=diag, K=K, mode="hf")
+
+
 def test_add_rmsnorm_glu_single_kernel_back_to_back_and_graph():
     """Consecutive calls on one stream share a workspace (also replayed in a
     CUDA graph), each reading the residual the previous one wrote."""
