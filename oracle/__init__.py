@@ -60,6 +60,9 @@ def _bind(lib):
     lib.oracle_add_rmsnorm_glu.restype = i32
     lib.oracle_silu_mul.argtypes = [u16p, i64, u16p, i64, i32, i32, i32]
     lib.oracle_silu_mul.restype = i32
+    f32p = ctypes.POINTER(ctypes.c_float)
+    lib.oracle_gdn_gates.argtypes = [u16p, i64, u16p, i64, f32p, f32p, f64p, u16p, i32, i32]
+    lib.oracle_gdn_gates.restype = i32
     return lib
 
 
@@ -181,3 +184,19 @@ def silu_mul(x, mode="fused", lib=None):
     if st != 0:
         raise ValueError("oracle_silu_mul: bad arguments")
     return out
+
+
+def gdn_gates(a, b, A_log, dt_bias, lib=None):
+    """(g [T,H] float64, beta [T,H] bf16 bits) from a, b [T,H] bf16 bits and
+    A_log, dt_bias [H] float32; see oracle_gdn_gates."""
+    a, b = np.ascontiguousarray(_u16(a)), np.ascontiguousarray(_u16(b))
+    T, H = a.shape
+    A_log = np.ascontiguousarray(A_log, dtype=np.float32)
+    dt_bias = np.ascontiguousarray(dt_bias, dtype=np.float32)
+    g = np.zeros((T, H), dtype=np.float64)
+    beta = np.zeros((T, H), dtype=np.uint16)
+    st = (lib or load()).oracle_gdn_gates(_ptr(a), H, _ptr(b), H, _ptr(A_log, ctypes.c_float),
+                                          _ptr(dt_bias, ctypes.c_float), _ptr(g, ctypes.c_double), _ptr(beta), T, H)
+    if st != 0:
+        raise ValueError("oracle_gdn_gates: bad arguments")
+    return g, beta

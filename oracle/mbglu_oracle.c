@@ -369,3 +369,47 @@ int oracle_silu_mul(const uint16_t *x, int64_t ldx, uint16_t *out, int64_t ldo, 
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* gdn_gates: the decay and write gates of the gated-delta-net layers       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The gates the same segment-KI work fuses beside the GLU ([8602/fused_glu]
+ * commit "feat ... gdn_gates": "beta=sigmoid(b) and
+ * g=-exp(A_log)*softplus(a+dt_bias) with fp32 math and the numerically stable
+ * softplus branch"; [9057/Changes]: "Preserve FP32 GDN decay gates"; strided
+ * inputs: "row-stride input, no contiguous copies").  For every token t < T
+ * and head j < H:
+ *   x    = fp32( a[t, j] + dt_bias[j] )       the binary32 addition the fp32
+ *                                             math performs (a is bf16)
+ *   g    = -exp(A_log[j]) * softplus(x)       returned in binary64
+ *   beta = bf16( sigmoid(b[t, j]) )           one rounding
+ * with softplus(x) = log(1 + e^x) (PyTorch's F.softplus returns x itself for
+ * x > 20, which differs from log(1 + e^x) by less than 2^-64 relative) and
+ * sigmoid(y) = 1 / (1 + e^-y).  The exact values are computed in binary64;
+ * the stable forms (x + log1p(e^-x) for x > 0) keep every digit.
+ * Returns 0, or -1 on bad arguments.
+ */
+static double oracle_softplus(double x)
+{
+    return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));
+}
+
+int oracle_gdn_gates(const uint16_t *a, int64_t lda, const uint16_t *b, int64_t ldb,
+                     const float *A_log, const float *dt_bias,
+                     double *g, uint16_t *beta, int T, int H)
+{
+    if (T < 0 || H < 0) return -1;
+    if (T == 0 || H == 0) return 0;
+    if (!a || !b || !A_log || !dt_bias || !g || !beta || lda < H || ldb < H) return -1;
+    for (int t = 0; t < T; ++t) {
+        for (int j = 0; j < H; ++j) {
+            const float x = (float)oracle_bf16_to_double(a[(int64_t)t * lda + j]) + dt_bias[j];
+            g[(int64_t)t * H + j] = -exp((double)A_log[j]) * oracle_softplus((double)x);
+            const double y = oracle_bf16_to_double(b[(int64_t)t * ldb + j]);
+            beta[(int64_t)t * H + j] = oracle_bf16_round(1.0 / (1.0 + exp(-y)));
+        }
+    }
+    return 0;
+}

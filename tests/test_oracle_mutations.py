@@ -7,6 +7,7 @@ missing epsilon), builds it with the oracle's own flags, and runs a compact
 set of the pins from ``test_oracle_pins.py`` against it.  The unmodified
 source must pass the same set.  Everything runs on the CPU.
 """
+import math
 import os
 import shutil
 from fractions import Fraction
@@ -42,6 +43,10 @@ MUTATIONS = {
                                 "const double g = oracle_bf16_to_double(up[n]);"),
     "silu_mul_hf_unrounded_silu": ("o = oracle_bf16_round(oracle_bf16_to_double(sb) * u);",
                                    "o = oracle_bf16_round(oracle_silu(g) * u);"),
+    "gdn_softplus_unstable": ("return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));", "return log1p(exp(x));"),
+    "gdn_sigmoid_sign": ("oracle_bf16_round(1.0 / (1.0 + exp(-y)))", "oracle_bf16_round(1.0 / (1.0 + exp(y)))"),
+    "gdn_x_not_binary32": ("const float x = (float)oracle_bf16_to_double(a[(int64_t)t * lda + j]) + dt_bias[j];",
+                           "const double x = oracle_bf16_to_double(a[(int64_t)t * lda + j]) + (double)dt_bias[j];"),
 }
 
 
@@ -93,6 +98,25 @@ def quick_pins(lib) -> list:
     s0, h0 = oracle.add_rmsnorm(x, x ^ np.uint16(0x8000), w, 1e-6, lib=lib)
     if not (np.all(s0 == 0) and np.all(h0 == 0)):
         fails.append("norm_cancelled")
+    # gdn_gates: g against binary64 on x = fp32(a + dt_bias), a huge x, beta exact
+    rng = np.random.default_rng(8)
+    ga = gi.bits(torch.tensor(np.append(rng.normal(0, 3, 31), 1000.0), dtype=torch.float32).to(torch.bfloat16))[None, :]
+    gb_ = gi.bits(torch.tensor(rng.normal(0, 3, 32), dtype=torch.float32).to(torch.bfloat16))[None, :]
+    A_log = rng.normal(0, 1, 32).astype(np.float32)
+    dt = rng.normal(0, 1, 32).astype(np.float32)
+    gg, bb = oracle.gdn_gates(ga, gb_, A_log, dt, lib=lib)
+    xa = (((ga.astype(np.uint32) << 16).view(np.float32)) + dt[None, :]).astype(np.float32).astype(np.float64)
+    want = -np.exp(A_log.astype(np.float64)) * np.where(xa > 0, xa + np.log1p(np.exp(-np.abs(xa))),
+                                                        np.log1p(np.exp(np.minimum(xa, 0))))
+    if not np.all(np.abs(gg - want) <= 1e-13 * np.abs(want)):
+        fails.append("gdn_g")
+    yb = (gb_.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for j in range(32):
+        if bb[0, j] != rne_bf16(Fraction(1) / (1 + Fraction(math.exp(-float(yb[0, j]))))):
+            # exp in binary64 is within 1 ulp; only a tie-close value could differ
+            if abs(oracle.bf16_to_float(int(bb[0, j])) - 1 / (1 + math.exp(-yb[0, j]))) > 2 ** -9:
+                fails.append("gdn_beta")
+                break
     # silu_mul, both modes, against exact rounding (gate half first)
     g = gi.bits(gi.normal_bf16((64,), 2.0, 0, "mut-sg"))
     u = gi.bits(gi.normal_bf16((64,), 2.0, 0, "mut-su"))

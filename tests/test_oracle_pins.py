@@ -530,3 +530,53 @@ def test_silu_mul_halves_orientation_strides_and_closed_forms():
     body = gi.bits(gi.normal_bf16((M, 2 * N), 1.0, 0, "sms"))
     wide[:, :2 * N] = body
     assert np.array_equal(oracle.silu_mul(wide[:, :2 * N], "fused"), oracle.silu_mul(body, "fused"))
+
+
+# ---------------------------------------------------------------------------
+# gdn_gates: beta = sigmoid(b), g = -exp(A_log) * softplus(a + dt_bias)
+# ---------------------------------------------------------------------------
+
+def _gdn_inputs(T=7, H=24, seed=0):
+    rng = np.random.default_rng(seed)
+    a = gi.bits(torch.tensor(rng.normal(0, 3, (T, H)), dtype=torch.float32).to(torch.bfloat16))
+    b = gi.bits(torch.tensor(rng.normal(0, 3, (T, H)), dtype=torch.float32).to(torch.bfloat16))
+    A_log = rng.normal(0, 1, H).astype(np.float32)
+    dt_bias = rng.normal(0, 1, H).astype(np.float32)
+    return a, b, A_log, dt_bias
+
+
+def test_gdn_gates_match_arbitrary_precision():
+    """g against mpmath at 120 bits on x = fp32(a + dt_bias) (numpy's IEEE
+    float32 addition), beta against exact rounding of the exact sigmoid."""
+    mpmath = pytest.importorskip("mpmath")
+    a, b, A_log, dt_bias = _gdn_inputs()
+    g, beta = oracle.gdn_gates(a, b, A_log, dt_bias)
+    af = (a.astype(np.uint32) << 16).view(np.float32)
+    bf = (b.astype(np.uint32) << 16).view(np.float32)
+    x = (af + dt_bias[None, :]).astype(np.float32)          # binary32 addition
+    with mpmath.workprec(120):
+        for t in range(a.shape[0]):
+            for j in range(a.shape[1]):
+                xe = mpmath.mpf(float(x[t, j]))
+                ge = -mpmath.exp(mpmath.mpf(float(A_log[j]))) * mpmath.log(1 + mpmath.exp(xe))
+                assert abs(g[t, j] - float(ge)) <= 1e-15 * abs(float(ge))
+                ye = mpmath.mpf(float(bf[t, j]))
+                se = 1 / (1 + mpmath.exp(-ye))
+                assert beta[t, j] == rne_bf16(mpf_to_fraction(se)), (t, j)
+
+
+def test_gdn_gates_closed_forms_and_tails():
+    bits = lambda v: gi.bits(torch.tensor(v, dtype=torch.float32).to(torch.bfloat16))   # noqa: E731
+    a = bits([[0.0, 1000.0, -80.0, 40.0]])
+    b = bits([[0.0, 3.0, -3.0, 100.0]])
+    A_log = np.array([0.0, 0.0, 1.0, np.log(2.0)], dtype=np.float32)
+    dt = np.zeros(4, dtype=np.float32)
+    g, beta = oracle.gdn_gates(a, b, A_log, dt)
+    assert abs(g[0, 0] + math.log(2.0)) < 1e-15                                 # softplus(0) = ln 2
+    assert abs(g[0, 1] + 1000.0) < 1e-12                                        # softplus(x) -> x, no overflow
+    assert abs(g[0, 2] / (-math.e * math.exp(-80.0)) - 1) < 1e-12              # softplus(x) -> e^x
+    assert abs(g[0, 3] / (-float(np.exp(np.float32(np.log(2.0)), dtype=np.float64)) * 40.0) - 1) < 1e-15
+    assert beta[0, 0] == 0x3F00                                                 # sigmoid(0) = 1/2
+    s3 = oracle.bf16_to_float(int(beta[0, 1])) + oracle.bf16_to_float(int(beta[0, 2]))
+    assert abs(s3 - 1.0) <= 2 ** -8                                              # sigmoid(-y) = 1 - sigmoid(y)
+    assert beta[0, 3] == 0x3F80                                                 # rounds to 1
