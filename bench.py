@@ -39,7 +39,8 @@ import glu_inputs as gi  # noqa: E402
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 # mbglu_last_variant() -> the kernel that streams the weights
-KERNEL_NAMES = {1: "glu_stream_kernel", 2: "glu_generic_kernel", 4: "glu_mma_kernel", 5: "silu_mul_kernel"}
+KERNEL_NAMES = {1: "glu_stream_kernel", 2: "glu_generic_kernel", 4: "glu_mma_kernel", 5: "silu_mul_kernel",
+                6: "gdn_gates_kernel"}
 KERNEL_SOURCES = ["memory_bound_glu_gb300/csrc/glu_kernels.cuh", "memory_bound_glu_gb300/csrc/ptx.cuh",
                   "memory_bound_glu_gb300/csrc/mbglu_api.cu"]
 
@@ -200,6 +201,8 @@ def oracle_sample_rate(w, M, mode, seconds, max_rows=None):
     threads = oracle.default_threads()
     if w.op == "silu_mul":
         return _oracle_silu_mul_rate(w, M, mode, seconds)
+    if w.op == "gdn_gates":
+        return _oracle_gdn_rate(w, M, seconds)
     g, u = gi.layer_weights(w, 0)
     gb, ub = gi.bits(g), gi.bits(u)
     rows = w.N if max_rows is None else min(w.N, max_rows)
@@ -244,6 +247,26 @@ def _oracle_silu_mul_rate(w, M, mode, seconds, rows=64):
     return per_call * n / el / 1e9, desc, 1, el / n, per_call
 
 
+def _oracle_gdn_rate(w, T, seconds, tokens=4096):
+    """gdn_gates: the oracle (single-threaded C) on the first `tokens` tokens of
+    input 0, repeated until `seconds` pass."""
+    import oracle
+    a, b, A_log, dt = gi.gdn_inputs(w, min(T, tokens), 0)
+    ab, bb, An, dn = gi.bits(a), gi.bits(b), A_log.numpy(), dt.numpy()
+    per_call = w.algorithmic_bytes(ab.shape[0])
+    oracle.gdn_gates(ab, bb, An, dn)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.gdn_gates(ab, bb, An, dn)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    desc = (f"{n} oracle calls of gdn_gates on tokens 0..{ab.shape[0] - 1} of input 0 (of T={T}), H={w.N}, "
+            f"1 thread, {el:.1f} s")
+    return per_call * n / el / 1e9, desc, 1, el / n, per_call
+
+
 def run_reference(args, w, M, mode, world, rank):
     """Reference arm: the fp64 oracle on the host cores, bounded steps."""
     if rank != 0:
@@ -252,6 +275,19 @@ def run_reference(args, w, M, mode, world, rank):
     import oracle
     if w.op == "silu_mul":
         return _reference_silu_mul(args, w, M, mode, world, steps, warm)
+    if w.op == "gdn_gates":
+        v, desc, thr, el, _ = _oracle_gdn_rate(w, M, max(1.0, 60.0 / (steps + warm)))
+        line = {
+            "impl": "reference", "metric": "GLU GEMV achieved HBM GB/s (cold L2), us/call at M=1",
+            "value": round(v, 4), "unit": "GB/s", "higher_is_better": True, "n_gpus": world,
+            "steps": steps, "warmup": warm, "ms_per_step": round(el * 1e3, 4),
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(w, M, mode, w.layers),
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }
+        print(json.dumps(line), flush=True)
+        return
     g, u = gi.layer_weights(w, 0)
     threads = oracle.default_threads()
     # size the per-step row sample so the whole run stays within ~2 minutes
@@ -321,8 +357,9 @@ def _reference_silu_mul(args, w, M, mode, world, steps, warm):
 def config_dict(w, M, mode, layers, norm_kernels=None):
     wb = w.input_bytes(M) * layers
     extra = {} if w.op == "glu_gemv" or norm_kernels is None else {"norm_kernels": norm_kernels}
-    return {"workload": w.name, "op": w.op, "M": M, "K": w.K, "N": w.N, "mode": mode, "layers": layers, **extra,
-            "l2": f"inputs larger than L2: {layers} cycled {'inputs' if w.op == 'silu_mul' else 'weight pairs'}, "
+    return {"workload": w.name, "op": w.op, "M": M, "K": w.K, "N": w.N,
+            "mode": None if w.op == "gdn_gates" else mode, "layers": layers, **extra,
+            "l2": f"inputs larger than L2: {layers} cycled {'inputs' if w.op in ('silu_mul', 'gdn_gates') else 'weight pairs'}, "
                   f"{wb / 1e9:.2f} GB",
             "launch": f"one CUDA graph of {layers} calls per step",
             "launch_policy": _policy_name()}
@@ -364,7 +401,7 @@ def main():
 
     # inputs: resident in HBM before the timed region
     gates, ups = [], []
-    for layer in range(L if w.op != "silu_mul" else 0):
+    for layer in range(L if w.op in ("glu_gemv", "add_rmsnorm_glu") else 0):
         g, u = gi.layer_weights(w, layer)
         gates.append(g.to(dev))
         ups.append(u.to(dev))
@@ -372,6 +409,10 @@ def main():
     if w.op == "silu_mul":
         xs_cpu = [gi.projections(w, M, layer) for layer in range(L)]
         xs = [t.to(dev) for t in xs_cpu]
+    elif w.op == "gdn_gates":
+        gdn_cpu = [gi.gdn_inputs(w, M, layer) for layer in range(L)]
+        gdn = [tuple(t.to(dev) for t in four) for four in gdn_cpu]
+        gs = [torch.empty((M, w.N), dtype=torch.float32, device=dev) for _ in range(L)]
     elif w.op == "glu_gemv":
         h_cpu = gi.hidden(w, M)
         h = h_cpu.to(dev)
@@ -388,6 +429,8 @@ def main():
         for i in range(L):
             if w.op == "silu_mul":
                 mb.silu_mul(xs[i], out=outs[i], mode=mode)
+            elif w.op == "gdn_gates":
+                mb.gdn_gates(gdn[i][0], gdn[i][1], gdn[i][2], gdn[i][3], g=gs[i], beta=outs[i])
             elif w.op == "glu_gemv":
                 mb.glu_gemv(h, gates[i], ups[i], out=outs[i], mode=mode)
             else:
@@ -442,9 +485,12 @@ def main():
 
     # e2e: the public Python API, pinned host input -> device, results -> host
     e2e = None
-    e2e_steps = min(args.e2e_steps, 10) if w.op == "silu_mul" else args.e2e_steps   # 318 MB to copy per step
+    e2e_steps = min(args.e2e_steps, 10) if w.op in ("silu_mul", "gdn_gates") else args.e2e_steps   # 100s of MB
     if e2e_steps > 0:
-        if w.op == "silu_mul":
+        if w.op == "gdn_gates":
+            ab_host = [(t[0].pin_memory(), t[1].pin_memory()) for t in gdn_cpu]
+            in_bytes = sum(x.numel() + y.numel() for x, y in ab_host) * 2
+        elif w.op == "silu_mul":
             xs_host = [t.pin_memory() for t in xs_cpu]
             in_bytes = sum(t.numel() for t in xs_host) * 2
         elif w.op == "glu_gemv":
@@ -457,7 +503,11 @@ def main():
         out_host = torch.empty((L, M, w.N), dtype=torch.bfloat16).pin_memory()
 
         def e2e_step():
-            if w.op == "silu_mul":
+            if w.op == "gdn_gates":
+                for i in range(L):
+                    gdn[i][0].copy_(ab_host[i][0], non_blocking=True)
+                    gdn[i][1].copy_(ab_host[i][1], non_blocking=True)
+            elif w.op == "silu_mul":
                 for i in range(L):
                     xs[i].copy_(xs_host[i], non_blocking=True)
             elif w.op == "glu_gemv":

@@ -99,7 +99,7 @@ def small_int_bf16(shape: Sequence[int], seed: int, lo: int = -8, hi: int = 8) -
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                      # "glu_gemv", "add_rmsnorm_glu" or "silu_mul"
+    op: str                      # "glu_gemv", "add_rmsnorm_glu", "silu_mul" or "gdn_gates"
     Ms: tuple                    # batch rows exercised
     K: int
     N: int
@@ -113,17 +113,22 @@ class Workload:
     seed: int = 0
 
     def weight_bytes(self) -> int:
-        return 0 if self.op == "silu_mul" else 2 * self.N * self.K * 2
+        return 0 if self.op in ("silu_mul", "gdn_gates") else 2 * self.N * self.K * 2
 
     def input_bytes(self, M: int) -> int:
-        """Per call: both weights for the GEMV paths; x [M, 2N] for silu_mul."""
-        return M * 2 * self.N * 2 if self.op == "silu_mul" else self.weight_bytes()
+        """Per call: both weights for the GEMV paths; x [M, 2N] for silu_mul;
+        a, b [M, N] for gdn_gates (M tokens, N heads)."""
+        if self.op in ("silu_mul", "gdn_gates"):
+            return M * 2 * self.N * 2
+        return self.weight_bytes()
 
     def algorithmic_bytes(self, M: int) -> int:
         """Bytes a call must move at least once: both weights, inputs, outputs."""
         b = self.weight_bytes() + M * self.N * 2
         if self.op == "silu_mul":     # x [M, 2N] read, out [M, N] written
             b += M * 2 * self.N * 2
+        elif self.op == "gdn_gates":  # a, b read (bf16); g (fp32), beta (bf16) written; A_log, dt_bias read
+            return M * self.N * (2 + 2 + 4 + 2) + 2 * self.N * 4
         elif self.op == "glu_gemv":
             b += M * self.K * 2
         else:  # x, residual read; residual written; norm_w read
@@ -151,6 +156,9 @@ WORKLOADS = {
         # the standalone epilogue on a prefill batch (halves layout [M, 2N]):
         # 4096 tokens of the Qwen3.5-4B MLP; two inputs of 159 MB cycled for cold L2
         Workload("silu_mul_m4096_n9728", "silu_mul", (4096,), 0, 9728, ("hf", "fused"), 2, 0.0),
+        # the gated-delta-net gates beside the GLU: 262144 tokens x 32 heads, four
+        # cycled inputs (134 MB of a, b) for cold L2; no rounding mode applies
+        Workload("gdn_gates_t262144_h32", "gdn_gates", (262144,), 0, 32, ("hf",), 4, 0.0),
     ]
 }
 
@@ -179,6 +187,17 @@ def projections(w: Workload, M: int, layer: int = 0, seed: Optional[int] = None)
     M tokens side by side, N(0, h_std) (projections of a unit-variance hidden
     state through N(0, 1/sqrt(K)) weights)."""
     return normal_bf16((M, 2 * w.N), w.h_std, w.seed if seed is None else seed, w.name, "x", layer)
+
+
+def gdn_inputs(w: Workload, T: int, layer: int = 0, seed: Optional[int] = None):
+    """(a, b) bf16 [T, H] CPU tensors ~ N(0, 3) and (A_log, dt_bias) float32 [H]
+    ~ N(0, 1) for gdn_gates: T tokens, H = w.N heads."""
+    s = w.seed if seed is None else seed
+    a = normal_bf16((T, w.N), 3.0, s, w.name, "a", layer)
+    b = normal_bf16((T, w.N), 3.0, s, w.name, "b", layer)
+    A_log = normal_bf16((w.N,), 1.0, s, w.name, "A_log").float()
+    dt_bias = normal_bf16((w.N,), 1.0, s, w.name, "dt_bias").float()
+    return a, b, A_log, dt_bias
 
 
 def norm_inputs(w: Workload, M: int, seed: Optional[int] = None):

@@ -250,6 +250,33 @@ mbglu_status silu_mul(const mbglu_bf16 *x, int64_t ldx, mbglu_bf16 *out, int64_t
                       int M, int N, mbglu_mode mode, cudaStream_t stream);
 
 /*
+ * gdn_gates -- the decay and write gates of the gated-delta-net layers, which
+ * the same segment-KI work fuses beside the GLU.  DeepSpeed PR #8602 commit
+ * adding gdn_gates ("beta=sigmoid(b) and g=-exp(A_log)*softplus(a+dt_bias)
+ * with fp32 math and the numerically stable softplus branch", strided input);
+ * PR #9057 "Changes" ("Preserve FP32 GDN decay gates").  For token t < T and
+ * head j < H:
+ *   x = a[t][j] + dt_bias[j]                 (fp32 addition; a is bf16)
+ *   g[t][j]    = -exp(A_log[j]) * softplus(x)   fp32, softplus(x) = log(1 + e^x)
+ *                                                 in its stable form
+ *   beta[t][j] = bf16(sigmoid(b[t][j]))         one rounding
+ *   a, b     [T][H] bf16 with row strides lda, ldb >= H (views into a wider
+ *            projection output are fine);
+ *   A_log, dt_bias  [H] fp32 (bf16 parameters widen exactly);
+ *   g        [T][H] fp32, row stride ldg >= H; beta [T][H] bf16, ldbeta >= H;
+ *            neither may overlap an input or the other output.
+ * Device pointers owned by the caller; asynchronous on `stream`; no
+ * allocation.  T == 0 or H == 0 is a no-op.  Errors: MBGLU_ERR_SHAPE (T or H
+ * negative), MBGLU_ERR_NULL, MBGLU_ERR_STRIDE, MBGLU_ERR_ALIGN (bf16 pointers
+ * not 2-byte, fp32 pointers not 4-byte aligned), MBGLU_ERR_ALIAS,
+ * MBGLU_ERR_CUDA.
+ */
+mbglu_status gdn_gates(const mbglu_bf16 *a, int64_t lda, const mbglu_bf16 *b, int64_t ldb,
+                       const float *A_log, const float *dt_bias,
+                       float *g, int64_t ldg, mbglu_bf16 *beta, int64_t ldbeta,
+                       int T, int H, cudaStream_t stream);
+
+/*
  * Launch policy, process-wide (default MBGLU_POLICY_PREFETCH).  It decides how
  * a call's kernels are ordered after the kernel that precedes them on the
  * stream; results are identical under every policy.
@@ -288,7 +315,8 @@ int mbglu_last_cuda_error(void);
 
 /* Which kernel the calling thread's last successful call launched:
  * 0 none (no-op), 1 streaming kernel (CUDA-core FMA), 2 generic kernel,
- * 3 zero fill, 4 tensor-core streaming kernel (batch >= 3), 5 silu_mul. */
+ * 3 zero fill, 4 tensor-core streaming kernel (batch >= 3), 5 silu_mul,
+ * 6 gdn_gates. */
 int mbglu_last_variant(void);
 
 /*

@@ -23,7 +23,7 @@ WORKSPACE_BYTES = 256
 
 # Every symbol include/mbglu.h declares.
 EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu_strided", "add_rmsnorm_glu_noalloc",
-           "silu_mul",
+           "silu_mul", "gdn_gates",
            "mbglu_set_launch_policy",
            "mbglu_get_launch_policy",
            "mbglu_status_string", "mbglu_abi_version", "mbglu_last_cuda_error", "mbglu_last_variant",
@@ -56,6 +56,8 @@ def _bind(l):
                                           vp, ctypes.c_size_t, vp]
     l.add_rmsnorm_glu_strided.restype = i32
     l.silu_mul.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp]
+    l.gdn_gates.argtypes = [vp, i64, vp, i64, vp, vp, vp, i64, vp, i64, i32, i32, vp]
+    l.gdn_gates.restype = i32
     l.silu_mul.restype = i32
     l.mbglu_status_string.argtypes = [i32]
     l.mbglu_status_string.restype = ctypes.c_char_p
@@ -216,10 +218,43 @@ def silu_mul(x, out=None, mode="fused", stream=None):
     return out2.view(N) if squeeze else out
 
 
+def gdn_gates(a, b, A_log, dt_bias, g=None, beta=None, stream=None):
+    """Gated-delta-net gates: g = -exp(A_log) * softplus(a + dt_bias) (fp32)
+    and beta = sigmoid(b) (bf16), per token and head.  a, b are [T, H] bf16
+    (row-strided views allowed, contiguous last dimension); A_log, dt_bias are
+    contiguous [H] float32.  Returns (g, beta)."""
+    _check(a, "a", 2)
+    _check(b, "b", 2)
+    T, H = a.shape
+    if tuple(b.shape) != (T, H):
+        raise ValueError(f"b must be [{T},{H}]")
+    for t, name in ((A_log, "A_log"), (dt_bias, "dt_bias")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.float32 or not t.is_cuda or tuple(t.shape) != (H,) \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of shape [{H}]")
+    dev = a.device
+    if g is None:
+        g = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if beta is None:
+        beta = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if g.dtype != torch.float32 or tuple(g.shape) != (T, H) or (g.numel() and g.stride(-1) != 1):
+        raise ValueError(f"g must be a float32 [{T},{H}] tensor with a contiguous last dimension")
+    _check(beta, "beta", 2)
+    if tuple(beta.shape) != (T, H):
+        raise ValueError(f"beta must be [{T},{H}]")
+    with torch.cuda.device(dev):
+        st = lib().gdn_gates(a.data_ptr(), a.stride(0), b.data_ptr(), b.stride(0), A_log.data_ptr(),
+                             dt_bias.data_ptr(), g.data_ptr(), g.stride(0), beta.data_ptr(), beta.stride(0), T, H,
+                             _stream_handle(dev, stream))
+    if st != 0:
+        raise MbgluError(st, "gdn_gates")
+    return g, beta
+
+
 def last_variant() -> int:
     """Kernel the calling thread's last call launched: 0 none, 1 streaming
     (CUDA-core), 2 generic, 3 zero fill, 4 tensor-core streaming (batch >= 3),
-    5 silu_mul."""
+    5 silu_mul, 6 gdn_gates."""
     return lib().mbglu_last_variant()
 
 

@@ -1424,4 +1424,38 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *x, int64_
     }
 }
 
+// ---------------------------------------------------------------------------
+// gdn_gates: decay and write gates of the gated-delta-net layers
+// ---------------------------------------------------------------------------
+// PR #8602 ("fused_glu" commit: "beta=sigmoid(b) and
+// g=-exp(A_log)*softplus(a+dt_bias) with fp32 math and the numerically stable
+// softplus branch"); PR #9057 ("Changes": fp32 decay gates).  For token t,
+// head j: x = a + dt_bias[j] (fp32), g = -exp(A_log[j]) * softplus(x) (fp32),
+// beta = bf16(sigmoid(b)).  softplus in its stable form: x + log1p(e^-x) for
+// x > 0, log1p(e^x) otherwise -- never e^x of a large x -- and sigmoid from
+// e^-|y| likewise.  Elementwise; a and b are row-strided views (e.g. columns
+// of one projection output).
+__global__ void __launch_bounds__(256) gdn_gates_kernel(const uint16_t *a, int64_t lda, const uint16_t *b,
+                                                        int64_t ldb, const float *A_log, const float *dt_bias,
+                                                        float *g, int64_t ldg, uint16_t *beta, int64_t ldbeta,
+                                                        int T, int H)
+{
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int64_t total = static_cast<int64_t>(T) * H;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / H, j = i - t * H;
+        const float x = bf16_to_f32(a[t * lda + j]) + dt_bias[j];
+        const float sp = x > 0.0f ? x + log1pf(expf(-x)) : log1pf(expf(x));
+        g[t * ldg + j] = -expf(A_log[j]) * sp;
+        // sigmoid without overflow: 1/(1 + e^-y) sends e^-y to +inf in fp32 for
+        // y < -88.7 and returns 0, although e^y is still a (subnormal) bf16
+        // value down to y ~ -92
+        const float y = bf16_to_f32(b[t * ldb + j]);
+        const float ty = expf(-fabsf(y));
+        beta[t * ldbeta + j] = f32_to_bf16((y >= 0.0f ? 1.0f : ty) / (1.0f + ty));
+    }
+}
+
 }  // namespace mbglu

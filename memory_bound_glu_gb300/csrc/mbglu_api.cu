@@ -26,7 +26,7 @@ using mbglu::GluParams;
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_variant = 0;
 
-enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4, kSiluMul = 5 };
+enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4, kSiluMul = 5, kGdnGates = 6 };
 
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kBarRegion = 1024;        // mbarriers, stage -> group table, group counter
@@ -527,6 +527,49 @@ mbglu_status mbglu_set_launch_policy(int policy)
 int mbglu_get_launch_policy(void) { return g_policy.load(std::memory_order_relaxed); }
 int mbglu_last_cuda_error(void) { return t_last_cuda_error; }
 int mbglu_last_variant(void) { return t_last_variant; }
+
+mbglu_status gdn_gates(const mbglu_bf16 *a, int64_t lda, const mbglu_bf16 *b, int64_t ldb, const float *A_log,
+                       const float *dt_bias, float *g, int64_t ldg, mbglu_bf16 *beta, int64_t ldbeta, int T, int H,
+                       cudaStream_t stream)
+{
+    t_last_variant = kNone;
+    if (T < 0 || H < 0) return MBGLU_ERR_SHAPE;
+    if (T == 0 || H == 0) return MBGLU_OK;
+    if (!a || !b || !A_log || !dt_bias || !g || !beta) return MBGLU_ERR_NULL;
+    if (lda < H || ldb < H || ldg < H || ldbeta < H) return MBGLU_ERR_STRIDE;
+    if (!aligned(a, 2) || !aligned(b, 2) || !aligned(beta, 2) || !aligned(A_log, 4) || !aligned(dt_bias, 4) ||
+        !aligned(g, 4))
+        return MBGLU_ERR_ALIGN;
+    const int64_t ab = matrix_bytes(T, H, lda), bb = matrix_bytes(T, H, ldb), betab = matrix_bytes(T, H, ldbeta);
+    const int64_t gbytes = matrix_bytes(T, H, ldg) * 2, pb = static_cast<int64_t>(H) * 4;   // fp32: twice bf16's
+    const void *ins[4] = {a, b, A_log, dt_bias};
+    const int64_t inb[4] = {ab, bb, pb, pb};
+    for (int k = 0; k < 4; ++k)
+        if (overlaps(g, gbytes, ins[k], inb[k]) || overlaps(beta, betab, ins[k], inb[k])) return MBGLU_ERR_ALIAS;
+    if (overlaps(g, gbytes, beta, betab)) return MBGLU_ERR_ALIAS;
+    const DeviceInfo *d = nullptr;
+    mbglu_status st = device_info(&d);
+    if (st != MBGLU_OK) return st;
+    const int policy = g_policy.load(std::memory_order_relaxed);
+    const int64_t work = static_cast<int64_t>(T) * H;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(d->sm_count) * 8,
+                                                                            (work + 255) / 256)));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = policy != MBGLU_POLICY_SERIAL ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, mbglu::gdn_gates_kernel, reinterpret_cast<const uint16_t *>(a), lda,
+                                             reinterpret_cast<const uint16_t *>(b), ldb, A_log, dt_bias, g, ldg,
+                                             reinterpret_cast<uint16_t *>(beta), ldbeta, T, H);
+    if (e != cudaSuccess) return cuda_fail(e);
+    t_last_variant = kGdnGates;
+    return MBGLU_OK;
+}
 
 mbglu_status silu_mul(const mbglu_bf16 *x, int64_t ldx, mbglu_bf16 *out, int64_t ldo, int M, int N,
                       mbglu_mode mode, cudaStream_t stream)

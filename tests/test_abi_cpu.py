@@ -106,6 +106,24 @@ def test_add_rmsnorm_glu_strided_validation(kw, code):
     assert mb.lib().mbglu_last_variant() == 0
 
 
+def gates(a=X, lda=64, b=R, ldb=64, A=W, dt=W + 4096, g=O, ldg=32, be=H, ldbe=32, T=3, Hh=32):
+    return mb.lib().gdn_gates(a, lda, b, ldb, A, dt, g, ldg, be, ldbe, T, Hh, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), SHAPE), (dict(Hh=-1), SHAPE),
+    (dict(a=0), NULL), (dict(b=0), NULL), (dict(A=0), NULL), (dict(dt=0), NULL), (dict(g=0), NULL), (dict(be=0), NULL),
+    (dict(lda=31), STRIDE), (dict(ldb=0), STRIDE), (dict(ldg=31), STRIDE), (dict(ldbe=8), STRIDE),
+    (dict(a=X + 1), ALIGN), (dict(A=W + 2), ALIGN), (dict(g=O + 2), ALIGN), (dict(be=H + 1), ALIGN),
+    (dict(g=X + 64), ALIAS), (dict(be=R + 2 * 64 * 2), ALIAS), (dict(g=W), ALIAS), (dict(be=O + 4 * 32 * 2), ALIAS),
+    (dict(T=0), OK), (dict(Hh=0), OK),
+])
+def test_gdn_gates_validation(kw, code):
+    """Host-side validation of gdn_gates (no GPU: rejections and no-op sizes)."""
+    assert gates(**kw) == code
+    assert mb.lib().mbglu_last_variant() == 0
+
+
 def silu(x=X, ldx=64, o=O, ldo=32, M=2, N=32, mode=0):
     return mb.lib().silu_mul(x, ldx, o, ldo, M, N, mode, None)
 

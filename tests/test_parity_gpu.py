@@ -568,7 +568,7 @@ def _layer(name, layer):
     return gi.layer_weights(gi.WORKLOADS[name], layer)
 
 
-FULL_CASES = [(w.name, M, mode) for w in gi.WORKLOADS.values() if w.op != "silu_mul"   # own tests
+FULL_CASES = [(w.name, M, mode) for w in gi.WORKLOADS.values() if w.op in ("glu_gemv", "add_rmsnorm_glu")
               for M in w.Ms for mode in w.modes]
 
 
