@@ -64,3 +64,17 @@ def test_reference_arm_under_torchrun_prints_one_line():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    """The profile records' source hash covers the code the compiler sees:
+    editing a comment keeps it, editing code changes it."""
+    sys.path.insert(0, ROOT)
+    import bench
+    base = 'int f(int x) { return x + 1; }  // add one\n/* doc */ const char *s = "a//b /* not a comment */";\n'
+    same = '/* header */\nint f(int x)\n{\n    return x + 1;   // plus one\n}\nconst char *s = "a//b /* not a comment */";'
+    other = 'int f(int x) { return x + 2; }\nconst char *s = "a//b /* not a comment */";'
+    assert bench._code_only(base) == bench._code_only(same)
+    assert bench._code_only(base) != bench._code_only(other)
+    assert '"a//b /* not a comment */"' in bench._code_only(base)
+    assert len(bench.kernel_source_hash()) == 16
