@@ -12,18 +12,24 @@
 // GB300 design (the pages' warp-per-row Ada kernel with scalar loads is prior
 // art only):
 //   * one persistent CTA per SM, a balanced contiguous range of rows each;
-//   * every warp owns a private ring of shared-memory stages that its lane 0
-//     fills with bulk asynchronous copies (cp.async.bulk, mbarrier completion,
-//     L2 evict-first hint): one stage = a group of consecutive rows of BOTH
-//     matrices, >= 8 KB per copy, ~160 KB of weights in flight per SM;
+//   * every warp owns a private ring of shared-memory stages filled with
+//     asynchronous copies (mbarrier completion, L2 evict-first hint): one
+//     stage holds a group of rows of BOTH matrices;
 //   * with programmatic dependent launch the first stages are requested
 //     before waiting on the preceding kernel, so consecutive calls overlap
 //     one call's tail with the next call's ramp;
-//   * h (or the normed h) sits in shared memory for the whole kernel;
-//   * lanes take 16-byte chunks, packed fp32x2 FMAs, a warp butterfly
-//     reduction, and the epilogue of the requested rounding mode;
 //   * every wait is bounded (globaltimer); a timeout records an error word and
 //     returns instead of hanging or trapping.
+// Kernels in this file:
+//   glu_stream_kernel   batch 1-2, CUDA cores: 1-D bulk copies of whole rows,
+//                       h in registers at batch 1, packed fp32x2 FMAs and a
+//                       warp butterfly; optional add + RMSNorm prologue;
+//   glu_mma_kernel      batch 3-16, tensor cores (mma.sync m16n8k16): one TMA
+//                       box per matrix per stage, static per-warp unit ranges
+//                       with exact accumulator hand-off, h staged in up to two
+//                       K-phases; optional add + RMSNorm prologue;
+//   glu_generic_kernel  any 2-byte-aligned operands (the correctness path);
+//   residual_add_kernel, zero_fill_kernel, silu_mul_kernel, gdn_gates_kernel.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>
