@@ -6,7 +6,11 @@
  *
  * for a small batch (1 <= M <= 16) of bf16 hidden rows, reading the two
  * nn.Linear-layout weight matrices in place (no concatenated copy), with an
- * optional fused residual-add + zero-centred RMSNorm in front.
+ * optional fused residual-add + zero-centred RMSNorm in front
+ * (add_rmsnorm_glu and its one-kernel, strided and no-allocation forms).
+ * Beside it, two ops of the same fused segment: silu_mul, the GLU epilogue
+ * alone on projections a concatenated-weight GEMM has computed, and
+ * gdn_gates, the gates of the gated-delta-net layers.
  *
  * Sources (DeepSpeed pull requests, as printed on their web pages):
  *   [8602/PlanB]   PR #8602 "feat(rollout): HybridEngineRollout graph capture
@@ -39,7 +43,8 @@
  *     ld_gate and ld_up multiples of 8, and K a multiple of 8.  Other
  *     2-byte-aligned inputs run on a slower generic kernel with identical
  *     arithmetic rules.
- *   - Results are bitwise deterministic run to run (no atomics in any sum).
+ *   - Results are bitwise deterministic run to run (no atomics in any sum)
+ *     and do not depend on where a row falls in the matrix.
  */
 #ifndef MBGLU_H
 #define MBGLU_H
@@ -68,7 +73,9 @@ typedef uint16_t mbglu_bf16;   /* raw bf16 bits */
  *                    in fp32, out = bf16(sb * ub).
  *                    [8602/PlanB] b>1 fallback; [9057/Changes] "Restore HF's
  *                    intermediate BF16 rounding in ... GLU".
- * SiLU(x) = x / (1 + exp(-x)) with the precise expf and IEEE division.
+ * SiLU(x) = x / (1 + exp(-x)) with the precise expf and IEEE division,
+ * evaluated from e^-|x| so that no intermediate overflows (silu_mul takes a
+ * correctly rounded reciprocal in place of the division).
  */
 typedef enum { MBGLU_MODE_FUSED = 0, MBGLU_MODE_HF = 1 } mbglu_mode;
 
