@@ -63,6 +63,9 @@ def _bind(lib):
     f32p = ctypes.POINTER(ctypes.c_float)
     lib.oracle_gdn_gates.argtypes = [u16p, i64, u16p, i64, f32p, f32p, f64p, u16p, i32, i32]
     lib.oracle_gdn_gates.restype = i32
+    lib.oracle_glu_backward.argtypes = [u16p, i64, u16p, i64, u16p, i64, u16p, i64, i32, i32, i32,
+                                        f64p, f64p, f64p, f64p, f64p, i32]
+    lib.oracle_glu_backward.restype = i32
     return lib
 
 
@@ -200,3 +203,21 @@ def gdn_gates(a, b, A_log, dt_bias, lib=None):
     if st != 0:
         raise ValueError("oracle_gdn_gates: bad arguments")
     return g, beta
+
+
+def glu_backward(h, gate_w, up_w, dout, nthreads=None, lib=None):
+    """Gradients of out = SiLU(h Wg^T) * (h Wu^T) for an upstream dout, in
+    binary64: (grad_h [M,K], grad_gate [N,K], grad_up [N,K]); inputs are bf16
+    bits (see oracle_glu_backward)."""
+    h, gw, uw, d = (np.ascontiguousarray(_u16(a)) for a in (h, gate_w, up_w, dout))
+    M, K = h.shape
+    N = gw.shape[0]
+    dG = np.zeros((M, N)); dU = np.zeros((M, N))
+    gh = np.zeros((M, K)); gg = np.zeros((N, K)); gu = np.zeros((N, K))
+    f = lambda a: _ptr(a, ctypes.c_double)  # noqa: E731
+    st = (lib or load()).oracle_glu_backward(_ptr(h), K, _ptr(gw), K, _ptr(uw), K, _ptr(d), N, M, N, K,
+                                             f(dG), f(dU), f(gh), f(gg), f(gu),
+                                             nthreads or default_threads())
+    if st != 0:
+        raise ValueError("oracle_glu_backward: bad arguments")
+    return gh, gg, gu

@@ -413,3 +413,117 @@ int oracle_gdn_gates(const uint16_t *a, int64_t lda, const uint16_t *b, int64_t 
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Backward of the dual-weight GLU GEMV                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * [8602/PlanB]: the autograd wrapper saves (hidden, gate_w, up_w) and lets
+ * "gradients flow naturally"; its three gradients matched the composite
+ * F.silu(h @ Wg.T) * (h @ Wu.T) exactly in fp32 ("Verification Results").
+ * So the backward is the gradient of out = SiLU(G) * U with G = h . Wg[n],
+ * U = h . Wu[n], for an upstream gradient dout [M][N]:
+ *   SiLU'(G) = s (1 + G (1 - s)),  s = 1 / (1 + e^-G)
+ *   dG[m,n]  = dout[m,n] * U * SiLU'(G)
+ *   dU[m,n]  = dout[m,n] * SiLU(G)
+ *   grad_h[m,k]  = sum_n dG[m,n] Wg[n,k] + dU[m,n] Wu[n,k]   (n in order)
+ *   grad_Wg[n,k] = sum_m dG[m,n] h[m,k]                     (m in order)
+ *   grad_Wu[n,k] = sum_m dU[m,n] h[m,k]
+ * Everything in binary64 on the exact bf16 inputs; the gradients are returned
+ * in binary64 ([M][K], [N][K], [N][K], row-major, contiguous).
+ */
+typedef struct {
+    const uint16_t *h, *gate_w, *up_w, *dout;
+    int64_t ldh, ld_gate, ld_up, ldd;
+    int M, N, K;
+    double *dG, *dU;                 /* [M][N] scratch */
+    double *grad_h, *grad_gate, *grad_up;
+    int lo, hi;                      /* this worker's n (phase 1) or k (phase 2) range */
+} bwd_job;
+
+static void bwd_rows(const bwd_job *j)   /* phase 1: dG, dU, and the weight gradients of rows [lo, hi) */
+{
+    for (int n = j->lo; n < j->hi; ++n) {
+        const uint16_t *grow = j->gate_w + (int64_t)n * j->ld_gate;
+        const uint16_t *urow = j->up_w + (int64_t)n * j->ld_up;
+        for (int m = 0; m < j->M; ++m) {
+            const uint16_t *hrow = j->h + (int64_t)m * j->ldh;
+            double G = 0.0, U = 0.0;
+            for (int k = 0; k < j->K; ++k) {
+                const double hk = oracle_bf16_to_double(hrow[k]);
+                G += hk * oracle_bf16_to_double(grow[k]);
+                U += hk * oracle_bf16_to_double(urow[k]);
+            }
+            const double s = 1.0 / (1.0 + exp(-G));
+            const double d = oracle_bf16_to_double(j->dout[(int64_t)m * j->ldd + n]);
+            j->dG[(int64_t)m * j->N + n] = d * U * (s * (1.0 + G * (1.0 - s)));
+            j->dU[(int64_t)m * j->N + n] = d * oracle_silu(G);
+        }
+        for (int k = 0; k < j->K; ++k) {
+            double sg = 0.0, su = 0.0;
+            for (int m = 0; m < j->M; ++m) {
+                const double hk = oracle_bf16_to_double(j->h[(int64_t)m * j->ldh + k]);
+                sg += j->dG[(int64_t)m * j->N + n] * hk;
+                su += j->dU[(int64_t)m * j->N + n] * hk;
+            }
+            j->grad_gate[(int64_t)n * j->K + k] = sg;
+            j->grad_up[(int64_t)n * j->K + k] = su;
+        }
+    }
+}
+
+static void bwd_cols(const bwd_job *j)   /* phase 2: grad_h for columns [lo, hi) */
+{
+    for (int m = 0; m < j->M; ++m)
+        for (int k = j->lo; k < j->hi; ++k) {
+            double acc = 0.0;
+            for (int n = 0; n < j->N; ++n) {
+                acc += j->dG[(int64_t)m * j->N + n] * oracle_bf16_to_double(j->gate_w[(int64_t)n * j->ld_gate + k]);
+                acc += j->dU[(int64_t)m * j->N + n] * oracle_bf16_to_double(j->up_w[(int64_t)n * j->ld_up + k]);
+            }
+            j->grad_h[(int64_t)m * j->K + k] = acc;
+        }
+}
+
+static void *bwd_rows_worker(void *arg) { bwd_rows((const bwd_job *)arg); return NULL; }
+static void *bwd_cols_worker(void *arg) { bwd_cols((const bwd_job *)arg); return NULL; }
+
+/* Splits [0, total) over nthreads workers running fn; the split changes only the wall time. */
+static void bwd_run(bwd_job *base, int total, int nthreads, void *(*fn)(void *))
+{
+    bwd_job jobs[256];
+    pthread_t tids[256];
+    if (nthreads > total) nthreads = total;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = *base;
+        jobs[t].lo = (int)(((int64_t)total * t) / nthreads);
+        jobs[t].hi = (int)(((int64_t)total * (t + 1)) / nthreads);
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        if (nthreads == 1 || pthread_create(&tids[t], NULL, fn, &jobs[t]) != 0) break;
+        ++started;
+    }
+    for (int t = 0; t < started; ++t) pthread_join(tids[t], NULL);
+    for (int t = started; t < nthreads; ++t) fn(&jobs[t]);
+}
+
+/* Returns 0, or -1 on bad arguments (the scratch is the caller's dG, dU [M][N]). */
+int oracle_glu_backward(const uint16_t *h, int64_t ldh, const uint16_t *gate_w, int64_t ld_gate,
+                        const uint16_t *up_w, int64_t ld_up, const uint16_t *dout, int64_t ldd,
+                        int M, int N, int K, double *dG, double *dU,
+                        double *grad_h, double *grad_gate, double *grad_up, int nthreads)
+{
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (M == 0 || N == 0 || K == 0) return 0;
+    if (!h || !gate_w || !up_w || !dout || !dG || !dU || !grad_h || !grad_gate || !grad_up) return -1;
+    if (ldh < K || ld_gate < K || ld_up < K || ldd < N) return -1;
+    bwd_job base = {h, gate_w, up_w, dout, ldh, ld_gate, ld_up, ldd, M, N, K, dG, dU,
+                    grad_h, grad_gate, grad_up, 0, 0};
+    bwd_run(&base, N, nthreads, bwd_rows_worker);   /* every dG, dU before any grad_h */
+    bwd_run(&base, K, nthreads, bwd_cols_worker);
+    return 0;
+}

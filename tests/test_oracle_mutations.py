@@ -25,7 +25,8 @@ EPS32 = float(np.float32(1e-6))
 
 MUTATIONS = {
     "silu_sign": ("x / (1.0 + exp(-x))", "x / (1.0 + exp(x))"),
-    "dropped_first_term": ("for (int k = 0; k < j->K; ++k)", "for (int k = 1; k < j->K; ++k)"),
+    "dropped_first_term": ("for (int k = 0; k < j->K; ++k) {\n                const double hk = oracle_bf16_to_double(hrow[k]);\n                const double pg",
+                           "for (int k = 1; k < j->K; ++k) {\n                const double hk = oracle_bf16_to_double(hrow[k]);\n                const double pg"),
     "up_reads_gate": ("const double pu = hk * oracle_bf16_to_double(urow[k]);",
                       "const double pu = hk * oracle_bf16_to_double(grow[k]);"),
     "hf_up_rounds_gate": ("const uint16_t ub = oracle_bf16_round(U);", "const uint16_t ub = oracle_bf16_round(G);"),
@@ -34,7 +35,8 @@ MUTATIONS = {
                            "o = oracle_bf16_round(oracle_bf16_to_double(oracle_bf16_round(oracle_silu(G))) * U);"),
     "ties_away": ("(rem == half && (n & 1))", "(rem == half)"),
     "no_subnormals": ("(e >= -126) ? (e - 7) : -133", "(e - 7)"),
-    "batch_row_index": ("hrow = j->h + (int64_t)m * j->ldh", "hrow = j->h"),
+    "batch_row_index": ("hrow = j->h + (int64_t)m * j->ldh;\n        for (int n = j->n0;",
+                        "hrow = j->h;\n        for (int n = j->n0;"),
     "norm_mean_divisor": ("ss / (double)K", "ss / (double)(K + 1)"),
     "norm_scale_not_centred": ("1.0 + oracle_bf16_to_double(norm_w[k])", "oracle_bf16_to_double(norm_w[k])"),
     "norm_eps_dropped": ("sqrt(var + e)", "sqrt(var)"),
@@ -45,6 +47,8 @@ MUTATIONS = {
                                    "o = oracle_bf16_round(oracle_silu(g) * u);"),
     "gdn_softplus_unstable": ("return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));", "return log1p(exp(x));"),
     "gdn_sigmoid_sign": ("oracle_bf16_round(1.0 / (1.0 + exp(-y)))", "oracle_bf16_round(1.0 / (1.0 + exp(y)))"),
+    "bwd_dsilu_missing_term": ("d * U * (s * (1.0 + G * (1.0 - s)))", "d * U * s"),
+    "bwd_up_grad_from_dG": ("su += j->dU[(int64_t)m * j->N + n] * hk;", "su += j->dG[(int64_t)m * j->N + n] * hk;"),
     "gdn_x_not_binary32": ("const float x = (float)oracle_bf16_to_double(a[(int64_t)t * lda + j]) + dt_bias[j];",
                            "const double x = oracle_bf16_to_double(a[(int64_t)t * lda + j]) + (double)dt_bias[j];"),
 }
@@ -98,6 +102,17 @@ def quick_pins(lib) -> list:
     s0, h0 = oracle.add_rmsnorm(x, x ^ np.uint16(0x8000), w, 1e-6, lib=lib)
     if not (np.all(s0 == 0) and np.all(h0 == 0)):
         fails.append("norm_cancelled")
+    # backward: against fp64 autograd of the composite
+    bh = gi.bits(gi.normal_bf16((2, 12), 1.0, 0, "mut-bh"))
+    bg = gi.bits(gi.normal_bf16((9, 12), 0.3, 0, "mut-bg"))
+    bu = gi.bits(gi.normal_bf16((9, 12), 0.3, 0, "mut-bu"))
+    bd = gi.bits(gi.normal_bf16((2, 9), 1.0, 0, "mut-bd"))
+    got = oracle.glu_backward(bh, bg, bu, bd, lib=lib)
+    f64 = lambda a: torch.from_numpy((a.astype(np.uint32) << 16).view(np.float32).astype(np.float64))  # noqa: E731
+    ht, gt, ut = (f64(a).requires_grad_(True) for a in (bh, bg, bu))
+    ref = torch.autograd.grad(torch.nn.functional.silu(ht @ gt.T) * (ht @ ut.T), (ht, gt, ut), grad_outputs=f64(bd))
+    if any(np.abs(x - r.numpy()).max() > 1e-12 * np.abs(r.numpy()).max() for x, r in zip(got, ref)):
+        fails.append("backward")
     # gdn_gates: g against binary64 on x = fp32(a + dt_bias), a huge x, beta exact
     rng = np.random.default_rng(8)
     ga = gi.bits(torch.tensor(np.append(rng.normal(0, 3, 31), 1000.0), dtype=torch.float32).to(torch.bfloat16))[None, :]

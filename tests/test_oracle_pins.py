@@ -580,3 +580,66 @@ def test_gdn_gates_closed_forms_and_tails():
     s3 = oracle.bf16_to_float(int(beta[0, 1])) + oracle.bf16_to_float(int(beta[0, 2]))
     assert abs(s3 - 1.0) <= 2 ** -8                                              # sigmoid(-y) = 1 - sigmoid(y)
     assert beta[0, 3] == 0x3F80                                                 # rounds to 1
+
+
+# ---------------------------------------------------------------------------
+# backward of the dual-weight GLU GEMV
+# ---------------------------------------------------------------------------
+
+def _bwd_inputs(M=3, N=20, K=24, seed=0):
+    h = gi.bits(gi.normal_bf16((M, K), 1.0, seed, "bw-h"))
+    gw = gi.bits(gi.normal_bf16((N, K), 0.3, seed, "bw-g"))
+    uw = gi.bits(gi.normal_bf16((N, K), 0.3, seed, "bw-u"))
+    d = gi.bits(gi.normal_bf16((M, N), 1.0, seed, "bw-d"))
+    return h, gw, uw, d
+
+
+def _f64(bits_):
+    return torch.from_numpy((np.asarray(bits_, np.uint32) << 16).view(np.float32).astype(np.float64))
+
+
+def test_glu_backward_matches_fp64_autograd():
+    """The three gradients against PyTorch autograd of the fp64 composite
+    F.silu(h @ Wg.T) * (h @ Wu.T) on the same (exact) inputs."""
+    h, gw, uw, d = _bwd_inputs()
+    gh, gg, gu = oracle.glu_backward(h, gw, uw, d)
+    ht, gt, ut = (_f64(a).requires_grad_(True) for a in (h, gw, uw))
+    out = torch.nn.functional.silu(ht @ gt.T) * (ht @ ut.T)
+    rh, rg, ru = torch.autograd.grad(out, (ht, gt, ut), grad_outputs=_f64(d))
+    for got, ref in ((gh, rh), (gg, rg), (gu, ru)):
+        ref = ref.numpy()
+        assert np.abs(got - ref).max() <= 1e-12 * np.abs(ref).max()
+
+
+def test_glu_backward_finite_differences():
+    """Central differences of sum(dout * out) in binary64 along a few
+    coordinates of h, Wg and Wu."""
+    h, gw, uw, d = _bwd_inputs(M=2, N=6, K=5, seed=1)
+    gh, gg, gu = oracle.glu_backward(h, gw, uw, d)
+    H, G, U, D = (_f64(a).numpy() for a in (h, gw, uw, d))
+
+    def f(H_, G_, U_):
+        g = H_ @ G_.T
+        return float(np.sum(D * (g / (1 + np.exp(-g))) * (H_ @ U_.T)))
+
+    eps = 1e-6
+    for arr, grad, idx in ((H, gh, (1, 3)), (G, gg, (4, 2)), (U, gu, (0, 0)), (U, gu, (5, 4))):
+        p, m = arr.copy(), arr.copy()
+        p[idx] += eps
+        m[idx] -= eps
+        args_p = [p if arr is x else x for x in (H, G, U)]
+        args_m = [m if arr is x else x for x in (H, G, U)]
+        fd = (f(*args_p) - f(*args_m)) / (2 * eps)
+        assert abs(fd - grad[idx]) <= 1e-6 * max(1.0, abs(fd)), (idx, fd, grad[idx])
+
+
+def test_glu_backward_closed_forms_and_threads():
+    h, gw, uw, d = _bwd_inputs(seed=2)
+    gh, gg, gu = oracle.glu_backward(h, gw, uw, np.zeros_like(d))
+    assert not gh.any() and not gg.any() and not gu.any()             # no upstream gradient
+    gh, gg, gu = oracle.glu_backward(h, gw, np.zeros_like(uw), d)      # up_w = 0: U = 0
+    assert not gh.any() and not gg.any() and gu.any()                  # only dWu = (dout*SiLU(G))^T h
+    a = oracle.glu_backward(h, gw, uw, d, nthreads=1)
+    b = oracle.glu_backward(h, gw, uw, d, nthreads=7)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
