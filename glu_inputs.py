@@ -145,6 +145,9 @@ WORKLOADS = {
         # batched decode, both modes
         Workload("gemv_k2560_n9728_batched", "glu_gemv", (1, 2, 4, 8), 2560, 9728, ("fused", "hf"), 32,
                  1 / math.sqrt(2560)),
+        # batched decode at 32 and 64 rows (row blocks of 16, one pass over the
+        # weights each), HF-boundary rounding
+        Workload("gemv_k2560_n9728_wide", "glu_gemv", (32, 64), 2560, 9728, ("hf",), 32, 1 / math.sqrt(2560)),
         # fused residual-add + zero-centred RMSNorm prologue
         Workload("norm_gemv_k2560_n9728", "add_rmsnorm_glu", (1, 4, 8), 2560, 9728, ("hf",), 32,
                  1 / math.sqrt(2560)),

@@ -4,7 +4,7 @@
  *
  *   out[m, n] = SiLU( sum_k h[m,k] * gate_w[n,k] ) * ( sum_k h[m,k] * up_w[n,k] )
  *
- * for a small batch (1 <= M <= 16) of bf16 hidden rows, reading the two
+ * for a small batch (1 <= M <= 64) of bf16 hidden rows, reading the two
  * nn.Linear-layout weight matrices in place (no concatenated copy), with an
  * optional fused residual-add + zero-centred RMSNorm in front
  * (add_rmsnorm_glu and its one-kernel, strided and no-allocation forms).
@@ -36,8 +36,9 @@
  *   - Calls are asynchronous on `stream` (0 = the legacy default stream); no
  *     host synchronisation, no host reads of device data.
  *   - Arguments are validated on the host before anything is launched; a
- *     non-zero status means nothing was launched.  No C++ exception crosses
- *     this boundary.
+ *     non-zero status other than MBGLU_ERR_CUDA means nothing was launched
+ *     (MBGLU_ERR_CUDA may follow kernels of the same call that did launch).
+ *     No C++ exception crosses this boundary.
  *   - The fast kernels stream both weight matrices through shared memory
  *     with bulk asynchronous copies; they need gate_w/up_w 16-byte aligned,
  *     ld_gate and ld_up multiples of 8, and K a multiple of 8.  Other
@@ -45,6 +46,12 @@
  *     arithmetic rules.
  *   - Results are bitwise deterministic run to run (no atomics in any sum)
  *     and do not depend on where a row falls in the matrix.
+ *   - One pass of the GEMV kernels takes up to MBGLU_BLOCK_M = 16 batch rows.
+ *     A batch of 17..64 rows (PR #9057, the commit squashing the A100
+ *     optimisation session, runs decode at batch 8, 32 and 64) runs as row
+ *     blocks of 16, the remainder last, each block a full pass
+ *     over both weights: M = 64 streams the weights four times.  Each row's
+ *     result is the one a call on that row alone gives.
  */
 #ifndef MBGLU_H
 #define MBGLU_H
@@ -57,8 +64,9 @@
 extern "C" {
 #endif
 
-#define MBGLU_ABI_VERSION 1
-#define MBGLU_MAX_M 16
+#define MBGLU_ABI_VERSION 2
+#define MBGLU_MAX_M 64     /* batch rows per call */
+#define MBGLU_BLOCK_M 16   /* batch rows per pass over the weights */
 
 typedef uint16_t mbglu_bf16;   /* raw bf16 bits */
 
@@ -83,7 +91,7 @@ typedef int mbglu_status;
 #define MBGLU_OK            0
 #define MBGLU_ERR_NULL      1   /* a required pointer is NULL */
 #define MBGLU_ERR_SHAPE     2   /* M, N or K negative; M > MBGLU_MAX_M; K == 0 with the norm;
-                                   add_rmsnorm_glu with M*K*2 bytes above its shared-memory limit */
+                                   add_rmsnorm_glu with one pass's rows above its shared-memory limit */
 #define MBGLU_ERR_STRIDE    3   /* a leading dimension smaller than the row it holds */
 #define MBGLU_ERR_ALIGN     4   /* a pointer not 2-byte aligned */
 #define MBGLU_ERR_MODE      5   /* mode is neither FUSED nor HF */
@@ -131,13 +139,15 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh,
  * Per row, in fp32:  var = mean_k s^2;  h = bf16( (s * rsqrt(var + eps)) *
  * (1 + (float)norm_w) );  then out = GLU(h) in `mode` (mode affects only
  * the GLU epilogue; s and h round to bf16 in both modes).
- *   1 <= K, 0 <= M <= MBGLU_MAX_M, M*K*2 bytes must fit the kernel's
- *   shared-memory budget (M*K <= 81920, e.g. M=16 with K=5120).
+ *   1 <= K, 0 <= M <= MBGLU_MAX_M, and the rows of one pass must fit the
+ *   kernel's shared-memory budget: min(M, MBGLU_BLOCK_M)*K <= 81920 (K <= 5120
+ *   once M >= 16).
  *   out must not overlap any input; residual must not overlap x partially,
  *   nor norm_w, gate_w, up_w (MBGLU_ERR_ALIAS).  residual == x is allowed.
  * Two kernels run on `stream`: the residual add, then the GEMV, which reads
  * residual only after the add has completed (see the launch policy below
- * for what each may do before its predecessor has finished).
+ * for what each may do before its predecessor has finished); above
+ * MBGLU_BLOCK_M rows, the two per row block.
  */
 mbglu_status add_rmsnorm_glu(const mbglu_bf16 *x, mbglu_bf16 *residual,
                              const mbglu_bf16 *norm_w, float eps,
@@ -323,7 +333,8 @@ int mbglu_last_cuda_error(void);
 /* Which kernel the calling thread's last successful call launched:
  * 0 none (no-op), 1 streaming kernel (CUDA-core FMA), 2 generic kernel,
  * 3 zero fill, 4 tensor-core streaming kernel (batch >= 3), 5 silu_mul,
- * 6 gdn_gates. */
+ * 6 gdn_gates, 7 row blocks (a batch above MBGLU_BLOCK_M: one of 1-4 per
+ * block). */
 int mbglu_last_variant(void);
 
 /*

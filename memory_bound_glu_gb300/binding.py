@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(HERE, "libmbglu.so")
 MODE_FUSED = 0
 MODE_HF = 1
 _MODES = {"fused": MODE_FUSED, "hf": MODE_HF, MODE_FUSED: MODE_FUSED, MODE_HF: MODE_HF}
-MAX_M = 16
+MAX_M = 64        # batch rows per call (MBGLU_MAX_M)
+BLOCK_M = 16      # batch rows per pass over the weights (MBGLU_BLOCK_M)
 WORKSPACE_BYTES = 256
 
 # Every symbol include/mbglu.h declares.

@@ -26,7 +26,11 @@ using mbglu::GluParams;
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_variant = 0;
 
-enum Variant { kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4, kSiluMul = 5, kGdnGates = 6 };
+enum Variant {
+    kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4, kSiluMul = 5, kGdnGates = 6,
+    kRowBlocks = 7   // a batch above kBlockRows, run as row blocks
+};
+constexpr int kBlockRows = mbglu::kMaxM;   // rows one GEMV kernel takes (its batch tile)
 
 constexpr int kMaxDevices = 64;
 constexpr uint32_t kBarRegion = 1024;        // mbarriers, stage -> group table, group counter
@@ -623,11 +627,16 @@ const char *mbglu_status_string(mbglu_status s)
     }
 }
 
-mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
-                      const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
-                      mbglu_mode mode, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+// Every argument check of glu_gemv, on the whole call: nothing launches when
+// one fails.
+mbglu_status check_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
+                        const mbglu_bf16 *up_w, int64_t ld_up, const mbglu_bf16 *out, int64_t ldo, int M, int N,
+                        int K, mbglu_mode mode)
 {
-    t_last_variant = kNone;
     if (mode != MBGLU_MODE_FUSED && mode != MBGLU_MODE_HF) return MBGLU_ERR_MODE;
     if (M < 0 || N < 0 || K < 0 || M > MBGLU_MAX_M) return MBGLU_ERR_SHAPE;
     if (M == 0 || N == 0) return MBGLU_OK;
@@ -639,7 +648,14 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
     if (K > 0 && (overlaps(out, ob, h, matrix_bytes(M, K, ldh)) || overlaps(out, ob, gate_w, matrix_bytes(N, K, ld_gate)) ||
                   overlaps(out, ob, up_w, matrix_bytes(N, K, ld_up))))
         return MBGLU_ERR_ALIAS;
+    return MBGLU_OK;
+}
 
+// The GEMV on 1 <= M <= kBlockRows rows, N >= 1, arguments already checked.
+mbglu_status gemv_block(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
+                        const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
+                        mbglu_mode mode, cudaStream_t stream)
+{
     const DeviceInfo *d = nullptr;
     mbglu_status st = device_info(&d);
     if (st != MBGLU_OK) return st;
@@ -714,23 +730,46 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
     return st;
 }
 
+}  // namespace
+
+extern "C" {
+
+mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
+                      const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
+                      mbglu_mode mode, cudaStream_t stream)
+{
+    t_last_variant = kNone;
+    mbglu_status st = check_gemv(h, ldh, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode);
+    if (st != MBGLU_OK || M == 0 || N == 0) return st;
+    if (M <= kBlockRows) return gemv_block(h, ldh, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode, stream);
+    // a batch above one kernel's tile: row blocks of kBlockRows, the remainder
+    // last, each a full pass over the weights (rows are independent, and every
+    // kernel's result for a row does not depend on the rows beside it)
+    for (int m0 = 0; m0 < M; m0 += kBlockRows) {
+        const int mb = std::min(kBlockRows, M - m0);
+        st = gemv_block(K > 0 ? h + static_cast<int64_t>(m0) * ldh : h, ldh, gate_w, ld_gate, up_w, ld_up,
+                        out + static_cast<int64_t>(m0) * ldo, ldo, mb, N, K, mode, stream);
+        if (st != MBGLU_OK) {
+            t_last_variant = kNone;
+            return st;
+        }
+    }
+    t_last_variant = kRowBlocks;
+    return MBGLU_OK;
+}
+
 }  // extern "C"
 
 namespace {
 
-// Both add_rmsnorm_glu entry points.  ws == nullptr: residual-add kernel, then
-// the GEMV with the norm prologue.  ws != nullptr: one kernel (the add is
-// formed in shared memory, residual written back by the last CTA), where the
-// fast kernels apply; otherwise the two-kernel path.
-mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
-                                  const mbglu_bf16 *gate_w, int64_t ld_gate, const mbglu_bf16 *up_w, int64_t ld_up,
-                                  mbglu_bf16 *out, int64_t ldo, int M, int N, int K, mbglu_mode mode, int *ws,
-                                  cudaStream_t stream)
+// Every argument check of the add_rmsnorm_glu entry points, on the whole call.
+mbglu_status check_norm(const mbglu_bf16 *x, const mbglu_bf16 *residual, const mbglu_bf16 *norm_w,
+                        const mbglu_bf16 *gate_w, int64_t ld_gate, const mbglu_bf16 *up_w, int64_t ld_up,
+                        const mbglu_bf16 *out, int64_t ldo, int M, int N, int K, mbglu_mode mode, const int *ws)
 {
-    t_last_variant = kNone;
     if (mode != MBGLU_MODE_FUSED && mode != MBGLU_MODE_HF) return MBGLU_ERR_MODE;
     if (M < 0 || N < 0 || K <= 0 || M > MBGLU_MAX_M) return MBGLU_ERR_SHAPE;
-    if (static_cast<int64_t>(M) * K > kNormMaxMK) return MBGLU_ERR_SHAPE;
+    if (static_cast<int64_t>(std::min(M, kBlockRows)) * K > kNormMaxMK) return MBGLU_ERR_SHAPE;
     if (M == 0) return MBGLU_OK;
     if (!x || !residual || !norm_w || (N > 0 && (!gate_w || !up_w || !out))) return MBGLU_ERR_NULL;
     if (N > 0 && (ld_gate < K || ld_up < K || ldo < N)) return MBGLU_ERR_STRIDE;
@@ -751,7 +790,19 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
             (N > 0 && (overlaps(ws, wsb, gate_w, gb) || overlaps(ws, wsb, up_w, ub) || overlaps(ws, wsb, out, ob))))
             return MBGLU_ERR_ALIAS;
     }
+    return MBGLU_OK;
+}
 
+// add_rmsnorm_glu on 1 <= M <= kBlockRows rows, arguments already checked.
+// ws == nullptr: residual-add kernel, then the GEMV with the norm prologue.
+// ws != nullptr: one kernel (the add is formed in shared memory, residual
+// written back by the last CTA), where the fast kernels apply; otherwise the
+// two-kernel path.
+mbglu_status norm_block(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
+                        const mbglu_bf16 *gate_w, int64_t ld_gate, const mbglu_bf16 *up_w, int64_t ld_up,
+                        mbglu_bf16 *out, int64_t ldo, int M, int N, int K, mbglu_mode mode, int *ws,
+                        cudaStream_t stream)
+{
     const DeviceInfo *d = nullptr;
     mbglu_status st = device_info(&d);
     if (st != MBGLU_OK) return st;
@@ -881,6 +932,33 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
     st = launch(mbglu::glu_generic_kernel<true>, dim3(generic_grid(*d, N)), dim3(256), smem, stream, pdl, p);
     if (st == MBGLU_OK) t_last_variant = kGeneric;
     return st;
+}
+
+mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_bf16 *norm_w, float eps,
+                                  const mbglu_bf16 *gate_w, int64_t ld_gate, const mbglu_bf16 *up_w, int64_t ld_up,
+                                  mbglu_bf16 *out, int64_t ldo, int M, int N, int K, mbglu_mode mode, int *ws,
+                                  cudaStream_t stream)
+{
+    t_last_variant = kNone;
+    mbglu_status st = check_norm(x, residual, norm_w, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode, ws);
+    if (st != MBGLU_OK || M == 0) return st;
+    if (M <= kBlockRows)
+        return norm_block(x, residual, norm_w, eps, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode, ws, stream);
+    // row blocks, as glu_gemv: the add, the statistic and the normed row are
+    // per row.  Consecutive blocks share the workspace, which every completed
+    // single-kernel call leaves zero.
+    for (int m0 = 0; m0 < M; m0 += kBlockRows) {
+        const int mb = std::min(kBlockRows, M - m0);
+        const int64_t xo = static_cast<int64_t>(m0) * K;
+        st = norm_block(x + xo, residual + xo, norm_w, eps, gate_w, ld_gate, up_w, ld_up,
+                        N > 0 ? out + static_cast<int64_t>(m0) * ldo : out, ldo, mb, N, K, mode, ws, stream);
+        if (st != MBGLU_OK) {
+            t_last_variant = kNone;
+            return st;
+        }
+    }
+    t_last_variant = N > 0 ? kRowBlocks : kNone;   // N == 0: the residual adds alone, as for one block
+    return MBGLU_OK;
 }
 
 }  // namespace

@@ -62,7 +62,10 @@ def norm(x=X, r=R, w=W, g=G, u=U, o=O, M=2, N=32, K=64, mode=1):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(mode=2), MODE), (dict(mode=-1), MODE),
-    (dict(M=-1), SHAPE), (dict(N=-1), SHAPE), (dict(K=-1), SHAPE), (dict(M=17), SHAPE),
+    (dict(M=-1), SHAPE), (dict(N=-1), SHAPE), (dict(K=-1), SHAPE), (dict(M=65), SHAPE),
+    # a batch of row blocks is checked whole before any block launches: out
+    # overlaps h only from h's row 30 on, past the first block
+    (dict(M=40, o=H + 2 * 64 * 30), ALIAS), (dict(M=40, ldh=64, h=O - 2 * 64 * 39), ALIAS),
     (dict(h=0), NULL), (dict(g=0), NULL), (dict(u=0), NULL), (dict(o=0), NULL),
     (dict(ldh=63), STRIDE), (dict(ldg=10), STRIDE), (dict(ldu=0), STRIDE), (dict(ldo=31), STRIDE),
     (dict(h=H + 1), ALIGN), (dict(g=G + 1), ALIGN), (dict(u=U + 3), ALIGN), (dict(o=O + 1), ALIGN),
@@ -76,7 +79,10 @@ def test_glu_gemv_validation(kw, code):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(mode=3), MODE), (dict(K=0), SHAPE), (dict(M=17), SHAPE), (dict(M=16, K=8192), SHAPE),
+    (dict(mode=3), MODE), (dict(K=0), SHAPE), (dict(M=65), SHAPE), (dict(M=16, K=8192), SHAPE),
+    (dict(M=40, K=8192), SHAPE),                      # one pass holds 16 rows of s: 16 * K <= 81920
+    (dict(M=40, o=R + 2 * 64 * 30), ALIAS),           # out meets residual's row 30, past the first block
+    (dict(M=40, r=X + 2 * 64 * 20), ALIAS),           # residual overlaps x partially, from row 20 on
     (dict(x=0), NULL), (dict(r=0), NULL), (dict(w=0), NULL), (dict(g=0), NULL), (dict(o=0), NULL),
     (dict(x=X + 1), ALIGN), (dict(r=R + 1), ALIGN), (dict(o=O + 1), ALIGN),
     (dict(o=X), ALIAS), (dict(o=R + 2), ALIAS), (dict(o=W), ALIAS), (dict(o=G), ALIAS),
@@ -94,7 +100,8 @@ def norm_strided(x=X, r=R, w=W, g=G, ldg=96, u=U, ldu=72, o=O, ldo=40, M=2, N=32
 
 @pytest.mark.parametrize("kw,code", [
     (dict(ldg=63), STRIDE), (dict(ldu=10), STRIDE), (dict(ldo=31), STRIDE),
-    (dict(mode=3), MODE), (dict(K=0), SHAPE), (dict(M=17), SHAPE),
+    (dict(mode=3), MODE), (dict(K=0), SHAPE), (dict(M=65), SHAPE),
+    (dict(M=33, o=G - 2 * 40 * 32), ALIAS),   # only out's row 32 (the third block) meets gate_w
     (dict(g=G + 1), ALIGN), (dict(ws=X + 0x1000000 + 8), ALIGN), (dict(ws=X + 0x1000000, wsb=255), SHAPE),
     (dict(o=G + 2 * 96 * 31), ALIAS), (dict(r=U + 2 * 72 * 5), ALIAS), (dict(ws=O + 2 * 40), ALIAS),
     (dict(M=0), OK),
@@ -181,7 +188,8 @@ def norm_ws(ws=WS, nbytes=256, **kw):
 @pytest.mark.parametrize("kw,code", [
     (dict(ws=0), NULL), (dict(nbytes=255), SHAPE), (dict(ws=WS + 8), ALIGN),
     (dict(ws=X), ALIAS), (dict(ws=O + 64), ALIAS), (dict(ws=G + 1024), ALIAS),
-    (dict(M=17), SHAPE), (dict(mode=2), MODE), (dict(x=0), NULL), (dict(M=0), OK),
+    (dict(M=65), SHAPE), (dict(mode=2), MODE), (dict(x=0), NULL), (dict(M=0), OK),
+    (dict(M=48, ws=X + 2 * 64 * 47), ALIAS),          # the workspace sits in x's last block
 ])
 def test_add_rmsnorm_glu_ws_validation(kw, code):
     assert norm_ws(**kw) == code

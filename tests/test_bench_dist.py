@@ -78,3 +78,19 @@ def test_kernel_source_hash_ignores_comments_only():
     assert bench._code_only(base) != bench._code_only(other)
     assert '"a//b /* not a comment */"' in bench._code_only(base)
     assert len(bench.kernel_source_hash()) == 16
+
+
+def test_row_block_count_matches_the_header():
+    """bench.py counts a call's passes over the weights with the header's
+    batch rows per pass; the batch limit and the binding agree with it."""
+    import re
+    sys.path.insert(0, ROOT)
+    import bench
+    import glu_inputs as gi
+    import memory_bound_glu_gb300 as mb
+    hdr = open(os.path.join(ROOT, "include", "mbglu.h")).read()
+    assert int(re.search(r"#define MBGLU_BLOCK_M (\d+)", hdr).group(1)) == bench.BLOCK_M == mb.BLOCK_M
+    assert int(re.search(r"#define MBGLU_MAX_M (\d+)", hdr).group(1)) == mb.MAX_M
+    w = gi.WORKLOADS["gemv_k2560_n9728_wide"]
+    assert [bench.row_blocks(w, M) for M in (1, 16, 17, 32, 33, 64)] == [1, 1, 2, 2, 3, 4]
+    assert bench.row_blocks(gi.WORKLOADS["silu_mul_m4096_n9728"], 4096) == 1

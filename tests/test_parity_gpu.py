@@ -41,7 +41,7 @@ def oracle_glu(h, g, u, mode):
 
 def parity(got, ref, tau_info, what=""):
     tau, diag, K, mode = tau_info
-    if mb.last_variant() == 4:      # tensor-core accumulation bound
+    if mb.last_variant() in (4, 7):   # tensor-core accumulation bound (7: row blocks, mostly tensor core)
         diag["acc"] = "mma"
         tau = tol.conditioning_floor(diag, K, mode)
     return tol.assert_parity(got, ref, tau, what, diag=diag, K=K, mode=mode)
@@ -242,7 +242,7 @@ def test_degenerate_sizes():
     assert mb.last_variant() == 3
     assert (gi.bits(o.cpu()) == 0).all()
     with pytest.raises(mb.MbgluError):
-        mb.glu_gemv(torch.zeros((17, K), dtype=torch.bfloat16, device=DEV), w, w)
+        mb.glu_gemv(torch.zeros((mb.MAX_M + 1, K), dtype=torch.bfloat16, device=DEV), w, w)
 
 
 @pytest.mark.parametrize("mode", ["fused", "hf"])
@@ -579,7 +579,7 @@ def test_full_size_workload(name, M, mode):
     g, u = _layer(name, layer)
     if w.op == "glu_gemv":
         h = gi.hidden(w, M)
-        st = check(h, g, u, mode, f"{name} M={M} {mode}", variant=1)
+        st = check(h, g, u, mode, f"{name} M={M} {mode}", variant=1 if M <= mb.BLOCK_M else 7)
     else:
         x, r, nw = gi.norm_inputs(w, M)
         st = check_norm(x, r, nw, g, u, mode, eps=w.eps, what=f"{name} M={M}", variant=1)
