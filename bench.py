@@ -121,18 +121,23 @@ def kernel_source_hash():
 
 
 def recorded_traffic(workload, M, mode):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel
-    sources still hash to what was profiled; else None."""
+    """(current, last): DRAM bytes per launch from the committed ncu summary.
+    current is the figure if the kernel sources still hash to what was
+    profiled, else None; last describes the newest capture either way (None
+    if the workload was never captured)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
     except Exception:
-        return None
+        return None, None
     rec = d.get(f"{workload}/M{M}/{mode}")
-    if not rec or rec.get("source_hash") != kernel_source_hash():
-        return None
-    return rec.get("dram_bytes_per_launch")
+    if not rec:
+        return None, None
+    same = rec.get("source_hash") == kernel_source_hash()
+    last = {"dram_bytes_per_launch": rec.get("dram_bytes_per_launch"), "kernel": rec.get("kernel"),
+            "source_hash": rec.get("source_hash"), "sources_changed_since": not same}
+    return (rec.get("dram_bytes_per_launch") if same else None), last
 
 
 class ClockSampler:
@@ -593,7 +598,7 @@ def main():
         cpu = {"value": round(v, 4), "unit": "GB/s", "cores": thr, "kind": "oracle", "sample": desc}
 
     if rank == 0:
-        traffic = recorded_traffic(w.name, M, mode)
+        traffic, traffic_last = recorded_traffic(w.name, M, mode)
         line = {
             "metric": "GLU GEMV achieved HBM GB/s (cold L2), us/call at M=1",
             "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -605,7 +610,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": round(launch_gbs, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(launch_gbs / peak, 4), "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                          if peak_kind == "measured" else "fallback 6.8 TB/s",
-                         "traffic": traffic, "kernel": kernel_name,
+                         "traffic": traffic, "traffic_last_capture": traffic_last, "kernel": kernel_name,
                          "achieved_how": "algorithmic bytes per launch / (CUDA-event time of the timed "
                                          "graph replays / launches)"
                                          + (f"; {blocks} row blocks per call, each streaming both weights"

@@ -94,3 +94,20 @@ def test_row_block_count_matches_the_header():
     w = gi.WORKLOADS["gemv_k2560_n9728_wide"]
     assert [bench.row_blocks(w, M) for M in (1, 16, 17, 32, 33, 64)] == [1, 1, 2, 2, 3, 4]
     assert bench.row_blocks(gi.WORKLOADS["silu_mul_m4096_n9728"], 4096) == 1
+
+
+def test_recorded_traffic_is_current_only_for_the_profiled_sources(monkeypatch):
+    """traffic is reported only while the kernel sources hash to the profiled
+    ones; otherwise it is None and the last capture is described, marked as
+    taken on other sources."""
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["gemv_k2560_n9728/M1/hf"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: rec["source_hash"])
+    cur, last = bench.recorded_traffic("gemv_k2560_n9728", 1, "hf")
+    assert cur == rec["dram_bytes_per_launch"] and last["sources_changed_since"] is False
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    cur, last = bench.recorded_traffic("gemv_k2560_n9728", 1, "hf")
+    assert cur is None and last["sources_changed_since"] is True
+    assert last["dram_bytes_per_launch"] == rec["dram_bytes_per_launch"]
+    assert bench.recorded_traffic("gemv_k2560_n9728_wide", 64, "hf") == (None, None)
