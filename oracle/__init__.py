@@ -48,6 +48,8 @@ def _bind(lib):
     lib.oracle_bf16_round.restype = ctypes.c_uint16
     lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
     lib.oracle_bf16_to_double.restype = ctypes.c_double
+    lib.oracle_bf16_round_array.argtypes = [f64p, u16p, i64]
+    lib.oracle_bf16_round_array.restype = None
     lib.oracle_silu.argtypes = [ctypes.c_double]
     lib.oracle_silu.restype = ctypes.c_double
     lib.oracle_glu_gemv.argtypes = [u16p, i64, u16p, i64, u16p, i64, u16p, i64,
@@ -107,6 +109,14 @@ def _ptr(a, ctype=ctypes.c_uint16):
 
 def bf16_round(x: float, lib=None) -> int:
     return int((lib or load()).oracle_bf16_round(float(x)))
+
+
+def bf16_round_array(x, lib=None) -> np.ndarray:
+    """bf16 bits of every binary64 value in x (bf16_round, elementwise)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    (lib or load()).oracle_bf16_round_array(_ptr(x, ctypes.c_double), _ptr(out), x.size)
+    return out
 
 
 def bf16_to_float(bits: int, lib=None) -> float:

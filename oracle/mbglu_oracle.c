@@ -112,6 +112,12 @@ uint16_t oracle_bf16_round(double x)
     return (uint16_t)(sign | bits);
 }
 
+/* oracle_bf16_round over an array: out[i] = oracle_bf16_round(x[i]). */
+void oracle_bf16_round_array(const double *x, uint16_t *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_round(x[i]);
+}
+
 /* ------------------------------------------------------------------------ */
 /* SiLU                                                                      */
 /* ------------------------------------------------------------------------ */

@@ -218,3 +218,46 @@ def norm_rounding_slack(s_bits, norm_w_bits, eps, gate_bits, up_bits):
     dG = slack @ np.abs(bf16_bits_to_f64(gate_bits)).T
     dU = slack @ np.abs(bf16_bits_to_f64(up_bits)).T
     return dG, dU
+
+
+# ---------------------------------------------------------------------------
+# the backward (glu_backward)
+# ---------------------------------------------------------------------------
+#
+# Each gradient is an fp32 sum rounded once to bf16, and the same bar
+# applies: 1 ULP of the oracle on >= 99.9%, relative error <= 1e-2
+# elsewhere, floored at what fp32 alone can move the output.  The floors:
+#   * g, u carry the forward's accumulation error eg = gamma*Ag, eu = gamma*Au
+#     (tensor-core bound, the looser of the two kernels');
+#   * dG = d*u*SiLU'(g) moves by |d|*(|SiLU'(G)|*eu + |U|*max|SiLU''|*eg)
+#     with max|SiLU''| = 1/2 (at 0), plus its own fp32 evaluation, bounded
+#     by 16 * 2^-24 relative (expf, two divisions, three products);
+#     dU = d*SiLU(g) by |d|*max|SiLU'|*eg (max|SiLU'| < 1.1) plus the same;
+#   * grad_h = sum over 2N products (any order: depth <= 2N + 64), grad_W
+#     = sum over M products (depth M + 1), each with the dG, dU error above
+#     carried through |W| or |h|.
+
+BWD_EVAL_REL = 16 * 2.0 ** -24
+SILU_D1_MAX = 1.1
+SILU_D2_MAX = 0.5
+
+
+def backward_floors(h, gate, up, dout, G, U, Ag, Au, K):
+    """(tau_h [M,K], tau_gate [N,K], tau_up [N,K]) from fp64 operands (h, gate,
+    up, dout as values) and the forward's diagnostics G, U, Ag, Au [M,N]."""
+    gamma = accumulation_gamma(K, {"acc": "mma"})
+    eg, eu = gamma * Ag, gamma * Au
+    ad = np.abs(dout)
+    ds = _dsilu(G)
+    dG = dout * U * ds
+    dU = dout * _silu(G)
+    edG = ad * (np.abs(ds) * eu + np.abs(U) * SILU_D2_MAX * eg) + BWD_EVAL_REL * np.abs(dG)
+    edU = ad * SILU_D1_MAX * eg + BWD_EVAL_REL * np.abs(dU)
+    M, N = G.shape
+    ag, au, ah = np.abs(gate), np.abs(up), np.abs(h)
+    g2n = (2 * N + 64) * 2.0 ** -24
+    tau_h = edG @ ag + edU @ au + g2n * (np.abs(dG) @ ag + np.abs(dU) @ au)
+    gm = (M + 1) * 2.0 ** -24
+    tau_gate = edG.T @ ah + gm * (np.abs(dG).T @ ah)
+    tau_up = edU.T @ ah + gm * (np.abs(dU).T @ ah)
+    return tau_h, tau_gate, tau_up
