@@ -124,6 +124,47 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh,
                       cudaStream_t stream);
 
 /*
+ * glu_backward -- the gradients of glu_gemv's exact composite
+ * out = SiLU(h gate_w^T) * (h up_w^T) for an upstream gradient dout.
+ * [8602/PlanB] "Plan B Design": an autograd.Function reading the original
+ * Parameters, so that gradients flow to gate.weight and up.weight (the
+ * "Verification Results" compare them with the composite's).  In fp32 from
+ * the bf16 operands:
+ *   g, u     = the forward's dot products (fp32 accumulation)
+ *   dG       = dout * u * SiLU'(g),  dU = dout * SiLU(g)        [M, N] fp32
+ *   grad_h    = dG gate_w + dU up_w                              [M, K]
+ *   grad_gate = dG^T h,  grad_up = dU^T h                        [N, K]
+ * each gradient rounded once to bf16.  The HF mode's roundings have no
+ * gradient of their own (casts pass gradients through), so this is the
+ * backward of both modes.
+ *   h, gate_w, up_w  as glu_gemv                              (read)
+ *   dout     [M, N] bf16, row stride ldd >= N                 (read)
+ *   grad_h   [M, K] bf16, row stride ldgh >= K, or NULL to skip it
+ *   grad_gate, grad_up  [N, K] bf16, row strides ldgg, ldgu >= K; both
+ *            NULL to skip them, or both given
+ *   workspace  device memory of glu_backward_workspace_bytes(M, N, K)
+ *            bytes, 16-byte aligned, owned by the caller; its contents are
+ *            undefined afterwards
+ *   0 <= M <= MBGLU_BLOCK_M, N >= 0, K >= 0.  K == 0: no-op.  M == 0 or
+ *   N == 0: the gradients that remain are written as zeros (no workspace
+ *   needed).
+ * Outputs must not overlap the inputs, one another or the workspace
+ * (MBGLU_ERR_ALIAS).  Asynchronous on `stream`; no allocation; the sums run
+ * in a fixed order, so results are bitwise deterministic.
+ */
+size_t glu_backward_workspace_bytes(int M, int N, int K);
+mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh,
+                          const mbglu_bf16 *gate_w, int64_t ld_gate,
+                          const mbglu_bf16 *up_w, int64_t ld_up,
+                          const mbglu_bf16 *dout, int64_t ldd,
+                          mbglu_bf16 *grad_h, int64_t ldgh,
+                          mbglu_bf16 *grad_gate, int64_t ldgg,
+                          mbglu_bf16 *grad_up, int64_t ldgu,
+                          int M, int N, int K,
+                          void *workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+/*
  * add_rmsnorm_glu -- residual add + zero-centred RMSNorm, then glu_gemv on
  * the normed rows.  [9057/Changes] "Restore HF's intermediate BF16 rounding in
  * residual/RMSNorm ... construct zero-centered norm scales in FP32".
@@ -334,7 +375,7 @@ int mbglu_last_cuda_error(void);
  * 0 none (no-op), 1 streaming kernel (CUDA-core FMA), 2 generic kernel,
  * 3 zero fill, 4 tensor-core streaming kernel (batch >= 3), 5 silu_mul,
  * 6 gdn_gates, 7 row blocks (a batch above MBGLU_BLOCK_M: one of 1-4 per
- * block). */
+ * block), 8 glu_backward. */
 int mbglu_last_variant(void);
 
 /*

@@ -24,7 +24,7 @@ WORKSPACE_BYTES = 256
 
 # Every symbol include/mbglu.h declares.
 EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu_strided", "add_rmsnorm_glu_noalloc",
-           "silu_mul", "gdn_gates",
+           "silu_mul", "gdn_gates", "glu_backward", "glu_backward_workspace_bytes",
            "mbglu_set_launch_policy",
            "mbglu_get_launch_policy",
            "mbglu_status_string", "mbglu_abi_version", "mbglu_last_cuda_error", "mbglu_last_variant",
@@ -59,6 +59,11 @@ def _bind(l):
     l.silu_mul.argtypes = [vp, i64, vp, i64, i32, i32, i32, vp]
     l.gdn_gates.argtypes = [vp, i64, vp, i64, vp, vp, vp, i64, vp, i64, i32, i32, vp]
     l.gdn_gates.restype = i32
+    l.glu_backward_workspace_bytes.argtypes = [i32, i32, i32]
+    l.glu_backward_workspace_bytes.restype = ctypes.c_size_t
+    l.glu_backward.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32, i32, i32,
+                               vp, ctypes.c_size_t, vp]
+    l.glu_backward.restype = i32
     l.silu_mul.restype = i32
     l.mbglu_status_string.argtypes = [i32]
     l.mbglu_status_string.restype = ctypes.c_char_p
@@ -134,6 +139,81 @@ def glu_gemv(h, gate_w, up_w, out=None, mode="fused", stream=None):
     if st != 0:
         raise MbgluError(st, "glu_gemv")
     return out2.view(N) if squeeze else out
+
+
+def glu_backward(h, gate_w, up_w, dout, grad_h=None, grad_gate=None, grad_up=None, want_h=True, want_w=True,
+                 workspace=None, stream=None):
+    """Gradients of glu_gemv's SiLU(h @ gate_w.T) * (h @ up_w.T) for an
+    upstream dout [M,N] (bf16): returns (grad_h [M,K], grad_gate [N,K],
+    grad_up [N,K]), bf16, each None where not wanted.  Output tensors may be
+    passed in (any row stride, contiguous last dimension); the workspace is a
+    byte tensor of glu_backward_workspace_bytes(M, N, K), allocated here by
+    torch's allocator when not given."""
+    _check(h, "h", 2)
+    _check(gate_w, "gate_w", 2)
+    _check(up_w, "up_w", 2)
+    _check(dout, "dout", 2)
+    M, K = h.shape
+    N = gate_w.shape[0]
+    if tuple(gate_w.shape) != (N, K) or tuple(up_w.shape) != (N, K) or tuple(dout.shape) != (M, N):
+        raise ValueError(f"expected gate_w, up_w [{N},{K}] and dout [{M},{N}]")
+    dev = h.device
+    if want_h and grad_h is None:
+        grad_h = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    if want_w and grad_gate is None:
+        grad_gate = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    if want_w and grad_up is None:
+        grad_up = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+    if not want_h:
+        grad_h = None
+    if not want_w:
+        grad_gate = grad_up = None
+    for t, name, shape in ((grad_h, "grad_h", (M, K)), (grad_gate, "grad_gate", (N, K)), (grad_up, "grad_up", (N, K))):
+        if t is not None:
+            _check(t, name, 2)
+            if tuple(t.shape) != shape or t.device != dev:
+                raise ValueError(f"{name} must be {list(shape)} on {dev}")
+    need = lib().glu_backward_workspace_bytes(M, N, K)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wsp = workspace.data_ptr() if workspace is not None else None
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+
+    def ptr(t):
+        return (t.data_ptr(), t.stride(0)) if t is not None else (None, 0)
+
+    with torch.cuda.device(dev):
+        st = lib().glu_backward(h.data_ptr(), h.stride(0), gate_w.data_ptr(), gate_w.stride(0), up_w.data_ptr(),
+                                up_w.stride(0), dout.data_ptr(), dout.stride(0), *ptr(grad_h), *ptr(grad_gate),
+                                *ptr(grad_up), M, N, K, wsp, wsb, _stream_handle(dev, stream))
+    if st != 0:
+        raise MbgluError(st, "glu_backward")
+    return grad_h, grad_gate, grad_up
+
+
+class DualWeightGlu(torch.autograd.Function):
+    """out = SiLU(h @ gate_w.T) * (h @ up_w.T) with the weights read in place
+    and gradients for h, gate_w and up_w ([8602/PlanB] "Plan B Design": the
+    autograd.Function reads the original Parameters, so gradients flow)."""
+
+    @staticmethod
+    def forward(ctx, h, gate_w, up_w, mode="fused"):
+        ctx.save_for_backward(h, gate_w, up_w)
+        return glu_gemv(h, gate_w, up_w, mode=mode)
+
+    @staticmethod
+    def backward(ctx, dout):
+        h, gate_w, up_w = ctx.saved_tensors
+        squeeze = h.dim() == 1
+        h2 = h.unsqueeze(0) if squeeze else h
+        d2 = dout.reshape(h2.shape[0], -1).to(torch.bfloat16)
+        if d2.stride(-1) != 1:
+            d2 = d2.contiguous()
+        gh, gg, gu = glu_backward(h2, gate_w, up_w, d2, want_h=ctx.needs_input_grad[0],
+                                  want_w=ctx.needs_input_grad[1] or ctx.needs_input_grad[2])
+        if gh is not None and squeeze:
+            gh = gh.view(-1)
+        return gh, gg if ctx.needs_input_grad[1] else None, gu if ctx.needs_input_grad[2] else None, None
 
 
 def new_workspace(device=None):

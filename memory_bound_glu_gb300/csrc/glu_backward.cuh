@@ -1,0 +1,233 @@
+// glu_backward.cuh -- the backward of the dual-weight GLU GEMV.
+//
+// DeepSpeed PR #8602, comment "Plan B: Dual-Weight GEMV -- Investigation
+// Results & Implementation", section "Plan B Design: kernel adapts to the
+// weights": an autograd.Function that reads the original Parameters, so that
+// gradients reach gate.weight and up.weight; "Verification Results" checks
+// them against the composite.  For out = SiLU(g) * u with g = h Wg^T and
+// u = h Wu^T, and an upstream gradient dout:
+//
+//   dG = dout * u * SiLU'(g)        dU = dout * SiLU(g)            [M][N]
+//   grad_h    = dG Wg + dU Wu                                      [M][K]
+//   grad_gate = dG^T h,  grad_up = dU^T h                          [N][K]
+//
+// Three steps, each streaming about one weight-sized volume of HBM:
+//   1. the forward kernels with the backward epilogue (glu_store with
+//      kModeBwd) recompute g and u and write dG, dU in fp32;
+//   2. glu_bwd_h_kernel: CTA (column block, row split) sums its rows of both
+//      weights, times dG and dU, over 512 columns into an fp32 partial;
+//      glu_bwd_h_reduce_kernel adds the partials in split order and rounds;
+//   3. glu_bwd_w_kernel: the outer products, written once as bf16 (h in
+//      shared memory where it fits).
+// Every sum runs in a fixed order: results are bitwise deterministic.
+#pragma once
+
+#include "glu_kernels.cuh"
+
+namespace mbglu {
+
+struct BwdParams {
+    const uint16_t *h;
+    int64_t ldh;
+    const uint16_t *gate;
+    int64_t ld_gate;
+    const uint16_t *up;
+    int64_t ld_up;
+    const float *dG, *dU;   // [M][N], row stride N
+    float *part;            // grad_h partials [nsplit][M][K]
+    uint16_t *grad_h;
+    int64_t ldgh;
+    uint16_t *grad_gate;
+    int64_t ldgg;
+    uint16_t *grad_up;
+    int64_t ldgu;
+    int M, N, K;
+    int vec_w;              // gate, up rows 8-byte aligned: 4-element loads
+    int vec_out;            // grad_gate, grad_up rows and h 16-byte aligned, K % 8 == 0: 8-element access
+    int h_smem;             // glu_bwd_w_kernel: h staged in shared memory
+};
+
+constexpr int kBwdCols = 512;        // glu_bwd_h_kernel: columns per CTA, 4 per thread
+constexpr int kBwdRowChunk = 256;    // glu_bwd_h_kernel: rows of dG, dU staged at a time
+constexpr int kBwdMaxSplits = 48;    // glu_bwd_h_kernel: row splits of N (partials in the workspace)
+
+// 4 consecutive bf16 of a weight row as fp32 (zeros past the row's end)
+__device__ __forceinline__ void load4_bf16(const uint16_t *ptr, bool vec, int left, float (&v)[4])
+{
+    if (vec) {
+        const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(ptr));
+        v[0] = bf16_lo(w.x);
+        v[1] = bf16_hi(w.x);
+        v[2] = bf16_lo(w.y);
+        v[3] = bf16_hi(w.y);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = i < left ? bf16_to_f32(ptr[i]) : 0.0f;
+    }
+}
+
+// grad_h partials.  blockIdx.x: 512 columns, 4 per thread (threads 0..127
+// take rows n0, n0+2, ..., threads 128..255 rows n0+1, n0+3, ...);
+// blockIdx.y: rows [n0, n1) of N.  part[y][m][k] = the two halves' sums of
+// dG[m][n] Wg[n][k] + dU[m][n] Wu[n][k], added half 0 + half 1.
+template <int MB>
+__global__ void __launch_bounds__(256) glu_bwd_h_kernel(const BwdParams q)
+{
+    extern __shared__ __align__(16) float bwd_s[];   // [2][M][kBwdRowChunk]; then [MB * 4][128]
+    const int nb = blockIdx.y, nsplit = gridDim.y;
+    const int n0 = static_cast<int>((static_cast<int64_t>(q.N) * nb) / nsplit);
+    const int n1 = static_cast<int>((static_cast<int64_t>(q.N) * (nb + 1)) / nsplit);
+    const int c = threadIdx.x & 127, half = threadIdx.x >> 7;
+    const int k = blockIdx.x * kBwdCols + 4 * c;
+    const bool vec = q.vec_w && k + 4 <= q.K;
+    float *dg_s = bwd_s, *du_s = bwd_s + q.M * kBwdRowChunk;
+
+    float acc[MB][4];
+#pragma unroll
+    for (int m = 0; m < MB; ++m)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[m][i] = 0.0f;
+
+    for (int c0 = n0; c0 < n1; c0 += kBwdRowChunk) {
+        const int rows = min(kBwdRowChunk, n1 - c0);
+        __syncthreads();   // the previous chunk's reads are done
+        for (int i = threadIdx.x; i < q.M * rows; i += blockDim.x) {
+            const int m = i / rows, j = i - m * rows;
+            dg_s[m * kBwdRowChunk + j] = q.dG[static_cast<int64_t>(m) * q.N + c0 + j];
+            du_s[m * kBwdRowChunk + j] = q.dU[static_cast<int64_t>(m) * q.N + c0 + j];
+        }
+        __syncthreads();
+        if (k < q.K) {
+#pragma unroll 4
+            for (int j = half; j < rows; j += 2) {
+                const int64_t n = c0 + j;
+                float wg[4], wu[4];
+                load4_bf16(q.gate + n * q.ld_gate + k, vec, q.K - k, wg);
+                load4_bf16(q.up + n * q.ld_up + k, vec, q.K - k, wu);
+#pragma unroll
+                for (int m = 0; m < MB; ++m) {
+                    if (m < q.M) {
+                        const float a = dg_s[m * kBwdRowChunk + j], b = du_s[m * kBwdRowChunk + j];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[m][i] = fmaf(b, wu[i], fmaf(a, wg[i], acc[m][i]));
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();   // dG, dU no longer read: the same shared memory combines the halves
+    float *red = bwd_s;
+    if (half == 1) {
+#pragma unroll
+        for (int m = 0; m < MB; ++m)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red[(m * 4 + i) * 128 + c] = acc[m][i];
+    }
+    __syncthreads();
+    if (half == 0 && k < q.K) {
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            if (m < q.M) {
+                float *dst = q.part + (static_cast<int64_t>(nb) * q.M + m) * q.K + k;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (k + i < q.K) dst[i] = acc[m][i] + red[(m * 4 + i) * 128 + c];
+            }
+        }
+    }
+}
+
+// grad_h[m][k] = bf16( part[0][m][k] + part[1][m][k] + ... ), splits in order
+__global__ void __launch_bounds__(256) glu_bwd_h_reduce_kernel(const BwdParams q, int nsplit)
+{
+    const int64_t total = static_cast<int64_t>(q.M) * q.K;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t m = i / q.K, k = i - m * q.K;
+        float s = q.part[i];
+        for (int b = 1; b < nsplit; ++b) s += q.part[static_cast<int64_t>(b) * total + i];
+        q.grad_h[m * q.ldgh + k] = f32_to_bf16(s);
+    }
+}
+
+// 8 consecutive bf16 as fp32 (zeros past `left`)
+__device__ __forceinline__ void load8_bf16(const uint16_t *ptr, bool vec, int left, float (&v)[8])
+{
+    if (vec) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(ptr);
+        v[0] = bf16_lo(w.x);
+        v[1] = bf16_hi(w.x);
+        v[2] = bf16_lo(w.y);
+        v[3] = bf16_hi(w.y);
+        v[4] = bf16_lo(w.z);
+        v[5] = bf16_hi(w.z);
+        v[6] = bf16_lo(w.w);
+        v[7] = bf16_hi(w.w);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = i < left ? bf16_to_f32(ptr[i]) : 0.0f;
+    }
+}
+
+__device__ __forceinline__ void store8_bf16(uint16_t *ptr, bool vec, int left, const float (&v)[8])
+{
+    if (vec) {
+        __stcs(reinterpret_cast<uint4 *>(ptr), make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                          pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7])));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < left) ptr[i] = f32_to_bf16(v[i]);
+    }
+}
+
+// grad_gate[n][k] = bf16( sum_m dG[m][n] h[m][k] ), grad_up likewise with dU;
+// the m-sum in order m = 0, 1, ... .  Rows n are dealt over the CTAs, 8
+// columns per thread.
+template <int MB>
+__global__ void __launch_bounds__(256) glu_bwd_w_kernel(const BwdParams q)
+{
+    extern __shared__ __align__(16) uint16_t hw_s[];   // h [M][K], row stride K (h_smem)
+    const uint16_t *hb = q.h;
+    int64_t hld = q.ldh;
+    if (q.h_smem) {
+        const int64_t total = static_cast<int64_t>(q.M) * q.K;
+        for (int64_t i = threadIdx.x; i < total; i += blockDim.x) {
+            const int64_t m = i / q.K, k = i - m * q.K;
+            hw_s[i] = q.h[m * q.ldh + k];
+        }
+        __syncthreads();
+        hb = hw_s;
+        hld = q.K;
+    }
+    for (int64_t n = blockIdx.x; n < q.N; n += gridDim.x) {
+        float a[MB], b[MB];
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            a[m] = m < q.M ? q.dG[static_cast<int64_t>(m) * q.N + n] : 0.0f;
+            b[m] = m < q.M ? q.dU[static_cast<int64_t>(m) * q.N + n] : 0.0f;
+        }
+        for (int k = 8 * threadIdx.x; k < q.K; k += 8 * blockDim.x) {
+            const bool vec = q.vec_out && k + 8 <= q.K;
+            float sg[8], su[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sg[i] = su[i] = 0.0f;
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                if (m < q.M) {
+                    float hv[8];
+                    load8_bf16(hb + m * hld + k, vec, q.K - k, hv);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        sg[i] = fmaf(a[m], hv[i], sg[i]);
+                        su[i] = fmaf(b[m], hv[i], su[i]);
+                    }
+                }
+            }
+            store8_bf16(q.grad_gate + n * q.ldgg + k, vec, q.K - k, sg);
+            store8_bf16(q.grad_up + n * q.ldgu + k, vec, q.K - k, su);
+        }
+    }
+}
+
+}  // namespace mbglu

@@ -77,7 +77,14 @@ struct GluParams {
     int *ws;                 // arrival counters, 0 between calls
     uint32_t off_s;
     int helper_warp;         // single-kernel path: the extra warp that writes the residual slice (-1: none)
+    // backward (mode == kModeBwd): the epilogue reads dout and writes the
+    // fp32 gradients of g and u, [M][N] with row stride N, instead of out
+    const uint16_t *dout;
+    int64_t ldd;
+    float *dG, *dU;
 };
+
+constexpr int kModeBwd = 2;   // internal mode of the forward kernels: the backward's dG, dU epilogue
 
 // ---------------------------------------------------------------------------
 // scalar helpers
@@ -114,6 +121,34 @@ __device__ __forceinline__ uint16_t glu_epilogue(float g, float u, int mode)
     const float ub = round_to_bf16(u);
     const float sb = round_to_bf16(silu_f32(gb));
     return f32_to_bf16(sb * ub);
+}
+
+// SiLU(x) and SiLU'(x) = sigma(x) * (1 + x * (1 - sigma(x))), from t = e^-|x|
+// so that nothing overflows: sigma = 1/(1+t), 1 - sigma = t/(1+t) for x >= 0,
+// and the two swapped below.  Precise expf and IEEE division.
+__device__ __forceinline__ void silu_and_derivative(float x, float &silu, float &dsilu)
+{
+    const float t = expf(-fabsf(x));
+    const float sig = (x >= 0.0f ? 1.0f : t) / (1.0f + t);
+    const float rest = (x >= 0.0f ? t : 1.0f) / (1.0f + t);   // 1 - sigma
+    silu = x * sig;
+    dsilu = sig * (1.0f + x * rest);
+}
+
+// The store of one output of the GEMV kernels.  Forward modes: out = the GLU
+// epilogue.  kModeBwd ([8602/PlanB] autograd wrapper: the gradients of
+// SiLU(g) * u): dG = dout * u * SiLU'(g), dU = dout * SiLU(g), in fp32.
+__device__ __forceinline__ void glu_store(const GluParams &p, int m, int64_t n, float g, float u)
+{
+    if (p.mode == kModeBwd) {
+        const float d = bf16_to_f32(p.dout[m * p.ldd + n]);
+        float sl, ds;
+        silu_and_derivative(g, sl, ds);
+        p.dG[static_cast<int64_t>(m) * p.N + n] = (d * u) * ds;
+        p.dU[static_cast<int64_t>(m) * p.N + n] = d * sl;
+    } else {
+        p.out[m * p.ldo + n] = glu_epilogue(g, u, p.mode);
+    }
 }
 
 __device__ __forceinline__ float warp_allsum(float v)
@@ -816,7 +851,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
                 }
             const int r = lane / MB, m = lane - (lane / MB) * MB;
             if (lane < R * MB && m < p.M && row0 + r < r1)
-                p.out[m * p.ldo + row0 + r] = glu_epilogue(gsel, usel, p.mode);
+                glu_store(p, m, row0 + r, gsel, usel);
         }
     }
 }
@@ -1237,7 +1272,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
             for (int q = 0; q < 4; ++q) {
                 const int m = m0 + (q >> 1) * 8, nn = n + (q & 1);
                 if (m < p.M && nn < r1 && nn < row0 + R)
-                    p.out[m * p.ldo + nn] = glu_epilogue(g0[q] + g1[q], v0[q] + v1[q], p.mode);
+                    glu_store(p, m, nn, g0[q] + g1[q], v0[q] + v1[q]);
                 g0[q] = g1[q] = v0[q] = v1[q] = 0.f;
             }
         }
@@ -1306,7 +1341,7 @@ __global__ void __launch_bounds__(256) glu_generic_kernel(const GluParams p)
             }
             g = warp_allsum(g);
             u = warp_allsum(u);
-            if (lane == 0) p.out[m * p.ldo + row] = glu_epilogue(g, u, p.mode);
+            if (lane == 0) glu_store(p, m, row, g, u);
         }
     }
 }

@@ -18,6 +18,7 @@
 
 #include "mbglu.h"
 #include "glu_kernels.cuh"
+#include "glu_backward.cuh"
 
 namespace {
 
@@ -28,7 +29,8 @@ thread_local int t_last_variant = 0;
 
 enum Variant {
     kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4, kSiluMul = 5, kGdnGates = 6,
-    kRowBlocks = 7   // a batch above kBlockRows, run as row blocks
+    kRowBlocks = 7,  // a batch above kBlockRows, run as row blocks
+    kBackward = 8    // glu_backward
 };
 constexpr int kBlockRows = mbglu::kMaxM;   // rows one GEMV kernel takes (its batch tile)
 
@@ -159,6 +161,24 @@ cudaError_t allow_smem_generic(int optin)
                                 optin - static_cast<int>(a.sharedSizeBytes));
 }
 
+constexpr int kBwdHSmemMax = 96 * 1024;   // glu_bwd_w_kernel: h in shared memory up to this (two CTAs per SM)
+
+cudaError_t allow_smem_bwd()
+{
+    cudaError_t e = cudaSuccess;
+#define MBGLU_ALLOW_BWD(MB)                                                                                  \
+    if (e == cudaSuccess)                                                                                    \
+        e = cudaFuncSetAttribute(mbglu::glu_bwd_w_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 kBwdHSmemMax);
+    MBGLU_ALLOW_BWD(1)
+    MBGLU_ALLOW_BWD(2)
+    MBGLU_ALLOW_BWD(4)
+    MBGLU_ALLOW_BWD(8)
+    MBGLU_ALLOW_BWD(16)
+#undef MBGLU_ALLOW_BWD
+    return e;
+}
+
 mbglu_status device_info(const DeviceInfo **out)
 {
     int dev = 0;
@@ -174,7 +194,8 @@ mbglu_status device_info(const DeviceInfo **out)
             cudaSuccess)
             return cuda_fail(e);
         const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_mma<false>(d.smem_optin),
-                                    allow_smem_mma<true>(d.smem_optin), allow_smem_generic(d.smem_optin)};
+                                    allow_smem_mma<true>(d.smem_optin), allow_smem_generic(d.smem_optin),
+                                    allow_smem_bwd()};
         for (cudaError_t x : errs)
             if (x != cudaSuccess) return cuda_fail(x);
         d.ready = true;
@@ -651,10 +672,19 @@ mbglu_status check_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate
     return MBGLU_OK;
 }
 
+// The backward's first step: the GEMV kernels' epilogue writes dG, dU
+// (fp32 [M][N]) from dout instead of out.
+struct BwdEpilogue {
+    const mbglu_bf16 *dout;
+    int64_t ldd;
+    float *dG, *dU;
+};
+
 // The GEMV on 1 <= M <= kBlockRows rows, N >= 1, arguments already checked.
+// bwd != nullptr: K >= 1, and the epilogue is the backward's (out unused).
 mbglu_status gemv_block(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
                         const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
-                        mbglu_mode mode, cudaStream_t stream)
+                        mbglu_mode mode, cudaStream_t stream, const BwdEpilogue *bwd = nullptr)
 {
     const DeviceInfo *d = nullptr;
     mbglu_status st = device_info(&d);
@@ -666,6 +696,13 @@ mbglu_status gemv_block(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate
     p.prefetch = policy == MBGLU_POLICY_PREFETCH;
     p.out = out;
     p.ldo = ldo;
+    if (bwd) {
+        p.mode = mbglu::kModeBwd;
+        p.dout = bwd->dout;
+        p.ldd = bwd->ldd;
+        p.dG = bwd->dG;
+        p.dU = bwd->dU;
+    }
     if (K == 0) {
         const int grid = std::max(1, std::min(d->sm_count, static_cast<int>((static_cast<int64_t>(M) * N + 255) / 256)));
         cudaLaunchConfig_t cfg = {};
@@ -755,6 +792,153 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
         }
     }
     t_last_variant = kRowBlocks;
+    return MBGLU_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+int bwd_splits(int N) { return std::max(1, std::min(mbglu::kBwdMaxSplits, N / 256)); }
+
+int64_t round256(int64_t b) { return (b + 255) & ~static_cast<int64_t>(255); }
+
+mbglu_status launch_plain(cudaError_t e)
+{
+    return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t glu_backward_workspace_bytes(int M, int N, int K)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || M > kBlockRows) return 0;
+    return static_cast<size_t>(round256(2 * static_cast<int64_t>(M) * N * 4) +
+                               round256(static_cast<int64_t>(bwd_splits(N)) * M * K * 4));
+}
+
+mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
+                          const mbglu_bf16 *up_w, int64_t ld_up, const mbglu_bf16 *dout, int64_t ldd,
+                          mbglu_bf16 *grad_h, int64_t ldgh, mbglu_bf16 *grad_gate, int64_t ldgg,
+                          mbglu_bf16 *grad_up, int64_t ldgu, int M, int N, int K, void *workspace,
+                          size_t workspace_bytes, cudaStream_t stream)
+{
+    t_last_variant = kNone;
+    if (M < 0 || N < 0 || K < 0 || M > kBlockRows) return MBGLU_ERR_SHAPE;
+    const bool want_h = grad_h != nullptr, want_w = grad_gate != nullptr || grad_up != nullptr;
+    if (want_w && (!grad_gate || !grad_up)) return MBGLU_ERR_NULL;
+    if (K == 0) return MBGLU_OK;   // every gradient has K columns
+    // shapes where one factor is empty: the gradients that remain are sums of nothing
+    const bool full = M > 0 && N > 0;
+    if (full && (!h || !gate_w || !up_w || !dout || !workspace)) return MBGLU_ERR_NULL;
+    if ((M > 0 && want_h && ldgh < K) || (N > 0 && want_w && (ldgg < K || ldgu < K))) return MBGLU_ERR_STRIDE;
+    if (full && (ldh < K || ld_gate < K || ld_up < K || ldd < N)) return MBGLU_ERR_STRIDE;
+    if (!aligned(h, 2) || !aligned(gate_w, 2) || !aligned(up_w, 2) || !aligned(dout, 2) || !aligned(grad_h, 2) ||
+        !aligned(grad_gate, 2) || !aligned(grad_up, 2) || !aligned(workspace, 16))
+        return MBGLU_ERR_ALIGN;
+    const size_t need = glu_backward_workspace_bytes(M, N, K);
+    if (full && workspace_bytes < need) return MBGLU_ERR_SHAPE;
+    // outputs against inputs and one another
+    const int64_t hb = matrix_bytes(M, K, ldh), gb = matrix_bytes(N, K, ld_gate), ub = matrix_bytes(N, K, ld_up);
+    const int64_t db = matrix_bytes(M, N, ldd);
+    const int64_t ghb = want_h ? matrix_bytes(M, K, ldgh) : 0;
+    const int64_t ggb = want_w ? matrix_bytes(N, K, ldgg) : 0, gub = want_w ? matrix_bytes(N, K, ldgu) : 0;
+    const int64_t wsb = full ? static_cast<int64_t>(need) : 0;
+    const void *ins[4] = {h, gate_w, up_w, dout};
+    const int64_t inb[4] = {full ? hb : 0, full ? gb : 0, full ? ub : 0, full ? db : 0};
+    const void *outs[4] = {grad_h, grad_gate, grad_up, workspace};
+    const int64_t outb[4] = {ghb, ggb, gub, wsb};
+    for (int i = 0; i < 4; ++i) {
+        for (int j = 0; j < 4; ++j)
+            if (overlaps(outs[i], outb[i], ins[j], inb[j])) return MBGLU_ERR_ALIAS;
+        for (int j = i + 1; j < 4; ++j)
+            if (overlaps(outs[i], outb[i], outs[j], outb[j])) return MBGLU_ERR_ALIAS;
+    }
+    if (M == 0 && N == 0) return MBGLU_OK;
+    if (!full) {   // N == 0: grad_h = 0; M == 0: grad_gate = grad_up = 0
+        cudaError_t e = cudaSuccess;
+        if (N == 0 && want_h)
+            e = cudaMemset2DAsync(grad_h, static_cast<size_t>(ldgh) * 2, 0, static_cast<size_t>(K) * 2, M, stream);
+        if (e == cudaSuccess && M == 0 && want_w) {
+            e = cudaMemset2DAsync(grad_gate, static_cast<size_t>(ldgg) * 2, 0, static_cast<size_t>(K) * 2, N, stream);
+            if (e == cudaSuccess)
+                e = cudaMemset2DAsync(grad_up, static_cast<size_t>(ldgu) * 2, 0, static_cast<size_t>(K) * 2, N, stream);
+        }
+        return launch_plain(e);
+    }
+
+    const DeviceInfo *d = nullptr;
+    mbglu_status st = device_info(&d);
+    if (st != MBGLU_OK) return st;
+    float *dG = static_cast<float *>(workspace);
+    float *dU = dG + static_cast<int64_t>(M) * N;
+    float *part = reinterpret_cast<float *>(static_cast<char *>(workspace) + round256(2 * static_cast<int64_t>(M) * N * 4));
+
+    // 1) dG, dU: the forward kernels with the backward epilogue
+    const BwdEpilogue be = {dout, ldd, dG, dU};
+    st = gemv_block(h, ldh, gate_w, ld_gate, up_w, ld_up, nullptr, 0, M, N, K, MBGLU_MODE_FUSED, stream, &be);
+    if (st != MBGLU_OK) return st;
+
+    mbglu::BwdParams q = {};
+    q.h = h;
+    q.ldh = ldh;
+    q.gate = gate_w;
+    q.ld_gate = ld_gate;
+    q.up = up_w;
+    q.ld_up = ld_up;
+    q.dG = dG;
+    q.dU = dU;
+    q.part = part;
+    q.grad_h = grad_h;
+    q.ldgh = ldgh;
+    q.grad_gate = grad_gate;
+    q.ldgg = ldgg;
+    q.grad_up = grad_up;
+    q.ldgu = ldgu;
+    q.M = M;
+    q.N = N;
+    q.K = K;
+    q.vec_w = aligned(gate_w, 8) && aligned(up_w, 8) && ld_gate % 4 == 0 && ld_up % 4 == 0;
+    const int MB = batch_tile(M);
+    cudaError_t e = cudaSuccess;
+    // 2) grad_h: partials over row splits, then their sum in split order
+    if (want_h) {
+        const int nsplit = bwd_splits(N);
+        const dim3 grid((K + mbglu::kBwdCols - 1) / mbglu::kBwdCols, nsplit);
+        const size_t smem = static_cast<size_t>(std::max(2 * M * mbglu::kBwdRowChunk, MB * 4 * 128)) * 4;
+        switch (MB) {
+            case 1: mbglu::glu_bwd_h_kernel<1><<<grid, 256, smem, stream>>>(q); break;
+            case 2: mbglu::glu_bwd_h_kernel<2><<<grid, 256, smem, stream>>>(q); break;
+            case 4: mbglu::glu_bwd_h_kernel<4><<<grid, 256, smem, stream>>>(q); break;
+            case 8: mbglu::glu_bwd_h_kernel<8><<<grid, 256, smem, stream>>>(q); break;
+            default: mbglu::glu_bwd_h_kernel<16><<<grid, 256, smem, stream>>>(q); break;
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+        const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(d->sm_count * 4,
+                                                                                   (static_cast<int64_t>(M) * K + 255) / 256)));
+        mbglu::glu_bwd_h_reduce_kernel<<<rgrid, 256, 0, stream>>>(q, nsplit);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    }
+    // 3) grad_gate, grad_up: the outer products, h in shared memory where it fits
+    if (want_w) {
+        const int64_t hbytes = static_cast<int64_t>(M) * K * 2;
+        q.h_smem = hbytes <= kBwdHSmemMax;
+        q.vec_out = K % 8 == 0 && aligned(grad_gate, 16) && aligned(grad_up, 16) && ldgg % 8 == 0 && ldgu % 8 == 0 &&
+                    (q.h_smem || (aligned(h, 16) && ldh % 8 == 0));
+        const size_t smem = q.h_smem ? static_cast<size_t>(hbytes) : 0;
+        const int wgrid = std::max(1, std::min(N, d->sm_count * 2));
+        switch (MB) {
+            case 1: mbglu::glu_bwd_w_kernel<1><<<wgrid, 256, smem, stream>>>(q); break;
+            case 2: mbglu::glu_bwd_w_kernel<2><<<wgrid, 256, smem, stream>>>(q); break;
+            case 4: mbglu::glu_bwd_w_kernel<4><<<wgrid, 256, smem, stream>>>(q); break;
+            case 8: mbglu::glu_bwd_w_kernel<8><<<wgrid, 256, smem, stream>>>(q); break;
+            default: mbglu::glu_bwd_w_kernel<16><<<wgrid, 256, smem, stream>>>(q); break;
+        }
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+    }
+    t_last_variant = kBackward;
     return MBGLU_OK;
 }
 

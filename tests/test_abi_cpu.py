@@ -193,3 +193,37 @@ def norm_ws(ws=WS, nbytes=256, **kw):
 ])
 def test_add_rmsnorm_glu_ws_validation(kw, code):
     assert norm_ws(**kw) == code
+
+
+D, GH, GG, GU, BW = (0x7F0000000000 + i * (1 << 32) for i in range(10, 15))
+
+
+def bwd(h=H, ldh=64, g=G, ldg=64, u=U, ldu=64, d=D, ldd=32, gh=GH, ldgh=64, gg=GG, ldgg=64, gu=GU, ldgu=64,
+        M=2, N=32, K=64, ws=BW, wsb=1 << 20):
+    return mb.lib().glu_backward(h, ldh, g, ldg, u, ldu, d, ldd, gh, ldgh, gg, ldgg, gu, ldgu, M, N, K, ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(M=-1), SHAPE), (dict(N=-1), SHAPE), (dict(K=-1), SHAPE), (dict(M=17), SHAPE),
+    (dict(h=0), NULL), (dict(d=0), NULL), (dict(ws=0), NULL), (dict(gg=0), NULL), (dict(gu=0), NULL),
+    (dict(ldh=63), STRIDE), (dict(ldd=31), STRIDE), (dict(ldgh=60), STRIDE), (dict(ldgu=1), STRIDE),
+    (dict(h=H + 1), ALIGN), (dict(gh=GH + 1), ALIGN), (dict(ws=BW + 8), ALIGN),
+    (dict(wsb=1000), SHAPE),
+    (dict(gh=H), ALIAS), (dict(gg=G + 64), ALIAS), (dict(gu=D), ALIAS), (dict(ws=GG), ALIAS),
+    (dict(gu=GG + 2 * 64 * 31), ALIAS),
+    (dict(K=0), OK), (dict(K=0, h=0, d=0, ws=0), OK), (dict(M=0, N=0), OK),
+])
+def test_glu_backward_validation(kw, code):
+    """Host-side validation of glu_backward (no GPU: rejections and the
+    shapes that launch nothing)."""
+    assert bwd(**kw) == code
+    assert mb.lib().mbglu_last_variant() == 0
+
+
+def test_glu_backward_workspace_bytes():
+    lib = mb.lib()
+    # dG and dU in fp32, then one fp32 [M][K] partial per row split (N / 256, 1..48)
+    assert lib.glu_backward_workspace_bytes(4, 1000, 512) == 32000 + 3 * 4 * 512 * 4
+    assert lib.glu_backward_workspace_bytes(16, 9728, 2560) == 16 * 9728 * 8 + 38 * 16 * 2560 * 4
+    assert lib.glu_backward_workspace_bytes(1, 100000, 64) == 800000 + 48 * 64 * 4
+    assert lib.glu_backward_workspace_bytes(17, 10, 10) == 0 and lib.glu_backward_workspace_bytes(0, 10, 10) == 0
