@@ -47,7 +47,9 @@ def row_blocks(w, M):
     """Row blocks (passes over the weights) of one call of workload w at M rows."""
     return -(-M // BLOCK_M) if w.op in ("glu_gemv", "add_rmsnorm_glu") and M > BLOCK_M else 1
 KERNEL_NAMES = {1: "glu_stream_kernel", 2: "glu_generic_kernel", 4: "glu_mma_kernel", 5: "silu_mul_kernel",
-                6: "gdn_gates_kernel"}
+                6: "gdn_gates_kernel",
+                8: "glu_backward (the forward kernel with the dG/dU epilogue, glu_bwd_h_kernel, "
+                   "glu_bwd_h_reduce_kernel, glu_bwd_w_kernel)"}
 KERNEL_SOURCES = ["memory_bound_glu_gb300/csrc/glu_kernels.cuh", "memory_bound_glu_gb300/csrc/ptx.cuh",
                   "memory_bound_glu_gb300/csrc/mbglu_api.cu"]
 
@@ -248,6 +250,11 @@ def oracle_sample_rate(w, M, mode, seconds, max_rows=None):
         hb = gi.bits(gi.hidden(w, M))
         call = lambda: oracle.glu_gemv(hb, gb, ub, mode, nthreads=threads)  # noqa: E731
         per_call = 2 * rows * w.K * 2 + M * w.K * 2 + M * rows * 2
+    elif w.op == "glu_backward":
+        hb = gi.bits(gi.hidden(w, M))
+        db = np.ascontiguousarray(gi.bits(gi.upstream(w, M))[:, :rows])
+        call = lambda: oracle.glu_backward(hb, gb, ub, db, nthreads=threads)  # noqa: E731
+        per_call = 4 * rows * w.K * 2 + 2 * M * w.K * 2 + M * rows * 2
     else:
         x, r, nw = (gi.bits(t) for t in gi.norm_inputs(w, M))
         call = lambda: oracle.add_rmsnorm_glu(x, r, nw, w.eps, gb, ub, mode, nthreads=threads)  # noqa: E731
@@ -328,11 +335,16 @@ def run_reference(args, w, M, mode, world, rank):
     g, u = gi.layer_weights(w, 0)
     threads = oracle.default_threads()
     # size the per-step row sample so the whole run stays within ~2 minutes
-    hb = gi.bits(gi.hidden(w, M)) if w.op == "glu_gemv" else None
+    hb = gi.bits(gi.hidden(w, M)) if w.op in ("glu_gemv", "glu_backward") else None
+    db = gi.bits(gi.upstream(w, M)) if w.op == "glu_backward" else None
     probe_rows = min(w.N, 256)
     t0 = time.perf_counter()
-    oracle.glu_gemv(hb if hb is not None else gi.bits(gi.norm_inputs(w, M)[0]),
-                    gi.bits(g[:probe_rows]), gi.bits(u[:probe_rows]), mode, nthreads=threads)
+    if w.op == "glu_backward":
+        oracle.glu_backward(hb, gi.bits(g[:probe_rows]), gi.bits(u[:probe_rows]),
+                            np.ascontiguousarray(db[:, :probe_rows]), nthreads=threads)
+    else:
+        oracle.glu_gemv(hb if hb is not None else gi.bits(gi.norm_inputs(w, M)[0]),
+                        gi.bits(g[:probe_rows]), gi.bits(u[:probe_rows]), mode, nthreads=threads)
     per_row = (time.perf_counter() - t0) / probe_rows
     budget = 120.0 / (steps + warm)
     rows = int(max(8, min(w.N, budget / max(per_row, 1e-9))))
@@ -340,6 +352,10 @@ def run_reference(args, w, M, mode, world, rank):
     if w.op == "glu_gemv":
         call = lambda: oracle.glu_gemv(hb, gb, ub, mode, nthreads=threads)  # noqa: E731
         per_step = 2 * rows * w.K * 2 + M * w.K * 2 + M * rows * 2
+    elif w.op == "glu_backward":
+        dr = np.ascontiguousarray(db[:, :rows])
+        call = lambda: oracle.glu_backward(hb, gb, ub, dr, nthreads=threads)  # noqa: E731
+        per_step = 4 * rows * w.K * 2 + 2 * M * w.K * 2 + M * rows * 2
     else:
         x, r, nw = (gi.bits(t) for t in gi.norm_inputs(w, M))
         call = lambda: oracle.add_rmsnorm_glu(x, r, nw, w.eps, gb, ub, mode, nthreads=threads)  # noqa: E731
@@ -440,7 +456,7 @@ def main():
 
     # inputs: resident in HBM before the timed region
     gates, ups = [], []
-    for layer in range(L if w.op in ("glu_gemv", "add_rmsnorm_glu") else 0):
+    for layer in range(L if w.op in ("glu_gemv", "add_rmsnorm_glu", "glu_backward") else 0):
         g, u = gi.layer_weights(w, layer)
         gates.append(g.to(dev))
         ups.append(u.to(dev))
@@ -455,6 +471,13 @@ def main():
     elif w.op == "glu_gemv":
         h_cpu = gi.hidden(w, M)
         h = h_cpu.to(dev)
+    elif w.op == "glu_backward":
+        h_cpu, d_cpu = gi.hidden(w, M), gi.upstream(w, M)
+        h, dout = h_cpu.to(dev), d_cpu.to(dev)
+        grad_gates = [torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+        grad_ups = [torch.empty((w.N, w.K), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+        grad_hs = torch.empty((L, M, w.K), dtype=torch.bfloat16, device=dev)
+        bws = torch.empty(mb.lib().glu_backward_workspace_bytes(M, w.N, w.K), dtype=torch.uint8, device=dev)
     else:
         x_cpu, r_cpu, nw_cpu = gi.norm_inputs(w, M)
         x, nw = x_cpu.to(dev), nw_cpu.to(dev)
@@ -466,6 +489,8 @@ def main():
     blocks = row_blocks(w, M)
     block_rows = [min(BLOCK_M, M - m0) for m0 in range(0, M, BLOCK_M)] if blocks > 1 else [M]
     launches_per_call = blocks * (2 if (w.op == "add_rmsnorm_glu" and not single) else 1)
+    if w.op == "glu_backward":
+        launches_per_call = 4
 
     def one_step():
         for i in range(L):
@@ -475,6 +500,9 @@ def main():
                 mb.gdn_gates(gdn[i][0], gdn[i][1], gdn[i][2], gdn[i][3], g=gs[i], beta=outs[i])
             elif w.op == "glu_gemv":
                 mb.glu_gemv(h, gates[i], ups[i], out=outs[i], mode=mode)
+            elif w.op == "glu_backward":
+                mb.glu_backward(h, gates[i], ups[i], dout, grad_h=grad_hs[i], grad_gate=grad_gates[i],
+                                grad_up=grad_ups[i], workspace=bws)
             else:
                 mb.add_rmsnorm_glu(x, residuals[i], nw, w.eps, gates[i], ups[i], out=outs[i], mode=mode,
                                    workspace=ws)
@@ -553,11 +581,17 @@ def main():
         elif w.op == "glu_gemv":
             h_host = h_cpu.pin_memory()
             in_bytes = h_host.numel() * 2
+        elif w.op == "glu_backward":
+            h_host, d_host = h_cpu.pin_memory(), d_cpu.pin_memory()
+            in_bytes = (h_host.numel() + d_host.numel()) * 2
         else:
             x_host = x_cpu.pin_memory()
             r_host = r_cpu.pin_memory()
             in_bytes = (x_host.numel() + r_host.numel() * L) * 2
-        out_host = torch.empty((L, M, w.N), dtype=torch.bfloat16).pin_memory()
+        # the step's result read back: out, or for the backward grad_h (the
+        # weight gradients stay on the device, where an optimizer uses them)
+        result = grad_hs if w.op == "glu_backward" else outs
+        out_host = torch.empty(tuple(result.shape), dtype=torch.bfloat16).pin_memory()
 
         def e2e_step():
             if w.op == "gdn_gates":
@@ -569,12 +603,15 @@ def main():
                     xs[i].copy_(xs_host[i], non_blocking=True)
             elif w.op == "glu_gemv":
                 h.copy_(h_host, non_blocking=True)
+            elif w.op == "glu_backward":
+                h.copy_(h_host, non_blocking=True)
+                dout.copy_(d_host, non_blocking=True)
             else:
                 x.copy_(x_host, non_blocking=True)
                 for i in range(L):
                     residuals[i].copy_(r_host, non_blocking=True)
             one_step()
-            out_host.copy_(outs, non_blocking=True)
+            out_host.copy_(result, non_blocking=True)
 
         with torch.cuda.stream(stream):
             for _ in range(5):

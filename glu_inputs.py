@@ -99,7 +99,7 @@ def small_int_bf16(shape: Sequence[int], seed: int, lo: int = -8, hi: int = 8) -
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    op: str                      # "glu_gemv", "add_rmsnorm_glu", "silu_mul" or "gdn_gates"
+    op: str                      # "glu_gemv", "add_rmsnorm_glu", "glu_backward", "silu_mul" or "gdn_gates"
     Ms: tuple                    # batch rows exercised
     K: int
     N: int
@@ -131,6 +131,8 @@ class Workload:
             return M * self.N * (2 + 2 + 4 + 2) + 2 * self.N * 4
         elif self.op == "glu_gemv":
             b += M * self.K * 2
+        elif self.op == "glu_backward":   # weights read and their gradients written; h, dout read; grad_h written
+            return 2 * self.weight_bytes() + 2 * M * self.K * 2 + M * self.N * 2
         else:  # x, residual read; residual written; norm_w read
             b += 3 * M * self.K * 2 + self.K * 2
         return b
@@ -148,6 +150,8 @@ WORKLOADS = {
         # batched decode at 32 and 64 rows (row blocks of 16, one pass over the
         # weights each), HF-boundary rounding
         Workload("gemv_k2560_n9728_wide", "glu_gemv", (32, 64), 2560, 9728, ("hf",), 32, 1 / math.sqrt(2560)),
+        # the backward of the K=2560, N=9728 layer (gradients of h and both weights)
+        Workload("bwd_k2560_n9728", "glu_backward", (1, 8), 2560, 9728, ("fused",), 16, 1 / math.sqrt(2560)),
         # fused residual-add + zero-centred RMSNorm prologue
         Workload("norm_gemv_k2560_n9728", "add_rmsnorm_glu", (1, 4, 8), 2560, 9728, ("hf",), 32,
                  1 / math.sqrt(2560)),
@@ -183,6 +187,11 @@ def layer_weights(w: Workload, layer: int, seed: Optional[int] = None):
 def hidden(w: Workload, M: int, seed: Optional[int] = None) -> torch.Tensor:
     """h [M, K] bf16 CPU tensor (glu_gemv input)."""
     return normal_bf16((M, w.K), w.h_std, w.seed if seed is None else seed, w.name, "h", M)
+
+
+def upstream(w: Workload, M: int, seed: Optional[int] = None) -> torch.Tensor:
+    """dout [M, N] bf16 CPU tensor ~ N(0, 1): the upstream gradient of glu_backward."""
+    return normal_bf16((M, w.N), 1.0, w.seed if seed is None else seed, w.name, "dout", M)
 
 
 def projections(w: Workload, M: int, layer: int = 0, seed: Optional[int] = None) -> torch.Tensor:
