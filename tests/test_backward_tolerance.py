@@ -94,3 +94,63 @@ def test_bf16_round_array_is_the_scalar_rounding():
     x = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-45, 40, 2000),
                         [0.0, -0.0, np.inf, -np.inf, np.nan, 3.3895e38, 3.4e38, 1e-40, -9.2e-41]])
     assert np.array_equal(oracle.bf16_round_array(x), np.array([oracle.bf16_round(v) for v in x], dtype=np.uint16))
+
+
+def _fma32(a, b, c):
+    """fp32 fused multiply-add, elementwise: the product of two fp32 values is
+    exact in binary64 and the sum is rounded once to fp32 (a second rounding
+    in binary64 first can differ only at exact fp32 ties, far rarer than the
+    bar's allowance)."""
+    return (a.astype(np.float64) * b.astype(np.float64) + c.astype(np.float64)).astype(np.float32)
+
+
+def _kernel_order_backward(h, g, u, d):
+    """glu_backward's sums in the kernels' order (csrc/glu_backward.cuh): dG,
+    dU from fp32 g, u; grad_h per 512-column block and row split as two
+    alternating-row FMA chains (dG*Wg then dU*Wu per row) added half 0 +
+    half 1, then the splits summed in order; grad_W as an FMA chain over
+    m = 0, 1, ...  g and u themselves come from an fp32 GEMM (their own
+    order is the forward's, checked by the forward's bar)."""
+    h32, g32, u32, d32 = (_f64(a).astype(np.float32) for a in (h, g, u, d))
+    M, K = h32.shape
+    N = g32.shape[0]
+    G, U = h32 @ g32.T, h32 @ u32.T
+    with np.errstate(over="ignore"):
+        t = np.exp(-np.abs(G))
+    one = np.float32(1.0)
+    sig = np.where(G >= 0, one, t) / (one + t)
+    rest = np.where(G >= 0, t, one) / (one + t)
+    silu, dsilu = G * sig, sig * (one + G * rest)
+    dG, dU = ((d32 * U) * dsilu).astype(np.float32), (d32 * silu).astype(np.float32)
+    nsplit = max(1, min(48, N // 256))
+    part = np.zeros((nsplit, M, K), dtype=np.float32)
+    for b in range(nsplit):
+        n0, n1 = N * b // nsplit, N * (b + 1) // nsplit
+        halves = []
+        for half in (0, 1):
+            acc = np.zeros((M, K), dtype=np.float32)
+            for n in range(n0 + half, n1, 2):
+                acc = _fma32(dG[:, n:n + 1], g32[n][None, :], acc)
+                acc = _fma32(dU[:, n:n + 1], u32[n][None, :], acc)
+            halves.append(acc)
+        part[b] = halves[0] + halves[1]
+    grad_h = part[0].copy()
+    for b in range(1, nsplit):
+        grad_h = (grad_h + part[b]).astype(np.float32)
+    sg = np.zeros((N, K), dtype=np.float32)
+    su = np.zeros((N, K), dtype=np.float32)
+    for m in range(M):
+        sg = _fma32(dG[m][:, None], h32[m][None, :], sg)
+        su = _fma32(dU[m][:, None], h32[m][None, :], su)
+    return tuple(_bits_from_f32(x) for x in (grad_h, sg, su))
+
+
+@pytest.mark.parametrize("M,N,K,seed", [(1, 1300, 600, 4), (16, 2048, 1024, 5)])
+def test_kernel_order_backward_meets_the_bar(M, N, K, seed):
+    """The kernels' own summation order (row splits of 256+ rows, alternating
+    rows per half, in-order split sums) passes the bar."""
+    h, g, u, d = _case(M, N, K, seed)
+    refs, floors = _reference(h, g, u, d)
+    got = _kernel_order_backward(h, g, u, d)
+    for name, a, r, tau in zip(("grad_h", "grad_gate", "grad_up"), got, refs, floors):
+        tol.assert_parity(a, r, tau, f"kernel order {name} M={M}")
