@@ -91,11 +91,11 @@ __global__ void __launch_bounds__(256) glu_bwd_h_kernel(const BwdParams q)
     for (int c0 = n0; c0 < n1; c0 += kBwdRowChunk) {
         const int rows = min(kBwdRowChunk, n1 - c0);
         __syncthreads();   // the previous chunk's reads are done
-        for (int i = threadIdx.x; i < q.M * rows; i += blockDim.x) {
-            const int m = i / rows, j = i - m * rows;
-            dg_s[m * kBwdRowChunk + j] = q.dG[static_cast<int64_t>(m) * q.N + c0 + j];
-            du_s[m * kBwdRowChunk + j] = q.dU[static_cast<int64_t>(m) * q.N + c0 + j];
-        }
+        for (int m = 0; m < q.M; ++m)
+            for (int j = threadIdx.x; j < rows; j += blockDim.x) {
+                dg_s[m * kBwdRowChunk + j] = q.dG[static_cast<int64_t>(m) * q.N + c0 + j];
+                du_s[m * kBwdRowChunk + j] = q.dU[static_cast<int64_t>(m) * q.N + c0 + j];
+            }
         __syncthreads();
         if (k < q.K) {
 #pragma unroll 4
@@ -191,11 +191,9 @@ __global__ void __launch_bounds__(256) glu_bwd_w_kernel(const BwdParams q)
     const uint16_t *hb = q.h;
     int64_t hld = q.ldh;
     if (q.h_smem) {
-        const int64_t total = static_cast<int64_t>(q.M) * q.K;
-        for (int64_t i = threadIdx.x; i < total; i += blockDim.x) {
-            const int64_t m = i / q.K, k = i - m * q.K;
-            hw_s[i] = q.h[m * q.ldh + k];
-        }
+        for (int m = 0; m < q.M; ++m)
+            for (int k = threadIdx.x; k < q.K; k += blockDim.x)
+                hw_s[static_cast<int64_t>(m) * q.K + k] = q.h[m * q.ldh + k];
         __syncthreads();
         hb = hw_s;
         hld = q.K;
