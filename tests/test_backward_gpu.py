@@ -143,19 +143,3 @@ def test_autograd_function_matches_glu_backward():
     torch.cuda.synchronize()
     for a, b in zip((h.grad, g.grad, u.grad), ref):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
-
-
-def test_backward_full_size_headline_layer():
-    """K = 2560, N = 9728 (the headline layer) at batch 1 and 8: every
-    gradient on the GPU; grad_h whole and 512 sampled rows of the weight
-    gradients against the oracle."""
-    w = gi.WORKLOADS["gemv_k2560_n9728"]
-    g, u = gi.layer_weights(w, 0)
-    rows = np.sort(np.random.default_rng(2).choice(w.N, 512, replace=False))
-    for M in (1, 8):
-        h = gi.hidden(w, M)
-        d = gi.normal_bf16((M, w.N), 1.0, M, "bwf-d")
-        got = mb.glu_backward(h.to(DEV), g.to(DEV), u.to(DEV), d.to(DEV))
-        torch.cuda.synchronize()
-        _check(tuple(t.cpu() for t in got), h, g, u, d, f"full size M={M}", rows=rows)
-    assert mb.read_device_error() == 0
