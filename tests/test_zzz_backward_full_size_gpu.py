@@ -1,7 +1,7 @@
 """glu_backward at full size: the K = 2560, N = 9728 layer at batch 1 and 8,
 against the fp64 oracle (grad_h whole, 512 sampled rows of each weight
-gradient).  Collected after the forward's GPU tests, so that with -x a
-failure here leaves them already run."""
+gradient).  Collected after every other GPU test file, so that with -x a
+failure here leaves them all already run."""
 import numpy as np
 import pytest
 import torch
