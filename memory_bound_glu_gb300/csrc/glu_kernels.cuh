@@ -111,9 +111,9 @@ __device__ __forceinline__ float silu_f32(float x)
     return (x >= 0.0f ? x : x * t) / (1.0f + t);
 }
 
-// mode 0 (FUSED): one rounding.  mode 1 (HF): the bf16 composite's roundings
-// of g, u, SiLU(g) and the product (PR #9057 "Changes": "Restore HF's
-// intermediate BF16 rounding in ... GLU").  sb * ub is exact in fp32.
+// mode 0 (FUSED): one rounding.  mode 1 (HF): the bf16 composite's roundings:
+// g, u, SiLU(g) and the product each round to bf16 (PR #9057, section
+// "Changes").  sb * ub is exact in fp32.
 __device__ __forceinline__ uint16_t glu_epilogue(float g, float u, int mode)
 {
     if (mode == 0) return f32_to_bf16(silu_f32(g) * u);
@@ -159,6 +159,184 @@ __device__ __forceinline__ float warp_allsum(float v)
 }
 
 // ---------------------------------------------------------------------------
+// The normed row, correctly rounded: h = bf16( s * (mean_k s^2 + eps)^-1/2 *
+// (1 + w) ) is the bf16 value nearest to the exact real number.  A plain
+// fp32 chain (sum, sqrt, two products: a few fp32 ulps in all) rounds h to
+// the other bf16 neighbour wherever the exact value lies that close to a
+// midpoint -- about 3e-5 of the elements -- and in HF mode one such element
+// of a row shifts g and u of every output of that row enough to re-round a
+// few percent of them.  So:
+//   * the statistic is summed in double-float (a pair of fp32 words whose sum
+//     carries the value), each s^2 (exact in fp32) added with Knuth's
+//     error-free TwoSum, the thread partials combined the same way;
+//   * (var + eps)^-1/2 starts from rsqrtf and takes one Newton step,
+//     y (1 + e/2) with e = 1 - v y^2 formed with exact products (FMA), to
+//     about 2^-44 relative, kept as inv_hi + inv_lo;
+//   * each element is formed in fp32 first; if it lies within 5 fp32 ulps
+//     of a bf16 midpoint (which bounds the fp32 chain's error) it is formed
+//     again in double-float (Dekker's exact products) and rounded from that.
+// The statistic is exact up to ~2^-46 and the element up to ~2^-44, so h is
+// the correctly rounded value except where the exact value lies within
+// ~2^-44 relative of a midpoint.  Every path computes the same h.
+// ---------------------------------------------------------------------------
+
+// s = fl(a + b), e = (a + b) - s exactly (TwoSum; the _rn intrinsics keep
+// the compiler from contracting or reordering it)
+__device__ __forceinline__ float two_sum(float a, float b, float &e)
+{
+    const float s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+    return s;
+}
+
+__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+
+// A thread's sum of squares as two packed double-float accumulators (the
+// even and the odd elements of its chunks).
+struct SumSq {
+    float2 hi, lo;
+};
+
+__device__ __forceinline__ SumSq sumsq_zero()
+{
+    SumSq a;
+    a.hi = a.lo = make_float2(0.0f, 0.0f);
+    return a;
+}
+
+// acc += x (x exact), TwoSum on both packed lanes
+__device__ __forceinline__ void sumsq_add(SumSq &acc, float2 x)
+{
+    const float2 t = __fadd2_rn(acc.hi, x);
+    const float2 bp = __fadd2_rn(t, neg2(acc.hi));
+    const float2 e = __fadd2_rn(__fadd2_rn(acc.hi, neg2(__fadd2_rn(t, neg2(bp)))), __fadd2_rn(x, neg2(bp)));
+    acc.lo = __fadd2_rn(acc.lo, e);
+    acc.hi = t;
+}
+
+// the squares of 8 bf16 (exact in fp32) into acc
+__device__ __forceinline__ void sumsq_bf16x8(uint4 v, SumSq &acc)
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 a = make_float2(bf16_lo(w[j]), bf16_hi(w[j]));
+        sumsq_add(acc, __fmul2_rn(a, a));
+    }
+}
+
+// (hi, lo) of a thread's accumulators: hi the fp32 sum of the two lanes, lo
+// every remaining part (small against hi)
+__device__ __forceinline__ float2 sumsq_total(const SumSq &a)
+{
+    float e;
+    const float hi = two_sum(a.hi.x, a.hi.y, e);
+    return make_float2(hi, __fadd_rn(e, __fadd_rn(a.lo.x, a.lo.y)));
+}
+
+// (hi, lo) += (bhi, blo), renormalised so that |lo| <= ulp(hi) / 2 (for
+// non-negative sums, where the error of hi + bhi is far below the sum)
+__device__ __forceinline__ void df_add(float &hi, float &lo, float bhi, float blo)
+{
+    float e;
+    const float t = two_sum(hi, bhi, e);
+    e = __fadd_rn(e, __fadd_rn(lo, blo));
+    hi = __fadd_rn(t, e);
+    lo = __fsub_rn(e, __fsub_rn(hi, t));
+}
+
+// the butterfly of a double-float over the warp: every lane gets the same sum
+__device__ __forceinline__ void df_warp_allsum(float &hi, float &lo)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float oh = __shfl_xor_sync(0xffffffffu, hi, off);
+        const float ol = __shfl_xor_sync(0xffffffffu, lo, off);
+        df_add(hi, lo, oh, ol);
+    }
+}
+
+// (inv_hi, inv_lo) = (S / K + eps)^-1/2 for the row's sum of squares S = hi + lo
+__device__ __forceinline__ float2 norm_inv(float hi, float lo, int K, float eps)
+{
+    const float kf = static_cast<float>(K);
+    const float q = __fdiv_rn(hi, kf);
+    const float rem = __fmaf_rn(-q, kf, hi);                  // hi - q K, exact
+    float vh = q, vl = __fdiv_rn(__fadd_rn(rem, lo), kf);
+    df_add(vh, vl, eps, 0.0f);
+    const float y = rsqrtf(vh);
+    const float y2 = __fmul_rn(y, y);
+    const float y2l = __fmaf_rn(y, y, -y2);                   // y^2 = y2 + y2l exactly
+    const float t = __fmul_rn(vh, y2);
+    const float tl = __fmaf_rn(vl, y2, __fmaf_rn(vh, y2l, __fmaf_rn(vh, y2, -t)));
+    const float e = __fsub_rn(__fsub_rn(1.0f, t), tl);       // 1 - v y^2; 1 - t is exact (t near 1)
+    const float c = __fmul_rn(__fmul_rn(0.5f, y), e);
+    const float ih = __fadd_rn(y, c);
+    return make_float2(ih, __fsub_rn(c, __fsub_rn(ih, y)));
+}
+
+// one element of h from s, w and the row's (inv_hi, inv_lo), in double-float
+__device__ __forceinline__ uint16_t norm_elem_df(float sv, float w, float ih, float il)
+{
+    float al;
+    const float ah = two_sum(1.0f, w, al);                    // 1 + w = ah + al exactly
+    const float ph = __fmul_rn(sv, ih);
+    const float pl = __fmaf_rn(sv, il, __fmaf_rn(sv, ih, -ph));
+    const float qh = __fmul_rn(ph, ah);
+    const float ql = __fmaf_rn(ph, al, __fmaf_rn(pl, ah, __fmaf_rn(ph, ah, -qh)));
+    const float t = __fadd_rn(qh, ql);
+    const float l = __fsub_rn(ql, __fsub_rn(t, qh));
+    const uint32_t b = __float_as_uint(t);
+    if ((b & 0xffffu) == 0x8000u && l != 0.0f) {
+        // t sits on a bf16 midpoint and the exact value lies past it on l's side
+        const bool away = (l > 0.0f) == (t > 0.0f);
+        return static_cast<uint16_t>((b >> 16) + (away ? 1u : 0u));
+    }
+    return f32_to_bf16(t);
+}
+
+// the element in fp32: (s * inv_hi) * (1 + w)
+__device__ __forceinline__ float norm_elem_f32(float sv, float w, float ih)
+{
+    return __fmul_rn(__fmul_rn(sv, ih), __fadd_rn(1.0f, w));
+}
+
+// true if the fp32 element lies within 5 fp32 ulps of a bf16 midpoint, the
+// most the fp32 chain can be off: only then can its rounding be wrong
+__device__ __forceinline__ bool near_midpoint(float v) { return (__float_as_uint(v) & 0xffffu) - 0x7ffbu <= 10u; }
+
+__device__ __forceinline__ uint16_t norm_elem(float sv, float w, float ih, float il)
+{
+    const float v = norm_elem_f32(sv, w, ih);
+    return near_midpoint(v) ? norm_elem_df(sv, w, ih, il) : f32_to_bf16(v);
+}
+
+// 8 elements of h from 8 of s and of w (bf16 pairs); the double-float
+// evaluation runs for the whole chunk in the rare case one element needs it
+__device__ __forceinline__ uint4 norm_chunk(uint4 v, uint4 w, float ih, float il)
+{
+    const uint32_t sv[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    uint32_t o[4];
+    bool near = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float lo = norm_elem_f32(bf16_lo(sv[j]), bf16_lo(ww[j]), ih);
+        const float hi = norm_elem_f32(bf16_hi(sv[j]), bf16_hi(ww[j]), ih);
+        near |= near_midpoint(lo) | near_midpoint(hi);
+        o[j] = pack_bf16x2(lo, hi);
+    }
+    if (near) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[j] = static_cast<uint32_t>(norm_elem(bf16_lo(sv[j]), bf16_lo(ww[j]), ih, il)) |
+                   (static_cast<uint32_t>(norm_elem(bf16_hi(sv[j]), bf16_hi(ww[j]), ih, il)) << 16);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ---------------------------------------------------------------------------
 // prologues: h into shared memory
 // ---------------------------------------------------------------------------
 
@@ -183,102 +361,57 @@ __device__ __forceinline__ void load_h_to_smem(const GluParams &p, uint16_t *h_s
     }
 }
 
-// Zero-centred RMSNorm of the updated residual rows (PR #9057 "Changes"):
-//   var = mean_k s^2 (fp32, fixed reduction order), inv = 1 / sqrt(var + eps),
-//   h = bf16( (s * inv) * (1 + w) ) with the (1 + w) scale built in fp32.
-// Every CTA runs the same code on the same data, so every CTA gets the same h.
-// red: [kMaxWarps][MB] shared floats; inv_s: [MB].  Writes rows_out rows of
-// h_s (rows M..rows_out-1 zero); M <= MB.
-// src: the s rows (row stride sstride; default: residual in global memory);
-// may be h_s itself (each chunk is read before the same thread overwrites it).
-// w_src: norm_w (default: global memory).
+// Zero-centred RMSNorm of the updated residual rows for the generic kernel
+// (PR #9057 "Changes"): var = mean_k s^2, inv = (var + eps)^-1/2,
+// h = bf16( s * inv * (1 + w) ), correctly rounded (see norm_elem); 2-byte
+// accesses, any alignment.  Every CTA runs the same code on the same data, so
+// every CTA gets the same h -- the same h as the streaming kernels' prologue.
+// red: [kMaxWarps][MB] shared double-floats; inv_s: [2 MB].  Writes
+// rows_out rows of h_s (rows M..rows_out-1 zero, row stride K); M <= MB.
+// s: the residual rows in global memory (p.s, row stride K).
 template <int MB>
-__device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s, float (*red)[MB],
-                                              float *inv_s, int rows_out, int hstride = 0,
-                                              const uint16_t *src = nullptr, int sstride = 0,
-                                              const uint16_t *w_src = nullptr)
+__device__ __forceinline__ void norm_prologue(const GluParams &p, uint16_t *h_s, float2 (*red)[MB],
+                                              float *inv_s, int rows_out)
 {
-    if (hstride == 0) hstride = p.K;
-    if (sstride == 0) sstride = p.K;
-    const uint16_t *sp = src ? src : p.s;
-    const uint16_t *wp = w_src ? w_src : p.norm_w;   // norm_w: shared-memory copy or global
+    const uint16_t *sp = p.s;
+    const uint16_t *wp = p.norm_w;
     const int K = p.K, tid = threadIdx.x, nthr = blockDim.x;
     const int warp = tid >> 5, lane = tid & 31, nw = nthr >> 5;
-    float ss[MB];
+    float hi[MB], lo[MB];
 #pragma unroll
-    for (int m = 0; m < MB; ++m) ss[m] = 0.0f;
-    if (p.vec_in) {
-        const int nch = K >> 3;
-        for (int c = tid; c < nch; c += nthr) {
+    for (int m = 0; m < MB; ++m) hi[m] = lo[m] = 0.0f;
+    for (int k = tid; k < K; k += nthr) {
 #pragma unroll
-            for (int m = 0; m < MB; ++m) {
-                if (m < p.M) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(sp + static_cast<int64_t>(m) * sstride + c * 8);
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
-                        ss[m] = fmaf(a, a, ss[m]);
-                        ss[m] = fmaf(b, b, ss[m]);
-                    }
-                }
-            }
-        }
-    } else {
-        for (int k = tid; k < K; k += nthr) {
-#pragma unroll
-            for (int m = 0; m < MB; ++m) {
-                if (m < p.M) {
-                    const float a = bf16_to_f32(sp[static_cast<int64_t>(m) * sstride + k]);
-                    ss[m] = fmaf(a, a, ss[m]);
-                }
+        for (int m = 0; m < MB; ++m) {
+            if (m < p.M) {
+                const float a = bf16_to_f32(sp[static_cast<int64_t>(m) * K + k]);
+                float e;
+                hi[m] = two_sum(hi[m], __fmul_rn(a, a), e);
+                lo[m] = __fadd_rn(lo[m], e);
             }
         }
     }
 #pragma unroll
     for (int m = 0; m < MB; ++m) {
-        const float t = warp_allsum(ss[m]);
-        if (lane == 0) red[warp][m] = t;
+        df_warp_allsum(hi[m], lo[m]);
+        if (lane == 0) red[warp][m] = make_float2(hi[m], lo[m]);
     }
     __syncthreads();
-    if (tid < MB) {
-        float t = 0.0f;
-        for (int w = 0; w < nw; ++w) t += red[w][tid];
-        inv_s[tid] = 1.0f / sqrtf(t / static_cast<float>(K) + p.eps);
+    if (tid < p.M) {
+        float th = 0.0f, tl = 0.0f;
+        for (int w = 0; w < nw; ++w) df_add(th, tl, red[w][tid].x, red[w][tid].y);
+        const float2 inv = norm_inv(th, tl, K, p.eps);
+        inv_s[2 * tid] = inv.x;
+        inv_s[2 * tid + 1] = inv.y;
     }
     __syncthreads();
-    if (p.vec_in) {
-        const int nch = K >> 3;
-        for (int i = tid; i < rows_out * nch; i += nthr) {
-            const int m = i / nch, c = i - m * nch;
-            uint4 o = make_uint4(0, 0, 0, 0);
-            if (m < p.M) {
-                const float inv = inv_s[m];
-                const uint4 v = *reinterpret_cast<const uint4 *>(sp + static_cast<int64_t>(m) * sstride + c * 8);
-                const uint4 wv = *reinterpret_cast<const uint4 *>(wp + c * 8);
-                const uint32_t sv[4] = {v.x, v.y, v.z, v.w};
-                const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-                uint32_t r[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float lo = (bf16_lo(sv[j]) * inv) * (1.0f + bf16_lo(ww[j]));
-                    const float hi = (bf16_hi(sv[j]) * inv) * (1.0f + bf16_hi(ww[j]));
-                    r[j] = pack_bf16x2(lo, hi);
-                }
-                o = make_uint4(r[0], r[1], r[2], r[3]);
-            }
-            *reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(m) * hstride + c * 8) = o;
-        }
-    } else {
-        for (int i = tid; i < rows_out * K; i += nthr) {
-            const int m = i / K, k = i - m * K;
-            uint16_t o = 0;
-            if (m < p.M) {
-                const float sv = bf16_to_f32(sp[static_cast<int64_t>(m) * sstride + k]);
-                o = f32_to_bf16((sv * inv_s[m]) * (1.0f + bf16_to_f32(wp[k])));
-            }
-            h_s[static_cast<int64_t>(m) * hstride + k] = o;
-        }
+    for (int i = tid; i < rows_out * K; i += nthr) {
+        const int m = i / K, k = i - m * K;
+        uint16_t o = 0;
+        if (m < p.M)
+            o = norm_elem(bf16_to_f32(sp[static_cast<int64_t>(m) * K + k]), bf16_to_f32(wp[k]), inv_s[2 * m],
+                          inv_s[2 * m + 1]);
+        h_s[static_cast<int64_t>(m) * K + k] = o;
     }
 }
 
@@ -335,18 +468,6 @@ __device__ __forceinline__ RowMap row_map(int M, int K)
     return r;
 }
 
-__device__ __forceinline__ float sum_squares_bf16x8(uint4 v, float ss)
-{
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
-        ss = fmaf(a, a, ss);
-        ss = fmaf(b, b, ss);
-    }
-    return ss;
-}
-
 __device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b)
 {
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
@@ -378,11 +499,11 @@ __device__ __forceinline__ void x_prefetch_rows(const GluParams &p, const RowMap
 
 // s = bf16(x + residual) formed in place in h_s (the fp32 sum of two bf16
 // values rounds to the same bf16 as the exact sum); returns this thread's
-// sum of s^2 over its chunks, in chunk order.
-__device__ __forceinline__ float add_rows_in_place(const GluParams &p, const RowMap &r, uint16_t *h_s, int hstride,
-                                                   XRows &x)
+// sum of s^2 over its chunks, in chunk order, as a double-float.
+__device__ __forceinline__ float2 add_rows_in_place(const GluParams &p, const RowMap &r, uint16_t *h_s, int hstride,
+                                                    XRows &x)
 {
-    float ss = 0.0f;
+    SumSq ss = sumsq_zero();
     uint4 *row = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
     for (int j0 = 0;; j0 += kXRows) {
         if (j0 > 0) x_prefetch_rows(p, r, x, j0);
@@ -392,65 +513,75 @@ __device__ __forceinline__ float add_rows_in_place(const GluParams &p, const Row
             if (r.active && c < r.nch) {
                 const uint4 sv = add_bf16x8(x.v[j], row[c]);
                 row[c] = sv;
-                ss = sum_squares_bf16x8(sv, ss);
+                sumsq_bf16x8(sv, ss);
             }
         }
         if (!r.active || r.c0 + (j0 + kXRows) * r.P >= r.nch) break;
     }
-    return ss;
+    return sumsq_total(ss);
 }
 
-// This thread's sum of s^2 over its chunks of h_s, in chunk order.
-__device__ __forceinline__ float square_rows(const RowMap &r, const uint16_t *h_s, int hstride)
+// This thread's sum of s^2 over its chunks of h_s, in chunk order, as a
+// double-float.
+__device__ __forceinline__ float2 square_rows(const RowMap &r, const uint16_t *h_s, int hstride)
 {
-    float ss = 0.0f;
-    if (!r.active) return ss;
+    SumSq ss = sumsq_zero();
+    if (!r.active) return make_float2(0.0f, 0.0f);
     const uint4 *row = reinterpret_cast<const uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
 #pragma unroll 4
-    for (int c = r.c0; c < r.nch; c += r.P) ss = sum_squares_bf16x8(row[c], ss);
-    return ss;
+    for (int c = r.c0; c < r.nch; c += r.P) sumsq_bf16x8(row[c], ss);
+    return sumsq_total(ss);
 }
 
 // Zero-centred RMSNorm of the rows in h_s, in place (PR #9057 "Changes"):
-//   var = mean_k s^2 (fp32), inv = 1 / sqrt(var + eps),
-//   h = bf16( (s * inv) * (1 + w) ) with the (1 + w) scale built in fp32.
-// ss: this thread's partial sum from square_rows or add_rows_in_place.  Row
-// m's partials are added by one warp (lane-strided, then a butterfly): a
-// fixed order, and every CTA computes the identical h.  part: blockDim
-// floats of shared memory; inv_s: M floats.  Rows M..rows_out-1 of h_s
-// become zero.  Ends with a barrier.
-__device__ __forceinline__ void norm_rows_in_place(const GluParams &p, const RowMap &r, float ss, uint16_t *h_s,
+//   var = mean_k s^2, inv = (var + eps)^-1/2, h = bf16( s * inv * (1 + w) ),
+// with (1 + w) formed exactly and h correctly rounded (see norm_elem).
+// ss: this thread's double-float partial from square_rows or
+// add_rows_in_place.  Row m's partials are added by one warp (lane-strided,
+// then a butterfly), first the high words in double-float, then the low
+// words: a fixed order, and every CTA computes the identical h.  part:
+// blockDim floats of shared memory; inv_s: 2 M floats.  Rows
+// M..rows_out-1 of h_s become zero.  Ends with a barrier.
+__device__ __forceinline__ void norm_rows_in_place(const GluParams &p, const RowMap &r, float2 ss, uint16_t *h_s,
                                                    int hstride, const uint16_t *w_s, float *part, float *inv_s,
                                                    int rows_out)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
-    part[tid] = ss;
+    part[tid] = ss.x;
+    __syncthreads();
+    for (int m = warp; m < p.M; m += nw) {
+        float hi = 0.0f, lo = 0.0f;
+        for (int i = lane; i < r.P; i += 32) {
+            float e;
+            hi = two_sum(hi, part[m * r.P + i], e);
+            lo = __fadd_rn(lo, e);
+        }
+        df_warp_allsum(hi, lo);
+        if (lane == 0) {
+            inv_s[2 * m] = hi;
+            inv_s[2 * m + 1] = lo;
+        }
+    }
+    __syncthreads();
+    part[tid] = ss.y;
     __syncthreads();
     for (int m = warp; m < p.M; m += nw) {
         float t = 0.0f;
-        for (int i = lane; i < r.P; i += 32) t += part[m * r.P + i];
+        for (int i = lane; i < r.P; i += 32) t = __fadd_rn(t, part[m * r.P + i]);
         t = warp_allsum(t);
-        if (lane == 0) inv_s[m] = 1.0f / sqrtf(t / static_cast<float>(p.K) + p.eps);
+        if (lane == 0) {
+            const float2 inv = norm_inv(inv_s[2 * m], __fadd_rn(inv_s[2 * m + 1], t), p.K, p.eps);
+            inv_s[2 * m] = inv.x;
+            inv_s[2 * m + 1] = inv.y;
+        }
     }
     __syncthreads();
     if (r.active) {
-        const float inv = inv_s[r.m];
+        const float ih = inv_s[2 * r.m], il = inv_s[2 * r.m + 1];
         uint4 *row = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
         const uint4 *wv = reinterpret_cast<const uint4 *>(w_s);
 #pragma unroll 4
-        for (int c = r.c0; c < r.nch; c += r.P) {
-            const uint4 v = row[c], w = wv[c];
-            const uint32_t sv[4] = {v.x, v.y, v.z, v.w};
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float lo = (bf16_lo(sv[j]) * inv) * (1.0f + bf16_lo(ww[j]));
-                const float hi = (bf16_hi(sv[j]) * inv) * (1.0f + bf16_hi(ww[j]));
-                o[j] = pack_bf16x2(lo, hi);
-            }
-            row[c] = make_uint4(o[0], o[1], o[2], o[3]);
-        }
+        for (int c = r.c0; c < r.nch; c += r.P) row[c] = norm_chunk(row[c], wv[c], ih, il);
     }
     for (int i = tid; i < (rows_out - p.M) * r.nch; i += blockDim.x) {
         const int m = p.M + i / r.nch, c = i - (i / r.nch) * r.nch;
@@ -574,7 +705,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[kMaxStreamWarps * 32];   // norm: one partial sum per thread
-    __shared__ float inv_s[MB];
+    __shared__ float inv_s[2 * MB];                // norm: (inv_hi, inv_lo) per row
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.stages, KS = p.KS, K = p.K, nseg = p.nseg;
@@ -693,7 +824,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
         XRows xr;
         if (p.fused) x_prefetch_rows(p, rm, xr);
         prologue_wait(pro_bar);
-        float ss;
+        float2 ss;
         if (p.fused) {
             if (threadIdx.x == 0) fused_arrive(p);
             ss = add_rows_in_place(p, rm, h_s, K, xr);
@@ -887,9 +1018,10 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
 // So each warp streams: [head of its last group, if cut] [whole groups]
 // [tail of its first group, if cut].  Heads never wait; a tail waits only on
 // a lower warp, so the hand-offs cannot deadlock, and every output's
-// arithmetic is independent of where its row falls.  Within a segment, even
-// and odd k16 steps go to two accumulator chains (halving the dependent MMA
-// chain), added in the epilogue.
+// arithmetic is independent of where its row falls.  Each segment's MMAs
+// form one chain from zero, which is then added (round to nearest) into the
+// group's fp32 totals: the tensor core's own accumulation need not round to
+// nearest, and its error would otherwise grow with K.
 //
 // Shared memory (dynamic):  [0, 1024)            mbarriers (ring, prologue, hand-off)
 //                           [off_h, off_s)       h_s[M + 1][K + 8] bf16 (row M = 0; no row M at M = 16)
@@ -940,7 +1072,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ float red[(kMaxStreamWarps + 1) * 32];   // norm: one partial sum per thread
-    __shared__ float inv_s[kMaxM];
+    __shared__ float inv_s[2 * kMaxM];                  // norm: (inv_hi, inv_lo) per row
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.stages, KS = p.KS, K = p.K, nseg = p.nseg;
@@ -1101,7 +1233,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         XRows xr;
         if (p.fused) x_prefetch_rows(p, rm, xr);
         prologue_wait(pro_bar);
-        float ss;
+        float2 ss;
         if (p.fused) {
             if (threadIdx.x == 0) fused_arrive(p);
             ss = add_rows_in_place(p, rm, h_s, HS, xr);
@@ -1144,7 +1276,10 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         return;
     }
 
-    // two chains per matrix: even k16 steps in *0, odd ones in *1
+    // per matrix: *0 the unit's MMA chain, started from zero at every unit;
+    // *1 the fp32 total, to which each unit's chain is added once (round to
+    // nearest).  The tensor core's own accumulation is not specified to round
+    // to nearest, so its chains stay at most one segment (<= 15 MMAs) long.
     float g0[4] = {0.f, 0.f, 0.f, 0.f}, g1[4] = {0.f, 0.f, 0.f, 0.f};
     float v0[4] = {0.f, 0.f, 0.f, 0.f}, v1[4] = {0.f, 0.f, 0.f, 0.f};
     float *const parked = reinterpret_cast<float *>(smem + p.off_piece);
@@ -1215,28 +1350,20 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
             const uint16_t *wg = ring + st * stage_elems + b_off;
             const uint16_t *wu = wg + R * RS;
             const uint16_t *ha = a_base + (k0 - k_lo);
-            int kk = 0;
 #pragma unroll 2
-            for (; kk + 1 < nk; kk += 2) {
+            for (int kk = 0; kk < nk; ++kk) {
                 uint32_t a0r, a1r, a2r, a3r, b0, b1, c0, c1r;
                 ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16);
                 ldmatrix_x2(b0, b1, wg + kk * 16);
                 ldmatrix_x2(c0, c1r, wu + kk * 16);
                 mma_bf16_16x8x16(g0, a0r, a1r, a2r, a3r, b0, b1);
                 mma_bf16_16x8x16(v0, a0r, a1r, a2r, a3r, c0, c1r);
-                ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16 + 16);
-                ldmatrix_x2(b0, b1, wg + kk * 16 + 16);
-                ldmatrix_x2(c0, c1r, wu + kk * 16 + 16);
-                mma_bf16_16x8x16(g1, a0r, a1r, a2r, a3r, b0, b1);
-                mma_bf16_16x8x16(v1, a0r, a1r, a2r, a3r, c0, c1r);
             }
-            if (kk < nk) {
-                uint32_t a0r, a1r, a2r, a3r, b0, b1, c0, c1r;
-                ldmatrix_x4(a0r, a1r, a2r, a3r, ha + kk * 16);
-                ldmatrix_x2(b0, b1, wg + kk * 16);
-                ldmatrix_x2(c0, c1r, wu + kk * 16);
-                mma_bf16_16x8x16(g0, a0r, a1r, a2r, a3r, b0, b1);
-                mma_bf16_16x8x16(v0, a0r, a1r, a2r, a3r, c0, c1r);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {   // the unit's chain into the totals
+                g1[q] = __fadd_rn(g1[q], g0[q]);
+                v1[q] = __fadd_rn(v1[q], v0[q]);
+                g0[q] = v0[q] = 0.f;
             }
             __syncwarp();
             if (i + S < n_total) {
@@ -1310,8 +1437,8 @@ template <bool NORM>
 __global__ void __launch_bounds__(256) glu_generic_kernel(const GluParams p)
 {
     extern __shared__ __align__(16) unsigned char smem_g[];
-    __shared__ float red[kMaxWarps][kMaxM];
-    __shared__ float inv_s[kMaxM];
+    __shared__ float2 red[kMaxWarps][kMaxM];
+    __shared__ float inv_s[2 * kMaxM];
     grid_dependency_wait();
     grid_launch_dependents();
     const uint16_t *hp = p.h;

@@ -20,3 +20,26 @@ def pytest_configure(config):
 def oracle_lib():
     import oracle
     return oracle.load()
+
+
+@pytest.fixture(autouse=True)
+def _parity_label(request):
+    import tolerance
+    tolerance.CURRENT_TEST[0] = request.node.nodeid
+    yield
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """Writes every parity comparison of the session (label, statistics,
+    verdict) to gpurun_out/parity_stats.json, or to $MBGLU_PARITY_STATS."""
+    import json
+    import tolerance
+    if not tolerance.RECORDS:
+        return
+    path = os.environ.get("MBGLU_PARITY_STATS", os.path.join(ROOT, "gpurun_out", "parity_stats.json"))
+    try:
+        os.makedirs(os.path.dirname(path), exist_ok=True)
+        with open(path, "w") as f:
+            json.dump(tolerance.RECORDS, f, indent=0)
+    except OSError:
+        pass

@@ -1,0 +1,162 @@
+"""The normed row h of add_rmsnorm_glu is correctly rounded on the GPU: the
+kernels' arithmetic (double-float statistic, Newton-refined 1/sqrt, an fp32
+element with a double-float re-evaluation near bf16 midpoints) emulated here
+in IEEE binary32 on the CPU gives the oracle's h bit for bit, while the plain
+fp32 chain does not.  CPU only.
+"""
+import numpy as np
+import pytest
+
+import glu_inputs as gi
+import oracle
+
+f32 = np.float32
+
+
+def _r(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float32)
+
+
+def _fma(a, b, c):
+    """a*b + c rounded once to binary32 (a*b is exact in binary64; the sums
+    used here are exact or far below the result's ulp)."""
+    return _r(np.asarray(a, np.float64) * np.asarray(b, np.float64) + np.asarray(c, np.float64))
+
+
+def _two_sum(a, b):
+    s = _r(a + b)
+    bp = _r(s - a)
+    e = _r(_r(a - _r(s - bp)) + _r(b - bp))
+    return s, e
+
+
+def _df_add(hi, lo, bhi, blo):
+    t, e = _two_sum(hi, bhi)
+    e = _r(e + _r(lo + blo))
+    h = _r(t + e)
+    return h, _r(e - _r(h - t))
+
+
+def _rsqrt_approx(v, skew):
+    """An approximate reciprocal square root: the binary32 value off by `skew`
+    ulps, as a hardware approximation may be."""
+    y = _r(1.0 / np.sqrt(np.asarray(v, np.float64)))
+    return (y.view(np.int32) + np.int32(skew)).view(np.float32)
+
+
+def _norm_inv(hi, lo, K, eps, skew):
+    kf = f32(K)
+    q = _r(hi / kf)
+    rem = _fma(-q, kf, hi)
+    vh, vl = q, _r(_r(rem + lo) / kf)
+    vh, vl = _df_add(vh, vl, f32(eps), f32(0))
+    y = _rsqrt_approx(vh, skew)
+    y2 = _r(y * y)
+    y2l = _fma(y, y, -y2)
+    t = _r(vh * y2)
+    tl = _fma(vl, y2, _fma(vh, y2l, _fma(vh, y2, -t)))
+    e = _r(_r(f32(1) - t) - tl)
+    c = _r(_r(f32(0.5) * y) * e)
+    ih = _r(y + c)
+    return ih, _r(c - _r(ih - y))
+
+
+def _rne_bits(x):
+    """binary32 -> bf16 bits, round to nearest even (finite inputs)."""
+    b = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _norm_elem(sv, w, ih, il, fallback=True):
+    v = _r(_r(sv * ih) * _r(f32(1) + w))
+    out = _rne_bits(v)
+    if not fallback:
+        return out
+    low = v.view(np.uint32) & np.uint32(0xFFFF)
+    near = (low.astype(np.int64) - 0x7FFB >= 0) & (low.astype(np.int64) - 0x7FFB <= 10)
+    if near.any():
+        s_, w_ = sv[near], w[near]
+        ih_ = np.broadcast_to(ih, sv.shape)[near]
+        il_ = np.broadcast_to(il, sv.shape)[near]
+        ah, al = _two_sum(f32(1), w_)
+        ph = _r(s_ * ih_)
+        pl = _fma(s_, il_, _fma(s_, ih_, -ph))
+        qh = _r(ph * ah)
+        ql = _fma(ph, al, _fma(pl, ah, _fma(ph, ah, -qh)))
+        t = _r(qh + ql)
+        l = _r(ql - _r(t - qh))
+        b = t.view(np.uint32)
+        res = _rne_bits(t)
+        tie = ((b & 0xFFFF) == 0x8000) & (l != 0)
+        away = (l > 0) == (t > 0)
+        res = np.where(tie, ((b >> 16) + away.astype(np.uint32)).astype(np.uint16), res)
+        out = out.copy()
+        out[near] = res
+    return out
+
+
+def kernel_norm(s_bits, w_bits, eps, skew=0, fallback=True, stat="twosum"):
+    """h bits [M, K] the way the kernels compute them.  stat: "twosum" (the
+    kernels' double-float sum), "plain" (an fp32 sum) or "f64" (a binary64 sum
+    split into two binary32 words: as exact as "twosum", and fast)."""
+    sv = (np.asarray(s_bits, np.uint32) << 16).view(np.float32)
+    w = (np.asarray(w_bits, np.uint32) << 16).view(np.float32)
+    M, K = sv.shape
+    out = np.empty((M, K), np.uint16)
+    for m in range(M):
+        sq = _r(sv[m] * sv[m])                     # exact
+        hi, lo = f32(0), f32(0)
+        if stat == "twosum":
+            for k in range(K):                      # TwoSum accumulation (any order is as good)
+                hi, e = _two_sum(hi, sq[k])
+                lo = _r(lo + e)
+        elif stat == "plain":
+            for k in range(K):
+                hi = _r(hi + sq[k])
+        else:
+            t = float(np.sum(sq.astype(np.float64)))
+            hi = f32(t)
+            lo = f32(t - float(hi))
+        ih, il = _norm_inv(hi, lo, K, eps, skew)
+        out[m] = _norm_elem(sv[m], w, ih, il, fallback)
+    return out
+
+
+def _case(M=48, K=2560, seed=11):
+    x = gi.bits(gi.normal_bf16((M, K), 1.0, seed, "ne-x"))
+    r = gi.bits(gi.normal_bf16((M, K), 1.0, seed, "ne-r"))
+    w = gi.bits(gi.normal_bf16((K,), 0.1, seed, "ne-w"))
+    g = gi.bits(gi.normal_bf16((1, K), 0.02, seed, "ne-g"))
+    _, s, h = oracle.add_rmsnorm_glu(x, r, w, 1e-6, g, g, "hf")
+    return s, w, h
+
+
+@pytest.fixture(scope="module")
+def case():
+    return _case()
+
+
+@pytest.mark.parametrize("skew", [-2, 0, 2])
+def test_kernel_norm_arithmetic_gives_the_correctly_rounded_h(case, skew):
+    s, w, h = case
+    got = kernel_norm(s, w, 1e-6, skew=skew)
+    bad = np.flatnonzero(got != h)
+    assert bad.size == 0, (bad[:8], got.reshape(-1)[bad[:8]], h.reshape(-1)[bad[:8]])
+
+
+def test_plain_fp32_chain_misrounds_some_elements(case):
+    """The reason for the double-float steps: without them h differs."""
+    s, w, h = case
+    plain = kernel_norm(s, w, 1e-6, fallback=False, stat="plain")
+    assert 0 < np.sum(plain != h) < 1e-3 * h.size
+
+
+def test_the_midpoint_fallback_is_needed():
+    """With an exact statistic but no re-evaluation near midpoints, the fp32
+    element (a few ulps of error) still misrounds now and then; with it, h is
+    exact on ~2M elements."""
+    s, w, h = _case(M=800, seed=12)
+    nofb = kernel_norm(s, w, 1e-6, fallback=False, stat="f64")
+    assert np.sum(nofb != h) > 0
+    got = kernel_norm(s, w, 1e-6, stat="f64", skew=1)
+    assert np.array_equal(got, h)

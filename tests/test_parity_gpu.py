@@ -392,8 +392,9 @@ def check_norm(x, r, w, g, u, mode, eps=1e-6, what="", variant=None, ws=None):
         assert mb.last_variant() == variant
     ref, res, hn = oracle.add_rmsnorm_glu(gi.bits(x), gi.bits(r), gi.bits(w), eps, gi.bits(g), gi.bits(u), mode)
     assert np.array_equal(gi.bits(rd.cpu()), res), f"residual {what}"
+    # the kernels' h is the correctly rounded one (the oracle's hn), so the
+    # GEMV part carries only its own fp32 accumulation
     _, diag = oracle.glu_gemv(hn, gi.bits(g), gi.bits(u), mode, diagnostics=True)
-    diag["dG_extra"], diag["dU_extra"] = tol.norm_rounding_slack(res, gi.bits(w), eps, gi.bits(g), gi.bits(u))
     K = x.shape[1]
     return parity(gi.bits(out.cpu()), ref, (tol.conditioning_floor(diag, K, mode), diag, K, mode), what)
 
@@ -464,8 +465,6 @@ def test_add_rmsnorm_glu_strided_weights_and_out(M, single):
     ref_o, _, hn = oracle.add_rmsnorm_glu(gi.bits(x.cpu()), gi.bits(r), gi.bits(w.cpu()), 1e-6, gi.bits(g.cpu()),
                                           gi.bits(u.cpu()), "hf")
     _, diag = oracle.glu_gemv(hn, gi.bits(g.cpu()), gi.bits(u.cpu()), "hf", diagnostics=True)
-    diag["dG_extra"], diag["dU_extra"] = tol.norm_rounding_slack(gi.bits(r_odd.cpu()), gi.bits(w.cpu()), 1e-6,
-                                                                 gi.bits(g.cpu()), gi.bits(u.cpu()))
     tol.assert_parity(gi.bits(out_odd.cpu()), ref_o, tol.conditioning_floor(diag, K, "hf"), "odd stride",
                       diag=diag, K=K, mode="hf")
 
@@ -568,8 +567,10 @@ def _layer(name, layer):
     return gi.layer_weights(gi.WORKLOADS[name], layer)
 
 
+# every workload at every batch in BOTH modes (the bar holds for each mode,
+# whichever mode the workload is timed in)
 FULL_CASES = [(w.name, M, mode) for w in gi.WORKLOADS.values() if w.op in ("glu_gemv", "add_rmsnorm_glu")
-              for M in w.Ms for mode in w.modes]
+              for M in w.Ms for mode in ("fused", "hf")]
 
 
 @pytest.mark.parametrize("name,M,mode", FULL_CASES)

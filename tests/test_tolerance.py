@@ -86,7 +86,8 @@ def test_hf_gate_flip_is_admissible_only_inside_the_box():
                 sim = flat.copy()
                 sim[i] = flipped
                 st = tol.compare(sim.reshape(out.shape), out, tau, diag, K, "hf")
-                assert st["alt_rounding"] == 1 and st["max_rel_elsewhere"] == 0.0
+                # accepted: within 1e-2 relative, or (steeper) through the error box
+                assert st["outside_1ulp"] == 1 and st["alt_rounding"] <= 1 and st["max_rel_elsewhere"] <= 1e-2
                 accepted += 1
         elif not any(reach) and dU[i] < abs(U[i]) * 2.0 ** -12:   # u well conditioned
             o = tol.ordered(flat[i:i + 1])[0]
@@ -124,10 +125,10 @@ def test_plausible_kernel_mistakes_fail(mode, mistake):
 
 
 @pytest.mark.parametrize("mode", ["hf", "fused"])
-def test_fp32_norm_rounding_is_covered_by_the_slack(mode):
-    """h from an fp32 norm (another reduction order) may differ from the
-    oracle's fp64 h in a few elements; the GEMV on it must still pass."""
-    import torch
+def test_norm_path_with_the_exact_h_meets_the_stated_bar(mode):
+    """add_rmsnorm_glu on the kernels' h (the correctly rounded one, which the
+    oracle also computes) followed by an fp32 GEMV in another order passes the
+    stated bar with no allowance for the norm."""
     M, N, K = 13, 1500, 2048
     x = gi.normal_bf16((M, K), 1.0, 13, "an-x")
     r = gi.normal_bf16((M, K), 1.0, 13, "an-r")
@@ -135,12 +136,29 @@ def test_fp32_norm_rounding_is_covered_by_the_slack(mode):
     g = gi.bits(gi.normal_bf16((N, K), K ** -0.5, 13, "an-g"))
     u = gi.bits(gi.normal_bf16((N, K), K ** -0.5, 13, "an-u"))
     ref, res, h64 = oracle.add_rmsnorm_glu(gi.bits(x), gi.bits(r), gi.bits(w), 1e-6, g, u, mode)
+    sim = _fp32_chain(h64, g, u, mode)
+    _, diag = oracle.glu_gemv(h64, g, u, mode, diagnostics=True)
+    st = tol.compare(sim, ref, tol.conditioning_floor(diag, K, mode), diag, K, mode)
+    assert tol.passes(st), st
+
+
+def test_an_fp32_norm_misses_the_stated_bar_in_hf_mode():
+    """Why the kernels round h correctly: an fp32 norm chain (another order)
+    flips a few elements of h, and in HF mode each flip re-rounds g or u on a
+    few percent of its row's outputs; on this case that alone takes the
+    outputs within 1 ULP of the oracle below 99.9%."""
+    import torch
+    M, N, K = 13, 1500, 2048
+    x = gi.normal_bf16((M, K), 1.0, 13, "an-x")
+    r = gi.normal_bf16((M, K), 1.0, 13, "an-r")
+    w = gi.normal_bf16((K,), 0.1, 13, "an-w")
+    g = gi.bits(gi.normal_bf16((N, K), K ** -0.5, 13, "an-g"))
+    u = gi.bits(gi.normal_bf16((N, K), K ** -0.5, 13, "an-u"))
+    ref, res, h64 = oracle.add_rmsnorm_glu(gi.bits(x), gi.bits(r), gi.bits(w), 1e-6, g, u, "hf")
     s = gi.from_bits(res).float()
     ss = (s * s).reshape(M, 256, K // 256).sum(-1).sum(-1, keepdim=True)   # another fp32 order
     inv = 1.0 / torch.sqrt(ss / K + 1e-6)
     h32 = gi.bits(((s * inv) * (1.0 + w.float())).to(torch.bfloat16))
-    sim = _fp32_chain(h32, g, u, mode)
-    _, diag = oracle.glu_gemv(h64, g, u, mode, diagnostics=True)
-    diag["dG_extra"], diag["dU_extra"] = tol.norm_rounding_slack(res, gi.bits(w), 1e-6, g, u)
-    st = tol.compare(sim, ref, tol.conditioning_floor(diag, K, mode), diag, K, mode)
-    assert tol.passes(st), st
+    assert np.sum(h32 != h64) > 0
+    st = tol.compare(_fp32_chain(h32, g, u, "hf"), ref)
+    assert st["within_1ulp_of_oracle"] < tol.STRICT_FLOOR, st

@@ -154,7 +154,6 @@ def test_add_rmsnorm_glu_row_blocks(M, path):
     ref, res, hn = oracle.add_rmsnorm_glu(gi.bits(x), gi.bits(r), gi.bits(w), 1e-6, gi.bits(g), gi.bits(u), mode)
     assert np.array_equal(gi.bits(rd.cpu()), res), "residual"
     _, diag = oracle.glu_gemv(hn, gi.bits(g), gi.bits(u), mode, diagnostics=True)
-    diag["dG_extra"], diag["dU_extra"] = tol.norm_rounding_slack(res, gi.bits(w), 1e-6, gi.bits(g), gi.bits(u))
     diag["acc"] = "mma"
     tol.assert_parity(gi.bits(out.cpu()), ref, tol.conditioning_floor(diag, K, mode), f"{path} M={M}",
                       diag=diag, K=K, mode=mode)

@@ -16,21 +16,24 @@ Readings used here:
         tau = |SiLU'(G)*U|*dg + |SiLU(G)|*du  (HF mode adds 2^-8*|G| to dg
               and 2^-8*|U| to du for the bf16 roundings of g and u).
     An output with |ref| < tau sits where u or SiLU(g)*u cancels.
-  * Rounding decisions taken from a sum (HF mode rounds g and u to bf16
-    before SiLU) may legitimately go either way when the exact sum lies
-    within dg (du) of a rounding midpoint; SiLU can then amplify one flip of
-    gb into a few output ULPs (its log-slope is about 4 at g = -5).  An output
-    outside 1 ULP is therefore also accepted when it lies within 1 ULP of the
-    range the mode's chain takes over g in [G - dg, G + dg], u in
-    [U - du, U + du] (interval arithmetic over the monotone pieces, SiLU's
-    minimum near g = -1.2785 included).  These are counted as "alt_rounding"
-    and, being correct results, count toward the 99.9%; plain 1-ULP agreement
-    with the oracle's own result must still reach 99%.
-  * add_rmsnorm_glu: the normed h is rounded to bf16 from an fp32 chain
-    (the pages fix the norm's precision at fp32).  Elements whose exact value
-    lies within that chain's error of a bf16 midpoint may round either way;
-    norm_rounding_slack() widens dg, du per row by sum_k ulp(h_k)*|w_nk| over
-    those elements.
+  * The stated bar is enforced literally: at least 99.9% of outputs lie
+    within 1 ULP of the oracle's own result (STRICT_FLOOR), for every op
+    and both modes.
+  * "Elsewhere" (the at most 0.1% outside 1 ULP): relative error floored at
+    tau must be <= 1e-2, unless the output is explained by the fp32 error
+    box: it lies within 1 ULP of the range the mode's chain takes over
+    g in [G - dg, G + dg], u in [U - du, U + du] (interval arithmetic over
+    the monotone pieces, SiLU's minimum near g = -1.2785 included).  Such
+    outputs are counted as "alt_rounding" and bounded: alt_rounding / n <=
+    ALT_MAX_FRAC.  Two readings produce them:
+      - HF mode rounds g and u to bf16 before SiLU: where the exact sum lies
+        within dg (du) of a bf16 midpoint both neighbours are correct, and
+        SiLU's log-slope (about 4 at g = -5) can turn one flip of gb into a
+        few output ULPs;
+      - an output so cancelled (|ref| < tau) that fp32 accumulation alone
+        can move it by its own size ("ill_conditioned").
+    Measured on the GPU: about 1e-4 of outputs in HF mode and 5e-5 in
+    FUSED mode (outlier-weight workloads), hence the bound 5e-4.
   * Non-finite outputs must match exactly.
 """
 from __future__ import annotations
@@ -81,7 +84,7 @@ def accumulation_gamma(K: int, diag=None) -> float:
 def conditioning_floor(diag, K: int, mode: str) -> np.ndarray:
     G, U, Ag, Au = diag["G"], diag["U"], diag["Ag"], diag["Au"]
     gamma = accumulation_gamma(K, diag)
-    dg, du = gamma * Ag + diag.get("dG_extra", 0.0), gamma * Au + diag.get("dU_extra", 0.0)
+    dg, du = gamma * Ag, gamma * Au
     if mode == "hf":
         dg = dg + 2.0 ** -8 * np.abs(G)
         du = du + 2.0 ** -8 * np.abs(U)
@@ -120,9 +123,6 @@ def alternative_ok(gpu_bits, diag, K: int, mode: str, idx) -> np.ndarray:
     gamma = accumulation_gamma(K, diag)
     dG = gamma * diag["Ag"].reshape(-1)[idx]
     dU = gamma * diag["Au"].reshape(-1)[idx]
-    if "dG_extra" in diag:
-        dG = dG + np.broadcast_to(diag["dG_extra"], diag["G"].shape).reshape(-1)[idx]
-        dU = dU + np.broadcast_to(diag["dU_extra"], diag["U"].shape).reshape(-1)[idx]
     f, b = bf16_bits_to_f64, _bf16_bits
     if mode == "hf":
         # rounding is monotone: the reachable gb, ub are the roundings of the ends
@@ -150,74 +150,59 @@ def compare(gpu_bits, ref_bits, tau=None, diag=None, K=None, mode=None) -> dict:
     nonfinite_mismatch = int(np.sum((~fin_r | ~fin_g) & (gpu_bits != ref_bits)))
     d = ulp_distance(gpu_bits, ref_bits)
     within = (d <= 1) & fin_r & fin_g
-    frac = float(np.mean(within | (~fin_r & (gpu_bits == ref_bits)))) if n else 1.0
+    strict = float(np.mean(within | (~fin_r & (gpu_bits == ref_bits)))) if n else 1.0
     floor = np.abs(r) if tau is None else np.maximum(np.abs(r), np.asarray(tau))
     with np.errstate(divide="ignore", invalid="ignore"):
         raw = np.where(floor > 0, np.abs(g - r) / floor, np.where(g == r, 0.0, np.inf))
     rel = np.where(within | ~fin_r, 0.0, raw)
     rel = np.where(np.isnan(rel), np.inf, rel)
     alt = 0
-    strict = frac
-    if diag is not None and np.any(rel > 0):
-        idx = np.flatnonzero((rel > 0).reshape(-1))
+    if diag is not None and np.any(rel > MAX_REL_ELSEWHERE):
+        idx = np.flatnonzero((rel > MAX_REL_ELSEWHERE).reshape(-1))
         okf = alternative_ok(gpu_bits, diag, K, mode, idx)
         flat = rel.reshape(-1).copy()
         flat[idx[okf]] = 0.0
         alt = int(okf.sum())
         rel = flat.reshape(rel.shape)
-        frac = frac + alt / n
-    ill = 0 if tau is None else int(np.sum(~within & fin_r & (np.abs(r) < np.asarray(tau))))
+    outside = ~within & fin_r
+    ill = 0 if tau is None else int(np.sum(outside & (np.abs(r) < np.asarray(tau))))
     return {
         "n": n,
         "exact_frac": float(np.mean(d == 0)) if n else 1.0,
-        "within_1ulp_frac": frac,          # of a correct result (oracle or admissible alternative)
-        "within_1ulp_of_oracle": strict,
+        "within_1ulp_of_oracle": strict,   # the stated bar: >= 0.999
+        "outside_1ulp": int(np.sum(outside)),
         "max_ulp": int(d.max()) if n else 0,
-        "max_rel_elsewhere": float(rel.max()) if n else 0.0,
+        "max_rel_elsewhere": float(rel.max()) if n else 0.0,   # outputs no reading explains
         "ill_conditioned": ill,
         "alt_rounding": alt,
         "nonfinite_mismatch": nonfinite_mismatch,
     }
 
 
-STRICT_FLOOR = 0.99   # sanity floor on plain 1-ULP agreement with the oracle's own result
+STRICT_FLOOR = 0.999    # 1 ULP of the oracle's own result on >= 99.9% of outputs
+ALT_MAX_FRAC = 5e-4     # outputs accepted through the fp32 error box (HF flips, cancellation)
 
 
 def passes(stats: dict) -> bool:
-    return (stats["within_1ulp_frac"] >= ULP_FRAC_REQUIRED
-            and stats.get("within_1ulp_of_oracle", 1.0) >= STRICT_FLOOR
+    n = max(1, stats["n"])
+    return (stats["within_1ulp_of_oracle"] >= STRICT_FLOOR
             and stats["max_rel_elsewhere"] <= MAX_REL_ELSEWHERE
+            and stats["alt_rounding"] <= ALT_MAX_FRAC * n
             and stats["nonfinite_mismatch"] == 0)
+
+
+# Every comparison assert_parity makes is kept here with its label; the test
+# session writes them out (tests/conftest.py) so the statistics behind each
+# "pass" can be read afterwards.
+RECORDS = []
+CURRENT_TEST = [""]
 
 
 def assert_parity(gpu_bits, ref_bits, tau=None, what="", diag=None, K=None, mode=None):
     st = compare(gpu_bits, ref_bits, tau, diag, K, mode)
+    RECORDS.append({"test": CURRENT_TEST[0], "what": what, **st, "pass": passes(st)})
     assert passes(st), f"parity failed {what}: {st}"
     return st
-
-
-def norm_rounding_slack(s_bits, norm_w_bits, eps, gate_bits, up_bits):
-    """(dG_extra, dU_extra) [M, N]: how far the GEMV's dot products may move
-    when the fp32 norm rounds an element of h to the other bf16 neighbour.
-    The kernels' statistic sums K/256 terms per thread, then 5 + 16 levels;
-    the scale adds sqrt, division and two products: eps_rel below bounds it."""
-    sv = bf16_bits_to_f64(s_bits)
-    w = bf16_bits_to_f64(norm_w_bits)
-    M, K = sv.shape
-    var = np.mean(sv * sv, axis=1, keepdims=True)
-    v = sv / np.sqrt(var + float(np.float32(eps))) * (1.0 + w)[None, :]
-    eps_rel = (-(-K // 256) + 32) * 2.0 ** -24
-    av = np.abs(v)
-    with np.errstate(divide="ignore"):
-        e = np.floor(np.log2(np.where(av > 0, av, 1.0)))
-    ulp = np.exp2(np.maximum(e, -126.0) - 7.0)
-    r = np.round(v / ulp)                      # nearest multiple of ulp (tie rule irrelevant here)
-    mid_dist = np.abs(np.abs(v / ulp - r) - 0.5) * ulp
-    amb = (mid_dist <= eps_rel * av + 1e-300) & (av > 0)
-    slack = np.where(amb, ulp, 0.0)            # [M, K]
-    dG = slack @ np.abs(bf16_bits_to_f64(gate_bits)).T
-    dU = slack @ np.abs(bf16_bits_to_f64(up_bits)).T
-    return dG, dU
 
 
 # ---------------------------------------------------------------------------
