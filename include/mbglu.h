@@ -79,8 +79,8 @@ typedef uint16_t mbglu_bf16;   /* raw bf16 bits */
  *                    F.silu(h @ Wg.T) * (h @ Wu.T) materialises it:
  *                    gb = bf16(g), ub = bf16(u), sb = bf16(SiLU(gb)) with SiLU
  *                    in fp32, out = bf16(sb * ub).
- *                    [8602/PlanB] b>1 fallback; [9057/Changes] "Restore HF's
- *                    intermediate BF16 rounding in ... GLU".
+ *                    [8602/PlanB] b>1 fallback; [9057/Changes]: the GLU
+ *                    keeps the bf16 roundings of HF's own code.
  * SiLU(x) = x / (1 + exp(-x)) with the precise expf and IEEE division,
  * evaluated from e^-|x| so that no intermediate overflows (silu_mul takes a
  * correctly rounded reciprocal in place of the division).
@@ -166,8 +166,8 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh,
 
 /*
  * add_rmsnorm_glu -- residual add + zero-centred RMSNorm, then glu_gemv on
- * the normed rows.  [9057/Changes] "Restore HF's intermediate BF16 rounding in
- * residual/RMSNorm ... construct zero-centered norm scales in FP32".
+ * the normed rows.  [9057/Changes]: the residual add and the RMSNorm keep
+ * HF's bf16 roundings, and the zero-centred scale (1 + w) is formed in fp32.
  *
  *   x         [M, K] bf16, contiguous                        (read)
  *   residual  [M, K] bf16, contiguous                        (read, then
@@ -233,9 +233,9 @@ mbglu_status add_rmsnorm_glu_ws(const mbglu_bf16 *x, mbglu_bf16 *residual,
  * add_rmsnorm_glu_ws) on weights and an output with explicit row strides:
  * gate_w and up_w [N][K] with row strides ld_gate, ld_up >= K, out [M][N]
  * with row stride ldo >= N (elements), e.g. views into a packed parameter
- * buffer or a wider activation buffer.  PR #9057, commit on decode attention
- * and the "real row stride": kernels take the true stride instead of assuming
- * a contiguous tensor, and reject a stride that cannot hold the row.  x,
+ * buffer or a wider activation buffer.  PR #9057, the decode-attention
+ * stride commit: kernels take the true row stride instead of assuming a
+ * contiguous tensor, and reject a stride that cannot hold the row.  x,
  * residual and norm_w stay contiguous.  workspace: NULL runs the two-kernel
  * path; otherwise as add_rmsnorm_glu_ws (MBGLU_WORKSPACE_BYTES, 16-byte
  * aligned, zero before first use).  Errors as add_rmsnorm_glu_ws, plus
@@ -264,8 +264,10 @@ mbglu_status add_rmsnorm_glu_strided(const mbglu_bf16 *x, mbglu_bf16 *residual,
  * than that returns MBGLU_ERR_SHAPE.  It calls no cudaMalloc, cudaFree or
  * other allocating routine.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) and keeps it: make that first call before any
- *     stream capture on that device.
+ *     (cudaGetSymbolAddress) and keeps it with the identity of the device's
+ *     context: make that first call before any stream capture on that device.
+ *     After a cudaDeviceReset the next call sees a new context and looks the
+ *     address up again (so that call, too, belongs outside stream capture).
  *   - Each call clears the counters with a stream-ordered cudaMemsetAsync
  *     before its kernel, because the array keeps what the last call left.
  *   - All calls share the one array: calls that may overlap on the GPU (on
@@ -309,11 +311,11 @@ mbglu_status silu_mul(const mbglu_bf16 *x, int64_t ldx, mbglu_bf16 *out, int64_t
 
 /*
  * gdn_gates -- the decay and write gates of the gated-delta-net layers, which
- * the same segment-KI work fuses beside the GLU.  DeepSpeed PR #8602 commit
- * adding gdn_gates ("beta=sigmoid(b) and g=-exp(A_log)*softplus(a+dt_bias)
- * with fp32 math and the numerically stable softplus branch", strided input);
- * PR #9057 "Changes" ("Preserve FP32 GDN decay gates").  For token t < T and
- * head j < H:
+ * the same segment-KI work fuses beside the GLU.  DeepSpeed PR #8602, the
+ * commit adding gdn_gates: a sigmoid write gate and the decay gate
+ * -exp(A_log) * softplus(a + dt_bias), computed in fp32 with the stable
+ * softplus form, on strided input; PR #9057 "Changes": the decay gates stay
+ * fp32.  For token t < T and head j < H:
  *   x = a[t][j] + dt_bias[j]                 (fp32 addition; a is bf16)
  *   g[t][j]    = -exp(A_log[j]) * softplus(x)   fp32, softplus(x) = log(1 + e^x)
  *                                                 in its stable form
@@ -377,6 +379,18 @@ int mbglu_last_cuda_error(void);
  * 6 gdn_gates, 7 row blocks (a batch above MBGLU_BLOCK_M: one of 1-4 per
  * block), 8 glu_backward. */
 int mbglu_last_variant(void);
+
+/* How many row blocks of the calling thread's last add_rmsnorm_glu* call ran
+ * as the single kernel (the workspace / no-allocation paths); 0 when every
+ * block took the two-kernel path or the call launched nothing. */
+int mbglu_last_single_kernel_blocks(void);
+
+/* Diagnostics: copies the first `count` ints of the current device's
+ * add_rmsnorm_glu_noalloc scratch array to host memory `words`, after a
+ * cudaDeviceSynchronize.  SYNCHRONOUS.  MBGLU_ERR_NULL for a null `words`,
+ * MBGLU_ERR_SHAPE for count < 0 or beyond MBGLU_NOALLOC_SCRATCH_BYTES,
+ * MBGLU_ERR_CUDA on a CUDA failure. */
+mbglu_status mbglu_noalloc_scratch_read(int *words, int count);
 
 /*
  * Reads and clears the device error word of the current device.  Kernels

@@ -28,7 +28,7 @@ EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu
            "mbglu_set_launch_policy",
            "mbglu_get_launch_policy",
            "mbglu_status_string", "mbglu_abi_version", "mbglu_last_cuda_error", "mbglu_last_variant",
-           "mbglu_read_device_error")
+           "mbglu_last_single_kernel_blocks", "mbglu_noalloc_scratch_read", "mbglu_read_device_error")
 POLICY_SERIAL, POLICY_PDL, POLICY_PREFETCH = 0, 1, 2
 
 _lib = None
@@ -70,6 +70,9 @@ def _bind(l):
     l.mbglu_abi_version.restype = i32
     l.mbglu_last_cuda_error.restype = i32
     l.mbglu_last_variant.restype = i32
+    l.mbglu_last_single_kernel_blocks.restype = i32
+    l.mbglu_noalloc_scratch_read.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
+    l.mbglu_noalloc_scratch_read.restype = i32
     l.mbglu_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     l.mbglu_read_device_error.restype = i32
     l.mbglu_set_launch_policy.argtypes = [i32]
@@ -139,6 +142,21 @@ def glu_gemv(h, gate_w, up_w, out=None, mode="fused", stream=None):
     if st != 0:
         raise MbgluError(st, "glu_gemv")
     return out2.view(N) if squeeze else out
+
+
+def column_shard(N: int, world: int, rank: int):
+    """Rows [lo, hi) of gate_w and up_w -- and columns of out -- that rank
+    `rank` of `world` owns when the GLU GEMV is split column-parallel over N
+    (DeepSpeed PR #8602, "Architecture Notes": the gate/up projections are
+    column-parallel under AutoTP and the segment needs no communication; the
+    all-reduce belongs to the row-parallel down projection after it).  The
+    shares are balanced (sizes differ by at most one row), disjoint, in rank
+    order, and cover [0, N).  Each rank then calls glu_gemv (or
+    add_rmsnorm_glu, whose prologue every rank repeats) on its rows of both
+    weights and writes out[:, lo:hi]; no collective is involved."""
+    if world < 1 or not 0 <= rank < world or N < 0:
+        raise ValueError(f"bad split: N={N}, world={world}, rank={rank}")
+    return (N * rank) // world, (N * (rank + 1)) // world
 
 
 def glu_backward(h, gate_w, up_w, dout, grad_h=None, grad_gate=None, grad_up=None, want_h=True, want_w=True,

@@ -42,6 +42,10 @@ struct BwdParams {
     uint16_t *grad_up;
     int64_t ldgu;
     int M, N, K;
+    int ldm;                // row stride of dG, dU (N; the rows kernel's block offset applies to the pointers)
+    int R, S;               // glu_bwd_rows_kernel: rows per stage, stages in the ring
+    uint32_t off_ring;      // glu_bwd_rows_kernel: ring offset in dynamic shared memory
+    int rows_cta;           // glu_bwd_rows_kernel: largest row share of a CTA
     int vec_w;              // gate, up rows 8-byte aligned: 4-element loads
     int vec_out;            // grad_gate, grad_up rows and h 16-byte aligned, K % 8 == 0: 8-element access
     int h_smem;             // glu_bwd_w_kernel: h staged in shared memory
@@ -132,6 +136,145 @@ __global__ void __launch_bounds__(256) glu_bwd_h_kernel(const BwdParams q)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (k + i < q.K) dst[i] = acc[m][i] + red[(m * 4 + i) * 128 + c];
+            }
+        }
+    }
+}
+
+// grad_h partials by whole rows: the main path (operands 16-byte aligned,
+// K % 8 == 0).  CTA b owns a balanced share [n0, n1) of the N rows of both
+// weights and every column; thread t owns the 8-column chunks t, t + T, ...
+// (CPT of them, T = blockDim.x <= 512).  The share streams through a ring of
+// S stages of R rows each (gate rows, then up rows; one bulk copy per matrix
+// and stage when the rows are contiguous), LAST rows first: the first step
+// read this share in rising order and left its tail in L2 (evict-last), so
+// much of it is read back from there.  For each row n (descending), thread t
+// adds dG[m][n] Wg[n][k] + dU[m][n] Wu[n][k] into its fp32 accumulators,
+// m < M <= MB.  part[b][m][k] receives the CTA's sums;
+// glu_bwd_h_reduce_kernel adds the CTAs in order.  The share's dG and dU are
+// staged in shared memory after the dependency wait; the first S stages of
+// weights are requested before it.
+// Dynamic shared memory: [0, 256) stage barriers, [256, off_ring) dG and dU
+// of the share ([2][MB][rows_cta] fp32), [off_ring, ...) the ring.
+constexpr int kBwdRowsThreads = 512;   // glu_bwd_rows_kernel: most threads per CTA
+
+template <int MB, int CPT>
+__global__ void __launch_bounds__(kBwdRowsThreads, 1) glu_bwd_rows_kernel(const BwdParams q)
+{
+    extern __shared__ __align__(128) unsigned char bwd_smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(bwd_smem);
+    float *dg_s = reinterpret_cast<float *>(bwd_smem + 256);
+    float *du_s = dg_s + MB * q.rows_cta;
+    uint16_t *ring = reinterpret_cast<uint16_t *>(bwd_smem + q.off_ring);
+    const int b = blockIdx.x, G = gridDim.x, K = q.K, R = q.R, S = q.S;
+    const int n0 = static_cast<int>((static_cast<int64_t>(q.N) * b) / G);
+    const int n1 = static_cast<int>((static_cast<int64_t>(q.N) * (b + 1)) / G);
+    const int rows = n1 - n0, nblk = (rows + R - 1) / R;
+    const int64_t stage_elems = static_cast<int64_t>(2) * R * K;
+    const bool contig = q.ld_gate == K && q.ld_up == K;
+    const uint64_t policy = l2_policy_evict_first();
+
+    // block j: rows [lo, hi) with hi = n1 - j R
+    auto fill = [&](int j) {
+        const int hi = n1 - j * R, lo = max(n0, hi - R), nr = hi - lo;
+        const int st = j % S;
+        uint16_t *dst = ring + st * stage_elems;
+        const uint32_t bytes = static_cast<uint32_t>(nr) * static_cast<uint32_t>(K) * 2u;
+        mbar_arrive_expect_tx(&full[st], 2u * bytes);
+        if (contig) {
+            bulk_g2s(dst, q.gate + static_cast<int64_t>(lo) * K, bytes, &full[st], policy);
+            bulk_g2s(dst + static_cast<int64_t>(R) * K, q.up + static_cast<int64_t>(lo) * K, bytes, &full[st], policy);
+        } else {
+            for (int i = 0; i < nr; ++i) {
+                bulk_g2s(dst + static_cast<int64_t>(i) * K, q.gate + (lo + i) * q.ld_gate, K * 2u, &full[st], policy);
+                bulk_g2s(dst + static_cast<int64_t>(R + i) * K, q.up + (lo + i) * q.ld_up, K * 2u, &full[st],
+                         policy);
+            }
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < S; ++st) mbar_init(&full[st], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int j = 0; j < min(S, nblk); ++j) fill(j);   // weights only: before the dependency wait
+    grid_dependency_wait();                                 // dG, dU of the first step
+    for (int i = threadIdx.x; i < q.M * rows; i += blockDim.x) {
+        const int m = i / rows, r = i - m * rows;
+        dg_s[m * q.rows_cta + r] = q.dG[static_cast<int64_t>(m) * q.ldm + n0 + r];
+        du_s[m * q.rows_cta + r] = q.dU[static_cast<int64_t>(m) * q.ldm + n0 + r];
+    }
+    __syncthreads();
+
+    float2 acc[CPT][MB][4];
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc)
+#pragma unroll
+        for (int m = 0; m < MB; ++m)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[cc][m][k] = make_float2(0.0f, 0.0f);
+
+    for (int j = 0; j < nblk; ++j) {
+        const int st = j % S;
+        const uint32_t phase = static_cast<uint32_t>(j / S) & 1u;
+        if (!mbar_wait_bounded(&full[st], phase, kWaitLimitNs)) {
+            atomicExch(&g_device_error, kErrTimeout);
+            mbar_wait_bounded(&full[st], phase, kWaitLimitNs);
+        }
+        const int hi = n1 - j * R, lo = max(n0, hi - R);
+        const uint16_t *gs = ring + st * stage_elems;
+        const uint16_t *us = gs + static_cast<int64_t>(R) * K;
+        for (int i = hi - lo - 1; i >= 0; --i) {   // descending rows
+            const int r = lo - n0 + i;
+            float2 a2[MB], b2[MB];
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                const float a = m < q.M ? dg_s[m * q.rows_cta + r] : 0.0f;
+                const float bb = m < q.M ? du_s[m * q.rows_cta + r] : 0.0f;
+                a2[m] = make_float2(a, a);
+                b2[m] = make_float2(bb, bb);
+            }
+#pragma unroll
+            for (int cc = 0; cc < CPT; ++cc) {
+                const int col = 8 * (threadIdx.x + cc * blockDim.x);
+                if (col < K) {
+                    const uint4 g4 = *reinterpret_cast<const uint4 *>(gs + static_cast<int64_t>(i) * K + col);
+                    const uint4 u4 = *reinterpret_cast<const uint4 *>(us + static_cast<int64_t>(i) * K + col);
+                    const float2 gv[4] = {make_float2(bf16_lo(g4.x), bf16_hi(g4.x)),
+                                          make_float2(bf16_lo(g4.y), bf16_hi(g4.y)),
+                                          make_float2(bf16_lo(g4.z), bf16_hi(g4.z)),
+                                          make_float2(bf16_lo(g4.w), bf16_hi(g4.w))};
+                    const float2 uv[4] = {make_float2(bf16_lo(u4.x), bf16_hi(u4.x)),
+                                          make_float2(bf16_lo(u4.y), bf16_hi(u4.y)),
+                                          make_float2(bf16_lo(u4.z), bf16_hi(u4.z)),
+                                          make_float2(bf16_lo(u4.w), bf16_hi(u4.w))};
+#pragma unroll
+                    for (int m = 0; m < MB; ++m)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            acc[cc][m][k] = __ffma2_rn(b2[m], uv[k], __ffma2_rn(a2[m], gv[k], acc[cc][m][k]));
+                }
+            }
+        }
+        __syncthreads();   // every thread is done with stage st
+        if (threadIdx.x == 0 && j + S < nblk) {
+            fence_proxy_async_smem();
+            fill(j + S);
+        }
+    }
+    grid_launch_dependents();
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) {
+        const int col = 8 * (threadIdx.x + cc * blockDim.x);
+        if (col >= K) continue;
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            if (m < q.M) {
+                float4 *dst = reinterpret_cast<float4 *>(q.part + (static_cast<int64_t>(b) * q.M + m) * K + col);
+                dst[0] = make_float4(acc[cc][m][0].x, acc[cc][m][0].y, acc[cc][m][1].x, acc[cc][m][1].y);
+                dst[1] = make_float4(acc[cc][m][2].x, acc[cc][m][2].y, acc[cc][m][3].x, acc[cc][m][3].y);
             }
         }
     }

@@ -15,6 +15,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "mbglu.h"
 #include "glu_kernels.cuh"
@@ -26,6 +27,7 @@ using mbglu::GluParams;
 
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_variant = 0;
+thread_local int t_last_single = 0;   // row blocks of the last norm call that ran as the single kernel
 
 enum Variant {
     kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4, kSiluMul = 5, kGdnGates = 6,
@@ -175,7 +177,22 @@ cudaError_t allow_smem_bwd()
     MBGLU_ALLOW_BWD(4)
     MBGLU_ALLOW_BWD(8)
     MBGLU_ALLOW_BWD(16)
+    MBGLU_ALLOW_BWD(32)
+    MBGLU_ALLOW_BWD(64)
 #undef MBGLU_ALLOW_BWD
+    return e;
+}
+
+cudaError_t allow_smem_bwd_rows(int optin)
+{
+    cudaError_t e = cudaSuccess;
+#define MBGLU_ALLOW_ROWS(TMB, TCPT)                                                                           \
+    if (e == cudaSuccess)                                                                                     \
+        e = cudaFuncSetAttribute(mbglu::glu_bwd_rows_kernel<TMB, TCPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                 optin);
+    MBGLU_ALLOW_ROWS(1, 1) MBGLU_ALLOW_ROWS(2, 1) MBGLU_ALLOW_ROWS(4, 1) MBGLU_ALLOW_ROWS(8, 1)
+    MBGLU_ALLOW_ROWS(1, 2) MBGLU_ALLOW_ROWS(2, 2) MBGLU_ALLOW_ROWS(4, 2)
+#undef MBGLU_ALLOW_ROWS
     return e;
 }
 
@@ -195,7 +212,7 @@ mbglu_status device_info(const DeviceInfo **out)
             return cuda_fail(e);
         const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_mma<false>(d.smem_optin),
                                     allow_smem_mma<true>(d.smem_optin), allow_smem_generic(d.smem_optin),
-                                    allow_smem_bwd()};
+                                    allow_smem_bwd(), allow_smem_bwd_rows(d.smem_optin)};
         for (cudaError_t x : errs)
             if (x != cudaSuccess) return cuda_fail(x);
         d.ready = true;
@@ -553,6 +570,8 @@ int mbglu_get_launch_policy(void) { return g_policy.load(std::memory_order_relax
 int mbglu_last_cuda_error(void) { return t_last_cuda_error; }
 int mbglu_last_variant(void) { return t_last_variant; }
 
+int mbglu_last_single_kernel_blocks(void) { return t_last_single; }
+
 mbglu_status gdn_gates(const mbglu_bf16 *a, int64_t lda, const mbglu_bf16 *b, int64_t ldb, const float *A_log,
                        const float *dt_bias, float *g, int64_t ldg, mbglu_bf16 *beta, int64_t ldbeta, int T, int H,
                        cudaStream_t stream)
@@ -801,6 +820,63 @@ namespace {
 
 int bwd_splits(int N) { return std::max(1, std::min(mbglu::kBwdMaxSplits, N / 256)); }
 
+constexpr int kBwdMaxParts = 256;   // glu_bwd_rows_kernel: most CTAs (partials of grad_h per pass)
+
+int batch_tile_wide(int M) { return M <= 16 ? batch_tile(M) : M <= 32 ? 32 : 64; }
+
+// Plan of glu_bwd_rows_kernel: one CTA per SM (at most kBwdMaxParts, at most
+// N), T = 32 * ceil(K / 8 / CPT / 32) <= 512 threads owning CPT 8-column
+// chunks each, stages of R rows of both matrices (>= 16 KB), as many stages
+// (2..16) as fit beside the share's dG and dU.  Passes of 8 rows (4 with two
+// chunks per thread) keep the accumulators in registers.
+struct BwdRowsPlan {
+    int grid = 0, threads = 0, cpt = 1, R = 1, S = 0, rows_cta = 0, pass_rows = 8;
+    uint32_t off_ring = 0, smem = 0;
+};
+
+bool plan_bwd_rows(const DeviceInfo &d, int N, int K, const void *gate_w, int64_t ld_gate, const void *up_w,
+                   int64_t ld_up, BwdRowsPlan &rp)
+{
+    if (K % 8 != 0 || !aligned(gate_w, 16) || !aligned(up_w, 16) || ld_gate % 8 != 0 || ld_up % 8 != 0) return false;
+    const int nchunk = K / 8;
+    rp.cpt = (nchunk + mbglu::kBwdRowsThreads - 1) / mbglu::kBwdRowsThreads;
+    if (rp.cpt > 2) return false;
+    rp.threads = 32 * ((nchunk + 32 * rp.cpt - 1) / (32 * rp.cpt));
+    rp.pass_rows = rp.cpt == 1 ? 8 : 4;
+    rp.grid = std::max(1, std::min({d.sm_count, kBwdMaxParts, N}));
+    rp.rows_cta = (N + rp.grid - 1) / rp.grid;
+    const uint32_t dgu = 2u * static_cast<uint32_t>(rp.pass_rows) * static_cast<uint32_t>(rp.rows_cta) * 4u;
+    rp.off_ring = (256u + dgu + 127u) & ~127u;
+    rp.R = std::max(1, std::min(rp.rows_cta, (16384 + 4 * K - 1) / (4 * K)));
+    const int64_t stage = 4ll * rp.R * K;
+    const int64_t room = static_cast<int64_t>(d.smem_optin) - rp.off_ring;
+    rp.S = static_cast<int>(std::min<int64_t>(16, room / stage));
+    if (rp.S < 2) return false;
+    rp.smem = rp.off_ring + static_cast<uint32_t>(rp.S * stage);
+    return true;
+}
+
+mbglu_status launch_bwd_rows(const BwdRowsPlan &rp, int MB, const mbglu::BwdParams &q, cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rp.grid);
+    cfg.blockDim = dim3(rp.threads);
+    cfg.dynamicSmemBytes = rp.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_policy.load(std::memory_order_relaxed) != MBGLU_POLICY_SERIAL ? 1 : 0;
+    cudaError_t e = cudaErrorInvalidValue;
+#define MBGLU_BWD_ROWS(TMB, TCPT)                                                             \
+    if (MB == TMB && rp.cpt == TCPT) e = cudaLaunchKernelEx(&cfg, mbglu::glu_bwd_rows_kernel<TMB, TCPT>, q);
+    MBGLU_BWD_ROWS(1, 1) MBGLU_BWD_ROWS(2, 1) MBGLU_BWD_ROWS(4, 1) MBGLU_BWD_ROWS(8, 1)
+    MBGLU_BWD_ROWS(1, 2) MBGLU_BWD_ROWS(2, 2) MBGLU_BWD_ROWS(4, 2)
+#undef MBGLU_BWD_ROWS
+    return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
+}
+
 int64_t round256(int64_t b) { return (b + 255) & ~static_cast<int64_t>(255); }
 
 mbglu_status launch_plain(cudaError_t e)
@@ -814,9 +890,12 @@ extern "C" {
 
 size_t glu_backward_workspace_bytes(int M, int N, int K)
 {
-    if (M <= 0 || N <= 0 || K <= 0 || M > kBlockRows) return 0;
-    return static_cast<size_t>(round256(2 * static_cast<int64_t>(M) * N * 4) +
-                               round256(static_cast<int64_t>(bwd_splits(N)) * M * K * 4));
+    if (M <= 0 || N <= 0 || K <= 0 || M > MBGLU_MAX_M) return 0;
+    // dG, dU; then the grad_h partials of one pass: up to kBwdMaxParts CTAs
+    // of the rows kernel at 8 rows, or kBwdMaxSplits splits at kBlockRows rows
+    const int64_t parts = std::max<int64_t>(static_cast<int64_t>(kBwdMaxParts) * std::min(M, 8),
+                                            static_cast<int64_t>(mbglu::kBwdMaxSplits) * std::min(M, kBlockRows));
+    return static_cast<size_t>(round256(2 * static_cast<int64_t>(M) * N * 4) + round256(parts * K * 4));
 }
 
 mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
@@ -826,7 +905,7 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
                           size_t workspace_bytes, cudaStream_t stream)
 {
     t_last_variant = kNone;
-    if (M < 0 || N < 0 || K < 0 || M > kBlockRows) return MBGLU_ERR_SHAPE;
+    if (M < 0 || N < 0 || K < 0 || M > MBGLU_MAX_M) return MBGLU_ERR_SHAPE;
     const bool want_h = grad_h != nullptr, want_w = grad_gate != nullptr || grad_up != nullptr;
     if (want_w && (!grad_gate || !grad_up)) return MBGLU_ERR_NULL;
     if (K == 0) return MBGLU_OK;   // every gradient has K columns
@@ -876,10 +955,16 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
     float *dU = dG + static_cast<int64_t>(M) * N;
     float *part = reinterpret_cast<float *>(static_cast<char *>(workspace) + round256(2 * static_cast<int64_t>(M) * N * 4));
 
-    // 1) dG, dU: the forward kernels with the backward epilogue
-    const BwdEpilogue be = {dout, ldd, dG, dU};
-    st = gemv_block(h, ldh, gate_w, ld_gate, up_w, ld_up, nullptr, 0, M, N, K, MBGLU_MODE_FUSED, stream, &be);
-    if (st != MBGLU_OK) return st;
+    // 1) dG, dU: the forward kernels with the backward epilogue, per block of
+    //    up to kBlockRows rows (the weights stay in L2 for step 2)
+    for (int m0 = 0; m0 < M; m0 += kBlockRows) {
+        const int mb = std::min(kBlockRows, M - m0);
+        const BwdEpilogue be = {dout + static_cast<int64_t>(m0) * ldd, ldd, dG + static_cast<int64_t>(m0) * N,
+                                dU + static_cast<int64_t>(m0) * N};
+        st = gemv_block(h + static_cast<int64_t>(m0) * ldh, ldh, gate_w, ld_gate, up_w, ld_up, nullptr, 0, mb, N, K,
+                        MBGLU_MODE_FUSED, stream, &be);
+        if (st != MBGLU_OK) return st;
+    }
 
     mbglu::BwdParams q = {};
     q.h = h;
@@ -888,8 +973,6 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
     q.ld_gate = ld_gate;
     q.up = up_w;
     q.ld_up = ld_up;
-    q.dG = dG;
-    q.dU = dU;
     q.part = part;
     q.grad_h = grad_h;
     q.ldgh = ldgh;
@@ -897,44 +980,72 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
     q.ldgg = ldgg;
     q.grad_up = grad_up;
     q.ldgu = ldgu;
-    q.M = M;
     q.N = N;
     q.K = K;
+    q.ldm = N;
     q.vec_w = aligned(gate_w, 8) && aligned(up_w, 8) && ld_gate % 4 == 0 && ld_up % 4 == 0;
-    const int MB = batch_tile(M);
     cudaError_t e = cudaSuccess;
-    // 2) grad_h: partials over row splits, then their sum in split order
+    // 2) grad_h: partials, then their sum in order; passes of up to 8 rows
+    //    (the rows kernel) or kBlockRows rows (the column-block kernel)
     if (want_h) {
-        const int nsplit = bwd_splits(N);
-        const dim3 grid((K + mbglu::kBwdCols - 1) / mbglu::kBwdCols, nsplit);
-        const size_t smem = static_cast<size_t>(std::max(2 * M * mbglu::kBwdRowChunk, MB * 4 * 128)) * 4;
-        switch (MB) {
-            case 1: mbglu::glu_bwd_h_kernel<1><<<grid, 256, smem, stream>>>(q); break;
-            case 2: mbglu::glu_bwd_h_kernel<2><<<grid, 256, smem, stream>>>(q); break;
-            case 4: mbglu::glu_bwd_h_kernel<4><<<grid, 256, smem, stream>>>(q); break;
-            case 8: mbglu::glu_bwd_h_kernel<8><<<grid, 256, smem, stream>>>(q); break;
-            default: mbglu::glu_bwd_h_kernel<16><<<grid, 256, smem, stream>>>(q); break;
+        BwdRowsPlan rp;
+        const bool rows_ok = plan_bwd_rows(*d, N, K, gate_w, ld_gate, up_w, ld_up, rp);
+        const int pass = rows_ok ? rp.pass_rows : kBlockRows;
+        for (int m0 = 0; m0 < M; m0 += pass) {
+            const int mb = std::min(pass, M - m0);
+            q.M = mb;
+            q.dG = dG + static_cast<int64_t>(m0) * N;
+            q.dU = dU + static_cast<int64_t>(m0) * N;
+            q.grad_h = grad_h + static_cast<int64_t>(m0) * ldgh;
+            int nparts = 0;
+            if (rows_ok) {
+                q.R = rp.R;
+                q.S = rp.S;
+                q.off_ring = rp.off_ring;
+                q.rows_cta = rp.rows_cta;
+                st = launch_bwd_rows(rp, batch_tile(mb), q, stream);
+                if (st != MBGLU_OK) return st;
+                nparts = rp.grid;
+            } else {
+                nparts = bwd_splits(N);
+                const dim3 grid((K + mbglu::kBwdCols - 1) / mbglu::kBwdCols, nparts);
+                const int MB = batch_tile(mb);
+                const size_t smem = static_cast<size_t>(std::max(2 * mb * mbglu::kBwdRowChunk, MB * 4 * 128)) * 4;
+                switch (MB) {
+                    case 1: mbglu::glu_bwd_h_kernel<1><<<grid, 256, smem, stream>>>(q); break;
+                    case 2: mbglu::glu_bwd_h_kernel<2><<<grid, 256, smem, stream>>>(q); break;
+                    case 4: mbglu::glu_bwd_h_kernel<4><<<grid, 256, smem, stream>>>(q); break;
+                    case 8: mbglu::glu_bwd_h_kernel<8><<<grid, 256, smem, stream>>>(q); break;
+                    default: mbglu::glu_bwd_h_kernel<16><<<grid, 256, smem, stream>>>(q); break;
+                }
+                if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+            }
+            const int rgrid = static_cast<int>(std::max<int64_t>(
+                1, std::min<int64_t>(d->sm_count * 4, (static_cast<int64_t>(mb) * K + 255) / 256)));
+            mbglu::glu_bwd_h_reduce_kernel<<<rgrid, 256, 0, stream>>>(q, nparts);
+            if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
         }
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
-        const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(d->sm_count * 4,
-                                                                                   (static_cast<int64_t>(M) * K + 255) / 256)));
-        mbglu::glu_bwd_h_reduce_kernel<<<rgrid, 256, 0, stream>>>(q, nsplit);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
     }
-    // 3) grad_gate, grad_up: the outer products, h in shared memory where it fits
+    // 3) grad_gate, grad_up: the outer products over all M rows, h in shared
+    //    memory where it fits
     if (want_w) {
+        q.M = M;
+        q.dG = dG;
+        q.dU = dU;
         const int64_t hbytes = static_cast<int64_t>(M) * K * 2;
         q.h_smem = hbytes <= kBwdHSmemMax;
         q.vec_out = K % 8 == 0 && aligned(grad_gate, 16) && aligned(grad_up, 16) && ldgg % 8 == 0 && ldgu % 8 == 0 &&
                     (q.h_smem || (aligned(h, 16) && ldh % 8 == 0));
         const size_t smem = q.h_smem ? static_cast<size_t>(hbytes) : 0;
         const int wgrid = std::max(1, std::min(N, d->sm_count * 2));
-        switch (MB) {
+        switch (batch_tile_wide(M)) {
             case 1: mbglu::glu_bwd_w_kernel<1><<<wgrid, 256, smem, stream>>>(q); break;
             case 2: mbglu::glu_bwd_w_kernel<2><<<wgrid, 256, smem, stream>>>(q); break;
             case 4: mbglu::glu_bwd_w_kernel<4><<<wgrid, 256, smem, stream>>>(q); break;
             case 8: mbglu::glu_bwd_w_kernel<8><<<wgrid, 256, smem, stream>>>(q); break;
-            default: mbglu::glu_bwd_w_kernel<16><<<wgrid, 256, smem, stream>>>(q); break;
+            case 16: mbglu::glu_bwd_w_kernel<16><<<wgrid, 256, smem, stream>>>(q); break;
+            case 32: mbglu::glu_bwd_w_kernel<32><<<wgrid, 256, smem, stream>>>(q); break;
+            default: mbglu::glu_bwd_w_kernel<64><<<wgrid, 256, smem, stream>>>(q); break;
         }
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
     }
@@ -1033,7 +1144,10 @@ mbglu_status norm_block(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_b
             const mbglu::MmaMaps maps = weight_maps(p);
             st = launch_mma(mbglu::glu_mma_kernel<true>, dim3(pl.grid), dim3((pl.warps + 1) * 32), pl.smem, stream,
                             pdl, p, maps);
-            if (st == MBGLU_OK) t_last_variant = kTensor;
+            if (st == MBGLU_OK) {
+                t_last_variant = kTensor;
+                ++t_last_single;
+            }
             return st;
         }
         if (plan_stream(*d, M, N, K, true, true, pl, true, sbytes, mbglu::kMaxStreamWarps - 1)) {
@@ -1045,7 +1159,10 @@ mbglu_status norm_block(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_b
             p.off_ring = pl.off_ring;
             p.helper_warp = pl.warps;   // one extra warp writes the residual slice
             st = launch_stream<true>(pl, p, stream, pdl);
-            if (st == MBGLU_OK) t_last_variant = kStream;
+            if (st == MBGLU_OK) {
+                t_last_variant = kStream;
+                ++t_last_single;
+            }
             return st;
         }
         p.fused = 0;
@@ -1124,6 +1241,7 @@ mbglu_status add_rmsnorm_glu_impl(const mbglu_bf16 *x, mbglu_bf16 *residual, con
                                   cudaStream_t stream)
 {
     t_last_variant = kNone;
+    t_last_single = 0;
     mbglu_status st = check_norm(x, residual, norm_w, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode, ws);
     if (st != MBGLU_OK || M == 0) return st;
     if (M <= kBlockRows)
@@ -1162,6 +1280,7 @@ mbglu_status add_rmsnorm_glu_strided(const mbglu_bf16 *x, mbglu_bf16 *residual, 
                                      void *workspace, size_t workspace_bytes, cudaStream_t stream)
 {
     t_last_variant = kNone;
+    t_last_single = 0;
     if (workspace) {
         if (workspace_bytes < MBGLU_WORKSPACE_BYTES) return MBGLU_ERR_SHAPE;
         if (!aligned(workspace, 16)) return MBGLU_ERR_ALIGN;
@@ -1176,6 +1295,7 @@ mbglu_status add_rmsnorm_glu_ws(const mbglu_bf16 *x, mbglu_bf16 *residual, const
                                 cudaStream_t stream)
 {
     t_last_variant = kNone;
+    t_last_single = 0;
     if (!workspace) return MBGLU_ERR_NULL;
     if (workspace_bytes < MBGLU_WORKSPACE_BYTES) return MBGLU_ERR_SHAPE;
     if (!aligned(workspace, 16)) return MBGLU_ERR_ALIGN;
@@ -1212,22 +1332,53 @@ static_assert(MBGLU_WORKSPACE_BYTES <= MBGLU_NOALLOC_SCRATCH_BYTES, "the array m
 
 std::mutex g_noalloc_mu;
 int *g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};
+
+// The identity of the current context (0 if the driver cannot tell): a
+// cudaDeviceReset destroys the context and a new one gets a new identity,
+// so an address kept from the old context is never reused.
+unsigned long long current_context_id()
+{
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static const std::pair<GetCurrent, GetId> fns = [] {
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            a = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            b = nullptr;
+        return std::make_pair(reinterpret_cast<GetCurrent>(a), reinterpret_cast<GetId>(b));
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!fns.first || !fns.second || fns.first(&ctx) != CUDA_SUCCESS || !ctx || fns.second(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
 // The array's device address on the current device.  In host code the name
 // g_noalloc_scratch is only a host-side stand-in, so the address is asked of
-// the runtime once per device (with that device current) and kept.
+// the runtime (with the device current) and kept per device together with the
+// context it belongs to; a new context (after cudaDeviceReset) looks it up again.
 mbglu_status noalloc_scratch(int **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
     if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
+    // 0 when no context is current on this thread yet: the address is then
+    // looked up (which makes one current) and looked up again next time
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
+    if (!g_noalloc_ptr[dev] || ctx == 0 || g_noalloc_ctx[dev] != ctx) {
         int *ptr = nullptr;
         e = cudaGetSymbolAddress(reinterpret_cast<void **>(&ptr), g_noalloc_scratch);
         if (e != cudaSuccess) return cuda_fail(e);
         g_noalloc_ptr[dev] = ptr;
+        g_noalloc_ctx[dev] = ctx;
     }
     *out = g_noalloc_ptr[dev];
     return MBGLU_OK;
@@ -1241,6 +1392,7 @@ extern "C" mbglu_status add_rmsnorm_glu_noalloc(const mbglu_bf16 *x, mbglu_bf16 
                                                 cudaStream_t stream)
 {
     t_last_variant = kNone;
+    t_last_single = 0;
     // the scratch this call needs must fit the array (the single kernel needs
     // one workspace whatever the shapes; the check states the limit)
     const size_t need = MBGLU_WORKSPACE_BYTES;
@@ -1253,4 +1405,17 @@ extern "C" mbglu_status add_rmsnorm_glu_noalloc(const mbglu_bf16 *x, mbglu_bf16 
     const cudaError_t e = cudaMemsetAsync(scratch, 0, need, stream);
     if (e != cudaSuccess) return cuda_fail(e);
     return add_rmsnorm_glu_ws(x, residual, norm_w, eps, gate_w, up_w, out, M, N, K, mode, scratch, need, stream);
+}
+
+// Diagnostics: the first `count` words of the current device's no-allocation
+// scratch array, after the device has finished its work.
+extern "C" mbglu_status mbglu_noalloc_scratch_read(int *words, int count)
+{
+    if (!words) return MBGLU_ERR_NULL;
+    if (count < 0 || count * sizeof(int) > MBGLU_NOALLOC_SCRATCH_BYTES) return MBGLU_ERR_SHAPE;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (count == 0) return MBGLU_OK;
+    if ((e = cudaMemcpyFromSymbol(words, g_noalloc_scratch, count * sizeof(int))) != cudaSuccess) return cuda_fail(e);
+    return MBGLU_OK;
 }

@@ -204,7 +204,7 @@ def bwd(h=H, ldh=64, g=G, ldg=64, u=U, ldu=64, d=D, ldd=32, gh=GH, ldgh=64, gg=G
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(M=-1), SHAPE), (dict(N=-1), SHAPE), (dict(K=-1), SHAPE), (dict(M=17), SHAPE),
+    (dict(M=-1), SHAPE), (dict(N=-1), SHAPE), (dict(K=-1), SHAPE), (dict(M=65), SHAPE),
     (dict(h=0), NULL), (dict(d=0), NULL), (dict(ws=0), NULL), (dict(gg=0), NULL), (dict(gu=0), NULL),
     (dict(ldh=63), STRIDE), (dict(ldd=31), STRIDE), (dict(ldgh=60), STRIDE), (dict(ldgu=1), STRIDE),
     (dict(h=H + 1), ALIGN), (dict(gh=GH + 1), ALIGN), (dict(ws=BW + 8), ALIGN),
@@ -223,7 +223,11 @@ def test_glu_backward_validation(kw, code):
 def test_glu_backward_workspace_bytes():
     lib = mb.lib()
     # dG and dU in fp32, then one fp32 [M][K] partial per row split (N / 256, 1..48)
-    assert lib.glu_backward_workspace_bytes(4, 1000, 512) == 32000 + 3 * 4 * 512 * 4
-    assert lib.glu_backward_workspace_bytes(16, 9728, 2560) == 16 * 9728 * 8 + 38 * 16 * 2560 * 4
-    assert lib.glu_backward_workspace_bytes(1, 100000, 64) == 800000 + 48 * 64 * 4
-    assert lib.glu_backward_workspace_bytes(17, 10, 10) == 0 and lib.glu_backward_workspace_bytes(0, 10, 10) == 0
+    # dG, dU [M][N] fp32, then the grad_h partials of one pass: 256 CTAs x
+    # min(M, 8) rows, or 48 splits x min(M, 16) rows, whichever is larger
+    r256 = lambda b: (b + 255) // 256 * 256  # noqa: E731
+    assert lib.glu_backward_workspace_bytes(4, 1000, 512) == 32000 + 256 * 4 * 512 * 4
+    assert lib.glu_backward_workspace_bytes(16, 9728, 2560) == 16 * 9728 * 8 + 256 * 8 * 2560 * 4
+    assert lib.glu_backward_workspace_bytes(1, 100000, 64) == 800000 + 256 * 64 * 4
+    assert lib.glu_backward_workspace_bytes(64, 10, 10) == r256(64 * 10 * 8) + r256(256 * 8 * 10 * 4)
+    assert lib.glu_backward_workspace_bytes(65, 10, 10) == 0 and lib.glu_backward_workspace_bytes(0, 10, 10) == 0

@@ -63,7 +63,33 @@ def test_backward_every_batch_tile(M):
     assert mb.read_device_error() == 0
 
 
-@pytest.mark.parametrize("N,K", [(1, 8), (7, 64), (256, 520), (3000, 2560), (513, 4100)])
+@pytest.mark.parametrize("M", [17, 32, 64])
+def test_backward_wide_batch(M):
+    """Batches above one pass: dG, dU per 16-row block, grad_h per pass of 8
+    rows, the weight gradients summed over all M rows at once."""
+    N, K = 1500, 1024
+    h, g, u, d = _inputs(M, N, K, M, "bwwide")
+    got = mb.glu_backward(h.to(DEV), g.to(DEV), u.to(DEV), d.to(DEV))
+    torch.cuda.synchronize()
+    assert mb.last_variant() == BACKWARD
+    _check(tuple(t.cpu() for t in got), h, g, u, d, f"M={M}")
+    assert mb.read_device_error() == 0
+
+
+def test_backward_autograd_at_batch_32():
+    """DualWeightGlu runs wherever its forward does: batch 32 (row blocks)."""
+    M, N, K = 32, 700, 512
+    h0, g0, u0, d0 = (t.to(DEV) for t in _inputs(M, N, K, 5, "bwa32"))
+    h = h0.clone().requires_grad_(True)
+    g = g0.clone().requires_grad_(True)
+    u = u0.clone().requires_grad_(True)
+    out = mb.DualWeightGlu.apply(h, g, u)
+    out.backward(d0)
+    torch.cuda.synchronize()
+    _check((h.grad.cpu(), g.grad.cpu(), u.grad.cpu()), h0.cpu(), g0.cpu(), u0.cpu(), d0.cpu(), "autograd M=32")
+
+
+@pytest.mark.parametrize("N,K", [(1, 8), (7, 64), (256, 520), (3000, 2560), (513, 4100), (300, 8192), (200, 9216)])
 def test_backward_shapes(N, K):
     M = 4
     h, g, u, d = _inputs(M, N, K, N, "bws")
@@ -124,8 +150,8 @@ def test_backward_degenerate_shapes():
     torch.cuda.synchronize()
     assert (gi.bits(gg.cpu()) == 0).all() and (gi.bits(gu.cpu()) == 0).all() and (gi.bits(gh.cpu()) == 0).all()
     with pytest.raises(mb.MbgluError):
-        mb.glu_backward(torch.zeros((17, K), dtype=torch.bfloat16, device=DEV), g, g,
-                        torch.zeros((17, 10), dtype=torch.bfloat16, device=DEV))
+        mb.glu_backward(torch.zeros((65, K), dtype=torch.bfloat16, device=DEV), g, g,
+                        torch.zeros((65, 10), dtype=torch.bfloat16, device=DEV))
 
 
 def test_autograd_function_matches_glu_backward():
