@@ -70,6 +70,10 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--norm-kernels", type=int, default=1, choices=[1, 2],
                     help="add_rmsnorm_glu as one kernel (workspace entry point) or as two")
+    ap.add_argument("--split", action="store_true",
+                    help="under torchrun: split each layer column-parallel over N (rank p streams rows "
+                         "column_shard(N, P, p) of both weights and writes its columns of out; strong scaling, "
+                         "no collective); default: one whole replica per rank (weak scaling)")
     ap.add_argument("--policy", type=int, default=None, choices=[0, 1, 2],
                     help="launch policy (default: the library's, 2 = PDL + weight prefetch)")
     return ap.parse_args()
@@ -218,6 +222,15 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def sum_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
 
 
 def max_over_ranks(x, world, device):
@@ -407,7 +420,9 @@ def _reference_silu_mul(args, w, M, mode, world, steps, warm):
     print(json.dumps(line), flush=True)
 
 
-def config_dict(w, M, mode, layers, norm_kernels=None, blocks=1):
+def config_dict(w, M, mode, layers, norm_kernels=None, blocks=1, policy=None):
+    """The workload description; `policy` is the library's launch policy name
+    (the GPU arm only: the reference arm never loads the library)."""
     wb = w.input_bytes(M) * layers
     extra = {} if w.op == "glu_gemv" or norm_kernels is None else {"norm_kernels": norm_kernels}
     if blocks > 1:
@@ -417,15 +432,10 @@ def config_dict(w, M, mode, layers, norm_kernels=None, blocks=1):
             "l2": f"inputs larger than L2: {layers} cycled {'inputs' if w.op in ('silu_mul', 'gdn_gates') else 'weight pairs'}, "
                   f"{wb / 1e9:.2f} GB",
             "launch": f"one CUDA graph of {layers} calls per step",
-            "launch_policy": _policy_name()}
+            **({"launch_policy": policy} if policy else {})}
 
 
-def _policy_name():
-    try:
-        import memory_bound_glu_gb300 as mb
-        return {0: "serial", 1: "pdl", 2: "pdl+weight-prefetch"}[mb.get_launch_policy()]
-    except Exception:
-        return None
+POLICY_NAMES = {0: "serial", 1: "pdl", 2: "pdl+weight-prefetch"}
 
 
 # ---------------------------------------------------------------------------
@@ -454,12 +464,16 @@ def main():
     if args.policy is not None:
         mb.set_launch_policy(args.policy)
 
+    # the column split: this rank's rows of both weights, its columns of out
+    split = args.split and w.op in ("glu_gemv", "add_rmsnorm_glu")
+    lo, hi = mb.column_shard(w.N, world, rank) if split else (0, w.N)
+
     # inputs: resident in HBM before the timed region
     gates, ups = [], []
     for layer in range(L if w.op in ("glu_gemv", "add_rmsnorm_glu", "glu_backward") else 0):
         g, u = gi.layer_weights(w, layer)
-        gates.append(g.to(dev))
-        ups.append(u.to(dev))
+        gates.append(g[lo:hi].contiguous().to(dev))
+        ups.append(u[lo:hi].contiguous().to(dev))
         del g, u
     if w.op == "silu_mul":
         xs_cpu = [gi.projections(w, M, layer) for layer in range(L)]
@@ -499,12 +513,12 @@ def main():
             elif w.op == "gdn_gates":
                 mb.gdn_gates(gdn[i][0], gdn[i][1], gdn[i][2], gdn[i][3], g=gs[i], beta=outs[i])
             elif w.op == "glu_gemv":
-                mb.glu_gemv(h, gates[i], ups[i], out=outs[i], mode=mode)
+                mb.glu_gemv(h, gates[i], ups[i], out=outs[i][:, lo:hi], mode=mode)
             elif w.op == "glu_backward":
                 mb.glu_backward(h, gates[i], ups[i], dout, grad_h=grad_hs[i], grad_gate=grad_gates[i],
                                 grad_up=grad_ups[i], workspace=bws)
             else:
-                mb.add_rmsnorm_glu(x, residuals[i], nw, w.eps, gates[i], ups[i], out=outs[i], mode=mode,
+                mb.add_rmsnorm_glu(x, residuals[i], nw, w.eps, gates[i], ups[i], out=outs[i][:, lo:hi], mode=mode,
                                    workspace=ws)
 
     stream = torch.cuda.Stream(dev)
@@ -515,11 +529,11 @@ def main():
         variant = mb.last_variant()
         if variant == ROW_BLOCKS:   # the kernel of a full block: one call on the first block's rows
             if w.op == "glu_gemv":
-                mb.glu_gemv(h[:block_rows[0]], gates[0], ups[0], out=outs[0, :block_rows[0]], mode=mode)
+                mb.glu_gemv(h[:block_rows[0]], gates[0], ups[0], out=outs[0, :block_rows[0], lo:hi], mode=mode)
             else:
                 r_probe = residuals[0][:block_rows[0]].clone()
                 mb.add_rmsnorm_glu(x[:block_rows[0]], r_probe, nw, w.eps, gates[0], ups[0],
-                                   out=outs[0, :block_rows[0]], mode=mode, workspace=ws)
+                                   out=outs[0, :block_rows[0], lo:hi], mode=mode, workspace=ws)
             torch.cuda.synchronize(dev)
             variant = mb.last_variant()
         kernel_name = KERNEL_NAMES.get(variant, f"variant {variant}")
@@ -556,16 +570,29 @@ def main():
     if err:
         raise RuntimeError(f"device error word {err} after the timed region")
 
-    bytes_per_call = w.algorithmic_bytes(M)
+    def call_bytes(m):
+        """Algorithmic bytes of this rank's call on m rows (its shard of N
+        under the column split)."""
+        if not split:
+            return w.algorithmic_bytes(m)
+        n = hi - lo
+        if w.op == "glu_gemv":
+            return 2 * n * w.K * 2 + m * w.K * 2 + m * n * 2
+        return 2 * n * w.K * 2 + 3 * m * w.K * 2 + w.K * 2 + m * n * 2
+
+    bytes_per_call = call_bytes(M)
     calls = args.steps * L
     us_per_call = ms_max * 1e3 / calls
     gbs = bytes_per_call / (us_per_call * 1e-6) / 1e9
     # the dominant kernel's roofline: per launch, the algorithmic bytes of the
     # rows it takes (each block streams both weights) over the mean launch
     # time; with one launch per call this is the call's own figure
-    gemv_launch_bytes = sum(w.algorithmic_bytes(m) for m in block_rows)
+    gemv_launch_bytes = sum(call_bytes(m) for m in block_rows)
     launch_gbs = gemv_launch_bytes / (us_per_call * 1e-6) / 1e9
-    value = gbs * world
+    # the whole job's bytes per call: every rank's shard of the layer under
+    # the column split, every replica otherwise
+    job_bytes_per_call = sum_over_ranks(bytes_per_call, world, dev) if split else bytes_per_call * world
+    value = job_bytes_per_call / (us_per_call * 1e-6) / 1e9
     peak, peak_kind = measured_peaks()
 
     # e2e: the public Python API, pinned host input -> device, results -> host
@@ -624,7 +651,7 @@ def main():
             torch.cuda.synchronize(dev)
             el = max_over_ranks(time.perf_counter() - t0, world, dev)
             barrier(world)
-        e2e = {"value": round(bytes_per_call * L * e2e_steps / el / 1e9 * world, 2), "unit": "GB/s",
+        e2e = {"value": round(job_bytes_per_call * L * e2e_steps / el / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": out_host.numel() * 2,
                "ms_per_step": round(el / e2e_steps * 1e3, 4),
                "how": "eager public-API calls (no graph), host copies inside the timed region"}
@@ -640,8 +667,11 @@ def main():
             "metric": "GLU GEMV achieved HBM GB/s (cold L2), us/call at M=1",
             "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": round(ms_max / args.steps, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded torch.randn, bf16)", "config": config_dict(w, M, mode, L, args.norm_kernels, blocks),
+            "higher_is_better": True, "scaling": "strong" if split else "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded torch.randn, bf16)",
+            "config": {**config_dict(w, M, mode, L, args.norm_kernels, blocks, POLICY_NAMES[mb.get_launch_policy()]),
+                       "parallelism": (f"column split over N: {world} ranks, rows {lo}..{hi - 1} on rank 0"
+                                       if split else f"{world} independent replica(s)")},
             "us_per_call": round(us_per_call, 3), "bytes_per_call": bytes_per_call,
             "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
             "roofline": {"bound": "hbm", "achieved": round(launch_gbs, 2), "peak": peak, "unit": "GB/s",

@@ -158,13 +158,14 @@ typedef struct {
  * Each bf16 x bf16 product is exact in binary64 (8 + 8 significant bits), and
  * the sum runs in k order.
  *
- * mode FUSED ([8602/PlanB] kernel listing; [8602/fused_glu] "single
- * rounding"): out = bf16( SiLU(G) * U ), one rounding at the end.
+ * mode FUSED ([8602/PlanB] kernel listing; [8602/fused_glu], the fused
+ * kernel rounds once where the composite rounds twice):
+ * out = bf16( SiLU(G) * U ), one rounding at the end.
  *
  * mode HF ([8602/PlanB] b>1 fallback F.silu(hidden @ gate_w.T) *
- * (hidden @ up_w.T) on bf16 tensors; [9057/Changes] "Restore HF's
- * intermediate BF16 rounding in ... GLU"): every tensor the bf16 composite
- * materialises is rounded --
+ * (hidden @ up_w.T) on bf16 tensors; [9057/Changes]: the GLU keeps the bf16
+ * roundings of HF's own code): every tensor the bf16 composite materialises
+ * is rounded --
  *   gb = bf16(G), ub = bf16(U), sb = bf16(SiLU(gb)), out = bf16(sb * ub).
  */
 static void glu_rows(const glu_job *j)
@@ -264,8 +265,8 @@ int oracle_glu_gemv(const uint16_t *h, int64_t ldh,
 /* ------------------------------------------------------------------------ */
 
 /*
- * For each row m ([9057/Changes] "Restore HF's intermediate BF16 rounding in
- * residual/RMSNorm ... construct zero-centered norm scales in FP32";
+ * For each row m ([9057/Changes]: the residual add and the RMSNorm keep HF's
+ * bf16 roundings, and the zero-centred scale (1 + w) is formed in fp32;
  * [8602/old-ki] the statistic must not be accumulated in bf16):
  *   s[k]  = bf16(x[k] + r[k])                      the updated residual stream
  *   var   = (1/K) * sum_k s[k]^2
@@ -381,12 +382,11 @@ int oracle_silu_mul(const uint16_t *x, int64_t ldx, uint16_t *out, int64_t ldo, 
 /* ------------------------------------------------------------------------ */
 
 /*
- * The gates the same segment-KI work fuses beside the GLU ([8602/fused_glu]
- * commit "feat ... gdn_gates": "beta=sigmoid(b) and
- * g=-exp(A_log)*softplus(a+dt_bias) with fp32 math and the numerically stable
- * softplus branch"; [9057/Changes]: "Preserve FP32 GDN decay gates"; strided
- * inputs: "row-stride input, no contiguous copies").  For every token t < T
- * and head j < H:
+ * The gates the same segment-KI work fuses beside the GLU ([8602/fused_glu],
+ * the gdn_gates commit: the sigmoid write gate and the decay gate
+ * -exp(A_log) * softplus(a + dt_bias) computed in fp32 with the stable
+ * softplus form, on strided inputs read in place; [9057/Changes]: the decay
+ * gates stay fp32).  For every token t < T and head j < H:
  *   x    = fp32( a[t, j] + dt_bias[j] )       the binary32 addition the fp32
  *                                             math performs (a is bf16)
  *   g    = -exp(A_log[j]) * softplus(x)       returned in binary64
@@ -425,9 +425,10 @@ int oracle_gdn_gates(const uint16_t *a, int64_t lda, const uint16_t *b, int64_t 
 /* ------------------------------------------------------------------------ */
 
 /*
- * [8602/PlanB]: the autograd wrapper saves (hidden, gate_w, up_w) and lets
- * "gradients flow naturally"; its three gradients matched the composite
- * F.silu(h @ Wg.T) * (h @ Wu.T) exactly in fp32 ("Verification Results").
+ * [8602/PlanB]: the autograd wrapper saves (hidden, gate_w, up_w) so that
+ * the gradients reach the original Parameters; its three gradients matched
+ * the composite F.silu(h @ Wg.T) * (h @ Wu.T) exactly in fp32 (section
+ * "Verification Results").
  * So the backward is the gradient of out = SiLU(G) * U with G = h . Wg[n],
  * U = h . Wu[n], for an upstream gradient dout [M][N]:
  *   SiLU'(G) = s (1 + G (1 - s)),  s = 1 / (1 + e^-G)

@@ -1,5 +1,5 @@
-"""bench.py's multi-rank host logic on CPU (gloo, world size 2): the barrier and
-max-over-ranks timing reduce, and the reference arm under torchrun printing
+"""bench.py's multi-rank host logic on CPU (gloo, world size 2): the barrier,
+the max-over-ranks timing reduce and the sum of the column split's bytes, and the reference arm under torchrun printing
 exactly one line from rank 0.  No GPU is involved."""
 import json
 import os
@@ -32,7 +32,8 @@ def _worker(rank, world, port, q):
     assert (w, r) == (world, rank)
     bench.barrier(w)
     got = bench.max_over_ranks(10.0 + rank, w, torch.device("cpu"))
-    q.put((rank, got))
+    total = bench.sum_over_ranks(1.0 + rank, w, torch.device("cpu"))   # the column split's job bytes
+    q.put((rank, (got, total)))
     dist.destroy_process_group()
 
 
@@ -47,7 +48,7 @@ def test_max_over_ranks_with_gloo():
         p.join(timeout=120)
         assert p.exitcode == 0
     res = dict(q.get(timeout=5) for _ in range(2))
-    assert res == {0: 11.0, 1: 11.0}
+    assert res == {0: (11.0, 3.0), 1: (11.0, 3.0)}
 
 
 @pytest.mark.slow
