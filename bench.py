@@ -39,14 +39,19 @@ import glu_inputs as gi  # noqa: E402
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 # mbglu_last_variant() -> the kernel that streams the weights
-ROW_BLOCKS = 7   # mbglu_last_variant() of a batch above one pass's rows
+ROW_BLOCKS = 7   # mbglu_last_variant() of a batch above one pass's rows, run as row blocks
+TCGEN05 = 9      # mbglu_last_variant() of a batch above 16 rows in one pass on the tcgen05 kernel
 BLOCK_M = 16     # batch rows per pass over the weights (MBGLU_BLOCK_M in include/mbglu.h)
 
 
 def row_blocks(w, M):
-    """Row blocks (passes over the weights) of one call of workload w at M rows."""
-    return -(-M // BLOCK_M) if w.op in ("glu_gemv", "add_rmsnorm_glu") and M > BLOCK_M else 1
+    """Row blocks (passes over the weights) of one call of workload w at M
+    rows: glu_gemv takes a batch above 16 rows in one pass (the tcgen05
+    kernel, on the aligned operands the bench uses); add_rmsnorm_glu runs it
+    as row blocks of 16."""
+    return -(-M // BLOCK_M) if w.op == "add_rmsnorm_glu" and M > BLOCK_M else 1
 KERNEL_NAMES = {1: "glu_stream_kernel", 2: "glu_generic_kernel", 4: "glu_mma_kernel", 5: "silu_mul_kernel",
+                9: "glu_tc_kernel (tcgen05)",
                 6: "gdn_gates_kernel",
                 8: "glu_backward (the forward kernel with the dG/dU epilogue, glu_bwd_h_kernel, "
                    "glu_bwd_h_reduce_kernel, glu_bwd_w_kernel)"}
@@ -503,8 +508,8 @@ def main():
     blocks = row_blocks(w, M)
     block_rows = [min(BLOCK_M, M - m0) for m0 in range(0, M, BLOCK_M)] if blocks > 1 else [M]
     launches_per_call = blocks * (2 if (w.op == "add_rmsnorm_glu" and not single) else 1)
-    if w.op == "glu_backward":
-        launches_per_call = 4
+    if w.op == "glu_backward":   # dG/dU per 16-row block, grad_h and its reduce per 8-row pass, the weight gradients
+        launches_per_call = -(-M // 16) + 2 * (-(-M // 8)) + 1
 
     def one_step():
         for i in range(L):
@@ -527,7 +532,12 @@ def main():
         one_step()  # first calls initialise the library's per-device table before capture
         torch.cuda.synchronize(dev)
         variant = mb.last_variant()
+        if variant == TCGEN05:      # the whole batch in one pass: one launch per call
+            blocks, block_rows, launches_per_call = 1, [M], 1
         if variant == ROW_BLOCKS:   # the kernel of a full block: one call on the first block's rows
+            blocks = -(-M // BLOCK_M)
+            block_rows = [min(BLOCK_M, M - m0) for m0 in range(0, M, BLOCK_M)]
+            launches_per_call = blocks * (2 if (w.op == "add_rmsnorm_glu" and not single) else 1)
             if w.op == "glu_gemv":
                 mb.glu_gemv(h[:block_rows[0]], gates[0], ups[0], out=outs[0, :block_rows[0], lo:hi], mode=mode)
             else:

@@ -46,12 +46,15 @@
  *     arithmetic rules.
  *   - Results are bitwise deterministic run to run (no atomics in any sum)
  *     and do not depend on where a row falls in the matrix.
- *   - One pass of the GEMV kernels takes up to MBGLU_BLOCK_M = 16 batch rows.
- *     A batch of 17..64 rows (PR #9057, the commit squashing the A100
- *     optimisation session, runs decode at batch 8, 32 and 64) runs as row
- *     blocks of 16, the remainder last, each block a full pass
- *     over both weights: M = 64 streams the weights four times.  Each row's
- *     result is the one a call on that row alone gives.
+ *   - A batch of 17..64 rows (PR #9057, the commit squashing the A100
+ *     optimisation session, runs decode at batch 8, 32 and 64) runs in one
+ *     pass over the weights on the fifth-generation tensor cores where
+ *     glu_gemv's operands are 16-byte aligned with row strides that are
+ *     multiples of 8 elements and K % 8 == 0.  Otherwise, and in the
+ *     add_rmsnorm_glu entry points, it runs as row blocks of MBGLU_BLOCK_M =
+ *     16 rows, the remainder last, each block a full pass over both weights
+ *     (M = 64 streams them four times); each row's result is then the one a
+ *     call on that row alone gives.
  */
 #ifndef MBGLU_H
 #define MBGLU_H
@@ -127,7 +130,7 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh,
  * glu_backward -- the gradients of glu_gemv's exact composite
  * out = SiLU(h gate_w^T) * (h up_w^T) for an upstream gradient dout.
  * [8602/PlanB] "Plan B Design": an autograd.Function reading the original
- * Parameters, so that gradients flow to gate.weight and up.weight (the
+ * Parameters, so that the gradients reach gate.weight and up.weight (the
  * "Verification Results" compare them with the composite's).  In fp32 from
  * the bf16 operands:
  *   g, u     = the forward's dot products (fp32 accumulation)
@@ -145,9 +148,10 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh,
  *   workspace  device memory of glu_backward_workspace_bytes(M, N, K)
  *            bytes, 16-byte aligned, owned by the caller; its contents are
  *            undefined afterwards
- *   0 <= M <= MBGLU_BLOCK_M, N >= 0, K >= 0.  K == 0: no-op.  M == 0 or
+ *   0 <= M <= MBGLU_MAX_M, N >= 0, K >= 0.  K == 0: no-op.  M == 0 or
  *   N == 0: the gradients that remain are written as zeros (no workspace
- *   needed).
+ *   needed).  Batches above 16 rows compute dG and dU per 16-row block and
+ *   grad_h per 8-row pass; the weight gradients sum over all M rows at once.
  * Outputs must not overlap the inputs, one another or the workspace
  * (MBGLU_ERR_ALIAS).  Asynchronous on `stream`; no allocation; the sums run
  * in a fixed order, so results are bitwise deterministic.
@@ -377,7 +381,8 @@ int mbglu_last_cuda_error(void);
  * 0 none (no-op), 1 streaming kernel (CUDA-core FMA), 2 generic kernel,
  * 3 zero fill, 4 tensor-core streaming kernel (batch >= 3), 5 silu_mul,
  * 6 gdn_gates, 7 row blocks (a batch above MBGLU_BLOCK_M: one of 1-4 per
- * block), 8 glu_backward. */
+ * block), 8 glu_backward, 9 the tcgen05 kernel (a batch above MBGLU_BLOCK_M in one
+ * pass). */
 int mbglu_last_variant(void);
 
 /* How many row blocks of the calling thread's last add_rmsnorm_glu* call ran

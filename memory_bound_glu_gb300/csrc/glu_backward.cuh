@@ -45,7 +45,8 @@ struct BwdParams {
     int ldm;                // row stride of dG, dU (N; the rows kernel's block offset applies to the pointers)
     int R, S;               // glu_bwd_rows_kernel: rows per stage, stages in the ring
     uint32_t off_ring;      // glu_bwd_rows_kernel: ring offset in dynamic shared memory
-    int rows_cta;           // glu_bwd_rows_kernel: largest row share of a CTA
+    int rows_cta;           // glu_bwd_rows_kernel, glu_bwd_hw_kernel: largest row share of a CTA
+    int col_groups;         // glu_bwd_hw_kernel: CTAs sharing a row share (each a group of column slices)
     int vec_w;              // gate, up rows 8-byte aligned: 4-element loads
     int vec_out;            // grad_gate, grad_up rows and h 16-byte aligned, K % 8 == 0: 8-element access
     int h_smem;             // glu_bwd_w_kernel: h staged in shared memory
@@ -280,6 +281,164 @@ __global__ void __launch_bounds__(kBwdRowsThreads, 1) glu_bwd_rows_kernel(const 
     }
 }
 
+// Steps 2 and 3 of the backward in one pass over the rows (M <= MB <= 8,
+// operands 16-byte aligned with row strides of whole chunks, K % 8 == 0):
+// CTA (s, c) owns a balanced share [n0, n1) of the N rows and a group of
+// Wc 256-column slices; warp w of the CTA owns one slice and lane l its
+// 8 columns k.  Each warp streams the share's rows of both weights for its
+// slice through its own ring of S stages (one TMA box of R rows x 256
+// columns per matrix and stage), LAST rows first -- the first step read the
+// share in rising order and left its tail in L2 -- with no CTA-wide barrier
+// in the loop.  For each row n, lane l
+//   * adds dG[m][n] Wg[n][k] + dU[m][n] Wu[n][k] into its fp32 grad_h
+//     partials (m < M), and
+//   * writes grad_gate[n][k] = bf16(sum_m dG[m][n] h[m][k]) and grad_up
+//     likewise (m in order), 16-byte streaming stores, h kept unpacked in
+//     registers.
+// So the weights are read once here and every gradient element is written
+// once.  part[s][m][k] receives the share's grad_h sums;
+// glu_bwd_h_reduce8_kernel adds the shares in order.  The share's dG and dU
+// are staged in shared memory after the dependency wait; the first stages of
+// weights are requested before it.
+// Dynamic shared memory: [0, 256) barriers [warp][stage], [256, off_ring)
+// dG and dU ([2][MB][rows_cta] fp32), [off_ring, ...) ring[warp][stage]
+// [2][R][256] bf16.
+constexpr int kBwdSlice = 256;   // columns per warp: one TMA box row (512 bytes)
+
+struct BwdMaps {
+    TensorMap gate, up;   // [N][K] bf16, box 256 x R, no swizzle
+};
+
+// the most warps (column slices) per CTA at batch tile MB: the registers of
+// 32 * warps threads (~190 each at MB = 8) must fit the SM's 65536
+__host__ __device__ constexpr int bwd_hw_warps(int MB) { return MB >= 8 ? 10 : MB >= 4 ? 14 : 16; }
+
+template <int MB>
+__global__ void __launch_bounds__(32 * bwd_hw_warps(MB), 1) glu_bwd_hw_kernel(const BwdParams q,
+                                                                            const __grid_constant__ BwdMaps maps)
+{
+    extern __shared__ __align__(128) unsigned char hw_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = q.S, R = q.R;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(hw_smem) + warp * S;
+    float *dg_s = reinterpret_cast<float *>(hw_smem + 256);
+    float *du_s = dg_s + MB * q.rows_cta;
+    const uint32_t stage_bytes = 2u * static_cast<uint32_t>(R) * kBwdSlice * 2u;
+    unsigned char *ring = hw_smem + q.off_ring + static_cast<uint32_t>(warp) * S * stage_bytes;
+    const int G = gridDim.x / q.col_groups;
+    const int share = blockIdx.x / q.col_groups, cgrp = blockIdx.x - share * q.col_groups;
+    const int n0 = static_cast<int>((static_cast<int64_t>(q.N) * share) / G);
+    const int n1 = static_cast<int>((static_cast<int64_t>(q.N) * (share + 1)) / G);
+    const int rows = n1 - n0, nblk = (rows + R - 1) / R;
+    const int x0 = (cgrp * static_cast<int>(blockDim.x >> 5) + warp) * kBwdSlice;   // the warp's first column
+    const int col = x0 + 8 * lane;
+    const bool active = x0 < q.K && col < q.K;
+    const uint64_t policy = l2_policy_evict_first();
+
+    // block j: rows [lo, hi) with hi = n1 - j R; the box starts at lo
+    auto fill = [&](int j) {
+        const int hi = n1 - j * R, lo = max(n0, hi - R);
+        const int st = j % S;
+        unsigned char *dst = ring + st * stage_bytes;
+        mbar_arrive_expect_tx(&bars[st], stage_bytes);
+        tma_load_2d(dst, &maps.gate, x0, lo, &bars[st], policy);
+        tma_load_2d(dst + stage_bytes / 2, &maps.up, x0, lo, &bars[st], policy);
+    };
+
+    if (lane == 0 && x0 < q.K) {
+        for (int st = 0; st < S; ++st) mbar_init(&bars[st], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (lane == 0 && x0 < q.K)
+        for (int j = 0; j < min(S, nblk); ++j) fill(j);   // weights only: before the dependency wait
+    grid_dependency_wait();                                 // dG, dU of the first step
+    for (int i = threadIdx.x; i < q.M * rows; i += blockDim.x) {
+        const int m = i / rows, r = i - m * rows;
+        dg_s[m * q.rows_cta + r] = q.dG[static_cast<int64_t>(m) * q.ldm + n0 + r];
+        du_s[m * q.rows_cta + r] = q.dU[static_cast<int64_t>(m) * q.ldm + n0 + r];
+    }
+    float2 hf[MB][4];   // h's 8 columns of this lane, unpacked once
+#pragma unroll
+    for (int m = 0; m < MB; ++m) {
+        const uint4 v = (m < q.M && active) ? *reinterpret_cast<const uint4 *>(q.h + m * q.ldh + col)
+                                            : make_uint4(0, 0, 0, 0);
+        hf[m][0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+        hf[m][1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+        hf[m][2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+        hf[m][3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
+    }
+    __syncthreads();   // dG, dU staged
+    if (x0 >= q.K) return;   // a slice past K (the last column group): no rows to stream
+
+    float2 acc[MB][4];
+#pragma unroll
+    for (int m = 0; m < MB; ++m)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[m][k] = make_float2(0.0f, 0.0f);
+
+    for (int j = 0; j < nblk; ++j) {
+        const int st = j % S;
+        const uint32_t phase = static_cast<uint32_t>(j / S) & 1u;
+        if (!mbar_wait_bounded(&bars[st], phase, kWaitLimitNs)) {
+            if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
+            mbar_wait_bounded(&bars[st], phase, kWaitLimitNs);
+        }
+        const int hi = n1 - j * R, lo = max(n0, hi - R);
+        const uint16_t *gs = reinterpret_cast<const uint16_t *>(ring + st * stage_bytes);
+        const uint16_t *us = gs + R * kBwdSlice;
+        if (active) {
+            for (int i = hi - lo - 1; i >= 0; --i) {   // descending rows
+                const int r = lo - n0 + i;
+                const int64_t n = lo + i;
+                const uint4 g4 = *reinterpret_cast<const uint4 *>(gs + i * kBwdSlice + 8 * lane);
+                const uint4 u4 = *reinterpret_cast<const uint4 *>(us + i * kBwdSlice + 8 * lane);
+                const float2 gv[4] = {make_float2(bf16_lo(g4.x), bf16_hi(g4.x)), make_float2(bf16_lo(g4.y), bf16_hi(g4.y)),
+                                      make_float2(bf16_lo(g4.z), bf16_hi(g4.z)), make_float2(bf16_lo(g4.w), bf16_hi(g4.w))};
+                const float2 uv[4] = {make_float2(bf16_lo(u4.x), bf16_hi(u4.x)), make_float2(bf16_lo(u4.y), bf16_hi(u4.y)),
+                                      make_float2(bf16_lo(u4.z), bf16_hi(u4.z)), make_float2(bf16_lo(u4.w), bf16_hi(u4.w))};
+                float2 sg[4], su[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) sg[k] = su[k] = make_float2(0.0f, 0.0f);
+#pragma unroll
+                for (int m = 0; m < MB; ++m) {
+                    const float a = dg_s[m * q.rows_cta + r], bb = du_s[m * q.rows_cta + r];
+                    const float2 a2 = make_float2(a, a), b2 = make_float2(bb, bb);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        acc[m][k] = __ffma2_rn(b2, uv[k], __ffma2_rn(a2, gv[k], acc[m][k]));
+                        sg[k] = __ffma2_rn(a2, hf[m][k], sg[k]);
+                        su[k] = __ffma2_rn(b2, hf[m][k], su[k]);
+                    }
+                }
+                __stcs(reinterpret_cast<uint4 *>(q.grad_gate + n * q.ldgg + col),
+                       make_uint4(pack_bf16x2(sg[0].x, sg[0].y), pack_bf16x2(sg[1].x, sg[1].y),
+                                  pack_bf16x2(sg[2].x, sg[2].y), pack_bf16x2(sg[3].x, sg[3].y)));
+                __stcs(reinterpret_cast<uint4 *>(q.grad_up + n * q.ldgu + col),
+                       make_uint4(pack_bf16x2(su[0].x, su[0].y), pack_bf16x2(su[1].x, su[1].y),
+                                  pack_bf16x2(su[2].x, su[2].y), pack_bf16x2(su[3].x, su[3].y)));
+            }
+        }
+        __syncwarp();
+        if (lane == 0 && j + S < nblk) {
+            fence_proxy_async_smem();
+            fill(j + S);
+        }
+        __syncwarp();
+    }
+    grid_launch_dependents();
+    if (active) {
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            if (m < q.M) {
+                float4 *dst = reinterpret_cast<float4 *>(q.part + (static_cast<int64_t>(share) * q.M + m) * q.K + col);
+                dst[0] = make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
+                dst[1] = make_float4(acc[m][2].x, acc[m][2].y, acc[m][3].x, acc[m][3].y);
+            }
+        }
+    }
+}
+
 // grad_h[m][k] = bf16( part[0][m][k] + part[1][m][k] + ... ), splits in order
 __global__ void __launch_bounds__(256) glu_bwd_h_reduce_kernel(const BwdParams q, int nsplit)
 {
@@ -290,6 +449,120 @@ __global__ void __launch_bounds__(256) glu_bwd_h_reduce_kernel(const BwdParams q
         float s = q.part[i];
         for (int b = 1; b < nsplit; ++b) s += q.part[static_cast<int64_t>(b) * total + i];
         q.grad_h[m * q.ldgh + k] = f32_to_bf16(s);
+    }
+}
+
+// grad_h[m][8c .. 8c+7] = bf16( the sum of the nsplit partials ), the main
+// path (K % 8 == 0): one warp per (row m, 8-column chunk c); lane l adds
+// partials l, l + 32, ... in order, then a fixed butterfly adds the lanes.
+__global__ void __launch_bounds__(256) glu_bwd_h_reduce8_kernel(const BwdParams q, int nsplit, int vec_store)
+{
+    const int lane = threadIdx.x & 31;
+    const int chunks = q.K >> 3;
+    const int64_t nwarp = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    const int64_t total = static_cast<int64_t>(q.M) * chunks;
+    for (int64_t w = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
+         w += nwarp) {
+        const int m = static_cast<int>(w / chunks), c = static_cast<int>(w - static_cast<int64_t>(m) * chunks);
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int b = lane; b < nsplit; b += 32) {
+            const float4 *src = reinterpret_cast<const float4 *>(q.part + (static_cast<int64_t>(b) * q.M + m) * q.K + 8 * c);
+            const float4 x = src[0], y = src[1];
+            v[0] += x.x;
+            v[1] += x.y;
+            v[2] += x.z;
+            v[3] += x.w;
+            v[4] += y.x;
+            v[5] += y.y;
+            v[6] += y.z;
+            v[7] += y.w;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], off);
+        if (lane == 0) {
+            uint16_t *dst = q.grad_h + static_cast<int64_t>(m) * q.ldgh + 8 * c;
+            if (vec_store) {
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                             pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) dst[i] = f32_to_bf16(v[i]);
+            }
+        }
+    }
+}
+
+// grad_gate[n][k] = bf16( sum_m dG[m][n] h[m][k] ), grad_up likewise with dU,
+// the m-sum in order m = 0, 1, ...: the main path at M <= MB <= 8 (K % 8 ==
+// 0, gradients and h 16-byte aligned with row strides of whole chunks).  CTA
+// b owns a balanced share [n0, n1) of the rows; thread t owns the 8-column
+// chunks t, t + T, ... (CPT of them) and keeps h's columns there in
+// registers; the share's dG and dU are staged in shared memory.  Each row's
+// two gradient rows are written once, with streaming stores.
+template <int MB, int CPT>
+__global__ void __launch_bounds__(kBwdRowsThreads, 1) glu_bwd_w_rows_kernel(const BwdParams q)
+{
+    extern __shared__ __align__(16) float wdg_s[];   // [2][MB][rows_cta]
+    float *du_s = wdg_s + MB * q.rows_cta;
+    const int b = blockIdx.x, G = gridDim.x, K = q.K;
+    const int n0 = static_cast<int>((static_cast<int64_t>(q.N) * b) / G);
+    const int n1 = static_cast<int>((static_cast<int64_t>(q.N) * (b + 1)) / G);
+    const int rows = n1 - n0;
+    grid_dependency_wait();
+    for (int i = threadIdx.x; i < q.M * rows; i += blockDim.x) {
+        const int m = i / rows, r = i - m * rows;
+        wdg_s[m * q.rows_cta + r] = q.dG[static_cast<int64_t>(m) * q.ldm + n0 + r];
+        du_s[m * q.rows_cta + r] = q.dU[static_cast<int64_t>(m) * q.ldm + n0 + r];
+    }
+    float2 hf[CPT][MB][4];   // h's columns of this thread, unpacked once
+#pragma unroll
+    for (int cc = 0; cc < CPT; ++cc) {
+        const int col = 8 * (threadIdx.x + cc * blockDim.x);
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            const uint4 v = (m < q.M && col < K) ? *reinterpret_cast<const uint4 *>(q.h + m * q.ldh + col)
+                                                 : make_uint4(0, 0, 0, 0);
+            hf[cc][m][0] = make_float2(bf16_lo(v.x), bf16_hi(v.x));
+            hf[cc][m][1] = make_float2(bf16_lo(v.y), bf16_hi(v.y));
+            hf[cc][m][2] = make_float2(bf16_lo(v.z), bf16_hi(v.z));
+            hf[cc][m][3] = make_float2(bf16_lo(v.w), bf16_hi(v.w));
+        }
+    }
+    __syncthreads();
+    grid_launch_dependents();
+    for (int r = 0; r < rows; ++r) {
+        const int64_t n = n0 + r;
+        float a[MB], bb[MB];
+#pragma unroll
+        for (int m = 0; m < MB; ++m) {
+            a[m] = m < q.M ? wdg_s[m * q.rows_cta + r] : 0.0f;
+            bb[m] = m < q.M ? du_s[m * q.rows_cta + r] : 0.0f;
+        }
+#pragma unroll
+        for (int cc = 0; cc < CPT; ++cc) {
+            const int col = 8 * (threadIdx.x + cc * blockDim.x);
+            if (col >= K) continue;
+            float2 sg[4], su[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sg[j] = su[j] = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int m = 0; m < MB; ++m) {
+                const float2 a2 = make_float2(a[m], a[m]), b2 = make_float2(bb[m], bb[m]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    sg[j] = __ffma2_rn(a2, hf[cc][m][j], sg[j]);
+                    su[j] = __ffma2_rn(b2, hf[cc][m][j], su[j]);
+                }
+            }
+            __stcs(reinterpret_cast<uint4 *>(q.grad_gate + n * q.ldgg + col),
+                   make_uint4(pack_bf16x2(sg[0].x, sg[0].y), pack_bf16x2(sg[1].x, sg[1].y),
+                              pack_bf16x2(sg[2].x, sg[2].y), pack_bf16x2(sg[3].x, sg[3].y)));
+            __stcs(reinterpret_cast<uint4 *>(q.grad_up + n * q.ldgu + col),
+                   make_uint4(pack_bf16x2(su[0].x, su[0].y), pack_bf16x2(su[1].x, su[1].y),
+                              pack_bf16x2(su[2].x, su[2].y), pack_bf16x2(su[3].x, su[3].y)));
+        }
     }
 }
 

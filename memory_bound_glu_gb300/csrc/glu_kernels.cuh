@@ -312,14 +312,13 @@ __device__ __forceinline__ uint16_t norm_elem(float sv, float w, float ih, float
     return near_midpoint(v) ? norm_elem_df(sv, w, ih, il) : f32_to_bf16(v);
 }
 
-// 8 elements of h from 8 of s and of w (bf16 pairs); the double-float
-// evaluation runs for the whole chunk in the rare case one element needs it
-__device__ __forceinline__ uint4 norm_chunk(uint4 v, uint4 w, float ih, float il)
+// 8 elements of h from 8 of s and of w (bf16 pairs) in fp32; `near` is set
+// if any of them needs the double-float evaluation (norm_fix_rows)
+__device__ __forceinline__ uint4 norm_chunk_f32(uint4 v, uint4 w, float ih, bool &near)
 {
     const uint32_t sv[4] = {v.x, v.y, v.z, v.w};
     const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
     uint32_t o[4];
-    bool near = false;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float lo = norm_elem_f32(bf16_lo(sv[j]), bf16_lo(ww[j]), ih);
@@ -327,13 +326,30 @@ __device__ __forceinline__ uint4 norm_chunk(uint4 v, uint4 w, float ih, float il
         near |= near_midpoint(lo) | near_midpoint(hi);
         o[j] = pack_bf16x2(lo, hi);
     }
-    if (near) {
-#pragma unroll
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The rare second pass of a thread one of whose chunks holds an element near
+// a bf16 midpoint: the chunks c0 + i P with bit i of `mask` set still hold s
+// (the fast pass left them alone) and are formed again element by element.
+// Out of line, so that the hot loop stays small: every CTA fetches that code
+// once per launch, and instruction-cache misses set the prologue's pace.
+__device__ __noinline__ void norm_fix_chunks(uint4 *row, const uint4 *w_row, int c0, int P, uint64_t mask, float ih,
+                                             float il)
+{
+    while (mask) {
+        const int i = __ffsll(static_cast<long long>(mask)) - 1;
+        mask &= mask - 1;
+        const int c = c0 + i * P;
+        const uint4 v = row[c], w = w_row[c];
+        const uint32_t sv[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+        uint32_t o[4];
         for (int j = 0; j < 4; ++j)
             o[j] = static_cast<uint32_t>(norm_elem(bf16_lo(sv[j]), bf16_lo(ww[j]), ih, il)) |
                    (static_cast<uint32_t>(norm_elem(bf16_hi(sv[j]), bf16_hi(ww[j]), ih, il)) << 16);
+        row[c] = make_uint4(o[0], o[1], o[2], o[3]);
     }
-    return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // ---------------------------------------------------------------------------
@@ -498,37 +514,31 @@ __device__ __forceinline__ void x_prefetch_rows(const GluParams &p, const RowMap
 }
 
 // s = bf16(x + residual) formed in place in h_s (the fp32 sum of two bf16
-// values rounds to the same bf16 as the exact sum); returns this thread's
-// sum of s^2 over its chunks, in chunk order, as a double-float.
-__device__ __forceinline__ float2 add_rows_in_place(const GluParams &p, const RowMap &r, uint16_t *h_s, int hstride,
-                                                    XRows &x)
+// values rounds to the same bf16 as the exact sum).
+__device__ __forceinline__ void add_rows_in_place(const GluParams &p, const RowMap &r, uint16_t *h_s, int hstride,
+                                                  XRows &x)
 {
-    SumSq ss = sumsq_zero();
     uint4 *row = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
     for (int j0 = 0;; j0 += kXRows) {
         if (j0 > 0) x_prefetch_rows(p, r, x, j0);
 #pragma unroll
         for (int j = 0; j < kXRows; ++j) {
             const int c = r.c0 + (j0 + j) * r.P;
-            if (r.active && c < r.nch) {
-                const uint4 sv = add_bf16x8(x.v[j], row[c]);
-                row[c] = sv;
-                sumsq_bf16x8(sv, ss);
-            }
+            if (r.active && c < r.nch) row[c] = add_bf16x8(x.v[j], row[c]);
         }
         if (!r.active || r.c0 + (j0 + kXRows) * r.P >= r.nch) break;
     }
-    return sumsq_total(ss);
 }
 
 // This thread's sum of s^2 over its chunks of h_s, in chunk order, as a
-// double-float.
+// double-float.  A compact loop: the prologue's code is fetched by every CTA
+// once per launch.
 __device__ __forceinline__ float2 square_rows(const RowMap &r, const uint16_t *h_s, int hstride)
 {
     SumSq ss = sumsq_zero();
     if (!r.active) return make_float2(0.0f, 0.0f);
     const uint4 *row = reinterpret_cast<const uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
-#pragma unroll 4
+#pragma unroll 1
     for (int c = r.c0; c < r.nch; c += r.P) sumsq_bf16x8(row[c], ss);
     return sumsq_total(ss);
 }
@@ -580,8 +590,18 @@ __device__ __forceinline__ void norm_rows_in_place(const GluParams &p, const Row
         const float ih = inv_s[2 * r.m], il = inv_s[2 * r.m + 1];
         uint4 *row = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
         const uint4 *wv = reinterpret_cast<const uint4 *>(w_s);
-#pragma unroll 4
-        for (int c = r.c0; c < r.nch; c += r.P) row[c] = norm_chunk(row[c], wv[c], ih, il);
+        uint64_t mask = 0;   // this thread's chunks left as s for norm_fix_chunks (at most 40 of them)
+        int i = 0;
+#pragma unroll 2
+        for (int c = r.c0; c < r.nch; c += r.P, ++i) {
+            bool near = false;
+            const uint4 hv = norm_chunk_f32(row[c], wv[c], ih, near);
+            if (near)
+                mask |= 1ull << i;
+            else
+                row[c] = hv;
+        }
+        if (mask) norm_fix_chunks(row, wv, r.c0, r.P, mask, ih, il);
     }
     for (int i = tid; i < (rows_out - p.M) * r.nch; i += blockDim.x) {
         const int m = p.M + i / r.nch, c = i - (i / r.nch) * r.nch;
@@ -744,7 +764,9 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
     fence_mbar_init();
     __syncthreads();
 
-    const uint64_t policy = l2_policy_evict_first();
+    // the backward's next step reads the weights again (last rows first):
+    // keep them in L2 in that mode
+    const uint64_t policy = p.mode == kModeBwd ? l2_policy_evict_last() : l2_policy_evict_first();
     // lane 0: request unit (group g, segment seg) into stage st
     auto issue = [&](int st, int g, int seg) {
         const int row0 = group_row0(g);
@@ -824,13 +846,11 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
         XRows xr;
         if (p.fused) x_prefetch_rows(p, rm, xr);
         prologue_wait(pro_bar);
-        float2 ss;
         if (p.fused) {
             if (threadIdx.x == 0) fused_arrive(p);
-            ss = add_rows_in_place(p, rm, h_s, K, xr);
-        } else {
-            ss = square_rows(rm, h_s, K);
+            add_rows_in_place(p, rm, h_s, K, xr);
         }
+        const float2 ss = square_rows(rm, h_s, K);
         norm_rows_in_place(p, rm, ss, h_s, K, nw_s, red, inv_s, MB);
     } else if constexpr (!HREG) {
         if (p.vec_in) {
@@ -1160,7 +1180,9 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     fence_mbar_init();
     __syncthreads();
 
-    const uint64_t policy = l2_policy_evict_first();
+    // the backward's next step reads the weights again (last rows first):
+    // keep them in L2 in that mode
+    const uint64_t policy = p.mode == kModeBwd ? l2_policy_evict_last() : l2_policy_evict_first();
     // Tensor copies need 128-byte aligned destinations: every stage and its
     // up half sit at multiples of 128 bytes from the ring (32 * (KS + 8) and
     // 16 * (KS + 8) bytes with KS % 16 == 0), so checking the ring suffices.
@@ -1233,13 +1255,11 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         XRows xr;
         if (p.fused) x_prefetch_rows(p, rm, xr);
         prologue_wait(pro_bar);
-        float2 ss;
         if (p.fused) {
             if (threadIdx.x == 0) fused_arrive(p);
-            ss = add_rows_in_place(p, rm, h_s, HS, xr);
-        } else {
-            ss = square_rows(rm, h_s, HS);
+            add_rows_in_place(p, rm, h_s, HS, xr);
         }
+        const float2 ss = square_rows(rm, h_s, HS);
         norm_rows_in_place(p, rm, ss, h_s, HS, nw_s, red, inv_s, p.M);
     } else if (p.vec_in) {
         if (threadIdx.x == 0) {
@@ -1562,12 +1582,24 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *x, int64_
     grid_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (vec) {
+        // chunk i = m * nch + c, visited i, i + stride, ...: (m, c) advance by
+        // (stride / nch, stride % nch) with a carry, one division per thread
         const int nch = N >> 3;
         const int64_t total = static_cast<int64_t>(M) * nch;
         int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+        const int64_t dm = stride / nch, dc = stride - dm * nch;
+        int64_t m0 = i / nch, c0 = i - m0 * nch;
+        auto step = [&](int64_t &m, int64_t &c) {
+            m += dm;
+            c += dc;
+            if (c >= nch) {
+                c -= nch;
+                ++m;
+            }
+        };
         for (; i + stride < total; i += 2 * stride) {
-            const int64_t m0 = i / nch, c0 = i - m0 * nch;
-            const int64_t i1 = i + stride, m1 = i1 / nch, c1 = i1 - m1 * nch;
+            int64_t m1 = m0, c1 = c0;
+            step(m1, c1);
             const uint16_t *r0 = x + m0 * ldx + c0 * 8, *r1 = x + m1 * ldx + c1 * 8;
             const uint4 g0 = __ldcs(reinterpret_cast<const uint4 *>(r0));
             const uint4 u0 = __ldcs(reinterpret_cast<const uint4 *>(r0 + N));
@@ -1575,9 +1607,11 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *x, int64_
             const uint4 u1 = __ldcs(reinterpret_cast<const uint4 *>(r1 + N));
             __stcs(reinterpret_cast<uint4 *>(out + m0 * ldo + c0 * 8), silu_mul_chunk(g0, u0, mode));
             __stcs(reinterpret_cast<uint4 *>(out + m1 * ldo + c1 * 8), silu_mul_chunk(g1, u1, mode));
+            m0 = m1;
+            c0 = c1;
+            step(m0, c0);
         }
         if (i < total) {
-            const int64_t m0 = i / nch, c0 = i - m0 * nch;
             const uint16_t *r0 = x + m0 * ldx + c0 * 8;
             const uint4 g0 = __ldcs(reinterpret_cast<const uint4 *>(r0));
             const uint4 u0 = __ldcs(reinterpret_cast<const uint4 *>(r0 + N));
@@ -1603,6 +1637,21 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *x, int64_
 // x > 0, log1p(e^x) otherwise -- never e^x of a large x -- and sigmoid from
 // e^-|y| likewise.  Elementwise; a and b are row-strided views (e.g. columns
 // of one projection output).
+// One (token, head) of gdn_gates: a, b the inputs, neg_a = -exp(A_log[j]),
+// dt = dt_bias[j].
+__device__ __forceinline__ void gdn_gate_one(float a, float b, float neg_a, float dt, float &g, uint16_t &beta)
+{
+    const float x = a + dt;
+    const float sp = x > 0.0f ? x + log1pf(expf(-x)) : log1pf(expf(x));
+    g = neg_a * sp;
+    // sigmoid without overflow: 1/(1 + e^-y) sends e^-y to +inf in fp32 for
+    // y < -88.7 and returns 0, although e^y is still a (subnormal) bf16
+    // value down to y ~ -92
+    const float ty = expf(-fabsf(b));
+    beta = f32_to_bf16((b >= 0.0f ? 1.0f : ty) / (1.0f + ty));
+}
+
+// Any shape: one thread per element.
 __global__ void __launch_bounds__(256) gdn_gates_kernel(const uint16_t *a, int64_t lda, const uint16_t *b,
                                                         int64_t ldb, const float *A_log, const float *dt_bias,
                                                         float *g, int64_t ldg, uint16_t *beta, int64_t ldbeta,
@@ -1614,15 +1663,62 @@ __global__ void __launch_bounds__(256) gdn_gates_kernel(const uint16_t *a, int64
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t t = i / H, j = i - t * H;
-        const float x = bf16_to_f32(a[t * lda + j]) + dt_bias[j];
-        const float sp = x > 0.0f ? x + log1pf(expf(-x)) : log1pf(expf(x));
-        g[t * ldg + j] = -expf(A_log[j]) * sp;
-        // sigmoid without overflow: 1/(1 + e^-y) sends e^-y to +inf in fp32 for
-        // y < -88.7 and returns 0, although e^y is still a (subnormal) bf16
-        // value down to y ~ -92
-        const float y = bf16_to_f32(b[t * ldb + j]);
-        const float ty = expf(-fabsf(y));
-        beta[t * ldbeta + j] = f32_to_bf16((y >= 0.0f ? 1.0f : ty) / (1.0f + ty));
+        gdn_gate_one(bf16_to_f32(a[t * lda + j]), bf16_to_f32(b[t * ldb + j]), -expf(A_log[j]), dt_bias[j],
+                     g[t * ldg + j], beta[t * ldbeta + j]);
+    }
+}
+
+// Up to kGdnMaxHeads heads, T * ceil(H/8) < 2^31: one thread per (token, 8
+// consecutive heads), 32-bit index arithmetic, the heads' -exp(A_log) and
+// dt_bias computed once per CTA into shared memory.  vec: H % 8 == 0 and
+// every row 16-byte aligned -- 16-byte loads of a and b, 16-byte stores of
+// g (two) and beta, all streaming.
+constexpr int kGdnMaxHeads = 4096;
+
+__global__ void __launch_bounds__(256) gdn_gates_chunk_kernel(const uint16_t *a, int64_t lda, const uint16_t *b,
+                                                              int64_t ldb, const float *A_log, const float *dt_bias,
+                                                              float *g, int64_t ldg, uint16_t *beta, int64_t ldbeta,
+                                                              int T, int H, int vec)
+{
+    __shared__ float neg_a_s[kGdnMaxHeads], dt_s[kGdnMaxHeads];
+    grid_dependency_wait();
+    grid_launch_dependents();
+    for (int j = threadIdx.x; j < H; j += blockDim.x) {
+        neg_a_s[j] = -expf(A_log[j]);
+        dt_s[j] = dt_bias[j];
+    }
+    __syncthreads();
+    const uint32_t hc = static_cast<uint32_t>(H + 7) >> 3;
+    const uint32_t items = static_cast<uint32_t>(T) * hc;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < items; i += gridDim.x * blockDim.x) {
+        const uint32_t t = i / hc;
+        const int j0 = static_cast<int>(i - t * hc) * 8;
+        const uint16_t *ar = a + static_cast<int64_t>(t) * lda + j0;
+        const uint16_t *br = b + static_cast<int64_t>(t) * ldb + j0;
+        float *gr = g + static_cast<int64_t>(t) * ldg + j0;
+        uint16_t *betar = beta + static_cast<int64_t>(t) * ldbeta + j0;
+        if (vec) {
+            const uint4 av = __ldcs(reinterpret_cast<const uint4 *>(ar));
+            const uint4 bv = __ldcs(reinterpret_cast<const uint4 *>(br));
+            const uint32_t aw[4] = {av.x, av.y, av.z, av.w}, bw[4] = {bv.x, bv.y, bv.z, bv.w};
+            float gv[8];
+            uint32_t be[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint16_t lo, hi;
+                gdn_gate_one(bf16_lo(aw[q]), bf16_lo(bw[q]), neg_a_s[j0 + 2 * q], dt_s[j0 + 2 * q], gv[2 * q], lo);
+                gdn_gate_one(bf16_hi(aw[q]), bf16_hi(bw[q]), neg_a_s[j0 + 2 * q + 1], dt_s[j0 + 2 * q + 1],
+                             gv[2 * q + 1], hi);
+                be[q] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            }
+            __stcs(reinterpret_cast<float4 *>(gr), make_float4(gv[0], gv[1], gv[2], gv[3]));
+            __stcs(reinterpret_cast<float4 *>(gr + 4), make_float4(gv[4], gv[5], gv[6], gv[7]));
+            __stcs(reinterpret_cast<uint4 *>(betar), make_uint4(be[0], be[1], be[2], be[3]));
+        } else {
+            const int n = min(8, H - j0);
+            for (int e = 0; e < n; ++e)
+                gdn_gate_one(bf16_to_f32(ar[e]), bf16_to_f32(br[e]), neg_a_s[j0 + e], dt_s[j0 + e], gr[e], betar[e]);
+        }
     }
 }
 

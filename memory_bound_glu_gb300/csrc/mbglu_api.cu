@@ -20,6 +20,7 @@
 #include "mbglu.h"
 #include "glu_kernels.cuh"
 #include "glu_backward.cuh"
+#include "glu_tc.cuh"
 
 namespace {
 
@@ -32,7 +33,8 @@ thread_local int t_last_single = 0;   // row blocks of the last norm call that r
 enum Variant {
     kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4, kSiluMul = 5, kGdnGates = 6,
     kRowBlocks = 7,  // a batch above kBlockRows, run as row blocks
-    kBackward = 8    // glu_backward
+    kBackward = 8,   // glu_backward
+    kTcGemv = 9      // the tcgen05 kernel (one pass for batch 17..64)
 };
 constexpr int kBlockRows = mbglu::kMaxM;   // rows one GEMV kernel takes (its batch tile)
 
@@ -77,6 +79,10 @@ struct Tuning {
     int mma_ks_min = 192;     // tensor-core plan: shortest K-segment worth one more warp
     int tma = 1;              // tensor-core kernel: whole groups by tensor copy (0: row by row)
     int phases = 0;           // tensor-core kernel: K-phases (0: automatic, 1: never, 2: always where allowed)
+    int tc = 1;               // batches of tc_min_m..64 on the tcgen05 kernel (0: row blocks)
+    int tc_min_m = 17;        // smallest batch that takes the tcgen05 kernel
+    int tc_split = 0;         // tcgen05 kernel: CTAs per tile (0: automatic, 1..4 where the plan allows)
+    int bwd_fused = 0;        // backward: steps 2 and 3 in one pass where they apply (0: separate kernels)
 };
 
 std::atomic<int> g_policy{MBGLU_POLICY_PREFETCH};
@@ -105,6 +111,10 @@ const Tuning &tuning()
         x.mma_ks_min = std::max(16, env_int("MBGLU_MMA_KS_MIN", 192));
         x.tma = env_int("MBGLU_TMA", 1) != 0;
         x.phases = std::min(2, std::max(0, env_int("MBGLU_PHASES", 0)));
+        x.tc = env_int("MBGLU_TC", 1) != 0;
+        x.tc_min_m = std::min(65, std::max(1, env_int("MBGLU_TC_MIN_M", 17)));
+        x.tc_split = std::min(mbglu::kTcMaxSplit, std::max(0, env_int("MBGLU_TC_SPLIT", 0)));
+        x.bwd_fused = env_int("MBGLU_BWD_FUSED", 0) != 0;
         return x;
     }();
     return t;
@@ -193,7 +203,17 @@ cudaError_t allow_smem_bwd_rows(int optin)
     MBGLU_ALLOW_ROWS(1, 1) MBGLU_ALLOW_ROWS(2, 1) MBGLU_ALLOW_ROWS(4, 1) MBGLU_ALLOW_ROWS(8, 1)
     MBGLU_ALLOW_ROWS(1, 2) MBGLU_ALLOW_ROWS(2, 2) MBGLU_ALLOW_ROWS(4, 2)
 #undef MBGLU_ALLOW_ROWS
+#define MBGLU_ALLOW_HW(TMB)                                                                                      \
+    if (e == cudaSuccess)                                                                                        \
+        e = cudaFuncSetAttribute(mbglu::glu_bwd_hw_kernel<TMB>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    MBGLU_ALLOW_HW(1) MBGLU_ALLOW_HW(2) MBGLU_ALLOW_HW(4) MBGLU_ALLOW_HW(8)
+#undef MBGLU_ALLOW_HW
     return e;
+}
+
+cudaError_t allow_smem_tc(int optin)
+{
+    return cudaFuncSetAttribute(mbglu::glu_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
 }
 
 mbglu_status device_info(const DeviceInfo **out)
@@ -212,7 +232,8 @@ mbglu_status device_info(const DeviceInfo **out)
             return cuda_fail(e);
         const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_mma<false>(d.smem_optin),
                                     allow_smem_mma<true>(d.smem_optin), allow_smem_generic(d.smem_optin),
-                                    allow_smem_bwd(), allow_smem_bwd_rows(d.smem_optin)};
+                                    allow_smem_bwd(), allow_smem_bwd_rows(d.smem_optin),
+                                    allow_smem_tc(d.smem_optin)};
         for (cudaError_t x : errs)
             if (x != cudaSuccess) return cuda_fail(x);
         d.ready = true;
@@ -496,15 +517,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 // Descriptor of an [N][K] bf16 weight (row stride ld elements) read in boxes
 // of box_k x 8 rows; elements past K or N read as zero.  False if the driver
 // rejects it (the kernel then copies row by row).
-bool encode_weight_map(mbglu::TensorMap *out, const void *base, int64_t ld, int N, int K, int box_k)
+bool encode_box_map(mbglu::TensorMap *out, const void *base, int64_t ld, int N, int K, int box_k, int box_rows)
 {
     static_assert(sizeof(CUtensorMap) == sizeof(mbglu::TensorMap), "tensor map size");
     const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
-    if (!fn || box_k > 256) return false;
+    if (!fn || box_k > 256 || box_rows < 1 || box_rows > 256) return false;
     CUtensorMap m;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(mbglu::kMmaRows)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t elem_strides[2] = {1u, 1u};
     if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -512,6 +533,11 @@ bool encode_weight_map(mbglu::TensorMap *out, const void *base, int64_t ld, int 
         return false;
     std::memcpy(out, &m, sizeof m);
     return true;
+}
+
+bool encode_weight_map(mbglu::TensorMap *out, const void *base, int64_t ld, int N, int K, int box_k)
+{
+    return encode_box_map(out, base, ld, N, K, box_k, mbglu::kMmaRows);
 }
 
 // Both weight descriptors for a tensor-core launch; p.tma says whether they
@@ -595,7 +621,13 @@ mbglu_status gdn_gates(const mbglu_bf16 *a, int64_t lda, const mbglu_bf16 *b, in
     mbglu_status st = device_info(&d);
     if (st != MBGLU_OK) return st;
     const int policy = g_policy.load(std::memory_order_relaxed);
-    const int64_t work = static_cast<int64_t>(T) * H;
+    // (token, 8 heads) per thread where the heads fit shared memory and the
+    // item count 32 bits; one element per thread otherwise
+    const int64_t chunks = static_cast<int64_t>(T) * ((H + 7) / 8);
+    const bool by_chunk = H <= mbglu::kGdnMaxHeads && chunks < (int64_t{1} << 31);
+    const int vec = H % 8 == 0 && aligned(a, 16) && aligned(b, 16) && aligned(g, 16) && aligned(beta, 16) &&
+                    lda % 8 == 0 && ldb % 8 == 0 && ldg % 4 == 0 && ldbeta % 8 == 0;
+    const int64_t work = by_chunk ? chunks : static_cast<int64_t>(T) * H;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(static_cast<int64_t>(d->sm_count) * 8,
                                                                             (work + 255) / 256)));
     cudaLaunchConfig_t cfg = {};
@@ -607,9 +639,13 @@ mbglu_status gdn_gates(const mbglu_bf16 *a, int64_t lda, const mbglu_bf16 *b, in
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = policy != MBGLU_POLICY_SERIAL ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, mbglu::gdn_gates_kernel, reinterpret_cast<const uint16_t *>(a), lda,
-                                             reinterpret_cast<const uint16_t *>(b), ldb, A_log, dt_bias, g, ldg,
-                                             reinterpret_cast<uint16_t *>(beta), ldbeta, T, H);
+    const uint16_t *a16 = reinterpret_cast<const uint16_t *>(a), *b16 = reinterpret_cast<const uint16_t *>(b);
+    uint16_t *beta16 = reinterpret_cast<uint16_t *>(beta);
+    const cudaError_t e =
+        by_chunk ? cudaLaunchKernelEx(&cfg, mbglu::gdn_gates_chunk_kernel, a16, lda, b16, ldb, A_log, dt_bias, g, ldg,
+                                      beta16, ldbeta, T, H, vec)
+                 : cudaLaunchKernelEx(&cfg, mbglu::gdn_gates_kernel, a16, lda, b16, ldb, A_log, dt_bias, g, ldg,
+                                      beta16, ldbeta, T, H);
     if (e != cudaSuccess) return cuda_fail(e);
     t_last_variant = kGdnGates;
     return MBGLU_OK;
@@ -786,6 +822,136 @@ mbglu_status gemv_block(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate
     return st;
 }
 
+// ---- the tcgen05 kernel (batch 17..64 in one pass) ----------------------------
+
+// A 2-D bf16 tensor map [rows][K] (row stride ld elements) with a box of 64 x
+// box_rows elements in the 128-byte swizzled layout; rows and columns past the
+// tensor arrive as zeros.
+bool encode_sw128_map(mbglu::TensorMap *out, const void *base, int64_t ld, int rows, int K, int box_rows)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
+    if (!fn || box_rows > 256) return false;
+    CUtensorMap m;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mbglu::kTcChunk), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t elem_strides[2] = {1u, 1u};
+    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::memcpy(out, &m, sizeof m);
+    return true;
+}
+
+struct TcPlan {
+    int Np = 0, nchunk = 0, ntiles = 0, ksplit = 1, stages = 0;
+    uint32_t smem = 0;
+};
+
+// Batch rows padded to a multiple of 16 (the MMA's N), 64-wide K chunks,
+// 128-row tiles; the K split (CTAs per tile, 1..4) that makes the longest
+// per-SM queue of work shortest (tiles * split CTAs in waves over the SMs),
+// the smaller one on a tie, with at least 2 chunks per CTA; as many stages
+// as fit, 2..8.  With a split of s, rank 0's stages must also hold the other
+// ranks' partial sums, (s - 1) x 2 Np x 128 fp32.
+bool plan_tc(const DeviceInfo &d, int M, int N, int K, TcPlan &pl)
+{
+    if (M < 1 || M > MBGLU_MAX_M || N < 1 || K < 1) return false;
+    pl.Np = (M + 15) / 16 * 16;
+    pl.nchunk = (K + mbglu::kTcChunk - 1) / mbglu::kTcChunk;
+    pl.ntiles = (N + mbglu::kTcRows - 1) / mbglu::kTcRows;
+    const uint32_t sbytes = 2 * mbglu::kTcWBytes + static_cast<uint32_t>(pl.Np) * 128u;
+    const int64_t room = static_cast<int64_t>(d.smem_optin) - mbglu::kTcHeader - mbglu::kTcSmemSlack;
+    pl.stages = static_cast<int>(std::min<int64_t>(mbglu::kTcMaxStages, room / sbytes));
+    if (pl.stages < 2) return false;
+    auto span = [&](int ks) {   // per-SM time in units of one full-K tile
+        const int64_t ctas = static_cast<int64_t>(pl.ntiles) * ks;
+        return static_cast<double>((ctas + d.sm_count - 1) / d.sm_count) / ks;
+    };
+    auto allowed = [&](int ks) {
+        return pl.nchunk >= 2 * ks &&
+               static_cast<int64_t>(pl.stages) * sbytes >= (ks - 1) * 2LL * pl.Np * mbglu::kTcRows * 4;
+    };
+    pl.ksplit = 1;
+    for (int ks = 2; ks <= mbglu::kTcMaxSplit; ++ks)
+        if (allowed(ks) && span(ks) < span(pl.ksplit)) pl.ksplit = ks;
+    if (tuning().tc_split > 0 && (tuning().tc_split == 1 || allowed(tuning().tc_split))) pl.ksplit = tuning().tc_split;
+    pl.smem = mbglu::kTcHeader + mbglu::kTcSmemSlack + static_cast<uint32_t>(pl.stages) * sbytes;
+    return true;
+}
+
+mbglu_status launch_tc(const TcPlan &pl, const mbglu::TcParams &p, const mbglu::TcMaps &maps, cudaStream_t stream,
+                       bool pdl)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.ntiles * pl.ksplit));
+    cfg.blockDim = dim3(mbglu::kTcThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (pl.ksplit > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(pl.ksplit);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = static_cast<unsigned>(n);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, mbglu::glu_tc_kernel, p, maps);
+    return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
+}
+
+// The batch on the tcgen05 kernel when it applies (tensor copies need
+// 16-byte aligned operands and row strides), MBGLU_OK with *done = true;
+// otherwise *done = false and nothing is launched.
+mbglu_status gemv_tc(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
+                     const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
+                     mbglu_mode mode, cudaStream_t stream, bool *done)
+{
+    *done = false;
+    if (!tuning().tc || M < tuning().tc_min_m || K % 8 != 0 || !aligned(h, 16) || !aligned(gate_w, 16) ||
+        !aligned(up_w, 16) || ldh % 8 != 0 || ld_gate % 8 != 0 || ld_up % 8 != 0)
+        return MBGLU_OK;
+    const DeviceInfo *d = nullptr;
+    mbglu_status st = device_info(&d);
+    if (st != MBGLU_OK) return st;
+    TcPlan pl;
+    if (!plan_tc(*d, M, N, K, pl)) return MBGLU_OK;
+    mbglu::TcMaps maps;
+    if (!encode_sw128_map(&maps.gate, gate_w, ld_gate, N, K, mbglu::kTcRows) ||
+        !encode_sw128_map(&maps.up, up_w, ld_up, N, K, mbglu::kTcRows) ||
+        !encode_sw128_map(&maps.h, h, ldh, M, K, pl.Np))
+        return MBGLU_OK;
+    const int policy = g_policy.load(std::memory_order_relaxed);
+    mbglu::TcParams p = {};
+    p.out = reinterpret_cast<uint16_t *>(out);
+    p.ldo = ldo;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.mode = static_cast<int>(mode);
+    p.Np = pl.Np;
+    p.nchunk = pl.nchunk;
+    p.ksplit = pl.ksplit;
+    p.stages = pl.stages;
+    p.prefetch = policy == MBGLU_POLICY_PREFETCH;
+    st = launch_tc(pl, p, maps, stream, policy != MBGLU_POLICY_SERIAL);
+    if (st == MBGLU_OK) {
+        *done = true;
+        t_last_variant = kTcGemv;
+    }
+    return st;
+}
+
+
 }  // namespace
 
 extern "C" {
@@ -797,6 +963,11 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w
     t_last_variant = kNone;
     mbglu_status st = check_gemv(h, ldh, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode);
     if (st != MBGLU_OK || M == 0 || N == 0) return st;
+    if (K > 0 && M >= tuning().tc_min_m) {   // one pass on the tcgen05 kernel where it applies
+        bool done = false;
+        st = gemv_tc(h, ldh, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode, stream, &done);
+        if (st != MBGLU_OK || done) return st;
+    }
     if (M <= kBlockRows) return gemv_block(h, ldh, gate_w, ld_gate, up_w, ld_up, out, ldo, M, N, K, mode, stream);
     // a batch above one kernel's tile: row blocks of kBlockRows, the remainder
     // last, each a full pass over the weights (rows are independent, and every
@@ -854,6 +1025,69 @@ bool plan_bwd_rows(const DeviceInfo &d, int N, int K, const void *gate_w, int64_
     if (rp.S < 2) return false;
     rp.smem = rp.off_ring + static_cast<uint32_t>(rp.S * stage);
     return true;
+}
+
+// Plan of glu_bwd_hw_kernel (steps 2 and 3 in one pass, M <= 8): K in
+// 256-column slices, one warp each; at most bwd_hw_warps(MB) warps per CTA,
+// so K may be cut into column groups (CTAs sharing one row share); row
+// shares so that all CTAs make about one wave; stages of R = 8 rows, as many
+// (2..8) as fit beside the share's dG and dU.
+struct BwdHwPlan {
+    int MB = 1, cg = 1, warps = 1, shares = 1, rows_cta = 0, R = 8, S = 0;
+    uint32_t off_ring = 0, smem = 0;
+};
+
+bool plan_bwd_hw(const DeviceInfo &d, int M, int N, int K, const void *h, int64_t ldh, const void *gate_w,
+                 int64_t ld_gate, const void *up_w, int64_t ld_up, const void *grad_gate, int64_t ldgg,
+                 const void *grad_up, int64_t ldgu, BwdHwPlan &hp)
+{
+    if (M > 8 || K % 8 != 0 || !aligned(h, 16) || ldh % 8 != 0 || !aligned(gate_w, 16) || !aligned(up_w, 16) ||
+        ld_gate % 8 != 0 || ld_up % 8 != 0 || !aligned(grad_gate, 16) || !aligned(grad_up, 16) || ldgg % 8 != 0 ||
+        ldgu % 8 != 0)
+        return false;
+    hp.MB = batch_tile(M);
+    const int wtot = (K + mbglu::kBwdSlice - 1) / mbglu::kBwdSlice;
+    const int wmax = mbglu::bwd_hw_warps(hp.MB);
+    hp.cg = (wtot + wmax - 1) / wmax;
+    hp.warps = (wtot + hp.cg - 1) / hp.cg;
+    hp.shares = std::max(1, std::min(N, d.sm_count / hp.cg));
+    hp.rows_cta = (N + hp.shares - 1) / hp.shares;
+    const uint32_t dgu = 2u * static_cast<uint32_t>(hp.MB) * static_cast<uint32_t>(hp.rows_cta) * 4u;
+    hp.off_ring = (256u + dgu + 127u) & ~127u;
+    const int64_t room = static_cast<int64_t>(d.smem_optin) - hp.off_ring;
+    for (int R = 8; R >= 2; R /= 2) {   // the tallest stage of which two per warp fit
+        hp.R = std::min(R, hp.rows_cta);
+        const int64_t stage = 2ll * hp.R * mbglu::kBwdSlice * 2;
+        hp.S = static_cast<int>(std::min<int64_t>({8, room / (hp.warps * stage), 32 / hp.warps}));
+        if (hp.S >= 2) {
+            hp.smem = hp.off_ring + static_cast<uint32_t>(hp.warps * hp.S * stage);
+            return true;
+        }
+    }
+    return false;
+}
+
+mbglu_status launch_bwd_hw(const BwdHwPlan &hp, const mbglu::BwdParams &q, const mbglu::BwdMaps &maps,
+                           cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(hp.shares * hp.cg);
+    cfg.blockDim = dim3(32 * hp.warps);
+    cfg.dynamicSmemBytes = hp.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_policy.load(std::memory_order_relaxed) != MBGLU_POLICY_SERIAL ? 1 : 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (hp.MB) {
+        case 1: e = cudaLaunchKernelEx(&cfg, mbglu::glu_bwd_hw_kernel<1>, q, maps); break;
+        case 2: e = cudaLaunchKernelEx(&cfg, mbglu::glu_bwd_hw_kernel<2>, q, maps); break;
+        case 4: e = cudaLaunchKernelEx(&cfg, mbglu::glu_bwd_hw_kernel<4>, q, maps); break;
+        default: e = cudaLaunchKernelEx(&cfg, mbglu::glu_bwd_hw_kernel<8>, q, maps); break;
+    }
+    return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
 }
 
 mbglu_status launch_bwd_rows(const BwdRowsPlan &rp, int MB, const mbglu::BwdParams &q, cudaStream_t stream)
@@ -985,6 +1219,32 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
     q.ldm = N;
     q.vec_w = aligned(gate_w, 8) && aligned(up_w, 8) && ld_gate % 4 == 0 && ld_up % 4 == 0;
     cudaError_t e = cudaSuccess;
+    // 2 + 3 in one pass over the rows where it applies (M <= 8, aligned):
+    // grad_h partials and both weight gradients, then the partials' sum
+    BwdHwPlan hp;
+    mbglu::BwdMaps hmaps;
+    if (want_h && want_w && tuning().bwd_fused &&
+        plan_bwd_hw(*d, M, N, K, h, ldh, gate_w, ld_gate, up_w, ld_up, grad_gate, ldgg, grad_up, ldgu, hp) &&
+        encode_box_map(&hmaps.gate, gate_w, ld_gate, N, K, mbglu::kBwdSlice, hp.R) &&
+        encode_box_map(&hmaps.up, up_w, ld_up, N, K, mbglu::kBwdSlice, hp.R)) {
+        q.M = M;
+        q.dG = dG;
+        q.dU = dU;
+        q.rows_cta = hp.rows_cta;
+        q.col_groups = hp.cg;
+        q.R = hp.R;
+        q.S = hp.S;
+        q.off_ring = hp.off_ring;
+        st = launch_bwd_hw(hp, q, hmaps, stream);
+        if (st != MBGLU_OK) return st;
+        const int64_t warps = static_cast<int64_t>(M) * (K / 8);
+        const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(d->sm_count * 8, (warps + 7) / 8)));
+        const int vec_store = aligned(grad_h, 16) && ldgh % 8 == 0;
+        mbglu::glu_bwd_h_reduce8_kernel<<<rgrid, 256, 0, stream>>>(q, hp.shares, vec_store);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+        t_last_variant = kBackward;
+        return MBGLU_OK;
+    }
     // 2) grad_h: partials, then their sum in order; passes of up to 8 rows
     //    (the rows kernel) or kBlockRows rows (the column-block kernel)
     if (want_h) {
@@ -1020,15 +1280,53 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
                 }
                 if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
             }
-            const int rgrid = static_cast<int>(std::max<int64_t>(
-                1, std::min<int64_t>(d->sm_count * 4, (static_cast<int64_t>(mb) * K + 255) / 256)));
-            mbglu::glu_bwd_h_reduce_kernel<<<rgrid, 256, 0, stream>>>(q, nparts);
+            if (rows_ok) {   // one warp per (row, 8 columns), the lanes over the partials
+                const int64_t warps = static_cast<int64_t>(mb) * (K / 8);
+                const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(d->sm_count * 8, (warps + 7) / 8)));
+                const int vec_store = aligned(grad_h, 16) && ldgh % 8 == 0;
+                mbglu::glu_bwd_h_reduce8_kernel<<<rgrid, 256, 0, stream>>>(q, nparts, vec_store);
+            } else {
+                const int rgrid = static_cast<int>(std::max<int64_t>(
+                    1, std::min<int64_t>(d->sm_count * 4, (static_cast<int64_t>(mb) * K + 255) / 256)));
+                mbglu::glu_bwd_h_reduce_kernel<<<rgrid, 256, 0, stream>>>(q, nparts);
+            }
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
         }
     }
     // 3) grad_gate, grad_up: the outer products over all M rows, h in shared
     //    memory where it fits
-    if (want_w) {
+    const int wcpt = (K / 8 + mbglu::kBwdRowsThreads - 1) / mbglu::kBwdRowsThreads;   // chunks per thread
+    if (want_w && K % 8 == 0 && (M <= 8 && wcpt == 1 || M <= 4 && wcpt == 2) &&
+        aligned(grad_gate, 16) && aligned(grad_up, 16) && ldgg % 8 == 0 && ldgu % 8 == 0 && aligned(h, 16) &&
+        ldh % 8 == 0) {
+        // the main path: whole rows per CTA, h in registers
+        q.M = M;
+        q.dG = dG;
+        q.dU = dU;
+        const int cpt = wcpt;
+        const int threads = 32 * ((K / 8 + 32 * cpt - 1) / (32 * cpt));
+        const int grid = std::max(1, std::min(2 * d->sm_count, N));
+        q.rows_cta = (N + grid - 1) / grid;
+        const size_t smem = 2u * 8u * static_cast<size_t>(q.rows_cta) * 4u;
+        const int MB = batch_tile(M);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(threads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = g_policy.load(std::memory_order_relaxed) != MBGLU_POLICY_SERIAL ? 1 : 0;
+        e = cudaErrorInvalidValue;
+#define MBGLU_BWD_W(TMB, TCPT)                                                                   \
+        if (MB == TMB && cpt == TCPT) e = cudaLaunchKernelEx(&cfg, mbglu::glu_bwd_w_rows_kernel<TMB, TCPT>, q);
+        MBGLU_BWD_W(1, 1) MBGLU_BWD_W(2, 1) MBGLU_BWD_W(4, 1) MBGLU_BWD_W(8, 1)
+        MBGLU_BWD_W(1, 2) MBGLU_BWD_W(2, 2) MBGLU_BWD_W(4, 2)
+#undef MBGLU_BWD_W
+        if (e != cudaSuccess) return cuda_fail(e);
+    } else if (want_w) {
         q.M = M;
         q.dG = dG;
         q.dU = dU;

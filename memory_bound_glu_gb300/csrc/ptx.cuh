@@ -74,6 +74,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return p;
 }
 
+// L2 policy: keep the lines (a second pass over the same bytes follows, or
+// every CTA reads them).
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // global to this CTA's shared memory; completion is counted on `bar`.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,

@@ -70,3 +70,28 @@ def test_gdn_gates_extremes_and_noop():
     e = torch.zeros((0, 8), dtype=torch.bfloat16, device=DEV)
     g0, b0 = mb.gdn_gates(e, e, torch.zeros(8, device=DEV), torch.zeros(8, device=DEV))
     assert g0.shape == (0, 8) and mb.last_variant() == 0
+
+
+def test_gdn_gates_paths_agree_bitwise():
+    """The three layouts -- 16-byte chunks of 8 heads, the same chunks element
+    by element (rows offset by one element), and one element per thread (more
+    heads than the per-CTA table holds) -- run the same arithmetic per
+    element: identical bits, and the last against the oracle."""
+    T, H = 257, 40
+    a = gi.normal_bf16((T, H), 3.0, 1, "gp-a").to(DEV)
+    b = gi.normal_bf16((T, H), 3.0, 1, "gp-b").to(DEV)
+    A_log = gi.normal_bf16((H,), 1.0, 1, "gp-A").float().to(DEV)
+    dt = gi.normal_bf16((H,), 1.0, 1, "gp-dt").float().to(DEV)
+    g_vec, beta_vec = mb.gdn_gates(a, b, A_log, dt)
+    buf = torch.zeros((2, T * H + 1), dtype=torch.bfloat16, device=DEV)
+    buf[0, 1:], buf[1, 1:] = a.reshape(-1), b.reshape(-1)
+    a1, b1 = buf[0, 1:].view(T, H), buf[1, 1:].view(T, H)          # 2-byte aligned rows only
+    g_el, beta_el = mb.gdn_gates(a1, b1, A_log, dt)
+    torch.cuda.synchronize()
+    assert torch.equal(g_vec.view(torch.int32), g_el.view(torch.int32))
+    assert torch.equal(beta_vec.view(torch.int16), beta_el.view(torch.int16))
+    Hw = 4104                                                        # above the per-CTA table: one element per thread
+    aw = gi.normal_bf16((3, Hw), 3.0, 2, "gp-aw").to(DEV)
+    Aw = gi.normal_bf16((Hw,), 1.0, 2, "gp-Aw").float().to(DEV)
+    dw = gi.normal_bf16((Hw,), 1.0, 2, "gp-dw").float().to(DEV)
+    check(aw, aw, Aw, dw, "H=4104")

@@ -41,7 +41,7 @@ def oracle_glu(h, g, u, mode):
 
 def parity(got, ref, tau_info, what=""):
     tau, diag, K, mode = tau_info
-    if mb.last_variant() in (4, 7):   # tensor-core accumulation bound (7: row blocks, mostly tensor core)
+    if mb.last_variant() in (4, 7, 9):   # tensor-core accumulation bound (7: row blocks, mostly; 9: tcgen05)
         diag["acc"] = "mma"
         tau = tol.conditioning_floor(diag, K, mode)
     return tol.assert_parity(got, ref, tau, what, diag=diag, K=K, mode=mode)
@@ -580,7 +580,7 @@ def test_full_size_workload(name, M, mode):
     g, u = _layer(name, layer)
     if w.op == "glu_gemv":
         h = gi.hidden(w, M)
-        st = check(h, g, u, mode, f"{name} M={M} {mode}", variant=1 if M <= mb.BLOCK_M else 7)
+        st = check(h, g, u, mode, f"{name} M={M} {mode}", variant=1 if M <= mb.BLOCK_M else 9)
     else:
         x, r, nw = gi.norm_inputs(w, M)
         st = check_norm(x, r, nw, g, u, mode, eps=w.eps, what=f"{name} M={M}", variant=1)

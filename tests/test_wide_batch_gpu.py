@@ -1,7 +1,8 @@
-"""GPU parity of batches above one pass's 16 rows (M = 17..64, decode at
-batch 32 and 64): glu_gemv and the add_rmsnorm_glu entry points run them as
-row blocks of 16, the remainder last, each block one call of the M <= 16
-kernels.
+"""GPU parity of batches above 16 rows (M = 17..64, decode at batch 32 and
+64): glu_gemv runs them in one pass on the tcgen05 kernel where its operands
+allow tensor copies, otherwise -- and the add_rmsnorm_glu entry points
+always -- as row blocks of 16, the remainder last, each block one call of
+the M <= 16 kernels.
 
 Checked against the fp64 oracle with the bar every other batch size meets
 (tolerance.py), with the tensor-core accumulation bound (blocks of 3 or more
@@ -24,7 +25,8 @@ pytestmark = pytest.mark.gpu
 
 mb = pytest.importorskip("memory_bound_glu_gb300")
 DEV = torch.device("cuda:0")
-ROW_BLOCKS = 7   # mbglu_last_variant() after a batch above 16 rows
+ROW_BLOCKS = 7   # mbglu_last_variant(): a batch above 16 rows as row blocks
+TCGEN05 = 9      # mbglu_last_variant(): the batch in one pass on the tcgen05 kernel
 
 
 @pytest.fixture(autouse=True)
@@ -41,26 +43,80 @@ def _gemv_parity(got_bits, h, g, u, mode, what):
     return tol.assert_parity(got_bits, ref, tol.conditioning_floor(diag, K, mode), what, diag=diag, K=K, mode=mode)
 
 
+def test_tcgen05_one_tile_one_chunk():
+    """The smallest case first: one 128-row tile, one 64-wide K chunk, batch
+    17 padded to 32 -- one stage, eight MMAs, no K split.  Distinct values
+    per row and column, so a transposed or misplaced operand cannot pass."""
+    M, N, K = 17, 128, 64
+    h = gi.normal_bf16((M, K), 1.0, 1, "tc1-h")
+    g = gi.normal_bf16((N, K), K ** -0.5, 1, "tc1-g")
+    u = gi.normal_bf16((N, K), K ** -0.5, 1, "tc1-u")
+    out = mb.glu_gemv(h.to(DEV), g.to(DEV), u.to(DEV), mode="fused")
+    torch.cuda.synchronize()
+    assert mb.last_variant() == TCGEN05
+    assert mb.read_device_error() == 0
+    _gemv_parity(gi.bits(out.cpu()), h, g, u, "fused", "one tile")
+
+
+@pytest.mark.parametrize("m0,k0", [(0, 0), (5, 17), (16, 40), (3, 63)])
+def test_tcgen05_one_hot_mapping(m0, k0):
+    """One tile, one chunk, structured: h = e(m0, k0) (a single 1), gate_w[n][k0]
+    = distinct values v_n, up_w[n][k0] = 1, zeros elsewhere.  Then g[m][n] =
+    v_n for m = m0 and 0 otherwise, u likewise 1 or 0, and out[m0][n] =
+    SiLU(v_n), every other output +0.  On a mismatch the message says where
+    the values landed (a transposed, shifted or swizzled operand shows as a
+    pattern)."""
+    M, N, K = 17, 128, 64
+    h = torch.zeros((M, K), dtype=torch.bfloat16)
+    h[m0, k0] = 1.0
+    v = (torch.arange(N, dtype=torch.float32) / 32.0 - 2.0).to(torch.bfloat16)   # -2 .. 1.97, exact in bf16
+    g = torch.zeros((N, K), dtype=torch.bfloat16)
+    g[:, k0] = v
+    u = torch.zeros((N, K), dtype=torch.bfloat16)
+    u[:, k0] = 1.0
+    out = mb.glu_gemv(h.to(DEV), g.to(DEV), u.to(DEV), mode="fused").float().cpu()
+    assert mb.last_variant() == TCGEN05
+    assert mb.read_device_error() == 0
+    ref = oracle.glu_gemv(gi.bits(h), gi.bits(g), gi.bits(u), "fused")
+    got = gi.bits(out.to(torch.bfloat16))
+    bad = np.argwhere(got != ref)
+    nz = np.argwhere(out.numpy() != 0)
+    assert bad.size == 0, (f"{len(bad)} outputs differ; first {bad[:8].tolist()}; nonzero outputs at rows "
+                           f"{sorted(set(nz[:, 0].tolist()))[:8]}, {len(nz)} in all (expected row {m0}, {N})")
+
+
 @pytest.mark.parametrize("mode", ["fused", "hf"])
 @pytest.mark.parametrize("M", [17, 18, 24, 32, 33, 40, 48, 63, 64])
-def test_glu_gemv_row_blocks(M, mode):
-    """Ragged N over the CTAs and a K with a short last segment; remainders
-    of 1 and 2 rows run the CUDA-core kernel, the others the tensor cores."""
+@pytest.mark.parametrize("path", ["tcgen05", "row blocks"])
+def test_glu_gemv_batch_17_to_64(M, mode, path):
+    """Ragged N (a partial last 128-row tile; partial 8-row groups) and a K
+    that ends inside a 64-wide chunk.  Aligned operands take the tcgen05
+    kernel in one pass; h with a row stride that is not a multiple of 8
+    elements takes the row blocks (remainders of 1 and 2 rows on the
+    CUDA-core kernel, the others on the mma.sync kernel)."""
     N, K = 1337, 1288
     h = gi.normal_bf16((M, K), 1.0, M, "wb-h")
     g = gi.normal_bf16((N, K), K ** -0.5, M, "wb-g")
     u = gi.normal_bf16((N, K), K ** -0.5, M, "wb-u")
-    out = mb.glu_gemv(h.to(DEV), g.to(DEV), u.to(DEV), mode=mode)
+    hd = h.to(DEV)
+    if path == "row blocks":
+        hw = torch.zeros((M, K + 1), dtype=torch.bfloat16, device=DEV)
+        hw[:, :K] = hd
+        hd = hw[:, :K]
+    out = mb.glu_gemv(hd, g.to(DEV), u.to(DEV), mode=mode)
     torch.cuda.synchronize()
-    assert mb.last_variant() == ROW_BLOCKS
-    _gemv_parity(gi.bits(out.cpu()), h, g, u, mode, f"M={M} {mode}")
+    assert mb.last_variant() == (TCGEN05 if path == "tcgen05" else ROW_BLOCKS)
+    _gemv_parity(gi.bits(out.cpu()), h, g, u, mode, f"M={M} {mode} {path}")
+    assert mb.read_device_error() == 0
 
 
 def test_row_blocks_equal_calls_on_each_block():
     """M = 50: blocks of 16, 16, 16 and 2 rows, bit for bit the calls on those
     rows alone."""
     M, N, K = 50, 2001, 2560
-    h = gi.normal_bf16((M, K), 1.0, 3, "wbe-h").to(DEV)
+    hw = torch.zeros((M, K + 3), dtype=torch.bfloat16, device=DEV)   # an odd row stride: row blocks
+    hw[:, :K] = gi.normal_bf16((M, K), 1.0, 3, "wbe-h").to(DEV)
+    h = hw[:, :K]
     g = gi.normal_bf16((N, K), K ** -0.5, 3, "wbe-g").to(DEV)
     u = gi.normal_bf16((N, K), K ** -0.5, 3, "wbe-u").to(DEV)
     whole = mb.glu_gemv(h, g, u, mode="hf")
@@ -83,7 +139,7 @@ def test_row_blocks_strided_operands_and_guard_band():
     out = buf[1:1 + M, 24:24 + N]
     mb.glu_gemv(hb.to(DEV)[:, 8:8 + K], gb.to(DEV)[:, :K], ub.to(DEV)[:, 16:16 + K], out=out, mode="hf")
     torch.cuda.synchronize()
-    assert mb.last_variant() == ROW_BLOCKS
+    assert mb.last_variant() == TCGEN05   # every row stride a multiple of 8 elements
     mask = torch.ones(buf.shape, dtype=torch.bool)
     mask[1:1 + M, 24:24 + N] = False
     assert (buf.float().cpu()[mask] == -7.0).all(), "wrote outside out"
@@ -162,7 +218,8 @@ def test_add_rmsnorm_glu_row_blocks(M, path):
 
 def test_full_size_batch_64():
     """The K = 2560, N = 9728 layer (the headline shape) at batch 64, both
-    modes: every output on the GPU, 1024 sampled features against the oracle."""
+    modes, on the tcgen05 kernel (76 tiles, K split over CTA pairs): every
+    output on the GPU, 1024 sampled features against the oracle."""
     w = gi.WORKLOADS["gemv_k2560_n9728"]
     g, u = gi.layer_weights(w, w.layers - 1)
     h = gi.hidden(w, 64)
@@ -171,7 +228,7 @@ def test_full_size_batch_64():
     for mode in ("hf", "fused"):
         out = mb.glu_gemv(hd, gd, ud, mode=mode)
         torch.cuda.synchronize()
-        assert mb.last_variant() == ROW_BLOCKS
+        assert mb.last_variant() == TCGEN05
         st = _gemv_parity(gi.bits(out.cpu())[:, feats], h, g[feats], u[feats], mode, f"M=64 {mode}, sampled")
         assert st["exact_frac"] > 0.9
     assert mb.read_device_error() == 0
