@@ -402,7 +402,9 @@ __global__ void __launch_bounds__(32 * bwd_hw_warps(MB), 1) glu_bwd_hw_kernel(co
                 for (int k = 0; k < 4; ++k) sg[k] = su[k] = make_float2(0.0f, 0.0f);
 #pragma unroll
                 for (int m = 0; m < MB; ++m) {
-                    const float a = dg_s[m * q.rows_cta + r], bb = du_s[m * q.rows_cta + r];
+                    // rows m >= M of the tile are padding: their dG, dU are not staged
+                    const float a = m < q.M ? dg_s[m * q.rows_cta + r] : 0.0f;
+                    const float bb = m < q.M ? du_s[m * q.rows_cta + r] : 0.0f;
                     const float2 a2 = make_float2(a, a), b2 = make_float2(bb, bb);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -465,17 +467,33 @@ __global__ void __launch_bounds__(256) glu_bwd_h_reduce8_kernel(const BwdParams 
          w += nwarp) {
         const int m = static_cast<int>(w / chunks), c = static_cast<int>(w - static_cast<int64_t>(m) * chunks);
         float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        for (int b = lane; b < nsplit; b += 32) {
-            const float4 *src = reinterpret_cast<const float4 *>(q.part + (static_cast<int64_t>(b) * q.M + m) * q.K + 8 * c);
-            const float4 x = src[0], y = src[1];
-            v[0] += x.x;
-            v[1] += x.y;
-            v[2] += x.z;
-            v[3] += x.w;
-            v[4] += y.x;
-            v[5] += y.y;
-            v[6] += y.z;
-            v[7] += y.w;
+        const int64_t pstride = static_cast<int64_t>(q.M) * q.K;   // between consecutive partials
+        const float *base = q.part + static_cast<int64_t>(m) * q.K + 8 * c;
+        for (int b0 = lane; b0 < nsplit; b0 += 32 * 4) {
+            // up to four partials of this lane in flight at once, added in order
+            float4 x[4], y[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int b = b0 + 32 * t;
+                if (b < nsplit) {
+                    const float4 *src = reinterpret_cast<const float4 *>(base + b * pstride);
+                    x[t] = src[0];
+                    y[t] = src[1];
+                } else {
+                    x[t] = y[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                v[0] += x[t].x;
+                v[1] += x[t].y;
+                v[2] += x[t].z;
+                v[3] += x[t].w;
+                v[4] += y[t].x;
+                v[5] += y[t].y;
+                v[6] += y[t].z;
+                v[7] += y[t].w;
+            }
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)

@@ -172,8 +172,8 @@ __device__ __forceinline__ float warp_allsum(float v)
 //   * (var + eps)^-1/2 starts from rsqrtf and takes one Newton step,
 //     y (1 + e/2) with e = 1 - v y^2 formed with exact products (FMA), to
 //     about 2^-44 relative, kept as inv_hi + inv_lo;
-//   * each element is formed in fp32 first; if it lies within 5 fp32 ulps
-//     of a bf16 midpoint (which bounds the fp32 chain's error) it is formed
+//   * each element is formed in fp32 first; if it lies within 8 fp32 ulps
+//     of a bf16 midpoint (the fp32 chain's error is at most 5) it is formed
 //     again in double-float (Dekker's exact products) and rounded from that.
 // The statistic is exact up to ~2^-46 and the element up to ~2^-44, so h is
 // the correctly rounded value except where the exact value lies within
@@ -215,24 +215,32 @@ __device__ __forceinline__ void sumsq_add(SumSq &acc, float2 x)
     acc.hi = t;
 }
 
-// the squares of 8 bf16 (exact in fp32) into acc
-__device__ __forceinline__ void sumsq_bf16x8(uint4 v, SumSq &acc)
+// the squares of 8 bf16 (exact in fp32) into four independent accumulators
+// (one per 32-bit word: four short dependency chains instead of one long)
+__device__ __forceinline__ void sumsq_bf16x8(uint4 v, SumSq (&acc)[4])
 {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float2 a = make_float2(bf16_lo(w[j]), bf16_hi(w[j]));
-        sumsq_add(acc, __fmul2_rn(a, a));
+        sumsq_add(acc[j], __fmul2_rn(a, a));
     }
 }
 
-// (hi, lo) of a thread's accumulators: hi the fp32 sum of the two lanes, lo
-// every remaining part (small against hi)
-__device__ __forceinline__ float2 sumsq_total(const SumSq &a)
+// (hi, lo) of a thread's accumulators: hi the fp32 sum of the high words
+// (TwoSum, errors kept), lo every remaining part (small against hi)
+__device__ __forceinline__ float2 sumsq_total(const SumSq (&a)[4])
 {
-    float e;
-    const float hi = two_sum(a.hi.x, a.hi.y, e);
-    return make_float2(hi, __fadd_rn(e, __fadd_rn(a.lo.x, a.lo.y)));
+    float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float e;
+        hi = two_sum(hi, a[j].hi.x, e);
+        lo = __fadd_rn(lo, __fadd_rn(e, a[j].lo.x));
+        hi = two_sum(hi, a[j].hi.y, e);
+        lo = __fadd_rn(lo, __fadd_rn(e, a[j].lo.y));
+    }
+    return make_float2(hi, lo);
 }
 
 // (hi, lo) += (bhi, blo), renormalised so that |lo| <= ulp(hi) / 2 (for
@@ -302,9 +310,9 @@ __device__ __forceinline__ float norm_elem_f32(float sv, float w, float ih)
     return __fmul_rn(__fmul_rn(sv, ih), __fadd_rn(1.0f, w));
 }
 
-// true if the fp32 element lies within 5 fp32 ulps of a bf16 midpoint, the
-// most the fp32 chain can be off: only then can its rounding be wrong
-__device__ __forceinline__ bool near_midpoint(float v) { return (__float_as_uint(v) & 0xffffu) - 0x7ffbu <= 10u; }
+// true if the fp32 element lies within 8 fp32 ulps of a bf16 midpoint (the
+// fp32 chain is off by at most 5): only then can its rounding be wrong
+__device__ __forceinline__ bool near_midpoint(float v) { return ((__float_as_uint(v) + 8u) & 0xfff0u) == 0x8000u; }
 
 __device__ __forceinline__ uint16_t norm_elem(float sv, float w, float ih, float il)
 {
@@ -535,7 +543,7 @@ __device__ __forceinline__ void add_rows_in_place(const GluParams &p, const RowM
 // once per launch.
 __device__ __forceinline__ float2 square_rows(const RowMap &r, const uint16_t *h_s, int hstride)
 {
-    SumSq ss = sumsq_zero();
+    SumSq ss[4] = {sumsq_zero(), sumsq_zero(), sumsq_zero(), sumsq_zero()};
     if (!r.active) return make_float2(0.0f, 0.0f);
     const uint4 *row = reinterpret_cast<const uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
 #pragma unroll 1
@@ -543,44 +551,43 @@ __device__ __forceinline__ float2 square_rows(const RowMap &r, const uint16_t *h
     return sumsq_total(ss);
 }
 
+// The norm's per-thread partial sums (high words, then low words, one pair
+// per thread of the block): in dynamic shared memory after norm_w, whose
+// region the planners size as round128(2 K) + kNormPartBytes.
+constexpr uint32_t kNormPartBytes = 2u * (kMaxStreamWarps + 1) * 32u * 4u;
+
+__device__ __forceinline__ float *norm_partials(unsigned char *smem, const GluParams &p)
+{
+    return reinterpret_cast<float *>(smem + p.off_s + ((static_cast<uint32_t>(p.K) * 2u + 127u) & ~127u));
+}
+
 // Zero-centred RMSNorm of the rows in h_s, in place (PR #9057 "Changes"):
 //   var = mean_k s^2, inv = (var + eps)^-1/2, h = bf16( s * inv * (1 + w) ),
 // with (1 + w) formed exactly and h correctly rounded (see norm_elem).
-// ss: this thread's double-float partial from square_rows or
-// add_rows_in_place.  Row m's partials are added by one warp (lane-strided,
-// then a butterfly), first the high words in double-float, then the low
-// words: a fixed order, and every CTA computes the identical h.  part:
-// blockDim floats of shared memory; inv_s: 2 M floats.  Rows
-// M..rows_out-1 of h_s become zero.  Ends with a barrier.
+// ss: this thread's double-float partial from square_rows.  Row m's
+// partials are added by one warp (lane-strided, then a butterfly), high words
+// in double-float, low words alongside: a fixed order, and every CTA
+// computes the identical h.  part: 2 blockDim floats of shared memory; inv_s:
+// 2 M floats.  Rows M..rows_out-1 of h_s become zero.  Ends with a barrier.
 __device__ __forceinline__ void norm_rows_in_place(const GluParams &p, const RowMap &r, float2 ss, uint16_t *h_s,
                                                    int hstride, const uint16_t *w_s, float *part, float *inv_s,
                                                    int rows_out)
 {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
+    const int nthr = blockDim.x;
     part[tid] = ss.x;
+    part[nthr + tid] = ss.y;
     __syncthreads();
     for (int m = warp; m < p.M; m += nw) {
         float hi = 0.0f, lo = 0.0f;
         for (int i = lane; i < r.P; i += 32) {
             float e;
             hi = two_sum(hi, part[m * r.P + i], e);
-            lo = __fadd_rn(lo, e);
+            lo = __fadd_rn(lo, __fadd_rn(e, part[nthr + m * r.P + i]));
         }
         df_warp_allsum(hi, lo);
         if (lane == 0) {
-            inv_s[2 * m] = hi;
-            inv_s[2 * m + 1] = lo;
-        }
-    }
-    __syncthreads();
-    part[tid] = ss.y;
-    __syncthreads();
-    for (int m = warp; m < p.M; m += nw) {
-        float t = 0.0f;
-        for (int i = lane; i < r.P; i += 32) t = __fadd_rn(t, part[m * r.P + i]);
-        t = warp_allsum(t);
-        if (lane == 0) {
-            const float2 inv = norm_inv(inv_s[2 * m], __fadd_rn(inv_s[2 * m + 1], t), p.K, p.eps);
+            const float2 inv = norm_inv(hi, lo, p.K, p.eps);
             inv_s[2 * m] = inv.x;
             inv_s[2 * m + 1] = inv.y;
         }
@@ -724,7 +731,6 @@ template <int MB, int R, bool NORM, bool HREG>
 __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(const GluParams p)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[kMaxStreamWarps * 32];   // norm: one partial sum per thread
     __shared__ float inv_s[2 * MB];                // norm: (inv_hi, inv_lo) per row
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -851,7 +857,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
             add_rows_in_place(p, rm, h_s, K, xr);
         }
         const float2 ss = square_rows(rm, h_s, K);
-        norm_rows_in_place(p, rm, ss, h_s, K, nw_s, red, inv_s, MB);
+        norm_rows_in_place(p, rm, ss, h_s, K, nw_s, norm_partials(smem, p), inv_s, MB);
     } else if constexpr (!HREG) {
         if (p.vec_in) {
             if (threadIdx.x == 0) {
@@ -1091,7 +1097,6 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
     glu_mma_kernel(const GluParams p, const __grid_constant__ MmaMaps maps)
 {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ float red[(kMaxStreamWarps + 1) * 32];   // norm: one partial sum per thread
     __shared__ float inv_s[2 * kMaxM];                  // norm: (inv_hi, inv_lo) per row
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1260,7 +1265,7 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
             add_rows_in_place(p, rm, h_s, HS, xr);
         }
         const float2 ss = square_rows(rm, h_s, HS);
-        norm_rows_in_place(p, rm, ss, h_s, HS, nw_s, red, inv_s, p.M);
+        norm_rows_in_place(p, rm, ss, h_s, HS, nw_s, norm_partials(smem, p), inv_s, p.M);
     } else if (p.vec_in) {
         if (threadIdx.x == 0) {
             mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(HW) * 2u);

@@ -82,7 +82,7 @@ struct Tuning {
     int tc = 1;               // batches of tc_min_m..64 on the tcgen05 kernel (0: row blocks)
     int tc_min_m = 17;        // smallest batch that takes the tcgen05 kernel
     int tc_split = 0;         // tcgen05 kernel: CTAs per tile (0: automatic, 1..4 where the plan allows)
-    int bwd_fused = 0;        // backward: steps 2 and 3 in one pass where they apply (0: separate kernels)
+    int bwd_fused = 1;        // backward: steps 2 and 3 in one pass where they apply (0: separate kernels)
 };
 
 std::atomic<int> g_policy{MBGLU_POLICY_PREFETCH};
@@ -114,7 +114,7 @@ const Tuning &tuning()
         x.tc = env_int("MBGLU_TC", 1) != 0;
         x.tc_min_m = std::min(65, std::max(1, env_int("MBGLU_TC_MIN_M", 17)));
         x.tc_split = std::min(mbglu::kTcMaxSplit, std::max(0, env_int("MBGLU_TC_SPLIT", 0)));
-        x.bwd_fused = env_int("MBGLU_BWD_FUSED", 0) != 0;
+        x.bwd_fused = env_int("MBGLU_BWD_FUSED", 1) != 0;
         return x;
     }();
     return t;
@@ -1419,7 +1419,8 @@ mbglu_status norm_block(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_b
                          (ld_up % 8 == 0) && p.vec_in;
 
     // single kernel: needs the fast kernels, 16-byte aligned x, and N > 0
-    const uint32_t nwbytes = (static_cast<uint32_t>(K) * 2u + 127u) & ~127u;   // norm_w in shared memory
+    // norm_w in shared memory, then the statistic's per-thread partials
+    const uint32_t nwbytes = ((static_cast<uint32_t>(K) * 2u + 127u) & ~127u) + mbglu::kNormPartBytes;
     if (ws && N > 0 && bulk_ok && aligned(x, 16)) {
         const uint32_t sbytes = nwbytes;   // s is formed in place where the residual rows land
         Plan pl;

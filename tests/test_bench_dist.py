@@ -92,8 +92,12 @@ def test_row_block_count_matches_the_header():
     hdr = open(os.path.join(ROOT, "include", "mbglu.h")).read()
     assert int(re.search(r"#define MBGLU_BLOCK_M (\d+)", hdr).group(1)) == bench.BLOCK_M == mb.BLOCK_M
     assert int(re.search(r"#define MBGLU_MAX_M (\d+)", hdr).group(1)) == mb.MAX_M
+    # glu_gemv takes batches above 16 rows in one pass (the tcgen05 kernel on
+    # the bench's aligned operands); add_rmsnorm_glu runs them as row blocks
     w = gi.WORKLOADS["gemv_k2560_n9728_wide"]
-    assert [bench.row_blocks(w, M) for M in (1, 16, 17, 32, 33, 64)] == [1, 1, 2, 2, 3, 4]
+    assert [bench.row_blocks(w, M) for M in (1, 16, 17, 32, 33, 64)] == [1] * 6
+    wn = gi.WORKLOADS["norm_gemv_k2560_n9728"]
+    assert [bench.row_blocks(wn, M) for M in (1, 16, 17, 32, 33, 64)] == [1, 1, 2, 2, 3, 4]
     assert bench.row_blocks(gi.WORKLOADS["silu_mul_m4096_n9728"], 4096) == 1
 
 

@@ -72,8 +72,7 @@ def _norm_elem(sv, w, ih, il, fallback=True):
     out = _rne_bits(v)
     if not fallback:
         return out
-    low = v.view(np.uint32) & np.uint32(0xFFFF)
-    near = (low.astype(np.int64) - 0x7FFB >= 0) & (low.astype(np.int64) - 0x7FFB <= 10)
+    near = ((v.view(np.uint32).astype(np.int64) + 8) & 0xFFF0) == 0x8000   # within 8 fp32 ulps of a midpoint
     if near.any():
         s_, w_ = sv[near], w[near]
         ih_ = np.broadcast_to(ih, sv.shape)[near]
