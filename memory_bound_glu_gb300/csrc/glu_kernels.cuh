@@ -522,31 +522,38 @@ __device__ __forceinline__ void x_prefetch_rows(const GluParams &p, const RowMap
 }
 
 // s = bf16(x + residual) formed in place in h_s (the fp32 sum of two bf16
-// values rounds to the same bf16 as the exact sum).
-__device__ __forceinline__ void add_rows_in_place(const GluParams &p, const RowMap &r, uint16_t *h_s, int hstride,
-                                                  XRows &x)
+// values rounds to the same bf16 as the exact sum); returns this thread's sum
+// of s^2 over its chunks as a double-float.  The statistic rides in the same
+// loop, where it hides under the latency of the x loads.
+__device__ __forceinline__ float2 add_rows_in_place(const GluParams &p, const RowMap &r, uint16_t *h_s, int hstride,
+                                                    XRows &x)
 {
+    SumSq ss[4] = {sumsq_zero(), sumsq_zero(), sumsq_zero(), sumsq_zero()};
     uint4 *row = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
     for (int j0 = 0;; j0 += kXRows) {
         if (j0 > 0) x_prefetch_rows(p, r, x, j0);
 #pragma unroll
         for (int j = 0; j < kXRows; ++j) {
             const int c = r.c0 + (j0 + j) * r.P;
-            if (r.active && c < r.nch) row[c] = add_bf16x8(x.v[j], row[c]);
+            if (r.active && c < r.nch) {
+                const uint4 sv = add_bf16x8(x.v[j], row[c]);
+                row[c] = sv;
+                sumsq_bf16x8(sv, ss);
+            }
         }
         if (!r.active || r.c0 + (j0 + kXRows) * r.P >= r.nch) break;
     }
+    return sumsq_total(ss);
 }
 
 // This thread's sum of s^2 over its chunks of h_s, in chunk order, as a
-// double-float.  A compact loop: the prologue's code is fetched by every CTA
-// once per launch.
+// double-float (the path whose s is already in shared memory).
 __device__ __forceinline__ float2 square_rows(const RowMap &r, const uint16_t *h_s, int hstride)
 {
     SumSq ss[4] = {sumsq_zero(), sumsq_zero(), sumsq_zero(), sumsq_zero()};
     if (!r.active) return make_float2(0.0f, 0.0f);
     const uint4 *row = reinterpret_cast<const uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
-#pragma unroll 1
+#pragma unroll 2
     for (int c = r.c0; c < r.nch; c += r.P) sumsq_bf16x8(row[c], ss);
     return sumsq_total(ss);
 }
@@ -599,7 +606,7 @@ __device__ __forceinline__ void norm_rows_in_place(const GluParams &p, const Row
         const uint4 *wv = reinterpret_cast<const uint4 *>(w_s);
         uint64_t mask = 0;   // this thread's chunks left as s for norm_fix_chunks (at most 40 of them)
         int i = 0;
-#pragma unroll 2
+#pragma unroll 4
         for (int c = r.c0; c < r.nch; c += r.P, ++i) {
             bool near = false;
             const uint4 hv = norm_chunk_f32(row[c], wv[c], ih, near);
@@ -852,11 +859,13 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
         XRows xr;
         if (p.fused) x_prefetch_rows(p, rm, xr);
         prologue_wait(pro_bar);
+        float2 ss;
         if (p.fused) {
             if (threadIdx.x == 0) fused_arrive(p);
-            add_rows_in_place(p, rm, h_s, K, xr);
+            ss = add_rows_in_place(p, rm, h_s, K, xr);
+        } else {
+            ss = square_rows(rm, h_s, K);
         }
-        const float2 ss = square_rows(rm, h_s, K);
         norm_rows_in_place(p, rm, ss, h_s, K, nw_s, norm_partials(smem, p), inv_s, MB);
     } else if constexpr (!HREG) {
         if (p.vec_in) {
@@ -1260,11 +1269,13 @@ __global__ void __launch_bounds__((kMaxStreamWarps + 1) * 32, 1)
         XRows xr;
         if (p.fused) x_prefetch_rows(p, rm, xr);
         prologue_wait(pro_bar);
+        float2 ss;
         if (p.fused) {
             if (threadIdx.x == 0) fused_arrive(p);
-            add_rows_in_place(p, rm, h_s, HS, xr);
+            ss = add_rows_in_place(p, rm, h_s, HS, xr);
+        } else {
+            ss = square_rows(rm, h_s, HS);
         }
-        const float2 ss = square_rows(rm, h_s, HS);
         norm_rows_in_place(p, rm, ss, h_s, HS, nw_s, norm_partials(smem, p), inv_s, p.M);
     } else if (p.vec_in) {
         if (threadIdx.x == 0) {

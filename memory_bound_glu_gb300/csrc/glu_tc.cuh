@@ -17,8 +17,8 @@
 // warp 1 owns the tensor memory, warps 2-5 read the accumulators (warp w may
 // read lanes 32 * (w % 4) .. +31).  With ksplit = 2..4 the CTAs of a tile
 // form a cluster: rank 0 frees its stage memory once its MMAs are done,
-// ranks 1.. write their partial sums there (slot r - 1) through distributed
-// shared memory, and rank 0 adds them (own, then ranks 1, 2, ... in order)
+// ranks 1.. write their partial sums there (slot r - 1, [128 rows][2 Np + 4]
+// fp32, 16-byte stores) through distributed shared memory, and rank 0 adds them (own, then ranks 1, 2, ... in order)
 // before the epilogue.  Every wait is bounded; every thread reaches the final
 // cluster barrier, so no CTA leaves while another may still touch its memory.
 #pragma once
@@ -29,20 +29,28 @@
 namespace mbglu {
 
 constexpr int kTcRows = 128;                              // weight rows per tile: the MMA's M
-constexpr int kTcChunk = 64;                              // K per stage: one 128-byte swizzled row
+constexpr int kTcBox = 64;                                // K per tensor copy: one 128-byte swizzled row
+constexpr int kTcBoxes = 2;                               // copies per matrix and stage, adjacent in K
+constexpr int kTcChunk = kTcBox * kTcBoxes;               // K per stage: 128 (256 bytes of each row)
 constexpr int kTcMaxStages = 8;
-constexpr uint32_t kTcWBytes = kTcRows * kTcChunk * 2;    // one matrix's chunk: 16 KB
+constexpr uint32_t kTcWBox = kTcRows * kTcBox * 2;        // one matrix's box: 16 KB
+constexpr uint32_t kTcWBytes = kTcWBox * kTcBoxes;        // one matrix's stage: 32 KB
 constexpr int kTcThreads = 192;
 constexpr uint32_t kTcHeader = 1024;                      // barriers, tensor-memory address
 constexpr uint32_t kTcSmemSlack = 1024;                   // room to align the stages to 1024 bytes
 constexpr int kTcMaxSplit = 4;                            // CTAs per tile at most (K split over a cluster)
+
+// Row pitch (fp32) of a rank's partial sums in rank 0's shared memory: a
+// weight row's Np g values then Np u values, 4 floats of padding so that the
+// 16-byte accesses of consecutive rows fall in different banks.
+__host__ __device__ constexpr int tc_part_pitch(int Np) { return 2 * Np + 4; }
 
 struct TcParams {
     uint16_t *out;
     int64_t ldo;
     int M, N, K, mode;
     int Np;          // batch rows padded to a multiple of 16: the MMA's N
-    int nchunk;      // 64-wide K chunks
+    int nchunk;      // kTcChunk-wide K chunks
     int ksplit;      // CTAs per tile (the cluster size), 1..kTcMaxSplit
     int stages;
     int prefetch;    // weight stages requested before the dependency wait
@@ -67,7 +75,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) glu_tc_kernel(const TcParams p,
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.stages, Np = p.Np, ks = p.ksplit;
-    const uint32_t sbytes = 2 * kTcWBytes + static_cast<uint32_t>(Np) * 128u;
+    const uint32_t hbox = static_cast<uint32_t>(Np) * 128u;   // one h box: Np rows of 64 columns
+    const uint32_t sbytes = 2 * kTcWBytes + hbox * kTcBoxes;
     const uint32_t rank = ks > 1 ? cluster_ctarank() : 0u;
     const int tile = static_cast<int>(blockIdx.x) / ks;
     const int c0 = p.nchunk * static_cast<int>(rank) / ks;
@@ -103,15 +112,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) glu_tc_kernel(const TcParams p,
             const uint64_t pol_h = l2_policy_evict_last();   // every tile reads h
             const int row0 = tile * kTcRows;
             const int pre = p.prefetch ? min(S, nch) : 0;
+            // a stage: gate boxes, up boxes, h boxes; the boxes of one matrix
+            // adjacent in K and issued back to back (longer runs of each row)
+            auto load_w = [&](int s, int k) {
+                unsigned char *st = stages + s * sbytes;
+#pragma unroll
+                for (int b = 0; b < kTcBoxes; ++b)
+                    tma_load_2d(st + b * kTcWBox, &maps.gate, k + b * kTcBox, row0, &full[s], pol_w);
+#pragma unroll
+                for (int b = 0; b < kTcBoxes; ++b)
+                    tma_load_2d(st + kTcWBytes + b * kTcWBox, &maps.up, k + b * kTcBox, row0, &full[s], pol_w);
+            };
+            auto load_h = [&](int s, int k) {
+                unsigned char *st = stages + s * sbytes + 2 * kTcWBytes;
+#pragma unroll
+                for (int b = 0; b < kTcBoxes; ++b) tma_load_2d(st + b * hbox, &maps.h, k + b * kTcBox, 0, &full[s], pol_h);
+            };
             for (int i = 0; i < pre; ++i) {   // weights only: nothing before the wait may depend on the predecessor
-                unsigned char *st = stages + i * sbytes;
                 mbar_arrive_expect_tx(&full[i], sbytes);
-                tma_load_2d(st, &maps.gate, (c0 + i) * kTcChunk, row0, &full[i], pol_w);
-                tma_load_2d(st + kTcWBytes, &maps.up, (c0 + i) * kTcChunk, row0, &full[i], pol_w);
+                load_w(i, (c0 + i) * kTcChunk);
             }
             grid_dependency_wait();
-            for (int i = 0; i < pre; ++i)
-                tma_load_2d(stages + i * sbytes + 2 * kTcWBytes, &maps.h, (c0 + i) * kTcChunk, 0, &full[i], pol_h);
+            for (int i = 0; i < pre; ++i) load_h(i, (c0 + i) * kTcChunk);
             int issued = pre;
             for (int i = pre; i < nch; ++i) {
                 const int s = i % S;
@@ -119,12 +141,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) glu_tc_kernel(const TcParams p,
                     ok = false;
                     break;
                 }
-                unsigned char *st = stages + s * sbytes;
                 const int k = (c0 + i) * kTcChunk;
                 mbar_arrive_expect_tx(&full[s], sbytes);
-                tma_load_2d(st, &maps.gate, k, row0, &full[s], pol_w);
-                tma_load_2d(st + kTcWBytes, &maps.up, k, row0, &full[s], pol_w);
-                tma_load_2d(st + 2 * kTcWBytes, &maps.h, k, 0, &full[s], pol_h);
+                load_w(s, k);
+                load_h(s, k);
                 issued = i + 1;
             }
             // none of this CTA's copies may still be in flight when it leaves:
@@ -149,13 +169,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) glu_tc_kernel(const TcParams p,
             }
             tc_fence_after();
             unsigned char *st = stages + s * sbytes;
-            const uint64_t ag = smem_desc_sw128(st), au = smem_desc_sw128(st + kTcWBytes);
-            const uint64_t bh = smem_desc_sw128(st + 2 * kTcWBytes);
 #pragma unroll
-            for (int kk = 0; kk < kTcChunk / 16; ++kk) {
-                const bool acc = i > 0 || kk > 0;
-                tc_mma_bf16(tmem, ag + 2 * kk, bh + 2 * kk, idesc, acc);
-                tc_mma_bf16(tmem + ucol, au + 2 * kk, bh + 2 * kk, idesc, acc);
+            for (int b = 0; b < kTcBoxes; ++b) {
+                const uint64_t ag = smem_desc_sw128(st + b * kTcWBox);
+                const uint64_t au = smem_desc_sw128(st + kTcWBytes + b * kTcWBox);
+                const uint64_t bh = smem_desc_sw128(st + 2 * kTcWBytes + b * hbox);
+#pragma unroll
+                for (int kk = 0; kk < kTcBox / 16; ++kk) {
+                    const bool acc = i > 0 || b > 0 || kk > 0;
+                    tc_mma_bf16(tmem, ag + 2 * kk, bh + 2 * kk, idesc, acc);
+                    tc_mma_bf16(tmem + ucol, au + 2 * kk, bh + 2 * kk, idesc, acc);
+                }
             }
             tc_commit(&empty[s]);   // the stage is free once these MMAs have read it
         }
@@ -181,19 +205,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) glu_tc_kernel(const TcParams p,
                 have_partial = __all_sync(0xffffffffu, mbar_wait_cluster_bounded(red_bar, 0, kWaitLimitNs));
                 if (!have_partial) ok = false;
             }
-            const float *part = reinterpret_cast<const float *>(stages);   // [rank - 1][2 Np][128]
-            const int slot = 2 * Np * kTcRows;
+            // [rank - 1][128 rows][2 Np + 4] fp32: a row's g then u partials
+            const float *part = reinterpret_cast<const float *>(stages);
+            const int pitch = tc_part_pitch(Np), slot = kTcRows * pitch;
             for (int c = 0; c < Np; c += 16) {
                 float g[16], u[16];
                 tmem_ld16(taddr + static_cast<uint32_t>(c), g);
                 tmem_ld16(taddr + ucol + static_cast<uint32_t>(c), u);
                 if (have_partial) {
                     for (int r = 1; r < ks; ++r) {
-                        const float *pr = part + (r - 1) * slot;
+                        const float4 *pg = reinterpret_cast<const float4 *>(part + (r - 1) * slot + row * pitch + c);
+                        const float4 *pu = reinterpret_cast<const float4 *>(part + (r - 1) * slot + row * pitch + Np + c);
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            g[j] += pr[(c + j) * kTcRows + row];
-                            u[j] += pr[(Np + c + j) * kTcRows + row];
+                        for (int j = 0; j < 4; ++j) {
+                            const float4 a = pg[j], b = pu[j];
+                            g[4 * j] += a.x;
+                            g[4 * j + 1] += a.y;
+                            g[4 * j + 2] += a.z;
+                            g[4 * j + 3] += a.w;
+                            u[4 * j] += b.x;
+                            u[4 * j + 1] += b.y;
+                            u[4 * j + 2] += b.z;
+                            u[4 * j + 3] += b.w;
                         }
                     }
                 }
@@ -208,14 +241,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) glu_tc_kernel(const TcParams p,
             // memory once rank 0 frees it
             const bool go = __all_sync(0xffffffffu, mbar_wait_cluster_bounded(go_bar, 0, kWaitLimitNs));
             if (!go) ok = false;
-            const uint32_t dst = map_to_rank(stages, 0) + (rank - 1) * static_cast<uint32_t>(2 * Np * kTcRows * 4);
-            for (int c = 0; c < 2 * Np; c += 16) {   // partial row c: g's column c, or u's column c - Np
+            const int pitch = tc_part_pitch(Np);
+            const uint32_t dst = map_to_rank(stages, 0) +
+                                 static_cast<uint32_t>(((rank - 1) * kTcRows + row) * pitch * 4);
+            for (int c = 0; c < 2 * Np; c += 16) {   // g's columns 0..Np-1, then u's
                 float v[16];
                 tmem_ld16(taddr + (c < Np ? static_cast<uint32_t>(c) : ucol + static_cast<uint32_t>(c - Np)), v);
                 if (go) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        st_cluster_f32(dst + static_cast<uint32_t>(((c + j) * kTcRows + row) * 4), v[j]);
+                    for (int j = 0; j < 4; ++j)
+                        st_cluster_v4_f32(dst + static_cast<uint32_t>((c + 4 * j) * 4), v[4 * j], v[4 * j + 1],
+                                          v[4 * j + 2], v[4 * j + 3]);
                 }
             }
             mbar_arrive_remote(map_to_rank(red_bar, 0));   // also after a timeout, so rank 0 is not kept waiting

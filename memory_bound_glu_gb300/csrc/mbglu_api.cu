@@ -834,7 +834,7 @@ bool encode_sw128_map(mbglu::TensorMap *out, const void *base, int64_t ld, int r
     CUtensorMap m;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mbglu::kTcChunk), static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mbglu::kTcBox), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t elem_strides[2] = {1u, 1u};
     if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -861,7 +861,7 @@ bool plan_tc(const DeviceInfo &d, int M, int N, int K, TcPlan &pl)
     pl.Np = (M + 15) / 16 * 16;
     pl.nchunk = (K + mbglu::kTcChunk - 1) / mbglu::kTcChunk;
     pl.ntiles = (N + mbglu::kTcRows - 1) / mbglu::kTcRows;
-    const uint32_t sbytes = 2 * mbglu::kTcWBytes + static_cast<uint32_t>(pl.Np) * 128u;
+    const uint32_t sbytes = 2 * mbglu::kTcWBytes + static_cast<uint32_t>(pl.Np) * 128u * mbglu::kTcBoxes;
     const int64_t room = static_cast<int64_t>(d.smem_optin) - mbglu::kTcHeader - mbglu::kTcSmemSlack;
     pl.stages = static_cast<int>(std::min<int64_t>(mbglu::kTcMaxStages, room / sbytes));
     if (pl.stages < 2) return false;
@@ -870,14 +870,16 @@ bool plan_tc(const DeviceInfo &d, int M, int N, int K, TcPlan &pl)
         return static_cast<double>((ctas + d.sm_count - 1) / d.sm_count) / ks;
     };
     auto allowed = [&](int ks) {
-        return pl.nchunk >= 2 * ks &&
-               static_cast<int64_t>(pl.stages) * sbytes >= (ks - 1) * 2LL * pl.Np * mbglu::kTcRows * 4;
+        return pl.nchunk >= 2 * ks && (ks - 1) * 4LL * mbglu::kTcRows * mbglu::tc_part_pitch(pl.Np) <= room;
     };
     pl.ksplit = 1;
     for (int ks = 2; ks <= mbglu::kTcMaxSplit; ++ks)
         if (allowed(ks) && span(ks) < span(pl.ksplit)) pl.ksplit = ks;
     if (tuning().tc_split > 0 && (tuning().tc_split == 1 || allowed(tuning().tc_split))) pl.ksplit = tuning().tc_split;
-    pl.smem = mbglu::kTcHeader + mbglu::kTcSmemSlack + static_cast<uint32_t>(pl.stages) * sbytes;
+    // rank 0's stage memory also takes the other ranks' partial sums after its MMAs
+    const int64_t parts = (pl.ksplit - 1) * 4LL * mbglu::kTcRows * mbglu::tc_part_pitch(pl.Np);
+    pl.smem = mbglu::kTcHeader + mbglu::kTcSmemSlack +
+              static_cast<uint32_t>(std::max<int64_t>(static_cast<int64_t>(pl.stages) * sbytes, parts));
     return true;
 }
 

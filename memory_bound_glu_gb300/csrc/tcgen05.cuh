@@ -133,6 +133,13 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v)
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// 16 bytes (addr 16-byte aligned) into another CTA's shared memory
+__device__ __forceinline__ void st_cluster_v4_f32(uint32_t addr, float a, float b, float c, float d)
+{
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
 // Arrival on an mbarrier of another CTA of the cluster, releasing this
 // thread's earlier writes at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_addr)

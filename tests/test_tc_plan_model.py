@@ -18,14 +18,17 @@ import itertools
 import pytest
 
 SMS, OPTIN = 152, 232448               # GB300: SMs, max dynamic + static shared memory per block
-ROWS, CHUNK, WBYTES, HEADER, SLACK, MAX_STAGES = 128, 64, 128 * 64 * 2, 1024, 1024, 8
+BOX, BOXES = 64, 2                     # K per tensor copy (128 bytes, the swizzle row); copies per matrix and stage
+ROWS, CHUNK, HEADER, SLACK, MAX_STAGES = 128, BOX * BOXES, 1024, 1024, 8
+WBOX = ROWS * BOX * 2                  # one matrix's box
+WBYTES = WBOX * BOXES                  # one matrix's stage
 
 
 def plan(M, N, K):
     Np = (M + 15) // 16 * 16
     nchunk = -(-K // CHUNK)
     ntiles = -(-N // ROWS)
-    sbytes = 2 * WBYTES + Np * 128
+    sbytes = 2 * WBYTES + Np * 128 * BOXES
     stages = min(MAX_STAGES, (OPTIN - HEADER - SLACK) // sbytes)
     if stages < 2:
         return None
@@ -35,11 +38,12 @@ def plan(M, N, K):
 
     ks = 1
     for k in range(2, 5):
-        fits = stages * sbytes >= (k - 1) * 2 * Np * ROWS * 4
+        fits = (k - 1) * ROWS * (2 * Np + 4) * 4 <= OPTIN - HEADER - SLACK
         if nchunk >= 2 * k and fits and span(k) < span(ks):
             ks = k
+    parts = (ks - 1) * ROWS * (2 * Np + 4) * 4    # rank 0's stage memory also takes the partial sums
     return dict(Np=Np, nchunk=nchunk, ntiles=ntiles, ks=ks, stages=stages, sbytes=sbytes,
-                smem=HEADER + SLACK + stages * sbytes)
+                smem=HEADER + SLACK + max(stages * sbytes, parts))
 
 
 @pytest.mark.parametrize("M", list(range(1, 65)))
@@ -54,8 +58,11 @@ def test_tc_plan_and_addressing(M):
             base = base_off + ((1024 - base_off % 1024) % 1024)
             assert base % 1024 == 0 and base - base_off + HEADER + S * sb <= p["smem"]
             for s in range(S):
-                for off in (0, WBYTES, 2 * WBYTES):
+                offs = [b * WBOX for b in range(BOXES)] + [WBYTES + b * WBOX for b in range(BOXES)] + \
+                       [2 * WBYTES + b * Np * 128 for b in range(BOXES)]
+                for off in offs:                                          # every box a swizzled tile
                     assert (base + HEADER + s * sb + off) % 1024 == 0
+                assert 2 * WBYTES + BOXES * Np * 128 == sb
         ncols = 64 if 2 * Np <= 64 else 128
         ucol = ncols // 2
         assert ncols & (ncols - 1) == 0 and 32 <= ncols <= 512
@@ -67,10 +74,14 @@ def test_tc_plan_and_addressing(M):
             for i in (0, nch - 1):
                 x = (c0 + i) * CHUNK
                 assert x % 64 == 0 and x < K
+                for b in range(BOXES):                                    # later boxes may lie past K: zeros
+                    assert (x + b * BOX) % 64 == 0
         if ks > 1:
-            assert S * sb >= (ks - 1) * 2 * Np * ROWS * 4                  # the other ranks' partial slots
-            for r in range(1, ks):                                        # each slot inside rank 0's stages
-                assert (r - 1) * 2 * Np * ROWS * 4 + 2 * Np * ROWS * 4 <= S * sb
+            room = p["smem"] - HEADER - SLACK                               # rank 0's stage memory, allocated
+            pitch = 2 * Np + 4                                            # [128 rows][2 Np + 4] fp32 per rank
+            assert (pitch * 4) % 16 == 0 and (pitch * 4) % 128 == 16      # 16-byte rows, banks apart
+            for r in range(1, ks):                                        # each partial slot inside it
+                assert (r - 1) * ROWS * pitch * 4 + ROWS * pitch * 4 <= room
         for tile in (0, p["ntiles"] - 1):
             assert tile * ROWS < N
         assert p["ntiles"] * ks <= 2 ** 31 - 1
