@@ -115,4 +115,4 @@ def test_recorded_traffic_is_current_only_for_the_profiled_sources(monkeypatch):
     cur, last = bench.recorded_traffic("gemv_k2560_n9728", 1, "hf")
     assert cur is None and last["sources_changed_since"] is True
     assert last["dram_bytes_per_launch"] == rec["dram_bytes_per_launch"]
-    assert bench.recorded_traffic("gemv_k2560_n9728_wide", 64, "hf") == (None, None)
+    assert bench.recorded_traffic("gemv_k2560_n9728_wide", 32, "hf") == (None, None)
