@@ -385,6 +385,15 @@ int mbglu_last_cuda_error(void);
  * pass). */
 int mbglu_last_variant(void);
 
+/* Which kernels the calling thread's last glu_backward took for the
+ * gradients' second step: 0 none (the call launched no such step), 1 the
+ * separate grad_h and weight-gradient kernels, 2 one pass on the CUDA cores
+ * (M <= 2, or the tensor-core pass off), 3 one pass on the tensor cores
+ * (mma.sync; dG and dU enter as three bf16 terms, exact for normal fp32
+ * values).  Both one-pass kernels need M <= 8, K % 8 == 0, 16-byte aligned
+ * weights and weight gradients with row strides of whole 16-byte units. */
+int mbglu_last_backward_path(void);
+
 /* How many row blocks of the calling thread's last add_rmsnorm_glu* call ran
  * as the single kernel (the workspace / no-allocation paths); 0 when every
  * block took the two-kernel path or the call launched nothing. */

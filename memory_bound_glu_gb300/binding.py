@@ -28,7 +28,8 @@ EXPORTS = ("glu_gemv", "add_rmsnorm_glu", "add_rmsnorm_glu_ws", "add_rmsnorm_glu
            "mbglu_set_launch_policy",
            "mbglu_get_launch_policy",
            "mbglu_status_string", "mbglu_abi_version", "mbglu_last_cuda_error", "mbglu_last_variant",
-           "mbglu_last_single_kernel_blocks", "mbglu_noalloc_scratch_read", "mbglu_read_device_error")
+           "mbglu_last_single_kernel_blocks", "mbglu_noalloc_scratch_read", "mbglu_read_device_error",
+           "mbglu_last_backward_path")
 POLICY_SERIAL, POLICY_PDL, POLICY_PREFETCH = 0, 1, 2
 
 _lib = None
@@ -71,6 +72,7 @@ def _bind(l):
     l.mbglu_last_cuda_error.restype = i32
     l.mbglu_last_variant.restype = i32
     l.mbglu_last_single_kernel_blocks.restype = i32
+    l.mbglu_last_backward_path.restype = i32
     l.mbglu_noalloc_scratch_read.argtypes = [ctypes.POINTER(ctypes.c_int), i32]
     l.mbglu_noalloc_scratch_read.restype = i32
     l.mbglu_read_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -354,8 +356,15 @@ def gdn_gates(a, b, A_log, dt_bias, g=None, beta=None, stream=None):
 def last_variant() -> int:
     """Kernel the calling thread's last call launched: 0 none, 1 streaming
     (CUDA-core), 2 generic, 3 zero fill, 4 tensor-core streaming (batch >= 3),
-    5 silu_mul, 6 gdn_gates."""
+    5 silu_mul, 6 gdn_gates, 7 row blocks, 8 glu_backward, 9 tcgen05."""
     return lib().mbglu_last_variant()
+
+
+def last_backward_path() -> int:
+    """The second step of the calling thread's last glu_backward: 0 none, 1
+    separate kernels, 2 one pass on the CUDA cores, 3 one pass on the tensor
+    cores."""
+    return lib().mbglu_last_backward_path()
 
 
 def read_device_error() -> int:

@@ -46,7 +46,9 @@ struct BwdParams {
     int R, S;               // glu_bwd_rows_kernel: rows per stage, stages in the ring
     uint32_t off_ring;      // glu_bwd_rows_kernel: ring offset in dynamic shared memory
     int rows_cta;           // glu_bwd_rows_kernel, glu_bwd_hw_kernel: largest row share of a CTA
-    int col_groups;         // glu_bwd_hw_kernel: CTAs sharing a row share (each a group of column slices)
+    int col_groups;         // glu_bwd_hw_kernel, glu_bwd_mma_kernel: CTAs sharing a row share (each a group of column slices)
+    int rows_pad;           // glu_bwd_mma_kernel: rows_cta rounded up to a multiple of 16
+    uint32_t off_mn, off_nm;   // glu_bwd_mma_kernel: staged dG, dU (two layouts)
     int vec_w;              // gate, up rows 8-byte aligned: 4-element loads
     int vec_out;            // grad_gate, grad_up rows and h 16-byte aligned, K % 8 == 0: 8-element access
     int h_smem;             // glu_bwd_w_kernel: h staged in shared memory
@@ -437,6 +439,326 @@ __global__ void __launch_bounds__(32 * bwd_hw_warps(MB), 1) glu_bwd_hw_kernel(co
                 dst[0] = make_float4(acc[m][0].x, acc[m][0].y, acc[m][1].x, acc[m][1].y);
                 dst[1] = make_float4(acc[m][2].x, acc[m][2].y, acc[m][3].x, acc[m][3].y);
             }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Steps 2 and 3 on the tensor cores (glu_bwd_mma_kernel, M = 3..8)
+// ---------------------------------------------------------------------------
+// The pass of glu_bwd_hw_kernel with both contractions as bf16 MMAs
+// (mma.sync, fp32 accumulators):
+//   grad_h^T[k][m] += sum_n W[n][k] dG[m][n]    A = W^T from the stage, B = dG
+//   grad_W[n][k]    = sum_m dG[m][n] h[m][k]    A = dG^T,               B = h
+// dG and dU are fp32 and the MMA multiplies bf16, so each value x enters as
+// three bf16 terms: hi = bf16(x), mid = bf16(x - hi), lo = bf16(x - hi - mid)
+// (each difference exact in fp32).  bf16 keeps 8 of fp32's 24 significant
+// bits, so the three terms hold x exactly (unless lo falls below bf16's
+// normal range), and a product of two bf16 values is exact in fp32: the MMAs
+// see the same products as fp32 arithmetic would.  grad_h takes one m16n8k16
+// per term; grad_W lays the terms along the MMA's reduction, [hi m0..7 | mid
+// m0..7] against [h; h] (m16n8k16) and lo m0..7 against h (m16n8k8).  The
+// batch is padded to 8 with zero rows.
+//
+// A CTA owns a row share [n0, n1) and a group of column slices.  Its rows go
+// in blocks of 16, block b = [n0 + 16 b, n0 + 16 b + 16), the LAST block
+// first (the first step read the share in rising order and left its tail in
+// L2).  A block's tensor copy may run past n1 into the next share, or past N
+// where it reads zeros: those rows meet dG = dU = 0 (the staging is
+// zero-padded) and their weight gradients are not stored.  Warp w of column
+// group c owns the columns [x0, x0 + 64 NB), x0 = (c W + w) 64 NB, as NB
+// boxes of 64 columns x 16 rows per matrix and stage, 128-byte swizzled:
+// 16-byte chunk j of row r sits at r * 128 + ((j ^ (r & 7)) << 4), so the
+// transposed matrix loads of a column pair meet no bank conflict.  The
+// weight gradients need no weights, so a stage goes back to the copy engine
+// as soon as grad_h has read it.  In grad_W's MMAs, column j of tile t
+// (t = 4 p + t') stands for weight column 32 p + 8 (j / 2) + 2 t' + j % 2 of
+// the warp's slice: over the four tiles of a group, lane (g, c) then holds
+// 8 consecutive columns of rows g and g + 8, stored as one 16-byte piece
+// each.  part[s][m][k] receives the share's grad_h sums;
+// glu_bwd_h_reduce8_kernel adds the shares in order.
+//
+// Shared memory (dynamic, from a 1024-byte aligned base):
+//   [0, 512)                 mbarriers [warp][stage]
+//   [off_mn, + 96 rs)        [matrix][hi, mid, lo][8][rs] bf16, rs = rows_pad + 8: dG, dU
+//                            with the share's rows contiguous (the B operand of grad_h)
+//   [off_nm, + 96 rows_pad)  [matrix][rows_pad][24] bf16: row n holds hi m0..7, mid m0..7,
+//                            lo m0..7 (the A operand of grad_W; 48-byte rows meet no
+//                            bank conflict)
+//   [off_ring, ...)          ring [warp][stage][matrix][NB][16][64] bf16
+// at most 12 warps: the 160 registers a thread needs at NB = 2 leave room for
+// 3 warps on each of the SM's four register files
+__host__ __device__ constexpr int bwd_mma_warps(int NB) { return NB >= 4 ? 8 : 12; }
+constexpr uint32_t kBwdMmaBox = 16u * 128u;   // one 64-column x 16-row box, bytes
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// MMAs as plain (non-volatile) asm: register operands only, so the compiler
+// may interleave independent accumulators
+__device__ __forceinline__ void mma16_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// the same with C = 0
+__device__ __forceinline__ void mma16_bf16_z(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %10, %10, %10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+__device__ __forceinline__ void mma8_bf16(float (&d)[4], const uint32_t (&a)[2], uint32_t b0)
+{
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(b0));
+}
+
+// x = hi + mid + lo, each bf16 (exact for normal x down to 2^-110 or so);
+// mid = lo = 0 when hi is not finite
+__device__ __forceinline__ void split3_bf16(float x, uint16_t (&t)[3])
+{
+    t[0] = f32_to_bf16(x);
+    const float h = bf16_to_f32(t[0]);
+    if (!isfinite(h)) {
+        t[1] = t[2] = 0;
+        return;
+    }
+    const float r = x - h;
+    t[1] = f32_to_bf16(r);
+    t[2] = f32_to_bf16(r - bf16_to_f32(t[1]));
+}
+
+// One 16-row x 64-column piece of a weight gradient (two groups of four
+// tiles): D = [hi | mid]^T [h; h] + lo^T h, rounded to bf16 and stored.  a,
+// a8: the A fragments of the block's rows; hb[t0 .. t0 + 7]: the B fragments
+// (h[2c][k], h[2c+1][k]) at the tiles' permuted columns; dst: row g of the
+// piece's first column; nr valid rows, kleft columns left in the row.
+template <int NH>
+__device__ __forceinline__ void bwd_mma_w_tile(const uint32_t (&a)[4], const uint32_t (&a8)[2],
+                                               const uint32_t (&hb)[NH], int t0, uint16_t *dst, int64_t ld, int nr,
+                                               int kleft, int lane)
+{
+    float d[8][4];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) mma16_bf16_z(d[t], a, hb[t0 + t], hb[t0 + t]);
+#pragma unroll
+    for (int t = 0; t < 8; ++t) mma8_bf16(d[t], a8, hb[t0 + t]);
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+        const int col = 32 * p + 8 * c;
+        if (col >= kleft) continue;
+        const int t = 4 * p;
+        if (g < nr)
+            __stcs(reinterpret_cast<uint4 *>(dst + col),
+                   make_uint4(pack_bf16x2(d[t][0], d[t][1]), pack_bf16x2(d[t + 1][0], d[t + 1][1]),
+                              pack_bf16x2(d[t + 2][0], d[t + 2][1]), pack_bf16x2(d[t + 3][0], d[t + 3][1])));
+        if (g + 8 < nr)
+            __stcs(reinterpret_cast<uint4 *>(dst + 8 * ld + col),
+                   make_uint4(pack_bf16x2(d[t][2], d[t][3]), pack_bf16x2(d[t + 1][2], d[t + 1][3]),
+                              pack_bf16x2(d[t + 2][2], d[t + 2][3]), pack_bf16x2(d[t + 3][2], d[t + 3][3])));
+    }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(32 * bwd_mma_warps(NB), 1) glu_bwd_mma_kernel(const BwdParams q,
+                                                                              const __grid_constant__ BwdMaps maps)
+{
+    extern __shared__ __align__(128) unsigned char bm_raw[];
+    unsigned char *sm = bm_raw + ((1024u - (smem_addr(bm_raw) & 1023u)) & 1023u);
+    constexpr uint32_t kMat = NB * kBwdMmaBox;   // one matrix's part of a stage
+    constexpr uint32_t kStage = 2 * kMat;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int W = static_cast<int>(blockDim.x >> 5), S = q.S;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm) + warp * S;
+    unsigned char *ring = sm + q.off_ring + static_cast<uint32_t>(warp) * S * kStage;
+    const uint32_t ring_a = smem_addr(ring);
+    const uint32_t mn = smem_addr(sm + q.off_mn), nm = smem_addr(sm + q.off_nm);
+    const int rp = q.rows_pad, rs = rp + 8;
+    const int G = gridDim.x / q.col_groups;
+    const int share = blockIdx.x / q.col_groups, cgrp = blockIdx.x - share * q.col_groups;
+    const int n0 = static_cast<int>((static_cast<int64_t>(q.N) * share) / G);
+    const int n1 = static_cast<int>((static_cast<int64_t>(q.N) * (share + 1)) / G);
+    const int rows = n1 - n0, nblk = (rows + 15) >> 4;
+    const int x0 = (cgrp * W + warp) * (64 * NB);   // the warp's first column
+    const bool live = x0 < q.K;
+    const uint64_t policy = l2_policy_evict_first();
+
+    // the j-th block in order, block nblk - 1 - j, into stage j % S
+    auto fill = [&](int j) {
+        const int y = n0 + 16 * (nblk - 1 - j);
+        const int st = j % S;
+        unsigned char *dst = ring + st * kStage;
+        mbar_arrive_expect_tx(&bars[st], kStage);
+#pragma unroll
+        for (int i = 0; i < NB; ++i) {
+            tma_load_2d(dst + i * kBwdMmaBox, &maps.gate, x0 + 64 * i, y, &bars[st], policy);
+            tma_load_2d(dst + kMat + i * kBwdMmaBox, &maps.up, x0 + 64 * i, y, &bars[st], policy);
+        }
+    };
+
+    if (lane == 0 && live) {
+        for (int st = 0; st < S; ++st) mbar_init(&bars[st], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (lane == 0 && live)
+        for (int j = 0; j < min(S, nblk); ++j) fill(j);   // weights only: before the dependency wait
+    grid_dependency_wait();                                 // dG, dU of the first step
+
+    {   // dG, dU of the share as three bf16 terms, zero past the share and past M
+        uint16_t *mnp = reinterpret_cast<uint16_t *>(sm + q.off_mn);
+        uint16_t *nmp = reinterpret_cast<uint16_t *>(sm + q.off_nm);
+        for (int i = threadIdx.x; i < 8 * rp; i += blockDim.x) {
+            const int m = i / rp, r = i - m * rp;
+            float x[2] = {0.0f, 0.0f};
+            if (m < q.M && r < rows) {
+                x[0] = q.dG[static_cast<int64_t>(m) * q.ldm + n0 + r];
+                x[1] = q.dU[static_cast<int64_t>(m) * q.ldm + n0 + r];
+            }
+#pragma unroll
+            for (int mat = 0; mat < 2; ++mat) {
+                uint16_t t[3];
+                split3_bf16(x[mat], t);
+#pragma unroll
+                for (int e = 0; e < 3; ++e) {
+                    mnp[((mat * 3 + e) * 8 + m) * rs + r] = t[e];
+                    nmp[(mat * rp + r) * 24 + 8 * e + m] = t[e];
+                }
+            }
+        }
+    }
+    // B fragments of grad_W: hb[t] = (h[2c][k], h[2c+1][k]) with k the weight
+    // column of MMA column g in tile t = 4 p + t'
+    const int g4 = lane >> 2, c4 = lane & 3;
+    uint32_t hb[8 * NB];
+#pragma unroll
+    for (int t = 0; t < 8 * NB; ++t) {
+        const int k = x0 + 32 * (t >> 2) + 8 * (g4 >> 1) + 2 * (t & 3) + (g4 & 1);
+        uint32_t lo = 0, hi = 0;
+        if (k < q.K) {
+            if (2 * c4 < q.M) lo = q.h[static_cast<int64_t>(2 * c4) * q.ldh + k];
+            if (2 * c4 + 1 < q.M) hi = q.h[static_cast<int64_t>(2 * c4 + 1) * q.ldh + k];
+        }
+        hb[t] = lo | (hi << 16);
+    }
+    __syncthreads();   // dG, dU staged
+    if (!live) return;   // a slice past K (the last column group): no rows to stream
+
+    float acc[4 * NB][4];
+#pragma unroll
+    for (int i = 0; i < 4 * NB; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][e] = 0.0f;
+
+    const int mi = lane >> 3, ri = lane & 7;
+    for (int j = 0; j < nblk; ++j) {
+        const int st = j % S;
+        const uint32_t phase = static_cast<uint32_t>(j / S) & 1u;
+        if (!mbar_wait_bounded(&bars[st], phase, kWaitLimitNs)) {
+            if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
+            mbar_wait_bounded(&bars[st], phase, kWaitLimitNs);
+        }
+        const int nb0 = 16 * (nblk - 1 - j);   // the block's first row in the share
+        const int nr = min(16, rows - nb0);
+        const uint32_t sg = ring_a + st * kStage, su = sg + kMat;
+        {   // grad_h: the stage's weights, as W^T by transposed matrix loads.  B:
+            // dG, dU at the block's rows (hi n0-7, hi n8-15, mid n0-7, mid n8-15;
+            // then lo n0-7, lo n8-15)
+            uint32_t bg[4], bu[4], bg8[2], bu8[2];
+            const uint32_t off = static_cast<uint32_t>(((mi >> 1) * 8 + ri) * rs + nb0 + 8 * (mi & 1)) * 2u;
+            const uint32_t off8 = static_cast<uint32_t>((16 + ri) * rs + nb0 + 8 * (mi & 1)) * 2u;
+            const uint32_t up = 48u * static_cast<uint32_t>(rs);
+            ldsm_x4(bg, mn + off);
+            ldsm_x2(bg8, mn + off8);
+            ldsm_x4(bu, mn + up + off);
+            ldsm_x2(bu8, mn + up + off8);
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {
+                // the box's four 16-column groups, their MMAs interleaved term by term
+#pragma unroll
+                for (int mat = 0; mat < 2; ++mat) {
+                    uint32_t a[4][4];
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int n = ri + 8 * (mi >> 1), chunk = 2 * q4 + (mi & 1);
+                        ldsm_x4_trans(a[q4], (mat ? su : sg) +
+                                                 static_cast<uint32_t>(i * kBwdMmaBox + n * 128 + ((chunk ^ ri) << 4)));
+                    }
+                    const uint32_t(&b)[4] = mat ? bu : bg;
+                    const uint32_t(&b8)[2] = mat ? bu8 : bg8;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) mma16_bf16(acc[4 * i + q4], a[q4], b[0], b[1]);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) mma16_bf16(acc[4 * i + q4], a[q4], b[2], b[3]);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) mma16_bf16(acc[4 * i + q4], a[q4], b8[0], b8[1]);
+                }
+            }
+        }
+        // the weight gradients need no weights: the stage goes back to the
+        // copy engine now, and its next block streams in meanwhile
+        __syncwarp();
+        if (lane == 0 && j + S < nblk) {
+            fence_proxy_async_smem();
+            fill(j + S);
+        }
+        {   // grad_W's A: rows nb0 .. nb0 + 15 of [hi | mid], then of lo
+            uint32_t ag[4], au[4], ag8[2], au8[2];
+            const int n = nb0 + ri + 8 * (mi & 1);
+            const uint32_t off = static_cast<uint32_t>(n * 48 + ((mi >> 1) << 4));
+            const uint32_t off8 = static_cast<uint32_t>(n * 48 + 32);
+            const uint32_t up = 48u * static_cast<uint32_t>(rp);
+            ldsm_x4(ag, nm + off);
+            ldsm_x2(ag8, nm + off8);
+            ldsm_x4(au, nm + up + off);
+            ldsm_x2(au8, nm + up + off8);
+            const int64_t nrow = static_cast<int64_t>(n0) + nb0 + g4;   // row g of the block
+#pragma unroll
+            for (int i = 0; i < NB; ++i) {   // grad_gate, grad_up: the box's 16 x 64 pieces
+                const int col = x0 + 64 * i;
+                bwd_mma_w_tile(ag, ag8, hb, 8 * i, q.grad_gate + nrow * q.ldgg + col, q.ldgg, nr, q.K - col, lane);
+                bwd_mma_w_tile(au, au8, hb, 8 * i, q.grad_up + nrow * q.ldgu + col, q.ldgu, nr, q.K - col, lane);
+            }
+        }
+    }
+    grid_launch_dependents();
+    // acc[gq]: D[k][m] with k = x0 + 16 gq + g (+8), m = 2c (+1)
+#pragma unroll
+    for (int gq = 0; gq < 4 * NB; ++gq) {
+        const int k = x0 + 16 * gq + g4;
+        const int m = 2 * c4;
+        float *p0 = q.part + (static_cast<int64_t>(share) * q.M + m) * q.K;
+        if (m < q.M) {
+            if (k < q.K) p0[k] = acc[gq][0];
+            if (k + 8 < q.K) p0[k + 8] = acc[gq][2];
+        }
+        if (m + 1 < q.M) {
+            if (k < q.K) p0[q.K + k] = acc[gq][1];
+            if (k + 8 < q.K) p0[q.K + k + 8] = acc[gq][3];
         }
     }
 }

@@ -95,9 +95,12 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 __device__ __forceinline__ uint16_t f32_to_bf16(float x) { return __bfloat16_as_ushort(__float2bfloat16_rn(x)); }
 __device__ __forceinline__ float round_to_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+// two floats rounded to nearest-even bf16 in one paired conversion
+// (cvt.rn.bf16x2.f32), lo in the low half
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
-    return static_cast<uint32_t>(f32_to_bf16(lo)) | (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
 }
 
 // SiLU(x) = x / (1 + e^-x) = x * e^x / (1 + e^x), evaluated with t = e^-|x| so

@@ -29,6 +29,7 @@ using mbglu::GluParams;
 thread_local int t_last_cuda_error = 0;
 thread_local int t_last_variant = 0;
 thread_local int t_last_single = 0;   // row blocks of the last norm call that ran as the single kernel
+thread_local int t_last_bwd = 0;      // the last glu_backward's second step (mbglu_last_backward_path)
 
 enum Variant {
     kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4, kSiluMul = 5, kGdnGates = 6,
@@ -65,6 +66,9 @@ std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 
 // Overrides for tuning sweeps only; every default is chosen by plan_stream.
+// glu_bwd_mma_kernel: 64-column boxes per warp (2: 128-column slices; 4 measured slower)
+constexpr int kBwdNB = 2;
+
 struct Tuning {
     int warps = 0;            // warps per CTA of the streaming kernel (0: automatic)
     int rows = 0;             // rows per stage R in {1,2,4} (0: automatic)
@@ -83,6 +87,8 @@ struct Tuning {
     int tc_min_m = 17;        // smallest batch that takes the tcgen05 kernel
     int tc_split = 0;         // tcgen05 kernel: CTAs per tile (0: automatic, 1..4 where the plan allows)
     int bwd_fused = 1;        // backward: steps 2 and 3 in one pass where they apply (0: separate kernels)
+    int bwd_mma_min_m = 3;    // backward: smallest batch whose one-pass step takes the tensor cores (9: never)
+    int bwd_warps = 0;        // backward on the tensor cores: warps per CTA (0: automatic)
 };
 
 std::atomic<int> g_policy{MBGLU_POLICY_PREFETCH};
@@ -115,6 +121,8 @@ const Tuning &tuning()
         x.tc_min_m = std::min(65, std::max(1, env_int("MBGLU_TC_MIN_M", 17)));
         x.tc_split = std::min(mbglu::kTcMaxSplit, std::max(0, env_int("MBGLU_TC_SPLIT", 0)));
         x.bwd_fused = env_int("MBGLU_BWD_FUSED", 1) != 0;
+        x.bwd_mma_min_m = std::min(9, std::max(1, env_int("MBGLU_BWD_MMA_MIN_M", 3)));
+        x.bwd_warps = std::min(mbglu::bwd_mma_warps(kBwdNB), std::max(0, env_int("MBGLU_BWD_WARPS", 0)));
         return x;
     }();
     return t;
@@ -208,6 +216,9 @@ cudaError_t allow_smem_bwd_rows(int optin)
         e = cudaFuncSetAttribute(mbglu::glu_bwd_hw_kernel<TMB>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
     MBGLU_ALLOW_HW(1) MBGLU_ALLOW_HW(2) MBGLU_ALLOW_HW(4) MBGLU_ALLOW_HW(8)
 #undef MBGLU_ALLOW_HW
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mbglu::glu_bwd_mma_kernel<kBwdNB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin);
     return e;
 }
 
@@ -597,6 +608,8 @@ int mbglu_last_cuda_error(void) { return t_last_cuda_error; }
 int mbglu_last_variant(void) { return t_last_variant; }
 
 int mbglu_last_single_kernel_blocks(void) { return t_last_single; }
+
+int mbglu_last_backward_path(void) { return t_last_bwd; }
 
 mbglu_status gdn_gates(const mbglu_bf16 *a, int64_t lda, const mbglu_bf16 *b, int64_t ldb, const float *A_log,
                        const float *dt_bias, float *g, int64_t ldg, mbglu_bf16 *beta, int64_t ldbeta, int T, int H,
@@ -1092,6 +1105,76 @@ mbglu_status launch_bwd_hw(const BwdHwPlan &hp, const mbglu::BwdParams &q, const
     return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
 }
 
+// Plan of glu_bwd_mma_kernel (steps 2 and 3 on the tensor cores, M <= 8):
+// K in slices of 64 NB columns, one warp each; W warps per CTA cut K into
+// cg column groups, and the SMs into row shares of about N / (SMs / cg) rows;
+// stages of 16 rows, as many (2..4) as fit beside the staged dG, dU.  Of the
+// warp counts that fit, the most warps (each warp's chain of dependent steps
+// is what bounds the pass), then the most stages.
+struct BwdMmaPlan {
+    int NB = 2, cg = 1, warps = 1, shares = 1, rows_cta = 0, rows_pad = 0, S = 0;
+    uint32_t off_mn = 0, off_nm = 0, off_ring = 0, smem = 0;
+};
+
+bool plan_bwd_mma(const DeviceInfo &d, int M, int N, int K, const void *h, int64_t ldh, const void *gate_w,
+                  int64_t ld_gate, const void *up_w, int64_t ld_up, const void *grad_gate, int64_t ldgg,
+                  const void *grad_up, int64_t ldgu, BwdMmaPlan &mp)
+{
+    if (M > 8 || K % 8 != 0 || !aligned(gate_w, 16) || !aligned(up_w, 16) || ld_gate % 8 != 0 ||
+        ld_up % 8 != 0 || !aligned(grad_gate, 16) || !aligned(grad_up, 16) || ldgg % 8 != 0 || ldgu % 8 != 0)
+        return false;
+    const int NB = kBwdNB;
+    const int slice = 64 * NB;
+    const int wtot = (K + slice - 1) / slice;
+    const int wmax = tuning().bwd_warps > 0 ? tuning().bwd_warps : mbglu::bwd_mma_warps(NB);
+    const int wmin = tuning().bwd_warps > 0 ? tuning().bwd_warps : 1;
+    const int64_t stage = 2ll * NB * mbglu::kBwdMmaBox;
+    bool found = false;
+    int64_t best = -1;
+    for (int w = wmax; w >= wmin; --w) {
+        BwdMmaPlan c;
+        c.NB = NB;
+        c.cg = (wtot + w - 1) / w;
+        c.warps = (wtot + c.cg - 1) / c.cg;   // the same groups, balanced
+        if (c.warps != w) continue;
+        c.shares = std::max(1, std::min({(N + 15) / 16, d.sm_count / c.cg, kBwdMaxParts}));
+        c.rows_cta = (N + c.shares - 1) / c.shares;
+        c.rows_pad = (c.rows_cta + 15) / 16 * 16;
+        c.off_mn = 512;
+        c.off_nm = c.off_mn + 96u * static_cast<uint32_t>(c.rows_pad + 8);
+        c.off_ring = (c.off_nm + 96u * static_cast<uint32_t>(c.rows_pad) + 1023u) & ~1023u;
+        const int64_t room = static_cast<int64_t>(d.smem_optin) - 1024 - c.off_ring;   // 1024: base alignment
+        if (room <= 0) continue;
+        c.S = static_cast<int>(std::min<int64_t>({4, room / (c.warps * stage), 64 / c.warps}));
+        if (c.S < 2) continue;
+        c.smem = c.off_ring + static_cast<uint32_t>(c.warps * c.S * stage) + 1024u;
+        const int64_t score = 16ll * c.warps + c.S;
+        if (score > best) {
+            best = score;
+            mp = c;
+            found = true;
+        }
+    }
+    return found;
+}
+
+mbglu_status launch_bwd_mma(const BwdMmaPlan &mp, const mbglu::BwdParams &q, const mbglu::BwdMaps &maps,
+                            cudaStream_t stream)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(mp.shares * mp.cg);
+    cfg.blockDim = dim3(32 * mp.warps);
+    cfg.dynamicSmemBytes = mp.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = g_policy.load(std::memory_order_relaxed) != MBGLU_POLICY_SERIAL ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, mbglu::glu_bwd_mma_kernel<kBwdNB>, q, maps);
+    return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
+}
+
 mbglu_status launch_bwd_rows(const BwdRowsPlan &rp, int MB, const mbglu::BwdParams &q, cudaStream_t stream)
 {
     cudaLaunchConfig_t cfg = {};
@@ -1141,6 +1224,7 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
                           size_t workspace_bytes, cudaStream_t stream)
 {
     t_last_variant = kNone;
+    t_last_bwd = 0;
     if (M < 0 || N < 0 || K < 0 || M > MBGLU_MAX_M) return MBGLU_ERR_SHAPE;
     const bool want_h = grad_h != nullptr, want_w = grad_gate != nullptr || grad_up != nullptr;
     if (want_w && (!grad_gate || !grad_up)) return MBGLU_ERR_NULL;
@@ -1222,7 +1306,35 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
     q.vec_w = aligned(gate_w, 8) && aligned(up_w, 8) && ld_gate % 4 == 0 && ld_up % 4 == 0;
     cudaError_t e = cudaSuccess;
     // 2 + 3 in one pass over the rows where it applies (M <= 8, aligned):
-    // grad_h partials and both weight gradients, then the partials' sum
+    // grad_h partials and both weight gradients, then the partials' sum.
+    // From bwd_mma_min_m rows on, the pass runs on the tensor cores.
+    BwdMmaPlan mp;
+    mbglu::BwdMaps mmaps;
+    if (want_h && want_w && tuning().bwd_fused && M >= tuning().bwd_mma_min_m &&
+        plan_bwd_mma(*d, M, N, K, h, ldh, gate_w, ld_gate, up_w, ld_up, grad_gate, ldgg, grad_up, ldgu, mp) &&
+        encode_sw128_map(&mmaps.gate, gate_w, ld_gate, N, K, 16) &&
+        encode_sw128_map(&mmaps.up, up_w, ld_up, N, K, 16)) {
+        q.M = M;
+        q.dG = dG;
+        q.dU = dU;
+        q.rows_cta = mp.rows_cta;
+        q.rows_pad = mp.rows_pad;
+        q.col_groups = mp.cg;
+        q.S = mp.S;
+        q.off_mn = mp.off_mn;
+        q.off_nm = mp.off_nm;
+        q.off_ring = mp.off_ring;
+        st = launch_bwd_mma(mp, q, mmaps, stream);
+        if (st != MBGLU_OK) return st;
+        t_last_bwd = 3;
+        const int64_t warps = static_cast<int64_t>(M) * (K / 8);
+        const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(d->sm_count * 8, (warps + 7) / 8)));
+        const int vec_store = aligned(grad_h, 16) && ldgh % 8 == 0;
+        mbglu::glu_bwd_h_reduce8_kernel<<<rgrid, 256, 0, stream>>>(q, mp.shares, vec_store);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+        t_last_variant = kBackward;
+        return MBGLU_OK;
+    }
     BwdHwPlan hp;
     mbglu::BwdMaps hmaps;
     if (want_h && want_w && tuning().bwd_fused &&
@@ -1239,6 +1351,7 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
         q.off_ring = hp.off_ring;
         st = launch_bwd_hw(hp, q, hmaps, stream);
         if (st != MBGLU_OK) return st;
+        t_last_bwd = 2;
         const int64_t warps = static_cast<int64_t>(M) * (K / 8);
         const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(d->sm_count * 8, (warps + 7) / 8)));
         const int vec_store = aligned(grad_h, 16) && ldgh % 8 == 0;
@@ -1350,6 +1463,7 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
     }
     t_last_variant = kBackward;
+    t_last_bwd = 1;
     return MBGLU_OK;
 }
 

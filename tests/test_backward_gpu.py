@@ -59,7 +59,27 @@ def test_backward_every_batch_tile(M):
     got = mb.glu_backward(h.to(DEV), g.to(DEV), u.to(DEV), d.to(DEV))
     torch.cuda.synchronize()
     assert mb.last_variant() == BACKWARD
+    assert mb.last_backward_path() == (2 if M <= 2 else 3 if M <= 8 else 1)
     _check(tuple(t.cpu() for t in got), h, g, u, d, f"M={M}")
+    assert mb.read_device_error() == 0
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (3, 17, 8),        # one column box, 8 columns in it; shares of 8-9 rows (one partial block)
+    (6, 1000, 192),    # K a multiple of 64, not of 128: the last slice's second box lies past K
+    (7, 2049, 1032),   # a box with 8 columns in it; partial top blocks
+    (8, 40, 4096),     # 32 slices in several column groups; every share one partial block
+    (4, 9728, 2560),   # the headline layer at batch 4
+])
+def test_backward_tensor_core_pass(M, N, K):
+    """The one-pass step on the tensor cores (dG, dU as three bf16 terms):
+    ragged column slices and row blocks, against the oracle."""
+    h, g, u, d = _inputs(M, N, K, 100 + M, "bwtc")
+    got = mb.glu_backward(h.to(DEV), g.to(DEV), u.to(DEV), d.to(DEV))
+    torch.cuda.synchronize()
+    assert mb.last_backward_path() == 3
+    rows = None if N <= 2049 else np.sort(np.random.default_rng(M).choice(N, 600, replace=False))
+    _check(tuple(t.cpu() for t in got), h, g, u, d, f"tensor-core pass M={M} N={N} K={K}", rows=rows)
     assert mb.read_device_error() == 0
 
 
@@ -113,6 +133,7 @@ def test_backward_strided_and_subsets():
     ou = torch.full((N, K + 1), float("nan"), dtype=torch.bfloat16, device=DEV)
     mb.glu_backward(hd, gd, ud, dd, grad_h=oh[:, :K], grad_gate=og[:, 8:], grad_up=ou[:, :K])
     torch.cuda.synchronize()
+    assert mb.last_backward_path() == 1   # K % 8 != 0: the separate kernels
     assert torch.isnan(oh[:, K:].float()).all() and torch.isnan(og[:, :8].float()).all()
     assert torch.isnan(ou[:, K:].float()).all()
     full = (oh[:, :K].cpu(), og[:, 8:].cpu(), ou[:, :K].cpu())

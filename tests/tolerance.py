@@ -220,7 +220,11 @@ def assert_parity(gpu_bits, ref_bits, tau=None, what="", diag=None, K=None, mode
 #     dU = d*SiLU(g) by |d|*max|SiLU'|*eg (max|SiLU'| < 1.1) plus the same;
 #   * grad_h = sum over 2N products (any order: depth <= 2N + 64), grad_W
 #     = sum over M products (depth M + 1), each with the dG, dU error above
-#     carried through |W| or |h|.
+#     carried through |W| or |h|;
+#   * on the tensor cores (glu_bwd_mma_kernel) dG and dU enter exactly, as
+#     three bf16 terms, so grad_h sums 6N exact products and grad_W 3M, in
+#     the MMA's fp32 adds, bounded here as truncating (2^-23 each).  The
+#     floors take the looser of the two kernels' bounds.
 
 BWD_EVAL_REL = 16 * 2.0 ** -24
 SILU_D1_MAX = 1.1
@@ -240,9 +244,9 @@ def backward_floors(h, gate, up, dout, G, U, Ag, Au, K):
     edU = ad * SILU_D1_MAX * eg + BWD_EVAL_REL * np.abs(dU)
     M, N = G.shape
     ag, au, ah = np.abs(gate), np.abs(up), np.abs(h)
-    g2n = (2 * N + 64) * 2.0 ** -24
+    g2n = (6 * N + 64) * 2.0 ** -23
     tau_h = edG @ ag + edU @ au + g2n * (np.abs(dG) @ ag + np.abs(dU) @ au)
-    gm = (M + 1) * 2.0 ** -24
+    gm = (3 * M + 2) * 2.0 ** -23
     tau_gate = edG.T @ ah + gm * (np.abs(dG).T @ ah)
     tau_up = edU.T @ ah + gm * (np.abs(dU).T @ ah)
     return tau_h, tau_gate, tau_up
