@@ -51,13 +51,14 @@ def row_blocks(w, M):
     as row blocks of 16."""
     return -(-M // BLOCK_M) if w.op == "add_rmsnorm_glu" and M > BLOCK_M else 1
 KERNEL_NAMES = {1: "glu_stream_kernel", 2: "glu_generic_kernel", 4: "glu_mma_kernel", 5: "silu_mul_kernel",
-                9: "glu_tc_kernel (tcgen05)",
+                9: "glu_tc_kernel (tcgen05)", 10: "glu_slice_kernel",
                 6: "gdn_gates_kernel",
-                8: "glu_backward (the forward kernel with the dG/dU epilogue, glu_bwd_h_kernel, "
-                   "glu_bwd_h_reduce_kernel, glu_bwd_w_kernel)"}
+                8: "glu_backward (the forward kernel with the dG/dU epilogue, then glu_bwd_mma_kernel at "
+                   "M = 3-8 or glu_bwd_hw_kernel at M <= 2, and glu_bwd_h_reduce8_kernel)"}
 KERNEL_SOURCES = ["memory_bound_glu_gb300/csrc/glu_kernels.cuh", "memory_bound_glu_gb300/csrc/ptx.cuh",
                   "memory_bound_glu_gb300/csrc/mbglu_api.cu", "memory_bound_glu_gb300/csrc/glu_backward.cuh",
-                  "memory_bound_glu_gb300/csrc/glu_tc.cuh", "memory_bound_glu_gb300/csrc/tcgen05.cuh"]
+                  "memory_bound_glu_gb300/csrc/glu_tc.cuh", "memory_bound_glu_gb300/csrc/tcgen05.cuh",
+                  "memory_bound_glu_gb300/csrc/glu_slice.cuh"]
 
 
 def parse():

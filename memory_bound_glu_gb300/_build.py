@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmbglu.so")
 SOURCES = [os.path.join(HERE, "csrc", "mbglu_api.cu")]
 DEPS = SOURCES + [os.path.join(HERE, "csrc", f) for f in ("glu_kernels.cuh", "glu_backward.cuh", "glu_tc.cuh",
-                                                         "tcgen05.cuh", "ptx.cuh")] + \
+                                                         "glu_slice.cuh", "tcgen05.cuh", "ptx.cuh")] + \
     [os.path.join(ROOT, "include", "mbglu.h")]
 
 NVCC_FLAGS = [

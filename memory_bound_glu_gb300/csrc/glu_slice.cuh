@@ -1,0 +1,227 @@
+// glu_slice.cuh -- the dual-weight GLU GEMV at batch 1..8 on the tensor
+// cores, with h held in registers.
+//
+// DeepSpeed PR #8602, comment "Plan B: Dual-Weight GEMV", section "Plan B
+// Design": one pass over h reads gate_w and up_w in place and applies
+// SiLU(g) * u in the epilogue; the batched-decode shapes (M up to 8) are the
+// ones the comment's benchmark table runs.  g[m][n] = sum_k h[m][k] Wg[n][k],
+// u likewise, then the mode's epilogue (glu_epilogue) or the backward's dG, dU
+// (glu_store).
+//
+// Layout of the work.  A CTA owns a balanced share [r0, r1) of the N rows,
+// in groups of 8 (the MMA's n); the last group may run past r1 (its extra
+// rows belong to the next CTA or lie past N, where the copy reads zeros) and
+// only rows < r1 are stored.  Compute warp w owns the K columns [x0, x0 +
+// 256 SPW), x0 = 256 SPW w, as SPW segments of 256 columns: it holds h's MMA
+// fragments for those columns in registers for the whole kernel (32 SPW per
+// lane) and streams, for each of the CTA's groups in order, the group's 8
+// rows of both matrices over its segments through a private ring of S stages.
+// A stage is one segment: four 64-column x 8-row boxes per matrix (8 KB),
+// 128-byte swizzled (16-byte chunk j of row r at r * 128 + ((j ^ r) << 4)),
+// so each ldmatrix of 8 rows meets no bank conflict.  No h in shared memory,
+// so nearly all of it is ring: ~190 KB of weights in flight per SM.
+//
+// Arithmetic, for M <= 8: A (16 x 16) = h rows 0..7 (rows M..7 read as zero,
+// rows 8..15 are zero registers a1 and a3), B (16 x 8) = 8 weight rows, D = g (or u) for 8
+// batch rows x 8 features (d2, d3 stay zero).  Per segment one MMA chain per
+// matrix over its 16 k-steps, started from zero (the tensor core's adds are
+// not specified to round to nearest; a chain stays 16 MMAs long); the chains
+// are added to the warp's fp32 partial in segment order (round to nearest).
+// The warps' partials of a group go through a ring of kSliceSlots slots to
+// the epilogue warp (warp W), which adds them in warp order (round to
+// nearest) and stores.  Every sum runs in a fixed order: results are bitwise
+// deterministic and do not depend on the timing of the warps.
+//
+// Shared memory (dynamic, from a 1024-byte aligned base):
+//   [0, 512)        mbarriers [warp][stage] (W S <= 64)
+//   [512, 576)      slot barriers: full[kSliceSlots] (count 32 W), empty[kSliceSlots] (count 32)
+//   [1024, ...)     slots [kSliceSlots][W][4][32] fp32: lane l's g(m, n), g(m, n+1),
+//                   u(m, n), u(m, n+1), m = l / 4, n = 2 (l % 4)
+//   [off_ring, ...) ring [W][S][matrix][4][8][64] bf16
+#pragma once
+
+#include "glu_kernels.cuh"
+
+namespace mbglu {
+
+constexpr int kSliceBoxes = 4;                                  // 64-column boxes per segment
+constexpr int kSliceSeg = 64 * kSliceBoxes;                     // 256 columns
+constexpr uint32_t kSliceBox = 8u * 128u;                       // one 64 x 8 box, bytes
+constexpr uint32_t kSliceStage = 2u * kSliceBoxes * kSliceBox;  // both matrices, 8 KB
+constexpr int kSliceSlots = 4;                                  // group slots between warps and the epilogue warp
+// the most compute warps (plus the epilogue warp) at SPW segments per warp:
+// what the registers a thread needs (h's 32 SPW fragments and the rest)
+// leave on each of the SM's four register files
+__host__ __device__ constexpr int slice_max_warps(int spw) { return spw <= 1 ? 12 : spw == 2 ? 8 : 6; }
+constexpr uint32_t kSliceSlotBytes = 4u * 32u * 4u;             // one warp's partials of one group
+
+struct SliceMaps {
+    TensorMap gate, up;   // [N][K] bf16, box 64 x 8, 128-byte swizzle
+};
+
+template <int SPW>
+__global__ void __launch_bounds__(32 * (slice_max_warps(SPW) + 1), 1)
+    glu_slice_kernel(const GluParams p, const __grid_constant__ SliceMaps maps)
+{
+    extern __shared__ __align__(128) unsigned char sl_raw[];
+    unsigned char *sm = sl_raw + ((1024u - (smem_addr(sl_raw) & 1023u)) & 1023u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int W = static_cast<int>(blockDim.x >> 5) - 1;   // compute warps; warp W runs the epilogue
+    const int S = p.stages;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm);      // [W][S]
+    uint64_t *full = bars + 64;
+    uint64_t *empty = full + kSliceSlots;
+    float *slots = reinterpret_cast<float *>(sm + 1024);
+    const int r0 = static_cast<int>((static_cast<int64_t>(p.N) * blockIdx.x) / gridDim.x);
+    const int r1 = static_cast<int>((static_cast<int64_t>(p.N) * (blockIdx.x + 1)) / gridDim.x);
+    const int ngroups = (r1 - r0 + 7) >> 3;
+    const int x0 = warp * (SPW * kSliceSeg);
+    // this warp's segments: those that start before K
+    const int nseg = warp < W ? max(0, min(SPW, (p.K - x0 + kSliceSeg - 1) / kSliceSeg)) : 0;
+    const int nunits = ngroups * nseg;   // (group, segment), group-major
+    unsigned char *ring = sm + p.off_ring + static_cast<uint32_t>(warp) * S * kSliceStage;
+    // the backward's next step reads the weights again: keep them in L2 in that mode
+    const uint64_t policy = p.mode == kModeBwd ? l2_policy_evict_last() : l2_policy_evict_first();
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSliceSlots; ++s) {
+            mbar_init(&full[s], 32u * static_cast<uint32_t>(W));
+            mbar_init(&empty[s], 32u);
+        }
+    }
+    if (warp < W && lane == 0)
+        for (int st = 0; st < S; ++st) mbar_init(&bars[warp * S + st], 1);
+    fence_mbar_init();
+    __syncthreads();
+
+    // lane 0: unit u (group u / nseg, segment u % nseg) into stage u % S
+    auto fill = [&](int u) {
+        const int g = u / nseg, s = u - g * nseg;
+        const int st = u % S;
+        unsigned char *dst = ring + st * kSliceStage;
+        uint64_t *bar = &bars[warp * S + st];
+        const int y = r0 + 8 * g, x = x0 + s * kSliceSeg;
+        mbar_arrive_expect_tx(bar, kSliceStage);
+#pragma unroll
+        for (int i = 0; i < kSliceBoxes; ++i) {
+            tma_load_2d(dst + i * kSliceBox, &maps.gate, x + 64 * i, y, bar, policy);
+            tma_load_2d(dst + (kSliceBoxes + i) * kSliceBox, &maps.up, x + 64 * i, y, bar, policy);
+        }
+    };
+    // bounded waits for this warp's copies in flight, units u..u+S-1 (before an early return)
+    auto drain = [&](int u) {
+        if (lane == 0)
+            for (int v = u; v < min(u + S, nunits); ++v)
+                mbar_wait_bounded(&bars[warp * S + v % S], static_cast<uint32_t>((v / S) & 1), kWaitLimitNs);
+        __syncwarp();
+    };
+
+    if (p.prefetch && lane == 0)   // weights only: before the dependency wait
+        for (int u = 0; u < min(S, nunits); ++u) fill(u);
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (!p.prefetch && lane == 0)
+        for (int u = 0; u < min(S, nunits); ++u) fill(u);
+    __syncwarp();
+
+    if (warp == W) {   // the epilogue warp: each group's partials, added in warp order
+        const int m = lane >> 2, n = 2 * (lane & 3);
+        for (int g = 0; g < ngroups; ++g) {
+            const int sl = g % kSliceSlots;
+            if (!mbar_wait_bounded(&full[sl], static_cast<uint32_t>((g / kSliceSlots) & 1), kWaitLimitNs)) {
+                if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
+                return;
+            }
+            const float *src = slots + static_cast<int64_t>(sl) * W * (kSliceSlotBytes / 4);
+            float acc[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = src[e * 32 + lane];
+            for (int w = 1; w < W; ++w)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], src[(w * 4 + e) * 32 + lane]);
+            mbar_arrive(&empty[sl]);   // every lane, after its reads
+            const int row = r0 + 8 * g + n;
+            if (m < p.M) {
+                if (row < r1) glu_store(p, m, row, acc[0], acc[2]);
+                if (row + 1 < r1) glu_store(p, m, row + 1, acc[1], acc[3]);
+            }
+        }
+        return;
+    }
+
+    // h's A fragments: ha[2 j + e] = (h[g][k], h[g][k + 1]), k = x0 + 16 j + 8 e + 2 c
+    // (zero past K and for batch rows g >= M)
+    const int g4 = lane >> 2, c4 = lane & 3;
+    uint32_t ha[2 * 16 * SPW];
+#pragma unroll
+    for (int j = 0; j < 16 * SPW; ++j)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int k = x0 + 16 * j + 8 * e + 2 * c4;
+            uint32_t v = 0;
+            if (g4 < p.M && k < p.K) {
+                const uint16_t *src = p.h + static_cast<int64_t>(g4) * p.ldh + k;
+                v = p.vec_in ? *reinterpret_cast<const uint32_t *>(src)
+                             : static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 16);
+            }
+            ha[2 * j + e] = v;
+        }
+
+    const int mi = lane >> 3, ri = lane & 7;
+    int u = 0;
+    for (int g = 0; g < ngroups; ++g) {
+        float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // g(m, n), g(m, n+1), u(m, n), u(m, n+1)
+#pragma unroll
+        for (int s = 0; s < SPW; ++s) {
+            if (s >= nseg) break;
+            const int st = u % S;
+            if (!mbar_wait_bounded(&bars[warp * S + st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs)) {
+                if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
+                drain(u);
+                return;
+            }
+            const uint32_t sb = smem_addr(ring + st * kSliceStage);
+            float dg[4], du[4];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                // matrices: gate k 0-7, gate k 8-15, up k 0-7, up k 8-15 of this k-step
+                const int ch = 2 * j + (mi & 1);
+                uint32_t b[4];
+                ldsm_x4(b, sb + static_cast<uint32_t>((mi >> 1) * kSliceBoxes * kSliceBox + (ch >> 3) * kSliceBox +
+                                                      ri * 128 + (((ch & 7) ^ ri) << 4)));
+                const uint32_t a[4] = {ha[2 * (16 * s + j)], 0u, ha[2 * (16 * s + j) + 1], 0u};
+                if (j == 0) {
+                    mma16_bf16_z(dg, a, b[0], b[1]);
+                    mma16_bf16_z(du, a, b[2], b[3]);
+                } else {
+                    mma16_bf16(dg, a, b[0], b[1]);
+                    mma16_bf16(du, a, b[2], b[3]);
+                }
+            }
+            part[0] = __fadd_rn(part[0], dg[0]);
+            part[1] = __fadd_rn(part[1], dg[1]);
+            part[2] = __fadd_rn(part[2], du[0]);
+            part[3] = __fadd_rn(part[3], du[1]);
+            __syncwarp();
+            if (lane == 0 && u + S < nunits) {
+                fence_proxy_async_smem();
+                fill(u + S);   // the unit S ahead, into the stage just read
+            }
+            ++u;
+        }
+        // the group's partials to the epilogue warp
+        const int sl = g % kSliceSlots;
+        if (g >= kSliceSlots &&
+            !mbar_wait_bounded(&empty[sl], static_cast<uint32_t>((g / kSliceSlots - 1) & 1), kWaitLimitNs)) {
+            if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
+            drain(u);
+            return;
+        }
+        float *dst = slots + (static_cast<int64_t>(sl) * W + warp) * (kSliceSlotBytes / 4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dst[e * 32 + lane] = part[e];
+        mbar_arrive(&full[sl]);   // every lane: releases its own stores
+    }
+}
+
+}  // namespace mbglu

@@ -21,6 +21,7 @@
 #include "glu_kernels.cuh"
 #include "glu_backward.cuh"
 #include "glu_tc.cuh"
+#include "glu_slice.cuh"
 
 namespace {
 
@@ -35,7 +36,8 @@ enum Variant {
     kNone = 0, kStream = 1, kGeneric = 2, kZeroFill = 3, kTensor = 4, kSiluMul = 5, kGdnGates = 6,
     kRowBlocks = 7,  // a batch above kBlockRows, run as row blocks
     kBackward = 8,   // glu_backward
-    kTcGemv = 9      // the tcgen05 kernel (one pass for batch 17..64)
+    kTcGemv = 9,     // the tcgen05 kernel (one pass for batch 17..64)
+    kSlice = 10      // the K-slice tensor-core kernel (batch 3..8, h in registers)
 };
 constexpr int kBlockRows = mbglu::kMaxM;   // rows one GEMV kernel takes (its batch tile)
 
@@ -89,6 +91,9 @@ struct Tuning {
     int bwd_fused = 1;        // backward: steps 2 and 3 in one pass where they apply (0: separate kernels)
     int bwd_mma_min_m = 3;    // backward: smallest batch whose one-pass step takes the tensor cores (9: never)
     int bwd_warps = 0;        // backward on the tensor cores: warps per CTA (0: automatic)
+    int slice = 1;            // batches of slice_min_m..8 on the K-slice kernel where it applies (0: never)
+    int slice_min_m = 1;      // smallest batch that takes the K-slice kernel
+    int slice_spw = 0;        // K-slice kernel: 256-column segments per warp (0: automatic, 1..3)
 };
 
 std::atomic<int> g_policy{MBGLU_POLICY_PREFETCH};
@@ -123,6 +128,9 @@ const Tuning &tuning()
         x.bwd_fused = env_int("MBGLU_BWD_FUSED", 1) != 0;
         x.bwd_mma_min_m = std::min(9, std::max(1, env_int("MBGLU_BWD_MMA_MIN_M", 3)));
         x.bwd_warps = std::min(mbglu::bwd_mma_warps(kBwdNB), std::max(0, env_int("MBGLU_BWD_WARPS", 0)));
+        x.slice = env_int("MBGLU_SLICE", 1) != 0;
+        x.slice_min_m = std::min(9, std::max(1, env_int("MBGLU_SLICE_MIN_M", 1)));
+        x.slice_spw = std::min(3, std::max(0, env_int("MBGLU_SLICE_SPW", 0)));
         return x;
     }();
     return t;
@@ -222,6 +230,16 @@ cudaError_t allow_smem_bwd_rows(int optin)
     return e;
 }
 
+cudaError_t allow_smem_slice(int optin)
+{
+    cudaError_t e = cudaFuncSetAttribute(mbglu::glu_slice_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mbglu::glu_slice_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mbglu::glu_slice_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    return e;
+}
+
 cudaError_t allow_smem_tc(int optin)
 {
     return cudaFuncSetAttribute(mbglu::glu_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
@@ -244,7 +262,7 @@ mbglu_status device_info(const DeviceInfo **out)
         const cudaError_t errs[] = {allow_all_stream_kernels(d.smem_optin), allow_smem_mma<false>(d.smem_optin),
                                     allow_smem_mma<true>(d.smem_optin), allow_smem_generic(d.smem_optin),
                                     allow_smem_bwd(), allow_smem_bwd_rows(d.smem_optin),
-                                    allow_smem_tc(d.smem_optin)};
+                                    allow_smem_tc(d.smem_optin), allow_smem_slice(d.smem_optin)};
         for (cudaError_t x : errs)
             if (x != cudaSuccess) return cuda_fail(x);
         d.ready = true;
@@ -750,6 +768,71 @@ struct BwdEpilogue {
 
 // The GEMV on 1 <= M <= kBlockRows rows, N >= 1, arguments already checked.
 // bwd != nullptr: K >= 1, and the epilogue is the backward's (out unused).
+// Plan of glu_slice_kernel (batch 1..8, K >= 256): K in segments of
+// 256 columns, SPW per compute warp (h's fragments for them in registers:
+// 32 SPW per lane), W = ceil(segments / SPW) compute warps plus the epilogue
+// warp; one CTA per SM over balanced row shares; as many stages per warp
+// (2..6) as fit.  The smallest SPW that fits: more warps, each with a shorter
+// chain of dependent steps, beat deeper rings (K2560, M = 4: 16.0 us at SPW 1
+// with 2 stages, 18.0 at SPW 2 with 5).  Below mma_min_m rows only SPW 1: at
+// M = 1-2 it beats the CUDA-core streaming kernel (K2560 N9728, M = 1: 16.18
+// against 16.58 us), but SPW 2 does not (K4096: 36.8 against 35.2 us).
+bool encode_sw128_map(mbglu::TensorMap *out, const void *base, int64_t ld, int rows, int K, int box_rows);
+
+struct SlicePlan {
+    int spw = 1, warps = 1, stages = 0, grid = 1;
+    uint32_t off_ring = 0, smem = 0;
+};
+
+bool plan_slice(const DeviceInfo &d, int M, int N, int K, SlicePlan &sp)
+{
+    const Tuning &t = tuning();
+    if (!t.slice || M < t.slice_min_m || M > 8 || K < mbglu::kSliceSeg || K % 8 != 0 || N < 1) return false;
+    const int nseg = (K + mbglu::kSliceSeg - 1) / mbglu::kSliceSeg;
+    const int spw_max = M < t.mma_min_m ? 1 : 3;
+    for (int spw = 1; spw <= spw_max; ++spw) {
+        if (t.slice_spw && spw != t.slice_spw) continue;
+        const int W = (nseg + spw - 1) / spw;
+        if (W > mbglu::slice_max_warps(spw) || (W - 1) * spw >= nseg) continue;
+        SlicePlan c;
+        c.spw = spw;
+        c.warps = W;
+        c.off_ring = (1024u + mbglu::kSliceSlots * static_cast<uint32_t>(W) * mbglu::kSliceSlotBytes + 1023u) & ~1023u;
+        const int64_t room = static_cast<int64_t>(d.smem_optin) - 1024 - c.off_ring;   // 1024: base alignment
+        if (room <= 0) continue;
+        c.stages = static_cast<int>(std::min<int64_t>({6, room / (static_cast<int64_t>(W) * mbglu::kSliceStage),
+                                                       64 / W}));
+        if (c.stages < 2) continue;
+        c.smem = c.off_ring + static_cast<uint32_t>(W * c.stages) * mbglu::kSliceStage + 1024u;
+        c.grid = std::max(1, std::min(d.sm_count, (N + 7) / 8));
+        sp = c;
+        return true;
+    }
+    return false;
+}
+
+mbglu_status launch_slice(const SlicePlan &sp, const GluParams &p, const mbglu::SliceMaps &maps,
+                          cudaStream_t stream, bool pdl)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sp.grid);
+    cfg.blockDim = dim3(32 * (sp.warps + 1));
+    cfg.dynamicSmemBytes = sp.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (sp.spw) {
+        case 1: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<1>, p, maps); break;
+        case 2: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<2>, p, maps); break;
+        default: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<3>, p, maps); break;
+    }
+    return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
+}
+
 mbglu_status gemv_block(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate_w, int64_t ld_gate,
                         const mbglu_bf16 *up_w, int64_t ld_up, mbglu_bf16 *out, int64_t ldo, int M, int N, int K,
                         mbglu_mode mode, cudaStream_t stream, const BwdEpilogue *bwd = nullptr)
@@ -799,6 +882,17 @@ mbglu_status gemv_block(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate
     const bool bulk_ok = (K % 8 == 0) && aligned(gate_w, 16) && aligned(up_w, 16) && (ld_gate % 8 == 0) &&
                          (ld_up % 8 == 0);
     const bool h_vec = aligned(h, 16) && (ldh % 8 == 0);
+    SlicePlan sp;
+    mbglu::SliceMaps smaps;
+    if (bulk_ok && plan_slice(*d, M, N, K, sp) && encode_sw128_map(&smaps.gate, gate_w, ld_gate, N, K, 8) &&
+        encode_sw128_map(&smaps.up, up_w, ld_up, N, K, 8)) {
+        p.stages = sp.stages;
+        p.off_ring = sp.off_ring;
+        p.vec_in = h_vec;
+        st = launch_slice(sp, p, smaps, stream, pdl);
+        if (st == MBGLU_OK) t_last_variant = kSlice;
+        return st;
+    }
     if (bulk_ok && plan_mma(*d, M, N, K, pl, 0, mbglu::kMaxStreamWarps, h_vec)) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;

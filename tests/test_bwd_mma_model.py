@@ -19,14 +19,11 @@ tensor copy lands on a 1024-byte boundary with x a multiple of 8 elements."""
 import numpy as np
 import pytest
 
+from frag_model import C4, G4, LANE, MI, RI, Smem, bf16_rn, mma
+
 SMEM_OPTIN = 232448        # GB300: max dynamic shared memory per block (opt-in)
 BOX = 16 * 128             # one 64-column x 16-row box of bf16, bytes
 MAX_PARTS = 256
-
-LANE = np.arange(32)
-G4, C4 = LANE >> 2, LANE & 3     # mma: group id, thread in group
-MI, RI = LANE >> 3, LANE & 7     # ldmatrix / stmatrix: matrix, row of the lane's address
-
 
 def bwd_mma_warps(NB):
     return 8 if NB >= 4 else 12
@@ -66,13 +63,6 @@ def plan(M, N, K, sms, NB=2, warps=0):
     return best
 
 
-def bf16_rn(x):
-    """float32 -> the nearest bf16 (ties to even), as float32 (finite x)."""
-    b = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    r = ((b + 0x7FFF + ((b >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
-    return r.view(np.float32)
-
-
 def split3(x):
     """x = hi + mid + lo in bf16 terms, each difference taken in fp32."""
     x = x.astype(np.float32)
@@ -81,59 +71,6 @@ def split3(x):
     mid = bf16_rn(r)
     lo = bf16_rn((r - mid).astype(np.float32))
     return [t.astype(np.float64) for t in (hi, mid, lo)]
-
-
-class Smem:
-    """Shared memory as float64 slots, one per bf16 (byte offset // 2) from the
-    kernel's 1024-byte aligned base; every access names its region."""
-
-    def __init__(self, nbytes):
-        self.nbytes = nbytes
-        self.v = np.full(nbytes // 2, np.nan)
-
-    def rows16(self, addrs, region):
-        lo, hi = region
-        addrs = np.asarray(addrs)
-        assert np.all(addrs % 16 == 0), "matrix rows are 16-byte aligned"
-        assert np.all(addrs >= lo) and np.all(addrs + 16 <= hi), (addrs.min(), addrs.max(), region)
-        assert hi <= self.nbytes
-        return (addrs // 2)[:, None] + np.arange(8)[None, :]   # [lanes][8] slots
-
-    def ldsm(self, addrs, region, trans=False, x=4):
-        """ldmatrix .x4 / .x2: lanes 8i..8i+7 address the rows of matrix i; lane t
-        gets, per matrix, (row t/4, columns 2(t%4), +1), or the transpose's."""
-        addrs = np.asarray(addrs)[:8 * x]
-        vals = self.v[self.rows16(addrs, region)].reshape(x, 8, 8)   # [matrix][row][col]
-        assert not np.any(np.isnan(vals)), "read of unwritten shared memory"
-        if trans:
-            vals = vals.transpose(0, 2, 1)
-        out = np.empty((32, x, 2))
-        for e in range(2):
-            out[:, :, e] = vals[:, G4, 2 * C4 + e].T
-        return out
-
-
-def mma(d, a, b0, b1=None):
-    """mma.sync .row.col, d [32][4] += A x B from fragments: m16n8k16 (a: 4
-    registers, b0 and b1) or m16n8k8 (a: 2 registers, b0 only)."""
-    kk = 16 if a.shape[1] == 4 else 8
-    A = np.zeros((16, kk))
-    B = np.zeros((kk, 8))
-    D = np.zeros((16, 8))
-    for e in range(2):
-        A[G4, 2 * C4 + e] = a[:, 0, e]
-        A[G4 + 8, 2 * C4 + e] = a[:, 1, e]
-        B[2 * C4 + e, G4] = b0[:, e]
-        if kk == 16:
-            A[G4, 2 * C4 + 8 + e] = a[:, 2, e]
-            A[G4 + 8, 2 * C4 + 8 + e] = a[:, 3, e]
-            B[2 * C4 + 8 + e, G4] = b1[:, e]
-        D[G4, 2 * C4 + e] = d[:, e]
-        D[G4 + 8, 2 * C4 + e] = d[:, 2 + e]
-    D = D + A @ B
-    for e in range(2):
-        d[:, e] = D[G4, 2 * C4 + e]
-        d[:, 2 + e] = D[G4 + 8, 2 * C4 + e]
 
 
 def replay(M, N, K, sms, NB=2, warps=0, seed=0):

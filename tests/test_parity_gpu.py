@@ -41,7 +41,7 @@ def oracle_glu(h, g, u, mode):
 
 def parity(got, ref, tau_info, what=""):
     tau, diag, K, mode = tau_info
-    if mb.last_variant() in (4, 7, 9):   # tensor-core accumulation bound (7: row blocks, mostly; 9: tcgen05)
+    if mb.last_variant() in (4, 7, 9, 10):   # tensor-core accumulation bound (7: row blocks, mostly; 9: tcgen05)
         diag["acc"] = "mma"
         tau = tol.conditioning_floor(diag, K, mode)
     return tol.assert_parity(got, ref, tau, what, diag=diag, K=K, mode=mode)
@@ -53,7 +53,8 @@ def run_gpu(h, g, u, mode, **kw):
     return gi.bits(out.cpu())
 
 
-FAST = (1, 4)   # the streaming kernels: CUDA-core FMA, tensor core
+FAST = (1, 4, 10)   # the streaming kernels: CUDA-core FMA, tensor core, tensor core with h in registers
+SLICE = 10          # mbglu_last_variant(): the K-slice tensor-core kernel (batch 1..8; at 1-2 only K <= 3072)
 
 
 def check(h, g, u, mode, what="", variant=None):
@@ -109,13 +110,14 @@ def test_large_m16_k_uses_generic_when_h_does_not_fit():
 
 
 @pytest.mark.parametrize("M,N,K", [(16, 700, 4096), (13, 1337, 4096), (16, 153, 6144), (9, 700, 8192),
-                                   (16, 300, 8192)])
+                                   (16, 300, 8192), (8, 1000, 6144)])
 @pytest.mark.parametrize("mode", ["fused", "hf"])
 def test_tensor_core_k_phases(M, N, K, mode):
     """M*K too large to keep h whole beside a deep ring: the tensor-core kernel
     stages h through shared memory in two K-phases and carries every group's
     accumulators across the boundary (the last two shapes did not fit the
-    tensor-core kernel at all with h whole)."""
+    tensor-core kernel at all with h whole).  Batch 8 at K = 6144 lies past
+    the K-slice kernel's reach and runs here too."""
     h = gi.normal_bf16((M, K), 1.0, M, "kp-h")
     g = gi.normal_bf16((N, K), K ** -0.5, M, "kp-g")
     u = gi.normal_bf16((N, K), K ** -0.5, M, "kp-u")
@@ -165,11 +167,14 @@ def test_strided_views_fast_and_generic():
     parity(gi.bits(o2.cpu()), ref2, tau2, "unaligned")
 
 
-@pytest.mark.parametrize("K,ld_pad,h_off,expect", [(2560, 0, 0, 1), (2560, 64, 8, 1), (4096, 8, 1, 1),
-                                                    (1024, 0, 3, 1), (5120, 0, 0, 1), (2568, 0, 0, 1)])
+@pytest.mark.parametrize("K,ld_pad,h_off,expect", [(2560, 0, 0, SLICE), (2560, 64, 8, SLICE), (4096, 8, 1, 1),
+                                                    (1024, 0, 3, SLICE), (5120, 0, 0, 1), (2568, 0, 0, SLICE),
+                                                    (3584, 0, 2, 1)])
 def test_batch_one_paths(K, ld_pad, h_off, expect):
-    """M = 1: strided weight rows, an h that is not 16-byte aligned (h held in
-    registers), K above the register-resident limit (h in shared memory)."""
+    """M = 1: strided weight rows, an h that is not 16-byte aligned; up to
+    K = 3072 the K-slice kernel (h in registers, one segment per warp), above
+    it the CUDA-core streaming kernel (h in registers up to K = 4096, in shared
+    memory beyond)."""
     N = 2111
     hb = gi.normal_bf16((1, K + 8), 1.0, K, "m1-h")
     gb = gi.normal_bf16((N, K + ld_pad), K ** -0.5, K, "m1-g")
@@ -185,13 +190,14 @@ def test_batch_one_paths(K, ld_pad, h_off, expect):
 @pytest.mark.parametrize("M", [3, 4, 5, 8, 9, 12, 16])
 @pytest.mark.parametrize("mode", ["fused", "hf"])
 def test_tensor_core_kernel(M, mode):
-    """Batch >= 3 on the tensor-core kernel: ragged N (partial last 8-row
-    group), several K-segments, rows padded in shared memory."""
+    """Batch >= 3 on the tensor cores: ragged N (partial last 8-row group),
+    several K-segments; batches of 3..8 on the K-slice kernel (h in
+    registers), 9..16 on the kernel with h in shared memory."""
     N, K = 1339, 2560
     h = gi.normal_bf16((M, K), 1.0, M, "tc-h")
     g = gi.normal_bf16((N, K), K ** -0.5, M, "tc-g")
     u = gi.normal_bf16((N, K), K ** -0.5, M, "tc-u")
-    check(h, g, u, mode, f"tc M={M}", variant=4)
+    check(h, g, u, mode, f"tc M={M}", variant=SLICE if M <= 8 else 4)
 
 
 @pytest.mark.parametrize("K,ld_pad,h_off", [(1024, 8, 8), (4096, 0, 0), (2576, 16, 1), (1040, 0, 0)])
@@ -204,7 +210,7 @@ def test_tensor_core_kernel_strides_and_k(K, ld_pad, h_off):
     ref, tau = oracle_glu(h.contiguous(), g.contiguous(), u.contiguous(), "hf")
     out = mb.glu_gemv(hb.to(DEV)[:, h_off:h_off + K], gb.to(DEV)[:, :K], ub.to(DEV)[:, :K], mode="hf")
     torch.cuda.synchronize()
-    assert mb.last_variant() == 4
+    assert mb.last_variant() == SLICE
     parity(gi.bits(out.cpu()), ref, tau, f"tc K={K}")
 
 
