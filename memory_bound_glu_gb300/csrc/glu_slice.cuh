@@ -32,11 +32,22 @@
 // nearest) and stores.  Every sum runs in a fixed order: results are bitwise
 // deterministic and do not depend on the timing of the warps.
 //
+// NORM (add_rmsnorm_glu, [9057/Changes] zero-centred RMSNorm): the block
+// first forms h in shared memory with the norm prologue of the other kernels
+// (residual rows copied in, s = bf16(x + residual) when fused, the
+// double-float statistic and the correctly rounded h = bf16(s inv (1 + w)),
+// all threads taking part), at a row pitch of K + 8 so that the warps' loads
+// of their fragments meet no bank conflict; a barrier then hands the region
+// to the slots.  When fused, the epilogue warp writes this CTA's slice of the
+// residual at the end, once every CTA has read it (fused_residual_helper).
+//
 // Shared memory (dynamic, from a 1024-byte aligned base):
 //   [0, 512)        mbarriers [warp][stage] (W S <= 64)
 //   [512, 576)      slot barriers: full[kSliceSlots] (count 32 W), empty[kSliceSlots] (count 32)
+//   [784, 792)      NORM: the prologue copies' mbarrier (kProBarOffset)
 //   [1024, ...)     slots [kSliceSlots][W][4][32] fp32: lane l's g(m, n), g(m, n+1),
-//                   u(m, n), u(m, n+1), m = l / 4, n = 2 (l % 4)
+//                   u(m, n), u(m, n+1), m = l / 4, n = 2 (l % 4); NORM: first h_s[M][K + 8]
+//   [off_s, ...)    NORM: norm_w [K] bf16, then the statistic's partials (2 floats per thread)
 //   [off_ring, ...) ring [W][S][matrix][4][8][64] bf16
 #pragma once
 
@@ -59,11 +70,12 @@ struct SliceMaps {
     TensorMap gate, up;   // [N][K] bf16, box 64 x 8, 128-byte swizzle
 };
 
-template <int SPW>
+template <int SPW, bool NORM>
 __global__ void __launch_bounds__(32 * (slice_max_warps(SPW) + 1), 1)
     glu_slice_kernel(const GluParams p, const __grid_constant__ SliceMaps maps)
 {
     extern __shared__ __align__(128) unsigned char sl_raw[];
+    __shared__ float inv_s[2 * 8];   // NORM: (inv_hi, inv_lo) per row
     unsigned char *sm = sl_raw + ((1024u - (smem_addr(sl_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int W = static_cast<int>(blockDim.x >> 5) - 1;   // compute warps; warp W runs the epilogue
@@ -83,11 +95,16 @@ __global__ void __launch_bounds__(32 * (slice_max_warps(SPW) + 1), 1)
     // the backward's next step reads the weights again: keep them in L2 in that mode
     const uint64_t policy = p.mode == kModeBwd ? l2_policy_evict_last() : l2_policy_evict_first();
 
+    uint64_t *pro_bar = reinterpret_cast<uint64_t *>(sm + kProBarOffset);
+    uint16_t *h_s = reinterpret_cast<uint16_t *>(sm + 1024);   // NORM: [M][K + 8], before the slots
+    uint16_t *nw_s = reinterpret_cast<uint16_t *>(sm + p.off_s);
+    const int HS = p.K + 8;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kSliceSlots; ++s) {
             mbar_init(&full[s], 32u * static_cast<uint32_t>(W));
             mbar_init(&empty[s], 32u);
         }
+        if constexpr (NORM) mbar_init(pro_bar, 2);   // the norm_w copy and the residual copy
     }
     if (warp < W && lane == 0)
         for (int st = 0; st < S; ++st) mbar_init(&bars[warp * S + st], 1);
@@ -116,13 +133,46 @@ __global__ void __launch_bounds__(32 * (slice_max_warps(SPW) + 1), 1)
         __syncwarp();
     };
 
-    if (p.prefetch && lane == 0)   // weights only: before the dependency wait
-        for (int u = 0; u < min(S, nunits); ++u) fill(u);
+    auto copy_norm_w = [&]() {
+        if constexpr (NORM) {
+            if (threadIdx.x == 0) {
+                mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.K) * 2u);
+                bulk_g2s_plain(nw_s, p.norm_w, static_cast<uint32_t>(p.K) * 2u, pro_bar);
+            }
+        }
+    };
+    if (p.prefetch) {   // weights only: before the dependency wait
+        copy_norm_w();
+        if (lane == 0)
+            for (int u = 0; u < min(S, nunits); ++u) fill(u);
+    }
     grid_dependency_wait();
     grid_launch_dependents();
-    if (!p.prefetch && lane == 0)
-        for (int u = 0; u < min(S, nunits); ++u) fill(u);
+    if (!p.prefetch) {
+        copy_norm_w();
+        if (lane == 0)
+            for (int u = 0; u < min(S, nunits); ++u) fill(u);
+    }
     __syncwarp();
+
+    if constexpr (NORM) {   // h = the normed rows, in h_s (every thread of the block)
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(pro_bar, static_cast<uint32_t>(p.M) * static_cast<uint32_t>(p.K) * 2u);
+            copy_rows_async(h_s, HS, p.s, p.K, p.M, p.K, pro_bar);   // the residual rows, padded
+        }
+        const RowMap rm = row_map(p.M, p.K);
+        XRows xr;
+        if (p.fused) x_prefetch_rows(p, rm, xr);
+        prologue_wait(pro_bar);
+        float2 ss;
+        if (p.fused) {
+            if (threadIdx.x == 0) fused_arrive(p);
+            ss = add_rows_in_place(p, rm, h_s, HS, xr);
+        } else {
+            ss = square_rows(rm, h_s, HS);
+        }
+        norm_rows_in_place(p, rm, ss, h_s, HS, nw_s, norm_partials(sm, p), inv_s, p.M);   // ends with a barrier
+    }
 
     if (warp == W) {   // the epilogue warp: each group's partials, added in warp order
         const int m = lane >> 2, n = 2 * (lane & 3);
@@ -146,6 +196,9 @@ __global__ void __launch_bounds__(32 * (slice_max_warps(SPW) + 1), 1)
                 if (row + 1 < r1) glu_store(p, m, row + 1, acc[1], acc[3]);
             }
         }
+        if constexpr (NORM) {
+            if (p.fused) fused_residual_helper(p);   // this CTA's slice of residual = bf16(x + residual)
+        }
         return;
     }
 
@@ -160,13 +213,18 @@ __global__ void __launch_bounds__(32 * (slice_max_warps(SPW) + 1), 1)
             const int k = x0 + 16 * j + 8 * e + 2 * c4;
             uint32_t v = 0;
             if (g4 < p.M && k < p.K) {
-                const uint16_t *src = p.h + static_cast<int64_t>(g4) * p.ldh + k;
-                v = p.vec_in ? *reinterpret_cast<const uint32_t *>(src)
-                             : static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 16);
+                if constexpr (NORM) {
+                    v = *reinterpret_cast<const uint32_t *>(h_s + g4 * HS + k);
+                } else {
+                    const uint16_t *src = p.h + static_cast<int64_t>(g4) * p.ldh + k;
+                    v = p.vec_in ? *reinterpret_cast<const uint32_t *>(src)
+                                 : static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 16);
+                }
             }
             ha[2 * j + e] = v;
         }
 
+    if constexpr (NORM) bar_sync_named(1, 32 * W);   // every compute warp holds h: the slots may reuse h_s
     const int mi = lane >> 3, ri = lane & 7;
     int u = 0;
     for (int g = 0; g < ngroups; ++g) {

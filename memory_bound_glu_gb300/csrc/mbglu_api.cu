@@ -232,11 +232,18 @@ cudaError_t allow_smem_bwd_rows(int optin)
 
 cudaError_t allow_smem_slice(int optin)
 {
-    cudaError_t e = cudaFuncSetAttribute(mbglu::glu_slice_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mbglu::glu_slice_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mbglu::glu_slice_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    cudaError_t e = cudaSuccess;
+#define MBGLU_ALLOW_SLICE(TS, TN)                                                                                 \
+    if (e == cudaSuccess) {                                                                                       \
+        cudaFuncAttributes a{};                                                                                   \
+        e = cudaFuncGetAttributes(&a, mbglu::glu_slice_kernel<TS, TN>);                                          \
+        if (e == cudaSuccess)                                                                                     \
+            e = cudaFuncSetAttribute(mbglu::glu_slice_kernel<TS, TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+                                     optin - static_cast<int>(a.sharedSizeBytes));                               \
+    }
+    MBGLU_ALLOW_SLICE(1, false) MBGLU_ALLOW_SLICE(2, false) MBGLU_ALLOW_SLICE(3, false)
+    MBGLU_ALLOW_SLICE(1, true) MBGLU_ALLOW_SLICE(2, true) MBGLU_ALLOW_SLICE(3, true)
+#undef MBGLU_ALLOW_SLICE
     return e;
 }
 
@@ -781,13 +788,19 @@ bool encode_sw128_map(mbglu::TensorMap *out, const void *base, int64_t ld, int r
 
 struct SlicePlan {
     int spw = 1, warps = 1, stages = 0, grid = 1;
-    uint32_t off_ring = 0, smem = 0;
+    uint32_t off_s = 0, off_ring = 0, smem = 0;
 };
 
-bool plan_slice(const DeviceInfo &d, int M, int N, int K, SlicePlan &sp)
+// norm: the add_rmsnorm_glu variant, whose h_s[M][K + 8] shares the slots'
+// region and whose norm_w and statistic partials follow it at off_s; from
+// mma_min_m rows (K2560 N9728 single kernel: M = 4 21.7 against 22.2 us,
+// M = 8 23.5 against 24.0; at M = 1 the streaming kernel's 19.6 against 20.6)
+bool plan_slice(const DeviceInfo &d, int M, int N, int K, SlicePlan &sp, bool norm = false)
 {
     const Tuning &t = tuning();
-    if (!t.slice || M < t.slice_min_m || M > 8 || K < mbglu::kSliceSeg || K % 8 != 0 || N < 1) return false;
+    if (!t.slice || M < (norm ? t.mma_min_m : t.slice_min_m) || M > 8 || K < mbglu::kSliceSeg || K % 8 != 0 ||
+        N < 1)
+        return false;
     const int nseg = (K + mbglu::kSliceSeg - 1) / mbglu::kSliceSeg;
     const int spw_max = M < t.mma_min_m ? 1 : 3;
     for (int spw = 1; spw <= spw_max; ++spw) {
@@ -797,8 +810,17 @@ bool plan_slice(const DeviceInfo &d, int M, int N, int K, SlicePlan &sp)
         SlicePlan c;
         c.spw = spw;
         c.warps = W;
-        c.off_ring = (1024u + mbglu::kSliceSlots * static_cast<uint32_t>(W) * mbglu::kSliceSlotBytes + 1023u) & ~1023u;
-        const int64_t room = static_cast<int64_t>(d.smem_optin) - 1024 - c.off_ring;   // 1024: base alignment
+        uint32_t region = mbglu::kSliceSlots * static_cast<uint32_t>(W) * mbglu::kSliceSlotBytes;
+        c.off_s = (1024u + region + 127u) & ~127u;
+        uint32_t end = c.off_s;
+        if (norm) {
+            region = std::max(region, static_cast<uint32_t>(M) * static_cast<uint32_t>(K + 8) * 2u);
+            c.off_s = (1024u + region + 127u) & ~127u;
+            end = c.off_s + ((static_cast<uint32_t>(K) * 2u + 127u) & ~127u) + 2u * 32u * (W + 1) * 4u;
+        }
+        c.off_ring = (end + 1023u) & ~1023u;
+        // 1024: the base's alignment; 256: the kernel's static shared memory (inv_s)
+        const int64_t room = static_cast<int64_t>(d.smem_optin) - 1024 - 256 - c.off_ring;
         if (room <= 0) continue;
         c.stages = static_cast<int>(std::min<int64_t>({6, room / (static_cast<int64_t>(W) * mbglu::kSliceStage),
                                                        64 / W}));
@@ -811,6 +833,7 @@ bool plan_slice(const DeviceInfo &d, int M, int N, int K, SlicePlan &sp)
     return false;
 }
 
+template <bool NORM>
 mbglu_status launch_slice(const SlicePlan &sp, const GluParams &p, const mbglu::SliceMaps &maps,
                           cudaStream_t stream, bool pdl)
 {
@@ -826,9 +849,9 @@ mbglu_status launch_slice(const SlicePlan &sp, const GluParams &p, const mbglu::
     cfg.numAttrs = pdl ? 1 : 0;
     cudaError_t e = cudaErrorInvalidValue;
     switch (sp.spw) {
-        case 1: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<1>, p, maps); break;
-        case 2: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<2>, p, maps); break;
-        default: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<3>, p, maps); break;
+        case 1: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<1, NORM>, p, maps); break;
+        case 2: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<2, NORM>, p, maps); break;
+        default: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<3, NORM>, p, maps); break;
     }
     return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
 }
@@ -889,7 +912,7 @@ mbglu_status gemv_block(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate
         p.stages = sp.stages;
         p.off_ring = sp.off_ring;
         p.vec_in = h_vec;
-        st = launch_slice(sp, p, smaps, stream, pdl);
+        st = launch_slice<false>(sp, p, smaps, stream, pdl);
         if (st == MBGLU_OK) t_last_variant = kSlice;
         return st;
     }
@@ -1638,6 +1661,20 @@ mbglu_status norm_block(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_b
         p.x = x;
         p.residual = residual;
         p.ws = ws;
+        SlicePlan sp;
+        mbglu::SliceMaps smaps;
+        if (plan_slice(*d, M, N, K, sp, true) && encode_sw128_map(&smaps.gate, gate_w, ld_gate, N, K, 8) &&
+            encode_sw128_map(&smaps.up, up_w, ld_up, N, K, 8)) {   // the epilogue warp writes the residual slice
+            p.stages = sp.stages;
+            p.off_s = sp.off_s;
+            p.off_ring = sp.off_ring;
+            st = launch_slice<true>(sp, p, smaps, stream, pdl);
+            if (st == MBGLU_OK) {
+                t_last_variant = kSlice;
+                ++t_last_single;
+            }
+            return st;
+        }
         if (plan_mma(*d, M, N, K, pl, sbytes)) {   // + the helper warp: up to kMaxStreamWarps + 1 warps
             p.KS = pl.KS;
             p.nseg = pl.nseg;
@@ -1708,6 +1745,17 @@ mbglu_status norm_block(const mbglu_bf16 *x, mbglu_bf16 *residual, const mbglu_b
 
     // 2) the GEMV with the norm prologue, as a programmatic dependent launch
     Plan pl;
+    SlicePlan sp;
+    mbglu::SliceMaps smaps;
+    if (bulk_ok && plan_slice(*d, M, N, K, sp, true) && encode_sw128_map(&smaps.gate, gate_w, ld_gate, N, K, 8) &&
+        encode_sw128_map(&smaps.up, up_w, ld_up, N, K, 8)) {
+        p.stages = sp.stages;
+        p.off_s = sp.off_s;
+        p.off_ring = sp.off_ring;
+        st = launch_slice<true>(sp, p, smaps, stream, pdl);
+        if (st == MBGLU_OK) t_last_variant = kSlice;
+        return st;
+    }
     if (bulk_ok && plan_mma(*d, M, N, K, pl, nwbytes)) {
         p.KS = pl.KS;
         p.nseg = pl.nseg;

@@ -124,6 +124,13 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const TensorMap *map, int
         : "memory");
 }
 
+// Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads, a
+// multiple of 32: whole warps of the block.
+__device__ __forceinline__ void bar_sync_named(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Orders this thread's earlier generic-proxy shared-memory accesses before
 // later asynchronous-proxy accesses (a bulk copy refilling a consumed stage).
 __device__ __forceinline__ void fence_proxy_async_smem()

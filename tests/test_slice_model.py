@@ -42,7 +42,7 @@ def plan(M, N, K, sms=SMS, spw_only=0, mma_min_m=3):
         if W > max_warps(spw) or (W - 1) * spw >= nseg:
             continue
         off_ring = (1024 + SLOTS * W * SLOT_BYTES + 1023) & ~1023
-        room = SMEM_OPTIN - 1024 - off_ring
+        room = SMEM_OPTIN - 1024 - 256 - off_ring
         if room <= 0:
             continue
         S = min(6, room // (W * STAGE), 64 // W)
