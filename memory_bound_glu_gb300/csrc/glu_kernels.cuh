@@ -1620,20 +1620,51 @@ __device__ __forceinline__ float silu_rcp_f32(float x)
     return (x >= 0.0f ? x : x * t) * __frcp_rn(1.0f + t);
 }
 
-__device__ __forceinline__ uint16_t silu_mul_epilogue(float g, float u, int mode)
+// SiLU by table.  g is a bf16 value, so SiLU(g) -- and in HF mode its bf16
+// rounding -- is a function of g's 16 bits.  Each CTA tabulates it, from the
+// same silu_rcp_f32, for the gates |g| in [2^-8, 2^7) (15 binades x 128
+// mantissas x 2 signs, 15 KB of fp32; a N(0, 1) gate lies there 99.7% of the
+// time) before its dependency wait; other gates take the direct path.  Then
+// FUSED: out = bf16(SiLU(g) u), one rounding; HF: out = bf16(bf16(SiLU(g)) u)
+// (the bf16 product is exact in fp32).  The results are bit for bit those of
+// evaluating SiLU at every output.
+constexpr int kSiluLutExp0 = 127 - 8;   // biased exponent of the table's first binade
+constexpr int kSiluLutBinades = 15;
+constexpr int kSiluLutSize = 2 * kSiluLutBinades * 128;
+
+__device__ __forceinline__ void silu_lut_build(float *lut, int mode)
 {
-    if (mode == 0) return f32_to_bf16(silu_rcp_f32(g) * u);
-    return f32_to_bf16(round_to_bf16(silu_rcp_f32(g)) * u);   // sb * ub is exact in fp32
+    for (int i = threadIdx.x; i < kSiluLutSize; i += blockDim.x) {
+        const int sign = i / (kSiluLutBinades * 128), rem = i - sign * (kSiluLutBinades * 128);
+        const uint32_t bits = (static_cast<uint32_t>(sign) << 15) |
+                              (static_cast<uint32_t>(kSiluLutExp0 + (rem >> 7)) << 7) | static_cast<uint32_t>(rem & 127);
+        const float sl = silu_rcp_f32(bf16_to_f32(static_cast<uint16_t>(bits)));
+        lut[i] = mode == 0 ? sl : round_to_bf16(sl);
+    }
 }
 
-__device__ __forceinline__ uint4 silu_mul_chunk(uint4 gv, uint4 uv, int mode)
+// out = epilogue(g, u) for one pair, g and u as bf16 bits
+__device__ __forceinline__ float silu_mul_lut_one(const float *lut, uint32_t gbits, uint32_t ubits, int mode)
+{
+    const int e = static_cast<int>((gbits >> 7) & 0xffu) - kSiluLutExp0;
+    float sl;
+    if (static_cast<unsigned>(e) < static_cast<unsigned>(kSiluLutBinades)) {
+        sl = lut[((gbits >> 15) * kSiluLutBinades + static_cast<uint32_t>(e)) * 128u + (gbits & 127u)];
+    } else {
+        sl = silu_rcp_f32(bf16_to_f32(static_cast<uint16_t>(gbits)));
+        if (mode != 0) sl = round_to_bf16(sl);
+    }
+    return sl * bf16_to_f32(static_cast<uint16_t>(ubits));
+}
+
+__device__ __forceinline__ uint4 silu_mul_chunk(const float *lut, uint4 gv, uint4 uv, int mode)
 {
     const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        o[j] = static_cast<uint32_t>(silu_mul_epilogue(bf16_lo(gw[j]), bf16_lo(uw[j]), mode)) |
-               (static_cast<uint32_t>(silu_mul_epilogue(bf16_hi(gw[j]), bf16_hi(uw[j]), mode)) << 16);
+        o[j] = pack_bf16x2(silu_mul_lut_one(lut, gw[j] & 0xffffu, uw[j] & 0xffffu, mode),
+                           silu_mul_lut_one(lut, gw[j] >> 16, uw[j] >> 16, mode));
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
@@ -1644,6 +1675,9 @@ __device__ __forceinline__ uint4 silu_mul_chunk(uint4 gv, uint4 uv, int mode)
 __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *x, int64_t ldx, uint16_t *out, int64_t ldo,
                                                        int M, int N, int mode, int vec)
 {
+    __shared__ float lut[kSiluLutSize];
+    silu_lut_build(lut, mode);   // no global input: before the dependency wait
+    __syncthreads();
     grid_dependency_wait();
     grid_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -1671,8 +1705,8 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *x, int64_
             const uint4 u0 = __ldcs(reinterpret_cast<const uint4 *>(r0 + N));
             const uint4 g1 = __ldcs(reinterpret_cast<const uint4 *>(r1));
             const uint4 u1 = __ldcs(reinterpret_cast<const uint4 *>(r1 + N));
-            __stcs(reinterpret_cast<uint4 *>(out + m0 * ldo + c0 * 8), silu_mul_chunk(g0, u0, mode));
-            __stcs(reinterpret_cast<uint4 *>(out + m1 * ldo + c1 * 8), silu_mul_chunk(g1, u1, mode));
+            __stcs(reinterpret_cast<uint4 *>(out + m0 * ldo + c0 * 8), silu_mul_chunk(lut, g0, u0, mode));
+            __stcs(reinterpret_cast<uint4 *>(out + m1 * ldo + c1 * 8), silu_mul_chunk(lut, g1, u1, mode));
             m0 = m1;
             c0 = c1;
             step(m0, c0);
@@ -1681,13 +1715,13 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *x, int64_
             const uint16_t *r0 = x + m0 * ldx + c0 * 8;
             const uint4 g0 = __ldcs(reinterpret_cast<const uint4 *>(r0));
             const uint4 u0 = __ldcs(reinterpret_cast<const uint4 *>(r0 + N));
-            __stcs(reinterpret_cast<uint4 *>(out + m0 * ldo + c0 * 8), silu_mul_chunk(g0, u0, mode));
+            __stcs(reinterpret_cast<uint4 *>(out + m0 * ldo + c0 * 8), silu_mul_chunk(lut, g0, u0, mode));
         }
     } else {
         const int64_t total = static_cast<int64_t>(M) * N;
         for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
             const int64_t m = i / N, n = i - m * N;
-            out[m * ldo + n] = silu_mul_epilogue(bf16_to_f32(x[m * ldx + n]), bf16_to_f32(x[m * ldx + N + n]), mode);
+            out[m * ldo + n] = f32_to_bf16(silu_mul_lut_one(lut, x[m * ldx + n], x[m * ldx + N + n], mode));
         }
     }
 }
