@@ -7,6 +7,7 @@ an exception is raised.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 
@@ -94,6 +95,16 @@ def lib():
     return _lib
 
 
+def _on(dev):
+    """The device context for a call on `dev`: none when it is already the
+    current device (the common case; entering torch.cuda.device costs a few
+    microseconds per call), else torch.cuda.device(dev)."""
+    idx = dev.index
+    if idx is None or idx == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(dev)
+
+
 def _stream_handle(device, stream):
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
@@ -137,7 +148,7 @@ def glu_gemv(h, gate_w, up_w, out=None, mode="fused", stream=None):
     _check(out2, "out", 2)
     if tuple(out2.shape) != (M, N) or out2.device != dev:
         raise ValueError(f"out must be [{M},{N}] on {dev}")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib().glu_gemv(h2.data_ptr(), h2.stride(0), gate_w.data_ptr(), gate_w.stride(0),
                             up_w.data_ptr(), up_w.stride(0), out2.data_ptr(), out2.stride(0),
                             M, N, K, _MODES[mode], _stream_handle(dev, stream))
@@ -202,7 +213,7 @@ def glu_backward(h, gate_w, up_w, dout, grad_h=None, grad_gate=None, grad_up=Non
     def ptr(t):
         return (t.data_ptr(), t.stride(0)) if t is not None else (None, 0)
 
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib().glu_backward(h.data_ptr(), h.stride(0), gate_w.data_ptr(), gate_w.stride(0), up_w.data_ptr(),
                                 up_w.stride(0), dout.data_ptr(), dout.stride(0), *ptr(grad_h), *ptr(grad_gate),
                                 *ptr(grad_up), M, N, K, wsp, wsb, _stream_handle(dev, stream))
@@ -270,7 +281,7 @@ def add_rmsnorm_glu(x, residual, norm_w, eps, gate_w, up_w, out=None, mode="hf",
         raise ValueError(f"out must be a [{M},{N}] tensor")
     if workspace is not None and not (workspace.is_cuda and workspace.device == dev and workspace.is_contiguous()):
         raise ValueError("workspace must be a contiguous CUDA tensor on the operands' device")
-    with torch.cuda.device(dev):
+    with _on(dev):
         if not (gate_w.is_contiguous() and up_w.is_contiguous() and out.is_contiguous()):
             wsp = workspace.data_ptr() if workspace is not None else None
             wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
@@ -312,7 +323,7 @@ def silu_mul(x, out=None, mode="fused", stream=None):
     _check(out2, "out", 2)
     if tuple(out2.shape) != (M, N) or out2.device != dev:
         raise ValueError(f"out must be [{M},{N}] on {dev}")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib().silu_mul(x2.data_ptr(), x2.stride(0), out2.data_ptr(), out2.stride(0), M, N, _MODES[mode],
                             _stream_handle(dev, stream))
     if st != 0:
@@ -344,7 +355,7 @@ def gdn_gates(a, b, A_log, dt_bias, g=None, beta=None, stream=None):
     _check(beta, "beta", 2)
     if tuple(beta.shape) != (T, H):
         raise ValueError(f"beta must be [{T},{H}]")
-    with torch.cuda.device(dev):
+    with _on(dev):
         st = lib().gdn_gates(a.data_ptr(), a.stride(0), b.data_ptr(), b.stride(0), A_log.data_ptr(),
                              dt_bias.data_ptr(), g.data_ptr(), g.stride(0), beta.data_ptr(), beta.stride(0), T, H,
                              _stream_handle(dev, stream))

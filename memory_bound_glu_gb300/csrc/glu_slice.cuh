@@ -21,16 +21,19 @@
 // so each ldmatrix of 8 rows meets no bank conflict.  No h in shared memory,
 // so nearly all of it is ring: ~190 KB of weights in flight per SM.
 //
-// Arithmetic, for M <= 8: A (16 x 16) = h rows 0..7 (rows M..7 read as zero,
-// rows 8..15 are zero registers a1 and a3), B (16 x 8) = 8 weight rows, D = g (or u) for 8
-// batch rows x 8 features (d2, d3 stay zero).  Per segment one MMA chain per
+// Arithmetic: A (16 x 16) = h's rows 0..15 at the k-step (rows >= M read as
+// zero; at MB = 8, for M <= 8, rows 8..15 are the zero registers a1 and a3),
+// B (16 x 8) = 8 weight rows, D = g (or u) for the batch rows x 8 features.  Per segment one MMA chain per
 // matrix over its 16 k-steps, started from zero (the tensor core's adds are
 // not specified to round to nearest; a chain stays 16 MMAs long); the chains
 // are added to the warp's fp32 partial in segment order (round to nearest).
-// The warps' partials of a group go through a ring of kSliceSlots slots to
-// the epilogue warp (warp W), which adds them in warp order (round to
-// nearest) and stores.  Every sum runs in a fixed order: results are bitwise
-// deterministic and do not depend on the timing of the warps.
+// The warps' partials of a group go through a ring of slots (4 at MB = 8, 2
+// at MB = 16) to the epilogue warp (warp W), which adds them in warp order
+// (round to nearest) and stores.  Every sum runs in a fixed order: results
+// are bitwise deterministic and do not depend on the timing of the warps.
+//
+// MB = 16 (batch 9..16) holds h's rows 8..15 too (64 registers per lane at
+// one segment per warp, so up to 10 warps: K up to 2560).
 //
 // NORM (add_rmsnorm_glu, [9057/Changes] zero-centred RMSNorm): the block
 // first forms h in shared memory with the norm prologue of the other kernels
@@ -43,10 +46,10 @@
 //
 // Shared memory (dynamic, from a 1024-byte aligned base):
 //   [0, 512)        mbarriers [warp][stage] (W S <= 64)
-//   [512, 576)      slot barriers: full[kSliceSlots] (count 32 W), empty[kSliceSlots] (count 32)
+//   [512, 576)      slot barriers: full[slots] (count 32 W), empty[slots] (count 32)
 //   [784, 792)      NORM: the prologue copies' mbarrier (kProBarOffset)
-//   [1024, ...)     slots [kSliceSlots][W][4][32] fp32: lane l's g(m, n), g(m, n+1),
-//                   u(m, n), u(m, n+1), m = l / 4, n = 2 (l % 4); NORM: first h_s[M][K + 8]
+//   [1024, ...)     slots [slots][W][NP][32] fp32: lane l's g(m, n), g(m, n+1)[, g(m+8, n),
+//                   g(m+8, n+1)], then u likewise, m = l / 4, n = 2 (l % 4); NORM: first h_s[M][K + 8]
 //   [off_s, ...)    NORM: norm_w [K] bf16, then the statistic's partials (2 floats per thread)
 //   [off_ring, ...) ring [W][S][matrix][4][8][64] bf16
 #pragma once
@@ -59,21 +62,33 @@ constexpr int kSliceBoxes = 4;                                  // 64-column box
 constexpr int kSliceSeg = 64 * kSliceBoxes;                     // 256 columns
 constexpr uint32_t kSliceBox = 8u * 128u;                       // one 64 x 8 box, bytes
 constexpr uint32_t kSliceStage = 2u * kSliceBoxes * kSliceBox;  // both matrices, 8 KB
-constexpr int kSliceSlots = 4;                                  // group slots between warps and the epilogue warp
 // the most compute warps (plus the epilogue warp) at SPW segments per warp:
 // what the registers a thread needs (h's 32 SPW fragments and the rest)
 // leave on each of the SM's four register files
-__host__ __device__ constexpr int slice_max_warps(int spw) { return spw <= 1 ? 12 : spw == 2 ? 8 : 6; }
-constexpr uint32_t kSliceSlotBytes = 4u * 32u * 4u;             // one warp's partials of one group
+__host__ __device__ constexpr int slice_max_warps(int spw, int mb = 8)
+{
+    return mb > 8 ? 10 : spw <= 1 ? 12 : spw == 2 ? 8 : 6;
+}
+// group slots between the compute warps and the epilogue warp (MB = 16
+// carries twice the partial sums per slot)
+__host__ __device__ constexpr int slice_slots(int mb) { return mb > 8 ? 2 : 4; }
+
+// one warp's partials of one group: 4 (MB = 8) or 8 (MB = 16) floats per lane
+__host__ __device__ constexpr uint32_t slice_slot_bytes(int mb) { return (mb > 8 ? 8u : 4u) * 32u * 4u; }
 
 struct SliceMaps {
     TensorMap gate, up;   // [N][K] bf16, box 64 x 8, 128-byte swizzle
 };
 
-template <int SPW, bool NORM>
-__global__ void __launch_bounds__(32 * (slice_max_warps(SPW) + 1), 1)
+template <int SPW, bool NORM, int MB>
+__global__ void __launch_bounds__(32 * (slice_max_warps(SPW, MB) + 1), 1)
     glu_slice_kernel(const GluParams p, const __grid_constant__ SliceMaps maps)
 {
+    static_assert(MB == 8 || MB == 16, "batch tile of 8 or 16 rows");
+    static_assert(!(NORM && MB > 8), "the norm variant takes batch 1..8");
+    constexpr int NP = MB > 8 ? 8 : 4;         // partial sums per lane and group
+    constexpr int NA = MB > 8 ? 4 : 2;         // A registers per k-step
+    constexpr int NSLOT = slice_slots(MB);
     extern __shared__ __align__(128) unsigned char sl_raw[];
     __shared__ float inv_s[2 * 8];   // NORM: (inv_hi, inv_lo) per row
     unsigned char *sm = sl_raw + ((1024u - (smem_addr(sl_raw) & 1023u)) & 1023u);
@@ -82,7 +97,7 @@ __global__ void __launch_bounds__(32 * (slice_max_warps(SPW) + 1), 1)
     const int S = p.stages;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm);      // [W][S]
     uint64_t *full = bars + 64;
-    uint64_t *empty = full + kSliceSlots;
+    uint64_t *empty = full + NSLOT;
     float *slots = reinterpret_cast<float *>(sm + 1024);
     const int r0 = static_cast<int>((static_cast<int64_t>(p.N) * blockIdx.x) / gridDim.x);
     const int r1 = static_cast<int>((static_cast<int64_t>(p.N) * (blockIdx.x + 1)) / gridDim.x);
@@ -100,7 +115,7 @@ __global__ void __launch_bounds__(32 * (slice_max_warps(SPW) + 1), 1)
     uint16_t *nw_s = reinterpret_cast<uint16_t *>(sm + p.off_s);
     const int HS = p.K + 8;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kSliceSlots; ++s) {
+        for (int s = 0; s < NSLOT; ++s) {
             mbar_init(&full[s], 32u * static_cast<uint32_t>(W));
             mbar_init(&empty[s], 32u);
         }
@@ -174,112 +189,143 @@ __global__ void __launch_bounds__(32 * (slice_max_warps(SPW) + 1), 1)
         norm_rows_in_place(p, rm, ss, h_s, HS, nw_s, norm_partials(sm, p), inv_s, p.M);   // ends with a barrier
     }
 
-    if (warp == W) {   // the epilogue warp: each group's partials, added in warp order
+    // the epilogue warp: each group's partials, added in warp order
+    auto epilogue = [&]() {
         const int m = lane >> 2, n = 2 * (lane & 3);
         for (int g = 0; g < ngroups; ++g) {
-            const int sl = g % kSliceSlots;
-            if (!mbar_wait_bounded(&full[sl], static_cast<uint32_t>((g / kSliceSlots) & 1), kWaitLimitNs)) {
+            const int sl = g % NSLOT;
+            if (!mbar_wait_bounded(&full[sl], static_cast<uint32_t>((g / NSLOT) & 1), kWaitLimitNs)) {
                 if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
                 return;
             }
-            const float *src = slots + static_cast<int64_t>(sl) * W * (kSliceSlotBytes / 4);
-            float acc[4];
+            const float *src = slots + static_cast<int64_t>(sl) * W * NP * 32;
+            float acc[NP];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] = src[e * 32 + lane];
+            for (int e = 0; e < NP; ++e) acc[e] = src[e * 32 + lane];
             for (int w = 1; w < W; ++w)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[e] = __fadd_rn(acc[e], src[(w * 4 + e) * 32 + lane]);
+                for (int e = 0; e < NP; ++e) acc[e] = __fadd_rn(acc[e], src[(w * NP + e) * 32 + lane]);
             mbar_arrive(&empty[sl]);   // every lane, after its reads
             const int row = r0 + 8 * g + n;
-            if (m < p.M) {
-                if (row < r1) glu_store(p, m, row, acc[0], acc[2]);
-                if (row + 1 < r1) glu_store(p, m, row + 1, acc[1], acc[3]);
+            // acc: g at (m, n), (m, n + 1)[, (m + 8, n), (m + 8, n + 1)], then u likewise
+#pragma unroll
+            for (int hh = 0; hh < MB / 8; ++hh) {
+                const int mm = m + 8 * hh;
+                if (mm < p.M) {
+                    if (row < r1) glu_store(p, mm, row, acc[2 * hh], acc[NP / 2 + 2 * hh]);
+                    if (row + 1 < r1) glu_store(p, mm, row + 1, acc[2 * hh + 1], acc[NP / 2 + 2 * hh + 1]);
+                }
             }
         }
         if constexpr (NORM) {
             if (p.fused) fused_residual_helper(p);   // this CTA's slice of residual = bf16(x + residual)
         }
-        return;
-    }
+    };
 
-    // h's A fragments: ha[2 j + e] = (h[g][k], h[g][k + 1]), k = x0 + 16 j + 8 e + 2 c
-    // (zero past K and for batch rows g >= M)
-    const int g4 = lane >> 2, c4 = lane & 3;
-    uint32_t ha[2 * 16 * SPW];
+    // a compute warp: its K-slice of every group of the share
+    auto compute = [&]() {
+        // h's A fragments: ha[NA j + ...] = (h[row][k], h[row][k + 1]) at k = x0 + 16 j + 8 e + 2 c for
+        // row = g (and g + 8 at MB = 16), in the order a0 (g, e 0), [a1 (g + 8, e 0),] a2 (g, e 1),
+        // [a3 (g + 8, e 1)]; zero past K and for batch rows >= M
+        const int g4 = lane >> 2, c4 = lane & 3;
+        uint32_t ha[NA * 16 * SPW];
 #pragma unroll
-    for (int j = 0; j < 16 * SPW; ++j)
+        for (int j = 0; j < 16 * SPW; ++j)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int k = x0 + 16 * j + 8 * e + 2 * c4;
-            uint32_t v = 0;
-            if (g4 < p.M && k < p.K) {
-                if constexpr (NORM) {
-                    v = *reinterpret_cast<const uint32_t *>(h_s + g4 * HS + k);
-                } else {
-                    const uint16_t *src = p.h + static_cast<int64_t>(g4) * p.ldh + k;
-                    v = p.vec_in ? *reinterpret_cast<const uint32_t *>(src)
-                                 : static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 16);
+            for (int e = 0; e < 2; ++e)
+#pragma unroll
+                for (int rr = 0; rr < MB / 8; ++rr) {
+                    const int k = x0 + 16 * j + 8 * e + 2 * c4, row = g4 + 8 * rr;
+                    uint32_t v = 0;
+                    if (row < p.M && k < p.K) {
+                        if constexpr (NORM) {
+                            v = *reinterpret_cast<const uint32_t *>(h_s + row * HS + k);
+                        } else {
+                            const uint16_t *src = p.h + static_cast<int64_t>(row) * p.ldh + k;
+                            v = p.vec_in ? *reinterpret_cast<const uint32_t *>(src)
+                                         : static_cast<uint32_t>(src[0]) | (static_cast<uint32_t>(src[1]) << 16);
+                        }
+                    }
+                    ha[NA * j + (MB / 8) * e + rr] = v;
                 }
-            }
-            ha[2 * j + e] = v;
-        }
 
-    if constexpr (NORM) bar_sync_named(1, 32 * W);   // every compute warp holds h: the slots may reuse h_s
-    const int mi = lane >> 3, ri = lane & 7;
-    int u = 0;
-    for (int g = 0; g < ngroups; ++g) {
-        float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // g(m, n), g(m, n+1), u(m, n), u(m, n+1)
+        if constexpr (NORM) bar_sync_named(1, 32 * W);   // every compute warp holds h: the slots may reuse h_s
+        const int mi = lane >> 3, ri = lane & 7;
+        int u = 0;
+        for (int g = 0; g < ngroups; ++g) {
+            float part[NP];
 #pragma unroll
-        for (int s = 0; s < SPW; ++s) {
-            if (s >= nseg) break;
-            const int st = u % S;
-            if (!mbar_wait_bounded(&bars[warp * S + st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs)) {
+            for (int e = 0; e < NP; ++e) part[e] = 0.0f;
+#pragma unroll
+            for (int s = 0; s < SPW; ++s) {
+                if (s >= nseg) break;
+                const int st = u % S;
+                if (!mbar_wait_bounded(&bars[warp * S + st], static_cast<uint32_t>((u / S) & 1), kWaitLimitNs)) {
+                    if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
+                    drain(u);
+                    return;
+                }
+                const uint32_t sb = smem_addr(ring + st * kSliceStage);
+                float dg[4], du[4];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    // matrices: gate k 0-7, gate k 8-15, up k 0-7, up k 8-15 of this k-step
+                    const int ch = 2 * j + (mi & 1);
+                    uint32_t b[4];
+                    ldsm_x4(b, sb + static_cast<uint32_t>((mi >> 1) * kSliceBoxes * kSliceBox + (ch >> 3) * kSliceBox +
+                                                          ri * 128 + (((ch & 7) ^ ri) << 4)));
+                    const int q = 16 * s + j;
+                    uint32_t a[4];
+                    if constexpr (MB > 8) {
+                        a[0] = ha[4 * q];
+                        a[1] = ha[4 * q + 1];
+                        a[2] = ha[4 * q + 2];
+                        a[3] = ha[4 * q + 3];
+                    } else {
+                        a[0] = ha[2 * q];
+                        a[1] = 0u;
+                        a[2] = ha[2 * q + 1];
+                        a[3] = 0u;
+                    }
+                    if (j == 0) {
+                        mma16_bf16_z(dg, a, b[0], b[1]);
+                        mma16_bf16_z(du, a, b[2], b[3]);
+                    } else {
+                        mma16_bf16(dg, a, b[0], b[1]);
+                        mma16_bf16(du, a, b[2], b[3]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < NP / 2; ++e) {
+                    part[e] = __fadd_rn(part[e], dg[e]);
+                    part[NP / 2 + e] = __fadd_rn(part[NP / 2 + e], du[e]);
+                }
+                __syncwarp();
+                if (lane == 0 && u + S < nunits) {
+                    fence_proxy_async_smem();
+                    fill(u + S);   // the unit S ahead, into the stage just read
+                }
+                ++u;
+            }
+            // the group's partials to the epilogue warp
+            const int sl = g % NSLOT;
+            if (g >= NSLOT &&
+                !mbar_wait_bounded(&empty[sl], static_cast<uint32_t>((g / NSLOT - 1) & 1), kWaitLimitNs)) {
                 if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
                 drain(u);
                 return;
             }
-            const uint32_t sb = smem_addr(ring + st * kSliceStage);
-            float dg[4], du[4];
+            float *dst = slots + (static_cast<int64_t>(sl) * W + warp) * NP * 32;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                // matrices: gate k 0-7, gate k 8-15, up k 0-7, up k 8-15 of this k-step
-                const int ch = 2 * j + (mi & 1);
-                uint32_t b[4];
-                ldsm_x4(b, sb + static_cast<uint32_t>((mi >> 1) * kSliceBoxes * kSliceBox + (ch >> 3) * kSliceBox +
-                                                      ri * 128 + (((ch & 7) ^ ri) << 4)));
-                const uint32_t a[4] = {ha[2 * (16 * s + j)], 0u, ha[2 * (16 * s + j) + 1], 0u};
-                if (j == 0) {
-                    mma16_bf16_z(dg, a, b[0], b[1]);
-                    mma16_bf16_z(du, a, b[2], b[3]);
-                } else {
-                    mma16_bf16(dg, a, b[0], b[1]);
-                    mma16_bf16(du, a, b[2], b[3]);
-                }
-            }
-            part[0] = __fadd_rn(part[0], dg[0]);
-            part[1] = __fadd_rn(part[1], dg[1]);
-            part[2] = __fadd_rn(part[2], du[0]);
-            part[3] = __fadd_rn(part[3], du[1]);
-            __syncwarp();
-            if (lane == 0 && u + S < nunits) {
-                fence_proxy_async_smem();
-                fill(u + S);   // the unit S ahead, into the stage just read
-            }
-            ++u;
+            for (int e = 0; e < NP; ++e) dst[e * 32 + lane] = part[e];
+            mbar_arrive(&full[sl]);   // every lane: releases its own stores
         }
-        // the group's partials to the epilogue warp
-        const int sl = g % kSliceSlots;
-        if (g >= kSliceSlots &&
-            !mbar_wait_bounded(&empty[sl], static_cast<uint32_t>((g / kSliceSlots - 1) & 1), kWaitLimitNs)) {
-            if (lane == 0) atomicExch(&g_device_error, kErrTimeout);
-            drain(u);
-            return;
-        }
-        float *dst = slots + (static_cast<int64_t>(sl) * W + warp) * (kSliceSlotBytes / 4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) dst[e * 32 + lane] = part[e];
-        mbar_arrive(&full[sl]);   // every lane: releases its own stores
-    }
+    };
+
+    if (warp == W)
+        epilogue();
+    else
+        compute();
 }
 
 }  // namespace mbglu

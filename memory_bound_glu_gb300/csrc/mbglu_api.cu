@@ -93,6 +93,7 @@ struct Tuning {
     int bwd_warps = 0;        // backward on the tensor cores: warps per CTA (0: automatic)
     int slice = 1;            // batches of slice_min_m..8 on the K-slice kernel where it applies (0: never)
     int slice_min_m = 1;      // smallest batch that takes the K-slice kernel
+    int slice16 = 1;          // batches of 9..16 on the K-slice kernel where it applies (0: never)
     int slice_spw = 0;        // K-slice kernel: 256-column segments per warp (0: automatic, 1..3)
 };
 
@@ -130,6 +131,7 @@ const Tuning &tuning()
         x.bwd_warps = std::min(mbglu::bwd_mma_warps(kBwdNB), std::max(0, env_int("MBGLU_BWD_WARPS", 0)));
         x.slice = env_int("MBGLU_SLICE", 1) != 0;
         x.slice_min_m = std::min(9, std::max(1, env_int("MBGLU_SLICE_MIN_M", 1)));
+        x.slice16 = env_int("MBGLU_SLICE16", 1) != 0;
         x.slice_spw = std::min(3, std::max(0, env_int("MBGLU_SLICE_SPW", 0)));
         return x;
     }();
@@ -233,16 +235,18 @@ cudaError_t allow_smem_bwd_rows(int optin)
 cudaError_t allow_smem_slice(int optin)
 {
     cudaError_t e = cudaSuccess;
-#define MBGLU_ALLOW_SLICE(TS, TN)                                                                                 \
+#define MBGLU_ALLOW_SLICE(TS, TN, TMB)                                                                            \
     if (e == cudaSuccess) {                                                                                       \
         cudaFuncAttributes a{};                                                                                   \
-        e = cudaFuncGetAttributes(&a, mbglu::glu_slice_kernel<TS, TN>);                                          \
+        e = cudaFuncGetAttributes(&a, mbglu::glu_slice_kernel<TS, TN, TMB>);                                     \
         if (e == cudaSuccess)                                                                                     \
-            e = cudaFuncSetAttribute(mbglu::glu_slice_kernel<TS, TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
+            e = cudaFuncSetAttribute(mbglu::glu_slice_kernel<TS, TN, TMB>,                                        \
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,                                 \
                                      optin - static_cast<int>(a.sharedSizeBytes));                               \
     }
-    MBGLU_ALLOW_SLICE(1, false) MBGLU_ALLOW_SLICE(2, false) MBGLU_ALLOW_SLICE(3, false)
-    MBGLU_ALLOW_SLICE(1, true) MBGLU_ALLOW_SLICE(2, true) MBGLU_ALLOW_SLICE(3, true)
+    MBGLU_ALLOW_SLICE(1, false, 8) MBGLU_ALLOW_SLICE(2, false, 8) MBGLU_ALLOW_SLICE(3, false, 8)
+    MBGLU_ALLOW_SLICE(1, true, 8) MBGLU_ALLOW_SLICE(2, true, 8) MBGLU_ALLOW_SLICE(3, true, 8)
+    MBGLU_ALLOW_SLICE(1, false, 16)
 #undef MBGLU_ALLOW_SLICE
     return e;
 }
@@ -553,22 +557,57 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 // Descriptor of an [N][K] bf16 weight (row stride ld elements) read in boxes
 // of box_k x 8 rows; elements past K or N read as zero.  False if the driver
 // rejects it (the kernel then copies row by row).
-bool encode_box_map(mbglu::TensorMap *out, const void *base, int64_t ld, int N, int K, int box_k, int box_rows)
+// Tiled 2-D descriptor of a bf16 [rows][K] matrix with row stride ld, box
+// box_k x box_rows.  The last 64 descriptors this thread encoded are kept
+// (direct-mapped on their arguments): a descriptor holds only the address,
+// the shape and the strides, so a kept one is exactly what encoding again
+// would give, whatever the memory holds now.
+bool encode_2d(mbglu::TensorMap *out, const void *base, int64_t ld, int rows, int K, int box_k, int box_rows,
+               CUtensorMapSwizzle swizzle)
 {
     static_assert(sizeof(CUtensorMap) == sizeof(mbglu::TensorMap), "tensor map size");
+    struct Entry {
+        const void *base = nullptr;
+        int64_t ld = 0;
+        int rows = 0, K = 0, box_k = 0, box_rows = 0, swizzle = -1;
+        mbglu::TensorMap map;
+    };
+    thread_local Entry cache[64];
+    const uint64_t hsh = (reinterpret_cast<uintptr_t>(base) >> 8) ^ (static_cast<uint64_t>(ld) * 0x9e3779b1u) ^
+                         (static_cast<uint64_t>(rows) << 7) ^ (static_cast<uint64_t>(K) << 17) ^
+                         (static_cast<uint64_t>(box_rows) << 3) ^ static_cast<uint64_t>(swizzle);
+    Entry &e = cache[(hsh ^ (hsh >> 6) ^ (hsh >> 12)) & 63u];
+    if (e.base == base && e.ld == ld && e.rows == rows && e.K == K && e.box_k == box_k && e.box_rows == box_rows &&
+        e.swizzle == static_cast<int>(swizzle)) {
+        *out = e.map;
+        return true;
+    }
     const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
     if (!fn || box_k > 256 || box_rows < 1 || box_rows > 256) return false;
     CUtensorMap m;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N)};
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_k), static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t elem_strides[2] = {1u, 1u};
     if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     std::memcpy(out, &m, sizeof m);
+    e.base = base;
+    e.ld = ld;
+    e.rows = rows;
+    e.K = K;
+    e.box_k = box_k;
+    e.box_rows = box_rows;
+    e.swizzle = static_cast<int>(swizzle);
+    e.map = *out;
     return true;
+}
+
+bool encode_box_map(mbglu::TensorMap *out, const void *base, int64_t ld, int N, int K, int box_k, int box_rows)
+{
+    return encode_2d(out, base, ld, N, K, box_k, box_rows, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 bool encode_weight_map(mbglu::TensorMap *out, const void *base, int64_t ld, int N, int K, int box_k)
@@ -787,21 +826,58 @@ struct BwdEpilogue {
 bool encode_sw128_map(mbglu::TensorMap *out, const void *base, int64_t ld, int rows, int K, int box_rows);
 
 struct SlicePlan {
-    int spw = 1, warps = 1, stages = 0, grid = 1;
+    int spw = 1, warps = 1, stages = 0, grid = 1, mb = 8;
     uint32_t off_s = 0, off_ring = 0, smem = 0;
 };
+
+// Shared-memory layout and ring depth of one candidate; false if fewer than
+// two stages fit.
+bool slice_layout(const DeviceInfo &d, int M, int K, bool norm, SlicePlan &c)
+{
+    const int W = c.warps;
+    uint32_t region = static_cast<uint32_t>(mbglu::slice_slots(c.mb)) * static_cast<uint32_t>(W) *
+                      mbglu::slice_slot_bytes(c.mb);
+    if (norm) region = std::max(region, static_cast<uint32_t>(M) * static_cast<uint32_t>(K + 8) * 2u);
+    c.off_s = (1024u + region + 127u) & ~127u;
+    uint32_t end = c.off_s;
+    if (norm) end = c.off_s + ((static_cast<uint32_t>(K) * 2u + 127u) & ~127u) + 2u * 32u * (W + 1) * 4u;
+    c.off_ring = (end + 1023u) & ~1023u;
+    // 1024: the base's alignment; 256: the kernel's static shared memory (inv_s)
+    const int64_t room = static_cast<int64_t>(d.smem_optin) - 1024 - 256 - c.off_ring;
+    if (room <= 0) return false;
+    c.stages = static_cast<int>(
+        std::min<int64_t>({6, room / (static_cast<int64_t>(W) * mbglu::kSliceStage), 64 / W}));
+    if (c.stages < 2) return false;
+    c.smem = c.off_ring + static_cast<uint32_t>(W * c.stages) * mbglu::kSliceStage + 1024u;
+    return true;
+}
 
 // norm: the add_rmsnorm_glu variant, whose h_s[M][K + 8] shares the slots'
 // region and whose norm_w and statistic partials follow it at off_s; from
 // mma_min_m rows (K2560 N9728 single kernel: M = 4 21.7 against 22.2 us,
-// M = 8 23.5 against 24.0; at M = 1 the streaming kernel's 19.6 against 20.6)
+// M = 8 23.5 against 24.0; at M = 1 the streaming kernel's 19.6 against 20.6).
+// Batch 9..16 (MB = 16, not with the norm): one segment per warp, up to 10
+// warps (K2560 N9728 M = 16: 18.5 against 19.9 us).  A cluster pair that
+// split K for larger K measured slower than the kernel with h in shared
+// memory (K4096 N14336 M = 16: 51.6 against 49.7 us), so K past 2560 stays
+// there.
 bool plan_slice(const DeviceInfo &d, int M, int N, int K, SlicePlan &sp, bool norm = false)
 {
     const Tuning &t = tuning();
-    if (!t.slice || M < (norm ? t.mma_min_m : t.slice_min_m) || M > 8 || K < mbglu::kSliceSeg || K % 8 != 0 ||
-        N < 1)
+    if (!t.slice || M < (norm ? t.mma_min_m : t.slice_min_m) || M > mbglu::kMaxM || K < mbglu::kSliceSeg ||
+        K % 8 != 0 || N < 1)
         return false;
     const int nseg = (K + mbglu::kSliceSeg - 1) / mbglu::kSliceSeg;
+    if (M > 8) {
+        if (norm || !t.slice16) return false;
+        SlicePlan c;
+        c.mb = 16;
+        c.warps = nseg;
+        if (c.warps > mbglu::slice_max_warps(1, 16) || !slice_layout(d, M, K, false, c)) return false;
+        c.grid = std::max(1, std::min(d.sm_count, (N + 7) / 8));
+        sp = c;
+        return true;
+    }
     const int spw_max = M < t.mma_min_m ? 1 : 3;
     for (int spw = 1; spw <= spw_max; ++spw) {
         if (t.slice_spw && spw != t.slice_spw) continue;
@@ -810,22 +886,7 @@ bool plan_slice(const DeviceInfo &d, int M, int N, int K, SlicePlan &sp, bool no
         SlicePlan c;
         c.spw = spw;
         c.warps = W;
-        uint32_t region = mbglu::kSliceSlots * static_cast<uint32_t>(W) * mbglu::kSliceSlotBytes;
-        c.off_s = (1024u + region + 127u) & ~127u;
-        uint32_t end = c.off_s;
-        if (norm) {
-            region = std::max(region, static_cast<uint32_t>(M) * static_cast<uint32_t>(K + 8) * 2u);
-            c.off_s = (1024u + region + 127u) & ~127u;
-            end = c.off_s + ((static_cast<uint32_t>(K) * 2u + 127u) & ~127u) + 2u * 32u * (W + 1) * 4u;
-        }
-        c.off_ring = (end + 1023u) & ~1023u;
-        // 1024: the base's alignment; 256: the kernel's static shared memory (inv_s)
-        const int64_t room = static_cast<int64_t>(d.smem_optin) - 1024 - 256 - c.off_ring;
-        if (room <= 0) continue;
-        c.stages = static_cast<int>(std::min<int64_t>({6, room / (static_cast<int64_t>(W) * mbglu::kSliceStage),
-                                                       64 / W}));
-        if (c.stages < 2) continue;
-        c.smem = c.off_ring + static_cast<uint32_t>(W * c.stages) * mbglu::kSliceStage + 1024u;
+        if (!slice_layout(d, M, K, norm, c)) continue;
         c.grid = std::max(1, std::min(d.sm_count, (N + 7) / 8));
         sp = c;
         return true;
@@ -848,10 +909,14 @@ mbglu_status launch_slice(const SlicePlan &sp, const GluParams &p, const mbglu::
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     cudaError_t e = cudaErrorInvalidValue;
-    switch (sp.spw) {
-        case 1: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<1, NORM>, p, maps); break;
-        case 2: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<2, NORM>, p, maps); break;
-        default: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<3, NORM>, p, maps); break;
+    if (sp.mb > 8) {
+        if constexpr (!NORM) e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<1, false, 16>, p, maps);
+    } else {
+        switch (sp.spw) {
+            case 1: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<1, NORM, 8>, p, maps); break;
+            case 2: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<2, NORM, 8>, p, maps); break;
+            default: e = cudaLaunchKernelEx(&cfg, mbglu::glu_slice_kernel<3, NORM, 8>, p, maps); break;
+        }
     }
     return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
 }
@@ -959,19 +1024,7 @@ mbglu_status gemv_block(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *gate
 // tensor arrive as zeros.
 bool encode_sw128_map(mbglu::TensorMap *out, const void *base, int64_t ld, int rows, int K, int box_rows)
 {
-    const PFN_cuTensorMapEncodeTiled_v12000 fn = tensor_map_encoder();
-    if (!fn || box_rows > 256) return false;
-    CUtensorMap m;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mbglu::kTcBox), static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t elem_strides[2] = {1u, 1u};
-    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, elem_strides,
-           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return false;
-    std::memcpy(out, &m, sizeof m);
-    return true;
+    return encode_2d(out, base, ld, rows, K, mbglu::kTcBox, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 struct TcPlan {

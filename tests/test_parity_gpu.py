@@ -54,7 +54,15 @@ def run_gpu(h, g, u, mode, **kw):
 
 
 FAST = (1, 4, 10)   # the streaming kernels: CUDA-core FMA, tensor core, tensor core with h in registers
-SLICE = 10          # mbglu_last_variant(): the K-slice tensor-core kernel (batch 1..8; at 1-2 only K <= 3072)
+SLICE = 10          # mbglu_last_variant(): the K-slice tensor-core kernel
+
+
+def tc_variant(M, K):
+    """The kernel a tensor-core batch (M >= 3, aligned operands, K % 16 == 0)
+    takes: the K-slice kernel where its plan fits (K up to 4608 at M <= 8, up to
+    2560 at M = 9..16), else the kernel with h in shared memory."""
+    fits = 256 <= K and (K <= 4608 if M <= 8 else K <= 2560)
+    return SLICE if fits else 4
 
 
 def check(h, g, u, mode, what="", variant=None):
@@ -121,18 +129,21 @@ def test_tensor_core_k_phases(M, N, K, mode):
     h = gi.normal_bf16((M, K), 1.0, M, "kp-h")
     g = gi.normal_bf16((N, K), K ** -0.5, M, "kp-g")
     u = gi.normal_bf16((N, K), K ** -0.5, M, "kp-u")
-    check(h, g, u, mode, f"M={M} N={N} K={K}", variant=4)
+    check(h, g, u, mode, f"M={M} N={N} K={K}", variant=tc_variant(M, K))
 
 
-def test_k_phases_deterministic_and_row_permutation_bitwise():
+@pytest.mark.parametrize("K", [4096, 6144])
+def test_k_phases_deterministic_and_row_permutation_bitwise(K):
     """With K-phases, as with one phase, a row's bits do not depend on where
-    the row falls (how the CTA's units are cut between warps and phases)."""
-    M, N, K = 16, 1500, 4096
+    the row falls (how the CTA's units are cut between warps and phases): batch
+    16 on the kernel with h in shared memory, in two K-phases at K = 4096 and
+    at K = 6144."""
+    M, N = 16, 1500
     h = gi.normal_bf16((M, K), 1.0, 7, "kpp-h").to(DEV)
     g = gi.normal_bf16((N, K), K ** -0.5, 7, "kpp-g").to(DEV)
     u = gi.normal_bf16((N, K), K ** -0.5, 7, "kpp-u").to(DEV)
     a = mb.glu_gemv(h, g, u, mode="hf")
-    assert mb.last_variant() == 4
+    assert mb.last_variant() == tc_variant(M, K)
     b = mb.glu_gemv(h, g, u, mode="hf")
     perm = torch.randperm(N, generator=torch.Generator().manual_seed(1)).to(DEV)
     c = mb.glu_gemv(h, g[perm], u[perm], mode="hf")
@@ -191,13 +202,13 @@ def test_batch_one_paths(K, ld_pad, h_off, expect):
 @pytest.mark.parametrize("mode", ["fused", "hf"])
 def test_tensor_core_kernel(M, mode):
     """Batch >= 3 on the tensor cores: ragged N (partial last 8-row group),
-    several K-segments; batches of 3..8 on the K-slice kernel (h in
-    registers), 9..16 on the kernel with h in shared memory."""
+    several K-segments, on the K-slice kernel (h in registers; 16-row tiles at
+    batch 9..16)."""
     N, K = 1339, 2560
     h = gi.normal_bf16((M, K), 1.0, M, "tc-h")
     g = gi.normal_bf16((N, K), K ** -0.5, M, "tc-g")
     u = gi.normal_bf16((N, K), K ** -0.5, M, "tc-u")
-    check(h, g, u, mode, f"tc M={M}", variant=SLICE if M <= 8 else 4)
+    check(h, g, u, mode, f"tc M={M}", variant=tc_variant(M, 2560))
 
 
 @pytest.mark.parametrize("K,ld_pad,h_off", [(1024, 8, 8), (4096, 0, 0), (2576, 16, 1), (1040, 0, 0)])

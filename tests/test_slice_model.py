@@ -27,39 +27,64 @@ SLOTS = 4
 SLOT_BYTES = 4 * 32 * 4
 
 
-def max_warps(spw):
-    return 12 if spw <= 1 else 8 if spw == 2 else 6
+def max_warps(spw, mb=8):
+    return 10 if mb > 8 else 12 if spw <= 1 else 8 if spw == 2 else 6
+
+
+def slots(mb):
+    return 2 if mb > 8 else 4
+
+
+def slot_bytes(mb):
+    return (8 if mb > 8 else 4) * 32 * 4
+
+
+def layout(c):
+    """Shared-memory layout and ring depth of one candidate (slice_layout)."""
+    W = c["warps"]
+    region = slots(c["mb"]) * W * slot_bytes(c["mb"])
+    c["off_s"] = (1024 + region + 127) & ~127
+    c["off_ring"] = (c["off_s"] + 1023) & ~1023
+    room = SMEM_OPTIN - 1024 - 256 - c["off_ring"]
+    if room <= 0:
+        return False
+    c["stages"] = min(6, room // (W * STAGE), 64 // W)
+    c["smem"] = c["off_ring"] + W * c["stages"] * STAGE + 1024
+    return c["stages"] >= 2
 
 
 def plan(M, N, K, sms=SMS, spw_only=0, mma_min_m=3):
-    if M < 1 or M > 8 or K < SEG or K % 8 or N < 1:
+    if M < 1 or M > 16 or K < SEG or K % 8 or N < 1:
         return None
     nseg = -(-K // SEG)
+    if M > 8:
+        c = dict(spw=1, mb=16, warps=nseg)
+        if nseg > max_warps(1, 16) or not layout(c):
+            return None
+        c["grid"] = max(1, min(sms, (N + 7) // 8))
+        return c
     for spw in ((1,) if M < mma_min_m else (1, 2, 3)):
         if spw_only and spw != spw_only:
             continue
         W = -(-nseg // spw)
         if W > max_warps(spw) or (W - 1) * spw >= nseg:
             continue
-        off_ring = (1024 + SLOTS * W * SLOT_BYTES + 1023) & ~1023
-        room = SMEM_OPTIN - 1024 - 256 - off_ring
-        if room <= 0:
+        c = dict(spw=spw, mb=8, warps=W)
+        if not layout(c):
             continue
-        S = min(6, room // (W * STAGE), 64 // W)
-        if S < 2:
-            continue
-        return dict(spw=spw, warps=W, stages=S, off_ring=off_ring, smem=off_ring + W * S * STAGE + 1024,
-                    grid=max(1, min(sms, (N + 7) // 8)))
+        c["grid"] = max(1, min(sms, (N + 7) // 8))
+        return c
     return None
 
 
 def replay(M, N, K, sms=SMS, spw_only=0, seed=0):
     p = plan(M, N, K, sms, spw_only)
     assert p is not None
-    W, S, spw = p["warps"], p["stages"], p["spw"]
-    assert p["smem"] <= SMEM_OPTIN and W * S <= 64 and W <= max_warps(spw)
-    assert p["off_ring"] >= 1024 + SLOTS * W * SLOT_BYTES and p["off_ring"] % 1024 == 0
-    assert 64 + 2 * SLOTS <= 128   # barrier words: [W][S], then full / empty
+    W, S, spw, mb = p["warps"], p["stages"], p["spw"], p["mb"]
+    NP, NA = (8, 4) if mb > 8 else (4, 2)
+    assert p["smem"] <= SMEM_OPTIN and W * S <= 64 and W <= max_warps(spw, mb)
+    assert p["off_s"] >= 1024 + slots(mb) * W * slot_bytes(mb) and p["off_ring"] % 1024 == 0
+    assert 64 + 2 * slots(mb) <= 72   # barrier words [512, 576)
     rng = np.random.default_rng(seed)
     q = lambda *shape: bf16_rn(rng.standard_normal(shape).astype(np.float32)).astype(np.float64)
     h, Wg, Wu = q(M, K), q(N, K), q(N, K)
@@ -68,70 +93,77 @@ def replay(M, N, K, sms=SMS, spw_only=0, seed=0):
     out_u = np.full((M, N), np.nan)
     n_out = np.zeros((M, N), int)
     avail = p["smem"] - 1024
-    for b in range(G):
-        r0, r1 = N * b // G, N * (b + 1) // G
+    for share in range(G):
+        r0, r1 = N * share // G, N * (share + 1) // G
         ngroups = -(-(r1 - r0) // 8)
-        mem = Smem(avail)
-        slots = np.full((SLOTS, W, 4, 32), np.nan)
+        sums = np.zeros((ngroups, NP, 32))
+        if True:
+            mem = Smem(avail)
+            for g in range(ngroups):
+                slot = np.full((W, NP, 32), np.nan)
+                for warp in range(W):
+                    x0 = warp * spw * SEG
+                    nseg = max(0, min(spw, -(-(K - x0) // SEG)))
+                    assert nseg >= 1, "every compute warp has a segment"
+                    ring = p["off_ring"] + warp * S * STAGE
+                    assert ring + S * STAGE <= avail
+                    # h fragments of this warp's columns: rows g and g + 8
+                    ha = np.zeros((16 * spw, 4, 32, 2))
+                    for j in range(16 * spw):
+                        for e in range(2):
+                            k = x0 + 16 * j + 8 * e + 2 * C4
+                            for rr in range(mb // 8):
+                                row = G4 + 8 * rr
+                                for t in range(2):
+                                    ok = (row < M) & (k + t < K)
+                                    ha[j, 2 * e + rr, :, t] = np.where(
+                                        ok, h[np.minimum(row, M - 1), np.minimum(k + t, K - 1)], 0.0)
+                    part = np.zeros((32, NP))
+                    for s in range(nseg):
+                        u = g * nseg + s
+                        st = u % S
+                        y, x = r0 + 8 * g, x0 + s * SEG
+                        assert 0 <= y < N
+                        for mat, Wm in ((0, Wg), (1, Wu)):
+                            for i in range(4):
+                                dst = ring + st * STAGE + (4 * mat + i) * BOX
+                                assert dst % 1024 == 0 and (x + 64 * i) % 8 == 0
+                                for r in range(8):
+                                    for c in range(64):
+                                        v = Wm[y + r, x + 64 * i + c] if (y + r < N and x + 64 * i + c < K) else 0.0
+                                        mem.v[(dst + r * 128 + (((c >> 3) ^ r) << 4) + (c & 7) * 2) // 2] = v
+                        sb = ring + st * STAGE
+                        dg = np.zeros((32, 4))
+                        du = np.zeros((32, 4))
+                        for j in range(16):
+                            ch = 2 * j + (MI & 1)
+                            addr = sb + (MI >> 1) * 4 * BOX + (ch >> 3) * BOX + RI * 128 + (((ch & 7) ^ RI) << 4)
+                            bfr = mem.ldsm(addr, (sb, sb + STAGE))
+                            a = ha[16 * s + j].transpose(1, 0, 2)   # [lane][a0..a3][2]
+                            mma(dg, a, bfr[:, 0], bfr[:, 1])
+                            mma(du, a, bfr[:, 2], bfr[:, 3])
+                        if mb == 8:
+                            assert np.all(dg[:, 2:] == 0) and np.all(du[:, 2:] == 0)
+                        part += np.concatenate([dg[:, :NP // 2], du[:, :NP // 2]], axis=1)
+                    slot[warp] = part.T
+                # the epilogue warp: the warps' partials in order
+                acc = slot[0].copy()
+                for w in range(1, W):
+                    acc += slot[w]
+                sums[g] = acc
         for g in range(ngroups):
-            sl = g % SLOTS
-            for warp in range(W):
-                x0 = warp * spw * SEG
-                nseg = max(0, min(spw, -(-(K - x0) // SEG)))
-                assert nseg >= 1, "every compute warp has a segment"
-                ring = p["off_ring"] + warp * S * STAGE
-                assert ring + S * STAGE <= avail
-                # h fragments of this warp's columns
-                ha = np.zeros((16 * spw, 2, 32, 2))
-                for j in range(16 * spw):
-                    for e in range(2):
-                        k = x0 + 16 * j + 8 * e + 2 * C4
-                        for t in range(2):
-                            ok = (G4 < M) & (k + t < K)
-                            ha[j, e, :, t] = np.where(ok, h[np.minimum(G4, M - 1), np.minimum(k + t, K - 1)], 0.0)
-                part = np.zeros((32, 4))
-                for s in range(nseg):
-                    u = g * nseg + s
-                    st = u % S
-                    # the copy of unit u into stage st (issued S units earlier; replayed here)
-                    y, x = r0 + 8 * g, x0 + s * SEG
-                    assert 0 <= y < N
-                    for mat, Wm in ((0, Wg), (1, Wu)):
-                        for i in range(4):
-                            dst = ring + st * STAGE + (4 * mat + i) * BOX
-                            assert dst % 1024 == 0 and (x + 64 * i) % 8 == 0
-                            for r in range(8):
-                                for c in range(64):
-                                    v = Wm[y + r, x + 64 * i + c] if (y + r < N and x + 64 * i + c < K) else 0.0
-                                    mem.v[(dst + r * 128 + (((c >> 3) ^ r) << 4) + (c & 7) * 2) // 2] = v
-                    sb = ring + st * STAGE
-                    dg = np.zeros((32, 4))
-                    du = np.zeros((32, 4))
-                    for j in range(16):
-                        ch = 2 * j + (MI & 1)
-                        addr = sb + (MI >> 1) * 4 * BOX + (ch >> 3) * BOX + RI * 128 + (((ch & 7) ^ RI) << 4)
-                        bfr = mem.ldsm(addr, (sb, sb + STAGE))
-                        a = np.zeros((32, 4, 2))
-                        a[:, 0] = ha[16 * s + j, 0]
-                        a[:, 2] = ha[16 * s + j, 1]
-                        mma(dg, a, bfr[:, 0], bfr[:, 1])
-                        mma(du, a, bfr[:, 2], bfr[:, 3])
-                    assert np.all(dg[:, 2:] == 0) and np.all(du[:, 2:] == 0)
-                    part += np.stack([dg[:, 0], dg[:, 1], du[:, 0], du[:, 1]], axis=1)
-                slots[sl, warp] = part.T
-            # the epilogue warp: the warps' partials in order, stores of rows < r1
-            acc = slots[sl, 0].copy()
-            for w in range(1, W):
-                acc += slots[sl, w]
+            acc = sums[g]
             for ln in range(32):
                 m, n = ln >> 2, r0 + 8 * g + 2 * (ln & 3)
-                if m >= M:
-                    continue
-                for dn, gi_, ui_ in ((0, 0, 2), (1, 1, 3)):
-                    if n + dn < r1:
-                        out_g[m, n + dn] = acc[gi_, ln]
-                        out_u[m, n + dn] = acc[ui_, ln]
-                        n_out[m, n + dn] += 1
+                for hh in range(mb // 8):
+                    mm = m + 8 * hh
+                    if mm >= M:
+                        continue
+                    for dn in range(2):
+                        if n + dn < r1:
+                            out_g[mm, n + dn] = acc[2 * hh + dn, ln]
+                            out_u[mm, n + dn] = acc[NP // 2 + 2 * hh + dn, ln]
+                            n_out[mm, n + dn] += 1
     assert np.all(n_out == 1), "each output stored exactly once"
     np.testing.assert_allclose(out_g, h @ Wg.T, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(out_u, h @ Wu.T, rtol=1e-12, atol=1e-12)
@@ -145,6 +177,8 @@ def replay(M, N, K, sms=SMS, spw_only=0, seed=0):
     (5, 64, 1288, 2, 2),       # two segments per warp, the last warp with one
     (8, 20, 2560, 3, 3),       # three per warp, ragged; shares under one group
     (4, 9, 4096, 1, 0),        # 16 segments, one CTA, one partial group
+    (16, 40, 2560, 4, 0),      # batch 16, 10 warps, one CTA per share
+    (11, 30, 1288, 3, 0),      # batch 11 (rows 11..15 zero), a segment past K
 ])
 def test_replay_matches_plain_dot_products(M, N, K, sms, spw):
     replay(M, N, K, sms, spw)
@@ -158,7 +192,10 @@ def test_plan_on_the_workloads():
             p = plan(M, 9728, K)
             assert p is not None and p["stages"] >= 2 and p["smem"] <= SMEM_OPTIN and p["grid"] == SMS
             assert p["warps"] * p["spw"] * SEG >= K
-    assert plan(8, 9728, 8192) is None and plan(9, 9728, 2560) is None and plan(8, 9728, 200) is None
+    assert plan(8, 9728, 8192) is None and plan(17, 9728, 2560) is None and plan(8, 9728, 200) is None
+    # batch 9-16: one segment per warp, up to 10 warps
+    assert plan(16, 9728, 2560)["warps"] == 10 and plan(16, 9728, 2560)["stages"] >= 2
+    assert plan(16, 14336, 4096) is None and plan(9, 9728, 2568) is None
     # batch 1-2: one segment per warp only (K <= 12 * 256)
     assert plan(1, 9728, 2560)["spw"] == 1 and plan(2, 9728, 3072)["spw"] == 1
     assert plan(1, 9728, 4096) is None and plan(2, 11008, 3080) is None
