@@ -389,9 +389,10 @@ int mbglu_last_variant(void);
  * gradients' second step: 0 none (the call launched no such step), 1 the
  * separate grad_h and weight-gradient kernels, 2 one pass on the CUDA cores
  * (M <= 2, or the tensor-core pass off), 3 one pass on the tensor cores
- * (mma.sync; dG and dU enter as three bf16 terms, exact for normal fp32
- * values).  Both one-pass kernels need M <= 8, K % 8 == 0, 16-byte aligned
- * weights and weight gradients with row strides of whole 16-byte units. */
+ * (M = 3..16; mma.sync; dG and dU enter as three bf16 terms, exact for
+ * normal fp32 values).  The one-pass kernels need K % 8 == 0, 16-byte
+ * aligned weights and weight gradients with row strides of whole 16-byte
+ * units, and M <= 8 (CUDA cores) or M <= 16 (tensor cores). */
 int mbglu_last_backward_path(void);
 
 /* How many row blocks of the calling thread's last add_rmsnorm_glu* call ran

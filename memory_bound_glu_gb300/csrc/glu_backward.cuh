@@ -48,7 +48,7 @@ struct BwdParams {
     int rows_cta;           // glu_bwd_rows_kernel, glu_bwd_hw_kernel: largest row share of a CTA
     int col_groups;         // glu_bwd_hw_kernel, glu_bwd_mma_kernel: CTAs sharing a row share (each a group of column slices)
     int rows_pad;           // glu_bwd_mma_kernel: rows_cta rounded up to a multiple of 16
-    uint32_t off_mn, off_nm;   // glu_bwd_mma_kernel: staged dG, dU (two layouts)
+    uint32_t off_nm;           // glu_bwd_mma_kernel: staged dG, dU
     int vec_w;              // gate, up rows 8-byte aligned: 4-element loads
     int vec_out;            // grad_gate, grad_up rows and h 16-byte aligned, K % 8 == 0: 8-element access
     int h_smem;             // glu_bwd_w_kernel: h staged in shared memory
@@ -444,7 +444,7 @@ __global__ void __launch_bounds__(32 * bwd_hw_warps(MB), 1) glu_bwd_hw_kernel(co
 }
 
 // ---------------------------------------------------------------------------
-// Steps 2 and 3 on the tensor cores (glu_bwd_mma_kernel, M = 3..8)
+// Steps 2 and 3 on the tensor cores (glu_bwd_mma_kernel, M = 3..16)
 // ---------------------------------------------------------------------------
 // The pass of glu_bwd_hw_kernel with both contractions as bf16 MMAs
 // (mma.sync, fp32 accumulators):
@@ -455,10 +455,12 @@ __global__ void __launch_bounds__(32 * bwd_hw_warps(MB), 1) glu_bwd_hw_kernel(co
 // (each difference exact in fp32).  bf16 keeps 8 of fp32's 24 significant
 // bits, so the three terms hold x exactly (unless lo falls below bf16's
 // normal range), and a product of two bf16 values is exact in fp32: the MMAs
-// see the same products as fp32 arithmetic would.  grad_h takes one m16n8k16
-// per term; grad_W lays the terms along the MMA's reduction, [hi m0..7 | mid
-// m0..7] against [h; h] (m16n8k16) and lo m0..7 against h (m16n8k8).  The
-// batch is padded to 8 with zero rows.
+// see the same products as fp32 arithmetic would.  The batch is padded to a
+// tile of MB = 8 or 16 rows with zero rows.
+//   * grad_h takes one m16n8k16 per term and 8-row batch tile.
+//   * grad_W lays the terms along the MMA's reduction.  At MB = 8 that is
+//     [hi m0..7 | mid m0..7] against [h; h] (m16n8k16) and lo m0..7 against
+//     h (m16n8k8); at MB = 16, one m16n8k16 per term over m0..15.
 //
 // A CTA owns a row share [n0, n1) and a group of column slices.  Its rows go
 // in blocks of 16, block b = [n0 + 16 b, n0 + 16 b + 16), the LAST block
@@ -478,17 +480,21 @@ __global__ void __launch_bounds__(32 * bwd_hw_warps(MB), 1) glu_bwd_hw_kernel(co
 // each.  part[s][m][k] receives the share's grad_h sums;
 // glu_bwd_h_reduce8_kernel adds the shares in order.
 //
+// dG and dU are staged once, as [matrix][rows_pad][PITCH] bf16: row n holds
+// hi for m = 0..MB-1, then mid, then lo (PITCH = 24 at MB = 8, 48 + 8 of
+// padding at MB = 16, so that 8 rows of a matrix load fall in 8 different
+// bank groups).  grad_W reads it as its A operand (ldmatrix); grad_h reads it
+// transposed (ldmatrix.trans) as its B operand.
+//
 // Shared memory (dynamic, from a 1024-byte aligned base):
-//   [0, 512)                 mbarriers [warp][stage]
-//   [off_mn, + 96 rs)        [matrix][hi, mid, lo][8][rs] bf16, rs = rows_pad + 8: dG, dU
-//                            with the share's rows contiguous (the B operand of grad_h)
-//   [off_nm, + 96 rows_pad)  [matrix][rows_pad][24] bf16: row n holds hi m0..7, mid m0..7,
-//                            lo m0..7 (the A operand of grad_W; 48-byte rows meet no
-//                            bank conflict)
-//   [off_ring, ...)          ring [warp][stage][matrix][NB][16][64] bf16
-// at most 12 warps: the 160 registers a thread needs at NB = 2 leave room for
-// 3 warps on each of the SM's four register files
-__host__ __device__ constexpr int bwd_mma_warps(int NB) { return NB >= 4 ? 8 : 12; }
+//   [0, 512)                   mbarriers [warp][stage]
+//   [off_nm, + 4 PITCH rp)     dG, dU as above (rp = rows_pad)
+//   [off_ring, ...)            ring [warp][stage][matrix][NB][16][64] bf16
+// at most 12 warps at MB = 8 (160 registers a thread leave room for 3 warps
+// on each of the SM's four register files), 8 at MB = 16 (twice the grad_h
+// accumulators and h fragments)
+__host__ __device__ constexpr int bwd_mma_warps(int NB, int MB = 8) { return MB > 8 ? 8 : NB >= 4 ? 8 : 12; }
+__host__ __device__ constexpr int bwd_mma_pitch(int MB) { return MB > 8 ? 56 : 24; }
 constexpr uint32_t kBwdMmaBox = 16u * 128u;   // one 64-column x 16-row box, bytes
 
 // x = hi + mid + lo, each bf16 (exact for normal x down to 2^-110 or so);
@@ -507,20 +513,30 @@ __device__ __forceinline__ void split3_bf16(float x, uint16_t (&t)[3])
 }
 
 // One 16-row x 64-column piece of a weight gradient (two groups of four
-// tiles): D = [hi | mid]^T [h; h] + lo^T h, rounded to bf16 and stored.  a,
-// a8: the A fragments of the block's rows; hb[t0 .. t0 + 7]: the B fragments
-// (h[2c][k], h[2c+1][k]) at the tiles' permuted columns; dst: row g of the
-// piece's first column; nr valid rows, kleft columns left in the row.
-template <int NH>
-__device__ __forceinline__ void bwd_mma_w_tile(const uint32_t (&a)[4], const uint32_t (&a8)[2],
-                                               const uint32_t (&hb)[NH], int t0, uint16_t *dst, int64_t ld, int nr,
-                                               int kleft, int lane)
+// tiles), rounded to bf16 and stored.  MB = 8: D = [hi | mid]^T [h; h] + lo^T h
+// (a, a8); MB = 16: D = hi^T h + mid^T h + lo^T h (aw[0..2]).  hb: the B
+// fragments (h[2c][k], h[2c+1][k][, h[8+2c][k], h[8+2c+1][k]]) of the tiles'
+// permuted columns from tile t0; dst: row g of the piece's first column; nr
+// valid rows, kleft columns left in the row.
+template <int MB, int NH>
+__device__ __forceinline__ void bwd_mma_w_tile(const uint32_t (&aw)[3][4], const uint32_t (&hb)[NH][2], int t0,
+                                               uint16_t *dst, int64_t ld, int nr, int kleft, int lane)
 {
     float d[8][4];
+    if constexpr (MB > 8) {
 #pragma unroll
-    for (int t = 0; t < 8; ++t) mma16_bf16_z(d[t], a, hb[t0 + t], hb[t0 + t]);
+        for (int t = 0; t < 8; ++t) mma16_bf16_z(d[t], aw[0], hb[t0 + t][0], hb[t0 + t][1]);
 #pragma unroll
-    for (int t = 0; t < 8; ++t) mma8_bf16(d[t], a8, hb[t0 + t]);
+        for (int t = 0; t < 8; ++t) mma16_bf16(d[t], aw[1], hb[t0 + t][0], hb[t0 + t][1]);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mma16_bf16(d[t], aw[2], hb[t0 + t][0], hb[t0 + t][1]);
+    } else {
+        const uint32_t a8[2] = {aw[2][0], aw[2][1]};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mma16_bf16_z(d[t], aw[0], hb[t0 + t][0], hb[t0 + t][0]);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) mma8_bf16(d[t], a8, hb[t0 + t][0]);
+    }
     const int g = lane >> 2, c = lane & 3;
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
@@ -538,10 +554,14 @@ __device__ __forceinline__ void bwd_mma_w_tile(const uint32_t (&a)[4], const uin
     }
 }
 
-template <int NB>
-__global__ void __launch_bounds__(32 * bwd_mma_warps(NB), 1) glu_bwd_mma_kernel(const BwdParams q,
-                                                                              const __grid_constant__ BwdMaps maps)
+template <int NB, int MB>
+__global__ void __launch_bounds__(32 * bwd_mma_warps(NB, MB), 1) glu_bwd_mma_kernel(const BwdParams q,
+                                                                                  const __grid_constant__ BwdMaps maps)
 {
+    static_assert(MB == 8 || MB == 16, "batch tile of 8 or 16 rows");
+    constexpr int NT = MB / 8;                    // 8-row batch tiles (grad_h's n8 tiles)
+    constexpr int PITCH = bwd_mma_pitch(MB);      // staged row, elements
+    constexpr int NC = 3 * NT;                    // (term, batch tile) chunks of a staged row
     extern __shared__ __align__(128) unsigned char bm_raw[];
     unsigned char *sm = bm_raw + ((1024u - (smem_addr(bm_raw) & 1023u)) & 1023u);
     constexpr uint32_t kMat = NB * kBwdMmaBox;   // one matrix's part of a stage
@@ -551,8 +571,9 @@ __global__ void __launch_bounds__(32 * bwd_mma_warps(NB), 1) glu_bwd_mma_kernel(
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm) + warp * S;
     unsigned char *ring = sm + q.off_ring + static_cast<uint32_t>(warp) * S * kStage;
     const uint32_t ring_a = smem_addr(ring);
-    const uint32_t mn = smem_addr(sm + q.off_mn), nm = smem_addr(sm + q.off_nm);
-    const int rp = q.rows_pad, rs = rp + 8;
+    const uint32_t nm = smem_addr(sm + q.off_nm);
+    const int rp = q.rows_pad;
+    const uint32_t mat_bytes = static_cast<uint32_t>(rp) * PITCH * 2u;   // one matrix's staged rows
     const int G = gridDim.x / q.col_groups;
     const int share = blockIdx.x / q.col_groups, cgrp = blockIdx.x - share * q.col_groups;
     const int n0 = static_cast<int>((static_cast<int64_t>(q.N) * share) / G);
@@ -585,9 +606,8 @@ __global__ void __launch_bounds__(32 * bwd_mma_warps(NB), 1) glu_bwd_mma_kernel(
     grid_dependency_wait();                                 // dG, dU of the first step
 
     {   // dG, dU of the share as three bf16 terms, zero past the share and past M
-        uint16_t *mnp = reinterpret_cast<uint16_t *>(sm + q.off_mn);
         uint16_t *nmp = reinterpret_cast<uint16_t *>(sm + q.off_nm);
-        for (int i = threadIdx.x; i < 8 * rp; i += blockDim.x) {
+        for (int i = threadIdx.x; i < MB * rp; i += blockDim.x) {
             const int m = i / rp, r = i - m * rp;
             float x[2] = {0.0f, 0.0f};
             if (m < q.M && r < rows) {
@@ -599,35 +619,38 @@ __global__ void __launch_bounds__(32 * bwd_mma_warps(NB), 1) glu_bwd_mma_kernel(
                 uint16_t t[3];
                 split3_bf16(x[mat], t);
 #pragma unroll
-                for (int e = 0; e < 3; ++e) {
-                    mnp[((mat * 3 + e) * 8 + m) * rs + r] = t[e];
-                    nmp[(mat * rp + r) * 24 + 8 * e + m] = t[e];
-                }
+                for (int e = 0; e < 3; ++e) nmp[(mat * rp + r) * PITCH + e * MB + m] = t[e];
             }
         }
     }
-    // B fragments of grad_W: hb[t] = (h[2c][k], h[2c+1][k]) with k the weight
-    // column of MMA column g in tile t = 4 p + t'
+    // B fragments of grad_W: hb[t] = (h[2c][k], h[2c+1][k]) [and (h[8+2c][k], h[8+2c+1][k])] with k the
+    // weight column of MMA column g in tile t = 4 p + t'
     const int g4 = lane >> 2, c4 = lane & 3;
-    uint32_t hb[8 * NB];
+    uint32_t hb[8 * NB][2];
 #pragma unroll
     for (int t = 0; t < 8 * NB; ++t) {
         const int k = x0 + 32 * (t >> 2) + 8 * (g4 >> 1) + 2 * (t & 3) + (g4 & 1);
-        uint32_t lo = 0, hi = 0;
-        if (k < q.K) {
-            if (2 * c4 < q.M) lo = q.h[static_cast<int64_t>(2 * c4) * q.ldh + k];
-            if (2 * c4 + 1 < q.M) hi = q.h[static_cast<int64_t>(2 * c4 + 1) * q.ldh + k];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t lo = 0, hi = 0;
+            const int m = 2 * c4 + 8 * half;
+            if (half < NT && k < q.K) {
+                if (m < q.M) lo = q.h[static_cast<int64_t>(m) * q.ldh + k];
+                if (m + 1 < q.M) hi = q.h[static_cast<int64_t>(m + 1) * q.ldh + k];
+            }
+            hb[t][half] = lo | (hi << 16);
         }
-        hb[t] = lo | (hi << 16);
     }
     __syncthreads();   // dG, dU staged
     if (!live) return;   // a slice past K (the last column group): no rows to stream
 
-    float acc[4 * NB][4];
+    float acc[NT][4 * NB][4];
 #pragma unroll
-    for (int i = 0; i < 4 * NB; ++i)
+    for (int mt = 0; mt < NT; ++mt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[i][e] = 0.0f;
+        for (int i = 0; i < 4 * NB; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mt][i][e] = 0.0f;
 
     const int mi = lane >> 3, ri = lane & 7;
     for (int j = 0; j < nblk; ++j) {
@@ -641,19 +664,29 @@ __global__ void __launch_bounds__(32 * bwd_mma_warps(NB), 1) glu_bwd_mma_kernel(
         const int nr = min(16, rows - nb0);
         const uint32_t sg = ring_a + st * kStage, su = sg + kMat;
         {   // grad_h: the stage's weights, as W^T by transposed matrix loads.  B:
-            // dG, dU at the block's rows (hi n0-7, hi n8-15, mid n0-7, mid n8-15;
-            // then lo n0-7, lo n8-15)
-            uint32_t bg[4], bu[4], bg8[2], bu8[2];
-            const uint32_t off = static_cast<uint32_t>(((mi >> 1) * 8 + ri) * rs + nb0 + 8 * (mi & 1)) * 2u;
-            const uint32_t off8 = static_cast<uint32_t>((16 + ri) * rs + nb0 + 8 * (mi & 1)) * 2u;
-            const uint32_t up = 48u * static_cast<uint32_t>(rs);
-            ldsm_x4(bg, mn + off);
-            ldsm_x2(bg8, mn + off8);
-            ldsm_x4(bu, mn + up + off);
-            ldsm_x2(bu8, mn + up + off8);
+            // dG, dU at the block's rows, per (term, batch tile) chunk: rows n 0-7
+            // then 8-15 of the staged layout, transposed
+            uint32_t bh[2][NC][2];
+#pragma unroll
+            for (int mat = 0; mat < 2; ++mat) {
+#pragma unroll
+                for (int c0 = 0; c0 < NC; c0 += 2) {
+                    const int ch = min(c0 + (mi >> 1), NC - 1);   // the x4 past the last chunk repeats it
+                    const uint32_t addr = nm + mat * mat_bytes +
+                                          static_cast<uint32_t>((nb0 + 8 * (mi & 1) + ri) * PITCH * 2 + ch * 16);
+                    uint32_t r[4];
+                    ldsm_x4_trans(r, addr);
+                    bh[mat][c0][0] = r[0];
+                    bh[mat][c0][1] = r[1];
+                    if (c0 + 1 < NC) {
+                        bh[mat][c0 + 1][0] = r[2];
+                        bh[mat][c0 + 1][1] = r[3];
+                    }
+                }
+            }
 #pragma unroll
             for (int i = 0; i < NB; ++i) {
-                // the box's four 16-column groups, their MMAs interleaved term by term
+                // the box's four 16-column groups, their MMAs interleaved chunk by chunk
 #pragma unroll
                 for (int mat = 0; mat < 2; ++mat) {
                     uint32_t a[4][4];
@@ -663,14 +696,11 @@ __global__ void __launch_bounds__(32 * bwd_mma_warps(NB), 1) glu_bwd_mma_kernel(
                         ldsm_x4_trans(a[q4], (mat ? su : sg) +
                                                  static_cast<uint32_t>(i * kBwdMmaBox + n * 128 + ((chunk ^ ri) << 4)));
                     }
-                    const uint32_t(&b)[4] = mat ? bu : bg;
-                    const uint32_t(&b8)[2] = mat ? bu8 : bg8;
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) mma16_bf16(acc[4 * i + q4], a[q4], b[0], b[1]);
+                    for (int c = 0; c < NC; ++c)
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) mma16_bf16(acc[4 * i + q4], a[q4], b[2], b[3]);
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) mma16_bf16(acc[4 * i + q4], a[q4], b8[0], b8[1]);
+                        for (int q4 = 0; q4 < 4; ++q4)
+                            mma16_bf16(acc[c % NT][4 * i + q4], a[q4], bh[mat][c][0], bh[mat][c][1]);
                 }
             }
         }
@@ -681,41 +711,51 @@ __global__ void __launch_bounds__(32 * bwd_mma_warps(NB), 1) glu_bwd_mma_kernel(
             fence_proxy_async_smem();
             fill(j + S);
         }
-        {   // grad_W's A: rows nb0 .. nb0 + 15 of [hi | mid], then of lo
-            uint32_t ag[4], au[4], ag8[2], au8[2];
+        {   // grad_W's A: rows nb0 .. nb0 + 15, per term (MB = 16) or [hi | mid], lo (MB = 8)
+            uint32_t ag[3][4], au[3][4];
             const int n = nb0 + ri + 8 * (mi & 1);
-            const uint32_t off = static_cast<uint32_t>(n * 48 + ((mi >> 1) << 4));
-            const uint32_t off8 = static_cast<uint32_t>(n * 48 + 32);
-            const uint32_t up = 48u * static_cast<uint32_t>(rp);
-            ldsm_x4(ag, nm + off);
-            ldsm_x2(ag8, nm + off8);
-            ldsm_x4(au, nm + up + off);
-            ldsm_x2(au8, nm + up + off8);
+#pragma unroll
+            for (int mat = 0; mat < 2; ++mat) {
+                uint32_t(&aw)[3][4] = mat ? au : ag;
+                const uint32_t row = nm + mat * mat_bytes + static_cast<uint32_t>(n * PITCH * 2);
+                if constexpr (MB > 8) {
+#pragma unroll
+                    for (int e = 0; e < 3; ++e) ldsm_x4(aw[e], row + static_cast<uint32_t>((2 * e + (mi >> 1)) << 4));
+                } else {
+                    uint32_t a8[2];
+                    ldsm_x4(aw[0], row + static_cast<uint32_t>((mi >> 1) << 4));
+                    ldsm_x2(a8, row + 32u);
+                    aw[2][0] = a8[0];
+                    aw[2][1] = a8[1];
+                }
+            }
             const int64_t nrow = static_cast<int64_t>(n0) + nb0 + g4;   // row g of the block
 #pragma unroll
             for (int i = 0; i < NB; ++i) {   // grad_gate, grad_up: the box's 16 x 64 pieces
                 const int col = x0 + 64 * i;
-                bwd_mma_w_tile(ag, ag8, hb, 8 * i, q.grad_gate + nrow * q.ldgg + col, q.ldgg, nr, q.K - col, lane);
-                bwd_mma_w_tile(au, au8, hb, 8 * i, q.grad_up + nrow * q.ldgu + col, q.ldgu, nr, q.K - col, lane);
+                bwd_mma_w_tile<MB>(ag, hb, 8 * i, q.grad_gate + nrow * q.ldgg + col, q.ldgg, nr, q.K - col, lane);
+                bwd_mma_w_tile<MB>(au, hb, 8 * i, q.grad_up + nrow * q.ldgu + col, q.ldgu, nr, q.K - col, lane);
             }
         }
     }
     grid_launch_dependents();
-    // acc[gq]: D[k][m] with k = x0 + 16 gq + g (+8), m = 2c (+1)
+    // acc[mt][gq]: D[k][m] with k = x0 + 16 gq + g (+8), m = 8 mt + 2c (+1)
 #pragma unroll
-    for (int gq = 0; gq < 4 * NB; ++gq) {
-        const int k = x0 + 16 * gq + g4;
-        const int m = 2 * c4;
-        float *p0 = q.part + (static_cast<int64_t>(share) * q.M + m) * q.K;
-        if (m < q.M) {
-            if (k < q.K) p0[k] = acc[gq][0];
-            if (k + 8 < q.K) p0[k + 8] = acc[gq][2];
+    for (int mt = 0; mt < NT; ++mt)
+#pragma unroll
+        for (int gq = 0; gq < 4 * NB; ++gq) {
+            const int k = x0 + 16 * gq + g4;
+            const int m = 8 * mt + 2 * c4;
+            float *p0 = q.part + (static_cast<int64_t>(share) * q.M + m) * q.K;
+            if (m < q.M) {
+                if (k < q.K) p0[k] = acc[mt][gq][0];
+                if (k + 8 < q.K) p0[k + 8] = acc[mt][gq][2];
+            }
+            if (m + 1 < q.M) {
+                if (k < q.K) p0[q.K + k] = acc[mt][gq][1];
+                if (k + 8 < q.K) p0[q.K + k + 8] = acc[mt][gq][3];
+            }
         }
-        if (m + 1 < q.M) {
-            if (k < q.K) p0[q.K + k] = acc[gq][1];
-            if (k + 8 < q.K) p0[q.K + k + 8] = acc[gq][3];
-        }
-    }
 }
 
 // grad_h[m][k] = bf16( part[0][m][k] + part[1][m][k] + ... ), splits in order

@@ -89,7 +89,7 @@ struct Tuning {
     int tc_min_m = 17;        // smallest batch that takes the tcgen05 kernel
     int tc_split = 0;         // tcgen05 kernel: CTAs per tile (0: automatic, 1..4 where the plan allows)
     int bwd_fused = 1;        // backward: steps 2 and 3 in one pass where they apply (0: separate kernels)
-    int bwd_mma_min_m = 3;    // backward: smallest batch whose one-pass step takes the tensor cores (9: never)
+    int bwd_mma_min_m = 3;    // backward: smallest batch whose one-pass step takes the tensor cores (17: never)
     int bwd_warps = 0;        // backward on the tensor cores: warps per CTA (0: automatic)
     int slice = 1;            // batches of slice_min_m..8 on the K-slice kernel where it applies (0: never)
     int slice_min_m = 1;      // smallest batch that takes the K-slice kernel
@@ -127,7 +127,7 @@ const Tuning &tuning()
         x.tc_min_m = std::min(65, std::max(1, env_int("MBGLU_TC_MIN_M", 17)));
         x.tc_split = std::min(mbglu::kTcMaxSplit, std::max(0, env_int("MBGLU_TC_SPLIT", 0)));
         x.bwd_fused = env_int("MBGLU_BWD_FUSED", 1) != 0;
-        x.bwd_mma_min_m = std::min(9, std::max(1, env_int("MBGLU_BWD_MMA_MIN_M", 3)));
+        x.bwd_mma_min_m = std::min(17, std::max(1, env_int("MBGLU_BWD_MMA_MIN_M", 3)));
         x.bwd_warps = std::min(mbglu::bwd_mma_warps(kBwdNB), std::max(0, env_int("MBGLU_BWD_WARPS", 0)));
         x.slice = env_int("MBGLU_SLICE", 1) != 0;
         x.slice_min_m = std::min(9, std::max(1, env_int("MBGLU_SLICE_MIN_M", 1)));
@@ -227,7 +227,10 @@ cudaError_t allow_smem_bwd_rows(int optin)
     MBGLU_ALLOW_HW(1) MBGLU_ALLOW_HW(2) MBGLU_ALLOW_HW(4) MBGLU_ALLOW_HW(8)
 #undef MBGLU_ALLOW_HW
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(mbglu::glu_bwd_mma_kernel<kBwdNB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(mbglu::glu_bwd_mma_kernel<kBwdNB, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mbglu::glu_bwd_mma_kernel<kBwdNB, 16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin);
     return e;
 }
@@ -1282,21 +1285,26 @@ mbglu_status launch_bwd_hw(const BwdHwPlan &hp, const mbglu::BwdParams &q, const
 // warp counts that fit, the most warps (each warp's chain of dependent steps
 // is what bounds the pass), then the most stages.
 struct BwdMmaPlan {
-    int NB = 2, cg = 1, warps = 1, shares = 1, rows_cta = 0, rows_pad = 0, S = 0;
-    uint32_t off_mn = 0, off_nm = 0, off_ring = 0, smem = 0;
+    int NB = 2, MB = 8, cg = 1, warps = 1, shares = 1, rows_cta = 0, rows_pad = 0, S = 0;
+    uint32_t off_nm = 0, off_ring = 0, smem = 0;
 };
 
 bool plan_bwd_mma(const DeviceInfo &d, int M, int N, int K, const void *h, int64_t ldh, const void *gate_w,
                   int64_t ld_gate, const void *up_w, int64_t ld_up, const void *grad_gate, int64_t ldgg,
                   const void *grad_up, int64_t ldgu, BwdMmaPlan &mp)
 {
-    if (M > 8 || K % 8 != 0 || !aligned(gate_w, 16) || !aligned(up_w, 16) || ld_gate % 8 != 0 ||
+    if (M > 16 || K % 8 != 0 || !aligned(gate_w, 16) || !aligned(up_w, 16) || ld_gate % 8 != 0 ||
         ld_up % 8 != 0 || !aligned(grad_gate, 16) || !aligned(grad_up, 16) || ldgg % 8 != 0 || ldgu % 8 != 0)
         return false;
     const int NB = kBwdNB;
+    const int MB = M > 8 ? 16 : 8;
+    const int pitch = mbglu::bwd_mma_pitch(MB);
+    // the workspace holds max(256 min(M, 8), 48 min(M, 16)) rows of K partials
+    const int parts_cap = std::max(kBwdMaxParts * std::min(M, 8), static_cast<int>(mbglu::kBwdMaxSplits) * M) / M;
     const int slice = 64 * NB;
     const int wtot = (K + slice - 1) / slice;
-    const int wmax = tuning().bwd_warps > 0 ? tuning().bwd_warps : mbglu::bwd_mma_warps(NB);
+    const int wmax = std::min(tuning().bwd_warps > 0 ? tuning().bwd_warps : mbglu::bwd_mma_warps(NB, MB),
+                              mbglu::bwd_mma_warps(NB, MB));
     const int wmin = tuning().bwd_warps > 0 ? tuning().bwd_warps : 1;
     const int64_t stage = 2ll * NB * mbglu::kBwdMmaBox;
     bool found = false;
@@ -1304,15 +1312,16 @@ bool plan_bwd_mma(const DeviceInfo &d, int M, int N, int K, const void *h, int64
     for (int w = wmax; w >= wmin; --w) {
         BwdMmaPlan c;
         c.NB = NB;
+        c.MB = MB;
         c.cg = (wtot + w - 1) / w;
         c.warps = (wtot + c.cg - 1) / c.cg;   // the same groups, balanced
         if (c.warps != w) continue;
-        c.shares = std::max(1, std::min({(N + 15) / 16, d.sm_count / c.cg, kBwdMaxParts}));
+        c.shares = std::max(1, std::min({(N + 15) / 16, d.sm_count / c.cg, parts_cap}));
         c.rows_cta = (N + c.shares - 1) / c.shares;
         c.rows_pad = (c.rows_cta + 15) / 16 * 16;
-        c.off_mn = 512;
-        c.off_nm = c.off_mn + 96u * static_cast<uint32_t>(c.rows_pad + 8);
-        c.off_ring = (c.off_nm + 96u * static_cast<uint32_t>(c.rows_pad) + 1023u) & ~1023u;
+        c.off_nm = 512;
+        c.off_ring = (c.off_nm + 4u * static_cast<uint32_t>(pitch) * static_cast<uint32_t>(c.rows_pad) + 1023u) &
+                     ~1023u;
         const int64_t room = static_cast<int64_t>(d.smem_optin) - 1024 - c.off_ring;   // 1024: base alignment
         if (room <= 0) continue;
         c.S = static_cast<int>(std::min<int64_t>({4, room / (c.warps * stage), 64 / c.warps}));
@@ -1341,7 +1350,8 @@ mbglu_status launch_bwd_mma(const BwdMmaPlan &mp, const mbglu::BwdParams &q, con
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = g_policy.load(std::memory_order_relaxed) != MBGLU_POLICY_SERIAL ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, mbglu::glu_bwd_mma_kernel<kBwdNB>, q, maps);
+    const cudaError_t e = mp.MB > 8 ? cudaLaunchKernelEx(&cfg, mbglu::glu_bwd_mma_kernel<kBwdNB, 16>, q, maps)
+                                    : cudaLaunchKernelEx(&cfg, mbglu::glu_bwd_mma_kernel<kBwdNB, 8>, q, maps);
     return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
 }
 
@@ -1491,7 +1501,6 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
         q.rows_pad = mp.rows_pad;
         q.col_groups = mp.cg;
         q.S = mp.S;
-        q.off_mn = mp.off_mn;
         q.off_nm = mp.off_nm;
         q.off_ring = mp.off_ring;
         st = launch_bwd_mma(mp, q, mmaps, stream);

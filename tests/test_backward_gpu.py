@@ -59,7 +59,7 @@ def test_backward_every_batch_tile(M):
     got = mb.glu_backward(h.to(DEV), g.to(DEV), u.to(DEV), d.to(DEV))
     torch.cuda.synchronize()
     assert mb.last_variant() == BACKWARD
-    assert mb.last_backward_path() == (2 if M <= 2 else 3 if M <= 8 else 1)
+    assert mb.last_backward_path() == (2 if M <= 2 else 3 if M <= 16 else 1)
     _check(tuple(t.cpu() for t in got), h, g, u, d, f"M={M}")
     assert mb.read_device_error() == 0
 
@@ -70,6 +70,8 @@ def test_backward_every_batch_tile(M):
     (7, 2049, 1032),   # a box with 8 columns in it; partial top blocks
     (8, 40, 4096),     # 32 slices in several column groups; every share one partial block
     (4, 9728, 2560),   # the headline layer at batch 4
+    (16, 2049, 1032),  # batch 16: two batch tiles, three terms each
+    (11, 9728, 2560),  # batch 11 on the headline layer (rows 11..15 of the tile zero)
 ])
 def test_backward_tensor_core_pass(M, N, K):
     """The one-pass step on the tensor cores (dG, dU as three bf16 terms):

@@ -25,15 +25,22 @@ SMEM_OPTIN = 232448        # GB300: max dynamic shared memory per block (opt-in)
 BOX = 16 * 128             # one 64-column x 16-row box of bf16, bytes
 MAX_PARTS = 256
 
-def bwd_mma_warps(NB):
-    return 8 if NB >= 4 else 12
+def bwd_mma_warps(NB, MB=8):
+    return 8 if MB > 8 else 8 if NB >= 4 else 12
+
+
+def pitch(MB):
+    return 56 if MB > 8 else 24
 
 
 def plan(M, N, K, sms, NB=2, warps=0):
-    if M > 8 or K % 8:
+    if M > 16 or K % 8:
         return None
+    MB = 16 if M > 8 else 8
+    P = pitch(MB)
+    parts_cap = max(MAX_PARTS * min(M, 8), 48 * M) // M
     wtot = -(-K // (64 * NB))
-    wmax = warps if warps > 0 else bwd_mma_warps(NB)
+    wmax = min(warps if warps > 0 else bwd_mma_warps(NB, MB), bwd_mma_warps(NB, MB))
     wmin = warps if warps > 0 else 1
     stage = 2 * NB * BOX
     best, best_score = None, -1
@@ -42,12 +49,11 @@ def plan(M, N, K, sms, NB=2, warps=0):
         W = -(-wtot // cg)
         if W != w:
             continue
-        shares = max(1, min((N + 15) // 16, sms // cg, MAX_PARTS))
+        shares = max(1, min((N + 15) // 16, sms // cg, parts_cap))
         rows_cta = -(-N // shares)
         rows_pad = -(-rows_cta // 16) * 16
-        off_mn = 512
-        off_nm = off_mn + 96 * (rows_pad + 8)
-        off_ring = (off_nm + 96 * rows_pad + 1023) & ~1023
+        off_nm = 512
+        off_ring = (off_nm + 4 * P * rows_pad + 1023) & ~1023
         room = SMEM_OPTIN - 1024 - off_ring
         if room <= 0:
             continue
@@ -57,9 +63,8 @@ def plan(M, N, K, sms, NB=2, warps=0):
         score = 16 * W + S
         if score > best_score:
             best_score = score
-            best = dict(NB=NB, cg=cg, warps=W, shares=shares, rows_cta=rows_cta, rows_pad=rows_pad, S=S,
-                        off_mn=off_mn, off_nm=off_nm, off_ring=off_ring, stage=stage,
-                        smem=off_ring + W * S * stage + 1024)
+            best = dict(NB=NB, MB=MB, cg=cg, warps=W, shares=shares, rows_cta=rows_cta, rows_pad=rows_pad, S=S,
+                        off_nm=off_nm, off_ring=off_ring, stage=stage, smem=off_ring + W * S * stage + 1024)
     return best
 
 
@@ -76,12 +81,15 @@ def split3(x):
 def replay(M, N, K, sms, NB=2, warps=0, seed=0):
     p = plan(M, N, K, sms, NB, warps)
     assert p is not None
-    W, S, cg, G = p["warps"], p["S"], p["cg"], p["shares"]
-    rp, rs = p["rows_pad"], p["rows_pad"] + 8
+    W, S, cg, G, MB = p["warps"], p["S"], p["cg"], p["shares"], p["MB"]
+    NT, P = MB // 8, pitch(MB)
+    NC = 3 * NT
+    rp = p["rows_pad"]
+    mat_bytes = rp * P * 2
     stage, kmat = p["stage"], NB * BOX
-    assert p["smem"] <= SMEM_OPTIN and W * S <= 64 and W <= bwd_mma_warps(NB)
-    assert p["off_nm"] >= p["off_mn"] + 96 * rs
-    assert p["off_ring"] >= p["off_nm"] + 96 * rp and p["off_ring"] % 1024 == 0 and stage % 1024 == 0
+    assert p["smem"] <= SMEM_OPTIN and W * S <= 64 and W <= bwd_mma_warps(NB, MB)
+    assert p["off_ring"] >= p["off_nm"] + 2 * mat_bytes and p["off_ring"] % 1024 == 0 and stage % 1024 == 0
+    assert (P * 2 // 16) % 2 == 1, "a staged row is an odd number of 16-byte units (no bank conflict)"
     rng = np.random.default_rng(seed)
     q = lambda *shape: bf16_rn(rng.standard_normal(shape).astype(np.float32)).astype(np.float64)
     h, Wg, Wu = q(M, K), q(N, K), q(N, K)
@@ -98,8 +106,7 @@ def replay(M, N, K, sms, NB=2, warps=0, seed=0):
     part = np.full((G, M, K), np.nan)
     n_part = np.zeros((G, M, K), int)
     avail = p["smem"] - 1024            # what lies past the aligned base in the worst case
-    R_MN = (p["off_mn"], p["off_mn"] + 96 * rs)
-    R_NM = (p["off_nm"], p["off_nm"] + 96 * rp)
+    R_NM = (p["off_nm"], p["off_nm"] + 2 * mat_bytes)
 
     for bid in range(G * cg):
         share, cgrp = divmod(bid, cg)
@@ -108,15 +115,14 @@ def replay(M, N, K, sms, NB=2, warps=0, seed=0):
         nblk = -(-rows // 16)
         assert rows <= p["rows_cta"] <= rp
         mem = Smem(avail)
-        # dG, dU staged as three bf16 terms in both layouts, zero past the share and M
-        for m in range(8):
+        # dG, dU staged as three bf16 terms: [matrix][rp][P], row n = hi m0.., mid m0.., lo m0..
+        for m in range(MB):
             for r in range(rp):
                 ok = m < M and r < rows
                 for mat, terms in ((0, tg), (1, tu)):
                     for e in range(3):
                         v = terms[e][m, n0 + r] if ok else 0.0
-                        mem.v[p["off_mn"] // 2 + ((mat * 3 + e) * 8 + m) * rs + r] = v   # [matrix][term][8][rs]
-                        mem.v[p["off_nm"] // 2 + (mat * rp + r) * 24 + 8 * e + m] = v    # [matrix][rp][24]
+                        mem.v[p["off_nm"] // 2 + (mat * rp + r) * P + e * MB + m] = v
         for warp in range(W):
             x0 = (cgrp * W + warp) * 64 * NB
             if x0 >= K:
@@ -140,56 +146,65 @@ def replay(M, N, K, sms, NB=2, warps=0, seed=0):
                                 assert R_RING[0] <= off < R_RING[1]
                                 mem.v[off // 2] = v
 
-            # h fragments: (h[2c][k], h[2c+1][k]), k the weight column of MMA
-            # column g in tile t = 4p + t'
-            hb = np.zeros((8 * NB, 32, 2))
+            # h fragments: (h[2c + 8 half][k], h[2c + 1 + 8 half][k]), k the weight
+            # column of MMA column g in tile t = 4p + t'
+            hb = np.zeros((8 * NB, 2, 32, 2))
             for t in range(8 * NB):
                 k = x0 + 32 * (t >> 2) + 8 * (G4 >> 1) + 2 * (t & 3) + (G4 & 1)
-                for e in range(2):
-                    m = 2 * C4 + e
-                    ok = (k < K) & (m < M)
-                    hb[t, :, e] = np.where(ok, h[np.minimum(m, M - 1), np.minimum(k, K - 1)], 0.0)
+                for half in range(NT):
+                    for e in range(2):
+                        m = 2 * C4 + e + 8 * half
+                        ok = (k < K) & (m < M)
+                        hb[t, half, :, e] = np.where(ok, h[np.minimum(m, M - 1), np.minimum(k, K - 1)], 0.0)
             for j in range(min(S, nblk)):
                 fill(j)
-            acc = np.zeros((4 * NB, 32, 4))
+            acc = np.zeros((NT, 4 * NB, 32, 4))
             for j in range(nblk):
                 st = j % S
                 nb0 = 16 * (nblk - 1 - j)
                 nr = min(16, rows - nb0)
                 sg = ring + st * stage
                 su = sg + kmat
-                off = (((MI >> 1) * 8 + RI) * rs + nb0 + 8 * (MI & 1)) * 2
-                off8 = ((16 + RI) * rs + nb0 + 8 * (MI & 1)) * 2
-                bg = mem.ldsm(p["off_mn"] + off, R_MN)
-                bg8 = mem.ldsm(p["off_mn"] + off8, R_MN, x=2)
-                bu = mem.ldsm(p["off_mn"] + 48 * rs + off, R_MN)
-                bu8 = mem.ldsm(p["off_mn"] + 48 * rs + off8, R_MN, x=2)
-                n = nb0 + RI + 8 * (MI & 1)
-                off = n * 48 + ((MI >> 1) << 4)
-                off8 = n * 48 + 32
-                ag = mem.ldsm(p["off_nm"] + off, R_NM)
-                ag8 = mem.ldsm(p["off_nm"] + off8, R_NM, x=2)
-                au = mem.ldsm(p["off_nm"] + 48 * rp + off, R_NM)
-                au8 = mem.ldsm(p["off_nm"] + 48 * rp + off8, R_NM, x=2)
+                # grad_h's B: per (term, batch tile) chunk, rows 0-7 then 8-15, transposed
+                bh = np.zeros((2, NC, 2, 32, 2))
+                for mat in range(2):
+                    for c0 in range(0, NC, 2):
+                        ch = np.minimum(c0 + (MI >> 1), NC - 1)
+                        addr = p["off_nm"] + mat * mat_bytes + (nb0 + 8 * (MI & 1) + RI) * P * 2 + ch * 16
+                        r = mem.ldsm(addr, R_NM, trans=True)
+                        bh[mat, c0] = r[:, 0:2].transpose(1, 0, 2)
+                        if c0 + 1 < NC:
+                            bh[mat, c0 + 1] = r[:, 2:4].transpose(1, 0, 2)
                 for i in range(NB):
-                    for q4 in range(4):
-                        nn = RI + 8 * (MI >> 1)
-                        chunk = 2 * q4 + (MI & 1)
-                        off = i * BOX + nn * 128 + ((chunk ^ RI) << 4)
-                        a = mem.ldsm(sg + off, (sg, sg + kmat), trans=True)
-                        mma(acc[4 * i + q4], a, bg[:, 0], bg[:, 1])
-                        mma(acc[4 * i + q4], a, bg[:, 2], bg[:, 3])
-                        mma(acc[4 * i + q4], a, bg8[:, 0], bg8[:, 1])
-                        a = mem.ldsm(su + off, (su, su + kmat), trans=True)
-                        mma(acc[4 * i + q4], a, bu[:, 0], bu[:, 1])
-                        mma(acc[4 * i + q4], a, bu[:, 2], bu[:, 3])
-                        mma(acc[4 * i + q4], a, bu8[:, 0], bu8[:, 1])
+                    for mat, sb in ((0, sg), (1, su)):
+                        for q4 in range(4):
+                            nn = RI + 8 * (MI >> 1)
+                            chunk = 2 * q4 + (MI & 1)
+                            a = mem.ldsm(sb + i * BOX + nn * 128 + ((chunk ^ RI) << 4), (sb, sb + kmat), trans=True)
+                            for c in range(NC):
+                                mma(acc[c % NT, 4 * i + q4], a, bh[mat, c, 0], bh[mat, c, 1])
+                if j + S < nblk:
+                    fill(j + S)
+                # grad_W's A
+                n = nb0 + RI + 8 * (MI & 1)
+                aws = []
+                for mat in range(2):
+                    row = p["off_nm"] + mat * mat_bytes + n * P * 2
+                    if MB > 8:
+                        aws.append([mem.ldsm(row + ((2 * e + (MI >> 1)) << 4), R_NM) for e in range(3)])
+                    else:
+                        aws.append([mem.ldsm(row + ((MI >> 1) << 4), R_NM), mem.ldsm(row + 32, R_NM, x=2)])
+                for i in range(NB):
                     col = x0 + 64 * i
-                    for af, af8, grad, cnt in ((ag, ag8, grad_g, n_g), (au, au8, grad_u, n_u)):
+                    for aw, grad, cnt in ((aws[0], grad_g, n_g), (aws[1], grad_u, n_u)):
                         d = np.zeros((8, 32, 4))
                         for t in range(8):
-                            mma(d[t], af, hb[8 * i + t], hb[8 * i + t])
-                            mma(d[t], af8, hb[8 * i + t])
+                            if MB > 8:
+                                for e in range(3):
+                                    mma(d[t], aw[e], hb[8 * i + t, 0], hb[8 * i + t, 1])
+                            else:
+                                mma(d[t], aw[0], hb[8 * i + t, 0], hb[8 * i + t, 0])
+                                mma(d[t], aw[1], hb[8 * i + t, 0])
                         for pp in range(2):
                             # lane (g, c): rows g and g + 8, columns 32 pp + 8 c .. + 7
                             for ln in range(32):
@@ -204,16 +219,15 @@ def replay(M, N, K, sms, NB=2, warps=0, seed=0):
                                         assert n0 <= gr < n1 and gc + 8 <= K and gc % 8 == 0
                                         grad[gr, gc:gc + 8] = v
                                         cnt[gr, gc:gc + 8] += 1
-                if j + S < nblk:
-                    fill(j + S)
-            for gq in range(4 * NB):
-                k = x0 + 16 * gq + G4
-                for t in range(32):
-                    for e, (dm, dk) in enumerate(((0, 0), (1, 0), (0, 8), (1, 8))):
-                        m, kk = 2 * C4[t] + dm, k[t] + dk
-                        if m < M and kk < K:
-                            part[share, m, kk] = acc[gq, t, e]
-                            n_part[share, m, kk] += 1
+            for mt in range(NT):
+                for gq in range(4 * NB):
+                    k = x0 + 16 * gq + G4
+                    for t in range(32):
+                        for e, (dm, dk) in enumerate(((0, 0), (1, 0), (0, 8), (1, 8))):
+                            m, kk = 8 * mt + 2 * C4[t] + dm, k[t] + dk
+                            if m < M and kk < K:
+                                part[share, m, kk] = acc[mt, gq, t, e]
+                                n_part[share, m, kk] += 1
 
     assert np.all(n_g == 1) and np.all(n_u == 1), "each weight-gradient element stored exactly once"
     assert np.all(n_part == 1), "each grad_h partial stored exactly once"
@@ -234,6 +248,8 @@ def replay(M, N, K, sms, NB=2, warps=0, seed=0):
     (5, 37, 264, 3, 2),       # slices past K, shares of 12-13 rows
     (2, 33, 3200, 8, 2),      # several column groups per share
     (8, 300, 136, 5, 2),      # two warps, shares of 60 rows (4 blocks through 2+ stages)
+    (16, 100, 1000, 6, 2),    # batch 16: two batch tiles, three terms per tile
+    (11, 37, 264, 3, 2),      # batch 11 (rows 11..15 zero), slices past K
 ])
 def test_replay_matches_plain_sums(M, N, K, sms, NB):
     replay(M, N, K, sms, NB)
@@ -244,7 +260,7 @@ def test_plan_on_gb300_shapes():
     least two stages, one CTA per SM."""
     for K, N in ((2560, 9728), (4096, 11008), (4096, 14336), (1024, 3072), (8192, 1000), (768, 1000)):
         for NB in (2,):
-            p = plan(8, N, K, 152, NB)
+            p = plan(16 if K < 8192 else 8, N, K, 152, NB)
             assert p is not None, (K, N, NB)
             assert p["S"] >= 2 and p["shares"] * p["cg"] <= 152 and p["smem"] <= SMEM_OPTIN
             assert p["warps"] * p["cg"] * 64 * NB >= K
