@@ -505,20 +505,26 @@ __device__ __forceinline__ uint4 add_bf16x8(uint4 a, uint4 b)
 }
 
 // Single-kernel add_rmsnorm_glu: x is read straight from global memory, the
-// first kXRows chunks of each thread before the residual copy is awaited (one
-// round trip for M*K <= 16 * blockDim * 8, e.g. M = 8, K = 4096 at 256
-// threads), the rest in batches of kXRows independent loads.
+// first NX chunks of each thread before the residual copy is awaited (one
+// round trip for M*K <= NX * blockDim * 8), the rest in batches of NX
+// independent loads.  The prologue runs once per launch, so its code is
+// fetched once per launch by each of the SM's schedulers: the kernels whose
+// shares fit take the smaller batch, whose unrolled loop is half the code.
 constexpr int kXRows = 16;
+constexpr int kXRowsSmall = 8;
 
-struct XRows {
-    uint4 v[kXRows];
+template <int NX>
+struct XRowsN {
+    uint4 v[NX];
 };
+using XRows = XRowsN<kXRows>;
 
-__device__ __forceinline__ void x_prefetch_rows(const GluParams &p, const RowMap &r, XRows &x, int j0 = 0)
+template <int NX>
+__device__ __forceinline__ void x_prefetch_rows(const GluParams &p, const RowMap &r, XRowsN<NX> &x, int j0 = 0)
 {
     const uint4 *xrow = reinterpret_cast<const uint4 *>(p.x) + static_cast<int64_t>(r.m) * r.nch;
 #pragma unroll
-    for (int j = 0; j < kXRows; ++j) {
+    for (int j = 0; j < NX; ++j) {
         const int c = r.c0 + (j0 + j) * r.P;
         x.v[j] = (r.active && c < r.nch) ? xrow[c] : make_uint4(0, 0, 0, 0);
     }
@@ -527,16 +533,18 @@ __device__ __forceinline__ void x_prefetch_rows(const GluParams &p, const RowMap
 // s = bf16(x + residual) formed in place in h_s (the fp32 sum of two bf16
 // values rounds to the same bf16 as the exact sum); returns this thread's sum
 // of s^2 over its chunks as a double-float.  The statistic rides in the same
-// loop, where it hides under the latency of the x loads.
+// loop, where it hides under the latency of the x loads.  The chunks are
+// taken in the same order for every NX, so the sum does not depend on it.
+template <int NX>
 __device__ __forceinline__ float2 add_rows_in_place(const GluParams &p, const RowMap &r, uint16_t *h_s, int hstride,
-                                                    XRows &x)
+                                                    XRowsN<NX> &x)
 {
     SumSq ss[4] = {sumsq_zero(), sumsq_zero(), sumsq_zero(), sumsq_zero()};
     uint4 *row = reinterpret_cast<uint4 *>(h_s + static_cast<int64_t>(r.m) * hstride);
-    for (int j0 = 0;; j0 += kXRows) {
+    for (int j0 = 0;; j0 += NX) {
         if (j0 > 0) x_prefetch_rows(p, r, x, j0);
 #pragma unroll
-        for (int j = 0; j < kXRows; ++j) {
+        for (int j = 0; j < NX; ++j) {
             const int c = r.c0 + (j0 + j) * r.P;
             if (r.active && c < r.nch) {
                 const uint4 sv = add_bf16x8(x.v[j], row[c]);
@@ -544,7 +552,7 @@ __device__ __forceinline__ float2 add_rows_in_place(const GluParams &p, const Ro
                 sumsq_bf16x8(sv, ss);
             }
         }
-        if (!r.active || r.c0 + (j0 + kXRows) * r.P >= r.nch) break;
+        if (!r.active || r.c0 + (j0 + NX) * r.P >= r.nch) break;
     }
     return sumsq_total(ss);
 }
@@ -609,7 +617,9 @@ __device__ __forceinline__ void norm_rows_in_place(const GluParams &p, const Row
         const uint4 *wv = reinterpret_cast<const uint4 *>(w_s);
         uint64_t mask = 0;   // this thread's chunks left as s for norm_fix_chunks (at most 40 of them)
         int i = 0;
-#pragma unroll 4
+        // not unrolled: eight independent elements per chunk already overlap, and the loop
+        // stays a few instruction-cache lines (each scheduler fetches it once per launch)
+#pragma unroll 1
         for (int c = r.c0; c < r.nch; c += r.P, ++i) {
             bool near = false;
             const uint4 hv = norm_chunk_f32(row[c], wv[c], ih, near);
@@ -859,7 +869,7 @@ __global__ void __launch_bounds__(kMaxStreamWarps * 32, 1) glu_stream_kernel(con
             bulk_g2s_plain(h_s, p.s, bytes, pro_bar);   // residual rows into h_s rows 0..M-1
         }
         const RowMap rm = row_map(p.M, K);
-        XRows xr;
+        XRowsN<kXRowsSmall> xr;
         if (p.fused) x_prefetch_rows(p, rm, xr);
         prologue_wait(pro_bar);
         float2 ss;

@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(32 * (slice_max_warps(SPW, MB) + 1), 1)
             copy_rows_async(h_s, HS, p.s, p.K, p.M, p.K, pro_bar);   // the residual rows, padded
         }
         const RowMap rm = row_map(p.M, p.K);
-        XRows xr;
+        XRowsN<kXRowsSmall> xr;
         if (p.fused) x_prefetch_rows(p, rm, xr);
         prologue_wait(pro_bar);
         float2 ss;
