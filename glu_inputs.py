@@ -147,8 +147,9 @@ WORKLOADS = {
         # batched decode, both modes
         Workload("gemv_k2560_n9728_batched", "glu_gemv", (1, 2, 4, 8), 2560, 9728, ("fused", "hf"), 32,
                  1 / math.sqrt(2560)),
-        # batched decode at 32 and 64 rows (row blocks of 16, one pass over the
-        # weights each), HF-boundary rounding
+        # batched decode at 32 and 64 rows (one pass over the weights on the
+        # tcgen05 kernel; row blocks of 16 where it does not apply), HF-boundary
+        # rounding
         Workload("gemv_k2560_n9728_wide", "glu_gemv", (32, 64), 2560, 9728, ("hf",), 32, 1 / math.sqrt(2560)),
         # the backward of the K=2560, N=9728 layer (gradients of h and both weights)
         Workload("bwd_k2560_n9728", "glu_backward", (1, 8), 2560, 9728, ("fused",), 16, 1 / math.sqrt(2560)),

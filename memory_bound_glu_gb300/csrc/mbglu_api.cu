@@ -557,11 +557,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
     return fn;
 }
 
-// Descriptor of an [N][K] bf16 weight (row stride ld elements) read in boxes
-// of box_k x 8 rows; elements past K or N read as zero.  False if the driver
-// rejects it (the kernel then copies row by row).
 // Tiled 2-D descriptor of a bf16 [rows][K] matrix with row stride ld, box
-// box_k x box_rows.  The last 64 descriptors this thread encoded are kept
+// box_k x box_rows; elements past K or rows read as zero.  False if the
+// driver rejects it (the caller then takes a path without tensor copies).
+// The last 64 descriptors this thread encoded are kept
 // (direct-mapped on their arguments): a descriptor holds only the address,
 // the shape and the strides, so a kept one is exactly what encoding again
 // would give, whatever the memory holds now.
