@@ -379,10 +379,11 @@ int mbglu_last_cuda_error(void);
 
 /* Which kernel the calling thread's last successful call launched:
  * 0 none (no-op), 1 streaming kernel (CUDA-core FMA), 2 generic kernel,
- * 3 zero fill, 4 tensor-core streaming kernel (batch >= 3), 5 silu_mul,
- * 6 gdn_gates, 7 row blocks (a batch above MBGLU_BLOCK_M: one of 1-4 per
- * block), 8 glu_backward, 9 the tcgen05 kernel (a batch above MBGLU_BLOCK_M in one
- * pass). */
+ * 3 zero fill, 4 tensor-core kernel with h in shared memory (batch >= 3),
+ * 5 silu_mul, 6 gdn_gates, 7 row blocks (a batch above MBGLU_BLOCK_M: one
+ * of 1, 2, 4, 10 per block), 8 glu_backward, 9 the tcgen05 kernel (a batch
+ * above MBGLU_BLOCK_M in one pass), 10 the K-slice tensor-core kernel (h's
+ * fragments in registers, batch 1..16). */
 int mbglu_last_variant(void);
 
 /* Which kernels the calling thread's last glu_backward took for the
