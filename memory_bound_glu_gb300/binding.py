@@ -366,8 +366,9 @@ def gdn_gates(a, b, A_log, dt_bias, g=None, beta=None, stream=None):
 
 def last_variant() -> int:
     """Kernel the calling thread's last call launched: 0 none, 1 streaming
-    (CUDA-core), 2 generic, 3 zero fill, 4 tensor-core streaming (batch >= 3),
-    5 silu_mul, 6 gdn_gates, 7 row blocks, 8 glu_backward, 9 tcgen05."""
+    (CUDA-core), 2 generic, 3 zero fill, 4 tensor cores with h in shared
+    memory (batch >= 3), 5 silu_mul, 6 gdn_gates, 7 row blocks, 8
+    glu_backward, 9 tcgen05, 10 the K-slice tensor-core kernel (batch 1..16)."""
     return lib().mbglu_last_variant()
 
 
