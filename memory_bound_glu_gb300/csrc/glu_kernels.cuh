@@ -20,16 +20,20 @@
 //     one call's tail with the next call's ramp;
 //   * every wait is bounded (globaltimer); a timeout records an error word and
 //     returns instead of hanging or trapping.
-// Kernels in this file:
-//   glu_stream_kernel   batch 1-2, CUDA cores: 1-D bulk copies of whole rows,
-//                       h in registers at batch 1, packed fp32x2 FMAs and a
-//                       warp butterfly; optional add + RMSNorm prologue;
-//   glu_mma_kernel      batch 3-16, tensor cores (mma.sync m16n8k16): one TMA
-//                       box per matrix per stage, static per-warp unit ranges
-//                       with exact accumulator hand-off, h staged in up to two
-//                       K-phases; optional add + RMSNorm prologue;
+// The K-slice tensor-core kernel, which takes batch 1-16 where its plan fits
+// (the headline shape among them), is in glu_slice.cuh.  Kernels in this file:
+//   glu_stream_kernel   batch 1-2 past the K-slice kernel's reach, CUDA cores:
+//                       1-D bulk copies of whole rows, h in registers at
+//                       batch 1, packed fp32x2 FMAs and a warp butterfly;
+//                       optional add + RMSNorm prologue;
+//   glu_mma_kernel      batch 3-16 past the K-slice kernel's reach, tensor
+//                       cores (mma.sync m16n8k16): one TMA box per matrix per
+//                       stage, static per-warp unit ranges with exact
+//                       accumulator hand-off, h staged in up to two K-phases;
+//                       optional add + RMSNorm prologue;
 //   glu_generic_kernel  any 2-byte-aligned operands (the correctness path);
-//   residual_add_kernel, zero_fill_kernel, silu_mul_kernel, gdn_gates_kernel.
+//   residual_add_kernel, zero_fill_kernel, silu_mul_kernel,
+//   gdn_gates_chunk_kernel, gdn_gates_kernel.
 #pragma once
 #include <cuda_bf16.h>
 #include <cstdint>

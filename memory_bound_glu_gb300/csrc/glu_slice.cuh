@@ -40,7 +40,8 @@
 // (residual rows copied in, s = bf16(x + residual) when fused, the
 // double-float statistic and the correctly rounded h = bf16(s inv (1 + w)),
 // all threads taking part), at a row pitch of K + 8 so that the warps' loads
-// of their fragments meet no bank conflict; a barrier then hands the region
+// of their fragments meet no bank conflict (K % 16 == 0; two rows share a
+// bank at K % 16 == 8); a barrier then hands the region
 // to the slots.  When fused, the epilogue warp writes this CTA's slice of the
 // residual at the end, once every CTA has read it (fused_residual_helper).
 //

@@ -39,12 +39,19 @@ def slot_bytes(mb):
     return (8 if mb > 8 else 4) * 32 * 4
 
 
-def layout(c):
-    """Shared-memory layout and ring depth of one candidate (slice_layout)."""
+def layout(c, M=0, K=0, norm=False):
+    """Shared-memory layout and ring depth of one candidate (slice_layout).
+    norm: h_s[M][K + 8] shares the slots' region; norm_w [K] and the
+    statistic's partials (2 floats per thread) follow at off_s."""
     W = c["warps"]
     region = slots(c["mb"]) * W * slot_bytes(c["mb"])
+    if norm:
+        region = max(region, M * (K + 8) * 2)
     c["off_s"] = (1024 + region + 127) & ~127
-    c["off_ring"] = (c["off_s"] + 1023) & ~1023
+    end = c["off_s"]
+    if norm:
+        end = c["off_s"] + ((2 * K + 127) & ~127) + 2 * 32 * (W + 1) * 4
+    c["off_ring"] = (end + 1023) & ~1023
     room = SMEM_OPTIN - 1024 - 256 - c["off_ring"]
     if room <= 0:
         return False
@@ -53,11 +60,13 @@ def layout(c):
     return c["stages"] >= 2
 
 
-def plan(M, N, K, sms=SMS, spw_only=0, mma_min_m=3):
-    if M < 1 or M > 16 or K < SEG or K % 8 or N < 1:
+def plan(M, N, K, sms=SMS, spw_only=0, mma_min_m=3, norm=False):
+    if M < 1 or M > 16 or K < SEG or K % 8 or N < 1 or (norm and M < mma_min_m):
         return None
     nseg = -(-K // SEG)
     if M > 8:
+        if norm:
+            return None
         c = dict(spw=1, mb=16, warps=nseg)
         if nseg > max_warps(1, 16) or not layout(c):
             return None
@@ -70,7 +79,7 @@ def plan(M, N, K, sms=SMS, spw_only=0, mma_min_m=3):
         if W > max_warps(spw) or (W - 1) * spw >= nseg:
             continue
         c = dict(spw=spw, mb=8, warps=W)
-        if not layout(c):
+        if not layout(c, M, K, norm):
             continue
         c["grid"] = max(1, min(sms, (N + 7) // 8))
         return c
@@ -199,3 +208,54 @@ def test_plan_on_the_workloads():
     # batch 1-2: one segment per warp only (K <= 12 * 256)
     assert plan(1, 9728, 2560)["spw"] == 1 and plan(2, 9728, 3072)["spw"] == 1
     assert plan(1, 9728, 4096) is None and plan(2, 11008, 3080) is None
+
+
+PRO_BAR = 784              # the prologue copies' mbarrier (kProBarOffset)
+STATIC_SMEM = 256          # the kernel's static shared memory (inv_s and alignment)
+
+
+@pytest.mark.parametrize("M", [3, 4, 5, 8])
+def test_norm_variant_layout(M):
+    """The add_rmsnorm_glu variant's shared memory, for every K the plan
+    takes: the barriers, the prologue barrier, h_s[M][K + 8] (which the slots
+    reuse after a barrier), norm_w and the statistic's partials at off_s, and
+    the 1024-byte aligned ring are disjoint and inside the allocation; every
+    bulk copy of the prologue starts and ends on 16-byte boundaries."""
+    taken = 0
+    for K in range(256, 4608 + 1, 8):
+        p = plan(M, 9728, K, norm=True)
+        if p is None:
+            continue
+        taken += 1
+        W, S, nslot = p["warps"], p["stages"], slots(p["mb"])
+        threads = 32 * (W + 1)
+        assert 8 * W * S <= 512 and 512 + 16 * nslot <= PRO_BAR and PRO_BAR + 8 <= 1024
+        hs_end = 1024 + M * (K + 8) * 2
+        assert hs_end <= p["off_s"] and 1024 + nslot * W * slot_bytes(p["mb"]) <= p["off_s"]
+        parts = p["off_s"] + ((2 * K + 127) & ~127)
+        assert parts + 2 * threads * 4 <= p["off_ring"] and p["off_ring"] % 1024 == 0
+        # the kernel rounds its base up to 1024 bytes: at most 1023 of the allocation
+        assert p["off_ring"] + W * S * STAGE + 1023 <= p["smem"]
+        assert p["smem"] + STATIC_SMEM <= SMEM_OPTIN and S >= 2
+        # residual rows land row by row at the padded pitch, norm_w in one copy
+        for r in range(M):
+            assert (1024 + r * (K + 8) * 2) % 16 == 0 and (2 * K) % 16 == 0
+        assert p["off_s"] % 16 == 0
+    assert taken > 0
+    # the K2560 shape of the norm workload: 10 compute warps, 2 stages
+    p = plan(M, 9728, 2560, norm=True)
+    assert p["warps"] == 10 and p["stages"] == 2 and p["spw"] == 1
+
+
+@pytest.mark.parametrize("K", [256, 1024, 2560, 2568, 4096])
+def test_norm_fragment_loads_and_bank_groups(K):
+    """The compute warps read their A fragments from h_s at a row pitch of
+    K + 8: lane (g, c) reads 4 bytes of row g at column k0 + 2 c.  With
+    K % 16 == 0 the 32 lanes hit 32 different banks; at K % 16 == 8 the pitch
+    puts two rows on each bank (the kernel is still correct, only slower)."""
+    words = [(g * (K + 8) * 2 + 4 * c) // 4 for g in range(8) for c in range(4)]
+    banks = {w % 32 for w in words}
+    if K % 16 == 0:
+        assert len(banks) == 32
+    else:
+        assert len(banks) == 16
