@@ -1743,9 +1743,10 @@ __global__ void __launch_bounds__(256) silu_mul_kernel(const uint16_t *x, int64_
 // ---------------------------------------------------------------------------
 // gdn_gates: decay and write gates of the gated-delta-net layers
 // ---------------------------------------------------------------------------
-// PR #8602 ("fused_glu" commit: "beta=sigmoid(b) and
-// g=-exp(A_log)*softplus(a+dt_bias) with fp32 math and the numerically stable
-// softplus branch"); PR #9057 ("Changes": fp32 decay gates).  For token t,
+// PR #8602, the "fused_glu" commit: the write gate is the sigmoid of b and
+// the decay gate is -exp(A_log) times the softplus of a + dt_bias, computed in
+// fp32 with softplus in its overflow-safe form; PR #9057 ("Changes"): the
+// decay gates stay fp32.  For token t,
 // head j: x = a + dt_bias[j] (fp32), g = -exp(A_log[j]) * softplus(x) (fp32),
 // beta = bf16(sigmoid(b)).  softplus in its stable form: x + log1p(e^-x) for
 // x > 0, log1p(e^x) otherwise -- never e^x of a large x -- and sigmoid from

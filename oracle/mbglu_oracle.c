@@ -151,8 +151,8 @@ typedef struct {
 } glu_job;
 
 /*
- * For each batch row m and output feature n ([8602/PlanB], "each warp
- * handles one output feature"):
+ * For each batch row m and output feature n ([8602/PlanB]: the listed
+ * kernel gives every output feature a warp of its own):
  *   G = sum_k h[m,k] * W_gate[n,k]      (the gate dot product)
  *   U = sum_k h[m,k] * W_up[n,k]        (the up dot product)
  * Each bf16 x bf16 product is exact in binary64 (8 + 8 significant bits), and
