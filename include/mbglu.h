@@ -104,9 +104,10 @@ typedef int mbglu_status;
                                    mbglu_read_device_error, never by a launch) */
 
 /*
- * glu_gemv -- the dual-weight GLU GEMV.  [8602/PlanB] "Plan B Design": the
- * kernel reads gate.weight and up.weight directly, fp32 accumulation, SiLU on
- * the gate product times the up product, one output per feature.
+ * glu_gemv -- the dual-weight GLU GEMV.  [8602/PlanB] "Plan B Design": both
+ * nn.Linear weights are used where they lie, the dot products accumulate in
+ * fp32, and each output feature is SiLU of its gate product times its up
+ * product.
  *
  *   h       [M, K] bf16, row stride ldh >= K          (read)
  *   gate_w  [N, K] bf16, row stride ld_gate >= K      (read, in place)

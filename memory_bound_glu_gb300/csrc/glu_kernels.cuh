@@ -5,9 +5,9 @@
 // DeepSpeed PR #8602, comment "Plan B: Dual-Weight GEMV", section "Plan B
 // Design: kernel adapts to the weights": both nn.Linear weights are read in
 // place, fp32 accumulation, SiLU(gate) * up with one round-to-nearest-even at
-// the end.  Section "Why cuBLAS-level performance is achievable at b=1": the
-// op is memory-bound -- every weight element is read once and multiplied
-// once -- so the design target is the HBM roofline.
+// the end.  Section "Why cuBLAS-level performance is achievable at b=1": each
+// weight element takes part in exactly one product, so the op is bound by the
+// bytes it streams, and the design target is the HBM roofline.
 //
 // GB300 design (the pages' warp-per-row Ada kernel with scalar loads is prior
 // art only):

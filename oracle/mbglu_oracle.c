@@ -340,9 +340,9 @@ int oracle_add_rmsnorm_glu(const uint16_t *x, uint16_t *residual,
 
 /*
  * The standalone epilogue of the prefill / large-batch route
- * ([8602/fused_glu]: a native "fused silu-mul kernel (halves layout, no
- * chunked views ...)", single rounding against the composite's double
- * rounding).  Each row of x holds both projections side by side, as a GEMM on
+ * ([8602/fused_glu]: a native kernel that applies SiLU and the product to
+ * the two halves of each row in place, rounding once where the composite
+ * rounds twice).  Each row of x holds both projections side by side, as a GEMM on
  * the concatenated [gate; up] weight leaves them: the gate half in columns
  * [0, N) and the up half in columns [N, 2N).  For every m < M, n < N:
  *   g = x[m, n], u = x[m, N + n]                 (bf16, exact in binary64)

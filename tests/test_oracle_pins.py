@@ -9,8 +9,8 @@ plants such slips in a copy of the oracle and checks they are caught.
 Method sources: DeepSpeed PR #8602 "Plan B: Dual-Weight GEMV" (kernel listing:
 fp32 dot products, SiLU(gate)*up, one round-to-nearest-even to bf16; b>1
 fallback F.silu(h@Wg.T)*(h@Wu.T) on bf16 tensors) and PR #9057 "Changes"
-(HF's intermediate bf16 rounding in residual/RMSNorm and GLU; zero-centred
-norm scale built in fp32).
+(the residual sum, the normed row and the GLU's intermediates round to bf16
+as HF's modules do; the zero-centred norm scale is formed in fp32).
 """
 import math
 import struct
