@@ -225,8 +225,8 @@ def glu_backward(h, gate_w, up_w, dout, grad_h=None, grad_gate=None, grad_up=Non
 class DualWeightGlu(torch.autograd.Function):
     """out = SiLU(h @ gate_w.T) * (h @ up_w.T) with the weights read in place
     and gradients for h, gate_w and up_w ([8602/PlanB] "Plan B Design": the
-    autograd.Function reads the original Parameters, so the gradients reach
-    the weights)."""
+    Function works on the model's own weight tensors, not on a copy, so their
+    gradients land on those tensors)."""
 
     @staticmethod
     def forward(ctx, h, gate_w, up_w, mode="fused"):
