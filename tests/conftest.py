@@ -31,7 +31,8 @@ def _parity_label(request):
 
 def pytest_sessionfinish(session, exitstatus):
     """Writes every parity comparison of the session (label, statistics,
-    verdict) to gpurun_out/parity_stats.json, or to $MBGLU_PARITY_STATS."""
+    verdict) as JSON to $MBGLU_PARITY_STATS, by default parity_stats.json in
+    the repository's untracked output folder."""
     import json
     import tolerance
     if not tolerance.RECORDS:
