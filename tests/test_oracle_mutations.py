@@ -49,6 +49,20 @@ MUTATIONS = {
     "gdn_sigmoid_sign": ("oracle_bf16_round(1.0 / (1.0 + exp(-y)))", "oracle_bf16_round(1.0 / (1.0 + exp(y)))"),
     "bwd_dsilu_missing_term": ("d * U * (s * (1.0 + G * (1.0 - s)))", "d * U * s"),
     "bwd_up_grad_from_dG": ("su += j->dU[(int64_t)m * j->N + n] * hk;", "su += j->dG[(int64_t)m * j->N + n] * hk;"),
+    "hf_product_on_unrounded_up": ("o = oracle_bf16_round(oracle_bf16_to_double(sb) * oracle_bf16_to_double(ub));",
+                                   "o = oracle_bf16_round(oracle_bf16_to_double(sb) * U);"),
+    "norm_stat_on_unrounded_sum": ("            const double sv = oracle_bf16_to_double(sr[k]);\n            ss += sv * sv;",
+                                   "            const double sv = oracle_bf16_to_double(xr[k]) + oracle_bf16_to_double(rr[k]);\n"
+                                   "            ss += sv * sv;"),
+    "bwd_dU_uses_dsilu": ("j->dU[(int64_t)m * j->N + n] = d * oracle_silu(G);",
+                          "j->dU[(int64_t)m * j->N + n] = d * (s * (1.0 + G * (1.0 - s)));"),
+    "bwd_grad_w_first_row_only": ("const double hk = oracle_bf16_to_double(j->h[(int64_t)m * j->ldh + k]);",
+                                  "const double hk = oracle_bf16_to_double(j->h[(int64_t)0 * j->ldh + k]);"),
+    "bwd_grad_h_drops_up_term": ("                acc += j->dU[(int64_t)m * j->N + n] * "
+                                 "oracle_bf16_to_double(j->up_w[(int64_t)n * j->ld_up + k]);\n", ""),
+    "bwd_grad_h_gate_reads_up": ("acc += j->dG[(int64_t)m * j->N + n] * oracle_bf16_to_double(j->gate_w[(int64_t)n * j->ld_gate + k]);",
+                                 "acc += j->dG[(int64_t)m * j->N + n] * oracle_bf16_to_double(j->up_w[(int64_t)n * j->ld_up + k]);"),
+    "gdn_decay_sign": ("g[(int64_t)t * H + j] = -exp((double)A_log[j])", "g[(int64_t)t * H + j] = exp((double)A_log[j])"),
     "gdn_x_not_binary32": ("const float x = (float)oracle_bf16_to_double(a[(int64_t)t * lda + j]) + dt_bias[j];",
                            "const double x = oracle_bf16_to_double(a[(int64_t)t * lda + j]) + (double)dt_bias[j];"),
 }
