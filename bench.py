@@ -153,6 +153,14 @@ def recorded_traffic(workload, M, mode):
     return (rec.get("dram_bytes_per_launch") if same else None), last
 
 
+def smi_id(local):
+    """The nvidia-smi id of this process's CUDA device `local`: its entry in
+    CUDA_VISIBLE_DEVICES when that variable remaps the devices (an index or a
+    UUID, both of which nvidia-smi --id takes), else `local` itself."""
+    ids = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    return ids[local] if 0 <= local < len(ids) else str(local)
+
+
 class ClockSampler:
     """nvidia-smi samples during the timed region (200 ms period)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -559,7 +567,7 @@ def main():
             graph.replay()
     torch.cuda.synchronize(dev)
 
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(smi_id(local))
     t_load0 = None
     if not args.no_clocks:
         sampler.start()

@@ -116,3 +116,19 @@ def test_recorded_traffic_is_current_only_for_the_profiled_sources(monkeypatch):
     assert cur is None and last["sources_changed_since"] is True
     assert last["dram_bytes_per_launch"] == rec["dram_bytes_per_launch"]
     assert bench.recorded_traffic("gemv_k2560_n9728_wide", 32, "hf") == (None, None)
+
+
+def test_clock_sampler_follows_cuda_visible_devices(monkeypatch):
+    """The clocks are sampled on the GPU the rank runs on: nvidia-smi numbers
+    the physical devices, CUDA those left visible."""
+    import bench
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES", raising=False)
+    assert bench.smi_id(0) == "0" and bench.smi_id(3) == "3"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "3")
+    assert bench.smi_id(0) == "3"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "4, 6,7")
+    assert [bench.smi_id(i) for i in range(3)] == ["4", "6", "7"]
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "GPU-0a1b2c3d-0000-1111-2222-333344445555")
+    assert bench.smi_id(0) == "GPU-0a1b2c3d-0000-1111-2222-333344445555"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "")
+    assert bench.smi_id(1) == "1"
