@@ -130,8 +130,8 @@ mbglu_status glu_gemv(const mbglu_bf16 *h, int64_t ldh,
 /*
  * glu_backward -- the gradients of glu_gemv's exact composite
  * out = SiLU(h gate_w^T) * (h up_w^T) for an upstream gradient dout.
- * [8602/PlanB] "Plan B Design": an autograd.Function reading the original
- * Parameters, so that the gradients reach gate.weight and up.weight (the
+ * [8602/PlanB] "Plan B Design": the autograd wrapper works on the model's
+ * own weight tensors, so their gradients land on those tensors (the
  * "Verification Results" compare them with the composite's).  In fp32 from
  * the bf16 operands:
  *   g, u     = the forward's dot products (fp32 accumulation)
