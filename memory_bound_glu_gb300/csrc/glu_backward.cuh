@@ -2,9 +2,9 @@
 //
 // DeepSpeed PR #8602, comment "Plan B: Dual-Weight GEMV -- Investigation
 // Results & Implementation", section "Plan B Design: kernel adapts to the
-// weights": an autograd.Function that reads the original Parameters, so that
-// gradients reach gate.weight and up.weight; "Verification Results" checks
-// them against the composite.  For out = SiLU(g) * u with g = h Wg^T and
+// weights": the autograd wrapper works on the model's own weight tensors, so
+// their gradients land on those tensors; "Verification Results" checks them
+// against the composite.  For out = SiLU(g) * u with g = h Wg^T and
 // u = h Wu^T, and an upstream gradient dout:
 //
 //   dG = dout * u * SiLU'(g)        dU = dout * SiLU(g)            [M][N]
