@@ -231,3 +231,53 @@ def test_glu_backward_workspace_bytes():
     assert lib.glu_backward_workspace_bytes(1, 100000, 64) == 800000 + 256 * 64 * 4
     assert lib.glu_backward_workspace_bytes(64, 10, 10) == r256(64 * 10 * 8) + r256(256 * 8 * 10 * 4)
     assert lib.glu_backward_workspace_bytes(65, 10, 10) == 0 and lib.glu_backward_workspace_bytes(0, 10, 10) == 0
+
+
+def _c_params():
+    """{function: [parameter type category, ...]} from the header's prototypes."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    text = re.sub(r"#.*", "", text)
+    out = {}
+    for m in re.finditer(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.M | re.S):
+        name, params = m.group(1), " ".join(m.group(2).split())
+        cats = []
+        for p in ([] if params in ("", "void") else params.split(",")):
+            p = p.strip()
+            if "*" in p or p.startswith("cudaStream_t"):
+                cats.append("ptr")
+            elif p.startswith("int64_t"):
+                cats.append("i64")
+            elif p.startswith("size_t"):
+                cats.append("size")
+            elif p.startswith("float"):
+                cats.append("f32")
+            elif p.split()[0] in ("int", "mbglu_mode", "mbglu_status"):
+                cats.append("i32")
+            else:
+                cats.append("?" + p)
+        out[name] = cats
+    return out
+
+
+def _ctypes_category(t):
+    if t is ctypes.c_void_p or (isinstance(t, type) and issubclass(t, ctypes._Pointer)):
+        return "ptr"
+    return {ctypes.c_int64: "i64", ctypes.c_size_t: "size", ctypes.c_float: "f32", ctypes.c_int: "i32"}[t]
+
+
+def test_binding_argument_types_match_the_prototypes():
+    """Every entry point the binding declares argument types for takes, in
+    the header, the same number of arguments of the same kinds (pointer,
+    64-bit, size_t, float, 32-bit), so ctypes marshals each call as the
+    C ABI expects."""
+    protos = _c_params()
+    lib = mb.lib()
+    checked = 0
+    for name in mb.EXPORTS:
+        fn = getattr(lib, name)
+        if fn.argtypes is None:
+            assert protos[name] == [], name
+            continue
+        assert [_ctypes_category(t) for t in fn.argtypes] == protos[name], name
+        checked += 1
+    assert checked >= 10
