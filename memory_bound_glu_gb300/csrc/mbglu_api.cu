@@ -37,7 +37,7 @@ enum Variant {
     kRowBlocks = 7,  // a batch above kBlockRows, run as row blocks
     kBackward = 8,   // glu_backward
     kTcGemv = 9,     // the tcgen05 kernel (one pass for batch 17..64)
-    kSlice = 10      // the K-slice tensor-core kernel (batch 3..8, h in registers)
+    kSlice = 10      // the K-slice tensor-core kernel (batch 1..16 where it applies, h in registers)
 };
 constexpr int kBlockRows = mbglu::kMaxM;   // rows one GEMV kernel takes (its batch tile)
 
@@ -1277,7 +1277,8 @@ mbglu_status launch_bwd_hw(const BwdHwPlan &hp, const mbglu::BwdParams &q, const
     return e == cudaSuccess ? MBGLU_OK : cuda_fail(e);
 }
 
-// Plan of glu_bwd_mma_kernel (steps 2 and 3 on the tensor cores, M <= 8):
+// Plan of glu_bwd_mma_kernel (steps 2 and 3 on the tensor cores, M <= 16 in
+// a batch tile MB of 8 or 16 rows):
 // K in slices of 64 NB columns, one warp each; W warps per CTA cut K into
 // cg column groups, and the SMs into row shares of about N / (SMs / cg) rows;
 // stages of 16 rows, as many (2..4) as fit beside the staged dG, dU.  Of the
@@ -1484,9 +1485,10 @@ mbglu_status glu_backward(const mbglu_bf16 *h, int64_t ldh, const mbglu_bf16 *ga
     q.ldm = N;
     q.vec_w = aligned(gate_w, 8) && aligned(up_w, 8) && ld_gate % 4 == 0 && ld_up % 4 == 0;
     cudaError_t e = cudaSuccess;
-    // 2 + 3 in one pass over the rows where it applies (M <= 8, aligned):
-    // grad_h partials and both weight gradients, then the partials' sum.
-    // From bwd_mma_min_m rows on, the pass runs on the tensor cores.
+    // 2 + 3 in one pass over the rows where it applies (aligned; M <= 8 on
+    // the CUDA cores, M <= 16 on the tensor cores): grad_h partials and both
+    // weight gradients, then the partials' sum.  From bwd_mma_min_m rows on,
+    // the pass runs on the tensor cores.
     BwdMmaPlan mp;
     mbglu::BwdMaps mmaps;
     if (want_h && want_w && tuning().bwd_fused && M >= tuning().bwd_mma_min_m &&
