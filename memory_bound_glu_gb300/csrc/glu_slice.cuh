@@ -1,10 +1,10 @@
-// glu_slice.cuh -- the dual-weight GLU GEMV at batch 1..8 on the tensor
+// glu_slice.cuh -- the dual-weight GLU GEMV at batch 1..16 on the tensor
 // cores, with h held in registers.
 //
 // DeepSpeed PR #8602, comment "Plan B: Dual-Weight GEMV", section "Plan B
 // Design": one pass over h reads gate_w and up_w in place and applies
-// SiLU(g) * u in the epilogue; the batched-decode shapes (M up to 8) are the
-// ones the comment's benchmark table runs.  g[m][n] = sum_k h[m][k] Wg[n][k],
+// SiLU(g) * u in the epilogue; PR #9057's A100 commit runs decode at batch 8
+// and above, and batch 1 is the comment's own case.  g[m][n] = sum_k h[m][k] Wg[n][k],
 // u likewise, then the mode's epilogue (glu_epilogue) or the backward's dG, dU
 // (glu_store).
 //
@@ -19,7 +19,8 @@
 // A stage is one segment: four 64-column x 8-row boxes per matrix (8 KB),
 // 128-byte swizzled (16-byte chunk j of row r at r * 128 + ((j ^ r) << 4)),
 // so each ldmatrix of 8 rows meets no bank conflict.  No h in shared memory,
-// so nearly all of it is ring: ~190 KB of weights in flight per SM.
+// so nearly all of it is ring: 160 KB of weights in flight per SM at K = 2560
+// (10 warps x 2 stages), 192 KB at K = 4096 (8 warps x 3 stages).
 //
 // Arithmetic: A (16 x 16) = h's rows 0..15 at the k-step (rows >= M read as
 // zero; at MB = 8, for M <= 8, rows 8..15 are the zero registers a1 and a3),
