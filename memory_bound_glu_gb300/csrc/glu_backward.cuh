@@ -11,14 +11,18 @@
 //   grad_h    = dG Wg + dU Wu                                      [M][K]
 //   grad_gate = dG^T h,  grad_up = dU^T h                          [N][K]
 //
-// Three steps, each streaming about one weight-sized volume of HBM:
+// The path for aligned operands, two passes over the weights:
 //   1. the forward kernels with the backward epilogue (glu_store with
 //      kModeBwd) recompute g and u and write dG, dU in fp32;
-//   2. glu_bwd_h_kernel: CTA (column block, row split) sums its rows of both
-//      weights, times dG and dU, over 512 columns into an fp32 partial;
-//      glu_bwd_h_reduce_kernel adds the partials in split order and rounds;
-//   3. glu_bwd_w_kernel: the outer products, written once as bf16 (h in
-//      shared memory where it fits).
+//   2. one pass that reads each weight block once for grad_h's partials and
+//      writes both weight gradients: glu_bwd_mma_kernel on the tensor cores
+//      (M = 3..16; dG and dU enter as three exact bf16 terms) or
+//      glu_bwd_hw_kernel on the CUDA cores (M <= 2); glu_bwd_h_reduce8_kernel
+//      then adds the partials in order and rounds grad_h once.
+// Batches above 16 rows and unaligned operands take three steps instead:
+// step 1 per 16-row block; grad_h by glu_bwd_rows_kernel (passes of 8 rows)
+// or glu_bwd_h_kernel with glu_bwd_h_reduce_kernel; the weight gradients by
+// glu_bwd_w_rows_kernel or glu_bwd_w_kernel.
 // Every sum runs in a fixed order: results are bitwise deterministic.
 #pragma once
 
